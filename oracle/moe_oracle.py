@@ -1,0 +1,458 @@
+"""fp64 CPU oracle of the Megatron-Core-style MoE expert layer.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and the
+benchmark's CPU-baseline / reference legs may import this module.  The CUDA
+library never calls it, shares no code with it and it imports nothing from the
+library.  It is deliberately plain and slow: numpy fp64, one step per function,
+in the order the layer is defined.
+
+Source: "Scalable Training of Mixture-of-Experts Models with Megatron Core"
+(summary page).  What each step follows there:
+
+* routing to a few experts per token: "Problem" section 1 (each input goes to
+  the two or three best-suited experts, the rest idle);
+* the router is kept in high precision: technical summary section 2.5
+  (selective precision: router, embedding and optimizer state stay FP32/BF16);
+* permutation of tokens into expert order with dynamic shapes, no host sync:
+  technical summary section 1, compute-efficiency wall, and section 2.4
+  (sync-free kernels: the GPU reads the shape information itself);
+* grouped GEMM over all experts: technical summary section 2.4;
+* routing weight applied before the activation computation so backward keeps
+  no extra intermediate: technical summary section 2.2 (memory-efficient
+  permutation);
+* MXFP8 expert GEMMs on Blackwell: technical summary section 2.5.
+
+The pages give no formula for any of these.  The readings taken where they are
+silent (gate formulas, selection key, tie rule, SwiGLU layout, where the gate
+multiplies, the MX scale rule) are listed with the design notes of the
+repository; each function below states the reading it implements.
+
+Every function here is pinned by a test in tests/test_oracle_*.py against
+something other than itself (brute force, closed forms, invariants, library
+routines, finite differences).  Parity pinned for all functions.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SOFTMAX = "softmax"
+SIGMOID = "sigmoid"
+
+
+# ---------------------------------------------------------------------------
+# Router (technical summary 2.5: router stays in high precision)
+# ---------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, w_router: np.ndarray) -> np.ndarray:
+    """logits[t, e] = <x_t, Wr_e>, fp64.  x [T,H], Wr [E,H] -> [T,E]."""
+    return np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
+
+
+def _sigmoid(v: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def selection_keys(logits: np.ndarray, score: str, bias=None) -> np.ndarray:
+    """Key each expert is ranked by.
+
+    softmax scoring: the logit itself (softmax is monotone, so ranking the raw
+    logit ranks the probability, without creating ties by rounding).
+    sigmoid scoring: sigmoid(logit) + bias_e; the bias changes only which
+    experts are chosen, never the gate values.
+    """
+    logits = np.asarray(logits, np.float64)
+    if score == SOFTMAX:
+        return logits.copy()
+    if score == SIGMOID:
+        b = 0.0 if bias is None else np.asarray(bias, np.float64)[None, :]
+        return _sigmoid(logits) + b
+    raise ValueError(score)
+
+
+def selection_keys_f32(logits_f32: np.ndarray, score: str, bias=None) -> np.ndarray:
+    """The same keys, computed in float32 (the kernel's precision for this
+    decision).  Used where an fp32 choice must be reproduced exactly."""
+    l32 = np.asarray(logits_f32, np.float32)
+    if score == SOFTMAX:
+        return l32.copy()
+    one = np.float32(1.0)
+    s = one / (one + np.exp(-l32))
+    if bias is not None:
+        s = s + np.asarray(bias, np.float32)[None, :]
+    return s.astype(np.float32)
+
+
+def topk_select(keys: np.ndarray, k: int) -> np.ndarray:
+    """For each token, the k experts with the largest key, ordered by key
+    descending; equal keys go to the lower expert id first.  [T,E] -> [T,k] int32."""
+    keys = np.asarray(keys)
+    T, E = keys.shape
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    # lexsort: last key is primary.  Primary: key descending; secondary: id ascending.
+    order = np.lexsort((ids, -keys), axis=-1)
+    return order[:, :k].astype(np.int32)
+
+
+def topk_gap(keys: np.ndarray, k: int) -> np.ndarray:
+    """Per token, key_(k) - key_(k+1) (inf when k == E): how close the choice of
+    the k-th expert was.  Tokens with a small gap may be routed differently by a
+    computation that rounds differently."""
+    keys = np.asarray(keys, np.float64)
+    T, E = keys.shape
+    if k >= E:
+        return np.full(T, np.inf)
+    srt = -np.sort(-keys, axis=-1)
+    gap = srt[:, k - 1] - srt[:, k]
+    # also the smallest gap among the chosen ones (order inside the top-k)
+    if k > 1:
+        inner = np.min(srt[:, :k - 1] - srt[:, 1:k], axis=-1)
+        gap = np.minimum(gap, inner)
+    return gap
+
+
+def gates_from_logits(logits: np.ndarray, sel: np.ndarray, score: str) -> np.ndarray:
+    """Gate weights of the chosen experts, normalised over the chosen set.
+
+    softmax: g_i = exp(l_{S_i}) / sum_{j in S} exp(l_j)   (equal to a full softmax
+             renormalised over S, so both wordings give one function);
+    sigmoid: g_i = sig(l_{S_i}) / sum_{j in S} sig(l_j)  (no extra scale factor).
+    """
+    logits = np.asarray(logits, np.float64)
+    l_sel = np.take_along_axis(logits, sel.astype(np.int64), axis=-1)
+    if score == SOFTMAX:
+        m = l_sel.max(axis=-1, keepdims=True)
+        e = np.exp(l_sel - m)
+        return e / e.sum(axis=-1, keepdims=True)
+    if score == SIGMOID:
+        s = _sigmoid(l_sel)
+        return s / s.sum(axis=-1, keepdims=True)
+    raise ValueError(score)
+
+
+def route(logits: np.ndarray, k: int, score: str, bias=None):
+    """Top-k routing of fp64 logits: returns (topk_idx [T,k] int32, gates [T,k] fp64)."""
+    keys = selection_keys(logits, score, bias)
+    sel = topk_select(keys, k)
+    return sel, gates_from_logits(logits, sel, score)
+
+
+# ---------------------------------------------------------------------------
+# Permutation into expert-contiguous order (technical summary 1 and 2.4:
+# dynamic shapes, sync-free; the shape information is counts and offsets)
+# ---------------------------------------------------------------------------
+
+def permutation_maps(topk_idx: np.ndarray, E: int, pad: int = 128) -> dict:
+    """Expert-contiguous row layout of the T*k (token, slot) pairs.
+
+    counts[e]   number of pairs routed to expert e
+    offsets     exclusive scan of counts (compact layout), length E+1
+    poffsets    exclusive scan of counts rounded up to ``pad`` rows, length E+1
+    slot_row    [T,k]: padded row of pair (t,i) = poffsets[e] + rank, where rank is
+                the number of earlier tokens t' < t routed to the same expert
+                (a stable counting sort by expert)
+    row_src     [poffsets[E]]: token of each padded row, -1 for padding rows
+    row_slot    [poffsets[E]]: slot i of each padded row, -1 for padding rows
+    """
+    idx = np.asarray(topk_idx, np.int64)
+    T, k = idx.shape
+    if idx.size and (idx.min() < 0 or idx.max() >= E):
+        raise ValueError("expert index out of range")
+    counts = np.zeros(E, np.int64)
+    for t in range(T):
+        for i in range(k):
+            counts[idx[t, i]] += 1
+    offsets = np.zeros(E + 1, np.int64)
+    poffsets = np.zeros(E + 1, np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+        poffsets[e + 1] = poffsets[e] + ((counts[e] + pad - 1) // pad) * pad
+    slot_row = np.zeros((T, k), np.int64)
+    row_src = np.full(int(poffsets[E]), -1, np.int64)
+    row_slot = np.full(int(poffsets[E]), -1, np.int64)
+    seen = np.zeros(E, np.int64)
+    for t in range(T):                  # ascending t: the order inside an expert
+        for i in range(k):
+            e = idx[t, i]
+            r = poffsets[e] + seen[e]
+            seen[e] += 1
+            slot_row[t, i] = r
+            row_src[r] = t
+            row_slot[r] = i
+    return {"counts": counts, "offsets": offsets, "poffsets": poffsets,
+            "slot_row": slot_row, "row_src": row_src, "row_slot": row_slot}
+
+
+def compact_rows(maps: dict) -> np.ndarray:
+    """Compact position offsets[e] + rank of each pair, [T,k] (same rank as slot_row)."""
+    pos = maps["slot_row"].copy()
+    po, of = maps["poffsets"], maps["offsets"]
+    E = len(po) - 1
+    for e in range(E):
+        m = (pos >= po[e]) & (pos < po[e + 1])
+        pos[m] = pos[m] - po[e] + of[e]
+    return pos
+
+
+def permute(x: np.ndarray, maps: dict) -> np.ndarray:
+    """x_perm[r] = x[row_src[r]], zero rows for padding."""
+    x = np.asarray(x)
+    src = maps["row_src"]
+    out = np.zeros((len(src),) + x.shape[1:], np.float64)
+    valid = src >= 0
+    out[valid] = x[src[valid]]
+    return out
+
+
+def unpermute_sum(o_perm: np.ndarray, maps: dict, shared=None) -> np.ndarray:
+    """y[t] = sum_i o_perm[slot_row[t,i]] (+ shared[t]); unweighted, because the
+    gate has already been applied inside the expert (technical summary 2.2)."""
+    slot_row = maps["slot_row"]
+    y = np.asarray(o_perm, np.float64)[slot_row].sum(axis=1)
+    if shared is not None:
+        y = y + np.asarray(shared, np.float64)
+    return y
+
+
+# ---------------------------------------------------------------------------
+# Expert MLP (SwiGLU).  W1_e = [W_gate; W_up] of shape [2F,H]; W2_e is [H,F].
+# ---------------------------------------------------------------------------
+
+def silu(v):
+    return v * _sigmoid(v)
+
+
+def silu_grad(v):
+    s = _sigmoid(v)
+    return s * (1.0 + v * (1.0 - s))
+
+
+def swiglu_expert(x_rows: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> np.ndarray:
+    """W2 ( silu(W_gate x) * (W_up x) ) for each row of x_rows."""
+    w1 = np.asarray(w1, np.float64)
+    F = w1.shape[0] // 2
+    z = np.asarray(x_rows, np.float64) @ w1.T
+    h = silu(z[:, :F]) * z[:, F:]
+    return h @ np.asarray(w2, np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# The layer
+# ---------------------------------------------------------------------------
+
+def moe_forward(x, w_router, w1, w2, k, score=SOFTMAX, bias=None,
+                w1_shared=None, w2_shared=None, routing=None, expert_fn=None):
+    """y_t = sum_i g_{t,i} * Expert_{S_t[i]}(x_t)  (+ SharedExpert(x_t)).
+
+    ``routing`` = (topk_idx, gates) replaces the router (router replay, or the
+    GPU's own routing when comparing the expert path alone).
+    ``expert_fn(e, rows)`` replaces the SwiGLU expert (used by the identity pin).
+    Returns a dict with y and the routing record.
+    """
+    x = np.asarray(x, np.float64)
+    T = x.shape[0]
+    E = np.asarray(w_router).shape[0] if w_router is not None else np.asarray(w1).shape[0]
+    logits = None
+    if routing is None:
+        logits = router_logits(x, w_router)
+        idx, gate = route(logits, k, score, bias)
+    else:
+        idx = np.asarray(routing[0], np.int64)
+        gate = np.asarray(routing[1], np.float64)
+    y = np.zeros_like(x)
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        rows = x[tok]
+        out = expert_fn(e, rows) if expert_fn is not None else swiglu_expert(rows, w1[e], w2[e])
+        np.add.at(y, tok, gate[tok, slot][:, None] * out)
+    if w1_shared is not None:
+        y += swiglu_expert(x, w1_shared, w2_shared)
+    return {"y": y, "logits": logits, "topk_idx": idx.astype(np.int32), "gates": gate}
+
+
+def router_backward(logits, sel, gates, dgate, score):
+    """dlogits [T,E] from the gate gradient.  Only the chosen experts' logits
+    receive gradient; the selection bias receives none.
+
+    softmax over the chosen set:  dl_j = g_j (dg_j - sum_i g_i dg_i)
+    sigmoid, normalised:          ds_j = (dg_j - sum_i g_i dg_i) / sum_S sig,
+                                  dl_j = ds_j sig_j (1 - sig_j)
+    """
+    logits = np.asarray(logits, np.float64)
+    sel = np.asarray(sel, np.int64)
+    g = np.asarray(gates, np.float64)
+    dg = np.asarray(dgate, np.float64)
+    inner = (g * dg).sum(axis=-1, keepdims=True)
+    if score == SOFTMAX:
+        dl_sel = g * (dg - inner)
+    elif score == SIGMOID:
+        l_sel = np.take_along_axis(logits, sel, axis=-1)
+        s = _sigmoid(l_sel)
+        ds = (dg - inner) / s.sum(axis=-1, keepdims=True)
+        dl_sel = ds * s * (1.0 - s)
+    else:
+        raise ValueError(score)
+    dlogits = np.zeros_like(logits)
+    np.put_along_axis(dlogits, sel, dl_sel, axis=-1)
+    return dlogits
+
+
+def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
+                 w1_shared=None, w2_shared=None, with_router=True):
+    """Gradients of L = <dy, y> with the routing held fixed (top-k is piecewise
+    constant), by the chain rule, in fp64.
+
+    Per routed pair (t,i), e = S_t[i], z = W1_e x_t = [a, b], h = silu(a) * b:
+      dgate[t,i] = <dy_t, W2_e h>
+      dh  = g * W2_e^T dy_t;  da = dh * b * silu'(a);  db = dh * silu(a)
+      dx_t += W1_e^T [da, db];  dW1_e += [da, db] x_t^T;  dW2_e += dy_t (g h)^T
+    Router: dlogits = router_backward(...); dx_t += Wr^T dl_t; dWr += dl_t x_t^T.
+    Shared expert: the same with g = 1 and no gate gradient.
+    """
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    T, H = x.shape
+    E = np.asarray(w1).shape[0]
+    F = np.asarray(w1).shape[1] // 2
+    idx = np.asarray(fwd["topk_idx"], np.int64)
+    gate = np.asarray(fwd["gates"], np.float64)
+    k = idx.shape[1]
+    dx = np.zeros_like(x)
+    dW1 = np.zeros((E, 2 * F, H))
+    dW2 = np.zeros((E, H, F))
+    dgate = np.zeros((T, k))
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        W1 = np.asarray(w1[e], np.float64)
+        W2 = np.asarray(w2[e], np.float64)
+        xe = x[tok]
+        z = xe @ W1.T
+        a, b = z[:, :F], z[:, F:]
+        h = silu(a) * b
+        g = gate[tok, slot][:, None]
+        dye = dy[tok]
+        dgate[tok, slot] = ((dye @ W2) * h).sum(axis=1)
+        dh = g * (dye @ W2)
+        da = dh * b * silu_grad(a)
+        db = dh * silu(a)
+        dz = np.concatenate([da, db], axis=1)
+        np.add.at(dx, tok, dz @ W1)
+        dW1[e] = dz.T @ xe
+        dW2[e] = dye.T @ (g * h)
+    out = {"dx": dx, "dW1": dW1, "dW2": dW2, "dgate": dgate}
+    if w1_shared is not None:
+        W1 = np.asarray(w1_shared, np.float64)
+        W2 = np.asarray(w2_shared, np.float64)
+        S = W1.shape[0] // 2
+        z = x @ W1.T
+        a, b = z[:, :S], z[:, S:]
+        h = silu(a) * b
+        dh = dy @ W2
+        dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
+        dx += dz @ W1
+        out["dW1_shared"] = dz.T @ x
+        out["dW2_shared"] = dy.T @ h
+    if with_router:
+        logits = fwd["logits"] if fwd.get("logits") is not None else router_logits(x, w_router)
+        dl = router_backward(logits, idx, gate, dgate, score)
+        dx += dl @ np.asarray(w_router, np.float64)
+        out["dlogits"] = dl
+        out["dWr"] = dl.T @ x
+    out["dx"] = dx
+    return out
+
+
+# ---------------------------------------------------------------------------
+# MXFP8: OCP Microscaling v1.0 (E8M0 block scale, 32 elements) with the
+# FP8 E4M3 element type (OCP 8-bit floating point v1.0: bias 7, no infinities,
+# largest finite 448, S.1111.111 is NaN).  Technical summary 2.5 names MXFP8 as
+# the Blackwell recipe; the block size 32 and element type are the MX format's.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+MX_BLOCK = 32
+E4M3_EMAX = 8          # exponent of the largest normal power of two, 2^8 = 256
+
+
+def e4m3_decode(code) -> np.ndarray:
+    """Value of each E4M3 bit pattern (uint8) as fp64; 0x7F / 0xFF give NaN."""
+    c = np.asarray(code, np.int64) & 0xFF
+    s = np.where(c & 0x80, -1.0, 1.0)
+    ex = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(ex == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(ex.astype(np.float64) - 7.0))
+    val = np.where((ex == 15) & (m == 7), np.nan, val)
+    return s * val
+
+
+def _round_half_even(v: np.ndarray) -> np.ndarray:
+    return np.round(v)          # numpy rounds halves to even
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Round fp64 values to E4M3, nearest-even, saturating to +-448 (the
+    'satfinite' behaviour).  Returns uint8 bit patterns.  Inputs must be finite."""
+    v = np.asarray(v, np.float64)
+    sign = np.signbit(v)
+    a = np.abs(v)
+    # quantisation step: 2^(p-3) for |v| in [2^p, 2^(p+1)), p >= -6; 2^-9 below 2^-6
+    _, p1 = np.frexp(a)                    # a = f * 2^p1, f in [0.5, 1)
+    p = np.maximum(p1 - 1, -6)
+    step = np.exp2((p - 3).astype(np.float64))
+    q = _round_half_even(a / step) * step
+    q = np.minimum(q, E4M3_MAX)
+    # encode q (now exactly representable)
+    _, qp1 = np.frexp(q)
+    qp = qp1 - 1
+    normal = q >= 2.0 ** -6
+    ex = np.where(normal, qp + 7, 0)
+    mant = np.where(normal, q / np.exp2(qp.astype(np.float64)) * 8.0 - 8.0, q / 2.0 ** -9)
+    code = (ex.astype(np.int64) << 3) | mant.astype(np.int64)
+    code = np.where(q == 0, 0, code)
+    code = code | np.where(sign, 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def mx_scale_exponent(amax) -> np.ndarray:
+    """Shared exponent of a block: floor(log2(amax)) - 8, clamped to E8M0's
+    range [-127, 127]; amax == 0 gives -127.  The X = 2^e rule of OCP MX v1.0
+    (the largest element lands in E4M3's top binade)."""
+    amax = np.asarray(amax, np.float64)
+    _, p1 = np.frexp(amax)
+    e = (p1 - 1) - E4M3_EMAX
+    e = np.where(amax == 0, -127, e)
+    return np.clip(e, -127, 127).astype(np.int64)
+
+
+def mxfp8_quantize(v, axis=-1):
+    """Quantise along ``axis`` in blocks of 32: returns (codes uint8, same shape;
+    scales uint8 E8M0 = exponent + 127, with the blocked axis divided by 32).
+    q = e4m3(v / 2^e) with e = mx_scale_exponent(max |v| over the block)."""
+    v = np.moveaxis(np.asarray(v, np.float64), axis, -1)
+    shp = v.shape
+    if shp[-1] % MX_BLOCK:
+        raise ValueError("blocked axis must be a multiple of 32")
+    blocks = v.reshape(shp[:-1] + (shp[-1] // MX_BLOCK, MX_BLOCK))
+    e = mx_scale_exponent(np.abs(blocks).max(axis=-1))
+    scaled = blocks / np.exp2(e.astype(np.float64))[..., None]
+    codes = e4m3_encode(scaled).reshape(shp)
+    scales = (e + 127).astype(np.uint8)
+    return np.moveaxis(codes, -1, axis), np.moveaxis(scales, -1, axis)
+
+
+def mxfp8_dequantize(codes, scales, axis=-1):
+    """Inverse map: value = e4m3(code) * 2^(scale - 127), block of 32 along axis."""
+    c = np.moveaxis(np.asarray(codes), axis, -1)
+    s = np.moveaxis(np.asarray(scales), axis, -1).astype(np.float64)
+    vals = e4m3_decode(c)
+    rep = np.repeat(np.exp2(s - 127.0), MX_BLOCK, axis=-1)
+    return np.moveaxis(vals * rep, -1, axis)
+
+
+def mxfp8_roundtrip(v, axis=-1):
+    """dequantize(quantize(v)) along axis: the operand an MXFP8 GEMM multiplies."""
+    c, s = mxfp8_quantize(v, axis)
+    return mxfp8_dequantize(c, s, axis)
