@@ -1,0 +1,261 @@
+/*
+ * moe_gb300.h — C ABI of the single-GPU Mixture-of-Experts expert layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer is the one the summary of "Scalable Training of Mixture-of-Experts
+ * Models with Megatron Core" describes:
+ *   - each token is sent to a few of many experts, the rest stay idle
+ *     (Problem, section 1);
+ *   - the router stays in high precision (technical summary 2.5, selective
+ *     precision);
+ *   - routing and permutation create dynamic shapes that must not cost host
+ *     synchronisation or many launches (technical summary 1, compute
+ *     efficiency wall); the GPU reads the shape information itself
+ *     (technical summary 2.4, sync-free kernels);
+ *   - all experts run in one grouped GEMM (technical summary 2.4);
+ *   - the routing weight is applied before the activation computation so that
+ *     backward needs no extra saved tensor (technical summary 2.2,
+ *     memory-efficient permutation).
+ * The pages give no API; the calls below follow that problem statement.
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers owned by the caller, row-major,
+ *     16-byte aligned.  The library allocates nothing in these calls.
+ *   - bf16 = IEEE bfloat16 (uint16 storage); fp32 = IEEE float.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  No call
+ *     synchronises the host or copies device data to the host, except
+ *     moe_read_device_status.
+ *   - Host-detectable errors return before any launch.  A launch failure
+ *     returns MOE_ERR_CUDA.  Errors found on the device (an expert index out
+ *     of range, a pipeline wait that timed out) are recorded in the status
+ *     word of the workspace; read it with moe_read_device_status.
+ *   - Only compute capability 10.3 (GB300) is supported; elsewhere every
+ *     compute call returns MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,  /* bad size, null pointer, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2,  /* not a GB300, or a shape outside the limits below */
+  MOE_ERR_CUDA = -3,         /* a CUDA runtime / driver call failed */
+  MOE_ERR_WORKSPACE = -4,    /* workspace or activation buffer too small */
+  MOE_ERR_BAD_INDEX = -5,    /* device: an expert index was outside [0, E) */
+  MOE_ERR_TIMEOUT = -6       /* device: a pipeline wait exceeded its limit */
+} moe_status;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+typedef enum { MOE_GEMM_BF16 = 0, MOE_GEMM_MXFP8 = 1 } moe_gemm_dtype;
+
+/* Layer shape.
+ *   T tokens, H hidden, E routed experts, k experts per token, F routed expert
+ *   SwiGLU width, S shared expert SwiGLU width (0 = no shared expert).
+ * Limits: 1 <= k <= 32, k <= E <= 256; H and F multiples of 128; S = 0 or a multiple
+ * of 128; 0 <= T and T*k < 2^31 - 128*E.
+ * score: softmax scoring selects on the raw logit and normalises exp(logit)
+ *   over the chosen k; sigmoid scoring selects on sigmoid(logit) + bias[e]
+ *   and normalises sigmoid(logit) over the chosen k.  Equal keys go to the
+ *   lower expert id.
+ */
+typedef struct {
+  int32_t T, H, E, k, F, S;
+  int32_t score;   /* moe_score_fn */
+  int32_t dtype;   /* moe_gemm_dtype (MOE_GEMM_BF16 only in this version) */
+} moe_config;
+
+/* Weights (device, bf16 unless noted).
+ *   w_router [E,H]; router_bias [E] fp32 or NULL (selection only);
+ *   w1 [E,2F,H]: rows 0..F-1 are the gate projection, rows F..2F-1 the up
+ *   projection; w2 [E,H,F]; w1_shared [2S,H], w2_shared [H,S] (NULL if S=0). */
+typedef struct {
+  const void* w_router;
+  const float* router_bias;
+  const void* w1;
+  const void* w2;
+  const void* w1_shared;
+  const void* w2_shared;
+} moe_weights;
+
+/* Weight gradients (device, fp32 outputs).  dw_router [E,H], dw1 [E,2F,H],
+ * dw2 [E,H,F], dw1_shared [2S,H], dw2_shared [H,S]. */
+typedef struct {
+  float* dw_router;
+  float* dw1;
+  float* dw2;
+  float* dw1_shared;
+  float* dw2_shared;
+} moe_grads;
+
+/* Byte offsets of the tensors kept in the activation buffer between the
+ * forward and the backward calls.  cap = rows of every expert-ordered buffer;
+ * each expert's rows start at a multiple of 128 ("padded offsets").
+ * Layout of each field:
+ *   logits fp32 [T,E]; topk_idx int32 [T,k] (descending key); topk_gate fp32 [T,k];
+ *   counts int32 [E]; offsets int32 [E+1] (compact); poffsets int32 [E+1] (padded);
+ *   slot_row int32 [T,k] (padded row of each (token, slot)); row_src int32 [cap]
+ *   (token of each padded row, -1 for padding); row_gate fp32 [cap] (0 for padding);
+ *   x_perm bf16 [cap,H]; z bf16 [cap,2F] (fc1 output); h bf16 [cap,F] (gate *
+ *   SwiGLU output); o bf16 [cap,H] (fc2 output);
+ *   zs bf16 [T,2S], hs bf16 [T,S], os bf16 [T,H] (shared expert, if S > 0);
+ *   backward only: dy_perm bf16 [cap,H]; dz bf16 [cap,2F]; dx_perm bf16 [cap,H];
+ *   dgate_part fp32 [cap, F/128]; dlogits fp32 [T,E]; row_dlogit fp32 [cap];
+ *   dzs bf16 [T,2S]; dxs bf16 [T,H].
+ * Fields that do not apply have offset SIZE_MAX. */
+typedef struct {
+  size_t logits, topk_idx, topk_gate, counts, offsets, poffsets, slot_row, row_src, row_gate;
+  size_t x_perm, z, h, o, zs, hs, os;
+  size_t dy_perm, dz, dx_perm, dgate_part, dlogits, row_dlogit, dzs, dxs;
+  size_t total;          /* bytes the activation buffer needs */
+  int32_t cap;           /* rows of the expert-ordered buffers */
+  int32_t backward;      /* 1 if the backward fields are present */
+} moe_act_layout;
+
+/* Name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t moe_version(void);
+
+/* Rows of the expert-ordered buffers: the worst case over all routings,
+ * T*k + 127*E rounded up to a multiple of 128.  Returns -1 on a bad config. */
+int32_t moe_capacity_rows(const moe_config* cfg);
+
+/* Fill `out` with the activation-buffer layout; with_backward = 1 adds the
+ * backward fields.  Host only. */
+moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, moe_act_layout* out);
+
+/* Bytes of scratch workspace every compute call below needs.  Host only.
+ * The workspace also holds the device status word; initialise it once with
+ * moe_workspace_init before first use. */
+size_t moe_workspace_bytes(const moe_config* cfg);
+
+/* Clear the device status word of `ws`.  Stream-ordered, does not block. */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then copy the device status word to *code
+ * (MOE_OK or the first device error since the last moe_workspace_init).
+ * The only call that blocks; keep it out of the hot path. */
+moe_status moe_read_device_status(const void* ws, int32_t* code, void* stream);
+
+/* --------------------------------------------------------------------------
+ * Step-level calls
+ * ----------------------------------------------------------------------- */
+
+/* Router GEMM and top-k gating.
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h]  (bf16 in, fp32 accumulate, fp32 out)
+ *   topk_idx[t,:] = the k experts with the largest key (key = logit for softmax,
+ *   sigmoid(logit) + bias[e] for sigmoid), by key descending, lower id first on ties;
+ *   topk_gate[t,:] = the normalised gates of those experts (fp32, sum to 1).
+ * x [T,H] bf16; w_router [E,H] bf16; bias [E] fp32 or NULL.
+ * Outputs: logits [T,E] fp32, topk_idx [T,k] int32, topk_gate [T,k] fp32. */
+moe_status moe_router_topk(const moe_config* cfg, const void* x, const void* w_router, const float* bias,
+                           float* logits, int32_t* topk_idx, float* topk_gate, void* ws, void* stream);
+
+/* Top-k gating of given fp32 logits (the second half of moe_router_topk). */
+moe_status moe_topk_gating(const moe_config* cfg, const float* logits, const float* bias, int32_t* topk_idx,
+                           float* topk_gate, void* stream);
+
+/* Sync-free permutation into expert-contiguous order (a stable counting sort
+ * of the T*k (token, slot) pairs by expert id; inside an expert, ascending
+ * token).  Any topk_idx may be given (router replay).  Outputs, all device:
+ *   counts [E], offsets [E+1], poffsets [E+1] (segments padded to 128 rows),
+ *   slot_row [T,k], row_src [cap] (-1 on padding), row_gate [cap] (topk_gate of
+ *   the pair, 0 on padding; topk_gate may be NULL, then row_gate is not written),
+ *   x_perm [cap,H] bf16 with x_perm[slot_row[t,i]] = x[t].  zero_pad = 1 also
+ *   zeroes the padding rows of x_perm (needed before weight gradients).
+ * An index outside [0,E) sets MOE_ERR_BAD_INDEX on the device; that pair is
+ * dropped and no out-of-range memory is written. */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_gate,
+                       int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
+                       int32_t* row_src, float* row_gate, void* x_perm, int32_t zero_pad, void* ws,
+                       void* stream);
+
+typedef enum {
+  /* z = A * W1_e^T, h = g * silu(z[:, :F]) * z[:, F:].  a = x_perm [cap,H],
+   * b = w1 [E,2F,H]; c = h [cap,F]; c2 = z [cap,2F] or NULL; row_gate [cap] or NULL (g = 1). */
+  MOE_GG_FC1_SWIGLU = 0,
+  /* o = A * W2_e^T.  a = h [cap,F], b = w2 [E,H,F]; c = o [cap,H]. */
+  MOE_GG_FC2 = 1,
+  /* dh = A * W2_e with A = dy_perm [cap,H], b = w2 [E,H,F]; epilogue with saved
+   * aux = z [cap,2F]: dz = [g dh b silu'(a), g dh silu(a)] -> c [cap,2F];
+   * dgate_part [cap, F/128] = partial sums of <dh, silu(a) b>. */
+  MOE_GG_DGRAD_FC2 = 2,
+  /* dx_perm = A * W1_e.  a = dz [cap,2F], b = w1 [E,2F,H]; c [cap,H]. */
+  MOE_GG_DGRAD_FC1 = 3,
+  /* dW1_e = A_e^T B_e over each expert's rows: a = dz [cap,2F], b = x_perm [cap,H];
+   * c = dw1 [E,2F,H] fp32 (zero for experts with no rows). */
+  MOE_GG_WGRAD_FC1 = 4,
+  /* dW2_e = A_e^T B_e: a = dy_perm [cap,H], b = h [cap,F]; c = dw2 [E,H,F] fp32. */
+  MOE_GG_WGRAD_FC2 = 5
+} moe_gg_op;
+
+/* Arguments of one grouped GEMM.  `poffsets` [E+1] (device) gives each expert's
+ * first padded row; the host never reads it.  With dense_rows > 0 the GEMM runs
+ * as one group of dense_rows rows instead (shared expert; poffsets ignored;
+ * for the WGRAD ops the contraction runs over dense_rows rows and c has one
+ * group).  Pass E in cfg as usual; the shapes H, F (or S for dense calls, see
+ * moe_grouped_gemm) come from cfg. */
+typedef struct {
+  int32_t op;             /* moe_gg_op */
+  int32_t dense_rows;     /* 0: routed; >0: one dense group of this many rows */
+  const void* a;
+  const void* b;
+  void* c;
+  void* c2;
+  const void* aux;
+  const float* row_gate;
+  float* dgate_part;
+  const int32_t* poffsets;
+} moe_gemm_args;
+
+/* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For
+ * dense calls (dense_rows > 0) the expert width is cfg->S if cfg->S > 0, else
+ * cfg->F. */
+moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, void* ws, void* stream);
+
+/* Combine: y[t] = sum_i o_perm[slot_row[t,i]] (+ shared_out[t]), summed in
+ * fp32 in slot order and rounded to bf16 once.  The gate is already inside
+ * o_perm (technical summary 2.2).  o_perm [cap,H] bf16, slot_row [T,k],
+ * shared_out [T,H] bf16 or NULL, y [T,H] bf16. */
+moe_status moe_unpermute(const moe_config* cfg, const void* o_perm, const int32_t* slot_row,
+                         const void* shared_out, void* y, void* stream);
+
+/* --------------------------------------------------------------------------
+ * Whole layer
+ * ----------------------------------------------------------------------- */
+
+/* Forward: y = sum_i g_i SwiGLU_{e_i}(x) (+ SharedSwiGLU(x)).
+ * x [T,H] bf16, y [T,H] bf16.  `act` holds everything backward needs (layout
+ * from moe_activation_layout(cfg, with_backward)); with_backward = 1 also
+ * zeroes the padding rows.  Fixed number of launches; no host sync. */
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, void* act,
+                             size_t act_bytes, int32_t with_backward, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward, data gradients.  Needs `act` from moe_layer_forward(with_backward=1)
+ * of the same x.  dy [T,H] bf16 -> dx [T,H] bf16 (through the experts, the
+ * shared expert and the router) and dgate [T,k] fp32 (NULL allowed).  Leaves
+ * the tensors the weight gradients need in `act`. */
+moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w, const void* x, const void* dy,
+                                    void* dx, float* dgate, void* act, size_t act_bytes, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* Backward, weight gradients (fp32, overwritten).  Call after
+ * moe_layer_backward_dgrad with the same `act`.  Experts that received no
+ * token get zero gradients.  x [T,H] bf16, dy [T,H] bf16. */
+moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w, const void* x, const void* dy,
+                                    const moe_grads* g, void* act, size_t act_bytes, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

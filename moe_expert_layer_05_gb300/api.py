@@ -1,0 +1,295 @@
+"""Python binding of libmoe_gb300.so (ctypes): the C-ABI calls under the same
+names, plus a small buffer holder that uses PyTorch only to allocate device
+memory and to pick the stream.  Every step of the layer runs in the library's
+CUDA kernels; there is no fallback path — if the library is missing or the GPU
+is not a GB300 the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+STATUS_NAMES = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error", -4: "workspace too small",
+                -5: "bad expert index", -6: "device wait timed out"}
+SCORE = {"softmax": 0, "sigmoid": 1}
+
+GG_FC1_SWIGLU, GG_FC2, GG_DGRAD_FC2, GG_DGRAD_FC1, GG_WGRAD_FC1, GG_WGRAD_FC2 = range(6)
+
+c_i32 = ctypes.c_int32
+c_vp = ctypes.c_void_p
+c_sz = ctypes.c_size_t
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", c_i32), ("H", c_i32), ("E", c_i32), ("k", c_i32), ("F", c_i32), ("S", c_i32),
+                ("score", c_i32), ("dtype", c_i32)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [("w_router", c_vp), ("router_bias", c_vp), ("w1", c_vp), ("w2", c_vp),
+                ("w1_shared", c_vp), ("w2_shared", c_vp)]
+
+
+class MoeGrads(ctypes.Structure):
+    _fields_ = [("dw_router", c_vp), ("dw1", c_vp), ("dw2", c_vp), ("dw1_shared", c_vp), ("dw2_shared", c_vp)]
+
+
+_LAYOUT_FIELDS = ["logits", "topk_idx", "topk_gate", "counts", "offsets", "poffsets", "slot_row", "row_src",
+                  "row_gate", "x_perm", "z", "h", "o", "zs", "hs", "os", "dy_perm", "dz", "dx_perm",
+                  "dgate_part", "dlogits", "row_dlogit", "dzs", "dxs"]
+
+
+class MoeActLayout(ctypes.Structure):
+    _fields_ = [(n, c_sz) for n in _LAYOUT_FIELDS] + [("total", c_sz), ("cap", c_i32), ("backward", c_i32)]
+
+
+class MoeGemmArgs(ctypes.Structure):
+    _fields_ = [("op", c_i32), ("dense_rows", c_i32), ("a", c_vp), ("b", c_vp), ("c", c_vp), ("c2", c_vp),
+                ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp)]
+
+
+_P = ctypes.POINTER
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [c_i32]),
+    "moe_version": (c_i32, []),
+    "moe_capacity_rows": (c_i32, [_P(MoeConfig)]),
+    "moe_activation_layout": (c_i32, [_P(MoeConfig), c_i32, _P(MoeActLayout)]),
+    "moe_workspace_bytes": (c_sz, [_P(MoeConfig)]),
+    "moe_workspace_init": (c_i32, [c_vp, c_sz, c_vp]),
+    "moe_read_device_status": (c_i32, [c_vp, _P(c_i32), c_vp]),
+    "moe_router_topk": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_topk_gating": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_permute": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
+                            c_vp, c_vp]),
+    "moe_grouped_gemm": (c_i32, [_P(MoeConfig), _P(MoeGemmArgs), c_vp, c_vp]),
+    "moe_unpermute": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_layer_forward": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_sz, c_i32, c_vp, c_sz,
+                                  c_vp]),
+    "moe_layer_backward_dgrad": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,
+                                         c_vp, c_sz, c_vp]),
+    "moe_layer_backward_wgrad": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, _P(MoeGrads), c_vp, c_sz,
+                                         c_vp, c_sz, c_vp]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libmoe_gb300.so (building it first if absent).  Raises if it cannot."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"libmoe_gb300.so not built ({path}); run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({code})")
+        self.code = code
+
+
+def check(code: int, what: str) -> None:
+    if code != MOE_OK:
+        raise MoeError(code, what)
+
+
+def ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def stream_ptr(stream=None) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def make_config(T, H, E, k, F, S=0, score="softmax", dtype="bf16") -> MoeConfig:
+    return MoeConfig(T, H, E, k, F, S, SCORE[score] if isinstance(score, str) else int(score),
+                     0 if dtype == "bf16" else 1)
+
+
+def config_of(workload, tokens: int | None = None) -> MoeConfig:
+    w = workload
+    return make_config(w.T if tokens is None else tokens, w.H, w.E, w.k, w.F, w.S, w.score, w.dtype)
+
+
+# ---------------------------------------------------------------- C calls, same names
+def moe_capacity_rows(cfg: MoeConfig) -> int:
+    return load().moe_capacity_rows(ctypes.byref(cfg))
+
+
+def moe_activation_layout(cfg: MoeConfig, with_backward: bool) -> MoeActLayout:
+    L = MoeActLayout()
+    check(load().moe_activation_layout(ctypes.byref(cfg), int(with_backward), ctypes.byref(L)),
+          "moe_activation_layout")
+    return L
+
+
+def moe_workspace_bytes(cfg: MoeConfig) -> int:
+    return load().moe_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    check(load().moe_workspace_init(ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)),
+          "moe_workspace_init")
+
+
+def moe_read_device_status(ws: torch.Tensor, stream=None) -> int:
+    code = c_i32(0)
+    check(load().moe_read_device_status(ptr(ws), ctypes.byref(code), stream_ptr(stream)), "moe_read_device_status")
+    return code.value
+
+
+def moe_router_topk(cfg, x, w_router, bias, logits, topk_idx, topk_gate, ws, stream=None) -> None:
+    check(load().moe_router_topk(ctypes.byref(cfg), ptr(x), ptr(w_router), ptr(bias), ptr(logits), ptr(topk_idx),
+                                 ptr(topk_gate), ptr(ws), stream_ptr(stream)), "moe_router_topk")
+
+
+def moe_topk_gating(cfg, logits, bias, topk_idx, topk_gate, stream=None) -> None:
+    check(load().moe_topk_gating(ctypes.byref(cfg), ptr(logits), ptr(bias), ptr(topk_idx), ptr(topk_gate),
+                                 stream_ptr(stream)), "moe_topk_gating")
+
+
+def moe_permute(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, slot_row, row_src, row_gate, x_perm,
+                zero_pad, ws, stream=None) -> None:
+    check(load().moe_permute(ctypes.byref(cfg), ptr(x), ptr(topk_idx), ptr(topk_gate), ptr(counts), ptr(offsets),
+                             ptr(poffsets), ptr(slot_row), ptr(row_src), ptr(row_gate), ptr(x_perm), int(zero_pad),
+                             ptr(ws), stream_ptr(stream)), "moe_permute")
+
+
+def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
+                     dense_rows=0, stream=None) -> None:
+    args = MoeGemmArgs(op, dense_rows, ptr(a), ptr(b), ptr(c), ptr(c2), ptr(aux), ptr(row_gate), ptr(dgate_part),
+                       ptr(poffsets))
+    check(load().moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), ptr(ws), stream_ptr(stream)),
+          "moe_grouped_gemm")
+
+
+def moe_unpermute(cfg, o_perm, slot_row, shared_out, y, stream=None) -> None:
+    check(load().moe_unpermute(ctypes.byref(cfg), ptr(o_perm), ptr(slot_row), ptr(shared_out), ptr(y),
+                               stream_ptr(stream)), "moe_unpermute")
+
+
+def moe_layer_forward(cfg, weights: MoeWeights, x, y, act, with_backward, ws, stream=None) -> None:
+    check(load().moe_layer_forward(ctypes.byref(cfg), ctypes.byref(weights), ptr(x), ptr(y), ptr(act),
+                                   act.numel() * act.element_size(), int(with_backward), ptr(ws),
+                                   ws.numel() * ws.element_size(), stream_ptr(stream)), "moe_layer_forward")
+
+
+def moe_layer_backward_dgrad(cfg, weights: MoeWeights, x, dy, dx, dgate, act, ws, stream=None) -> None:
+    check(load().moe_layer_backward_dgrad(ctypes.byref(cfg), ctypes.byref(weights), ptr(x), ptr(dy), ptr(dx),
+                                          ptr(dgate), ptr(act), act.numel() * act.element_size(), ptr(ws),
+                                          ws.numel() * ws.element_size(), stream_ptr(stream)),
+          "moe_layer_backward_dgrad")
+
+
+def moe_layer_backward_wgrad(cfg, weights: MoeWeights, x, dy, grads: MoeGrads, act, ws, stream=None) -> None:
+    check(load().moe_layer_backward_wgrad(ctypes.byref(cfg), ctypes.byref(weights), ptr(x), ptr(dy),
+                                          ctypes.byref(grads), ptr(act), act.numel() * act.element_size(),
+                                          ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)),
+          "moe_layer_backward_wgrad")
+
+
+# ---------------------------------------------------------------- buffers
+class MoELayer:
+    """Device buffers for one layer shape (weights are the caller's tensors).
+
+    Owns the activation buffer and the workspace (torch.uint8 device tensors)
+    and exposes views of the activation fields for inspection.
+    """
+
+    def __init__(self, cfg: MoeConfig, weights: dict, with_backward: bool = False, device="cuda"):
+        self.cfg = cfg
+        self.with_backward = with_backward
+        self.w = weights
+        self.layout = moe_activation_layout(cfg, with_backward)
+        self.act = torch.empty(self.layout.total, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(moe_workspace_bytes(cfg), 256), dtype=torch.uint8, device=device)
+        moe_workspace_init(self.ws)
+        self.cw = MoeWeights(ptr(weights["w_router"]), ptr(weights.get("bias")), ptr(weights["w1"]),
+                             ptr(weights["w2"]), ptr(weights.get("w1_shared")), ptr(weights.get("w2_shared")))
+
+    def view(self, name: str, dtype, shape) -> torch.Tensor:
+        off = getattr(self.layout, name)
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.act[off:off + nbytes].view(dtype).view(*shape)
+
+    def fields(self) -> dict:
+        c = self.cfg
+        cap = self.layout.cap
+        d = {
+            "logits": self.view("logits", torch.float32, (c.T, c.E)),
+            "topk_idx": self.view("topk_idx", torch.int32, (c.T, c.k)),
+            "topk_gate": self.view("topk_gate", torch.float32, (c.T, c.k)),
+            "counts": self.view("counts", torch.int32, (c.E,)),
+            "offsets": self.view("offsets", torch.int32, (c.E + 1,)),
+            "poffsets": self.view("poffsets", torch.int32, (c.E + 1,)),
+            "slot_row": self.view("slot_row", torch.int32, (c.T, c.k)),
+            "row_src": self.view("row_src", torch.int32, (cap,)),
+            "row_gate": self.view("row_gate", torch.float32, (cap,)),
+            "x_perm": self.view("x_perm", torch.bfloat16, (cap, c.H)),
+            "z": self.view("z", torch.bfloat16, (cap, 2 * c.F)),
+            "h": self.view("h", torch.bfloat16, (cap, c.F)),
+            "o": self.view("o", torch.bfloat16, (cap, c.H)),
+        }
+        if self.with_backward:
+            d.update({
+                "dy_perm": self.view("dy_perm", torch.bfloat16, (cap, c.H)),
+                "dz": self.view("dz", torch.bfloat16, (cap, 2 * c.F)),
+                "dx_perm": self.view("dx_perm", torch.bfloat16, (cap, c.H)),
+                "dlogits": self.view("dlogits", torch.float32, (c.T, c.E)),
+            })
+        return d
+
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty_like(x)
+        moe_layer_forward(self.cfg, self.cw, x, y, self.act, self.with_backward, self.ws, stream)
+        return y
+
+    def backward(self, x, dy, grads: dict | None = None, dx=None, dgate=None, stream=None):
+        c = self.cfg
+        dev = x.device
+        if dx is None:
+            dx = torch.empty_like(x)
+        if dgate is None:
+            dgate = torch.empty((c.T, c.k), dtype=torch.float32, device=dev)
+        if grads is None:
+            grads = {"dw_router": torch.empty((c.E, c.H), dtype=torch.float32, device=dev),
+                     "dw1": torch.empty((c.E, 2 * c.F, c.H), dtype=torch.float32, device=dev),
+                     "dw2": torch.empty((c.E, c.H, c.F), dtype=torch.float32, device=dev)}
+            if c.S > 0:
+                grads["dw1_shared"] = torch.empty((2 * c.S, c.H), dtype=torch.float32, device=dev)
+                grads["dw2_shared"] = torch.empty((c.H, c.S), dtype=torch.float32, device=dev)
+        moe_layer_backward_dgrad(c, self.cw, x, dy, dx, dgate, self.act, self.ws, stream)
+        g = MoeGrads(ptr(grads["dw_router"]), ptr(grads["dw1"]), ptr(grads["dw2"]), ptr(grads.get("dw1_shared")),
+                     ptr(grads.get("dw2_shared")))
+        moe_layer_backward_wgrad(c, self.cw, x, dy, g, self.act, self.ws, stream)
+        return dx, dgate, grads

@@ -1,0 +1,413 @@
+// C ABI of the library (declared in include/moe_gb300.h): argument checks on
+// the host, buffer layouts, and the fixed launch sequences of the layer's
+// forward and backward passes.  No call here allocates device memory,
+// synchronises, or reads a device value on the host.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_gb300.h"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+struct DevInfo {
+  int sms = 0;
+  bool gb300 = false;
+  bool probed = false;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+DevInfo& dev_info() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) {
+    static DevInfo none;
+    return none;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& info = g_dev[d];
+  if (!info.probed) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+    info.sms = sms > 0 ? sms : 1;
+    info.gb300 = (major == 10 && minor == 3);
+    info.probed = true;
+  }
+  return info;
+}
+}  // namespace
+
+int num_sms() { return dev_info().sms; }
+bool device_is_gb300() { return dev_info().gb300; }
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;   // status word region at the start of the workspace
+constexpr size_t kNone = SIZE_MAX;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool config_ok(const moe_config* c) {
+  if (c == nullptr) return false;
+  if (c->T < 0 || c->H <= 0 || c->E <= 0 || c->k <= 0 || c->F <= 0 || c->S < 0) return false;
+  if (c->k > kMaxK || c->k > c->E || c->E > kMaxE) return false;
+  if (c->H % 128 || c->F % 128 || c->S % 128) return false;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return false;
+  if (c->dtype != MOE_GEMM_BF16) return false;
+  const long long pairs = static_cast<long long>(c->T) * c->k;
+  if (pairs + 128LL * c->E >= (1LL << 31)) return false;
+  return true;
+}
+
+int cap_rows(const moe_config* c) {
+  const long long r = static_cast<long long>(c->T) * c->k + 127LL * c->E;
+  return static_cast<int>((r + 127) / 128 * 128);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dev_ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                   \
+  do {                                                  \
+    cudaError_t e_ = (expr);                            \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;         \
+  } while (0)
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+size_t hist_bytes(const moe_config* c) {
+  const long long pairs = static_cast<long long>(c->T) * c->k;
+  const long long nb = (pairs + kPairsPerBlock - 1) / kPairsPerBlock;
+  return static_cast<size_t>(nb) * c->E * sizeof(int32_t);
+}
+
+moe_status compute_layout(const moe_config* c, int with_bwd, moe_act_layout* L) {
+  if (!config_ok(c) || L == nullptr) return MOE_ERR_INVALID_ARG;
+  const size_t T = c->T, H = c->H, E = c->E, k = c->k, F = c->F, S = c->S;
+  const size_t cap = static_cast<size_t>(cap_rows(c));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + (bytes == 0 ? 1 : bytes));
+    return o;
+  };
+  L->cap = static_cast<int32_t>(cap);
+  L->backward = with_bwd ? 1 : 0;
+  L->logits = take(T * E * 4);
+  L->topk_idx = take(T * k * 4);
+  L->topk_gate = take(T * k * 4);
+  L->counts = take(E * 4);
+  L->offsets = take((E + 1) * 4);
+  L->poffsets = take((E + 1) * 4);
+  L->slot_row = take(T * k * 4);
+  L->row_src = take(cap * 4);
+  L->row_gate = take(cap * 4);
+  L->x_perm = take(cap * H * 2);
+  L->z = take(cap * 2 * F * 2);
+  L->h = take(cap * F * 2);
+  L->o = take(cap * H * 2);
+  if (S > 0) {
+    L->zs = take(T * 2 * S * 2);
+    L->hs = take(T * S * 2);
+    L->os = take(T * H * 2);
+  } else {
+    L->zs = L->hs = L->os = kNone;
+  }
+  if (with_bwd) {
+    L->dy_perm = take(cap * H * 2);
+    L->dz = take(cap * 2 * F * 2);
+    L->dx_perm = take(cap * H * 2);
+    L->dgate_part = take(cap * (F / 128) * 4);
+    L->dlogits = take(T * E * 4);
+    L->row_dlogit = take(cap * 4);
+    if (S > 0) {
+      L->dzs = take(T * 2 * S * 2);
+      L->dxs = take(T * H * 2);
+    } else {
+      L->dzs = L->dxs = kNone;
+    }
+  } else {
+    L->dy_perm = L->dz = L->dx_perm = L->dgate_part = L->dlogits = L->row_dlogit = L->dzs = L->dxs = kNone;
+  }
+  L->total = off;
+  return MOE_OK;
+}
+
+moe_status check_device() { return device_is_gb300() ? MOE_OK : MOE_ERR_UNSUPPORTED; }
+
+int* status_ptr(void* ws) { return static_cast<int*>(ws); }
+int32_t* hist_ptr(void* ws) { return at<int32_t>(ws, kStatusBytes); }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_WORKSPACE: return "workspace or activation buffer too small";
+    case MOE_ERR_BAD_INDEX: return "expert index out of range";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t moe_version(void) { return 0x000100; }
+
+int32_t moe_capacity_rows(const moe_config* cfg) { return config_ok(cfg) ? cap_rows(cfg) : -1; }
+
+moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, moe_act_layout* out) {
+  return compute_layout(cfg, with_backward, out);
+}
+
+size_t moe_workspace_bytes(const moe_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return kStatusBytes + align_up(hist_bytes(cfg));
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!dev_ptr_ok(ws) || ws_bytes < kStatusBytes) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, kStatusBytes, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_read_device_status(const void* ws, int32_t* code, void* stream) {
+  if (!dev_ptr_ok(ws) || code == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(cudaStreamSynchronize(st));
+  int32_t v = 0;
+  MOE_TRY(cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost));
+  *code = v;
+  return MOE_OK;
+}
+
+moe_status moe_topk_gating(const moe_config* cfg, const float* logits, const float* bias, int32_t* topk_idx,
+                           float* topk_gate, void* stream) {
+  if (!config_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(logits) || !dev_ptr_ok(topk_idx) || !dev_ptr_ok(topk_gate)))
+    return MOE_ERR_INVALID_ARG;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  return cuda_status(launch_topk(logits, cfg->score == MOE_SCORE_SIGMOID ? bias : nullptr, cfg->T, cfg->E, cfg->k,
+                                 cfg->score, topk_idx, topk_gate, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router_topk(const moe_config* cfg, const void* x, const void* w_router, const float* bias,
+                           float* logits, int32_t* topk_idx, float* topk_gate, void* ws, void* stream) {
+  if (!config_ok(cfg) || !dev_ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(w_router) || !dev_ptr_ok(logits) || !dev_ptr_ok(topk_idx) ||
+                     !dev_ptr_ok(topk_gate)))
+    return MOE_ERR_INVALID_ARG;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(gemm_router(x, w_router, cfg->T, cfg->H, cfg->E, logits, status_ptr(ws), st));
+  return moe_topk_gating(cfg, logits, bias, topk_idx, topk_gate, stream);
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_gate,
+                       int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row, int32_t* row_src,
+                       float* row_gate, void* x_perm, int32_t zero_pad, void* ws, void* stream) {
+  if (!config_ok(cfg) || !dev_ptr_ok(ws) || !dev_ptr_ok(counts) || !dev_ptr_ok(offsets) || !dev_ptr_ok(poffsets) ||
+      !dev_ptr_ok(row_src) || !dev_ptr_ok(x_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(topk_idx) || !dev_ptr_ok(slot_row))) return MOE_ERR_INVALID_ARG;
+  if (topk_gate != nullptr && !dev_ptr_ok(row_gate)) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(launch_permute_maps(topk_idx, topk_gate, cfg->T, cfg->E, cfg->k, hist_ptr(ws), counts, offsets, poffsets,
+                              slot_row, row_src, topk_gate != nullptr ? row_gate : nullptr, status_ptr(ws), st));
+  MOE_TRY(launch_gather_rows(x, slot_row, cfg->T, cfg->k, cfg->H, x_perm, st));
+  if (zero_pad) MOE_TRY(launch_zero_pad_rows(counts, poffsets, cfg->E, cfg->H, x_perm, st));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void* ws, void* stream) {
+  if (!config_ok(cfg) || a == nullptr || !dev_ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
+  if (!dev_ptr_ok(a->a) || !dev_ptr_ok(a->b) || !dev_ptr_ok(a->c)) return MOE_ERR_INVALID_ARG;
+  const bool dense = a->dense_rows > 0;
+  if (!dense && !dev_ptr_ok(a->poffsets)) return MOE_ERR_INVALID_ARG;
+  if (a->dense_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int H = cfg->H;
+  const int F = dense ? (cfg->S > 0 ? cfg->S : cfg->F) : cfg->F;
+  const int E = dense ? 1 : cfg->E;
+  const int rows = dense ? a->dense_rows : cap_rows(cfg);
+  const int32_t* po = dense ? nullptr : a->poffsets;
+  int* status = status_ptr(ws);
+  switch (a->op) {
+    case MOE_GG_FC1_SWIGLU:
+      if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
+      return cuda_status(gemm_fc1(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->row_gate, a->c, a->c2, status, st));
+    case MOE_GG_FC2:
+      return cuda_status(gemm_fc2(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st));
+    case MOE_GG_DGRAD_FC2:
+      if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
+      return cuda_status(gemm_dgrad_fc2(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->aux, a->row_gate, a->c,
+                                        a->dgate_part, status, st));
+    case MOE_GG_DGRAD_FC1:
+      return cuda_status(gemm_dgrad_fc1(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st));
+    case MOE_GG_WGRAD_FC1:
+      return cuda_status(gemm_wgrad(a->a, 2 * F, a->b, H, rows, E, po, a->dense_rows, static_cast<float*>(a->c),
+                                    status, st));
+    case MOE_GG_WGRAD_FC2:
+      return cuda_status(gemm_wgrad(a->a, H, a->b, F, rows, E, po, a->dense_rows, static_cast<float*>(a->c),
+                                    status, st));
+    default:
+      return MOE_ERR_INVALID_ARG;
+  }
+}
+
+moe_status moe_unpermute(const moe_config* cfg, const void* o_perm, const int32_t* slot_row, const void* shared_out,
+                         void* y, void* stream) {
+  if (!config_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(o_perm) || !dev_ptr_ok(slot_row) || !dev_ptr_ok(y))) return MOE_ERR_INVALID_ARG;
+  if (shared_out != nullptr && !aligned16(shared_out)) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  return cuda_status(launch_combine(o_perm, slot_row, shared_out, cfg->T, cfg->k, cfg->H, y,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, void* act,
+                             size_t act_bytes, int32_t with_backward, void* ws, size_t ws_bytes, void* stream) {
+  moe_act_layout L;
+  if (compute_layout(cfg, with_backward, &L) != MOE_OK || w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!dev_ptr_ok(act) || !dev_ptr_ok(ws) || !dev_ptr_ok(w->w_router) || !dev_ptr_ok(w->w1) || !dev_ptr_ok(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(y))) return MOE_ERR_INVALID_ARG;
+  if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
+  if (w->router_bias != nullptr && !aligned16(w->router_bias)) return MOE_ERR_INVALID_ARG;
+  if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = cfg->T, H = cfg->H, E = cfg->E, k = cfg->k, F = cfg->F, S = cfg->S, cap = L.cap;
+  int* status = status_ptr(ws);
+  float* logits = at<float>(act, L.logits);
+  int32_t* idx = at<int32_t>(act, L.topk_idx);
+  float* gate = at<float>(act, L.topk_gate);
+  int32_t* counts = at<int32_t>(act, L.counts);
+  int32_t* poff = at<int32_t>(act, L.poffsets);
+  int32_t* slot_row = at<int32_t>(act, L.slot_row);
+  float* row_gate = at<float>(act, L.row_gate);
+  void* x_perm = at<void>(act, L.x_perm);
+  void* h = at<void>(act, L.h);
+  void* o = at<void>(act, L.o);
+
+  // 1-2: router GEMM + top-k gating
+  MOE_TRY(gemm_router(x, w->w_router, T, H, E, logits, status, st));
+  MOE_TRY(launch_topk(logits, cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr, T, E, k, cfg->score, idx,
+                      gate, st));
+  // 3-4: sync-free permutation
+  MOE_TRY(launch_permute_maps(idx, gate, T, E, k, hist_ptr(ws), counts, at<int32_t>(act, L.offsets), poff, slot_row,
+                              at<int32_t>(act, L.row_src), row_gate, status, st));
+  MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
+  if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
+  // 5-6: grouped expert GEMMs; the gate multiplies the SwiGLU output inside fc1
+  MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, with_backward ? at<void>(act, L.z) : nullptr,
+                   status, st));
+  MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st));
+  const void* shared_out = nullptr;
+  if (S > 0 && T > 0) {
+    MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
+                     with_backward ? at<void>(act, L.zs) : nullptr, status, st));
+    MOE_TRY(gemm_fc2(at<void>(act, L.hs), T, S, w->w2_shared, 1, H, nullptr, T, at<void>(act, L.os), status, st));
+    shared_out = at<void>(act, L.os);
+  }
+  // 7: unweighted combine
+  MOE_TRY(launch_combine(o, slot_row, shared_out, T, k, H, y, st));
+  return MOE_OK;
+}
+
+moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w, const void* x, const void* dy,
+                                    void* dx, float* dgate, void* act, size_t act_bytes, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  moe_act_layout L;
+  if (compute_layout(cfg, 1, &L) != MOE_OK || w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!dev_ptr_ok(act) || !dev_ptr_ok(ws) || !dev_ptr_ok(w->w_router) || !dev_ptr_ok(w->w1) || !dev_ptr_ok(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(dy) || !dev_ptr_ok(dx))) return MOE_ERR_INVALID_ARG;
+  if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
+  if (dgate != nullptr && !aligned16(dgate)) return MOE_ERR_INVALID_ARG;
+  if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = cfg->T, H = cfg->H, E = cfg->E, k = cfg->k, F = cfg->F, S = cfg->S, cap = L.cap;
+  int* status = status_ptr(ws);
+  const int32_t* counts = at<int32_t>(act, L.counts);
+  const int32_t* poff = at<int32_t>(act, L.poffsets);
+  const int32_t* slot_row = at<int32_t>(act, L.slot_row);
+  void* dy_perm = at<void>(act, L.dy_perm);
+  void* dz = at<void>(act, L.dz);
+  void* dx_perm = at<void>(act, L.dx_perm);
+  float* dpart = at<float>(act, L.dgate_part);
+
+  MOE_TRY(launch_gather_rows(dy, slot_row, T, k, H, dy_perm, st));
+  MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, dy_perm, st));
+  MOE_TRY(gemm_dgrad_fc2(dy_perm, cap, H, w->w2, E, F, poff, 0, at<void>(act, L.z), at<float>(act, L.row_gate), dz,
+                         dpart, status, st));
+  MOE_TRY(gemm_dgrad_fc1(dz, cap, F, w->w1, E, H, poff, 0, dx_perm, status, st));
+  const void* dxs = nullptr;
+  if (S > 0 && T > 0) {
+    MOE_TRY(gemm_dgrad_fc2(dy, T, H, w->w2_shared, 1, S, nullptr, T, at<void>(act, L.zs), nullptr,
+                           at<void>(act, L.dzs), nullptr, status, st));
+    MOE_TRY(gemm_dgrad_fc1(at<void>(act, L.dzs), T, S, w->w1_shared, 1, H, nullptr, T, at<void>(act, L.dxs), status,
+                           st));
+    dxs = at<void>(act, L.dxs);
+  }
+  MOE_TRY(launch_dgrad_combine(dx_perm, slot_row, at<int32_t>(act, L.topk_idx), at<float>(act, L.topk_gate),
+                               at<float>(act, L.logits), dpart, F / 128, w->w_router, dxs, T, E, k, H, cfg->score, dx,
+                               dgate, at<float>(act, L.dlogits), at<float>(act, L.row_dlogit), st));
+  return MOE_OK;
+}
+
+moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w, const void* x, const void* dy,
+                                    const moe_grads* g, void* act, size_t act_bytes, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  moe_act_layout L;
+  if (compute_layout(cfg, 1, &L) != MOE_OK || w == nullptr || g == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!dev_ptr_ok(act) || !dev_ptr_ok(ws) || !dev_ptr_ok(g->dw_router) || !dev_ptr_ok(g->dw1) ||
+      !dev_ptr_ok(g->dw2))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(dy))) return MOE_ERR_INVALID_ARG;
+  if (cfg->S > 0 && (!dev_ptr_ok(g->dw1_shared) || !dev_ptr_ok(g->dw2_shared))) return MOE_ERR_INVALID_ARG;
+  if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = cfg->T, H = cfg->H, E = cfg->E, F = cfg->F, S = cfg->S, cap = L.cap;
+  int* status = status_ptr(ws);
+  const int32_t* counts = at<int32_t>(act, L.counts);
+  const int32_t* poff = at<int32_t>(act, L.poffsets);
+  MOE_TRY(gemm_wgrad(at<void>(act, L.dz), 2 * F, at<void>(act, L.x_perm), H, cap, E, poff, 0, g->dw1, status, st));
+  MOE_TRY(gemm_wgrad(at<void>(act, L.dy_perm), H, at<void>(act, L.h), F, cap, E, poff, 0, g->dw2, status, st));
+  MOE_TRY(launch_router_wgrad(at<void>(act, L.x_perm), at<float>(act, L.row_dlogit), counts, poff, E, H,
+                              g->dw_router, st));
+  if (S > 0) {
+    if (T > 0) {
+      MOE_TRY(gemm_wgrad(at<void>(act, L.dzs), 2 * S, x, H, T, 1, nullptr, T, g->dw1_shared, status, st));
+      MOE_TRY(gemm_wgrad(dy, H, at<void>(act, L.hs), S, T, 1, nullptr, T, g->dw2_shared, status, st));
+    } else {
+      MOE_TRY(cudaMemsetAsync(g->dw1_shared, 0, sizeof(float) * 2 * S * H, st));
+      MOE_TRY(cudaMemsetAsync(g->dw2_shared, 0, sizeof(float) * S * H, st));
+    }
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

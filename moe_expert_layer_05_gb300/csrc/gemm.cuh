@@ -1,0 +1,506 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// One CTA per SM walks a list of 128 x BN output tiles.  Warp roles:
+//   warp 0      TMA producer: streams A and B k-blocks (64 bf16 = one 128-B
+//               swizzle row) into a STAGES-deep shared-memory ring;
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
+//               K=16) into one of two TMEM accumulators;
+//   warps 2..5  epilogue: tcgen05.ld the finished accumulator (warp w reads
+//               TMEM lanes 32*(w%4)..+31, i.e. one output row per thread),
+//               apply the fused elementwise step and store to global memory,
+//               while the MMA warp already fills the other accumulator.
+//
+// Group shapes never reach the host.  For routed problems the kernel reads
+// the padded per-expert row offsets (every expert segment is a whole number of
+// 128-row tiles) from device memory and derives its tile list from them: this
+// is the grouped GEMM with device-side shapes that the Megatron Core MoE
+// summary describes (technical summary 2.4, grouped GEMM and sync-free
+// kernels).
+#pragma once
+#include "ptx.cuh"
+
+namespace moe {
+
+enum class Sched : int {
+  kRoutedM = 0,  // rows grouped by expert (padded offsets on device), K fixed
+  kDenseM = 1,   // one group of m_rows rows
+  kRoutedK = 2,  // contraction over each expert's rows (weight gradients)
+};
+
+enum class Epi : int {
+  kStoreF32 = 0,    // fp32 accumulator -> fp32
+  kStoreBf16 = 1,   // -> bf16
+  kSwiglu = 2,      // z = [gate | up] -> h = g * silu(gate) * up (bf16), z saved (bf16)
+  kSwigluBwd = 3,   // dh -> dz = [dgate_in | dup] (bf16) and partial <dh, h> per row
+};
+
+struct GemmParams {
+  const int* poffsets;     // [E+1] padded row offsets (kRoutedM, kRoutedK); nullptr = one group
+  int E;                   // number of groups
+  int m_rows;              // kDenseM: rows; kRoutedK: output rows per group
+  int k_len;               // contraction length (kRoutedM, kDenseM); kRoutedK without poffsets: rows
+  int n_tiles;             // output tiles along N
+  int m_tiles_w;           // kRoutedK: output tiles along M per group
+  int b_rows_per_group;    // rows of B's 2-D view that belong to one group
+  int b_half_offset;       // kSwiglu: row offset of the "up" half inside a group of B
+  void* c;                 // primary output
+  long long ldc;           // its row stride (elements)
+  long long c_group_stride;// kRoutedK: elements between groups of the output
+  void* c2;                // kSwiglu: z (nullable)
+  long long ldc2;
+  int half_cols;           // kSwiglu / kSwigluBwd: F (column offset of the up half in z / dz)
+  const __nv_bfloat16* aux;// kSwigluBwd: saved z
+  long long ld_aux;
+  const float* row_gate;   // per output row gate (nullptr: 1.0)
+  float* dgate_part;       // kSwigluBwd: [rows, n_tiles] partial dot products
+  int valid_cols;          // kStoreF32: store only columns < valid_cols
+  int rows_cap;            // rows allocated in the expert-ordered buffers (routed modes)
+  int* status;             // device status word (first error wins)
+};
+
+template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int BK = 64;
+  static constexpr int BN = BN_;
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
+  static constexpr Sched S = S_;
+  static constexpr Epi EP = EP_;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  static constexpr int TMEM_COLS_RAW = 2 * BN;
+  static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
+                                   : TMEM_COLS_RAW <= 128 ? 128 : TMEM_COLS_RAW <= 256 ? 256 : 512;
+  // Rows of one K-major B box (the SwiGLU tile loads gate and up halves as two boxes).
+  static constexpr int B_BOX_ROWS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
+  // Columns of the output a tile covers (SwiGLU: half of the accumulator).
+  static constexpr int OUT_COLS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
+  static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
+  static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile holds 128 gate + 128 up columns");
+  static_assert(STAGES >= 2, "pipeline depth");
+};
+
+struct TileInfo {
+  int group;     // expert
+  int m0;        // first A row (kRoutedM / kDenseM) or first output row (kRoutedK)
+  int n;         // N tile index
+  int num_kb;    // k-blocks
+  int k_row0;    // kRoutedK: first contraction row
+};
+
+template <class C>
+__device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_poff) {
+  if constexpr (C::S == Sched::kRoutedM) {
+    return (s_poff[p.E] / C::BM) * p.n_tiles;
+  } else if constexpr (C::S == Sched::kDenseM) {
+    return ((p.m_rows + C::BM - 1) / C::BM) * p.n_tiles;
+  } else {
+    return p.E * p.m_tiles_w * p.n_tiles;
+  }
+}
+
+template <class C>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_poff, int t) {
+  TileInfo ti;
+  if constexpr (C::S == Sched::kRoutedM) {
+    // largest e with (poff[e]/BM)*n_tiles <= t; empty experts share a prefix
+    // with the next one, so the result is always a non-empty expert.
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((s_poff[mid] / C::BM) * p.n_tiles <= t) lo = mid; else hi = mid - 1;
+    }
+    const int local = t - (s_poff[lo] / C::BM) * p.n_tiles;
+    const int mt = (s_poff[lo + 1] - s_poff[lo]) / C::BM;
+    ti.group = lo;
+    ti.n = local / mt;                       // n outer: a B panel stays hot in L2
+    ti.m0 = s_poff[lo] + (local % mt) * C::BM;
+    ti.num_kb = p.k_len / C::BK;
+    ti.k_row0 = 0;
+  } else if constexpr (C::S == Sched::kDenseM) {
+    const int mb = (p.m_rows + C::BM - 1) / C::BM;
+    ti.group = 0;
+    ti.n = t / mb;
+    ti.m0 = (t % mb) * C::BM;
+    ti.num_kb = p.k_len / C::BK;
+    ti.k_row0 = 0;
+  } else {
+    const int per = p.m_tiles_w * p.n_tiles;
+    ti.group = t / per;
+    const int r = t % per;
+    ti.m0 = (r / p.n_tiles) * C::BM;
+    ti.n = r % p.n_tiles;
+    if (p.poffsets != nullptr) {
+      ti.k_row0 = s_poff[ti.group];
+      ti.num_kb = (s_poff[ti.group + 1] - s_poff[ti.group]) / C::BK;
+    } else {
+      ti.k_row0 = 0;
+      ti.num_kb = (p.k_len + C::BK - 1) / C::BK;
+    }
+  }
+  return ti;
+}
+
+template <class C>
+__device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p,
+                                            const TileInfo& ti, int kb, uint8_t* a_dst, uint8_t* b_dst,
+                                            uint64_t* bar) {
+  const int k0 = kb * C::BK;
+  // ---- A
+  if constexpr (C::S == Sched::kRoutedK) {
+    // A[m, k] = Abuf[k_row0 + k, m0 + m]  (MN-major, two 64-wide chunks)
+    tma_load_2d(a_dst, tmA, bar, ti.m0, ti.k_row0 + k0);
+    tma_load_2d(a_dst + 8192, tmA, bar, ti.m0 + 64, ti.k_row0 + k0);
+  } else {
+    tma_load_2d(a_dst, tmA, bar, k0, ti.m0);
+  }
+  // ---- B
+  if constexpr (C::S == Sched::kRoutedK) {
+    #pragma unroll
+    for (int j = 0; j < C::BN / 64; ++j)
+      tma_load_2d(b_dst + j * 8192, tmB, bar, ti.n * C::BN + j * 64, ti.k_row0 + k0);
+  } else if constexpr (C::B_MN) {
+    // B[n, k] = W[group*K + k, n]   (weights stored [K, N] per group, N contiguous)
+    #pragma unroll
+    for (int j = 0; j < C::BN / 64; ++j)
+      tma_load_2d(b_dst + j * 8192, tmB, bar, ti.n * C::BN + j * 64, ti.group * p.b_rows_per_group + k0);
+  } else if constexpr (C::EP == Epi::kSwiglu) {
+    const int row = ti.group * p.b_rows_per_group + ti.n * (C::BN / 2);
+    tma_load_2d(b_dst, tmB, bar, k0, row);
+    tma_load_2d(b_dst + (C::BN / 2) * 128, tmB, bar, k0, row + p.b_half_offset);
+  } else {
+    tma_load_2d(b_dst, tmB, bar, k0, ti.group * p.b_rows_per_group + ti.n * C::BN);
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs / 4) return false;
+  }
+  return true;
+}
+
+template <class C>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
+                                              int quarter, int lane) {
+  const int r = quarter * 32 + lane;            // row inside the tile
+  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+  const bool no_mma = (ti.num_kb == 0);         // empty group: result is zero
+
+  if constexpr (C::S == Sched::kRoutedK) {
+    float* out = reinterpret_cast<float*>(p.c) + (long long)ti.group * p.c_group_stride +
+                 (long long)(ti.m0 + r) * p.ldc + (long long)ti.n * C::BN;
+    #pragma unroll 1
+    for (int c0 = 0; c0 < C::BN; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld_x16(tmem_acc + lane_addr + c0, v);
+      tmem_ld_wait(v);
+      float4* o4 = reinterpret_cast<float4*>(out + c0);
+      #pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float4 f;
+        f.x = no_mma ? 0.f : __uint_as_float(v[4 * j + 0]);
+        f.y = no_mma ? 0.f : __uint_as_float(v[4 * j + 1]);
+        f.z = no_mma ? 0.f : __uint_as_float(v[4 * j + 2]);
+        f.w = no_mma ? 0.f : __uint_as_float(v[4 * j + 3]);
+        o4[j] = f;
+      }
+    }
+    return;
+  } else {
+    const int row = ti.m0 + r;
+    const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
+
+    if constexpr (C::EP == Epi::kStoreF32) {
+      float* out = reinterpret_cast<float*>(p.c) + (long long)row * p.ldc;
+      #pragma unroll 1
+      for (int c0 = 0; c0 < C::BN; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem_acc + lane_addr + c0, v);
+        tmem_ld_wait(v);
+        const int colbase = ti.n * C::BN + c0;
+        if (row_ok) {
+          #pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (colbase + j < p.valid_cols) out[colbase + j] = __uint_as_float(v[j]);
+        }
+      }
+    } else if constexpr (C::EP == Epi::kStoreBf16) {
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.c) + (long long)row * p.ldc + (long long)ti.n * C::BN;
+      #pragma unroll 1
+      for (int c0 = 0; c0 < C::BN; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem_acc + lane_addr + c0, v);
+        tmem_ld_wait(v);
+        uint4 w0, w1;
+        w0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+        w0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+        w0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+        w0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+        w1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+        w1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+        w1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+        w1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+        if (row_ok) {
+          uint4* o = reinterpret_cast<uint4*>(out + c0);
+          o[0] = w0;
+          o[1] = w1;
+        }
+      }
+    } else if constexpr (C::EP == Epi::kSwiglu) {
+      // accumulator columns [0,128) = gate rows of W1, [128,256) = up rows
+      const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
+      const int col0 = ti.n * (C::BN / 2);
+      __nv_bfloat16* hout = reinterpret_cast<__nv_bfloat16*>(p.c) + (long long)row * p.ldc + col0;
+      __nv_bfloat16* zout = (p.c2 != nullptr)
+                                ? reinterpret_cast<__nv_bfloat16*>(p.c2) + (long long)row * p.ldc2 + col0
+                                : nullptr;
+      #pragma unroll 1
+      for (int c0 = 0; c0 < C::BN / 2; c0 += 16) {
+        uint32_t a[16], b[16];
+        tmem_ld_x16(tmem_acc + lane_addr + c0, a);
+        tmem_ld_x16(tmem_acc + lane_addr + (C::BN / 2) + c0, b);
+        tmem_ld_wait(a);
+        tmem_ld_wait(b);
+        uint32_t hw[8], za[8], zb[8];
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
+          const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
+          const float s0 = a0 / (1.0f + expf(-a0));
+          const float s1 = a1 / (1.0f + expf(-a1));
+          hw[j] = pack_bf16x2(g * s0 * b0, g * s1 * b1);
+          za[j] = pack_bf16x2(a0, a1);
+          zb[j] = pack_bf16x2(b0, b1);
+        }
+        if (row_ok) {
+          uint4* ho = reinterpret_cast<uint4*>(hout + c0);
+          ho[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          ho[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          if (zout != nullptr) {
+            uint4* zo = reinterpret_cast<uint4*>(zout + c0);
+            zo[0] = make_uint4(za[0], za[1], za[2], za[3]);
+            zo[1] = make_uint4(za[4], za[5], za[6], za[7]);
+            uint4* zo2 = reinterpret_cast<uint4*>(zout + p.half_cols + c0);
+            zo2[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+            zo2[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
+          }
+        }
+      }
+    } else {  // kSwigluBwd
+      const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
+      const int col0 = ti.n * C::BN;
+      const __nv_bfloat16* zrow = p.aux + (long long)(row_ok ? row : 0) * p.ld_aux + col0;
+      __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(p.c) + (long long)row * p.ldc + col0;
+      float dg = 0.f;
+      #pragma unroll 1
+      for (int c0 = 0; c0 < C::BN; c0 += 16) {
+        // rows past the end read row 0 (always present) so the warp stays converged
+        const uint4* pa = reinterpret_cast<const uint4*>(zrow + c0);
+        const uint4* pb = reinterpret_cast<const uint4*>(zrow + p.half_cols + c0);
+        const uint4 za0 = pa[0], za1 = pa[1], zb0 = pb[0], zb1 = pb[1];
+        uint32_t v[16];
+        tmem_ld_x16(tmem_acc + lane_addr + c0, v);
+        tmem_ld_wait(v);
+        const uint32_t zaw[8] = {za0.x, za0.y, za0.z, za0.w, za1.x, za1.y, za1.z, za1.w};
+        const uint32_t zbw[8] = {zb0.x, zb0.y, zb0.z, zb0.w, zb1.x, zb1.y, zb1.z, zb1.w};
+        uint32_t da[8], db[8];
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float av[2] = {bf16_lo(zaw[j]), bf16_hi(zaw[j])};
+          float bv[2] = {bf16_lo(zbw[j]), bf16_hi(zbw[j])};
+          float dav[2], dbv[2];
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float dh = no_mma ? 0.f : __uint_as_float(v[2 * j + u]);
+            const float sg = 1.0f / (1.0f + expf(-av[u]));
+            const float si = av[u] * sg;
+            dg += dh * si * bv[u];
+            const float dhg = g * dh;
+            dav[u] = dhg * bv[u] * sg * (1.0f + av[u] * (1.0f - sg));
+            dbv[u] = dhg * si;
+          }
+          da[j] = pack_bf16x2(dav[0], dav[1]);
+          db[j] = pack_bf16x2(dbv[0], dbv[1]);
+        }
+        if (row_ok) {
+          uint4* o = reinterpret_cast<uint4*>(dz + c0);
+          o[0] = make_uint4(da[0], da[1], da[2], da[3]);
+          o[1] = make_uint4(da[4], da[5], da[6], da[7]);
+          uint4* o2 = reinterpret_cast<uint4*>(dz + p.half_cols + c0);
+          o2[0] = make_uint4(db[0], db[1], db[2], db[3]);
+          o2[1] = make_uint4(db[4], db[5], db[6], db[7]);
+        }
+      }
+      if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * p.n_tiles + ti.n] = dg;
+    }
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(192, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int s_poff[257];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a_smem = smem;
+  uint8_t* b_smem = smem + C::STAGES * C::A_BYTES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (C::S != Sched::kDenseM && p.poffsets != nullptr) {
+    // offsets must be non-decreasing multiples of 128 inside the buffer;
+    // anything else is reported and no tile is processed.
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+      const int v = p.poffsets[i];
+      s_poff[i] = v;
+      const int prev = (i == 0) ? 0 : p.poffsets[i - 1];
+      if ((v & (C::BM - 1)) != 0 || v < prev || v > p.rows_cap || (i == 0 && v != 0)) s_bad = 1;
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (s_bad) {
+    if (threadIdx.x == 0) set_status(p.status, kErrBadIndex);
+  }
+  const int ntiles = s_bad ? 0 : total_tiles<C>(p, s_poff);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<C>(p, s_poff, t);
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          issue_loads<C>(&tmA, &tmB, p, ti, kb, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
+                         &full_bar[stage]);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // unwinding: let every load still in flight land before the CTA exits
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<C>(p, s_poff, t);
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * C::BN;
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_ptr)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
+          const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
+          #pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
+                                        : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
+                                        : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          any = true;
+          mma_commit(&empty_bar[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&tfull_bar[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok && any) {
+        mma_commit(&drain_bar);
+        mbar_wait_drain(&drain_bar, 0);
+      }
+    }
+  } else {
+    // -------------------------------------------------- epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C>(p, s_poff, t);
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
+      tc_fence_after_sync();
+      epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) set_status(p.status, kErrTimeout);
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,46 @@
+// Host-side helpers for the tcgen05 GEMM launchers: TMA descriptor encoding
+// (through the driver entry point, so the library needs no link-time libcuda)
+// and a typed launch wrapper.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemm.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// Encode a 2-D row-major tensor map with 128-byte swizzle.  inner = elements
+// per row, outer = rows, box = {box_inner, box_outer} elements.
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, uint64_t inner,
+                  uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+
+inline bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                           uint32_t box_outer) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, box_inner, box_outer);
+}
+
+template <class C>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+                        cudaStream_t st) {
+  static bool attr_set = false;
+  auto kern = grouped_gemm_kernel<C>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+inline GemmParams gemm_params_zero() {
+  GemmParams p{};
+  p.valid_cols = 1 << 30;
+  return p;
+}
+
+}  // namespace moe

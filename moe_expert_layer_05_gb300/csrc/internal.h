@@ -1,0 +1,66 @@
+// Launchers shared between the translation units of the library (not part of
+// the public ABI).  All pointers are device pointers; all calls are
+// stream-ordered and never synchronise.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kPadRows = 128;      // expert segments start at multiples of this
+constexpr int kPairsPerBlock = 256;  // (token, slot) pairs per counting-sort block
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 32;
+
+int num_sms();
+bool device_is_gb300();
+
+// ------------------------------------------------------------ routing (route.cu)
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int score, int32_t* idx,
+                        float* gate, cudaStream_t st);
+// Counting sort of T*k pairs by expert.  hist is scratch of
+// ceil(T*k/256) * E ints.
+cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
+                                int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
+                                int32_t* row_src, float* row_gate, int* status, cudaStream_t st);
+cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
+                               cudaStream_t st);
+cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,
+                                 cudaStream_t st);
+cudaError_t launch_combine(const void* o_perm, const int32_t* slot_row, const void* shared, int T, int k, int H,
+                           void* y, cudaStream_t st);
+// Backward per token: dgate from partial sums, router backward (dlogits and
+// per-row dlogit), dx = sum of expert rows + router term + shared term.
+cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, const int32_t* topk_idx,
+                                 const float* topk_gate, const float* logits, const float* dgate_part,
+                                 int n_part, const void* w_router, const void* dx_shared, int T, int E, int k,
+                                 int H, int score, void* dx, float* dgate, float* dlogits, float* row_dlogit,
+                                 cudaStream_t st);
+// dWr[e] = sum over expert e's rows of row_dlogit[r] * x_perm[r]  (fp32)
+cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, const int32_t* counts,
+                                const int32_t* poffsets, int E, int H, float* dw_router, cudaStream_t st);
+
+// ------------------------------------------------------------ GEMMs (gemm_*.cu)
+// logits[T,E] (fp32) = x[T,H] * Wr[E,H]^T
+cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, float* logits, int* status,
+                        cudaStream_t st);
+// h[cap,F] = g * silu(z_gate) * z_up with z = A[cap,H] * W1_e[2F,H]^T; z saved if non-null.
+// poffsets == nullptr: dense, rows = dense_rows, one group.
+cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E, int F, const int32_t* poffsets,
+                     int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st);
+// o[cap,H] = A[cap,F] * W2_e[H,F]^T
+cudaError_t gemm_fc2(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
+                     int dense_rows, void* o, int* status, cudaStream_t st);
+// dz[cap,2F] from dh = A[cap,H] * W2_e ([H,F]) with SwiGLU backward epilogue.
+cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
+                           const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate,
+                           void* dz, float* dgate_part, int* status, cudaStream_t st);
+// dx_perm[cap,H] = dz[cap,2F] * W1_e ([2F,H])
+cudaError_t gemm_dgrad_fc1(const void* dz, int rows_alloc, int F, const void* w1, int E, int H,
+                           const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st);
+// dW[e] (fp32 [M,N]) = A_e^T B_e, A [rows, M] bf16, B [rows, N] bf16 over each expert's rows
+// (poffsets) or over dense_rows rows (poffsets == nullptr, one group).
+cudaError_t gemm_wgrad(const void* a, int M, const void* b, int N, int rows_alloc, int E, const int32_t* poffsets,
+                       int dense_rows, float* dw, int* status, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,492 @@
+// Routing, permutation and combine kernels (CUDA cores, HBM-bound).
+//
+//  * top-k gating: one warp per token, warp-shuffle arg-max k times;
+//  * permutation: a stable counting sort of the T*k (token, slot) pairs by
+//    expert, done entirely on the device (per-block histograms, one scan
+//    block, a scatter) so the host never sees the expert sizes — the
+//    sync-free, dynamic-shape permutation of the Megatron Core MoE summary
+//    (technical summary 1 and 2.4);
+//  * gather / combine: 16-byte vector copies of token rows; the combine is an
+//    unweighted fp32 sum because the gate was applied inside the expert
+//    (technical summary 2.2, memory-efficient permutation).
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------- top-k
+struct Cand {
+  float key;
+  float logit;
+  int id;  // INT_MAX = none
+};
+
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  if (a.id == INT_MAX) return false;
+  if (b.id == INT_MAX) return true;
+  return a.key > b.key || (a.key == b.key && a.id < b.id);
+}
+
+__device__ __forceinline__ Cand shfl_cand(const Cand& c, int src_mask) {
+  Cand o;
+  o.key = __shfl_xor_sync(kFull, c.key, src_mask);
+  o.logit = __shfl_xor_sync(kFull, c.logit, src_mask);
+  o.id = __shfl_xor_sync(kFull, c.id, src_mask);
+  return o;
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                   int T, int E, int k, int score, int32_t* __restrict__ idx,
+                                                   float* __restrict__ gate) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const float* row = logits + (long long)warp * E;
+  float lg[PER_LANE], key[PER_LANE];
+  uint32_t taken = 0;
+  #pragma unroll
+  for (int j = 0; j < PER_LANE; ++j) {
+    const int e = lane + 32 * j;
+    lg[j] = (e < E) ? row[e] : 0.f;
+    if (score == 0) {
+      key[j] = lg[j];
+    } else {
+      key[j] = 1.0f / (1.0f + expf(-lg[j]));
+      if (bias != nullptr && e < E) key[j] += bias[e];
+    }
+    if (e >= E) taken |= 1u << j;
+  }
+  float sel_logit = 0.f;
+  int sel_id = 0;
+  float my_logit = 0.f;  // lane i keeps slot i
+  int my_id = 0;
+  for (int s = 0; s < k; ++s) {
+    Cand best{0.f, 0.f, INT_MAX};
+    #pragma unroll
+    for (int j = 0; j < PER_LANE; ++j) {
+      Cand c{key[j], lg[j], (taken >> j) & 1u ? INT_MAX : lane + 32 * j};
+      if (better(c, best)) best = c;
+    }
+    #pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const Cand o = shfl_cand(best, m);
+      if (better(o, best)) best = o;
+    }
+    sel_logit = best.logit;
+    sel_id = best.id;
+    if ((sel_id & 31) == lane) taken |= 1u << (sel_id >> 5);
+    if (lane == s) { my_logit = sel_logit; my_id = sel_id; }
+  }
+  // gates of the chosen k, normalised over them (lane s holds slot s)
+  float w;
+  if (score == 0) {
+    const float lmax = __shfl_sync(kFull, my_logit, 0);   // slot 0 has the largest logit
+    w = (lane < k) ? expf(my_logit - lmax) : 0.f;
+  } else {
+    w = (lane < k) ? 1.0f / (1.0f + expf(-my_logit)) : 0.f;
+  }
+  // sum in slot order (deterministic): lane 0 accumulates
+  float sum = 0.f;
+  for (int s = 0; s < k; ++s) sum += __shfl_sync(kFull, w, s);
+  if (lane < k) {
+    idx[(long long)warp * k + lane] = my_id;
+    gate[(long long)warp * k + lane] = w / sum;
+  }
+}
+
+// ---------------------------------------------------------------- counting sort
+// Stable rank of each pair of this block among the block's pairs with the
+// same expert; returns the expert (-1 for none / invalid) and the rank.
+// s_cnt: [8][E] ints.  Also leaves the block's per-expert totals in s_tot.
+__device__ __forceinline__ void block_stable_rank(const int32_t* __restrict__ idx, long long npairs, int E,
+                                                  int* s_cnt, int* s_tot, int* status, int& e_out,
+                                                  int& rank_out) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const long long p = (long long)blockIdx.x * kPairsPerBlock + tid;
+  int e = -1;
+  if (p < npairs) {
+    e = idx[p];
+    if (e < 0 || e >= E) {
+      set_status(status, kErrBadIndex);
+      e = -1;
+    }
+  }
+  for (int i = tid; i < 8 * E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  const unsigned peers = __match_any_sync(kFull, e);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && (__ffs(peers) - 1) == lane) s_cnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < E; x += blockDim.x) {
+    int run = 0;
+    #pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = s_cnt[w * E + x];
+      s_cnt[w * E + x] = run;
+      run += c;
+    }
+    s_tot[x] = run;
+  }
+  __syncthreads();
+  e_out = e;
+  rank_out = (e >= 0) ? s_cnt[warp * E + e] + rank_w : -1;
+}
+
+__global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __restrict__ idx, long long npairs,
+                                                               int E, int32_t* __restrict__ hist, int* status) {
+  __shared__ int s_cnt[8 * kMaxE];
+  __shared__ int s_tot[kMaxE];
+  int e, r;
+  block_stable_rank(idx, npairs, E, s_cnt, s_tot, status, e, r);
+  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)blockIdx.x * E + x] = s_tot[x];
+}
+
+// One block.  hist [NB][E] -> counts, offsets, poffsets, and in place
+// base[b][e] = poffsets[e] + sum_{b'<b} hist[b'][e].  Also marks padding rows.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int NB, int E,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ poffsets, int32_t* __restrict__ row_src,
+                                                    float* __restrict__ row_gate) {
+  __shared__ int s_part[1024];
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_poff[kMaxE + 1];
+  const int tid = threadIdx.x;
+  const int G = blockDim.x / E;                 // groups of E threads, each over a range of blocks
+  const int g = tid / E, e = tid % E;
+  const bool active = g < G;
+  const int per = (NB + G - 1) / G;
+  const int b0 = g * per, b1 = min(NB, b0 + per);
+  int sum = 0;
+  if (active) {
+    for (int b = b0; b < b1; ++b) sum += hist[(long long)b * E + e];
+    s_part[tid] = sum;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int c = 0;
+    for (int q = 0; q < G; ++q) c += s_part[q * E + tid];
+    s_cnt[tid] = c;
+    counts[tid] = c;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // scan over experts: lane handles a contiguous run of experts
+    const int per_lane = (E + 31) / 32;
+    const int e0 = tid * per_lane, e1 = min(E, e0 + per_lane);
+    int cs = 0, ps = 0;
+    for (int x = e0; x < e1; ++x) { cs += s_cnt[x]; ps += (s_cnt[x] + kPadRows - 1) / kPadRows * kPadRows; }
+    int ci = cs, pi = ps;
+    #pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int a = __shfl_up_sync(kFull, ci, d), b = __shfl_up_sync(kFull, pi, d);
+      if (tid >= d) { ci += a; pi += b; }
+    }
+    int c_ex = ci - cs, p_ex = pi - ps;
+    for (int x = e0; x < e1; ++x) {
+      offsets[x] = c_ex;
+      poffsets[x] = p_ex;
+      s_poff[x] = p_ex;
+      c_ex += s_cnt[x];
+      p_ex += (s_cnt[x] + kPadRows - 1) / kPadRows * kPadRows;
+    }
+    if (tid == 31) { offsets[E] = ci; poffsets[E] = pi; s_poff[E] = pi; }
+  }
+  __syncthreads();
+  if (active) {
+    int run = s_poff[e];
+    for (int q = 0; q < g; ++q) run += s_part[q * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const long long i = (long long)b * E + e;
+      const int c = hist[i];
+      hist[i] = run;
+      run += c;
+    }
+  }
+  // padding rows of every segment
+  for (int i = tid; i < E * kPadRows; i += blockDim.x) {
+    const int x = i / kPadRows, j = i % kPadRows;
+    const int r = s_poff[x] + s_cnt[x] + j;
+    if (r < s_poff[x + 1]) {
+      row_src[r] = -1;
+      if (row_gate != nullptr) row_gate[r] = 0.f;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPairsPerBlock) scatter_kernel(const int32_t* __restrict__ idx,
+                                                                 const float* __restrict__ gate, long long npairs,
+                                                                 int E, int k, const int32_t* __restrict__ base,
+                                                                 int32_t* __restrict__ slot_row,
+                                                                 int32_t* __restrict__ row_src,
+                                                                 float* __restrict__ row_gate) {
+  __shared__ int s_cnt[8 * kMaxE];
+  __shared__ int s_tot[kMaxE];
+  int e, r;
+  block_stable_rank(idx, npairs, E, s_cnt, s_tot, nullptr, e, r);
+  const long long p = (long long)blockIdx.x * kPairsPerBlock + threadIdx.x;
+  if (p >= npairs) return;
+  if (e < 0) {
+    slot_row[p] = -1;
+    return;
+  }
+  const int row = base[(long long)blockIdx.x * E + e] + r;
+  slot_row[p] = row;
+  row_src[row] = static_cast<int32_t>(p / k);
+  if (row_gate != nullptr) row_gate[row] = gate[p];
+}
+
+// ---------------------------------------------------------------- row copies
+// One block per token: read x[t] once, write it to its k rows.
+__global__ void __launch_bounds__(128) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ slot_row,
+                                                     int k, int vec_per_row, uint4* __restrict__ x_perm) {
+  const int t = blockIdx.x;
+  __shared__ int s_rows[kMaxK];
+  if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
+  __syncthreads();
+  const uint4* src = x + (long long)t * vec_per_row;
+  for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+    const uint4 val = __ldg(src + v);
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r >= 0) x_perm[(long long)r * vec_per_row + v] = val;
+    }
+  }
+}
+
+__global__ void zero_pad_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ poffsets,
+                                int vec_per_row, uint4* __restrict__ buf) {
+  const int e = blockIdx.x;
+  const int r0 = poffsets[e] + counts[e], r1 = poffsets[e + 1];
+  const long long n = (long long)(r1 - r0) * vec_per_row;
+  uint4* base = buf + (long long)r0 * vec_per_row;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
+  acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+  acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+  acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+  acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
+  return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                    pack_bf16x2(a[6], a[7]));
+}
+
+// y[t] = sum_i o[slot_row[t,i]] (+ shared[t]), fp32 in slot order, one rounding.
+__global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ o, const int32_t* __restrict__ slot_row,
+                                                      const uint4* __restrict__ shared, int k, int vec_per_row,
+                                                      uint4* __restrict__ y) {
+  const int t = blockIdx.x;
+  __shared__ int s_rows[kMaxK];
+  if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
+  __syncthreads();
+  for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r >= 0) add_bf16x8(acc, __ldg(o + (long long)r * vec_per_row + v));
+    }
+    if (shared != nullptr) add_bf16x8(acc, __ldg(shared + (long long)t * vec_per_row + v));
+    y[(long long)t * vec_per_row + v] = pack8(acc);
+  }
+}
+
+// ---------------------------------------------------------------- backward
+__global__ void __launch_bounds__(128) dgrad_combine_kernel(
+    const uint4* __restrict__ dx_perm, const int32_t* __restrict__ slot_row, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_gate, const float* __restrict__ logits, const float* __restrict__ dgate_part,
+    int n_part, const uint4* __restrict__ w_router, const uint4* __restrict__ dx_shared, int E, int k,
+    int vec_per_row, int score, uint4* __restrict__ dx, float* __restrict__ dgate, float* __restrict__ dlogits,
+    float* __restrict__ row_dlogit) {
+  const int t = blockIdx.x;
+  __shared__ int s_rows[kMaxK];
+  __shared__ int s_ids[kMaxK];
+  __shared__ float s_dl[kMaxK];
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int lane = tid;
+    int row = -1, id = 0;
+    float g = 0.f, dg = 0.f, lg = 0.f;
+    if (lane < k) {
+      row = slot_row[(long long)t * k + lane];
+      id = topk_idx[(long long)t * k + lane];
+      g = topk_gate[(long long)t * k + lane];
+      lg = logits[(long long)t * E + min(max(id, 0), E - 1)];
+      if (row >= 0)
+        for (int n = 0; n < n_part; ++n) dg += dgate_part[(long long)row * n_part + n];
+    }
+    // inner = sum_i g_i dg_i (slot order)
+    float inner = 0.f, ssum = 0.f;
+    const float sg = 1.0f / (1.0f + expf(-lg));
+    for (int s = 0; s < k; ++s) {
+      inner += __shfl_sync(kFull, g * dg, s);
+      ssum += __shfl_sync(kFull, sg, s);
+    }
+    float dl;
+    if (score == 0) {
+      dl = g * (dg - inner);
+    } else {
+      dl = (dg - inner) / ssum * sg * (1.0f - sg);
+    }
+    if (lane < k) {
+      s_rows[lane] = row;
+      s_ids[lane] = id;
+      s_dl[lane] = dl;
+      if (dgate != nullptr) dgate[(long long)t * k + lane] = dg;
+      if (row >= 0 && row_dlogit != nullptr) row_dlogit[row] = dl;
+    }
+  }
+  __syncthreads();
+  if (dlogits != nullptr) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      float v = 0.f;
+      for (int i = 0; i < k; ++i)
+        if (s_ids[i] == e) v = s_dl[i];
+      dlogits[(long long)t * E + e] = v;
+    }
+  }
+  for (int v = tid; v < vec_per_row; v += blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r >= 0) add_bf16x8(acc, __ldg(dx_perm + (long long)r * vec_per_row + v));
+    }
+    if (w_router != nullptr) {
+      for (int i = 0; i < k; ++i) {
+        const uint4 wv = __ldg(w_router + (long long)s_ids[i] * vec_per_row + v);
+        const float d = s_dl[i];
+        acc[0] += d * bf16_lo(wv.x); acc[1] += d * bf16_hi(wv.x);
+        acc[2] += d * bf16_lo(wv.y); acc[3] += d * bf16_hi(wv.y);
+        acc[4] += d * bf16_lo(wv.z); acc[5] += d * bf16_hi(wv.z);
+        acc[6] += d * bf16_lo(wv.w); acc[7] += d * bf16_hi(wv.w);
+      }
+    }
+    if (dx_shared != nullptr) add_bf16x8(acc, __ldg(dx_shared + (long long)t * vec_per_row + v));
+    dx[(long long)t * vec_per_row + v] = pack8(acc);
+  }
+}
+
+// grid (E, H/1024): each thread owns 8 columns, walks the expert's rows.
+__global__ void __launch_bounds__(128) router_wgrad_kernel(const uint4* __restrict__ x_perm,
+                                                           const float* __restrict__ row_dlogit,
+                                                           const int32_t* __restrict__ counts,
+                                                           const int32_t* __restrict__ poffsets, int vec_per_row,
+                                                           float* __restrict__ dw) {
+  const int e = blockIdx.x;
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;
+  if (v >= vec_per_row) return;
+  const int r0 = poffsets[e], n = counts[e];
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int r = 0;
+  for (; r + 4 <= n; r += 4) {
+    uint4 xv[4];
+    float d[4];
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      xv[u] = __ldg(x_perm + (long long)(r0 + r + u) * vec_per_row + v);
+      d[u] = row_dlogit[r0 + r + u];
+    }
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc[0] += d[u] * bf16_lo(xv[u].x); acc[1] += d[u] * bf16_hi(xv[u].x);
+      acc[2] += d[u] * bf16_lo(xv[u].y); acc[3] += d[u] * bf16_hi(xv[u].y);
+      acc[4] += d[u] * bf16_lo(xv[u].z); acc[5] += d[u] * bf16_hi(xv[u].z);
+      acc[6] += d[u] * bf16_lo(xv[u].w); acc[7] += d[u] * bf16_hi(xv[u].w);
+    }
+  }
+  for (; r < n; ++r) {
+    const uint4 xv = __ldg(x_perm + (long long)(r0 + r) * vec_per_row + v);
+    const float d = row_dlogit[r0 + r];
+    acc[0] += d * bf16_lo(xv.x); acc[1] += d * bf16_hi(xv.x);
+    acc[2] += d * bf16_lo(xv.y); acc[3] += d * bf16_hi(xv.y);
+    acc[4] += d * bf16_lo(xv.z); acc[5] += d * bf16_hi(xv.z);
+    acc[6] += d * bf16_lo(xv.w); acc[7] += d * bf16_hi(xv.w);
+  }
+  float4* out = reinterpret_cast<float4*>(dw + (long long)e * vec_per_row * 8 + (long long)v * 8);
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int score, int32_t* idx,
+                        float* gate, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + 7) / 8;
+  if (E <= 32) topk_kernel<1><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
+  else if (E <= 64) topk_kernel<2><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
+  else if (E <= 128) topk_kernel<4><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
+  else topk_kernel<8><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
+                                int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
+                                int32_t* row_src, float* row_gate, int* status, cudaStream_t st) {
+  const long long npairs = (long long)T * k;
+  const int NB = static_cast<int>((npairs + kPairsPerBlock - 1) / kPairsPerBlock);
+  if (NB > 0) count_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, E, hist, status);
+  scan_kernel<<<1, 1024, 0, st>>>(hist, NB, E, counts, offsets, poffsets, row_src, row_gate);
+  if (NB > 0)
+    scatter_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, gate, npairs, E, k, hist, slot_row, row_src,
+                                                  gate != nullptr ? row_gate : nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
+                               cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  gather_kernel<<<T, 128, 0, st>>>(static_cast<const uint4*>(x), slot_row, k, H / 8, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,
+                                 cudaStream_t st) {
+  zero_pad_kernel<<<E, 256, 0, st>>>(counts, poffsets, H / 8, static_cast<uint4*>(buf));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* o_perm, const int32_t* slot_row, const void* shared, int T, int k, int H,
+                           void* y, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<T, 128, 0, st>>>(static_cast<const uint4*>(o_perm), slot_row, static_cast<const uint4*>(shared),
+                                    k, H / 8, static_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, const int32_t* topk_idx,
+                                 const float* topk_gate, const float* logits, const float* dgate_part,
+                                 int n_part, const void* w_router, const void* dx_shared, int T, int E, int k,
+                                 int H, int score, void* dx, float* dgate, float* dlogits, float* row_dlogit,
+                                 cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  dgrad_combine_kernel<<<T, 128, 0, st>>>(
+      static_cast<const uint4*>(dx_perm), slot_row, topk_idx, topk_gate, logits, dgate_part, n_part,
+      static_cast<const uint4*>(w_router), static_cast<const uint4*>(dx_shared), E, k, H / 8, score,
+      static_cast<uint4*>(dx), dgate, dlogits, row_dlogit);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, const int32_t* counts,
+                                const int32_t* poffsets, int E, int H, float* dw_router, cudaStream_t st) {
+  const int vpr = H / 8;
+  dim3 grid(E, (vpr + 127) / 128);
+  router_wgrad_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x_perm), row_dlogit, counts, poffsets, vpr,
+                                            dw_router);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

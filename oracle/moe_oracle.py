@@ -48,6 +48,12 @@ def router_logits(x: np.ndarray, w_router: np.ndarray) -> np.ndarray:
     return np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
 
 
+def _shape(a):
+    """Shape of an array, or of an object that only exposes ``shape`` and
+    per-expert indexing (lets a test stream expert weights in one at a time)."""
+    return a.shape if hasattr(a, "shape") else np.asarray(a).shape
+
+
 def _sigmoid(v: np.ndarray) -> np.ndarray:
     return 1.0 / (1.0 + np.exp(-v))
 
@@ -250,7 +256,7 @@ def moe_forward(x, w_router, w1, w2, k, score=SOFTMAX, bias=None,
     """
     x = np.asarray(x, np.float64)
     T = x.shape[0]
-    E = np.asarray(w_router).shape[0] if w_router is not None else np.asarray(w1).shape[0]
+    E = _shape(w_router)[0] if w_router is not None else _shape(w1)[0]
     logits = None
     if routing is None:
         logits = router_logits(x, w_router)
@@ -313,8 +319,8 @@ def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
     x = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
     T, H = x.shape
-    E = np.asarray(w1).shape[0]
-    F = np.asarray(w1).shape[1] // 2
+    E = _shape(w1)[0]
+    F = _shape(w1)[1] // 2
     idx = np.asarray(fwd["topk_idx"], np.int64)
     gate = np.asarray(fwd["gates"], np.float64)
     k = idx.shape[1]
@@ -456,3 +462,88 @@ def mxfp8_roundtrip(v, axis=-1):
     """dequantize(quantize(v)) along axis: the operand an MXFP8 GEMM multiplies."""
     c, s = mxfp8_quantize(v, axis)
     return mxfp8_dequantize(c, s, axis)
+
+
+# ---------------------------------------------------------------------------
+# Step-level definitions in the expert-ordered (padded) row layout.  Each one
+# is the plain definition of one grouped step, expert by expert; composing
+# them gives moe_forward / moe_backward (pinned in tests/test_oracle_steps.py).
+# Rows of expert e: [poffsets[e], poffsets[e+1]), padding rows included.
+# ---------------------------------------------------------------------------
+
+def _segments(poffsets):
+    po = np.asarray(poffsets, np.int64)
+    return [(e, int(po[e]), int(po[e + 1])) for e in range(len(po) - 1)]
+
+
+def expert_fc1(x_perm, w1, poffsets, row_gate=None):
+    """z_r = W1_e x_r for each row r of expert e; h_r = g_r * silu(z_gate) * z_up
+    (the routing weight applied at the activation, technical summary 2.2)."""
+    x_perm = np.asarray(x_perm, np.float64)
+    F = _shape(w1)[1] // 2
+    rows = x_perm.shape[0]
+    z = np.zeros((rows, 2 * F))
+    for e, a, b in _segments(poffsets):
+        if b > a:
+            z[a:b] = x_perm[a:b] @ np.asarray(w1[e], np.float64).T
+    g = np.ones(rows) if row_gate is None else np.asarray(row_gate, np.float64)
+    h = g[:, None] * silu(z[:, :F]) * z[:, F:]
+    return z, h
+
+
+def expert_fc2(h, w2, poffsets):
+    """o_r = W2_e h_r."""
+    h = np.asarray(h, np.float64)
+    H = _shape(w2)[1]
+    o = np.zeros((h.shape[0], H))
+    for e, a, b in _segments(poffsets):
+        if b > a:
+            o[a:b] = h[a:b] @ np.asarray(w2[e], np.float64).T
+    return o
+
+
+def expert_dgrad_fc2(dy_perm, w2, z, poffsets, row_gate=None):
+    """dh'_r = W2_e^T dy_r; with a, b = z_r halves:  dgate_r = <dh'_r, silu(a) b>,
+    dz_r = [g dh' b silu'(a), g dh' silu(a)].  Returns (dz, dgate_rows)."""
+    dy_perm = np.asarray(dy_perm, np.float64)
+    z = np.asarray(z, np.float64)
+    F = z.shape[1] // 2
+    rows = dy_perm.shape[0]
+    dhp = np.zeros((rows, F))
+    for e, a, b in _segments(poffsets):
+        if b > a:
+            dhp[a:b] = dy_perm[a:b] @ np.asarray(w2[e], np.float64)
+    za, zb = z[:, :F], z[:, F:]
+    g = np.ones(rows) if row_gate is None else np.asarray(row_gate, np.float64)
+    dgate_rows = (dhp * silu(za) * zb).sum(axis=1)
+    dh = g[:, None] * dhp
+    dz = np.concatenate([dh * zb * silu_grad(za), dh * silu(za)], axis=1)
+    return dz, dgate_rows
+
+
+def expert_dgrad_fc1(dz, w1, poffsets):
+    """dx_r = W1_e^T dz_r."""
+    dz = np.asarray(dz, np.float64)
+    H = _shape(w1)[2]
+    dx = np.zeros((dz.shape[0], H))
+    for e, a, b in _segments(poffsets):
+        if b > a:
+            dx[a:b] = dz[a:b] @ np.asarray(w1[e], np.float64)
+    return dx
+
+
+def expert_wgrad(a_rows, b_rows, poffsets):
+    """dW_e = sum over expert e's rows of a_r b_r^T ([E, M, N]; zero for empty experts)."""
+    A = np.asarray(a_rows, np.float64)
+    B = np.asarray(b_rows, np.float64)
+    segs = _segments(poffsets)
+    out = np.zeros((len(segs), A.shape[1], B.shape[1]))
+    for e, a, b in segs:
+        if b > a:
+            out[e] = A[a:b].T @ B[a:b]
+    return out
+
+
+def dense_rows_of(n_rows):
+    """poffsets of one group holding rows [0, n_rows) (the shared expert)."""
+    return np.array([0, n_rows], np.int64)
