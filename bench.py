@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Throughput of the MoE expert layer on GB300 (one JSON line on rank 0).
+
+A step is one pass of the layer over one batch: router GEMM, top-k gating,
+sync-free permutation, grouped-GEMM SwiGLU experts with the gate applied at the
+activation, combine (plus dgrad + wgrad for workloads that train).  The default
+workload is the Mixtral-like forward layer (T=4096, H=4096, E=8, k=2,
+F=14336, bf16), seeded synthetic inputs.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on
+the launching stream, with L2 flushed (a 512 MB write) before every step outside
+the events; barrier + synchronize on both sides; the max over ranks.  With
+--gpus N under torchrun every rank runs its own tokens through replicated
+experts (no data-path collective): weak scaling.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs, make_inputs_on_device  # noqa: E402
+
+METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM TFLOPS as % of tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 512 << 20
+# dram__bytes_read.sum + dram__bytes_write.sum of one fc1 launch, from the ncu
+# capture summarised in profiles/ (None until captured for the current kernel).
+FC1_TRAFFIC_BYTES = None
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, use_cuda: bool):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend="nccl" if use_cuda else "gloo")
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput: tokens all ranks processed / slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_total_ms / 1e3)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.01)
+        self.lines.clear()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def read_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+class _F32Experts:
+    """Expert weights as fp32 numpy (exact bf16 values), per expert on demand."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+        self.shape = tuple(t.shape)
+        self.c = {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.c:
+            self.c[e] = self.t[e].to("cpu", torch.float32).numpy()
+        return self.c[e]
+
+    def warm(self):
+        for e in range(self.shape[0]):
+            self[e]
+        return self
+
+
+def oracle_forward_timed(w, inp_cpu, tokens: np.ndarray) -> float:
+    from oracle import moe_oracle as O
+    x = inp_cpu["x_np"][tokens]
+    t0 = time.perf_counter()
+    O.moe_forward(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], k=w.k, score=w.score,
+                  bias=inp_cpu["bias_np"], w1_shared=inp_cpu["w1s_np"], w2_shared=inp_cpu["w2s_np"])
+    return time.perf_counter() - t0
+
+
+def oracle_inputs(w, dinp) -> dict:
+    def npf(t):
+        return None if t is None else t.to("cpu", torch.float32).numpy().astype(np.float64)
+    return {"x_np": npf(dinp["x"]), "wr_np": npf(dinp["w_router"]), "bias_np": npf(dinp["bias"]),
+            "w1s_np": npf(dinp["w1_shared"]), "w2s_np": npf(dinp["w2_shared"]),
+            "w1": _F32Experts(dinp["w1"]).warm(), "w2": _F32Experts(dinp["w2"]).warm()}
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, dinp, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on the first n tokens; n grows until the run
+    takes at least a few seconds (bounded by budget_s)."""
+    inp = oracle_inputs(w, dinp)
+    n = 8
+    while True:
+        t = oracle_forward_timed(w, inp, np.arange(n))
+        if t >= budget_s / 3 or n >= w.T:
+            break
+        n = min(w.T, max(n * 2, int(n * (budget_s / 3) / max(t, 1e-3))))
+    return {"value": n / t, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"first {n} of {w.T} tokens, full forward (fp64 numpy), {t:.1f} s"}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args) -> dict | None:
+    from moe_expert_layer_05_gb300 import api
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (GB300); there is no CPU path")
+    torch.cuda.set_device(local)
+    dist_init(world, True)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    dinp = make_inputs_on_device(w, dev, seed=rank)
+    cfg = api.config_of(w)
+    layer = api.MoELayer(cfg, dinp, with_backward=w.backward, device=dev)
+    x = dinp["x"]
+    y = torch.empty_like(x)
+    dy = dinp["dy"]
+    grads = None
+    if w.backward:
+        layer.forward(x, y)
+        _, _, grads = layer.backward(x, dy)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.forward(x, y)
+        if w.backward:
+            layer.backward(x, dy, grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    l0 = api.moe_kernel_launches()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = api.moe_kernel_launches() - l0
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = aggregate(w.T, K, world, total_ms)
+    assert api.moe_read_device_status(layer.ws) == 0, "device status not ok"
+
+    # ---- the dominant kernel (fc1 grouped GEMM) alone, same inputs, same stream
+    fl = layer.fields()
+    Kk = max(10, min(K, 200))
+    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
+    z = fl["z"] if w.backward else None
+    for i in range(Kk):
+        flush.zero_()
+        s_ev[i].record(stream)
+        api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, fl["x_perm"], dinp["w1"], fl["h"], layer.ws, c2=z,
+                             row_gate=fl["row_gate"], poffsets=fl["poffsets"])
+        e_ev[i].record(stream)
+    torch.cuda.synchronize()
+    fc1_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(s_ev, e_ev))
+    # the rest of the forward chain, one stage at a time (context for the line)
+    stages = stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, Kk)
+    stages["fc1_grouped_gemm"] = fc1_ms
+
+    # ---- end to end: host buffers, copies inside the timed region
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_h.copy_(x)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e_s[i].record(stream)
+        x.copy_(x_h, non_blocking=True)
+        step()
+        y_h.copy_(y, non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_total = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), world, dev)
+
+    if rank != 0:
+        return None
+    peaks, peak_src = read_peaks()
+    R = w.T * w.k
+    fc1_flop = 4.0 * R * w.H * w.F
+    achieved = fc1_flop / (fc1_ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    fwd_flop = 6.0 * R * w.H * w.F + 6.0 * w.T * w.H * w.S
+    step_flop = fwd_flop * (3 if w.backward else 1)
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
+                   "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
+                   "l2": "flushed (512 MB write) before every timed step, outside the events",
+                   "parallelism": f"replicas x{world}"},
+        "expert_gemm_tflops_per_gpu": step_flop / (total_ms / K / 1e3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": "fc1 grouped GEMM (tcgen05, fused gated SwiGLU)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"bf16_tflops of {peak_src} peaks (burst; kernel timed alone)",
+                     "traffic": FC1_TRAFFIC_BYTES, "flop_per_launch": fc1_flop, "ms_per_launch": fc1_ms},
+        "stages_ms": stages,
+        "e2e": {"value": aggregate(w.T, K, world, e2e_total), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": y.numel() * y.element_size()},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w, dinp)
+    return out
+
+
+def stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, n) -> dict:
+    fl = layer.fields()
+    lay = layer.layout
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+
+    def timed(fn):
+        s = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            s[i].record(stream)
+            fn()
+            e[i].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in zip(s, e))
+
+    out = {}
+    out["router_topk"] = timed(lambda: api.moe_router_topk(cfg, x, dinp["w_router"], dinp["bias"], fl["logits"],
+                                                            fl["topk_idx"], fl["topk_gate"], layer.ws))
+    row_src = fl["row_src"]
+    out["permute"] = timed(lambda: api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"],
+                                                   fl["offsets"], fl["poffsets"], fl["slot_row"], row_src,
+                                                   fl["row_gate"], fl["x_perm"], 0, layer.ws))
+    out["fc2_grouped_gemm"] = timed(lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, fl["h"], dinp["w2"], fl["o"],
+                                                                 layer.ws, poffsets=fl["poffsets"]))
+    out["combine"] = timed(lambda: api.moe_unpermute(cfg, fl["o"], fl["slot_row"], None, y))
+    # algorithmic bytes of the two HBM-bound copies: (1+k)*T*H*2 each
+    nbytes = (1 + k) * T * H * 2
+    out["permute_gbs"] = nbytes / (out["permute"] / 1e3) / 1e9
+    out["combine_gbs"] = nbytes / (out["combine"] / 1e3) / 1e9
+    return out
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args) -> dict | None:
+    world, rank, local = dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+        dinp = make_inputs_on_device(w, torch.device("cuda", local), seed=0)
+    else:
+        dinp = make_inputs(w, seed=0)
+    inp = oracle_inputs(w, dinp)
+    # size the per-step sample so that W + K steps end within ~2 minutes
+    t1 = oracle_forward_timed(w, inp, np.arange(4)) / 4
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(w.T, per_step_budget / max(t1, 1e-6))))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_forward_timed(w, inp, np.sort(rng.choice(w.T, n, replace=False)))
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_forward_timed(w, inp, np.sort(rng.choice(w.T, n, replace=False)))
+    value = n * args.steps / total
+    sample = f"{n} random tokens of {w.T} per step (fp64 numpy oracle, full forward)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
+                   "score": w.score, "pass": "fwd"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    world, _, _ = dist_env()
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

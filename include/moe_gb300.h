@@ -124,6 +124,10 @@ const char* moe_status_string(moe_status s);
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int32_t moe_version(void);
 
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all devices, all streams).  Host only; for instrumentation. */
+uint64_t moe_kernel_launches(void);
+
 /* Rows of the expert-ordered buffers: the worst case over all routings,
  * T*k + 127*E rounded up to a multiple of 128.  Returns -1 on a bad config. */
 int32_t moe_capacity_rows(const moe_config* cfg);

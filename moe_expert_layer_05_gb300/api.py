@@ -57,6 +57,7 @@ _P = ctypes.POINTER
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [c_i32]),
     "moe_version": (c_i32, []),
+    "moe_kernel_launches": (ctypes.c_uint64, []),
     "moe_capacity_rows": (c_i32, [_P(MoeConfig)]),
     "moe_activation_layout": (c_i32, [_P(MoeConfig), c_i32, _P(MoeActLayout)]),
     "moe_workspace_bytes": (c_sz, [_P(MoeConfig)]),
@@ -293,3 +294,8 @@ class MoELayer:
                      ptr(grads.get("dw2_shared")))
         moe_layer_backward_wgrad(c, self.cw, x, dy, g, self.act, self.ws, stream)
         return dx, dgate, grads
+
+
+def moe_kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().moe_kernel_launches())

@@ -4,6 +4,7 @@
 // synchronises, or reads a device value on the host.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -42,6 +43,9 @@ DevInfo& dev_info() {
   return info;
 }
 }  // namespace
+
+std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n), std::memory_order_relaxed); }
 
 int num_sms() { return dev_info().sms; }
 bool device_is_gb300() { return dev_info().gb300; }
@@ -172,6 +176,8 @@ const char* moe_status_string(moe_status s) {
 }
 
 int32_t moe_version(void) { return 0x000100; }
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int32_t moe_capacity_rows(const moe_config* cfg) { return config_ok(cfg) ? cap_rows(cfg) : -1; }
 

@@ -34,6 +34,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   }
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -14,6 +14,8 @@ constexpr int kMaxK = 32;
 
 int num_sms();
 bool device_is_gb300();
+// Counts kernel launches issued by the library (process-wide).
+void count_launches(int n);
 
 // ------------------------------------------------------------ routing (route.cu)
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int score, int32_t* idx,

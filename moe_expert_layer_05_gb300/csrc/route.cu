@@ -430,6 +430,7 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
   else if (E <= 64) topk_kernel<2><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
   else if (E <= 128) topk_kernel<4><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
   else topk_kernel<8><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -443,6 +444,7 @@ cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, in
   if (NB > 0)
     scatter_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, gate, npairs, E, k, hist, slot_row, row_src,
                                                   gate != nullptr ? row_gate : nullptr);
+  count_launches(NB > 0 ? 3 : 1);
   return cudaGetLastError();
 }
 
@@ -450,12 +452,14 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, in
                                cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   gather_kernel<<<T, 128, 0, st>>>(static_cast<const uint4*>(x), slot_row, k, H / 8, static_cast<uint4*>(x_perm));
+  count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,
                                  cudaStream_t st) {
   zero_pad_kernel<<<E, 256, 0, st>>>(counts, poffsets, H / 8, static_cast<uint4*>(buf));
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -464,6 +468,7 @@ cudaError_t launch_combine(const void* o_perm, const int32_t* slot_row, const vo
   if (T == 0) return cudaSuccess;
   combine_kernel<<<T, 128, 0, st>>>(static_cast<const uint4*>(o_perm), slot_row, static_cast<const uint4*>(shared),
                                     k, H / 8, static_cast<uint4*>(y));
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -477,6 +482,7 @@ cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, c
       static_cast<const uint4*>(dx_perm), slot_row, topk_idx, topk_gate, logits, dgate_part, n_part,
       static_cast<const uint4*>(w_router), static_cast<const uint4*>(dx_shared), E, k, H / 8, score,
       static_cast<uint4*>(dx), dgate, dlogits, row_dlogit);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -486,6 +492,7 @@ cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, con
   dim3 grid(E, (vpr + 127) / 128);
   router_wgrad_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x_perm), row_dlogit, counts, poffsets, vpr,
                                             dw_router);
+  count_launches(1);
   return cudaGetLastError();
 }
 

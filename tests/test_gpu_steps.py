@@ -231,9 +231,11 @@ def test_gemm_fc1_fc2(lib, T, H, E, k, F, skew):
     zr, hr = O.expert_fc1(f64(a)[:used], LazyW(w1), m["poffsets"], rg[:used])
     assert_bf16_close(f64(z)[:used], zr, "z")
     assert_bf16_close(f64(h)[:used], hr, "h")
-    # fc2 against the GPU's own h would use a CUDA-path value as oracle input; use h rounded from the oracle's
+    # Chained check: the oracle's fc2 runs on its own h rounded to bf16, the GPU's on its h; the
+    # two h differ by one bf16 ulp wherever fp32 and fp64 z straddle a rounding boundary, so the
+    # bound carries an absolute term for those.  (test_gemm_fc2_alone checks fc2 on identical h.)
     or_ = O.expert_fc2(f64(to_bf16(hr.astype(np.float32))), LazyW(w2), m["poffsets"])
-    assert_bf16_close(f64(o)[:used], or_, "o", rel_l2_tol=8e-3, elem_rel=2.0 ** -6, elem_abs_frac=6e-3)
+    assert_bf16_close(f64(o)[:used], or_, "o", rel_l2_tol=8e-3, elem_rel=2.0 ** -6, elem_abs_frac=2e-2)
 
 
 class LazyW:
@@ -361,8 +363,8 @@ def test_unpermute(lib, T, E, k, H, shared):
                       None if sh is None else sh.to(DEV), y)
     torch.cuda.synchronize()
     ref = O.unpermute_sum(f64(o), m, None if sh is None else f64(sh))
-    # fp32 sum of k+1 bf16 values, one rounding: within one bf16 half-ulp of the exact sum
-    # unless the fp32 sum itself rounded (k+1 <= 33 terms: |fp32 err| <= 2^-19 |sum of |terms||)
+    # fp32 sum of k+1 bf16 values, one rounding to bf16 (unit roundoff 2^-8) of the exact sum,
+    # plus the fp32 sum's own rounding (k+1 <= 33 terms: |fp32 err| <= 2^-19 sum |terms|)
     got = f64(y)
     absum = np.abs(f64(o))[m["slot_row"]].sum(1) + (np.abs(f64(sh)) if shared else 0)
-    assert np.all(np.abs(got - ref) <= 2.0 ** -9 * np.abs(ref) + 2.0 ** -19 * absum + 1e-30)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 2.0 ** -19 * absum + 1e-30)
