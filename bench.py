@@ -19,6 +19,7 @@ experts (no data-path collective): weak scaling.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -189,16 +190,16 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w, dinp, budget_s: float = 12.0) -> dict:
-    """The oracle, as it stands, on the first n tokens; n grows until the run
-    takes at least a few seconds (bounded by budget_s)."""
+def cpu_baseline(w, dinp, target_s: float = 10.0) -> dict:
+    """The oracle, as it stands, on the first n tokens; n grows until one run
+    takes about target_s seconds (or covers all tokens)."""
     inp = oracle_inputs(w, dinp)
     n = 8
     while True:
         t = oracle_forward_timed(w, inp, np.arange(n))
-        if t >= budget_s / 3 or n >= w.T:
+        if t >= 0.7 * target_s or n >= w.T:
             break
-        n = min(w.T, max(n * 2, int(n * (budget_s / 3) / max(t, 1e-3))))
+        n = min(w.T, max(n * 2, int(n * target_s / max(t, 1e-3))))
     return {"value": n / t, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
             "sample": f"first {n} of {w.T} tokens, full forward (fp64 numpy), {t:.1f} s"}
 
@@ -214,6 +215,8 @@ def run_ours(args) -> dict | None:
     dist_init(world, True)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
     dinp = make_inputs_on_device(w, dev, seed=rank)
     cfg = api.config_of(w)
     layer = api.MoELayer(cfg, dinp, with_backward=w.backward, device=dev)
@@ -416,6 +419,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
