@@ -299,3 +299,11 @@ class MoELayer:
 def moe_kernel_launches() -> int:
     """Kernels the library has launched in this process so far."""
     return int(load().moe_kernel_launches())
+
+
+def moe_status_string(code: int) -> str:
+    return load().moe_status_string(int(code)).decode()
+
+
+def moe_version() -> int:
+    return int(load().moe_version())

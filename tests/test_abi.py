@@ -1,0 +1,85 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the public header declares, sizes and layouts are consistent,
+and bad arguments are rejected before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_layer_05_gb300 import api
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_gb300.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_function_is_exported():
+    lib = api.load()
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding wraps each under the same name
+    for n in names:
+        assert hasattr(api, n), f"binding lacks {n}"
+
+
+def test_status_strings_and_version():
+    lib = api.load()
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.moe_status_string(code)
+    assert lib.moe_version() > 0
+
+
+@pytest.mark.parametrize("T,H,E,k,F,S", [(4096, 4096, 8, 2, 14336, 0), (8192, 7168, 256, 8, 2048, 2048),
+                                         (0, 128, 8, 2, 128, 0), (1, 128, 8, 8, 128, 128)])
+def test_layout_is_consistent(T, H, E, k, F, S):
+    cfg = api.make_config(T, H, E, k, F, S)
+    cap = api.moe_capacity_rows(cfg)
+    assert cap % 128 == 0 and cap >= T * k + 127 * E
+    for bwd in (False, True):
+        L = api.moe_activation_layout(cfg, bwd)
+        assert L.cap == cap
+        fields = [(n, getattr(L, n)) for n, _ in api.MoeActLayout._fields_[:-3]]
+        used = sorted(v for n, v in fields if v != (1 << 64) - 1)
+        assert used == sorted(set(used)), "fields overlap"
+        assert all(v % 256 == 0 for v in used)
+        assert L.total >= used[-1]
+        assert (L.dz != (1 << 64) - 1) == bwd
+    assert api.moe_workspace_bytes(cfg) >= 256
+
+
+@pytest.mark.parametrize("bad", [dict(k=0), dict(k=9, E=8), dict(E=300, k=2), dict(H=100), dict(F=200),
+                                 dict(S=64), dict(T=-1), dict(k=33, E=64)])
+def test_bad_configs_rejected(bad):
+    base = dict(T=16, H=128, E=8, k=2, F=128, S=0)
+    base.update(bad)
+    cfg = api.make_config(**base)
+    assert api.moe_capacity_rows(cfg) == -1
+    assert api.moe_workspace_bytes(cfg) == 0
+    L = api.MoeActLayout()
+    assert api.load().moe_activation_layout(ctypes.byref(cfg), 0, ctypes.byref(L)) == -1
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch():
+    lib = api.load()
+    cfg = api.make_config(16, 128, 8, 2, 128)
+    w = api.MoeWeights(None, None, None, None, None, None)
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 16, 16, 16, 1 << 30, 0, 16, 1 << 20,
+                                 None) == -1
+    w = api.MoeWeights(16, None, 16, 16, None, None)
+    # misaligned x
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 17, 16, 16, 1 << 30, 0, 16, 1 << 20,
+                                 None) == -1
+    # activation buffer too small
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 16, 16, 16, 64, 0, 16, 1 << 20, None) == -4
+    args = api.MoeGemmArgs(0, 0, 16, 16, 16, None, None, None, None, None)  # routed without offsets
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), 16, None) == -1
+    args = api.MoeGemmArgs(9, 16, 16, 16, 16, None, None, None, None, None)
+    st = lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), 16, None)
+    assert st in (-1, -2)      # unknown op (or no GB300 here)
