@@ -182,6 +182,31 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        int32_t* row_src, float* row_gate, void* x_perm, int32_t zero_pad, void* ws,
                        void* stream);
 
+/* moe_permute without a workspace argument, for callers that cannot allocate
+ * device memory: for example a plugin that an inference engine hands only
+ * preallocated tensors, a host loop whose memory budget is fixed in advance,
+ * or code that must not pay the device-wide synchronisation of cudaMalloc.
+ * The pages have no counterpart to this call; it exists for such callers.
+ *
+ * Same arguments, outputs and layouts as moe_permute, minus `ws`.  The
+ * counting sort's scratch lives in a 1 MiB array of device memory owned by
+ * the library (every GPU that loads the library keeps it until the process
+ * exits), so the call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ * Limit: ceil(T*k/256) * E <= 262144 (e.g. T*k up to 262144 pairs with
+ * E = 256); larger shapes return MOE_ERR_WORKSPACE before any launch.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array: calls whose
+ * work overlaps on the GPU (other streams, other threads) race and must be
+ * ordered by the caller.  The array's old contents are never read.
+ * Device-side errors are not recorded (there is no status word): a pair with
+ * an expert index outside [0,E) is dropped and its slot_row entry is -1. */
+moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                               const float* topk_gate, int32_t* counts, int32_t* offsets, int32_t* poffsets,
+                               int32_t* slot_row, int32_t* row_src, float* row_gate, void* x_perm,
+                               int32_t zero_pad, void* stream);
+
 typedef enum {
   /* z = A * W1_e^T, h = g * silu(z[:, :F]) * z[:, F:].  a = x_perm [cap,H],
    * b = w1 [E,2F,H]; c = h [cap,F]; c2 = z [cap,2F] or NULL; row_gate [cap] or NULL (g = 1). */

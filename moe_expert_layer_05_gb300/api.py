@@ -67,6 +67,8 @@ _SIGS = {
     "moe_topk_gating": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_permute": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
                             c_vp, c_vp]),
+    "moe_permute_noalloc": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                    c_i32, c_vp]),
     "moe_grouped_gemm": (c_i32, [_P(MoeConfig), _P(MoeGemmArgs), c_vp, c_vp]),
     "moe_unpermute": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_layer_forward": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_sz, c_i32, c_vp, c_sz,
@@ -180,6 +182,15 @@ def moe_permute(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, slot_row
     check(load().moe_permute(ctypes.byref(cfg), ptr(x), ptr(topk_idx), ptr(topk_gate), ptr(counts), ptr(offsets),
                              ptr(poffsets), ptr(slot_row), ptr(row_src), ptr(row_gate), ptr(x_perm), int(zero_pad),
                              ptr(ws), stream_ptr(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, slot_row, row_src, row_gate,
+                        x_perm, zero_pad, stream=None) -> None:
+    """moe_permute for callers that cannot allocate: no workspace argument;
+    the scratch is a fixed 1 MiB device array inside the library."""
+    check(load().moe_permute_noalloc(ctypes.byref(cfg), ptr(x), ptr(topk_idx), ptr(topk_gate), ptr(counts),
+                                     ptr(offsets), ptr(poffsets), ptr(slot_row), ptr(row_src), ptr(row_gate),
+                                     ptr(x_perm), int(zero_pad), stream_ptr(stream)), "moe_permute_noalloc")
 
 
 def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
