@@ -68,7 +68,7 @@ typedef enum { MOE_GEMM_BF16 = 0, MOE_GEMM_MXFP8 = 1 } moe_gemm_dtype;
 typedef struct {
   int32_t T, H, E, k, F, S;
   int32_t score;   /* moe_score_fn */
-  int32_t dtype;   /* moe_gemm_dtype (MOE_GEMM_BF16 only in this version) */
+  int32_t dtype;   /* moe_gemm_dtype; MOE_GEMM_MXFP8 also needs T % 128 == 0 */
 } moe_config;
 
 /* Weights (device, bf16 unless noted).
@@ -82,6 +82,9 @@ typedef struct {
   const void* w2;
   const void* w1_shared;
   const void* w2_shared;
+  /* MOE_GEMM_MXFP8 only: the buffer moe_prepare_mxfp8_weights filled from the
+   * weights above (NULL for bf16). */
+  const void* mx;
 } moe_weights;
 
 /* Weight gradients (device, fp32 outputs).  dw_router [E,H], dw1 [E,2F,H],
@@ -232,6 +235,17 @@ typedef enum {
  * for the WGRAD ops the contraction runs over dense_rows rows and c has one
  * group).  Pass E in cfg as usual; the shapes H, F (or S for dense calls, see
  * moe_grouped_gemm) come from cfg. */
+/* MXFP8 (dtype == MOE_GEMM_MXFP8): every operand is E4M3 codes plus E8M0
+ * scales (see moe_quantize_mxfp8), K-major, blocks of 32 along the
+ * contraction: a and b are codes and a_scales / b_scales their scale tiles.
+ *   FC1_SWIGLU: a = x_perm [cap,H]; b = W1 rows gate/up interleaved
+ *               (MOE_MX_ROWS_GATE_UP of w1 [E,2F,H]).
+ *   FC2:        a = h [cap,F]; b = W2 [E*H,F] (MOE_MX_ROWS).
+ *   DGRAD_FC2:  a = dy_perm [cap,H]; b = W2^T [E,F,H] (MOE_MX_COLS_T of w2); aux = z (bf16).
+ *   DGRAD_FC1:  a = dz [cap,2F]; b = W1^T [E,H,2F] (MOE_MX_COLS_T of w1).
+ *   WGRAD_FC1:  a = dz^T [2F,cap], b = x_perm^T [H,cap] (MOE_MX_COLS_T).
+ *   WGRAD_FC2:  a = dy_perm^T [H,cap], b = h^T [F,cap] (MOE_MX_COLS_T).
+ * Dense calls need dense_rows % 128 == 0. */
 typedef struct {
   int32_t op;             /* moe_gg_op */
   int32_t dense_rows;     /* 0: routed; >0: one dense group of this many rows */
@@ -243,6 +257,8 @@ typedef struct {
   const float* row_gate;
   float* dgate_part;
   const int32_t* poffsets;
+  const void* a_scales;   /* MXFP8 only */
+  const void* b_scales;   /* MXFP8 only */
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For
@@ -256,6 +272,44 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* args, vo
  * shared_out [T,H] bf16 or NULL, y [T,H] bf16. */
 moe_status moe_unpermute(const moe_config* cfg, const void* o_perm, const int32_t* slot_row,
                          const void* shared_out, void* y, void* stream);
+
+/* --------------------------------------------------------------------------
+ * MXFP8 (technical summary 2.5: FP8 expert GEMMs and activations, router
+ * and combine kept in higher precision; the MXFP8 recipe on Blackwell).
+ * Element type E4M3, one E8M0 scale per block of 32 values along the
+ * contraction: X = 2^(floor(log2 amax) - 8) clamped to [2^-127, 2^127]
+ * (2^-127 for an all-zero block), code = E4M3(v / X) rounded to nearest even,
+ * saturated to +-448.
+ * Scale layout ("scale tiles"): for a codes matrix [R, C] (R % 128 == 0,
+ * C % 128 == 0) the R*C/32 scale bytes form 512-byte tiles, tile (i, j) covering
+ * rows 128i..128i+127 and blocks 4j..4j+3 (columns 128j..128j+127) at byte
+ * (i*(C/128) + j)*512; inside a tile the scale of row r, block b is at
+ * (r%32)*16 + (r/32)*4 + b.  This is the order the tensor cores' scale-factor
+ * copy consumes.
+ * ----------------------------------------------------------------------- */
+
+typedef enum {
+  MOE_MX_ROWS = 0,          /* src [batch*rows, cols] -> codes [batch*rows, cols], blocks along each row */
+  MOE_MX_COLS_T = 1,        /* src batch x [rows, cols] -> codes batch x [cols, rows], blocks along rows
+                               (each matrix transposed; scale tiles per matrix) */
+  MOE_MX_ROWS_GATE_UP = 2   /* as ROWS, rows of every [gate; up] matrix of `rows` rows reordered as
+                               gate 0..63, up 0..63, gate 64..127, up 64..127, ... (fc1 weights) */
+} moe_mx_mode;
+
+/* Quantise a bf16 tensor to MXFP8.  codes: batch*rows*cols bytes; scales:
+ * batch*rows*cols/32 bytes.  cols % 128 == 0; ROWS: batch*rows % 128 == 0;
+ * COLS_T and ROWS_GATE_UP: rows % 128 == 0. */
+moe_status moe_quantize_mxfp8(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t mode,
+                              uint8_t* codes, uint8_t* scales, void* stream);
+
+/* Bytes of the quantised-weight buffer an MXFP8 layer needs (moe_weights.mx). */
+size_t moe_mxfp8_weights_bytes(const moe_config* cfg);
+
+/* Quantise w1, w2 (and the shared expert) once into `mx`: the fc1/fc2 copies
+ * and the transposed copies the data gradients contract over.  Call again
+ * after every weight update. */
+moe_status moe_prepare_mxfp8_weights(const moe_config* cfg, const moe_weights* w, void* mx, size_t mx_bytes,
+                                     void* stream);
 
 /* --------------------------------------------------------------------------
  * Whole layer

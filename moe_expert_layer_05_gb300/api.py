@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA er
 SCORE = {"softmax": 0, "sigmoid": 1}
 
 GG_FC1_SWIGLU, GG_FC2, GG_DGRAD_FC2, GG_DGRAD_FC1, GG_WGRAD_FC1, GG_WGRAD_FC2 = range(6)
+MX_ROWS, MX_COLS_T, MX_ROWS_GATE_UP = range(3)
 
 c_i32 = ctypes.c_int32
 c_vp = ctypes.c_void_p
@@ -32,7 +33,7 @@ class MoeConfig(ctypes.Structure):
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [("w_router", c_vp), ("router_bias", c_vp), ("w1", c_vp), ("w2", c_vp),
-                ("w1_shared", c_vp), ("w2_shared", c_vp)]
+                ("w1_shared", c_vp), ("w2_shared", c_vp), ("mx", c_vp)]
 
 
 class MoeGrads(ctypes.Structure):
@@ -50,7 +51,8 @@ class MoeActLayout(ctypes.Structure):
 
 class MoeGemmArgs(ctypes.Structure):
     _fields_ = [("op", c_i32), ("dense_rows", c_i32), ("a", c_vp), ("b", c_vp), ("c", c_vp), ("c2", c_vp),
-                ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp)]
+                ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp),
+                ("a_scales", c_vp), ("b_scales", c_vp)]
 
 
 _P = ctypes.POINTER
@@ -71,6 +73,9 @@ _SIGS = {
                                     c_i32, c_vp]),
     "moe_grouped_gemm": (c_i32, [_P(MoeConfig), _P(MoeGemmArgs), c_vp, c_vp]),
     "moe_unpermute": (c_i32, [_P(MoeConfig), c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_quantize_mxfp8": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
+    "moe_mxfp8_weights_bytes": (c_sz, [_P(MoeConfig)]),
+    "moe_prepare_mxfp8_weights": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_sz, c_vp]),
     "moe_layer_forward": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_sz, c_i32, c_vp, c_sz,
                                   c_vp]),
     "moe_layer_backward_dgrad": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,
@@ -194,11 +199,26 @@ def moe_permute_noalloc(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, 
 
 
 def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
-                     dense_rows=0, stream=None) -> None:
+                     dense_rows=0, a_scales=None, b_scales=None, stream=None) -> None:
     args = MoeGemmArgs(op, dense_rows, ptr(a), ptr(b), ptr(c), ptr(c2), ptr(aux), ptr(row_gate), ptr(dgate_part),
-                       ptr(poffsets))
+                       ptr(poffsets), ptr(a_scales), ptr(b_scales))
     check(load().moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), ptr(ws), stream_ptr(stream)),
           "moe_grouped_gemm")
+
+
+def moe_quantize_mxfp8(src, batch, rows, cols, mode, codes, scales, stream=None) -> None:
+    check(load().moe_quantize_mxfp8(ptr(src), batch, rows, cols, mode, ptr(codes), ptr(scales),
+                                    stream_ptr(stream)), "moe_quantize_mxfp8")
+
+
+def moe_mxfp8_weights_bytes(cfg) -> int:
+    return int(load().moe_mxfp8_weights_bytes(ctypes.byref(cfg)))
+
+
+def moe_prepare_mxfp8_weights(cfg, weights: MoeWeights, mx, stream=None) -> None:
+    check(load().moe_prepare_mxfp8_weights(ctypes.byref(cfg), ctypes.byref(weights), ptr(mx),
+                                           mx.numel() * mx.element_size(), stream_ptr(stream)),
+          "moe_prepare_mxfp8_weights")
 
 
 def moe_unpermute(cfg, o_perm, slot_row, shared_out, y, stream=None) -> None:
@@ -243,7 +263,17 @@ class MoELayer:
         self.ws = torch.zeros(max(moe_workspace_bytes(cfg), 256), dtype=torch.uint8, device=device)
         moe_workspace_init(self.ws)
         self.cw = MoeWeights(ptr(weights["w_router"]), ptr(weights.get("bias")), ptr(weights["w1"]),
-                             ptr(weights["w2"]), ptr(weights.get("w1_shared")), ptr(weights.get("w2_shared")))
+                             ptr(weights["w2"]), ptr(weights.get("w1_shared")), ptr(weights.get("w2_shared")),
+                             None)
+        self.mx = None
+        if cfg.dtype == 1:
+            self.mx = torch.empty(moe_mxfp8_weights_bytes(cfg), dtype=torch.uint8, device=device)
+            self.cw.mx = ptr(self.mx)
+            self.prepare_weights()
+
+    def prepare_weights(self, stream=None) -> None:
+        """(MXFP8) quantise the weights into the layer's buffer; call after a weight update."""
+        moe_prepare_mxfp8_weights(self.cfg, self.cw, self.mx, stream)
 
     def view(self, name: str, dtype, shape) -> torch.Tensor:
         off = getattr(self.layout, name)

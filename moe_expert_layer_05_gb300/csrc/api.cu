@@ -68,7 +68,8 @@ bool config_ok(const moe_config* c) {
   if (c->k > kMaxK || c->k > c->E || c->E > kMaxE) return false;
   if (c->H % 128 || c->F % 128 || c->S % 128) return false;
   if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return false;
-  if (c->dtype != MOE_GEMM_BF16) return false;
+  if (c->dtype != MOE_GEMM_BF16 && c->dtype != MOE_GEMM_MXFP8) return false;
+  if (c->dtype == MOE_GEMM_MXFP8 && c->T % 128 != 0) return false;   // whole 128-row scale tiles
   const long long pairs = static_cast<long long>(c->T) * c->k;
   if (pairs + 128LL * c->E >= (1LL << 31)) return false;
   return true;
@@ -153,6 +154,78 @@ moe_status compute_layout(const moe_config* c, int with_bwd, moe_act_layout* L) 
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------- MXFP8 buffers
+struct MxBuf {
+  size_t q = kNone, sf = kNone;   // E4M3 codes, E8M0 scale tiles (codes / 32 bytes)
+};
+
+// Transient quantised activations, placed in the workspace after the
+// histograms.  The forward, dgrad and wgrad calls each use their own set; the
+// region is the largest of the three.
+struct MxWs {
+  MxBuf x, h, xs, hs;                             // forward
+  MxBuf dy, dz, dys, dzs;                         // dgrad
+  MxBuf dzT, xT, dyT, hT, dzsT, xsT, dysT, hsT;   // wgrad (transposed: blocks along tokens)
+  size_t total = 0;
+};
+
+MxWs mx_ws_layout(const moe_config* c) {
+  MxWs m;
+  const size_t T = c->T, H = c->H, F = c->F, S = c->S, cap = static_cast<size_t>(cap_rows(c));
+  size_t off = 0, end = 0;
+  auto buf = [&](size_t elems) {
+    MxBuf b;
+    b.q = off;
+    off = align_up(off + (elems ? elems : 1));
+    b.sf = off;
+    off = align_up(off + (elems / 32 ? elems / 32 : 1));
+    return b;
+  };
+  auto region = [&]() { end = off > end ? off : end; off = 0; };
+  m.x = buf(cap * H); m.h = buf(cap * F);
+  if (S) { m.xs = buf(T * H); m.hs = buf(T * S); }
+  region();
+  m.dy = buf(cap * H); m.dz = buf(cap * 2 * F);
+  if (S) { m.dys = buf(T * H); m.dzs = buf(T * 2 * S); }
+  region();
+  m.dzT = buf(2 * F * cap); m.xT = buf(H * cap); m.dyT = buf(H * cap); m.hT = buf(F * cap);
+  if (S) { m.dzsT = buf(2 * S * T); m.xsT = buf(H * T); m.dysT = buf(H * T); m.hsT = buf(S * T); }
+  region();
+  m.total = end;
+  return m;
+}
+
+// Quantised weights, prepared once by moe_prepare_mxfp8_weights.
+struct MxW {
+  MxBuf w1, w2, w1t, w2t, s1, s2, s1t, s2t;
+  size_t total = 0;
+};
+
+MxW mx_weight_layout(const moe_config* c) {
+  MxW m;
+  const size_t H = c->H, E = c->E, F = c->F, S = c->S;
+  size_t off = 0;
+  auto buf = [&](size_t elems) {
+    MxBuf b;
+    b.q = off;
+    off = align_up(off + elems);
+    b.sf = off;
+    off = align_up(off + elems / 32);
+    return b;
+  };
+  m.w1 = buf(E * 2 * F * H);    // [E*2F, H], gate/up interleaved in 64-row blocks (fc1)
+  m.w2 = buf(E * H * F);        // [E*H, F]  (fc2)
+  m.w1t = buf(E * H * 2 * F);   // [E, H, 2F] = W1_e^T, blocks along 2F (fc1 dgrad)
+  m.w2t = buf(E * F * H);       // [E, F, H]  = W2_e^T, blocks along H  (fc2 dgrad)
+  if (S) {
+    m.s1 = buf(2 * S * H); m.s2 = buf(H * S); m.s1t = buf(H * 2 * S); m.s2t = buf(S * H);
+  }
+  m.total = off;
+  return m;
+}
+
+size_t mx_ws_base(const moe_config* c) { return kStatusBytes + align_up(hist_bytes(c)); }
+
 moe_status check_device() { return device_is_gb300() ? MOE_OK : MOE_ERR_UNSUPPORTED; }
 
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
@@ -187,7 +260,64 @@ moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, m
 
 size_t moe_workspace_bytes(const moe_config* cfg) {
   if (!config_ok(cfg)) return 0;
-  return kStatusBytes + align_up(hist_bytes(cfg));
+  size_t b = kStatusBytes + align_up(hist_bytes(cfg));
+  if (cfg->dtype == MOE_GEMM_MXFP8) b += mx_ws_layout(cfg).total;
+  return b;
+}
+
+size_t moe_mxfp8_weights_bytes(const moe_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return mx_weight_layout(cfg).total;
+}
+
+moe_status moe_quantize_mxfp8(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t mode,
+                              uint8_t* codes, uint8_t* scales, void* stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(batch) * rows * cols;
+  if (n == 0) return MOE_OK;
+  if (!dev_ptr_ok(src) || !dev_ptr_ok(codes) || !dev_ptr_ok(scales)) return MOE_ERR_INVALID_ARG;
+  if (cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  switch (mode) {
+    case MOE_MX_ROWS:
+      if ((static_cast<long long>(batch) * rows) % 128 != 0) return MOE_ERR_INVALID_ARG;
+      return cuda_status(launch_quantize_rows(src, static_cast<long long>(batch) * rows, cols, 0, codes, scales, st));
+    case MOE_MX_ROWS_GATE_UP:
+      if (rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+      return cuda_status(
+          launch_quantize_rows(src, static_cast<long long>(batch) * rows, cols, rows / 2, codes, scales, st));
+    case MOE_MX_COLS_T:
+      if (rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+      return cuda_status(launch_quantize_cols(src, batch, rows, cols, codes, scales, st));
+    default:
+      return MOE_ERR_INVALID_ARG;
+  }
+}
+
+moe_status moe_prepare_mxfp8_weights(const moe_config* cfg, const moe_weights* w, void* mx, size_t mx_bytes,
+                                     void* stream) {
+  if (!config_ok(cfg) || w == nullptr || !dev_ptr_ok(mx) || !dev_ptr_ok(w->w1) || !dev_ptr_ok(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
+  const MxW L = mx_weight_layout(cfg);
+  if (mx_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int H = cfg->H, E = cfg->E, F = cfg->F, S = cfg->S;
+  auto q = [&](const MxBuf& b) { return at<uint8_t>(mx, b.q); };
+  auto f = [&](const MxBuf& b) { return at<uint8_t>(mx, b.sf); };
+  MOE_TRY(launch_quantize_rows(w->w1, static_cast<long long>(E) * 2 * F, H, F, q(L.w1), f(L.w1), st));
+  MOE_TRY(launch_quantize_rows(w->w2, static_cast<long long>(E) * H, F, 0, q(L.w2), f(L.w2), st));
+  MOE_TRY(launch_quantize_cols(w->w1, E, 2 * F, H, q(L.w1t), f(L.w1t), st));
+  MOE_TRY(launch_quantize_cols(w->w2, E, H, F, q(L.w2t), f(L.w2t), st));
+  if (S > 0) {
+    MOE_TRY(launch_quantize_rows(w->w1_shared, 2 * S, H, S, q(L.s1), f(L.s1), st));
+    MOE_TRY(launch_quantize_rows(w->w2_shared, H, S, 0, q(L.s2), f(L.s2), st));
+    MOE_TRY(launch_quantize_cols(w->w1_shared, 1, 2 * S, H, q(L.s1t), f(L.s1t), st));
+    MOE_TRY(launch_quantize_cols(w->w2_shared, 1, H, S, q(L.s2t), f(L.s2t), st));
+  }
+  return MOE_OK;
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -258,6 +388,34 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
   const int rows = dense ? a->dense_rows : cap_rows(cfg);
   const int32_t* po = dense ? nullptr : a->poffsets;
   int* status = status_ptr(ws);
+  if (cfg->dtype == MOE_GEMM_MXFP8) {
+    if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
+    if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+    switch (a->op) {
+      case MOE_GG_FC1_SWIGLU:
+        if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
+        return cuda_status(gemm_mx_fc1(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
+                                       a->row_gate, a->c, a->c2, status, st));
+      case MOE_GG_FC2:
+        return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->dense_rows,
+                                           a->c, status, st));
+      case MOE_GG_DGRAD_FC2:
+        if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
+        return cuda_status(gemm_mx_dgrad_fc2(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
+                                             a->aux, a->row_gate, a->c, a->dgate_part, status, st));
+      case MOE_GG_DGRAD_FC1:
+        return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, 2 * F, a->b, a->b_scales, E, H, po,
+                                           a->dense_rows, a->c, status, st));
+      case MOE_GG_WGRAD_FC1:
+        return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, 2 * F, a->b, a->b_scales, H, rows, E, po, a->dense_rows,
+                                         static_cast<float*>(a->c), status, st));
+      case MOE_GG_WGRAD_FC2:
+        return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, H, a->b, a->b_scales, F, rows, E, po, a->dense_rows,
+                                         static_cast<float*>(a->c), status, st));
+      default:
+        return MOE_ERR_INVALID_ARG;
+    }
+  }
   switch (a->op) {
     case MOE_GG_FC1_SWIGLU:
       if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
@@ -300,6 +458,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(y))) return MOE_ERR_INVALID_ARG;
   if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
   if (w->router_bias != nullptr && !aligned16(w->router_bias)) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_MXFP8 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
   if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (moe_status s = check_device(); s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -326,15 +485,40 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
   if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
   // 5-6: grouped expert GEMMs; the gate multiplies the SwiGLU output inside fc1
-  MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, with_backward ? at<void>(act, L.z) : nullptr,
-                   status, st));
-  MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st));
+  void* z = with_backward ? at<void>(act, L.z) : nullptr;
+  void* zs = with_backward && S > 0 ? at<void>(act, L.zs) : nullptr;
   const void* shared_out = nullptr;
-  if (S > 0 && T > 0) {
-    MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
-                     with_backward ? at<void>(act, L.zs) : nullptr, status, st));
-    MOE_TRY(gemm_fc2(at<void>(act, L.hs), T, S, w->w2_shared, 1, H, nullptr, T, at<void>(act, L.os), status, st));
-    shared_out = at<void>(act, L.os);
+  if (cfg->dtype == MOE_GEMM_MXFP8) {
+    // MXFP8 expert GEMMs: activations quantised (blocks of 32 along K) on the
+    // way in, weights prepared once; router, gates and combine stay fp32/bf16.
+    const MxWs M = mx_ws_layout(cfg);
+    const MxW W = mx_weight_layout(cfg);
+    char* mb = static_cast<char*>(ws) + mx_ws_base(cfg);
+    auto q = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.q); };
+    auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
+    auto wq = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
+    auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
+    MOE_TRY(launch_quantize_rows(x_perm, cap, H, 0, q(M.x), f(M.x), st));
+    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
+    MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st));
+    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st));
+    if (S > 0 && T > 0) {
+      MOE_TRY(launch_quantize_rows(x, T, H, 0, q(M.xs), f(M.xs), st));
+      MOE_TRY(gemm_mx_fc1(q(M.xs), f(M.xs), T, H, wq(W.s1), wf(W.s1), 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
+                          zs, status, st));
+      MOE_TRY(launch_quantize_rows(at<void>(act, L.hs), T, S, 0, q(M.hs), f(M.hs), st));
+      MOE_TRY(gemm_mx_nt_bf16(q(M.hs), f(M.hs), T, S, wq(W.s2), wf(W.s2), 1, H, nullptr, T, at<void>(act, L.os),
+                              status, st));
+      shared_out = at<void>(act, L.os);
+    }
+  } else {
+    MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, z, status, st));
+    MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st));
+    if (S > 0 && T > 0) {
+      MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs), zs, status, st));
+      MOE_TRY(gemm_fc2(at<void>(act, L.hs), T, S, w->w2_shared, 1, H, nullptr, T, at<void>(act, L.os), status, st));
+      shared_out = at<void>(act, L.os);
+    }
   }
   // 7: unweighted combine
   MOE_TRY(launch_combine(o, slot_row, shared_out, T, k, H, y, st));
@@ -351,6 +535,7 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
   if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(dy) || !dev_ptr_ok(dx))) return MOE_ERR_INVALID_ARG;
   if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
   if (dgate != nullptr && !aligned16(dgate)) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_MXFP8 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
   if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (moe_status s = check_device(); s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -366,16 +551,40 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
 
   MOE_TRY(launch_gather_rows(dy, slot_row, T, k, H, dy_perm, st));
   MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, dy_perm, st));
-  MOE_TRY(gemm_dgrad_fc2(dy_perm, cap, H, w->w2, E, F, poff, 0, at<void>(act, L.z), at<float>(act, L.row_gate), dz,
-                         dpart, status, st));
-  MOE_TRY(gemm_dgrad_fc1(dz, cap, F, w->w1, E, H, poff, 0, dx_perm, status, st));
   const void* dxs = nullptr;
-  if (S > 0 && T > 0) {
-    MOE_TRY(gemm_dgrad_fc2(dy, T, H, w->w2_shared, 1, S, nullptr, T, at<void>(act, L.zs), nullptr,
-                           at<void>(act, L.dzs), nullptr, status, st));
-    MOE_TRY(gemm_dgrad_fc1(at<void>(act, L.dzs), T, S, w->w1_shared, 1, H, nullptr, T, at<void>(act, L.dxs), status,
-                           st));
-    dxs = at<void>(act, L.dxs);
+  if (cfg->dtype == MOE_GEMM_MXFP8) {
+    const MxWs M = mx_ws_layout(cfg);
+    const MxW W = mx_weight_layout(cfg);
+    char* mb = static_cast<char*>(ws) + mx_ws_base(cfg);
+    auto q = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.q); };
+    auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
+    auto wq = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
+    auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
+    MOE_TRY(launch_quantize_rows(dy_perm, cap, H, 0, q(M.dy), f(M.dy), st));
+    MOE_TRY(gemm_mx_dgrad_fc2(q(M.dy), f(M.dy), cap, H, wq(W.w2t), wf(W.w2t), E, F, poff, 0, at<void>(act, L.z),
+                              at<float>(act, L.row_gate), dz, dpart, status, st));
+    MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st));
+    MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st));
+    if (S > 0 && T > 0) {
+      MOE_TRY(launch_quantize_rows(dy, T, H, 0, q(M.dys), f(M.dys), st));
+      MOE_TRY(gemm_mx_dgrad_fc2(q(M.dys), f(M.dys), T, H, wq(W.s2t), wf(W.s2t), 1, S, nullptr, T, at<void>(act, L.zs),
+                                nullptr, at<void>(act, L.dzs), nullptr, status, st));
+      MOE_TRY(launch_quantize_rows(at<void>(act, L.dzs), T, 2 * S, 0, q(M.dzs), f(M.dzs), st));
+      MOE_TRY(gemm_mx_nt_bf16(q(M.dzs), f(M.dzs), T, 2 * S, wq(W.s1t), wf(W.s1t), 1, H, nullptr, T,
+                              at<void>(act, L.dxs), status, st));
+      dxs = at<void>(act, L.dxs);
+    }
+  } else {
+    MOE_TRY(gemm_dgrad_fc2(dy_perm, cap, H, w->w2, E, F, poff, 0, at<void>(act, L.z), at<float>(act, L.row_gate), dz,
+                           dpart, status, st));
+    MOE_TRY(gemm_dgrad_fc1(dz, cap, F, w->w1, E, H, poff, 0, dx_perm, status, st));
+    if (S > 0 && T > 0) {
+      MOE_TRY(gemm_dgrad_fc2(dy, T, H, w->w2_shared, 1, S, nullptr, T, at<void>(act, L.zs), nullptr,
+                             at<void>(act, L.dzs), nullptr, status, st));
+      MOE_TRY(gemm_dgrad_fc1(at<void>(act, L.dzs), T, S, w->w1_shared, 1, H, nullptr, T, at<void>(act, L.dxs), status,
+                             st));
+      dxs = at<void>(act, L.dxs);
+    }
   }
   MOE_TRY(launch_dgrad_combine(dx_perm, slot_row, at<int32_t>(act, L.topk_idx), at<float>(act, L.topk_gate),
                                at<float>(act, L.logits), dpart, F / 128, w->w_router, dxs, T, E, k, H, cfg->score, dx,
@@ -393,6 +602,7 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(dy))) return MOE_ERR_INVALID_ARG;
   if (cfg->S > 0 && (!dev_ptr_ok(g->dw1_shared) || !dev_ptr_ok(g->dw2_shared))) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_MXFP8 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
   if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (moe_status s = check_device(); s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -400,18 +610,41 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
   int* status = status_ptr(ws);
   const int32_t* counts = at<int32_t>(act, L.counts);
   const int32_t* poff = at<int32_t>(act, L.poffsets);
-  MOE_TRY(gemm_wgrad(at<void>(act, L.dz), 2 * F, at<void>(act, L.x_perm), H, cap, E, poff, 0, g->dw1, status, st));
-  MOE_TRY(gemm_wgrad(at<void>(act, L.dy_perm), H, at<void>(act, L.h), F, cap, E, poff, 0, g->dw2, status, st));
-  MOE_TRY(launch_router_wgrad(at<void>(act, L.x_perm), at<float>(act, L.row_dlogit), counts, poff, E, H,
-                              g->dw_router, st));
-  if (S > 0) {
-    if (T > 0) {
+  if (cfg->dtype == MOE_GEMM_MXFP8) {
+    // contraction over tokens: transposed copies quantised along the tokens
+    const MxWs M = mx_ws_layout(cfg);
+    char* mb = static_cast<char*>(ws) + mx_ws_base(cfg);
+    auto q = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.q); };
+    auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
+    MOE_TRY(launch_quantize_cols(at<void>(act, L.dz), 1, cap, 2 * F, q(M.dzT), f(M.dzT), st));
+    MOE_TRY(launch_quantize_cols(at<void>(act, L.x_perm), 1, cap, H, q(M.xT), f(M.xT), st));
+    MOE_TRY(gemm_mx_wgrad(q(M.dzT), f(M.dzT), 2 * F, q(M.xT), f(M.xT), H, cap, E, poff, 0, g->dw1, status, st));
+    MOE_TRY(launch_quantize_cols(at<void>(act, L.dy_perm), 1, cap, H, q(M.dyT), f(M.dyT), st));
+    MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st));
+    MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, q(M.hT), f(M.hT), F, cap, E, poff, 0, g->dw2, status, st));
+    if (S > 0 && T > 0) {
+      MOE_TRY(launch_quantize_cols(at<void>(act, L.dzs), 1, T, 2 * S, q(M.dzsT), f(M.dzsT), st));
+      MOE_TRY(launch_quantize_cols(x, 1, T, H, q(M.xsT), f(M.xsT), st));
+      MOE_TRY(gemm_mx_wgrad(q(M.dzsT), f(M.dzsT), 2 * S, q(M.xsT), f(M.xsT), H, T, 1, nullptr, T, g->dw1_shared,
+                            status, st));
+      MOE_TRY(launch_quantize_cols(dy, 1, T, H, q(M.dysT), f(M.dysT), st));
+      MOE_TRY(launch_quantize_cols(at<void>(act, L.hs), 1, T, S, q(M.hsT), f(M.hsT), st));
+      MOE_TRY(gemm_mx_wgrad(q(M.dysT), f(M.dysT), H, q(M.hsT), f(M.hsT), S, T, 1, nullptr, T, g->dw2_shared, status,
+                            st));
+    }
+  } else {
+    MOE_TRY(gemm_wgrad(at<void>(act, L.dz), 2 * F, at<void>(act, L.x_perm), H, cap, E, poff, 0, g->dw1, status, st));
+    MOE_TRY(gemm_wgrad(at<void>(act, L.dy_perm), H, at<void>(act, L.h), F, cap, E, poff, 0, g->dw2, status, st));
+    if (S > 0 && T > 0) {
       MOE_TRY(gemm_wgrad(at<void>(act, L.dzs), 2 * S, x, H, T, 1, nullptr, T, g->dw1_shared, status, st));
       MOE_TRY(gemm_wgrad(dy, H, at<void>(act, L.hs), S, T, 1, nullptr, T, g->dw2_shared, status, st));
-    } else {
-      MOE_TRY(cudaMemsetAsync(g->dw1_shared, 0, sizeof(float) * 2 * S * H, st));
-      MOE_TRY(cudaMemsetAsync(g->dw2_shared, 0, sizeof(float) * S * H, st));
     }
+  }
+  MOE_TRY(launch_router_wgrad(at<void>(act, L.x_perm), at<float>(act, L.row_dlogit), counts, poff, E, H,
+                              g->dw_router, st));
+  if (S > 0 && T == 0) {
+    MOE_TRY(cudaMemsetAsync(g->dw1_shared, 0, sizeof(float) * 2 * S * H, st));
+    MOE_TRY(cudaMemsetAsync(g->dw2_shared, 0, sizeof(float) * S * H, st));
   }
   return MOE_OK;
 }

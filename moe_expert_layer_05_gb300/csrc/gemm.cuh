@@ -55,36 +55,50 @@ struct GemmParams {
   float* dgate_part;       // kSwigluBwd: [rows, n_tiles] partial dot products
   int valid_cols;          // kStoreF32: store only columns < valid_cols
   int rows_cap;            // rows allocated in the expert-ordered buffers (routed modes)
+  // MXFP8 only: E8M0 scale tiles of A and B (512 B per 128 rows x 128 K, see
+  // mxfp8.cu) and the number of tiles along K in one 128-row band of each.
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sfa_tiles_k;
+  int sfb_tiles_k;
   int* status;             // device status word (first error wins)
 };
 
-template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_>
+template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false>
 struct GemmCfg {
   static constexpr int BM = 128;
-  static constexpr int BK = 64;
+  static constexpr bool MX = MX_;                 // MXFP8 operands (E4M3 + E8M0 1x32 scales)
+  static constexpr int BK = MX ? 128 : 64;        // one 128-byte swizzle row per k-block
+  static constexpr int KSTEP = MX ? 32 : 16;      // K of one MMA instruction
   static constexpr int BN = BN_;
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
   static constexpr Sched S = S_;
   static constexpr Epi EP = EP_;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int SFA_BYTES = MX ? 512 : 0;
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
-  static constexpr int TMEM_COLS_RAW = 2 * BN;
+  static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of one stage's scales
+  static constexpr int TMEM_COLS_RAW = 2 * BN + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
                                    : TMEM_COLS_RAW <= 128 ? 128 : TMEM_COLS_RAW <= 256 ? 256 : 512;
   // Rows of one K-major B box (the SwiGLU tile loads gate and up halves as two boxes).
-  static constexpr int B_BOX_ROWS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
+  // (MXFP8: W1 is stored with gate and up rows interleaved in 64-row blocks, one box.)
+  static constexpr int B_BOX_ROWS = (EP == Epi::kSwiglu && !MX) ? BN / 2 : BN;
   // Columns of the output a tile covers (SwiGLU: half of the accumulator).
   static constexpr int OUT_COLS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
   static constexpr int THREADS = 192;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = MX ? idesc_mxf8_e4m3(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
-  static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile holds 128 gate + 128 up columns");
+  static_assert(EP != Epi::kSwiglu || BN == (MX ? 128 : 256), "SwiGLU tile: matching gate and up halves");
+  static_assert(!MX || (BN % 128 == 0 && !A_MN && !B_MN), "MXFP8 operands are K-major, 128-row scale tiles");
+  static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
   static_assert(STAGES >= 2, "pipeline depth");
 };
 
@@ -152,8 +166,30 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
 template <class C>
 __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p,
                                             const TileInfo& ti, int kb, uint8_t* a_dst, uint8_t* b_dst,
-                                            uint64_t* bar) {
+                                            uint8_t* sf_dst, uint64_t* bar) {
   const int k0 = kb * C::BK;
+  if constexpr (C::MX) {
+    // K-major E4M3 tiles (128 B per row) plus their 512-byte scale tiles.
+    int a_row, b_row, k_col;
+    if constexpr (C::S == Sched::kRoutedK) {
+      a_row = ti.m0;
+      b_row = ti.n * C::BN;
+      k_col = ti.k_row0 + k0;
+    } else {
+      a_row = ti.m0;
+      b_row = ti.group * p.b_rows_per_group + ti.n * C::BN;
+      k_col = k0;
+    }
+    tma_load_2d(a_dst, tmA, bar, k_col, a_row);
+    tma_load_2d(b_dst, tmB, bar, k_col, b_row);
+    const int kt = k_col / 128;
+    bulk_load(sf_dst, p.sfa + ((long long)(a_row / 128) * p.sfa_tiles_k + kt) * 512, 512, bar);
+    #pragma unroll
+    for (int i = 0; i < C::BN / 128; ++i)
+      bulk_load(sf_dst + 512 * (i + 1), p.sfb + ((long long)(b_row / 128 + i) * p.sfb_tiles_k + kt) * 512, 512,
+                bar);
+    return;
+  }
   // ---- A
   if constexpr (C::S == Sched::kRoutedK) {
     // A[m, k] = Abuf[k_row0 + k, m0 + m]  (MN-major, two 64-wide chunks)
@@ -363,6 +399,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_smem = smem;
   uint8_t* b_smem = smem + C::STAGES * C::A_BYTES;
+  uint8_t* sf_smem = b_smem + C::STAGES * C::B_BYTES;   // MXFP8 scale tiles (STAGES x (SFA + SFB))
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -425,7 +462,7 @@ __global__ void __launch_bounds__(192, 1)
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
           issue_loads<C>(&tmA, &tmB, p, ti, kb, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
-                         &full_bar[stage]);
+                         sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES), &full_bar[stage]);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -455,13 +492,30 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
           const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
-          #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
-            const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
-                                        : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
-                                        : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-            mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          if constexpr (C::MX) {
+            // scale tiles of this stage -> TMEM, then 4 MMAs of K=32; MMA kk reads byte kk
+            const uint32_t sf_addr = smem_u32(sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES));
+            const uint32_t sfa_t = tmem_base + 2 * C::BN + stage * C::SF_COLS;
+            const uint32_t sfb_t = sfa_t + 4;
+            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_plain16(sf_addr));
+            #pragma unroll
+            for (int i = 0; i < C::BN / 128; ++i)
+              tmem_cp_32x128b_warpx4(sfb_t + 4 * i, smem_desc_plain16(sf_addr + 512 * (i + 1)));
+            #pragma unroll
+            for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
+              const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+              mma_mxf8_ss(d_tmem, ad, bd, C::IDESC | idesc_sf_ids(kk, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+            #pragma unroll
+            for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
+              const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
+                                          : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+              const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
+                                          : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+              mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           any = true;
           mma_commit(&empty_bar[stage]);

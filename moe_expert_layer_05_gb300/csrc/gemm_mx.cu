@@ -1,0 +1,161 @@
+// MXFP8 GEMM launchers: the same persistent tcgen05 kernel with E4M3 operands
+// and E8M0 1x32 block scales (tcgen05.mma kind::mxf8f6f4.block_scale), the
+// recipe the Megatron Core MoE summary names for the expert GEMMs on
+// Blackwell (technical summary 2.5: expert GEMMs and activations in FP8, the
+// router and the rest in higher precision).
+//
+// Every operand is K-major E4M3 with its scale tiles (see mxfp8.cu).  Where the
+// contraction runs along the other dimension of a tensor (data gradients
+// through the weights, weight gradients over tokens) the operand is a
+// transposed quantised copy, so each 32-element block always lies along K.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_common.h"
+
+namespace moe {
+
+namespace {
+inline bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner, outer, 128, box_outer);
+}
+
+template <class C>
+cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int rows_alloc,
+                      int dense_rows, cudaStream_t st) {
+  int grid;
+  if constexpr (C::S == Sched::kRoutedK) {
+    grid = p.E * p.m_tiles_w * p.n_tiles;
+  } else if (p.poffsets != nullptr) {
+    grid = (rows_alloc / 128) * p.n_tiles;
+  } else {
+    grid = ((dense_rows + 127) / 128) * p.n_tiles;
+  }
+  return launch_gemm<C>(ta, tb, p, grid < num_sms() ? grid : num_sms(), st);
+}
+}  // namespace
+
+cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
+                        int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
+                        void* z, int* status, cudaStream_t st) {
+  // w1q rows of one expert are [gate 0..63, up 0..63, gate 64..127, up 64..127, ...]
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, aq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w1q, H, static_cast<uint64_t>(E) * 2 * F, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.m_rows = dense_rows;
+  p.k_len = H;
+  p.n_tiles = F / 64;
+  p.b_rows_per_group = 2 * F;
+  p.c = h;
+  p.ldc = F;
+  p.c2 = z;
+  p.ldc2 = 2 * F;
+  p.half_cols = F;
+  p.row_gate = row_gate;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(asf);
+  p.sfb = static_cast<const uint8_t*>(w1sf);
+  p.sfa_tiles_k = H / 128;
+  p.sfb_tiles_k = H / 128;
+  if (poffsets != nullptr)
+    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwiglu, true>>(ta, tb, p, rows_alloc,
+                                                                                      dense_rows, st);
+  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwiglu, true>>(ta, tb, p, rows_alloc, dense_rows,
+                                                                                   st);
+}
+
+// c [rows, N] bf16 = A [rows, K] x B_e [N, K]^T, both E4M3 with scales.
+cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
+                            int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
+                            cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, aq, K, rows_alloc, 128) || !make_tmap_u8(&tb, bq, K, static_cast<uint64_t>(E) * N, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.m_rows = dense_rows;
+  p.k_len = K;
+  p.n_tiles = N / 128;
+  p.b_rows_per_group = N;
+  p.c = c;
+  p.ldc = N;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(asf);
+  p.sfb = static_cast<const uint8_t*>(bsf);
+  p.sfa_tiles_k = K / 128;
+  p.sfb_tiles_k = K / 128;
+  if (poffsets != nullptr)
+    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kStoreBf16, true>>(ta, tb, p, rows_alloc,
+                                                                                         dense_rows, st);
+  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kStoreBf16, true>>(ta, tb, p, rows_alloc,
+                                                                                      dense_rows, st);
+}
+
+cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
+                              const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
+                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st) {
+  // B_e = W2_e^T [F, H], quantised along H
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, dyq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w2tq, H, static_cast<uint64_t>(E) * F, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.m_rows = dense_rows;
+  p.k_len = H;
+  p.n_tiles = F / 128;
+  p.b_rows_per_group = F;
+  p.c = dz;
+  p.ldc = 2 * F;
+  p.half_cols = F;
+  p.aux = static_cast<const __nv_bfloat16*>(z);
+  p.ld_aux = 2 * F;
+  p.row_gate = row_gate;
+  p.dgate_part = dgate_part;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(dysf);
+  p.sfb = static_cast<const uint8_t*>(w2tsf);
+  p.sfa_tiles_k = H / 128;
+  p.sfb_tiles_k = H / 128;
+  if (poffsets != nullptr)
+    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, p, rows_alloc,
+                                                                                         dense_rows, st);
+  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwigluBwd, true>>(ta, tb, p, rows_alloc,
+                                                                                      dense_rows, st);
+}
+
+cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
+                          int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
+                          cudaStream_t st) {
+  // A^T [M, rows] and B^T [N, rows], quantised along rows (the contraction)
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, atq, rows_alloc, M, 128) || !make_tmap_u8(&tb, btq, rows_alloc, N, 128))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = (poffsets != nullptr) ? E : 1;
+  p.m_rows = M;
+  p.k_len = dense_rows;
+  p.m_tiles_w = M / 128;
+  p.n_tiles = N / 128;
+  p.c = dw;
+  p.ldc = N;
+  p.c_group_stride = static_cast<long long>(M) * N;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(atsf);
+  p.sfb = static_cast<const uint8_t*>(btsf);
+  p.sfa_tiles_k = rows_alloc / 128;
+  p.sfb_tiles_k = rows_alloc / 128;
+  return launch_mx<GemmCfg<128, false, false, Sched::kRoutedK, Epi::kStoreF32, true>>(ta, tb, p, rows_alloc,
+                                                                                      dense_rows, st);
+}
+
+}  // namespace moe

@@ -65,4 +65,25 @@ cudaError_t gemm_dgrad_fc1(const void* dz, int rows_alloc, int F, const void* w1
 cudaError_t gemm_wgrad(const void* a, int M, const void* b, int N, int rows_alloc, int E, const int32_t* poffsets,
                        int dense_rows, float* dw, int* status, cudaStream_t st);
 
+// ------------------------------------------------------------ MXFP8 (mxfp8.cu, gemm_mx.cu)
+// Row mode: blocks of 32 along each row; gate_up_half > 0 also interleaves
+// the rows of every [gate; up] group of 2*half rows in 64-row blocks.
+cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
+                                 uint8_t* sf, cudaStream_t st);
+// Column mode: batch x [rows, cols] -> batch x [cols, rows], blocks along rows.
+cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
+                                 cudaStream_t st);
+cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
+                        int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
+                        void* z, int* status, cudaStream_t st);
+cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
+                            int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
+                            cudaStream_t st);
+cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
+                              const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
+                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st);
+cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
+                          int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
+                          cudaStream_t st);
+
 }  // namespace moe

@@ -1,0 +1,138 @@
+// MXFP8 quantisation (OCP Microscaling v1.0 with FP8 E4M3 elements): every
+// block of 32 consecutive values along the contraction dimension shares one
+// E8M0 scale X = 2^(floor(log2 amax) - 8), and each value is stored as
+// e4m3(v / X), rounded to nearest even and saturated to +-448.  This is the
+// MXFP8 recipe the Megatron Core MoE summary names for Blackwell (technical
+// summary 2.5); the block size and element type are the MX format's.
+//
+// Scales are written in the tiled order the tensor cores' scale-factor copy
+// (tcgen05.cp 32x128b, broadcast to the four lane quarters) consumes: one
+// 512-byte tile per 128 rows x 4 blocks (128 columns); inside a tile the scale
+// of row r, block b sits at byte (r % 32) * 16 + (r / 32) * 4 + b.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  // d[15:8] = e4m3(first source), d[7:0] = e4m3(second source)
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// E8M0 exponent of a block whose largest magnitude is amax.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  if (!(amax > 0.f)) return -127;
+  int e = ilogbf(amax) - 8;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ size_t sf_offset(int r, int b, int tiles_per_row) {
+  return (static_cast<size_t>(r >> 7) * tiles_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 +
+         (b & 3);
+}
+
+// Quantise 32 values held by this thread; writes 32 code bytes and returns the scale byte.
+__device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst) {
+  float amax = 0.f;
+  #pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mx_exponent(amax);
+  uint32_t w[8];
+  #pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint16_t lo = cvt_e4m3x2(ldexpf(v[4 * i + 0], -e), ldexpf(v[4 * i + 1], -e));
+    const uint16_t hi = cvt_e4m3x2(ldexpf(v[4 * i + 2], -e), ldexpf(v[4 * i + 3], -e));
+    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return static_cast<uint8_t>(e + 127);
+}
+
+// Output row of input row r when the rows come in groups of 2*half (an
+// expert's [gate; up] projection) and are interleaved in 64-row blocks:
+// gate 0..63, up 0..63, gate 64..127, up 64..127, ...  half == 0: identity.
+__device__ __forceinline__ long long gate_up_row(long long r, int half) {
+  if (half == 0) return r;
+  const long long g = r / (2 * half);
+  const int j = static_cast<int>(r % (2 * half));
+  const int up = j >= half ? 1 : 0;
+  const int jj = j - up * half;
+  return g * 2 * half + (jj / 64) * 128 + up * 64 + (jj % 64);
+}
+
+// Blocks along the row: src [rows, cols] bf16 -> codes [rows, cols], scales tiled.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ src, long long rows, int cols,
+                                                            int half, uint8_t* __restrict__ codes,
+                                                            uint8_t* __restrict__ sf) {
+  const int nb = cols / 32;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows * nb) return;
+  const long long r_in = i / nb;
+  const long long r = gate_up_row(r_in, half);
+  const int b = static_cast<int>(i % nb);
+  const uint4* p = src + (r_in * cols + b * 32) / 8;
+  float v[32];
+  #pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = p[q];
+    v[8 * q + 0] = bf16_lo(u.x); v[8 * q + 1] = bf16_hi(u.x);
+    v[8 * q + 2] = bf16_lo(u.y); v[8 * q + 3] = bf16_hi(u.y);
+    v[8 * q + 4] = bf16_lo(u.z); v[8 * q + 5] = bf16_hi(u.z);
+    v[8 * q + 6] = bf16_lo(u.w); v[8 * q + 7] = bf16_hi(u.w);
+  }
+  const uint8_t s = quantize32(v, codes + r * cols + b * 32);
+  sf[sf_offset(static_cast<int>(r), b, cols / 128)] = s;
+}
+
+// Blocks along the column, output transposed: src [rows, cols] bf16 ->
+// codes [cols, rows] (row c of the output = column c of the input), scales
+// tiled over the [cols, rows] output.  batch: independent matrices one after
+// another (expert weights).
+__global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
+                                                            int cols, uint8_t* __restrict__ codes,
+                                                            uint8_t* __restrict__ sf) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int rb = blockIdx.y;                 // block of 32 input rows
+  const long long mat = blockIdx.z;
+  if (c >= cols) return;
+  const __nv_bfloat16* s = src + mat * rows * cols + static_cast<long long>(rb) * 32 * cols + c;
+  float v[32];
+  #pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(s[static_cast<long long>(i) * cols]);
+  uint8_t* out = codes + mat * rows * cols + static_cast<long long>(c) * rows + rb * 32;
+  const uint8_t e = quantize32(v, out);
+  sf[mat * (static_cast<long long>(rows) * cols / 32) + sf_offset(c, rb, rows / 128)] = e;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
+                                 uint8_t* sf, cudaStream_t st) {
+  const long long n = rows * (cols / 32);
+  if (n == 0) return cudaSuccess;
+  quantize_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(static_cast<const uint4*>(src), rows,
+                                                                               cols, gate_up_half, codes, sf);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
+                                 cudaStream_t st) {
+  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  dim3 grid((cols + 255) / 256, rows / 32, batch);
+  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, sf);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

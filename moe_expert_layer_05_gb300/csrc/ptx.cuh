@@ -129,6 +129,44 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with E4M3 A and B and one E8M0
+// scale per 32 elements along K (MXFP8); K = 32 per instruction.  The scale
+// bytes come from TMEM; which byte of each 32-bit cell is used is part of idesc.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P;\n setp.ne.b32 P, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], P;\n}\n"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes from shared memory into TMEM, replicated into the
+// four 32-lane quarters: lane i (of every quarter), column c receives bytes
+// [4c, 4c+4) of row i.  Used for the MXFP8 scale factors.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// Shared-memory descriptor of a plain (unswizzled) block of rows of 16 bytes,
+// 8-row groups 128 bytes apart: the source of tmem_cp_32x128b_warpx4.
+__device__ __forceinline__ uint64_t smem_desc_plain16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 32;   // SBO: 8 rows x 16 B
+  d |= static_cast<uint64_t>(1) << 46;           // descriptor version for tcgen05
+  return d;                                      // layout type 0: no swizzle
+}
+
+// Non-tensor bulk copy global -> shared, completion as transaction bytes on bar.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -184,6 +222,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | ((b_mn_major ? 1u : 0u) << 16)            // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B,
+// fp32 D, E8M0 scale factors, K-major operands.  The scale-factor byte ids
+// (bits 4-5 for B, 29-30 for A) are or-ed in per MMA.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
+  return (0u << 7)                                   // A format E4M3
+         | (0u << 10)                                // B format E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale factor format E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
+  return (b_id << 4) | (a_id << 29);
 }
 
 // ---------------------------------------------------------------- misc

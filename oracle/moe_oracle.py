@@ -547,3 +547,123 @@ def expert_wgrad(a_rows, b_rows, poffsets):
 def dense_rows_of(n_rows):
     """poffsets of one group holding rows [0, n_rows) (the shared expert)."""
     return np.array([0, n_rows], np.int64)
+
+
+# ---------------------------------------------------------------------------
+# The layer under the MXFP8 recipe (technical summary 2.5: expert GEMMs and
+# their activations in FP8 with MX block scales; router, gates, combine in
+# high precision).  Each expert-GEMM operand passes through the MX quantiser
+# along that GEMM's contraction axis (blocks of 32 consecutive values):
+#   fc1:       x rows along H,  W1_e along H
+#   fc2:       h' = g*silu(a)*b along F (the gate is applied before the
+#              quantiser, as the layer applies it inside fc1), W2_e along F
+#   fc2 dgrad: dy rows along H, W2_e along H
+#   fc1 dgrad: dz rows along 2F, W1_e along 2F
+#   wgrad:     dz, x, dy, h' along the tokens of the expert, in expert order
+#              (ascending token), zero-padded to whole blocks
+# ``quant(v, axis)`` is the quantise-dequantise map; the identity gives back
+# the unquantised layer (tests/test_oracle_mx.py pins that).
+# ---------------------------------------------------------------------------
+
+def _pad_rows(a, mult=32):
+    r = a.shape[0]
+    p = (-r) % mult
+    if p == 0:
+        return a
+    return np.concatenate([a, np.zeros((p,) + a.shape[1:])], axis=0)
+
+
+def _q_tokens(a, quant):
+    """Quantise along the token axis in blocks of 32 rows (zero padding)."""
+    r = a.shape[0]
+    return quant(_pad_rows(a), 0)[:r]
+
+
+def moe_forward_mx(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=None, w2_shared=None,
+                   routing=None, quant=mxfp8_roundtrip):
+    x = np.asarray(x, np.float64)
+    T = x.shape[0]
+    E = _shape(w1)[0]
+    F = _shape(w1)[1] // 2
+    logits = None
+    if routing is None:
+        logits = router_logits(x, w_router)
+        idx, gate = route(logits, k, score, bias)
+    else:
+        idx = np.asarray(routing[0], np.int64)
+        gate = np.asarray(routing[1], np.float64)
+    y = np.zeros_like(x)
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        W1 = np.asarray(w1[e], np.float64)
+        W2 = np.asarray(w2[e], np.float64)
+        z = quant(x[tok], -1) @ quant(W1, -1).T
+        hp = gate[tok, slot][:, None] * silu(z[:, :F]) * z[:, F:]
+        np.add.at(y, tok, quant(hp, -1) @ quant(W2, -1).T)
+    if w1_shared is not None:
+        W1 = np.asarray(w1_shared, np.float64)
+        W2 = np.asarray(w2_shared, np.float64)
+        S = W1.shape[0] // 2
+        z = quant(x, -1) @ quant(W1, -1).T
+        y += quant(silu(z[:, :S]) * z[:, S:], -1) @ quant(W2, -1).T
+    return {"y": y, "logits": logits, "topk_idx": idx.astype(np.int32), "gates": gate}
+
+
+def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None, w2_shared=None,
+                    quant=mxfp8_roundtrip):
+    """Gradients as the MXFP8 recipe computes them: the chain rule of the
+    unquantised layer, with every expert-GEMM operand quantised along its
+    contraction axis (straight through the quantiser)."""
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    T, H = x.shape
+    E = _shape(w1)[0]
+    F = _shape(w1)[1] // 2
+    idx = np.asarray(fwd["topk_idx"], np.int64)
+    gate = np.asarray(fwd["gates"], np.float64)
+    k = idx.shape[1]
+    dx = np.zeros_like(x)
+    dW1 = np.zeros((E, 2 * F, H))
+    dW2 = np.zeros((E, H, F))
+    dgate = np.zeros((T, k))
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)          # ascending token: the expert's row order
+        if tok.size == 0:
+            continue
+        W1 = np.asarray(w1[e], np.float64)
+        W2 = np.asarray(w2[e], np.float64)
+        xe = x[tok]
+        z = quant(xe, -1) @ quant(W1, -1).T
+        a, b = z[:, :F], z[:, F:]
+        h = silu(a) * b
+        g = gate[tok, slot][:, None]
+        dye = dy[tok]
+        dhp = quant(dye, -1) @ quant(W2, 0)             # contraction over H
+        dgate[tok, slot] = (dhp * h).sum(axis=1)
+        dh = g * dhp
+        dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
+        np.add.at(dx, tok, quant(dz, -1) @ quant(W1, 0))  # contraction over 2F
+        dW1[e] = _q_tokens(dz, quant).T @ _q_tokens(xe, quant)
+        dW2[e] = _q_tokens(dye, quant).T @ _q_tokens(g * h, quant)
+    out = {"dW1": dW1, "dW2": dW2, "dgate": dgate}
+    if w1_shared is not None:
+        W1 = np.asarray(w1_shared, np.float64)
+        W2 = np.asarray(w2_shared, np.float64)
+        S = W1.shape[0] // 2
+        z = quant(x, -1) @ quant(W1, -1).T
+        a, b = z[:, :S], z[:, S:]
+        h = silu(a) * b
+        dh = quant(dy, -1) @ quant(W2, 0)
+        dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
+        dx += quant(dz, -1) @ quant(W1, 0)
+        out["dW1_shared"] = _q_tokens(dz, quant).T @ _q_tokens(x, quant)
+        out["dW2_shared"] = _q_tokens(dy, quant).T @ _q_tokens(h, quant)
+    logits = fwd["logits"] if fwd.get("logits") is not None else router_logits(x, w_router)
+    dl = router_backward(logits, idx, gate, dgate, score)
+    dx += dl @ np.asarray(w_router, np.float64)
+    out["dlogits"] = dl
+    out["dWr"] = dl.T @ x
+    out["dx"] = dx
+    return out

@@ -1,0 +1,271 @@
+"""GPU parity of the MXFP8 path through the C ABI.
+
+* the quantiser is bit-exact against the oracle's (codes and E8M0 scales),
+  over every finite bf16 value and in all three modes;
+* each MXFP8 grouped GEMM matches the oracle's fp64 GEMM on the same quantised
+  operands (the GPU quantises with its own kernel, the oracle with its own;
+  both are bit-exact, so the operands are identical);
+* the MXFP8 layer (forward, dgrad, wgrad) is within rel-L2 3e-2 of the fp64
+  oracle of the same recipe (operands quantised along the same axes), and
+  within the format's own error of the unquantised layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_bf16_close, f64, rel_l2
+from moe_expert_layer_05_gb300 import api
+from moe_expert_layer_05_gb300.inputs import Workload, make_inputs, random_topk_indices, to_bf16
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def untile(sf: torch.Tensor, R: int, C: int) -> np.ndarray:
+    """Scale tiles (512 B per 128 rows x 4 blocks) -> plain [R, C/32]."""
+    t = sf.cpu().numpy().reshape(R // 128, C // 128, 512)
+    r = np.arange(128)[:, None]
+    b = np.arange(4)[None, :]
+    idx = (r % 32) * 16 + (r // 32) * 4 + b
+    return t[:, :, idx].transpose(0, 2, 1, 3).reshape(R, C // 32)
+
+
+def quantize_gpu(x: torch.Tensor, mode: int, batch=1):
+    n = x.numel()
+    codes = torch.empty(n, dtype=torch.uint8, device=DEV)
+    sf = torch.empty(n // 32, dtype=torch.uint8, device=DEV)
+    if mode == api.MX_ROWS:
+        rows, cols = x.numel() // x.shape[-1], x.shape[-1]
+        api.moe_quantize_mxfp8(x, 1, rows, cols, mode, codes, sf)
+    else:
+        rows, cols = x.shape[-2], x.shape[-1]
+        api.moe_quantize_mxfp8(x, batch, rows, cols, mode, codes, sf)
+    return codes, sf
+
+
+def _rand(shape, seed, std=1.0):
+    return np.random.default_rng(seed).standard_normal(shape, dtype=np.float32) * np.float32(std)
+
+
+def test_quantize_every_finite_bf16_value(lib):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    vals = vals[np.isfinite(vals)]
+    vals = vals[np.argsort(np.abs(vals), kind="stable")]          # blocks of similar magnitude
+    n = int(np.ceil(len(vals) / (128 * 128))) * 128 * 128
+    full = np.zeros(n, np.float32)
+    full[:len(vals)] = vals
+    x = to_bf16(full.reshape(-1, 128))
+    codes, sf = quantize_gpu(x.to(DEV), api.MX_ROWS)
+    torch.cuda.synchronize()
+    oc, os_ = O.mxfp8_quantize(f64(x), axis=-1)
+    np.testing.assert_array_equal(codes.cpu().numpy().reshape(oc.shape), oc)
+    np.testing.assert_array_equal(untile(sf, *x.shape), os_)
+
+
+@pytest.mark.parametrize("R,C,scale", [(256, 512, 1.0), (128, 128, 1e-30), (384, 256, 1e30), (128, 7168, 3.0)])
+def test_quantize_rows(lib, R, C, scale):
+    v = _rand((R, C), R + C) * np.float32(scale)
+    v[5, 64:96] = 0.0                                               # an all-zero block
+    v[7, :32] *= np.float32(1e-3)
+    x = to_bf16(v)
+    codes, sf = quantize_gpu(x.to(DEV), api.MX_ROWS)
+    torch.cuda.synchronize()
+    oc, os_ = O.mxfp8_quantize(f64(x), axis=-1)
+    np.testing.assert_array_equal(codes.cpu().numpy().reshape(R, C), oc)
+    np.testing.assert_array_equal(untile(sf, R, C), os_)
+
+
+@pytest.mark.parametrize("B,R,C", [(1, 256, 384), (3, 128, 256), (2, 512, 128)])
+def test_quantize_cols_transposed(lib, B, R, C):
+    x = to_bf16(_rand((B, R, C), 7 + B))
+    codes, sf = quantize_gpu(x.to(DEV), api.MX_COLS_T, batch=B)
+    torch.cuda.synchronize()
+    codes = codes.cpu().numpy().reshape(B, C, R)
+    sfn = sf.reshape(B, -1)
+    for b in range(B):
+        oc, os_ = O.mxfp8_quantize(f64(x[b]).T, axis=-1)          # [C, R], blocks along R
+        np.testing.assert_array_equal(codes[b], oc)
+        np.testing.assert_array_equal(untile(sfn[b], C, R), os_)
+
+
+def test_quantize_gate_up_interleave(lib):
+    E, F, H = 2, 256, 128
+    x = to_bf16(_rand((E, 2 * F, H), 9))
+    codes, sf = quantize_gpu(x.to(DEV), api.MX_ROWS_GATE_UP, batch=E)
+    torch.cuda.synchronize()
+    got = codes.cpu().numpy().reshape(E, 2 * F, H)
+    gsf = untile(sf, E * 2 * F, H).reshape(E, 2 * F, H // 32)
+    oc, os_ = O.mxfp8_quantize(f64(x), axis=-1)
+    for e in range(E):
+        for j in range(2 * F):
+            up, jj = divmod(j, F)
+            r = (jj // 64) * 128 + up * 64 + jj % 64
+            np.testing.assert_array_equal(got[e, r], oc[e, j])
+            np.testing.assert_array_equal(gsf[e, r], os_[e, j])
+
+
+# ------------------------------------------------------------------ grouped GEMMs
+def _routed(T, H, E, k, F, skew, seed):
+    idx = random_topk_indices(T, E, k, seed=seed, skew=skew)
+    m = O.permutation_maps(idx, E, 128)
+    cfg = api.make_config(T, H, E, k, F, dtype="mxfp8")
+    cap = api.moe_capacity_rows(cfg)
+    used = int(m["poffsets"][-1])
+    valid = np.zeros(cap, bool)
+    valid[:used] = m["row_src"] >= 0
+    return cfg, m, cap, used, valid
+
+
+def _rows(cap, K, valid, seed, std=1.0):
+    a = _rand((cap, K), seed, std)
+    a[~valid] = 0.0
+    return to_bf16(a)
+
+
+def _ws(cfg):
+    ws = torch.zeros(api.moe_workspace_bytes(cfg), dtype=torch.uint8, device=DEV)
+    api.moe_workspace_init(ws)
+    return ws
+
+
+def deq(t_bf16, axis):
+    return O.mxfp8_roundtrip(f64(t_bf16), axis=axis)
+
+
+MX_CASES = [
+    # T, H, E, k, F, skew
+    (256, 256, 8, 2, 256, 0.0),
+    (640, 512, 16, 4, 384, 1.5),
+    (384, 256, 64, 8, 128, 1.0),
+]
+
+
+@pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
+def test_mx_gemm_forward(lib, T, H, E, k, F, skew):
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 3)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    x = _rows(cap, H, valid, 4)
+    w1 = to_bf16(_rand((E, 2 * F, H), 5, 0.05))
+    w2 = to_bf16(_rand((E, H, F), 6, 0.05))
+    rg = np.where(valid, np.abs(_rand((cap,), 7)), 0).astype(np.float32)
+    xq, xsf = quantize_gpu(x.to(DEV), api.MX_ROWS)
+    w1q, w1sf = quantize_gpu(w1.to(DEV), api.MX_ROWS_GATE_UP, batch=E)
+    h_in = _rows(cap, F, valid, 8)
+    hq, hsf = quantize_gpu(h_in.to(DEV), api.MX_ROWS)
+    w2q, w2sf = quantize_gpu(w2.to(DEV).reshape(E * H, F), api.MX_ROWS)
+    z = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=DEV)
+    h = torch.zeros((cap, F), dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+    ws = _ws(cfg)
+    api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, h, ws, c2=z, row_gate=torch.from_numpy(rg).to(DEV),
+                         poffsets=po, a_scales=xsf, b_scales=w1sf)
+    api.moe_grouped_gemm(cfg, api.GG_FC2, hq, w2q, o, ws, poffsets=po, a_scales=hsf, b_scales=w2sf)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(ws) == 0
+    zr, hr = O.expert_fc1(deq(x, -1)[:used], deq(w1, -1), m["poffsets"], rg[:used])
+    assert_bf16_close(f64(z)[:used], zr, "z (mxfp8)")
+    assert_bf16_close(f64(h)[:used], hr, "h (mxfp8)")
+    assert_bf16_close(f64(o)[:used], O.expert_fc2(deq(h_in, -1)[:used], deq(w2, -1), m["poffsets"]), "o (mxfp8)")
+
+
+@pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
+def test_mx_gemm_dgrad(lib, T, H, E, k, F, skew):
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 13)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    dy = _rows(cap, H, valid, 14)
+    z = _rows(cap, 2 * F, valid, 15)
+    dz_in = _rows(cap, 2 * F, valid, 16)
+    w1 = to_bf16(_rand((E, 2 * F, H), 17, 0.05))
+    w2 = to_bf16(_rand((E, H, F), 18, 0.05))
+    rg = np.where(valid, np.abs(_rand((cap,), 19)), 0).astype(np.float32)
+    dyq, dysf = quantize_gpu(dy.to(DEV), api.MX_ROWS)
+    w2tq, w2tsf = quantize_gpu(w2.to(DEV), api.MX_COLS_T, batch=E)        # [E, F, H]
+    dzq, dzsf = quantize_gpu(dz_in.to(DEV), api.MX_ROWS)
+    w1tq, w1tsf = quantize_gpu(w1.to(DEV), api.MX_COLS_T, batch=E)        # [E, H, 2F]
+    dz = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=DEV)
+    dpart = torch.zeros((cap, F // 128), dtype=torch.float32, device=DEV)
+    dx = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+    ws = _ws(cfg)
+    api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC2, dyq, w2tq, dz, ws, aux=z.to(DEV),
+                         row_gate=torch.from_numpy(rg).to(DEV), dgate_part=dpart, poffsets=po, a_scales=dysf,
+                         b_scales=w2tsf)
+    api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC1, dzq, w1tq, dx, ws, poffsets=po, a_scales=dzsf, b_scales=w1tsf)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(ws) == 0
+    # W2 quantised along H (its rows), W1 along 2F (its rows): blocks run along each weight's axis 1 of [E, ., .]
+    w2_deq = O.mxfp8_roundtrip(f64(w2), axis=1)
+    w1_deq = O.mxfp8_roundtrip(f64(w1), axis=1)
+    dzr, dgr = O.expert_dgrad_fc2(deq(dy, -1)[:used], w2_deq, f64(z)[:used], m["poffsets"], rg[:used])
+    assert_bf16_close(f64(dz)[:used], dzr, "dz (mxfp8)", rel_l2_tol=6e-3)
+    dg = f64(dpart)[:used].sum(1)
+    assert rel_l2(dg, dgr) < 2e-3
+    assert_bf16_close(f64(dx)[:used], O.expert_dgrad_fc1(deq(dz_in, -1)[:used], w1_deq, m["poffsets"]), "dx (mxfp8)")
+
+
+@pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
+def test_mx_gemm_wgrad(lib, T, H, E, k, F, skew):
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 23)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    dz = _rows(cap, 2 * F, valid, 24)
+    xp = _rows(cap, H, valid, 25)
+    dzT, dzTs = quantize_gpu(dz.to(DEV), api.MX_COLS_T)      # [2F, cap]
+    xT, xTs = quantize_gpu(xp.to(DEV), api.MX_COLS_T)        # [H, cap]
+    dw1 = torch.full((E, 2 * F, H), 7.0, dtype=torch.float32, device=DEV)
+    ws = _ws(cfg)
+    api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, dzT, xT, dw1, ws, poffsets=po, a_scales=dzTs, b_scales=xTs)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(ws) == 0
+    a = O.mxfp8_roundtrip(f64(dz), axis=0)[:used]            # blocks along tokens
+    b = O.mxfp8_roundtrip(f64(xp), axis=0)[:used]
+    ref = O.expert_wgrad(a, b, m["poffsets"])
+    scale = np.einsum("rm,rn->mn", np.abs(a), np.abs(b))
+    assert np.all(np.abs(f64(dw1) - ref) <= 2.0 ** -14 * scale[None] + 1e-6)
+    assert np.all(f64(dw1)[m["counts"] == 0] == 0)
+
+
+# ------------------------------------------------------------------ layer
+MX_LAYERS = {
+    "dsv3_mx_small": Workload("dsv3_mx_small", T=384, H=256, E=64, k=8, F=128, S=256, score="sigmoid", zipf_s=1.2,
+                              dtype="mxfp8", backward=True),
+    "mixtral_mx_small": Workload("mixtral_mx_small", T=256, H=512, E=8, k=2, F=768, dtype="mxfp8", backward=True),
+}
+
+
+@pytest.mark.parametrize("name", list(MX_LAYERS))
+def test_mx_layer_against_mxfp8_oracle(lib, name):
+    """The MXFP8 layer against the oracle of the same recipe (rel-L2 <= 3e-2),
+    and against the unquantised layer (the format's own error: < 15 %)."""
+    w = MX_LAYERS[name]
+    inp = make_inputs(w, seed=2)
+    dinp = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    layer = api.MoELayer(api.config_of(w), dinp, with_backward=True)
+    y = layer.forward(dinp["x"])
+    dx, dgate, grads = layer.backward(dinp["x"], dinp["dy"])
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(layer.ws) == 0
+    sh = dict(w1_shared=None if w.S == 0 else f64(inp["w1_shared"]),
+              w2_shared=None if w.S == 0 else f64(inp["w2_shared"]))
+    bias = None if inp["bias"] is None else f64(inp["bias"])
+    args = (f64(inp["x"]), f64(inp["w_router"]), f64(inp["w1"]), f64(inp["w2"]))
+    fwd = O.moe_forward_mx(*args, k=w.k, score=w.score, bias=bias, **sh)
+    keys = O.selection_keys(fwd["logits"], w.score, bias)
+    stable = O.topk_gap(keys, w.k) >= 1e-5
+    np.testing.assert_array_equal(layer.fields()["topk_idx"].cpu().numpy()[stable], fwd["topk_idx"][stable])
+    r_y = rel_l2(f64(y)[stable], fwd["y"][stable])
+    assert r_y <= 3e-2, r_y
+    plain = O.moe_forward(*args, k=w.k, score=w.score, bias=bias, **sh)
+    assert rel_l2(f64(y)[stable], plain["y"][stable]) < 0.15
+    bwd = O.moe_backward_mx(*args, fwd, f64(inp["dy"]), score=w.score, **sh)
+    assert rel_l2(f64(dx)[stable], bwd["dx"][stable]) <= 3e-2
+    assert rel_l2(f64(dgate)[stable], bwd["dgate"][stable]) <= 3e-2
+    touched = np.zeros(w.E, bool)
+    touched[fwd["topk_idx"][~stable].ravel()] = True
+    for gname, oname in (("dw1", "dW1"), ("dw2", "dW2"), ("dw_router", "dWr")):
+        r = rel_l2(f64(grads[gname])[~touched], bwd[oname][~touched])
+        assert r <= 3e-2, (gname, r)
+    if w.S and stable.all():
+        for gname, oname in (("dw1_shared", "dW1_shared"), ("dw2_shared", "dW2_shared")):
+            r = rel_l2(f64(grads[gname]), bwd[oname])
+            assert r <= 3e-2, (gname, r)
