@@ -166,12 +166,24 @@ class _F32Experts:
         return self
 
 
-def oracle_forward_timed(w, inp_cpu, tokens: np.ndarray) -> float:
+def _oracle_fns(w):
     from oracle import moe_oracle as O
+    if w.dtype == "mxfp8":
+        return O.moe_forward_mx, O.moe_backward_mx
+    return O.moe_forward, O.moe_backward
+
+
+def oracle_step_timed(w, inp_cpu, tokens: np.ndarray) -> float:
+    """One step of the oracle (forward, plus backward for training workloads)
+    on the given tokens; returns seconds."""
+    fwd_fn, bwd_fn = _oracle_fns(w)
     x = inp_cpu["x_np"][tokens]
+    sh = dict(w1_shared=inp_cpu["w1s_np"], w2_shared=inp_cpu["w2s_np"])
     t0 = time.perf_counter()
-    O.moe_forward(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], k=w.k, score=w.score,
-                  bias=inp_cpu["bias_np"], w1_shared=inp_cpu["w1s_np"], w2_shared=inp_cpu["w2s_np"])
+    fwd = fwd_fn(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], k=w.k, score=w.score, bias=inp_cpu["bias_np"],
+                 **sh)
+    if w.backward:
+        bwd_fn(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], fwd, inp_cpu["dy_np"][tokens], score=w.score, **sh)
     return time.perf_counter() - t0
 
 
@@ -179,8 +191,18 @@ def oracle_inputs(w, dinp) -> dict:
     def npf(t):
         return None if t is None else t.to("cpu", torch.float32).numpy().astype(np.float64)
     return {"x_np": npf(dinp["x"]), "wr_np": npf(dinp["w_router"]), "bias_np": npf(dinp["bias"]),
-            "w1s_np": npf(dinp["w1_shared"]), "w2s_np": npf(dinp["w2_shared"]),
-            "w1": _F32Experts(dinp["w1"]).warm(), "w2": _F32Experts(dinp["w2"]).warm()}
+            "w1s_np": npf(dinp["w1_shared"]), "w2s_np": npf(dinp["w2_shared"]), "dy_np": npf(dinp["dy"]),
+            "w1": _F32Experts(dinp["w1"]), "w2": _F32Experts(dinp["w2"])}
+
+
+def warm_experts(w, inp, tokens):
+    """Copy to host (untimed) the experts the given tokens route to."""
+    from oracle import moe_oracle as O
+    logits = O.router_logits(inp["x_np"][tokens], inp["wr_np"])
+    idx, _ = O.route(logits, w.k, w.score, inp["bias_np"])
+    for e in np.unique(idx):
+        inp["w1"][e]
+        inp["w2"][e]
 
 
 def host_cores() -> int:
@@ -196,12 +218,14 @@ def cpu_baseline(w, dinp, target_s: float = 10.0) -> dict:
     inp = oracle_inputs(w, dinp)
     n = 8
     while True:
-        t = oracle_forward_timed(w, inp, np.arange(n))
+        warm_experts(w, inp, np.arange(n))
+        t = oracle_step_timed(w, inp, np.arange(n))
         if t >= 0.7 * target_s or n >= w.T:
             break
         n = min(w.T, max(n * 2, int(n * target_s / max(t, 1e-3))))
+    what = "forward + backward" if w.backward else "forward"
     return {"value": n / t, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"first {n} of {w.T} tokens, full forward (fp64 numpy), {t:.1f} s"}
+            "sample": f"first {n} of {w.T} tokens, {what} (fp64 numpy), {t:.1f} s"}
 
 
 # ---------------------------------------------------------------- our arm
@@ -268,16 +292,30 @@ def run_ours(args) -> dict | None:
     s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
     e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
     z = fl["z"] if w.backward else None
+    mx = w.dtype == "mxfp8"
+    if mx:
+        # operands quantised by the library's own quantiser into bench-owned buffers
+        cap = layer.layout.cap
+        xq = torch.empty(cap * w.H, dtype=torch.uint8, device=dev)
+        xsf = torch.empty(cap * w.H // 32, dtype=torch.uint8, device=dev)
+        w1q = torch.empty(dinp["w1"].numel(), dtype=torch.uint8, device=dev)
+        w1sf = torch.empty(dinp["w1"].numel() // 32, dtype=torch.uint8, device=dev)
+        api.moe_quantize_mxfp8(fl["x_perm"], 1, cap, w.H, api.MX_ROWS, xq, xsf)
+        api.moe_quantize_mxfp8(dinp["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP, w1q, w1sf)
+        fc1_args = (xq, w1q, fl["h"], layer.ws)
+        fc1_kw = dict(c2=z, row_gate=fl["row_gate"], poffsets=fl["poffsets"], a_scales=xsf, b_scales=w1sf)
+    else:
+        fc1_args = (fl["x_perm"], dinp["w1"], fl["h"], layer.ws)
+        fc1_kw = dict(c2=z, row_gate=fl["row_gate"], poffsets=fl["poffsets"])
     for i in range(Kk):
         flush.zero_()
         s_ev[i].record(stream)
-        api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, fl["x_perm"], dinp["w1"], fl["h"], layer.ws, c2=z,
-                             row_gate=fl["row_gate"], poffsets=fl["poffsets"])
+        api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, *fc1_args, **fc1_kw)
         e_ev[i].record(stream)
     torch.cuda.synchronize()
     fc1_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(s_ev, e_ev))
     # the rest of the forward chain, one stage at a time (context for the line)
-    stages = stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, Kk)
+    stages = {} if mx else stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, Kk)
     stages["fc1_grouped_gemm"] = fc1_ms
 
     # ---- end to end: host buffers, copies inside the timed region
@@ -306,6 +344,10 @@ def run_ours(args) -> dict | None:
     fc1_flop = 4.0 * R * w.H * w.F
     achieved = fc1_flop / (fc1_ms / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
+    peak_note = f"bf16_tflops of {peak_src} peaks (burst; kernel timed alone)"
+    if mx:
+        peak *= 2.0   # dense fp8 / bf16 nominal ratio (4.5 / 2.25 PFLOP/s)
+        peak_note = f"2 x bf16_tflops of {peak_src} peaks (fp8:bf16 nominal ratio; burst)"
     fwd_flop = 6.0 * R * w.H * w.F + 6.0 * w.T * w.H * w.S
     step_flop = fwd_flop * (3 if w.backward else 1)
     out = {
@@ -319,16 +361,18 @@ def run_ours(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "mxfp8" if mx else "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
                    "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
                    "l2": "flushed (512 MB write) before every timed step, outside the events",
                    "parallelism": f"replicas x{world}"},
         "expert_gemm_tflops_per_gpu": step_flop / (total_ms / K / 1e3) / 1e12,
-        "roofline": {"bound": "tensor", "kernel": "fc1 grouped GEMM (tcgen05, fused gated SwiGLU)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "fc1 grouped GEMM (tcgen05" + (" mxf8f6f4 block-scaled" if mx else "") +
+                               ", fused gated SwiGLU)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"bf16_tflops of {peak_src} peaks (burst; kernel timed alone)",
+                     "peak_source": peak_note,
                      "traffic": FC1_TRAFFIC_BYTES, "flop_per_launch": fc1_flop, "ms_per_launch": fc1_ms},
         "stages_ms": stages,
         "e2e": {"value": aggregate(w.T, K, world, e2e_total), "unit": "tokens/s",
@@ -387,24 +431,28 @@ def run_reference(args) -> dict | None:
     else:
         dinp = make_inputs(w, seed=0)
     inp = oracle_inputs(w, dinp)
+    warm_experts(w, inp, np.arange(4))
     # size the per-step sample so that W + K steps end within ~2 minutes
-    t1 = oracle_forward_timed(w, inp, np.arange(4)) / 4
+    t1 = oracle_step_timed(w, inp, np.arange(4)) / 4
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(w.T, per_step_budget / max(t1, 1e-6))))
     rng = np.random.default_rng(0)
-    for _ in range(args.warmup):
-        oracle_forward_timed(w, inp, np.sort(rng.choice(w.T, n, replace=False)))
+    samples = [np.sort(rng.choice(w.T, n, replace=False)) for _ in range(args.warmup + args.steps)]
+    warm_experts(w, inp, np.unique(np.concatenate(samples)))   # host copies of the weights, untimed
+    for smp in samples[:args.warmup]:
+        oracle_step_timed(w, inp, smp)
     total = 0.0
-    for _ in range(args.steps):
-        total += oracle_forward_timed(w, inp, np.sort(rng.choice(w.T, n, replace=False)))
+    for smp in samples[args.warmup:]:
+        total += oracle_step_timed(w, inp, smp)
     value = n * args.steps / total
-    sample = f"{n} random tokens of {w.T} per step (fp64 numpy oracle, full forward)"
+    sample = (f"{n} random tokens of {w.T} per step (fp64 numpy oracle, "
+              f"{'forward + backward' if w.backward else 'forward'})")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
-                   "score": w.score, "pass": "fwd"},
+                   "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
