@@ -179,6 +179,8 @@ def oracle_step_timed(w, inp_cpu, tokens: np.ndarray) -> float:
     fwd_fn, bwd_fn = _oracle_fns(w)
     x = inp_cpu["x_np"][tokens]
     sh = dict(w1_shared=inp_cpu["w1s_np"], w2_shared=inp_cpu["w2s_np"])
+    if w.dtype == "mxfp8":
+        sh["weight_cache"] = inp_cpu["wcache"]      # weights quantised once, as the recipe does
     t0 = time.perf_counter()
     fwd = fwd_fn(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], k=w.k, score=w.score, bias=inp_cpu["bias_np"],
                  **sh)
@@ -192,7 +194,7 @@ def oracle_inputs(w, dinp) -> dict:
         return None if t is None else t.to("cpu", torch.float32).numpy().astype(np.float64)
     return {"x_np": npf(dinp["x"]), "wr_np": npf(dinp["w_router"]), "bias_np": npf(dinp["bias"]),
             "w1s_np": npf(dinp["w1_shared"]), "w2s_np": npf(dinp["w2_shared"]), "dy_np": npf(dinp["dy"]),
-            "w1": _F32Experts(dinp["w1"]), "w2": _F32Experts(dinp["w2"])}
+            "w1": _F32Experts(dinp["w1"]), "w2": _F32Experts(dinp["w2"]), "wcache": {}}
 
 
 def warm_experts(w, inp, tokens):
@@ -200,9 +202,21 @@ def warm_experts(w, inp, tokens):
     from oracle import moe_oracle as O
     logits = O.router_logits(inp["x_np"][tokens], inp["wr_np"])
     idx, _ = O.route(logits, w.k, w.score, inp["bias_np"])
+    quantised = w.dtype == "mxfp8"
     for e in np.unique(idx):
         inp["w1"][e]
         inp["w2"][e]
+        if quantised:
+            # the recipe quantises weights once; do it here, outside the timed oracle call
+            for name, W in (("w1", inp["w1"][e]), ("w2", inp["w2"][e])):
+                for axis in (-1, 0):
+                    key = (name, int(e), axis)
+                    if key not in inp["wcache"]:
+                        inp["wcache"][key] = O.mxfp8_roundtrip(W, axis)
+    if quantised and inp["w1s_np"] is not None:
+        for name, W in (("w1s", inp["w1s_np"]), ("w2s", inp["w2s_np"])):
+            for axis in (-1, 0):
+                inp["wcache"].setdefault((name, 0, axis), O.mxfp8_roundtrip(W, axis))
 
 
 def host_cores() -> int:
@@ -263,6 +277,27 @@ def run_ours(args) -> dict | None:
         step()
     torch.cuda.synchronize()
 
+    # One step as a CUDA graph (the layer issues a fixed launch sequence and no
+    # host sync, so it captures whole); --no-graph launches it eagerly.
+    run = step
+    launches_per_step = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()                      # warm the capture stream's first use
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        l0 = api.moe_kernel_launches()
+        with torch.cuda.graph(graph):
+            step()
+        launches_per_step = api.moe_kernel_launches() - l0
+        run = graph.replay
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+
     # ---- timed region
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -275,10 +310,12 @@ def run_ours(args) -> dict | None:
     for i in range(K):
         flush.zero_()
         starts[i].record(stream)
-        step()
+        run()
         ends[i].record(stream)
     torch.cuda.synchronize()
     launches = api.moe_kernel_launches() - l0
+    if launches_per_step is not None:
+        launches = launches_per_step * K      # graph replays: the library's kernels, counted at capture
     barrier(world)
     clk = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -366,7 +403,8 @@ def run_ours(args) -> dict | None:
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
                    "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
                    "l2": "flushed (512 MB write) before every timed step, outside the events",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "cuda_graph": not args.no_graph},
         "expert_gemm_tflops_per_gpu": step_flop / (total_ms / K / 1e3) / 1e12,
         "roofline": {"bound": "tensor",
                      "kernel": "fc1 grouped GEMM (tcgen05" + (" mxf8f6f4 block-scaled" if mx else "") +
@@ -467,6 +505,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each timed step eagerly, not as a CUDA graph")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()

@@ -196,7 +196,8 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
  * the library (every GPU that loads the library keeps it until the process
  * exits), so the call allocates nothing: no cudaMalloc, no cudaFree, no
  * allocating library routine.
- * Limit: ceil(T*k/256) * E <= 262144 (e.g. T*k up to 262144 pairs with
+ * Limit: ceil(T / floor(256/k)) * E <= 262144, i.e. ceil(T*k/256) * E when k
+ * divides 256 (e.g. T*k up to 262144 pairs with
  * E = 256); larger shapes return MOE_ERR_WORKSPACE before any launch.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call

@@ -97,8 +97,8 @@ T* at(void* base, size_t off) {
 }
 
 size_t hist_bytes(const moe_config* c) {
-  const long long pairs = static_cast<long long>(c->T) * c->k;
-  const long long nb = (pairs + kPairsPerBlock - 1) / kPairsPerBlock;
+  const long long tpb = kPairsPerBlock / c->k;            // tokens per counting-sort chunk
+  const long long nb = (c->T + tpb - 1) / tpb;
   return static_cast<size_t>(nb) * c->E * sizeof(int32_t);
 }
 
@@ -477,11 +477,10 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
 
   // 1-2: router GEMM + top-k gating
   MOE_TRY(gemm_router(x, w->w_router, T, H, E, logits, status, st));
-  MOE_TRY(launch_topk(logits, cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr, T, E, k, cfg->score, idx,
-                      gate, st));
-  // 3-4: sync-free permutation
-  MOE_TRY(launch_permute_maps(idx, gate, T, E, k, hist_ptr(ws), counts, at<int32_t>(act, L.offsets), poff, slot_row,
-                              at<int32_t>(act, L.row_src), row_gate, status, st));
+  // 2-4: top-k gating fused with the counting-sort histograms, scan, scatter (sync-free)
+  MOE_TRY(launch_topk_permute_maps(logits, cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr, T, E, k,
+                                   cfg->score, idx, gate, hist_ptr(ws), counts, at<int32_t>(act, L.offsets), poff,
+                                   slot_row, at<int32_t>(act, L.row_src), row_gate, st));
   MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
   if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
   // 5-6: grouped expert GEMMs; the gate multiplies the SwiGLU output inside fc1

@@ -20,11 +20,17 @@ void count_launches(int n);
 // ------------------------------------------------------------ routing (route.cu)
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int score, int32_t* idx,
                         float* gate, cudaStream_t st);
-// Counting sort of T*k pairs by expert.  hist is scratch of
-// ceil(T*k/256) * E ints.
+// Counting sort of T*k pairs by expert, in chunks of (256/k)*k pairs.  hist
+// is scratch of ceil(T / (256/k)) * E ints.
 cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
                                 int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
                                 int32_t* row_src, float* row_gate, int* status, cudaStream_t st);
+// Top-k gating of the logits fused with the chunk histograms, then the same
+// scan and scatter as launch_permute_maps.
+cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int T, int E, int k, int score,
+                                     int32_t* idx, float* gate, int32_t* hist, int32_t* counts, int32_t* offsets,
+                                     int32_t* poffsets, int32_t* slot_row, int32_t* row_src, float* row_gate,
+                                     cudaStream_t st);
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
                                cudaStream_t st);
 cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,

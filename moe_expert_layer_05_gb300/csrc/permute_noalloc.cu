@@ -25,7 +25,7 @@
 namespace moe {
 namespace {
 
-// Scratch for the counting sort: ceil(T*k/256) * E histogram entries.
+// Scratch for the counting sort: ceil(T / floor(256/k)) * E histogram entries.
 constexpr long long kNoAllocScratchInts = 1LL << 18;   // 1 MiB of int32
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
@@ -63,8 +63,8 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, 
     return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!aligned16(x) || !aligned16(topk_idx) || !aligned16(slot_row))) return MOE_ERR_INVALID_ARG;
   if (topk_gate != nullptr && !aligned16(row_gate)) return MOE_ERR_INVALID_ARG;
-  const long long pairs = static_cast<long long>(cfg->T) * cfg->k;
-  const long long blocks = (pairs + kPairsPerBlock - 1) / kPairsPerBlock;
+  const long long tokens_per_chunk = kPairsPerBlock / cfg->k;
+  const long long blocks = (cfg->T + tokens_per_chunk - 1) / tokens_per_chunk;
   if (blocks * cfg->E > kNoAllocScratchInts) return MOE_ERR_WORKSPACE;   // beyond the fixed scratch
   if (!device_is_gb300()) return MOE_ERR_UNSUPPORTED;
   int32_t* hist = scratch_on_current_device();

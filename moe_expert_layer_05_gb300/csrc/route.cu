@@ -43,14 +43,10 @@ __device__ __forceinline__ Cand shfl_cand(const Cand& c, int src_mask) {
   return o;
 }
 
+// Route one token (the whole warp): lane s < k receives slot s's expert and gate.
 template <int PER_LANE>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                                                   int T, int E, int k, int score, int32_t* __restrict__ idx,
-                                                   float* __restrict__ gate) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  const float* row = logits + (long long)warp * E;
+__device__ __forceinline__ void topk_one_token(const float* __restrict__ row, const float* __restrict__ bias, int E,
+                                               int k, int score, int lane, int& out_id, float& out_gate) {
   float lg[PER_LANE], key[PER_LANE];
   uint32_t taken = 0;
   #pragma unroll
@@ -65,9 +61,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
     if (e >= E) taken |= 1u << j;
   }
-  float sel_logit = 0.f;
-  int sel_id = 0;
-  float my_logit = 0.f;  // lane i keeps slot i
+  float my_logit = 0.f;  // lane s keeps slot s
   int my_id = 0;
   for (int s = 0; s < k; ++s) {
     Cand best{0.f, 0.f, INT_MAX};
@@ -81,12 +75,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       const Cand o = shfl_cand(best, m);
       if (better(o, best)) best = o;
     }
-    sel_logit = best.logit;
-    sel_id = best.id;
-    if ((sel_id & 31) == lane) taken |= 1u << (sel_id >> 5);
-    if (lane == s) { my_logit = sel_logit; my_id = sel_id; }
+    if ((best.id & 31) == lane) taken |= 1u << (best.id >> 5);
+    if (lane == s) { my_logit = best.logit; my_id = best.id; }
   }
-  // gates of the chosen k, normalised over them (lane s holds slot s)
+  // gates of the chosen k, normalised over them
   float w;
   if (score == 0) {
     const float lmax = __shfl_sync(kFull, my_logit, 0);   // slot 0 has the largest logit
@@ -94,33 +86,41 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   } else {
     w = (lane < k) ? 1.0f / (1.0f + expf(-my_logit)) : 0.f;
   }
-  // sum in slot order (deterministic): lane 0 accumulates
-  float sum = 0.f;
+  float sum = 0.f;                                        // slot order: deterministic
   for (int s = 0; s < k; ++s) sum += __shfl_sync(kFull, w, s);
+  out_id = my_id;
+  out_gate = w / sum;
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                   int T, int E, int k, int score, int32_t* __restrict__ idx,
+                                                   float* __restrict__ gate) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  int id;
+  float g;
+  topk_one_token<PER_LANE>(logits + (long long)warp * E, bias, E, k, score, lane, id, g);
   if (lane < k) {
-    idx[(long long)warp * k + lane] = my_id;
-    gate[(long long)warp * k + lane] = w / sum;
+    idx[(long long)warp * k + lane] = id;
+    gate[(long long)warp * k + lane] = g;
   }
 }
 
 // ---------------------------------------------------------------- counting sort
-// Stable rank of each pair of this block among the block's pairs with the
-// same expert; returns the expert (-1 for none / invalid) and the rank.
-// s_cnt: [8][E] ints.  Also leaves the block's per-expert totals in s_tot.
-__device__ __forceinline__ void block_stable_rank(const int32_t* __restrict__ idx, long long npairs, int E,
-                                                  int* s_cnt, int* s_tot, int* status, int& e_out,
-                                                  int& rank_out) {
+// The T*k (token, slot) pairs, in token-major order, are cut into chunks of
+// pb = (256/k)*k pairs (whole tokens); chunk b is one block of the count and
+// scatter kernels.  Stable rank of a pair = number of earlier pairs of the
+// same chunk with the same expert (earlier tokens: a token never picks an
+// expert twice).
+__host__ __device__ constexpr int pairs_per_chunk(int k) { return (kPairsPerBlock / k) * k; }
+
+// e: expert of this thread's pair (-1: none).  s_cnt [8][E], s_tot [E] in
+// shared memory.  Returns the stable rank; leaves per-expert totals in s_tot.
+__device__ __forceinline__ int block_stable_rank(int e, int E, int* s_cnt, int* s_tot) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const long long p = (long long)blockIdx.x * kPairsPerBlock + tid;
-  int e = -1;
-  if (p < npairs) {
-    e = idx[p];
-    if (e < 0 || e >= E) {
-      set_status(status, kErrBadIndex);
-      e = -1;
-    }
-  }
   for (int i = tid; i < 8 * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
   const unsigned peers = __match_any_sync(kFull, e);
@@ -138,49 +138,107 @@ __device__ __forceinline__ void block_stable_rank(const int32_t* __restrict__ id
     s_tot[x] = run;
   }
   __syncthreads();
-  e_out = e;
-  rank_out = (e >= 0) ? s_cnt[warp * E + e] + rank_w : -1;
+  return (e >= 0) ? s_cnt[warp * E + e] + rank_w : -1;
+}
+
+__device__ __forceinline__ int load_pair_expert(const int32_t* __restrict__ idx, long long npairs, int pb, int E,
+                                                int* status) {
+  const long long p = (long long)blockIdx.x * pb + threadIdx.x;
+  int e = -1;
+  if (threadIdx.x < pb && p < npairs) {
+    e = idx[p];
+    if (e < 0 || e >= E) {
+      set_status(status, kErrBadIndex);
+      e = -1;
+    }
+  }
+  return e;
 }
 
 __global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __restrict__ idx, long long npairs,
-                                                               int E, int32_t* __restrict__ hist, int* status) {
+                                                               int pb, int E, int32_t* __restrict__ hist,
+                                                               int* status) {
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
-  int e, r;
-  block_stable_rank(idx, npairs, E, s_cnt, s_tot, status, e, r);
+  const int e = load_pair_expert(idx, npairs, pb, E, status);
+  block_stable_rank(e, E, s_cnt, s_tot);
+  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)blockIdx.x * E + x] = s_tot[x];
+}
+
+// Top-k gating fused with the chunk histogram: block b routes the tokens of
+// chunk b (one warp per token, as topk_kernel) and then counts its pairs.
+template <int PER_LANE>
+__global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* __restrict__ logits,
+                                                                   const float* __restrict__ bias, int T, int E,
+                                                                   int k, int score, int32_t* __restrict__ idx,
+                                                                   float* __restrict__ gate,
+                                                                   int32_t* __restrict__ hist) {
+  __shared__ int s_idx[kPairsPerBlock];
+  __shared__ int s_cnt[8 * kMaxE];
+  __shared__ int s_tot[kMaxE];
+  const int tpb = kPairsPerBlock / k;            // tokens of this chunk
+  const int t0 = blockIdx.x * tpb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int u = warp; u < tpb; u += 8) {
+    const int t = t0 + u;
+    if (t >= T) break;
+    int id;
+    float g;
+    topk_one_token<PER_LANE>(logits + (long long)t * E, bias, E, k, score, lane, id, g);
+    if (lane < k) {
+      idx[(long long)t * k + lane] = id;
+      gate[(long long)t * k + lane] = g;
+      s_idx[u * k + lane] = id;
+    }
+  }
+  __syncthreads();
+  const int pb = tpb * k;
+  const long long npairs = (long long)T * k;
+  const long long p = (long long)blockIdx.x * pb + threadIdx.x;
+  const int e = (threadIdx.x < pb && p < npairs) ? s_idx[threadIdx.x] : -1;
+  block_stable_rank(e, E, s_cnt, s_tot);
   for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)blockIdx.x * E + x] = s_tot[x];
 }
 
 // One block.  hist [NB][E] -> counts, offsets, poffsets, and in place
 // base[b][e] = poffsets[e] + sum_{b'<b} hist[b'][e].  Also marks padding rows.
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int NB, int E,
+// Thread (e, g): expert e, group g of G lanes (G a power of two <= 32, G*E <=
+// 1024) owning a contiguous range of chunks; sums and prefixes across the G
+// lanes of one expert are warp shuffles.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int NB, int E, int G,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ poffsets, int32_t* __restrict__ row_src,
                                                     float* __restrict__ row_gate) {
-  __shared__ int s_part[1024];
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_poff[kMaxE + 1];
   const int tid = threadIdx.x;
-  const int G = blockDim.x / E;                 // groups of E threads, each over a range of blocks
-  const int g = tid / E, e = tid % E;
-  const bool active = g < G;
+  const int e = tid / G, g = tid % G;
+  const bool active = e < E;
   const int per = (NB + G - 1) / G;
-  const int b0 = g * per, b1 = min(NB, b0 + per);
+  const int b0 = min(NB, g * per), b1 = min(NB, b0 + per);
   int sum = 0;
   if (active) {
-    for (int b = b0; b < b1; ++b) sum += hist[(long long)b * E + e];
-    s_part[tid] = sum;
+    int b = b0;
+    for (; b + 4 <= b1; b += 4) {
+      const int v0 = hist[(long long)b * E + e], v1 = hist[(long long)(b + 1) * E + e];
+      const int v2 = hist[(long long)(b + 2) * E + e], v3 = hist[(long long)(b + 3) * E + e];
+      sum += v0 + v1 + v2 + v3;
+    }
+    for (; b < b1; ++b) sum += hist[(long long)b * E + e];
   }
-  __syncthreads();
-  if (tid < E) {
-    int c = 0;
-    for (int q = 0; q < G; ++q) c += s_part[q * E + tid];
-    s_cnt[tid] = c;
-    counts[tid] = c;
+  // inclusive prefix over the G lanes of this expert (lanes g of a group are consecutive)
+  int inc = sum;
+  for (int d = 1; d < G; d <<= 1) {
+    const int v = __shfl_up_sync(kFull, inc, d);
+    if (g >= d) inc += v;
+  }
+  const int total = __shfl_sync(kFull, inc, (tid & 31) | (G - 1));   // last lane of the group
+  if (active && g == 0) {
+    s_cnt[e] = total;
+    counts[e] = total;
   }
   __syncthreads();
   if (tid < 32) {
-    // scan over experts: lane handles a contiguous run of experts
     const int per_lane = (E + 31) / 32;
     const int e0 = tid * per_lane, e1 = min(E, e0 + per_lane);
     int cs = 0, ps = 0;
@@ -203,8 +261,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
   }
   __syncthreads();
   if (active) {
-    int run = s_poff[e];
-    for (int q = 0; q < g; ++q) run += s_part[q * E + e];
+    int run = s_poff[e] + inc - sum;
     for (int b = b0; b < b1; ++b) {
       const long long i = (long long)b * E + e;
       const int c = hist[i];
@@ -225,16 +282,17 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
 
 __global__ void __launch_bounds__(kPairsPerBlock) scatter_kernel(const int32_t* __restrict__ idx,
                                                                  const float* __restrict__ gate, long long npairs,
-                                                                 int E, int k, const int32_t* __restrict__ base,
+                                                                 int pb, int E, int k,
+                                                                 const int32_t* __restrict__ base,
                                                                  int32_t* __restrict__ slot_row,
                                                                  int32_t* __restrict__ row_src,
                                                                  float* __restrict__ row_gate) {
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
-  int e, r;
-  block_stable_rank(idx, npairs, E, s_cnt, s_tot, nullptr, e, r);
-  const long long p = (long long)blockIdx.x * kPairsPerBlock + threadIdx.x;
-  if (p >= npairs) return;
+  const int e = load_pair_expert(idx, npairs, pb, E, nullptr);
+  const int r = block_stable_rank(e, E, s_cnt, s_tot);
+  const long long p = (long long)blockIdx.x * pb + threadIdx.x;
+  if (threadIdx.x >= pb || p >= npairs) return;
   if (e < 0) {
     slot_row[p] = -1;
     return;
@@ -246,7 +304,8 @@ __global__ void __launch_bounds__(kPairsPerBlock) scatter_kernel(const int32_t* 
 }
 
 // ---------------------------------------------------------------- row copies
-// One block per token: read x[t] once, write it to its k rows.
+// One block per token: read x[t] once, write it to its k rows.  Each thread
+// keeps up to 4 16-byte loads in flight before storing.
 __global__ void __launch_bounds__(128) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ slot_row,
                                                      int k, int vec_per_row, uint4* __restrict__ x_perm) {
   const int t = blockIdx.x;
@@ -254,11 +313,22 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4* __restrict__ x
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
   __syncthreads();
   const uint4* src = x + (long long)t * vec_per_row;
-  for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
-    const uint4 val = __ldg(src + v);
+  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += 4 * blockDim.x) {
+    uint4 val[4];
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * blockDim.x;
+      if (v < vec_per_row) val[u] = __ldg(src + v);
+    }
     for (int i = 0; i < k; ++i) {
       const int r = s_rows[i];
-      if (r >= 0) x_perm[(long long)r * vec_per_row + v] = val;
+      if (r < 0) continue;
+      uint4* dst = x_perm + (long long)r * vec_per_row;
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < vec_per_row) dst[v] = val[u];
+      }
     }
   }
 }
@@ -285,6 +355,7 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
 }
 
 // y[t] = sum_i o[slot_row[t,i]] (+ shared[t]), fp32 in slot order, one rounding.
+// Each thread handles 2 vectors per pass with all k row loads issued first.
 __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ o, const int32_t* __restrict__ slot_row,
                                                       const uint4* __restrict__ shared, int k, int vec_per_row,
                                                       uint4* __restrict__ y) {
@@ -292,14 +363,31 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
   __shared__ int s_rows[kMaxK];
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
   __syncthreads();
-  for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int i = 0; i < k; ++i) {
-      const int r = s_rows[i];
-      if (r >= 0) add_bf16x8(acc, __ldg(o + (long long)r * vec_per_row + v));
+  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += 2 * blockDim.x) {
+    const int v1 = v0 + blockDim.x;
+    const bool has1 = v1 < vec_per_row;
+    float a0[8] = {0, 0, 0, 0, 0, 0, 0, 0}, a1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int i = 0;
+    for (; i + 2 <= k; i += 2) {
+      const int r0 = s_rows[i], r1 = s_rows[i + 1];
+      uint4 p0 = make_uint4(0, 0, 0, 0), p1 = p0, q0 = p0, q1 = p0;
+      if (r0 >= 0) { p0 = __ldg(o + (long long)r0 * vec_per_row + v0); if (has1) p1 = __ldg(o + (long long)r0 * vec_per_row + v1); }
+      if (r1 >= 0) { q0 = __ldg(o + (long long)r1 * vec_per_row + v0); if (has1) q1 = __ldg(o + (long long)r1 * vec_per_row + v1); }
+      add_bf16x8(a0, p0); add_bf16x8(a1, p1);
+      add_bf16x8(a0, q0); add_bf16x8(a1, q1);
     }
-    if (shared != nullptr) add_bf16x8(acc, __ldg(shared + (long long)t * vec_per_row + v));
-    y[(long long)t * vec_per_row + v] = pack8(acc);
+    for (; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r < 0) continue;
+      add_bf16x8(a0, __ldg(o + (long long)r * vec_per_row + v0));
+      if (has1) add_bf16x8(a1, __ldg(o + (long long)r * vec_per_row + v1));
+    }
+    if (shared != nullptr) {
+      add_bf16x8(a0, __ldg(shared + (long long)t * vec_per_row + v0));
+      if (has1) add_bf16x8(a1, __ldg(shared + (long long)t * vec_per_row + v1));
+    }
+    y[(long long)t * vec_per_row + v0] = pack8(a0);
+    if (has1) y[(long long)t * vec_per_row + v1] = pack8(a1);
   }
 }
 
@@ -434,18 +522,54 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
   return cudaGetLastError();
 }
 
+namespace {
+int chunks_of(int T, int k) { return (T + kPairsPerBlock / k - 1) / (kPairsPerBlock / k); }
+
+int scan_groups(int E) {
+  int G = 32;
+  while (G > 1 && G * E > 1024) G >>= 1;
+  return G;
+}
+
+cudaError_t launch_scan_scatter(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
+                                int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
+                                int32_t* row_src, float* row_gate, cudaStream_t st) {
+  const long long npairs = (long long)T * k;
+  const int NB = chunks_of(T, k);
+  scan_kernel<<<1, 1024, 0, st>>>(hist, NB, E, scan_groups(E), counts, offsets, poffsets, row_src, row_gate);
+  if (NB > 0)
+    scatter_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, gate, npairs, pairs_per_chunk(k), E, k, hist, slot_row,
+                                                  row_src, gate != nullptr ? row_gate : nullptr);
+  count_launches(NB > 0 ? 2 : 1);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
                                 int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
                                 int32_t* row_src, float* row_gate, int* status, cudaStream_t st) {
   const long long npairs = (long long)T * k;
-  const int NB = static_cast<int>((npairs + kPairsPerBlock - 1) / kPairsPerBlock);
-  if (NB > 0) count_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, E, hist, status);
-  scan_kernel<<<1, 1024, 0, st>>>(hist, NB, E, counts, offsets, poffsets, row_src, row_gate);
-  if (NB > 0)
-    scatter_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, gate, npairs, E, k, hist, slot_row, row_src,
-                                                  gate != nullptr ? row_gate : nullptr);
-  count_launches(NB > 0 ? 3 : 1);
-  return cudaGetLastError();
+  const int NB = chunks_of(T, k);
+  if (NB > 0) {
+    count_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, status);
+    count_launches(1);
+  }
+  return launch_scan_scatter(idx, gate, T, E, k, hist, counts, offsets, poffsets, slot_row, row_src, row_gate, st);
+}
+
+cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int T, int E, int k, int score,
+                                     int32_t* idx, float* gate, int32_t* hist, int32_t* counts, int32_t* offsets,
+                                     int32_t* poffsets, int32_t* slot_row, int32_t* row_src, float* row_gate,
+                                     cudaStream_t st) {
+  const int NB = chunks_of(T, k);
+  if (NB > 0) {
+    if (E <= 32) topk_hist_kernel<1><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    else if (E <= 64) topk_hist_kernel<2><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    else if (E <= 128) topk_hist_kernel<4><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    else topk_hist_kernel<8><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    count_launches(1);
+  }
+  return launch_scan_scatter(idx, gate, T, E, k, hist, counts, offsets, poffsets, slot_row, row_src, row_gate, st);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,

@@ -579,8 +579,23 @@ def _q_tokens(a, quant):
     return quant(_pad_rows(a), 0)[:r]
 
 
+def _weight_quantiser(quant, cache):
+    """quant for weights, memoised in ``cache`` (a dict) by (tensor, expert, axis):
+    the recipe quantises each weight once, so repeated calls may reuse it."""
+    if cache is None:
+        return lambda name, e, W, axis: quant(W, axis)
+
+    def qw(name, e, W, axis):
+        key = (name, e, axis)
+        if key not in cache:
+            cache[key] = quant(W, axis)
+        return cache[key]
+    return qw
+
+
 def moe_forward_mx(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=None, w2_shared=None,
-                   routing=None, quant=mxfp8_roundtrip):
+                   routing=None, quant=mxfp8_roundtrip, weight_cache=None):
+    qw = _weight_quantiser(quant, weight_cache)
     x = np.asarray(x, np.float64)
     T = x.shape[0]
     E = _shape(w1)[0]
@@ -599,23 +614,24 @@ def moe_forward_mx(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=N
             continue
         W1 = np.asarray(w1[e], np.float64)
         W2 = np.asarray(w2[e], np.float64)
-        z = quant(x[tok], -1) @ quant(W1, -1).T
+        z = quant(x[tok], -1) @ qw("w1", e, W1, -1).T
         hp = gate[tok, slot][:, None] * silu(z[:, :F]) * z[:, F:]
-        np.add.at(y, tok, quant(hp, -1) @ quant(W2, -1).T)
+        np.add.at(y, tok, quant(hp, -1) @ qw("w2", e, W2, -1).T)
     if w1_shared is not None:
         W1 = np.asarray(w1_shared, np.float64)
         W2 = np.asarray(w2_shared, np.float64)
         S = W1.shape[0] // 2
-        z = quant(x, -1) @ quant(W1, -1).T
-        y += quant(silu(z[:, :S]) * z[:, S:], -1) @ quant(W2, -1).T
+        z = quant(x, -1) @ qw("w1s", 0, W1, -1).T
+        y += quant(silu(z[:, :S]) * z[:, S:], -1) @ qw("w2s", 0, W2, -1).T
     return {"y": y, "logits": logits, "topk_idx": idx.astype(np.int32), "gates": gate}
 
 
 def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None, w2_shared=None,
-                    quant=mxfp8_roundtrip):
+                    quant=mxfp8_roundtrip, weight_cache=None):
     """Gradients as the MXFP8 recipe computes them: the chain rule of the
     unquantised layer, with every expert-GEMM operand quantised along its
     contraction axis (straight through the quantiser)."""
+    qw = _weight_quantiser(quant, weight_cache)
     x = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
     T, H = x.shape
@@ -635,16 +651,16 @@ def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None,
         W1 = np.asarray(w1[e], np.float64)
         W2 = np.asarray(w2[e], np.float64)
         xe = x[tok]
-        z = quant(xe, -1) @ quant(W1, -1).T
+        z = quant(xe, -1) @ qw("w1", e, W1, -1).T
         a, b = z[:, :F], z[:, F:]
         h = silu(a) * b
         g = gate[tok, slot][:, None]
         dye = dy[tok]
-        dhp = quant(dye, -1) @ quant(W2, 0)             # contraction over H
+        dhp = quant(dye, -1) @ qw("w2", e, W2, 0)           # contraction over H
         dgate[tok, slot] = (dhp * h).sum(axis=1)
         dh = g * dhp
         dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
-        np.add.at(dx, tok, quant(dz, -1) @ quant(W1, 0))  # contraction over 2F
+        np.add.at(dx, tok, quant(dz, -1) @ qw("w1", e, W1, 0))  # contraction over 2F
         dW1[e] = _q_tokens(dz, quant).T @ _q_tokens(xe, quant)
         dW2[e] = _q_tokens(dye, quant).T @ _q_tokens(g * h, quant)
     out = {"dW1": dW1, "dW2": dW2, "dgate": dgate}
@@ -652,12 +668,12 @@ def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None,
         W1 = np.asarray(w1_shared, np.float64)
         W2 = np.asarray(w2_shared, np.float64)
         S = W1.shape[0] // 2
-        z = quant(x, -1) @ quant(W1, -1).T
+        z = quant(x, -1) @ qw("w1s", 0, W1, -1).T
         a, b = z[:, :S], z[:, S:]
         h = silu(a) * b
-        dh = quant(dy, -1) @ quant(W2, 0)
+        dh = quant(dy, -1) @ qw("w2s", 0, W2, 0)
         dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
-        dx += quant(dz, -1) @ quant(W1, 0)
+        dx += quant(dz, -1) @ qw("w1s", 0, W1, 0)
         out["dW1_shared"] = _q_tokens(dz, quant).T @ _q_tokens(x, quant)
         out["dW2_shared"] = _q_tokens(dy, quant).T @ _q_tokens(h, quant)
     logits = fwd["logits"] if fwd.get("logits") is not None else router_logits(x, w_router)

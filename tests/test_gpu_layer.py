@@ -30,6 +30,7 @@ SMALL = {
     "dsv3_small": Workload("dsv3_small", T=384, H=256, E=256, k=8, F=128, S=256, score="sigmoid",
                            zipf_s=1.2, backward=True),
     "one_token": Workload("one_token", T=1, H=128, E=8, k=2, F=128, S=128, backward=True),
+    "odd_k": Workload("odd_k", T=200, H=128, E=16, k=3, F=128, backward=True),
 }
 
 

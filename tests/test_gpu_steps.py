@@ -100,6 +100,8 @@ PERM_CASES = [
     (517, 256, 8, 2.0, 256),    # many empty experts, a few hot
     (2000, 8, 1, 4.0, 128),     # one expert takes almost everything
     (0, 8, 2, 0.0, 128),
+    (500, 16, 3, 0.5, 128),     # k does not divide the 256-pair chunk
+    (300, 32, 6, 1.0, 128),
 ]
 
 

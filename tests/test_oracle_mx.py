@@ -63,3 +63,18 @@ def test_quantised_operands_are_representable():
     fwd = O.moe_forward_mx(x, wr, w1, w2, k=2, quant=spy)
     O.moe_backward_mx(x, wr, w1, w2, fwd, dy, quant=spy)
     assert set(calls) == {-1, 0}
+
+
+def test_weight_cache_changes_nothing():
+    x, wr, w1, w2, w1s, w2s, dy = _case(4, S=64)
+    kw = dict(w1_shared=w1s, w2_shared=w2s)
+    cache = {}
+    a = O.moe_forward_mx(x, wr, w1, w2, k=2, **kw)
+    b = O.moe_forward_mx(x, wr, w1, w2, k=2, weight_cache=cache, **kw)
+    c = O.moe_forward_mx(x, wr, w1, w2, k=2, weight_cache=cache, **kw)     # served from the cache
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["y"], c["y"])
+    ga = O.moe_backward_mx(x, wr, w1, w2, a, dy, **kw)
+    gb = O.moe_backward_mx(x, wr, w1, w2, a, dy, weight_cache=cache, **kw)
+    for n in ("dx", "dW1", "dW2", "dW1_shared", "dW2_shared"):
+        np.testing.assert_array_equal(ga[n], gb[n])

@@ -58,7 +58,7 @@ def test_noalloc_permute_matches_workspace_permute(first, second):
 
 
 def test_noalloc_permute_rejects_shapes_beyond_its_scratch():
-    # ceil(T*k/256) * E = 1025 * 256 > 262144: refused before any launch
+    # ceil(T / (256/k)) * E = 1025 * 256 > 262144: refused before any launch
     cfg = api.make_config(1025 * 32, 128, 256, 8, 128)
     with pytest.raises(api.MoeError) as ei:
         api.moe_permute_noalloc(cfg, 16, 16, None, 16, 16, 16, 16, 16, None, 16, 0)
