@@ -80,9 +80,14 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = MX ? 512 : 0;
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  // Outputs leave through TMA stores staged in shared memory (every epilogue
+  // but the router's narrow fp32 logits, whose rows need not be 16-byte sized).
+  static constexpr bool TMA_OUT = !(EP == Epi::kStoreF32 && S == Sched::kDenseM);
+  // two 4 KB staging buffers (32 rows x 128 B, 128B-swizzled) per epilogue warp
+  static constexpr int STAGING_BYTES = TMA_OUT ? 4 * 2 * 4096 : 0;
   static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
   static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of one stage's scales
   static constexpr int TMEM_COLS_RAW = 2 * BN + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
@@ -99,6 +104,7 @@ struct GemmCfg {
   static_assert(EP != Epi::kSwiglu || BN == (MX ? 128 : 256), "SwiGLU tile: matching gate and up halves");
   static_assert(!MX || (BN % 128 == 0 && !A_MN && !B_MN), "MXFP8 operands are K-major, 128-row scale tiles");
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
+  static_assert(SMEM_BYTES + 2048 <= 232448, "dynamic + static shared memory per CTA");
   static_assert(STAGES >= 2, "pipeline depth");
 };
 
@@ -382,9 +388,197 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
   }
 }
 
+// Per-warp staging of output chunks for TMA stores: two 4 KB buffers, each
+// 32 rows (one per lane) x 128 bytes in the 128-byte swizzled order (16-byte
+// chunk c of row r sits at chunk c ^ (r % 8)), so a warp's 16-byte stores hit
+// distinct banks.  Lane 0 issues the stores and owns the bulk groups.
+struct Stager {
+  uint8_t* buf;
+  int cur;
+  int lane;
+
+  __device__ __forceinline__ void begin() {   // the buffer about to be filled is no longer read by TMA
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+  }
+  __device__ __forceinline__ void put(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
+    const uint32_t base = smem_u32(buf + cur * 4096);
+    st_shared_v4(base + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, cc, d);
+  }
+  __device__ __forceinline__ void flush(const CUtensorMap* map, int x, int y) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, buf + cur * 4096, x, y);
+      bulk_commit_group();
+    }
+    cur ^= 1;
+  }
+  __device__ __forceinline__ void drain() {
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ void load32(uint32_t taddr, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  tmem_ld_x16(taddr, a);
+  tmem_ld_x16(taddr + 16, b);
+  tmem_ld_wait(a);
+  tmem_ld_wait(b);
+}
+
+// Epilogue with TMA stores.  Rows of the tile: warp quarter q owns rows
+// 32q..32q+31, lane = row.  Dense tiles past the last row are clipped by TMA.
+template <class C>
+__device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
+                                                  int quarter, int lane, Stager& st, const CUtensorMap* tmC,
+                                                  const CUtensorMap* tmC2) {
+  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t t0 = tmem_acc + lane_addr;
+  const bool no_mma = (ti.num_kb == 0);         // empty group (weight gradients): result is zero
+
+  if constexpr (C::EP == Epi::kStoreF32) {      // weight gradients: [group*M + row, col] fp32
+    const int y = ti.group * p.m_rows + ti.m0 + quarter * 32;
+    #pragma unroll 1
+    for (int c0 = 0; c0 < C::BN; c0 += 32) {
+      uint32_t a[16], b[16];
+      load32(t0 + c0, a, b);
+      st.begin();
+      #pragma unroll
+      for (int j = 0; j < 4; ++j) st.put(j, no_mma ? 0u : a[4 * j], no_mma ? 0u : a[4 * j + 1],
+                                        no_mma ? 0u : a[4 * j + 2], no_mma ? 0u : a[4 * j + 3]);
+      #pragma unroll
+      for (int j = 0; j < 4; ++j) st.put(4 + j, no_mma ? 0u : b[4 * j], no_mma ? 0u : b[4 * j + 1],
+                                        no_mma ? 0u : b[4 * j + 2], no_mma ? 0u : b[4 * j + 3]);
+      st.flush(tmC, ti.n * C::BN + c0, y);
+    }
+  } else if constexpr (C::EP == Epi::kStoreBf16) {
+    const int y = ti.m0 + quarter * 32;
+    #pragma unroll 1
+    for (int c0 = 0; c0 < C::BN; c0 += 64) {
+      st.begin();
+      #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[16], b[16];
+        load32(t0 + c0 + 32 * h, a, b);
+        uint32_t w[16];
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) w[8 + j] = pack_bf16x2(__uint_as_float(b[2 * j]), __uint_as_float(b[2 * j + 1]));
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) st.put(4 * h + j, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      }
+      st.flush(tmC, ti.n * C::BN + c0, y);
+    }
+  } else if constexpr (C::EP == Epi::kSwiglu) {
+    // accumulator columns [0, BN/2) = gate rows of W1, [BN/2, BN) = the matching up rows
+    const int row = ti.m0 + quarter * 32 + lane;
+    const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
+    const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
+    const int col0 = ti.n * (C::BN / 2);
+    const int y = ti.m0 + quarter * 32;
+    #pragma unroll 1
+    for (int c0 = 0; c0 < C::BN / 2; c0 += 64) {
+      st.begin();
+      #pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t a[16], b[16];
+        tmem_ld_x16(t0 + c0 + 16 * q, a);
+        tmem_ld_x16(t0 + C::BN / 2 + c0 + 16 * q, b);
+        tmem_ld_wait(a);
+        tmem_ld_wait(b);
+        uint32_t hw[8];
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
+          const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
+          hw[j] = pack_bf16x2(g * (a0 / (1.0f + expf(-a0))) * b0, g * (a1 / (1.0f + expf(-a1))) * b1);
+        }
+        st.put(2 * q, hw[0], hw[1], hw[2], hw[3]);
+        st.put(2 * q + 1, hw[4], hw[5], hw[6], hw[7]);
+      }
+      st.flush(tmC, col0 + c0, y);
+      if (p.c2 != nullptr) {                    // z, saved for backward: gate chunk then up chunk
+        #pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          st.begin();
+          #pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t a[16], b[16];
+            load32(t0 + half * (C::BN / 2) + c0 + 32 * h2, a, b);
+            uint32_t w[16];
+            #pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+            #pragma unroll
+            for (int j = 0; j < 8; ++j)
+              w[8 + j] = pack_bf16x2(__uint_as_float(b[2 * j]), __uint_as_float(b[2 * j + 1]));
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) st.put(4 * h2 + j, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
+          st.flush(tmC2, half * p.half_cols + col0 + c0, y);
+        }
+      }
+    }
+  } else {  // kSwigluBwd: dz gate half, then dz up half, per 64-column chunk
+    const int row = ti.m0 + quarter * 32 + lane;
+    const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
+    const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
+    const int col0 = ti.n * C::BN;
+    const __nv_bfloat16* zrow = p.aux + (long long)(row_ok ? row : 0) * p.ld_aux + col0;
+    const int y = ti.m0 + quarter * 32;
+    float dg = 0.f;
+    #pragma unroll 1
+    for (int c0 = 0; c0 < C::BN; c0 += 64) {
+      #pragma unroll 1
+      for (int half = 0; half < 2; ++half) {   // 0: d(gate input), 1: d(up input)
+        st.begin();
+        #pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          const int c = c0 + 16 * q;
+          const uint4* pa = reinterpret_cast<const uint4*>(zrow + c);
+          const uint4* pb = reinterpret_cast<const uint4*>(zrow + p.half_cols + c);
+          const uint4 za0 = pa[0], za1 = pa[1], zb0 = pb[0], zb1 = pb[1];
+          uint32_t v[16];
+          tmem_ld_x16(t0 + c, v);
+          tmem_ld_wait(v);
+          const uint32_t zaw[8] = {za0.x, za0.y, za0.z, za0.w, za1.x, za1.y, za1.z, za1.w};
+          const uint32_t zbw[8] = {zb0.x, zb0.y, zb0.z, zb0.w, zb1.x, zb1.y, zb1.z, zb1.w};
+          uint32_t out[8];
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float o2[2];
+            #pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float av = u ? bf16_hi(zaw[j]) : bf16_lo(zaw[j]);
+              const float bv = u ? bf16_hi(zbw[j]) : bf16_lo(zbw[j]);
+              const float dh = no_mma ? 0.f : __uint_as_float(v[2 * j + u]);
+              const float sg = 1.0f / (1.0f + expf(-av));
+              const float si = av * sg;
+              const float dhg = g * dh;
+              if (half == 0) {
+                dg += dh * si * bv;
+                o2[u] = dhg * bv * sg * (1.0f + av * (1.0f - sg));
+              } else {
+                o2[u] = dhg * si;
+              }
+            }
+            out[j] = pack_bf16x2(o2[0], o2[1]);
+          }
+          st.put(2 * q, out[0], out[1], out[2], out[3]);
+          st.put(2 * q + 1, out[4], out[5], out[6], out[7]);
+        }
+        st.flush(tmC, half * p.half_cols + col0 + c0, y);
+      }
+    }
+    if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * p.n_tiles + ti.n] = dg;
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                         const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
@@ -400,6 +594,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* a_smem = smem;
   uint8_t* b_smem = smem + C::STAGES * C::A_BYTES;
   uint8_t* sf_smem = b_smem + C::STAGES * C::B_BYTES;   // MXFP8 scale tiles (STAGES x (SFA + SFB))
+  uint8_t* stage_smem = sf_smem + C::STAGES * (C::SFA_BYTES + C::SFB_BYTES);   // epilogue staging (1 KB aligned)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -535,16 +730,22 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    Stager st{stage_smem + (warp - 2) * 8192, 0, lane};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = decode_tile<C>(p, s_poff, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
       tc_fence_after_sync();
-      epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
+      if constexpr (C::TMA_OUT) {
+        epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::BN, quarter, lane, st, &tmC, &tmC2);
+      } else {
+        epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if constexpr (C::TMA_OUT) st.drain();     // every TMA store has finished before the CTA exits
   }
 
   __syncwarp();

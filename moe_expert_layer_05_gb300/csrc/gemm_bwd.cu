@@ -33,14 +33,16 @@ cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const voi
   p.dgate_part = dgate_part;
   p.rows_cap = rows_alloc;
   p.status = status;
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
     using C = GemmCfg<128, false, true, Sched::kRoutedM, Epi::kSwigluBwd>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
-    return launch_gemm<C>(ta, tb, p, upper < num_sms() ? upper : num_sms(), st);
+    return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
   }
   using C = GemmCfg<128, false, true, Sched::kDenseM, Epi::kSwigluBwd>;
   const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
-  return launch_gemm<C>(ta, tb, p, tiles < num_sms() ? tiles : num_sms(), st);
+  return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 
 namespace {
@@ -63,14 +65,16 @@ cudaError_t dgrad_fc1_bn(const void* dz, int rows_alloc, int F, const void* w1, 
   p.ldc = H;
   p.rows_cap = rows_alloc;
   p.status = status;
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, dx_perm, H, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
     using C = GemmCfg<BN, false, true, Sched::kRoutedM, Epi::kStoreBf16>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
-    return launch_gemm<C>(ta, tb, p, upper < num_sms() ? upper : num_sms(), st);
+    return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
   }
   using C = GemmCfg<BN, false, true, Sched::kDenseM, Epi::kStoreBf16>;
   const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
-  return launch_gemm<C>(ta, tb, p, tiles < num_sms() ? tiles : num_sms(), st);
+  return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 
 template <int BN>
@@ -92,9 +96,11 @@ cudaError_t wgrad_bn(const void* a, int M, const void* b, int N, int rows_alloc,
   p.c_group_stride = static_cast<long long>(M) * N;
   p.rows_cap = rows_alloc;
   p.status = status;
+  CUtensorMap tc;
+  if (!make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M)) return cudaErrorInvalidValue;
   using C = GemmCfg<BN, true, true, Sched::kRoutedK, Epi::kStoreF32>;
   const int tiles = p.E * p.m_tiles_w * p.n_tiles;
-  return launch_gemm<C>(ta, tb, p, tiles < num_sms() ? tiles : num_sms(), st);
+  return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 }  // namespace
 

@@ -23,8 +23,8 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, u
 }
 
 template <class C>
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
-                        cudaStream_t st) {
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
+                        const GemmParams& p, int grid, cudaStream_t st) {
   static bool attr_set = false;
   auto kern = grouped_gemm_kernel<C>;
   if (!attr_set) {
@@ -33,9 +33,17 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
     attr_set = true;
   }
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, tc, tc2, p);
   count_launches(1);
   return cudaGetLastError();
+}
+
+// Output map for the TMA-store epilogue: boxes of 128 bytes x 32 rows, 128B swizzle.
+inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 64, 32);
+}
+inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32);
 }
 
 inline GemmParams gemm_params_zero() {

@@ -65,7 +65,7 @@ cudaError_t router_bn(const void* x, const void* wr, int T, int H, int E, float*
   p.rows_cap = T;
   p.status = status;
   const int tiles = (T + 127) / 128;
-  return launch_gemm<C>(ta, tb, p, tiles < num_sms() ? tiles : num_sms(), st);
+  return launch_gemm<C>(ta, tb, ta, ta, p, tiles < num_sms() ? tiles : num_sms(), st);   // plain stores
 }
 
 }  // namespace
@@ -102,14 +102,18 @@ cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E
   p.row_gate = row_gate;
   p.rows_cap = rows_alloc;
   p.status = status;
+  CUtensorMap tc, tz;
+  if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
+    return cudaErrorInvalidValue;
+  if (z == nullptr) tz = tc;
   if (poffsets != nullptr) {
     using C = GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwiglu>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
-    return launch_gemm<C>(ta, tb, p, upper < num_sms() ? upper : num_sms(), st);
+    return launch_gemm<C>(ta, tb, tc, tz, p, upper < num_sms() ? upper : num_sms(), st);
   }
   using C = GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwiglu>;
   const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
-  return launch_gemm<C>(ta, tb, p, tiles < num_sms() ? tiles : num_sms(), st);
+  return launch_gemm<C>(ta, tb, tc, tz, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 
 namespace {
@@ -131,14 +135,16 @@ cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, 
   p.ldc = H;
   p.rows_cap = rows_alloc;
   p.status = status;
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, o, H, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
     using C = GemmCfg<BN, false, false, Sched::kRoutedM, Epi::kStoreBf16>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
-    return launch_gemm<C>(ta, tb, p, upper < num_sms() ? upper : num_sms(), st);
+    return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
   }
   using C = GemmCfg<BN, false, false, Sched::kDenseM, Epi::kStoreBf16>;
   const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
-  return launch_gemm<C>(ta, tb, p, tiles < num_sms() ? tiles : num_sms(), st);
+  return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 }  // namespace
 

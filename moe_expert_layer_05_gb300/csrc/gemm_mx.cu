@@ -21,8 +21,8 @@ inline bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uin
 }
 
 template <class C>
-cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int rows_alloc,
-                      int dense_rows, cudaStream_t st) {
+cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
+                      const GemmParams& p, int rows_alloc, int dense_rows, cudaStream_t st) {
   int grid;
   if constexpr (C::S == Sched::kRoutedK) {
     grid = p.E * p.m_tiles_w * p.n_tiles;
@@ -31,7 +31,7 @@ cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPa
   } else {
     grid = ((dense_rows + 127) / 128) * p.n_tiles;
   }
-  return launch_gemm<C>(ta, tb, p, grid < num_sms() ? grid : num_sms(), st);
+  return launch_gemm<C>(ta, tb, tc, tc2, p, grid < num_sms() ? grid : num_sms(), st);
 }
 }  // namespace
 
@@ -61,11 +61,15 @@ cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, 
   p.sfb = static_cast<const uint8_t*>(w1sf);
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
+  CUtensorMap tc, tz;
+  if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
+    return cudaErrorInvalidValue;
+  if (z == nullptr) tz = tc;
   if (poffsets != nullptr)
-    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwiglu, true>>(ta, tb, p, rows_alloc,
+    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwiglu, true>>(ta, tb, tc, tz, p, rows_alloc,
                                                                                       dense_rows, st);
-  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwiglu, true>>(ta, tb, p, rows_alloc, dense_rows,
-                                                                                   st);
+  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwiglu, true>>(ta, tb, tc, tz, p, rows_alloc,
+                                                                                   dense_rows, st);
 }
 
 // c [rows, N] bf16 = A [rows, K] x B_e [N, K]^T, both E4M3 with scales.
@@ -90,10 +94,12 @@ cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int
   p.sfb = static_cast<const uint8_t*>(bsf);
   p.sfa_tiles_k = K / 128;
   p.sfb_tiles_k = K / 128;
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, c, N, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr)
-    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kStoreBf16, true>>(ta, tb, p, rows_alloc,
+    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
                                                                                          dense_rows, st);
-  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kStoreBf16, true>>(ta, tb, p, rows_alloc,
+  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
                                                                                       dense_rows, st);
 }
 
@@ -124,10 +130,12 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
   p.sfb = static_cast<const uint8_t*>(w2tsf);
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr)
-    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, p, rows_alloc,
+    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p, rows_alloc,
                                                                                          dense_rows, st);
-  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwigluBwd, true>>(ta, tb, p, rows_alloc,
+  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p, rows_alloc,
                                                                                       dense_rows, st);
 }
 
@@ -154,7 +162,9 @@ cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* 
   p.sfb = static_cast<const uint8_t*>(btsf);
   p.sfa_tiles_k = rows_alloc / 128;
   p.sfb_tiles_k = rows_alloc / 128;
-  return launch_mx<GemmCfg<128, false, false, Sched::kRoutedK, Epi::kStoreF32, true>>(ta, tb, p, rows_alloc,
+  CUtensorMap tc;
+  if (!make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M)) return cudaErrorInvalidValue;
+  return launch_mx<GemmCfg<128, false, false, Sched::kRoutedK, Epi::kStoreF32, true>>(ta, tb, tc, tc, p, rows_alloc,
                                                                                       dense_rows, st);
 }
 
