@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FLUSH_BYTES = 512 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one fc1 launch, from the ncu
 # capture summarised in profiles/ (None until captured for the current kernel).
-FC1_TRAFFIC_BYTES = None
+FC1_TRAFFIC_BYTES = 2.193e9   # profiles/fc1_grouped_gemm_mixtral_full.md (bf16 Mixtral-like fc1)
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -411,7 +411,8 @@ def run_ours(args) -> dict | None:
                                ", fused gated SwiGLU)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": peak_note,
-                     "traffic": FC1_TRAFFIC_BYTES, "flop_per_launch": fc1_flop, "ms_per_launch": fc1_ms},
+                     "traffic": (FC1_TRAFFIC_BYTES if (w.name == "mixtral" and not mx) else None),
+                     "flop_per_launch": fc1_flop, "ms_per_launch": fc1_ms},
         "stages_ms": stages,
         "e2e": {"value": aggregate(w.T, K, world, e2e_total), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
