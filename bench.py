@@ -255,6 +255,8 @@ def run_ours(args) -> dict | None:
     w = WORKLOADS[args.workload]
     if args.tokens is not None:
         w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
+    if args.experts is not None:
+        w = dataclasses.replace(w, E=args.experts, name=f"{w.name}_E{args.experts}")
     dinp = make_inputs_on_device(w, dev, seed=rank)
     cfg = api.config_of(w)
     layer = api.MoELayer(cfg, dinp, with_backward=w.backward, device=dev)
@@ -509,6 +511,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each timed step eagerly, not as a CUDA graph")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (smaller cases for profiler captures; not a bench line)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -294,12 +294,13 @@ typedef enum {
   MOE_MX_COLS_T = 1,        /* src batch x [rows, cols] -> codes batch x [cols, rows], blocks along rows
                                (each matrix transposed; scale tiles per matrix) */
   MOE_MX_ROWS_GATE_UP = 2   /* as ROWS, rows of every [gate; up] matrix of `rows` rows reordered as
-                               gate 0..63, up 0..63, gate 64..127, up 64..127, ... (fc1 weights) */
+                               gate 0..127, up 0..127, gate 128..255, up 128..255, ... (fc1 weights;
+                               rows % 256 == 0) */
 } moe_mx_mode;
 
 /* Quantise a bf16 tensor to MXFP8.  codes: batch*rows*cols bytes; scales:
  * batch*rows*cols/32 bytes.  cols % 128 == 0; ROWS: batch*rows % 128 == 0;
- * COLS_T and ROWS_GATE_UP: rows % 128 == 0. */
+ * COLS_T: rows % 128 == 0; ROWS_GATE_UP: rows % 256 == 0. */
 moe_status moe_quantize_mxfp8(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t mode,
                               uint8_t* codes, uint8_t* scales, void* stream);
 

@@ -88,7 +88,8 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """libmoe_gb300.so built in-tree, or the file MOE_GB300_LIBRARY names."""
+    return os.environ.get("MOE_GB300_LIBRARY") or _build.LIB_PATH
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:

@@ -213,7 +213,7 @@ MxW mx_weight_layout(const moe_config* c) {
     off = align_up(off + elems / 32);
     return b;
   };
-  m.w1 = buf(E * 2 * F * H);    // [E*2F, H], gate/up interleaved in 64-row blocks (fc1)
+  m.w1 = buf(E * 2 * F * H);    // [E*2F, H], gate/up interleaved in 128-row blocks (fc1)
   m.w2 = buf(E * H * F);        // [E*H, F]  (fc2)
   m.w1t = buf(E * H * 2 * F);   // [E, H, 2F] = W1_e^T, blocks along 2F (fc1 dgrad)
   m.w2t = buf(E * F * H);       // [E, F, H]  = W2_e^T, blocks along H  (fc2 dgrad)
@@ -284,7 +284,7 @@ moe_status moe_quantize_mxfp8(const void* src, int32_t batch, int32_t rows, int3
       if ((static_cast<long long>(batch) * rows) % 128 != 0) return MOE_ERR_INVALID_ARG;
       return cuda_status(launch_quantize_rows(src, static_cast<long long>(batch) * rows, cols, 0, codes, scales, st));
     case MOE_MX_ROWS_GATE_UP:
-      if (rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+      if (rows % 256 != 0) return MOE_ERR_INVALID_ARG;
       return cuda_status(
           launch_quantize_rows(src, static_cast<long long>(batch) * rows, cols, rows / 2, codes, scales, st));
     case MOE_MX_COLS_T:

@@ -83,17 +83,25 @@ struct GemmCfg {
   // Outputs leave through TMA stores staged in shared memory (every epilogue
   // but the router's narrow fp32 logits, whose rows need not be 16-byte sized).
   static constexpr bool TMA_OUT = !(EP == Epi::kStoreF32 && S == Sched::kDenseM);
-  // two 4 KB staging buffers (32 rows x 128 B, 128B-swizzled) per epilogue warp
-  static constexpr int STAGING_BYTES = TMA_OUT ? 4 * 2 * 4096 : 0;
-  static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
+  // Shared memory: the k-block ring plus 4 KB staging buffers (32 rows x 128 B,
+  // 128B-swizzled) per epilogue warp -- two each, or one where two would cost
+  // the ring its fourth stage.
+  static constexpr int SMEM_BUDGET = 232448 - 2048 - 1024;
+  static constexpr int RING_IF_TWO = (SMEM_BUDGET - (TMA_OUT ? 4 * 2 * 4096 : 0)) / STAGE_BYTES;
+  static constexpr int STAGING_BUFS = (TMA_OUT && RING_IF_TWO < 4) ? 1 : 2;
+  static constexpr int STAGING_BYTES = TMA_OUT ? 4 * STAGING_BUFS * 4096 : 0;
+  static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
   static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of one stage's scales
-  static constexpr int TMEM_COLS_RAW = 2 * BN + STAGES * SF_COLS;
+  // TMEM accumulators: two (epilogue of tile i overlaps MMAs of tile i+1),
+  // or one where two 256-column accumulators would leave no room for scales.
+  static constexpr int ACC_BUFS = (MX && BN == 256) ? 1 : 2;
+  static constexpr int TMEM_COLS_RAW = ACC_BUFS * BN + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
                                    : TMEM_COLS_RAW <= 128 ? 128 : TMEM_COLS_RAW <= 256 ? 256 : 512;
   // Rows of one K-major B box (the SwiGLU tile loads gate and up halves as two boxes).
-  // (MXFP8: W1 is stored with gate and up rows interleaved in 64-row blocks, one box.)
+  // (MXFP8: W1 is stored with gate and up rows interleaved in 128-row blocks, one box.)
   static constexpr int B_BOX_ROWS = (EP == Epi::kSwiglu && !MX) ? BN / 2 : BN;
   // Columns of the output a tile covers (SwiGLU: half of the accumulator).
   static constexpr int OUT_COLS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
@@ -101,7 +109,7 @@ struct GemmCfg {
   static constexpr uint32_t IDESC = MX ? idesc_mxf8_e4m3(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
-  static_assert(EP != Epi::kSwiglu || BN == (MX ? 128 : 256), "SwiGLU tile: matching gate and up halves");
+  static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile: 128 gate + 128 matching up columns");
   static_assert(!MX || (BN % 128 == 0 && !A_MN && !B_MN), "MXFP8 operands are K-major, 128-row scale tiles");
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
   static_assert(SMEM_BYTES + 2048 <= 232448, "dynamic + static shared memory per CTA");
@@ -392,13 +400,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 // 32 rows (one per lane) x 128 bytes in the 128-byte swizzled order (16-byte
 // chunk c of row r sits at chunk c ^ (r % 8)), so a warp's 16-byte stores hit
 // distinct banks.  Lane 0 issues the stores and owns the bulk groups.
+template <int NBUF>
 struct Stager {
   uint8_t* buf;
   int cur;
   int lane;
 
   __device__ __forceinline__ void begin() {   // the buffer about to be filled is no longer read by TMA
-    if (lane == 0) bulk_wait_group_read<1>();
+    if (lane == 0) bulk_wait_group_read<NBUF - 1>();
     __syncwarp();
   }
   __device__ __forceinline__ void put(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
@@ -412,7 +421,7 @@ struct Stager {
       tma_store_2d(map, buf + cur * 4096, x, y);
       bulk_commit_group();
     }
-    cur ^= 1;
+    cur = (NBUF == 1) ? 0 : cur ^ 1;
   }
   __device__ __forceinline__ void drain() {
     if (lane == 0) bulk_wait_group_all();
@@ -431,7 +440,8 @@ __device__ __forceinline__ void load32(uint32_t taddr, uint32_t (&a)[16], uint32
 // 32q..32q+31, lane = row.  Dense tiles past the last row are clipped by TMA.
 template <class C>
 __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
-                                                  int quarter, int lane, Stager& st, const CUtensorMap* tmC,
+                                                  int quarter, int lane, Stager<C::STAGING_BUFS>& st,
+                                                  const CUtensorMap* tmC,
                                                   const CUtensorMap* tmC2) {
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t t0 = tmem_acc + lane_addr;
@@ -583,8 +593,8 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t tfull_bar[C::ACC_BUFS];
+  __shared__ __align__(8) uint64_t tempty_bar[C::ACC_BUFS];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -604,7 +614,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], 4);
     }
@@ -690,7 +700,7 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (C::MX) {
             // scale tiles of this stage -> TMEM, then 4 MMAs of K=32; MMA kk reads byte kk
             const uint32_t sf_addr = smem_u32(sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES));
-            const uint32_t sfa_t = tmem_base + 2 * C::BN + stage * C::SF_COLS;
+            const uint32_t sfa_t = tmem_base + C::ACC_BUFS * C::BN + stage * C::SF_COLS;
             const uint32_t sfb_t = sfa_t + 4;
             tmem_cp_32x128b_warpx4(sfa_t, smem_desc_plain16(sf_addr));
             #pragma unroll
@@ -718,7 +728,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         mma_commit(&tfull_bar[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == C::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok && any) {
         mma_commit(&drain_bar);
@@ -730,7 +740,7 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    Stager st{stage_smem + (warp - 2) * 8192, 0, lane};
+    Stager<C::STAGING_BUFS> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * 4096), 0, lane};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileInfo ti = decode_tile<C>(p, s_poff, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
@@ -743,7 +753,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
     }
     if constexpr (C::TMA_OUT) st.drain();     // every TMA store has finished before the CTA exits
   }

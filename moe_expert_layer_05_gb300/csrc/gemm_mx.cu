@@ -38,16 +38,16 @@ cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
                         void* z, int* status, cudaStream_t st) {
-  // w1q rows of one expert are [gate 0..63, up 0..63, gate 64..127, up 64..127, ...]
+  // w1q rows of one expert are [gate 0..127, up 0..127, gate 128..255, up 128..255, ...]
   CUtensorMap ta, tb;
-  if (!make_tmap_u8(&ta, aq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w1q, H, static_cast<uint64_t>(E) * 2 * F, 128))
+  if (!make_tmap_u8(&ta, aq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w1q, H, static_cast<uint64_t>(E) * 2 * F, 256))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
   p.poffsets = poffsets;
   p.E = E;
   p.m_rows = dense_rows;
   p.k_len = H;
-  p.n_tiles = F / 64;
+  p.n_tiles = F / 128;
   p.b_rows_per_group = 2 * F;
   p.c = h;
   p.ldc = F;
@@ -66,25 +66,26 @@ cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, 
     return cudaErrorInvalidValue;
   if (z == nullptr) tz = tc;
   if (poffsets != nullptr)
-    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwiglu, true>>(ta, tb, tc, tz, p, rows_alloc,
+    return launch_mx<GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwiglu, true>>(ta, tb, tc, tz, p, rows_alloc,
                                                                                       dense_rows, st);
-  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kSwiglu, true>>(ta, tb, tc, tz, p, rows_alloc,
+  return launch_mx<GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwiglu, true>>(ta, tb, tc, tz, p, rows_alloc,
                                                                                    dense_rows, st);
 }
 
-// c [rows, N] bf16 = A [rows, K] x B_e [N, K]^T, both E4M3 with scales.
-cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
-                            int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
-                            cudaStream_t st) {
+namespace {
+template <int BN>
+cudaError_t mx_nt_bf16_bn(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
+                          int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
+                          cudaStream_t st) {
   CUtensorMap ta, tb;
-  if (!make_tmap_u8(&ta, aq, K, rows_alloc, 128) || !make_tmap_u8(&tb, bq, K, static_cast<uint64_t>(E) * N, 128))
+  if (!make_tmap_u8(&ta, aq, K, rows_alloc, 128) || !make_tmap_u8(&tb, bq, K, static_cast<uint64_t>(E) * N, BN))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
   p.poffsets = poffsets;
   p.E = E;
   p.m_rows = dense_rows;
   p.k_len = K;
-  p.n_tiles = N / 128;
+  p.n_tiles = N / BN;
   p.b_rows_per_group = N;
   p.c = c;
   p.ldc = N;
@@ -97,10 +98,20 @@ cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, c, N, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr)
-    return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
-                                                                                         dense_rows, st);
-  return launch_mx<GemmCfg<128, false, false, Sched::kDenseM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
-                                                                                      dense_rows, st);
+    return launch_mx<GemmCfg<BN, false, false, Sched::kRoutedM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                        dense_rows, st);
+  return launch_mx<GemmCfg<BN, false, false, Sched::kDenseM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                     dense_rows, st);
+}
+}  // namespace
+
+// c [rows, N] bf16 = A [rows, K] x B_e [N, K]^T, both E4M3 with scales.
+cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
+                            int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
+                            cudaStream_t st) {
+  if (N % 256 == 0)
+    return mx_nt_bf16_bn<256>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st);
+  return mx_nt_bf16_bn<128>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st);
 }
 
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
@@ -139,12 +150,14 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
                                                                                       dense_rows, st);
 }
 
-cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
-                          int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
-                          cudaStream_t st) {
+namespace {
+template <int BN>
+cudaError_t mx_wgrad_bn(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
+                        int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
+                        cudaStream_t st) {
   // A^T [M, rows] and B^T [N, rows], quantised along rows (the contraction)
   CUtensorMap ta, tb;
-  if (!make_tmap_u8(&ta, atq, rows_alloc, M, 128) || !make_tmap_u8(&tb, btq, rows_alloc, N, 128))
+  if (!make_tmap_u8(&ta, atq, rows_alloc, M, 128) || !make_tmap_u8(&tb, btq, rows_alloc, N, BN))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
   p.poffsets = poffsets;
@@ -152,7 +165,7 @@ cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* 
   p.m_rows = M;
   p.k_len = dense_rows;
   p.m_tiles_w = M / 128;
-  p.n_tiles = N / 128;
+  p.n_tiles = N / BN;
   p.c = dw;
   p.ldc = N;
   p.c_group_stride = static_cast<long long>(M) * N;
@@ -164,8 +177,17 @@ cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* 
   p.sfb_tiles_k = rows_alloc / 128;
   CUtensorMap tc;
   if (!make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M)) return cudaErrorInvalidValue;
-  return launch_mx<GemmCfg<128, false, false, Sched::kRoutedK, Epi::kStoreF32, true>>(ta, tb, tc, tc, p, rows_alloc,
-                                                                                      dense_rows, st);
+  return launch_mx<GemmCfg<BN, false, false, Sched::kRoutedK, Epi::kStoreF32, true>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                     dense_rows, st);
+}
+}  // namespace
+
+cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
+                          int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
+                          cudaStream_t st) {
+  if (N % 256 == 0)
+    return mx_wgrad_bn<256>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
+  return mx_wgrad_bn<128>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
 }
 
 }  // namespace moe

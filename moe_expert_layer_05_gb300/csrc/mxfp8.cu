@@ -59,15 +59,15 @@ __device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst
 }
 
 // Output row of input row r when the rows come in groups of 2*half (an
-// expert's [gate; up] projection) and are interleaved in 64-row blocks:
-// gate 0..63, up 0..63, gate 64..127, up 64..127, ...  half == 0: identity.
+// expert's [gate; up] projection) and are interleaved in 128-row blocks:
+// gate 0..127, up 0..127, gate 128..255, up 128..255, ...  half == 0: identity.
 __device__ __forceinline__ long long gate_up_row(long long r, int half) {
   if (half == 0) return r;
   const long long g = r / (2 * half);
   const int j = static_cast<int>(r % (2 * half));
   const int up = j >= half ? 1 : 0;
   const int jj = j - up * half;
-  return g * 2 * half + (jj / 64) * 128 + up * 64 + (jj % 64);
+  return g * 2 * half + (jj / 128) * 256 + up * 128 + (jj % 128);
 }
 
 // Blocks along the row: src [rows, cols] bf16 -> codes [rows, cols], scales tiled.

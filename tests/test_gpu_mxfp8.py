@@ -101,7 +101,7 @@ def test_quantize_gate_up_interleave(lib):
     for e in range(E):
         for j in range(2 * F):
             up, jj = divmod(j, F)
-            r = (jj // 64) * 128 + up * 64 + jj % 64
+            r = (jj // 128) * 256 + up * 128 + jj % 128
             np.testing.assert_array_equal(got[e, r], oc[e, j])
             np.testing.assert_array_equal(gsf[e, r], os_[e, j])
 
