@@ -261,7 +261,7 @@ class MoELayer:
         self.w = weights
         self.layout = moe_activation_layout(cfg, with_backward)
         self.act = torch.empty(self.layout.total, dtype=torch.uint8, device=device)
-        self.ws = torch.zeros(max(moe_workspace_bytes(cfg), 1024), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(moe_workspace_bytes(cfg), 256), dtype=torch.uint8, device=device)
         moe_workspace_init(self.ws)
         self.cw = MoeWeights(ptr(weights["w_router"]), ptr(weights.get("bias")), ptr(weights["w1"]),
                              ptr(weights["w2"]), ptr(weights.get("w1_shared")), ptr(weights.get("w2_shared")),

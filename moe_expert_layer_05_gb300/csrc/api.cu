@@ -57,10 +57,7 @@ using namespace moe;
 namespace {
 
 constexpr size_t kAlign = 256;
-// Workspace: [status word + split-K counters][histograms][split-K partial tiles][MXFP8 buffers]
-constexpr size_t kStatusBytes = 1024;
-constexpr size_t kSplitKCounters = 256;                          // byte offset of the counters
-constexpr size_t kSplitKBytes = 160ull * 128 * 256 * 4;          // partial tiles of one wave
+constexpr size_t kStatusBytes = 256;   // status word region at the start of the workspace
 constexpr size_t kNone = SIZE_MAX;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -227,19 +224,11 @@ MxW mx_weight_layout(const moe_config* c) {
   return m;
 }
 
-size_t splitk_base(const moe_config* c) { return kStatusBytes + align_up(hist_bytes(c)); }
-size_t mx_ws_base(const moe_config* c) { return splitk_base(c) + kSplitKBytes; }
+size_t mx_ws_base(const moe_config* c) { return kStatusBytes + align_up(hist_bytes(c)); }
 
 moe_status check_device() { return device_is_gb300() ? MOE_OK : MOE_ERR_UNSUPPORTED; }
 
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
-SplitK splitk_of(void* ws, const moe_config* c) {
-  SplitK sk;
-  sk.part = at<float>(ws, splitk_base(c));
-  sk.part_bytes = kSplitKBytes;
-  sk.cnt = at<int>(ws, kSplitKCounters);
-  return sk;
-}
 int32_t* hist_ptr(void* ws) { return at<int32_t>(ws, kStatusBytes); }
 
 }  // namespace
@@ -271,7 +260,7 @@ moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, m
 
 size_t moe_workspace_bytes(const moe_config* cfg) {
   if (!config_ok(cfg)) return 0;
-  size_t b = mx_ws_base(cfg);
+  size_t b = kStatusBytes + align_up(hist_bytes(cfg));
   if (cfg->dtype == MOE_GEMM_MXFP8) b += mx_ws_layout(cfg).total;
   return b;
 }
@@ -399,7 +388,6 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
   const int rows = dense ? a->dense_rows : cap_rows(cfg);
   const int32_t* po = dense ? nullptr : a->poffsets;
   int* status = status_ptr(ws);
-  const SplitK sk = splitk_of(ws, cfg);
   if (cfg->dtype == MOE_GEMM_MXFP8) {
     if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
     if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
@@ -407,17 +395,17 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
       case MOE_GG_FC1_SWIGLU:
         if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
         return cuda_status(gemm_mx_fc1(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
-                                       a->row_gate, a->c, a->c2, status, st, sk));
+                                       a->row_gate, a->c, a->c2, status, st));
       case MOE_GG_FC2:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->dense_rows,
-                                           a->c, status, st, sk));
+                                           a->c, status, st));
       case MOE_GG_DGRAD_FC2:
         if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
         return cuda_status(gemm_mx_dgrad_fc2(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
-                                             a->aux, a->row_gate, a->c, a->dgate_part, status, st, sk));
+                                             a->aux, a->row_gate, a->c, a->dgate_part, status, st));
       case MOE_GG_DGRAD_FC1:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, 2 * F, a->b, a->b_scales, E, H, po,
-                                           a->dense_rows, a->c, status, st, sk));
+                                           a->dense_rows, a->c, status, st));
       case MOE_GG_WGRAD_FC1:
         return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, 2 * F, a->b, a->b_scales, H, rows, E, po, a->dense_rows,
                                          static_cast<float*>(a->c), status, st));
@@ -431,15 +419,15 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
   switch (a->op) {
     case MOE_GG_FC1_SWIGLU:
       if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
-      return cuda_status(gemm_fc1(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->row_gate, a->c, a->c2, status, st, sk));
+      return cuda_status(gemm_fc1(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->row_gate, a->c, a->c2, status, st));
     case MOE_GG_FC2:
-      return cuda_status(gemm_fc2(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st, sk));
+      return cuda_status(gemm_fc2(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st));
     case MOE_GG_DGRAD_FC2:
       if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
       return cuda_status(gemm_dgrad_fc2(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->aux, a->row_gate, a->c,
-                                        a->dgate_part, status, st, sk));
+                                        a->dgate_part, status, st));
     case MOE_GG_DGRAD_FC1:
-      return cuda_status(gemm_dgrad_fc1(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st, sk));
+      return cuda_status(gemm_dgrad_fc1(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st));
     case MOE_GG_WGRAD_FC1:
       return cuda_status(gemm_wgrad(a->a, 2 * F, a->b, H, rows, E, po, a->dense_rows, static_cast<float*>(a->c),
                                     status, st));
@@ -476,7 +464,6 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = cfg->T, H = cfg->H, E = cfg->E, k = cfg->k, F = cfg->F, S = cfg->S, cap = L.cap;
   int* status = status_ptr(ws);
-  const SplitK sk = splitk_of(ws, cfg);
   float* logits = at<float>(act, L.logits);
   int32_t* idx = at<int32_t>(act, L.topk_idx);
   float* gate = at<float>(act, L.topk_gate);
@@ -511,24 +498,24 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     auto wq = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
     auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
     MOE_TRY(launch_quantize_rows(x_perm, cap, H, 0, q(M.x), f(M.x), st));
-    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st, sk));
+    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
     MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st));
-    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st, sk));
+    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st));
     if (S > 0 && T > 0) {
       MOE_TRY(launch_quantize_rows(x, T, H, 0, q(M.xs), f(M.xs), st));
       MOE_TRY(gemm_mx_fc1(q(M.xs), f(M.xs), T, H, wq(W.s1), wf(W.s1), 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
-                          zs, status, st, sk));
+                          zs, status, st));
       MOE_TRY(launch_quantize_rows(at<void>(act, L.hs), T, S, 0, q(M.hs), f(M.hs), st));
       MOE_TRY(gemm_mx_nt_bf16(q(M.hs), f(M.hs), T, S, wq(W.s2), wf(W.s2), 1, H, nullptr, T, at<void>(act, L.os),
-                              status, st, sk));
+                              status, st));
       shared_out = at<void>(act, L.os);
     }
   } else {
-    MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, z, status, st, sk));
-    MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st, sk));
+    MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, z, status, st));
+    MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st));
     if (S > 0 && T > 0) {
-      MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs), zs, status, st, sk));
-      MOE_TRY(gemm_fc2(at<void>(act, L.hs), T, S, w->w2_shared, 1, H, nullptr, T, at<void>(act, L.os), status, st, sk));
+      MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs), zs, status, st));
+      MOE_TRY(gemm_fc2(at<void>(act, L.hs), T, S, w->w2_shared, 1, H, nullptr, T, at<void>(act, L.os), status, st));
       shared_out = at<void>(act, L.os);
     }
   }
@@ -553,7 +540,6 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = cfg->T, H = cfg->H, E = cfg->E, k = cfg->k, F = cfg->F, S = cfg->S, cap = L.cap;
   int* status = status_ptr(ws);
-  const SplitK sk = splitk_of(ws, cfg);
   const int32_t* counts = at<int32_t>(act, L.counts);
   const int32_t* poff = at<int32_t>(act, L.poffsets);
   const int32_t* slot_row = at<int32_t>(act, L.slot_row);
@@ -575,27 +561,27 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
     auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
     MOE_TRY(launch_quantize_rows(dy_perm, cap, H, 0, q(M.dy), f(M.dy), st));
     MOE_TRY(gemm_mx_dgrad_fc2(q(M.dy), f(M.dy), cap, H, wq(W.w2t), wf(W.w2t), E, F, poff, 0, at<void>(act, L.z),
-                              at<float>(act, L.row_gate), dz, dpart, status, st, sk));
+                              at<float>(act, L.row_gate), dz, dpart, status, st));
     MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st));
-    MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st, sk));
+    MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st));
     if (S > 0 && T > 0) {
       MOE_TRY(launch_quantize_rows(dy, T, H, 0, q(M.dys), f(M.dys), st));
       MOE_TRY(gemm_mx_dgrad_fc2(q(M.dys), f(M.dys), T, H, wq(W.s2t), wf(W.s2t), 1, S, nullptr, T, at<void>(act, L.zs),
-                                nullptr, at<void>(act, L.dzs), nullptr, status, st, sk));
+                                nullptr, at<void>(act, L.dzs), nullptr, status, st));
       MOE_TRY(launch_quantize_rows(at<void>(act, L.dzs), T, 2 * S, 0, q(M.dzs), f(M.dzs), st));
       MOE_TRY(gemm_mx_nt_bf16(q(M.dzs), f(M.dzs), T, 2 * S, wq(W.s1t), wf(W.s1t), 1, H, nullptr, T,
-                              at<void>(act, L.dxs), status, st, sk));
+                              at<void>(act, L.dxs), status, st));
       dxs = at<void>(act, L.dxs);
     }
   } else {
     MOE_TRY(gemm_dgrad_fc2(dy_perm, cap, H, w->w2, E, F, poff, 0, at<void>(act, L.z), at<float>(act, L.row_gate), dz,
-                           dpart, status, st, sk));
-    MOE_TRY(gemm_dgrad_fc1(dz, cap, F, w->w1, E, H, poff, 0, dx_perm, status, st, sk));
+                           dpart, status, st));
+    MOE_TRY(gemm_dgrad_fc1(dz, cap, F, w->w1, E, H, poff, 0, dx_perm, status, st));
     if (S > 0 && T > 0) {
       MOE_TRY(gemm_dgrad_fc2(dy, T, H, w->w2_shared, 1, S, nullptr, T, at<void>(act, L.zs), nullptr,
-                             at<void>(act, L.dzs), nullptr, status, st, sk));
+                             at<void>(act, L.dzs), nullptr, status, st));
       MOE_TRY(gemm_dgrad_fc1(at<void>(act, L.dzs), T, S, w->w1_shared, 1, H, nullptr, T, at<void>(act, L.dxs), status,
-                             st, sk));
+                             st));
       dxs = at<void>(act, L.dxs);
     }
   }

@@ -55,12 +55,6 @@ struct GemmParams {
   float* dgate_part;       // kSwigluBwd: [rows, n_tiles] partial dot products
   int valid_cols;          // kStoreF32: store only columns < valid_cols
   int rows_cap;            // rows allocated in the expert-ordered buffers (routed modes)
-  // Split-K of the last, partial wave of tiles (nullptr: off): fp32 partial
-  // tiles [sk_max_parts][128][BN] and one arrival counter per split tile
-  // (zero at launch; the reducing chunk resets it).
-  float* sk_part;
-  int* sk_cnt;
-  int sk_max_parts;
   // MXFP8 only: E8M0 scale tiles of A and B (512 B per 128 rows x 128 K, see
   // mxfp8.cu) and the number of tiles along K in one 128-row band of each.
   const uint8_t* sfa;
@@ -126,23 +120,8 @@ struct TileInfo {
   int group;     // expert
   int m0;        // first A row (kRoutedM / kDenseM) or first output row (kRoutedK)
   int n;         // N tile index
-  int num_kb;    // k-blocks of this unit of work
+  int num_kb;    // k-blocks
   int k_row0;    // kRoutedK: first contraction row
-  int kb0;       // first k-block of this unit (split-K chunks start past 0)
-  int split;     // 0: whole tile; 1: a partial chunk; 2: the last chunk, which reduces
-  int sk_tile;   // split tile index (split != 0)
-  int sk_chunk;  // chunk index
-  int sk_chunks; // chunks of this tile
-};
-
-// How the persistent grid walks the work: whole tiles, except that the tiles
-// of a last, partial wave (at most half the grid) may each be cut into S
-// k-ranges run by otherwise idle CTAs.
-struct UnitPlan {
-  int full;      // units [0, full) are whole tiles
-  int tail;      // tiles after them
-  int S;         // chunks per tail tile (1: tail tiles are whole too)
-  int units;
 };
 
 template <class C>
@@ -195,52 +174,6 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
       ti.num_kb = (p.k_len + C::BK - 1) / C::BK;
     }
   }
-  return ti;
-}
-
-template <class C>
-__device__ __forceinline__ UnitPlan plan_units(const GemmParams& p, int ntiles) {
-  UnitPlan u{ntiles, 0, 1, ntiles};
-  if constexpr (C::S != Sched::kRoutedK && C::TMA_OUT) {
-    if (p.sk_part != nullptr && p.sk_cnt != nullptr) {
-      const int G = static_cast<int>(gridDim.x);
-      const int full = (ntiles / G) * G;
-      const int tail = ntiles - full;
-      const int nkb = p.k_len / C::BK;
-      int S = tail > 0 ? G / tail : 1;
-      S = S < nkb / 8 ? S : nkb / 8;     // at least 8 k-blocks per chunk
-      S = S < 16 ? S : 16;
-      if (tail > 0 && 2 * tail <= G && S >= 2 && tail * (S - 1) <= p.sk_max_parts && tail <= 192) {
-        u.full = full;
-        u.tail = tail;
-        u.S = S;
-        u.units = full + tail * S;
-      }
-    }
-  }
-  return u;
-}
-
-template <class C>
-__device__ __forceinline__ TileInfo decode_unit(const GemmParams& p, const int* s_poff, const UnitPlan& up, int u) {
-  if (up.S == 1 || u < up.full) {
-    TileInfo ti = decode_tile<C>(p, s_poff, u);
-    ti.kb0 = 0;
-    ti.split = 0;
-    ti.sk_tile = ti.sk_chunk = 0;
-    ti.sk_chunks = 1;
-    return ti;
-  }
-  const int v = u - up.full;
-  const int tile = v / up.S, chunk = v % up.S;
-  TileInfo ti = decode_tile<C>(p, s_poff, up.full + tile);
-  const int nkb = ti.num_kb;
-  ti.kb0 = chunk * nkb / up.S;
-  ti.num_kb = (chunk + 1) * nkb / up.S - ti.kb0;
-  ti.split = (chunk == up.S - 1) ? 2 : 1;
-  ti.sk_tile = tile;
-  ti.sk_chunk = chunk;
-  ti.sk_chunks = up.S;
   return ti;
 }
 
@@ -463,32 +396,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
   }
 }
 
-// Source of accumulator values in the epilogue: TMEM, plus (for the reducing
-// chunk of a split tile) the fp32 partial tiles of the earlier chunks, added
-// in chunk order so the result does not depend on timing.
-struct AccSrc {
-  const float* part;   // [nparts][128][bn] for this tile, or nullptr
-  int nparts;
-  int row;             // row of the tile this thread owns
-  int bn;
-  __device__ __forceinline__ void fix(uint32_t (&v)[16], int col) const {
-    if (part == nullptr) return;
-    float s[16];
-    #pragma unroll
-    for (int j = 0; j < 16; ++j) s[j] = 0.f;
-    for (int c = 0; c < nparts; ++c) {
-      const float4* q = reinterpret_cast<const float4*>(part + ((size_t)c * 128 + row) * bn + col);
-      #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 f = __ldcg(q + j);
-        s[4 * j] += f.x; s[4 * j + 1] += f.y; s[4 * j + 2] += f.z; s[4 * j + 3] += f.w;
-      }
-    }
-    #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(s[j] + __uint_as_float(v[j]));
-  }
-};
-
 // Per-warp staging of output chunks for TMA stores: two 4 KB buffers, each
 // 32 rows (one per lane) x 128 bytes in the 128-byte swizzled order (16-byte
 // chunk c of row r sits at chunk c ^ (r % 8)), so a warp's 16-byte stores hit
@@ -522,14 +429,11 @@ struct Stager {
   }
 };
 
-__device__ __forceinline__ void load32(uint32_t taddr, uint32_t (&a)[16], uint32_t (&b)[16], const AccSrc& src,
-                                       int col) {
+__device__ __forceinline__ void load32(uint32_t taddr, uint32_t (&a)[16], uint32_t (&b)[16]) {
   tmem_ld_x16(taddr, a);
   tmem_ld_x16(taddr + 16, b);
   tmem_ld_wait(a);
   tmem_ld_wait(b);
-  src.fix(a, col);
-  src.fix(b, col + 16);
 }
 
 // Epilogue with TMA stores.  Rows of the tile: warp quarter q owns rows
@@ -538,7 +442,7 @@ template <class C>
 __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
                                                   int quarter, int lane, Stager<C::STAGING_BUFS>& st,
                                                   const CUtensorMap* tmC,
-                                                  const CUtensorMap* tmC2, const AccSrc& src) {
+                                                  const CUtensorMap* tmC2) {
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t t0 = tmem_acc + lane_addr;
   const bool no_mma = (ti.num_kb == 0);         // empty group (weight gradients): result is zero
@@ -548,7 +452,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN; c0 += 32) {
       uint32_t a[16], b[16];
-      load32(t0 + c0, a, b, src, c0);
+      load32(t0 + c0, a, b);
       st.begin();
       #pragma unroll
       for (int j = 0; j < 4; ++j) st.put(j, no_mma ? 0u : a[4 * j], no_mma ? 0u : a[4 * j + 1],
@@ -566,7 +470,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
       #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t a[16], b[16];
-        load32(t0 + c0 + 32 * h, a, b, src, c0 + 32 * h);
+        load32(t0 + c0 + 32 * h, a, b);
         uint32_t w[16];
         #pragma unroll
         for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
@@ -594,8 +498,6 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         tmem_ld_x16(t0 + C::BN / 2 + c0 + 16 * q, b);
         tmem_ld_wait(a);
         tmem_ld_wait(b);
-        src.fix(a, c0 + 16 * q);
-        src.fix(b, C::BN / 2 + c0 + 16 * q);
         uint32_t hw[8];
         #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -614,7 +516,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t a[16], b[16];
-            load32(t0 + half * (C::BN / 2) + c0 + 32 * h2, a, b, src, half * (C::BN / 2) + c0 + 32 * h2);
+            load32(t0 + half * (C::BN / 2) + c0 + 32 * h2, a, b);
             uint32_t w[16];
             #pragma unroll
             for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
@@ -650,7 +552,6 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           uint32_t v[16];
           tmem_ld_x16(t0 + c, v);
           tmem_ld_wait(v);
-          src.fix(v, c);
           const uint32_t zaw[8] = {za0.x, za0.y, za0.z, za0.w, za1.x, za1.y, za1.z, za1.w};
           const uint32_t zbw[8] = {zb0.x, zb0.y, zb0.z, zb0.w, zb1.x, zb1.y, zb1.z, zb1.w};
           uint32_t out[8];
@@ -682,56 +583,6 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     }
     if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * p.n_tiles + ti.n] = dg;
   }
-}
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// A partial chunk of a split tile: write the fp32 accumulator to its slot and
-// count the chunk in (all 128 epilogue threads take part).
-template <class C>
-__device__ __forceinline__ void store_partial(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc, int quarter,
-                                              int lane) {
-  const int row = quarter * 32 + lane;
-  const uint32_t t0 = tmem_acc + (static_cast<uint32_t>(quarter * 32) << 16);
-  float* dst = p.sk_part + ((size_t)(ti.sk_tile * (ti.sk_chunks - 1) + ti.sk_chunk) * 128 + row) * C::BN;
-  #pragma unroll 1
-  for (int c0 = 0; c0 < C::BN; c0 += 16) {
-    uint32_t v[16];
-    tmem_ld_x16(t0 + c0, v);
-    tmem_ld_wait(v);
-    float4* d4 = reinterpret_cast<float4*>(dst + c0);
-    #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                          __uint_as_float(v[4 * j + 3]));
-  }
-  __threadfence();
-  epi_bar();
-  if (threadIdx.x == 64) atomicAdd(p.sk_cnt + ti.sk_tile, 1);
-}
-
-// The reducing chunk: wait (bounded) until every earlier chunk of the tile
-// has been counted in, then reset the counter for the next launch.
-__device__ __forceinline__ void wait_partials(const GemmParams& p, const TileInfo& ti, volatile int* abort) {
-  if (threadIdx.x == 64) {
-    const unsigned long long t0 = global_timer_ns();
-    while (ld_acquire(p.sk_cnt + ti.sk_tile) < ti.sk_chunks - 1) {
-      if (*abort || global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        break;
-      }
-      __nanosleep(64);
-    }
-    p.sk_cnt[ti.sk_tile] = 0;
-    __threadfence();
-  }
-  epi_bar();
 }
 
 template <class C>
@@ -802,8 +653,6 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) set_status(p.status, kErrBadIndex);
   }
   const int ntiles = s_bad ? 0 : total_tiles<C>(p, s_poff);
-  const UnitPlan plan = plan_units<C>(p, ntiles);
-  const int nunits = plan.units;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -812,9 +661,9 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x) {
-        const TileInfo ti = decode_unit<C>(p, s_poff, plan, t);
-        for (int kb = ti.kb0; kb < ti.kb0 + ti.num_kb; ++kb) {
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<C>(p, s_poff, t);
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
           issue_loads<C>(&tmA, &tmB, p, ti, kb, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
@@ -838,12 +687,12 @@ __global__ void __launch_bounds__(192, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, any = false;
-      for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x) {
-        const TileInfo ti = decode_unit<C>(p, s_poff, plan, t);
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<C>(p, s_poff, t);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * C::BN;
-        for (int kb = ti.kb0; kb < ti.kb0 + ti.num_kb; ++kb) {
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_ptr)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
@@ -861,8 +710,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
               const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-              mma_mxf8_ss(d_tmem, ad, bd, C::IDESC | idesc_sf_ids(kk, kk), sfa_t, sfb_t,
-                          ((kb - ti.kb0) | kk) != 0 ? 1u : 0u);
+              mma_mxf8_ss(d_tmem, ad, bd, C::IDESC | idesc_sf_ids(kk, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
             }
           } else {
             #pragma unroll
@@ -871,7 +719,7 @@ __global__ void __launch_bounds__(192, 1)
                                           : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
                                           : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-              mma_bf16_ss(d_tmem, ad, bd, C::IDESC, ((kb - ti.kb0) | kk) != 0 ? 1u : 0u);
+              mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
             }
           }
           any = true;
@@ -893,22 +741,12 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     Stager<C::STAGING_BUFS> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * 4096), 0, lane};
-    for (int t = blockIdx.x; t < nunits; t += gridDim.x) {
-      const TileInfo ti = decode_unit<C>(p, s_poff, plan, t);
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile<C>(p, s_poff, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
       tc_fence_after_sync();
       if constexpr (C::TMA_OUT) {
-        if (ti.split == 1) {
-          store_partial<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
-        } else {
-          AccSrc src{nullptr, 0, quarter * 32 + lane, C::BN};
-          if (ti.split == 2) {
-            wait_partials(p, ti, abort_ptr);
-            src.part = p.sk_part + (size_t)ti.sk_tile * (ti.sk_chunks - 1) * 128 * C::BN;
-            src.nparts = ti.sk_chunks - 1;
-          }
-          epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::BN, quarter, lane, st, &tmC, &tmC2, src);
-        }
+        epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::BN, quarter, lane, st, &tmC, &tmC2);
       } else {
         epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
       }

@@ -11,7 +11,7 @@ namespace moe {
 
 cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
                            const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate,
-                           void* dz, float* dgate_part, int* status, cudaStream_t st, const SplitK& sk) {
+                           void* dz, float* dgate_part, int* status, cudaStream_t st) {
   // B[n=f, k=h] = W2_e[h, f]: W2 seen as [E*H rows, F cols], N contiguous (MN-major).
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, dy_perm, H, rows_alloc, 64, 128) ||
@@ -33,7 +33,6 @@ cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const voi
   p.dgate_part = dgate_part;
   p.rows_cap = rows_alloc;
   p.status = status;
-  set_splitk<128>(p, sk);
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
@@ -49,8 +48,7 @@ cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const voi
 namespace {
 template <int BN>
 cudaError_t dgrad_fc1_bn(const void* dz, int rows_alloc, int F, const void* w1, int E, int H,
-                         const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st,
-                         const SplitK& sk) {
+                         const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st) {
   // B[n=h, k=j] = W1_e[j, h]: W1 seen as [E*2F rows, H cols] (MN-major).
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, dz, 2 * F, rows_alloc, 64, 128) ||
@@ -67,7 +65,6 @@ cudaError_t dgrad_fc1_bn(const void* dz, int rows_alloc, int F, const void* w1, 
   p.ldc = H;
   p.rows_cap = rows_alloc;
   p.status = status;
-  set_splitk<BN>(p, sk);
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, dx_perm, H, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
@@ -108,10 +105,9 @@ cudaError_t wgrad_bn(const void* a, int M, const void* b, int N, int rows_alloc,
 }  // namespace
 
 cudaError_t gemm_dgrad_fc1(const void* dz, int rows_alloc, int F, const void* w1, int E, int H,
-                           const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st, const SplitK& sk) {
-  if (H % 256 == 0)
-    return dgrad_fc1_bn<256>(dz, rows_alloc, F, w1, E, H, poffsets, dense_rows, dx_perm, status, st, sk);
-  return dgrad_fc1_bn<128>(dz, rows_alloc, F, w1, E, H, poffsets, dense_rows, dx_perm, status, st, sk);
+                           const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st) {
+  if (H % 256 == 0) return dgrad_fc1_bn<256>(dz, rows_alloc, F, w1, E, H, poffsets, dense_rows, dx_perm, status, st);
+  return dgrad_fc1_bn<128>(dz, rows_alloc, F, w1, E, H, poffsets, dense_rows, dx_perm, status, st);
 }
 
 cudaError_t gemm_wgrad(const void* a, int M, const void* b, int N, int rows_alloc, int E, const int32_t* poffsets,

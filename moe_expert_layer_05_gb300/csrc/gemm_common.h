@@ -46,13 +46,6 @@ inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, uint64_t cols,
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32);
 }
 
-template <int BN>
-inline void set_splitk(GemmParams& p, const SplitK& sk) {
-  p.sk_part = sk.part;
-  p.sk_cnt = sk.cnt;
-  p.sk_max_parts = sk.part != nullptr ? static_cast<int>(sk.part_bytes / (128ull * BN * 4)) : 0;
-}
-
 inline GemmParams gemm_params_zero() {
   GemmParams p{};
   p.valid_cols = 1 << 30;

@@ -81,7 +81,7 @@ cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, floa
 }
 
 cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E, int F, const int32_t* poffsets,
-                     int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st, const SplitK& sk) {
+                     int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a, H, rows_alloc, 64, 128) ||
       !make_tmap_bf16(&tb, w1, H, static_cast<uint64_t>(E) * 2 * F, 64, 128))
@@ -102,7 +102,6 @@ cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E
   p.row_gate = row_gate;
   p.rows_cap = rows_alloc;
   p.status = status;
-  set_splitk<256>(p, sk);
   CUtensorMap tc, tz;
   if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
     return cudaErrorInvalidValue;
@@ -120,7 +119,7 @@ cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E
 namespace {
 template <int BN>
 cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
-                   int dense_rows, void* o, int* status, cudaStream_t st, const SplitK& sk) {
+                   int dense_rows, void* o, int* status, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a, F, rows_alloc, 64, 128) ||
       !make_tmap_bf16(&tb, w2, F, static_cast<uint64_t>(E) * H, 64, BN))
@@ -136,7 +135,6 @@ cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, 
   p.ldc = H;
   p.rows_cap = rows_alloc;
   p.status = status;
-  set_splitk<BN>(p, sk);
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, o, H, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
@@ -151,9 +149,9 @@ cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, 
 }  // namespace
 
 cudaError_t gemm_fc2(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
-                     int dense_rows, void* o, int* status, cudaStream_t st, const SplitK& sk) {
-  if (H % 256 == 0) return fc2_bn<256>(a, rows_alloc, F, w2, E, H, poffsets, dense_rows, o, status, st, sk);
-  return fc2_bn<128>(a, rows_alloc, F, w2, E, H, poffsets, dense_rows, o, status, st, sk);
+                     int dense_rows, void* o, int* status, cudaStream_t st) {
+  if (H % 256 == 0) return fc2_bn<256>(a, rows_alloc, F, w2, E, H, poffsets, dense_rows, o, status, st);
+  return fc2_bn<128>(a, rows_alloc, F, w2, E, H, poffsets, dense_rows, o, status, st);
 }
 
 }  // namespace moe

@@ -37,7 +37,7 @@ cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
-                        void* z, int* status, cudaStream_t st, const SplitK& sk) {
+                        void* z, int* status, cudaStream_t st) {
   // w1q rows of one expert are [gate 0..127, up 0..127, gate 128..255, up 128..255, ...]
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, aq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w1q, H, static_cast<uint64_t>(E) * 2 * F, 256))
@@ -61,7 +61,6 @@ cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, 
   p.sfb = static_cast<const uint8_t*>(w1sf);
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
-  set_splitk<256>(p, sk);
   CUtensorMap tc, tz;
   if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
     return cudaErrorInvalidValue;
@@ -77,7 +76,7 @@ namespace {
 template <int BN>
 cudaError_t mx_nt_bf16_bn(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
                           int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
-                          cudaStream_t st, const SplitK& sk) {
+                          cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, aq, K, rows_alloc, 128) || !make_tmap_u8(&tb, bq, K, static_cast<uint64_t>(E) * N, BN))
     return cudaErrorInvalidValue;
@@ -96,7 +95,6 @@ cudaError_t mx_nt_bf16_bn(const void* aq, const void* asf, int rows_alloc, int K
   p.sfb = static_cast<const uint8_t*>(bsf);
   p.sfa_tiles_k = K / 128;
   p.sfb_tiles_k = K / 128;
-  set_splitk<BN>(p, sk);
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, c, N, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr)
@@ -110,15 +108,15 @@ cudaError_t mx_nt_bf16_bn(const void* aq, const void* asf, int rows_alloc, int K
 // c [rows, N] bf16 = A [rows, K] x B_e [N, K]^T, both E4M3 with scales.
 cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
                             int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
-                            cudaStream_t st, const SplitK& sk) {
+                            cudaStream_t st) {
   if (N % 256 == 0)
-    return mx_nt_bf16_bn<256>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st, sk);
-  return mx_nt_bf16_bn<128>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st, sk);
+    return mx_nt_bf16_bn<256>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st);
+  return mx_nt_bf16_bn<128>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st);
 }
 
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
-                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st, const SplitK& sk) {
+                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st) {
   // B_e = W2_e^T [F, H], quantised along H
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, dyq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w2tq, H, static_cast<uint64_t>(E) * F, 128))
@@ -143,7 +141,6 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
   p.sfb = static_cast<const uint8_t*>(w2tsf);
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
-  set_splitk<128>(p, sk);
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr)

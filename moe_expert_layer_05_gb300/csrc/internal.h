@@ -48,15 +48,6 @@ cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, c
 cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, const int32_t* counts,
                                 const int32_t* poffsets, int E, int H, float* dw_router, cudaStream_t st);
 
-// Split-K of a grouped GEMM's last partial wave: an fp32 partial-tile buffer
-// and per-tile counters (zero before the first launch; kept zero after each).
-// Launches sharing it must be ordered on one stream.  part == nullptr: off.
-struct SplitK {
-  float* part = nullptr;
-  size_t part_bytes = 0;
-  int* cnt = nullptr;
-};
-
 // ------------------------------------------------------------ GEMMs (gemm_*.cu)
 // logits[T,E] (fp32) = x[T,H] * Wr[E,H]^T
 cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, float* logits, int* status,
@@ -64,21 +55,17 @@ cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, floa
 // h[cap,F] = g * silu(z_gate) * z_up with z = A[cap,H] * W1_e[2F,H]^T; z saved if non-null.
 // poffsets == nullptr: dense, rows = dense_rows, one group.
 cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E, int F, const int32_t* poffsets,
-                     int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st,
-                     const SplitK& sk = SplitK{});
+                     int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st);
 // o[cap,H] = A[cap,F] * W2_e[H,F]^T
 cudaError_t gemm_fc2(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
-                     int dense_rows, void* o, int* status, cudaStream_t st,
-                     const SplitK& sk = SplitK{});
+                     int dense_rows, void* o, int* status, cudaStream_t st);
 // dz[cap,2F] from dh = A[cap,H] * W2_e ([H,F]) with SwiGLU backward epilogue.
 cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
                            const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate,
-                           void* dz, float* dgate_part, int* status, cudaStream_t st,
-                           const SplitK& sk = SplitK{});
+                           void* dz, float* dgate_part, int* status, cudaStream_t st);
 // dx_perm[cap,H] = dz[cap,2F] * W1_e ([2F,H])
 cudaError_t gemm_dgrad_fc1(const void* dz, int rows_alloc, int F, const void* w1, int E, int H,
-                           const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st,
-                           const SplitK& sk = SplitK{});
+                           const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st);
 // dW[e] (fp32 [M,N]) = A_e^T B_e, A [rows, M] bf16, B [rows, N] bf16 over each expert's rows
 // (poffsets) or over dense_rows rows (poffsets == nullptr, one group).
 cudaError_t gemm_wgrad(const void* a, int M, const void* b, int N, int rows_alloc, int E, const int32_t* poffsets,
@@ -94,16 +81,13 @@ cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols,
                                  cudaStream_t st);
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
-                        void* z, int* status, cudaStream_t st,
-                        const SplitK& sk = SplitK{});
+                        void* z, int* status, cudaStream_t st);
 cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
                             int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
-                            cudaStream_t st,
-                            const SplitK& sk = SplitK{});
+                            cudaStream_t st);
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
-                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st,
-                              const SplitK& sk = SplitK{});
+                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st);
 cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
                           cudaStream_t st);

@@ -31,7 +31,7 @@ SMALL = {
                            zipf_s=1.2, backward=True),
     "one_token": Workload("one_token", T=1, H=128, E=8, k=2, F=128, S=128, backward=True),
     "odd_k": Workload("odd_k", T=200, H=128, E=16, k=3, F=128, backward=True),
-    "wide_ffn": Workload("wide_ffn", T=256, H=256, E=8, k=2, F=2048, backward=True),   # split-K tails
+    "wide_ffn": Workload("wide_ffn", T=256, H=256, E=8, k=2, F=2048, backward=True),   # few tiles, long K
 }
 
 
@@ -221,9 +221,8 @@ def test_layer_full_size_qwen3_fwd_bwd_sampled(lib):
     assert rel_l2(f64(grads["dw_router"][e_star]), bwd_e["dWr"][e_star]) <= 1e-2
 
 
-def test_split_k_tail_is_deterministic(lib):
-    """Few tiles with long K: the last wave is split along K and reduced in a
-    fixed chunk order, so reruns are bit-identical."""
+def test_few_tiles_long_k_is_deterministic(lib):
+    """Few tiles with long K (fewer tiles than SMs): reruns are bit-identical."""
     w = SMALL["wide_ffn"]
     dinp = _to_dev(make_inputs(w, seed=7))
     layer = _layer(w, dinp, True)

@@ -230,7 +230,7 @@ MX_LAYERS = {
     "dsv3_mx_small": Workload("dsv3_mx_small", T=384, H=256, E=64, k=8, F=128, S=256, score="sigmoid", zipf_s=1.2,
                               dtype="mxfp8", backward=True),
     "mixtral_mx_small": Workload("mixtral_mx_small", T=256, H=512, E=8, k=2, F=768, dtype="mxfp8", backward=True),
-    "wide_mx": Workload("wide_mx", T=256, H=256, E=8, k=2, F=2048, dtype="mxfp8", backward=True),   # split-K tails
+    "wide_mx": Workload("wide_mx", T=256, H=256, E=8, k=2, F=2048, dtype="mxfp8", backward=True),   # few tiles, long K
 }
 
 

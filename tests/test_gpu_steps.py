@@ -210,7 +210,7 @@ GEMM_CASES = [
     (256, 128, 8, 2, 256, 0.0),       # tiny workload shape
     (700, 256, 16, 4, 384, 1.5),      # hot and empty experts, several tiles
     (300, 512, 128, 8, 128, 1.0),     # fine-grained experts
-    (256, 256, 8, 2, 2048, 0.0),      # few tiles, long K: fc2 / fc1-dgrad split along K across idle SMs
+    (256, 256, 8, 2, 2048, 0.0),      # few tiles, long K
 ]
 
 
