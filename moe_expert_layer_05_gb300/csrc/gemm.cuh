@@ -1,11 +1,12 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05).
 //
-// One CTA per SM walks a list of 128 x BN output tiles.  Warp roles:
+// One CTA per SM walks a list of 128 x BN output tiles (256 x BN where two
+// 128-row MMAs share each B k-block).  Warp roles:
 //   warp 0      TMA producer: streams A and B k-blocks (64 bf16 = one 128-B
 //               swizzle row) into a STAGES-deep shared-memory ring;
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
 //               K=16) into one of two TMEM accumulators;
-//   warps 2..5  epilogue: tcgen05.ld the finished accumulator (warp w reads
+//   warps 2..   epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32*(w%4)..+31, i.e. one output row per thread),
 //               apply the fused elementwise step and store to global memory,
 //               while the MMA warp already fills the other accumulator.
@@ -64,9 +65,11 @@ struct GemmParams {
   int* status;             // device status word (first error wins)
 };
 
-template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false>
+template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false, bool M256_ = false>
 struct GemmCfg {
-  static constexpr int BM = 128;
+  static constexpr int BM = 128;                  // M of one MMA instruction
+  static constexpr bool M256 = M256_;             // 256-row tiles: two MMAs share each B k-block
+  static constexpr int TILE_M = M256 ? 256 : 128;
   static constexpr bool MX = MX_;                 // MXFP8 operands (E4M3 + E8M0 1x32 scales)
   static constexpr int BK = MX ? 128 : 64;        // one 128-byte swizzle row per k-block
   static constexpr int KSTEP = MX ? 32 : 16;      // K of one MMA instruction
@@ -75,7 +78,7 @@ struct GemmCfg {
   static constexpr bool B_MN = B_MN_;
   static constexpr Sched S = S_;
   static constexpr Epi EP = EP_;
-  static constexpr int A_BYTES = BM * 128;
+  static constexpr int A_BYTES = TILE_M * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int SFA_BYTES = MX ? 512 : 0;
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
@@ -83,21 +86,32 @@ struct GemmCfg {
   // Outputs leave through TMA stores staged in shared memory (every epilogue
   // but the router's narrow fp32 logits, whose rows need not be 16-byte sized).
   static constexpr bool TMA_OUT = !(EP == Epi::kStoreF32 && S == Sched::kDenseM);
-  // Shared memory: the k-block ring plus 4 KB staging buffers (32 rows x 128 B,
-  // 128B-swizzled) per epilogue warp -- two each, or one where two would cost
-  // the ring its fourth stage.
-  static constexpr int SMEM_BUDGET = 232448 - 2048 - 1024;
-  static constexpr int RING_IF_TWO = (SMEM_BUDGET - (TMA_OUT ? 4 * 2 * 4096 : 0)) / STAGE_BYTES;
+  // Epilogue warps: four (one per TMEM lane quarter), or eight for 256-row
+  // tiles, where the second four write rows 128..255 at the same time.
+  static constexpr int EPI_WARPS = M256 ? 8 : 4;
+  // Shared memory (all of it dynamic): the k-block ring, 4 KB staging buffers
+  // (32 rows x 128 B, 128B-swizzled) per epilogue warp -- two each, or one
+  // where two would cost the ring its fourth stage -- and the bookkeeping
+  // (barriers, expert offsets, tile prefix).  The ring starts on a 1024-byte
+  // boundary; up to 1 KB of slack is kept for that where it fits, and the
+  // kernel checks the base it is given before it touches anything.
+  static constexpr int BOOK_BYTES = M256 ? 2304 : 1280;
+  static constexpr int SLACK_MIN = M256 ? 0 : 1024;
+  static constexpr int SMEM_BUDGET = 232448 - BOOK_BYTES - SLACK_MIN;
+  static constexpr int RING_IF_TWO = (SMEM_BUDGET - (TMA_OUT ? EPI_WARPS * 2 * 4096 : 0)) / STAGE_BYTES;
   static constexpr int STAGING_BUFS = (TMA_OUT && RING_IF_TWO < 4) ? 1 : 2;
-  static constexpr int STAGING_BYTES = TMA_OUT ? 4 * STAGING_BUFS * 4096 : 0;
+  static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * 4096 : 0;
   static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
+  static constexpr int SMEM_USED = STAGES * STAGE_BYTES + STAGING_BYTES + BOOK_BYTES;
+  static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
   static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of one stage's scales
   // TMEM accumulators: two (epilogue of tile i overlaps MMAs of tile i+1),
-  // or one where two 256-column accumulators would leave no room for scales.
-  static constexpr int ACC_BUFS = (MX && BN == 256) ? 1 : 2;
-  static constexpr int TMEM_COLS_RAW = ACC_BUFS * BN + STAGES * SF_COLS;
+  // or one where two would not fit next to the scales (MXFP8, N=256) or in
+  // 512 columns at all (256-row tiles of N=256: 2 x 256 columns per tile).
+  static constexpr int ACC_COLS = (M256 ? 2 : 1) * BN;
+  static constexpr int ACC_BUFS = ((MX && BN == 256) || 2 * ACC_COLS > 512) ? 1 : 2;
+  static constexpr int TMEM_COLS_RAW = ACC_BUFS * ACC_COLS + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
                                    : TMEM_COLS_RAW <= 128 ? 128 : TMEM_COLS_RAW <= 256 ? 256 : 512;
   // Rows of one K-major B box (the SwiGLU tile loads gate and up halves as two boxes).
@@ -105,14 +119,16 @@ struct GemmCfg {
   static constexpr int B_BOX_ROWS = (EP == Epi::kSwiglu && !MX) ? BN / 2 : BN;
   // Columns of the output a tile covers (SwiGLU: half of the accumulator).
   static constexpr int OUT_COLS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr uint32_t IDESC = MX ? idesc_mxf8_e4m3(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
   static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile: 128 gate + 128 matching up columns");
   static_assert(!MX || (BN % 128 == 0 && !A_MN && !B_MN), "MXFP8 operands are K-major, 128-row scale tiles");
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
-  static_assert(SMEM_BYTES + 2048 <= 232448, "dynamic + static shared memory per CTA");
+  static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
+  static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
+  static_assert(SMEM_USED <= SMEM_BYTES && SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(STAGES >= 2, "pipeline depth");
 };
 
@@ -122,23 +138,63 @@ struct TileInfo {
   int n;         // N tile index
   int num_kb;    // k-blocks
   int k_row0;    // kRoutedK: first contraction row
+  bool half1;    // 256-row tiles: rows m0+128..m0+255 belong to this tile
 };
 
+// 256-row tiles of a routed problem: expert e has ceil(blocks_e / 2) row pairs
+// (blocks of 128 rows) per N tile; s_tpre[e] = tiles of the experts before e.
+__device__ __forceinline__ void build_pair_prefix(const int* s_poff, int E, int n_tiles, int* s_tpre) {
+  // one warp: lane l owns a contiguous run of experts
+  const int lane = threadIdx.x & 31;
+  const int per = (E + 31) / 32;
+  const int e0 = lane * per, e1 = min(E, e0 + per);
+  int sum = 0;
+  for (int e = e0; e < e1; ++e) sum += ((s_poff[e + 1] - s_poff[e]) / 128 + 1) / 2 * n_tiles;
+  int inc = sum;
+  #pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += v;
+  }
+  int run = inc - sum;
+  for (int e = e0; e < e1; ++e) {
+    s_tpre[e] = run;
+    run += ((s_poff[e + 1] - s_poff[e]) / 128 + 1) / 2 * n_tiles;
+  }
+  if (lane == 31) s_tpre[E] = inc;
+}
+
 template <class C>
-__device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_poff) {
+__device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_poff, const int* s_tpre) {
   if constexpr (C::S == Sched::kRoutedM) {
+    if constexpr (C::M256) return s_tpre[p.E];
     return (s_poff[p.E] / C::BM) * p.n_tiles;
   } else if constexpr (C::S == Sched::kDenseM) {
-    return ((p.m_rows + C::BM - 1) / C::BM) * p.n_tiles;
+    return ((p.m_rows + C::TILE_M - 1) / C::TILE_M) * p.n_tiles;
   } else {
     return p.E * p.m_tiles_w * p.n_tiles;
   }
 }
 
 template <class C>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_poff, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_poff, const int* s_tpre, int t) {
   TileInfo ti;
-  if constexpr (C::S == Sched::kRoutedM) {
+  ti.half1 = false;
+  if constexpr (C::S == Sched::kRoutedM && C::M256) {
+    int lo = 0, hi = p.E - 1;          // largest e with s_tpre[e] <= t (a non-empty expert)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tpre[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int local = t - s_tpre[lo];
+    const int mt = ((s_poff[lo + 1] - s_poff[lo]) / 128 + 1) / 2;
+    ti.group = lo;
+    ti.n = local / mt;                       // n outer: a B panel stays hot in L2
+    ti.m0 = s_poff[lo] + (local % mt) * 256;
+    ti.half1 = ti.m0 + 128 < s_poff[lo + 1];
+    ti.num_kb = p.k_len / C::BK;
+    ti.k_row0 = 0;
+  } else if constexpr (C::S == Sched::kRoutedM) {
     // largest e with (poff[e]/BM)*n_tiles <= t; empty experts share a prefix
     // with the next one, so the result is always a non-empty expert.
     int lo = 0, hi = p.E - 1;
@@ -154,10 +210,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     ti.num_kb = p.k_len / C::BK;
     ti.k_row0 = 0;
   } else if constexpr (C::S == Sched::kDenseM) {
-    const int mb = (p.m_rows + C::BM - 1) / C::BM;
+    const int mb = (p.m_rows + C::TILE_M - 1) / C::TILE_M;
     ti.group = 0;
     ti.n = t / mb;
-    ti.m0 = (t % mb) * C::BM;
+    ti.m0 = (t % mb) * C::TILE_M;
+    ti.half1 = C::M256 && (ti.m0 + 128 < p.m_rows);
     ti.num_kb = p.k_len / C::BK;
     ti.k_row0 = 0;
   } else {
@@ -503,7 +560,10 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         for (int j = 0; j < 8; ++j) {
           const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
           const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
-          hw[j] = pack_bf16x2(g * (a0 / (1.0f + expf(-a0))) * b0, g * (a1 / (1.0f + expf(-a1))) * b1);
+          // silu(a) = a / (1 + e^-a) with the fast exponential and divide: their
+          // relative error (~1e-6) is far below the bf16 rounding of h
+          hw[j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
+                              g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
         }
         st.put(2 * q, hw[0], hw[1], hw[2], hw[3]);
         st.put(2 * q + 1, hw[4], hw[5], hw[6], hw[7]);
@@ -585,26 +645,52 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
   }
 }
 
+// Barriers and per-launch tables, kept at the end of dynamic shared memory.
 template <class C>
-__global__ void __launch_bounds__(192, 1)
+struct GemmBook {
+  uint64_t full_bar[C::STAGES];
+  uint64_t empty_bar[C::STAGES];
+  uint64_t tfull_bar[C::ACC_BUFS];
+  uint64_t tempty_bar[C::ACC_BUFS];
+  uint64_t drain_bar;
+  uint32_t tmem_slot;
+  int abort_flag;
+  int bad;
+  int poff[257];
+  int tpre[C::M256 ? 257 : 1];
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                         const GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[C::ACC_BUFS];
-  __shared__ __align__(8) uint64_t tempty_bar[C::ACC_BUFS];
-  __shared__ __align__(8) uint64_t drain_bar;
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
-  __shared__ int s_poff[257];
-
+  static_assert(sizeof(GemmBook<C>) <= C::BOOK_BYTES, "bookkeeping size");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  {
+    // the ring needs a 1024-byte aligned base inside the allocation
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad + C::SMEM_USED > static_cast<uint32_t>(C::SMEM_BYTES)) {
+      if (threadIdx.x == 0) set_status(p.status, kErrLaunch);
+      return;
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_smem = smem;
   uint8_t* b_smem = smem + C::STAGES * C::A_BYTES;
   uint8_t* sf_smem = b_smem + C::STAGES * C::B_BYTES;   // MXFP8 scale tiles (STAGES x (SFA + SFB))
   uint8_t* stage_smem = sf_smem + C::STAGES * (C::SFA_BYTES + C::SFB_BYTES);   // epilogue staging (1 KB aligned)
+  GemmBook<C>& bk = *reinterpret_cast<GemmBook<C>*>(stage_smem + C::STAGING_BYTES);
+  uint64_t* full_bar = bk.full_bar;
+  uint64_t* empty_bar = bk.empty_bar;
+  uint64_t* tfull_bar = bk.tfull_bar;
+  uint64_t* tempty_bar = bk.tempty_bar;
+  uint64_t& drain_bar = bk.drain_bar;
+  uint32_t& tmem_slot = bk.tmem_slot;
+  int& abort_flag = bk.abort_flag;
+  int& s_bad = bk.bad;
+  int* s_poff = bk.poff;
+  int* s_tpre = bk.tpre;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -616,7 +702,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4);
+      mbar_init(&tempty_bar[a], C::EPI_WARPS);
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -626,7 +712,6 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   if (C::S != Sched::kDenseM && p.poffsets != nullptr) {
@@ -652,7 +737,11 @@ __global__ void __launch_bounds__(192, 1)
   if (s_bad) {
     if (threadIdx.x == 0) set_status(p.status, kErrBadIndex);
   }
-  const int ntiles = s_bad ? 0 : total_tiles<C>(p, s_poff);
+  if constexpr (C::M256 && C::S == Sched::kRoutedM) {
+    if (warp == 0 && !s_bad) build_pair_prefix(s_poff, p.E, p.n_tiles, s_tpre);
+    __syncthreads();
+  }
+  const int ntiles = s_bad ? 0 : total_tiles<C>(p, s_poff, s_tpre);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -662,7 +751,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile<C>(p, s_poff, t);
+        const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
@@ -688,10 +777,10 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true, any = false;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile<C>(p, s_poff, t);
+        const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * C::BN;
+        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_ptr)) { ok = false; break; }
           tc_fence_after_sync();
@@ -700,7 +789,7 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (C::MX) {
             // scale tiles of this stage -> TMEM, then 4 MMAs of K=32; MMA kk reads byte kk
             const uint32_t sf_addr = smem_u32(sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES));
-            const uint32_t sfa_t = tmem_base + C::ACC_BUFS * C::BN + stage * C::SF_COLS;
+            const uint32_t sfa_t = tmem_base + C::ACC_BUFS * C::ACC_COLS + stage * C::SF_COLS;
             const uint32_t sfb_t = sfa_t + 4;
             tmem_cp_32x128b_warpx4(sfa_t, smem_desc_plain16(sf_addr));
             #pragma unroll
@@ -720,6 +809,12 @@ __global__ void __launch_bounds__(192, 1)
               const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
                                           : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
               mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (C::M256) {
+                // rows 128..255 of the A tile (16 KB further on) against the same B k-block
+                if (ti.half1)
+                  mma_bf16_ss(d_tmem + C::BN, smem_desc_sw128(a_addr + 16384 + kk * 32, 16, 1024), bd, C::IDESC,
+                              (kb | kk) != 0 ? 1u : 0u);
+              }
             }
           }
           any = true;
@@ -736,17 +831,25 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..5)
-    const int quarter = warp & 3;
+    // ---------------------------------------- epilogue (warps 2 .. 1 + EPI_WARPS)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;          // TMEM lanes a warp may read: 32 * (warp % 4) onwards
+    const int part = ew >> 2;              // 256-row tiles: which 128-row half this warp writes
     int acc = 0;
     uint32_t acc_phase = 0;
-    Stager<C::STAGING_BUFS> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * 4096), 0, lane};
+    Stager<C::STAGING_BUFS> st{stage_smem + ew * (C::STAGING_BUFS * 4096), 0, lane};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile<C>(p, s_poff, t);
+      const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
       tc_fence_after_sync();
-      if constexpr (C::TMA_OUT) {
-        epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::BN, quarter, lane, st, &tmC, &tmC2);
+      if constexpr (C::M256) {
+        if (part == 0 || ti.half1) {
+          TileInfo th = ti;
+          th.m0 += 128 * part;
+          epilogue_tile_tma<C>(p, th, tmem_base + acc * C::ACC_COLS + part * C::BN, quarter, lane, st, &tmC, &tmC2);
+        }
+      } else if constexpr (C::TMA_OUT) {
+        epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::ACC_COLS, quarter, lane, st, &tmC, &tmC2);
       } else {
         epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
       }

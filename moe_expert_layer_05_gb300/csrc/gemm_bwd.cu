@@ -50,8 +50,9 @@ template <int BN>
 cudaError_t dgrad_fc1_bn(const void* dz, int rows_alloc, int F, const void* w1, int E, int H,
                          const int32_t* poffsets, int dense_rows, void* dx_perm, int* status, cudaStream_t st) {
   // B[n=h, k=j] = W1_e[j, h]: W1 seen as [E*2F rows, H cols] (MN-major).
+  constexpr bool M256 = (BN == 256);     // 256-row tiles where two MMAs can share a 256-wide B k-block
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, dz, 2 * F, rows_alloc, 64, 128) ||
+  if (!make_tmap_bf16(&ta, dz, 2 * F, rows_alloc, 64, M256 ? 256 : 128) ||
       !make_tmap_bf16(&tb, w1, H, static_cast<uint64_t>(E) * 2 * F, 64, 64))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
@@ -68,12 +69,12 @@ cudaError_t dgrad_fc1_bn(const void* dz, int rows_alloc, int F, const void* w1, 
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, dx_perm, H, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
-    using C = GemmCfg<BN, false, true, Sched::kRoutedM, Epi::kStoreBf16>;
+    using C = GemmCfg<BN, false, true, Sched::kRoutedM, Epi::kStoreBf16, false, M256>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
     return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
   }
-  using C = GemmCfg<BN, false, true, Sched::kDenseM, Epi::kStoreBf16>;
-  const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
+  using C = GemmCfg<BN, false, true, Sched::kDenseM, Epi::kStoreBf16, false, M256>;
+  const int tiles = ((dense_rows + C::TILE_M - 1) / C::TILE_M) * p.n_tiles;
   return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 

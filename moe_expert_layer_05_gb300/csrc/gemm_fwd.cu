@@ -83,7 +83,7 @@ cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, floa
 cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E, int F, const int32_t* poffsets,
                      int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st) {
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, a, H, rows_alloc, 64, 128) ||
+  if (!make_tmap_bf16(&ta, a, H, rows_alloc, 64, 256) ||
       !make_tmap_bf16(&tb, w1, H, static_cast<uint64_t>(E) * 2 * F, 64, 128))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
@@ -107,12 +107,12 @@ cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E
     return cudaErrorInvalidValue;
   if (z == nullptr) tz = tc;
   if (poffsets != nullptr) {
-    using C = GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwiglu>;
+    using C = GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwiglu, false, true>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
     return launch_gemm<C>(ta, tb, tc, tz, p, upper < num_sms() ? upper : num_sms(), st);
   }
-  using C = GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwiglu>;
-  const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
+  using C = GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwiglu, false, true>;
+  const int tiles = ((dense_rows + 255) / 256) * p.n_tiles;
   return launch_gemm<C>(ta, tb, tc, tz, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 
@@ -120,8 +120,9 @@ namespace {
 template <int BN>
 cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
                    int dense_rows, void* o, int* status, cudaStream_t st) {
+  constexpr bool M256 = (BN == 256);     // 256-row tiles where two MMAs can share a 256-wide B k-block
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, a, F, rows_alloc, 64, 128) ||
+  if (!make_tmap_bf16(&ta, a, F, rows_alloc, 64, M256 ? 256 : 128) ||
       !make_tmap_bf16(&tb, w2, F, static_cast<uint64_t>(E) * H, 64, BN))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
@@ -138,12 +139,12 @@ cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, 
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, o, H, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
-    using C = GemmCfg<BN, false, false, Sched::kRoutedM, Epi::kStoreBf16>;
+    using C = GemmCfg<BN, false, false, Sched::kRoutedM, Epi::kStoreBf16, false, M256>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
     return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
   }
-  using C = GemmCfg<BN, false, false, Sched::kDenseM, Epi::kStoreBf16>;
-  const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
+  using C = GemmCfg<BN, false, false, Sched::kDenseM, Epi::kStoreBf16, false, M256>;
+  const int tiles = ((dense_rows + C::TILE_M - 1) / C::TILE_M) * p.n_tiles;
   return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 }  // namespace

@@ -10,7 +10,8 @@
 namespace moe {
 
 // Device status codes (same values as moe_status in the public header).
-enum : int { kStatusOk = 0, kErrBadIndex = -5, kErrTimeout = -6 };
+// kErrLaunch: a kernel found its launch unusable (shared memory it cannot align).
+enum : int { kStatusOk = 0, kErrLaunch = -3, kErrBadIndex = -5, kErrTimeout = -6 };
 
 // A wait that has not completed after this long is treated as a hang: the
 // kernel records kErrTimeout and unwinds instead of spinning forever.
