@@ -140,11 +140,15 @@ int32_t moe_capacity_rows(const moe_config* cfg);
 moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, moe_act_layout* out);
 
 /* Bytes of scratch workspace every compute call below needs.  Host only.
- * The workspace also holds the device status word; initialise it once with
- * moe_workspace_init before first use. */
+ * The first 256 bytes of the workspace hold the device status word and the
+ * grouped GEMMs' tile counter (ints 32 and 33), which hands out output tiles
+ * in order and is back at zero after every GEMM launch.  Initialise them
+ * once with moe_workspace_init before first use.  Calls that share one
+ * workspace must not overlap on the GPU (issue them on one stream). */
 size_t moe_workspace_bytes(const moe_config* cfg);
 
-/* Clear the device status word of `ws`.  Stream-ordered, does not block. */
+/* Clear the device status word and the tile counter of `ws` (its first 256
+ * bytes).  Stream-ordered, does not block. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, then copy the device status word to *code

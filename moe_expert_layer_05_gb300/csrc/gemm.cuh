@@ -63,6 +63,7 @@ struct GemmParams {
   int sfa_tiles_k;
   int sfb_tiles_k;
   int* status;             // device status word (first error wins)
+  int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
 };
 
 template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false, bool M256_ = false>
@@ -95,7 +96,7 @@ struct GemmCfg {
   // (barriers, expert offsets, tile prefix).  The ring starts on a 1024-byte
   // boundary; up to 1 KB of slack is kept for that where it fits, and the
   // kernel checks the base it is given before it touches anything.
-  static constexpr int BOOK_BYTES = M256 ? 2304 : 1280;
+  static constexpr int BOOK_BYTES = M256 ? 2432 : 1408;
   static constexpr int SLACK_MIN = M256 ? 0 : 1024;
   static constexpr int SMEM_BUDGET = 232448 - BOOK_BYTES - SLACK_MIN;
   static constexpr int RING_IF_TWO = (SMEM_BUDGET - (TMA_OUT ? EPI_WARPS * 2 * 4096 : 0)) / STAGE_BYTES;
@@ -645,9 +646,20 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
   }
 }
 
+// Tiles are handed out in index order from a counter in global memory: the
+// producer takes the next index with one atomicAdd per tile, so tiles that
+// share an expert's weight panel (consecutive indices) start at about the same
+// time on different SMs and the panel is read from HBM once, not once per
+// tile.  The producer passes each index to the MMA and epilogue warps through
+// a small ring in shared memory; -1 ends the list.  The last CTA to finish
+// puts the counter back to zero for the next launch.
+constexpr int kSchedDepth = 4;
+
 // Barriers and per-launch tables, kept at the end of dynamic shared memory.
 template <class C>
 struct GemmBook {
+  uint64_t sched_full[kSchedDepth];
+  uint64_t sched_empty[kSchedDepth];
   uint64_t full_bar[C::STAGES];
   uint64_t empty_bar[C::STAGES];
   uint64_t tfull_bar[C::ACC_BUFS];
@@ -656,9 +668,20 @@ struct GemmBook {
   uint32_t tmem_slot;
   int abort_flag;
   int bad;
+  int sched_tile[kSchedDepth];
   int poff[257];
   int tpre[C::M256 ? 257 : 1];
 };
+
+// Called once per CTA after its producer took its last tile index.
+__device__ __forceinline__ void sched_finish(int* sched) {
+  if (sched == nullptr) return;
+  __threadfence();
+  if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(sched, 0);
+    atomicExch(sched + 1, 0);
+  }
+}
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -671,7 +694,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // the ring needs a 1024-byte aligned base inside the allocation
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     if (pad + C::SMEM_USED > static_cast<uint32_t>(C::SMEM_BYTES)) {
-      if (threadIdx.x == 0) set_status(p.status, kErrLaunch);
+      if (threadIdx.x == 0) {
+        set_status(p.status, kErrLaunch);
+        sched_finish(p.sched);
+      }
       return;
     }
   }
@@ -703,6 +729,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], C::EPI_WARPS);
+    }
+    for (int j = 0; j < kSchedDepth; ++j) {
+      mbar_init(&bk.sched_full[j], 1);
+      mbar_init(&bk.sched_empty[j], 1 + C::EPI_WARPS);   // the MMA thread and every epilogue warp
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -750,7 +780,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      int next = (p.sched != nullptr) ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kSchedDepth;
+        if (!mbar_wait(&bk.sched_empty[slot], ((j / kSchedDepth) & 1) ^ 1u, abort_ptr)) { ok = false; break; }
+        const int t = (next < ntiles) ? next : -1;
+        bk.sched_tile[slot] = t;
+        mbar_arrive(&bk.sched_full[slot]);
+        if (t < 0) break;
+        // the next index is reserved now; its value is first needed one tile later
+        next = (p.sched != nullptr) ? atomicAdd(p.sched, 1) : t + static_cast<int>(gridDim.x);
         const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
@@ -762,6 +801,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      sched_finish(p.sched);
       if (!ok) {
         // unwinding: let every load still in flight land before the CTA exits
         for (int s = 0; s < C::STAGES; ++s)
@@ -776,7 +816,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, any = false;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kSchedDepth;
+        if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr)) { ok = false; break; }
+        const int t = bk.sched_tile[slot];
+        mbar_arrive(&bk.sched_empty[slot]);
+        if (t < 0) break;
         const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
         tc_fence_after_sync();
@@ -838,7 +883,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     Stager<C::STAGING_BUFS> st{stage_smem + ew * (C::STAGING_BUFS * 4096), 0, lane};
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    for (int j = 0;; ++j) {
+      const int slot = j % kSchedDepth;
+      if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr)) break;
+      const int t = bk.sched_tile[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bk.sched_empty[slot]);
+      if (t < 0) break;
       const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
       tc_fence_after_sync();

@@ -33,7 +33,9 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     attr_set = true;
   }
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, tc, tc2, p);
+  GemmParams q = p;
+  q.sched = (p.status != nullptr) ? p.status + kSchedCounterWord : nullptr;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, tc, tc2, q);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -17,6 +17,11 @@ enum : int { kStatusOk = 0, kErrLaunch = -3, kErrBadIndex = -5, kErrTimeout = -6
 // kernel records kErrTimeout and unwinds instead of spinning forever.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// The device status word is the first int of a 256-byte region at the start of
+// the workspace; ints kSchedCounterWord and kSchedCounterWord + 1 of that
+// region are the grouped GEMMs' tile counter (zero between launches).
+constexpr int kSchedCounterWord = 32;
+
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }

@@ -116,8 +116,9 @@ def test_layer_small(lib, name):
 def test_layer_graph_capture_and_determinism(lib):
     """The layer issues no host sync and a fixed launch sequence, so the whole
     forward + backward captures into one CUDA graph; replays give results
-    bit-identical to eager runs (the permutation is a stable counting sort, no
-    atomics decide any order)."""
+    bit-identical to eager runs (the permutation is a stable counting sort; the
+    GEMMs' tile counter decides which SM runs a tile, never how it is
+    computed).  The counter is back at zero after every launch."""
     w = SMALL["qwen3_small"]
     dinp = _to_dev(make_inputs(w, seed=5))
     layer = _layer(w, dinp, True)
@@ -151,6 +152,8 @@ def test_layer_graph_capture_and_determinism(lib):
         assert torch.equal(dgate, dg0)
         assert torch.equal(grads["dw1"], dw10)
     assert api.moe_read_device_status(layer.ws) == 0
+    words = layer.ws[:256].view(torch.int32).cpu()
+    assert int(words[32]) == 0 and int(words[33]) == 0
 
 
 def _full_case(name, n_sample, seed=0):
