@@ -468,8 +468,17 @@ struct Stager {
     if (lane == 0) bulk_wait_group_read<NBUF - 1>();
     __syncwarp();
   }
+  __device__ __forceinline__ void begin_all() {   // every buffer is no longer read by TMA
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  }
   __device__ __forceinline__ void put(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
     const uint32_t base = smem_u32(buf + cur * 4096);
+    st_shared_v4(base + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, cc, d);
+  }
+  // into the buffer after the current one (two buffers filled in one pass)
+  __device__ __forceinline__ void put_next(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
+    const uint32_t base = smem_u32(buf + (cur ^ 1) * 4096);
     st_shared_v4(base + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, cc, d);
   }
   __device__ __forceinline__ void flush(const CUtensorMap* map, int x, int y) {
@@ -524,18 +533,19 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     const int y = ti.m0 + quarter * 32;
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN; c0 += 64) {
+      uint32_t v[4][16];                        // 64 columns in one TMEM round trip
+      #pragma unroll
+      for (int h = 0; h < 4; ++h) tmem_ld_x16(t0 + c0 + 16 * h, v[h]);
+      #pragma unroll
+      for (int h = 0; h < 4; ++h) tmem_ld_wait(v[h]);
       st.begin();
       #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t a[16], b[16];
-        load32(t0 + c0 + 32 * h, a, b);
-        uint32_t w[16];
+      for (int h = 0; h < 4; ++h) {
+        uint32_t w[8];
         #pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
-        #pragma unroll
-        for (int j = 0; j < 8; ++j) w[8 + j] = pack_bf16x2(__uint_as_float(b[2 * j]), __uint_as_float(b[2 * j + 1]));
-        #pragma unroll
-        for (int j = 0; j < 4; ++j) st.put(4 * h + j, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(v[h][2 * j]), __uint_as_float(v[h][2 * j + 1]));
+        st.put(2 * h, w[0], w[1], w[2], w[3]);
+        st.put(2 * h + 1, w[4], w[5], w[6], w[7]);
       }
       st.flush(tmC, ti.n * C::BN + c0, y);
     }
@@ -550,12 +560,23 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     for (int c0 = 0; c0 < C::BN / 2; c0 += 64) {
       st.begin();
       #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t a[16], b[16];
-        tmem_ld_x16(t0 + c0 + 16 * q, a);
-        tmem_ld_x16(t0 + C::BN / 2 + c0 + 16 * q, b);
-        tmem_ld_wait(a);
-        tmem_ld_wait(b);
+      for (int qq = 0; qq < 4; qq += 2) {
+       uint32_t av[2][16], bv[2][16];            // two 16-column groups per TMEM round trip
+       #pragma unroll
+       for (int u = 0; u < 2; ++u) {
+         tmem_ld_x16(t0 + c0 + 16 * (qq + u), av[u]);
+         tmem_ld_x16(t0 + C::BN / 2 + c0 + 16 * (qq + u), bv[u]);
+       }
+       #pragma unroll
+       for (int u = 0; u < 2; ++u) {
+         tmem_ld_wait(av[u]);
+         tmem_ld_wait(bv[u]);
+       }
+       #pragma unroll
+       for (int u = 0; u < 2; ++u) {
+        const int q = qq + u;
+        const uint32_t* a = av[u];
+        const uint32_t* b = bv[u];
         uint32_t hw[8];
         #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -568,6 +589,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         }
         st.put(2 * q, hw[0], hw[1], hw[2], hw[3]);
         st.put(2 * q + 1, hw[4], hw[5], hw[6], hw[7]);
+       }
       }
       st.flush(tmC, col0 + c0, y);
       if (p.c2 != nullptr) {                    // z, saved for backward: gate chunk then up chunk
@@ -591,7 +613,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         }
       }
     }
-  } else {  // kSwigluBwd: dz gate half, then dz up half, per 64-column chunk
+  } else {  // kSwigluBwd: dz gate and up chunks of each 64 columns in one pass
+    static_assert(C::STAGING_BUFS == 2, "the gate and up chunks are staged side by side");
     const int row = ti.m0 + quarter * 32 + lane;
     const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
     const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
@@ -601,46 +624,50 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     float dg = 0.f;
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN; c0 += 64) {
-      #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {   // 0: d(gate input), 1: d(up input)
-        st.begin();
-        #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          const int c = c0 + 16 * q;
-          const uint4* pa = reinterpret_cast<const uint4*>(zrow + c);
-          const uint4* pb = reinterpret_cast<const uint4*>(zrow + p.half_cols + c);
-          const uint4 za0 = pa[0], za1 = pa[1], zb0 = pb[0], zb1 = pb[1];
-          uint32_t v[16];
-          tmem_ld_x16(t0 + c, v);
-          tmem_ld_wait(v);
-          const uint32_t zaw[8] = {za0.x, za0.y, za0.z, za0.w, za1.x, za1.y, za1.z, za1.w};
-          const uint32_t zbw[8] = {zb0.x, zb0.y, zb0.z, zb0.w, zb1.x, zb1.y, zb1.z, zb1.w};
-          uint32_t out[8];
-          #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float o2[2];
-            #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const float av = u ? bf16_hi(zaw[j]) : bf16_lo(zaw[j]);
-              const float bv = u ? bf16_hi(zbw[j]) : bf16_lo(zbw[j]);
-              const float dh = no_mma ? 0.f : __uint_as_float(v[2 * j + u]);
-              const float sg = 1.0f / (1.0f + expf(-av));
-              const float si = av * sg;
-              const float dhg = g * dh;
-              if (half == 0) {
-                dg += dh * si * bv;
-                o2[u] = dhg * bv * sg * (1.0f + av * (1.0f - sg));
-              } else {
-                o2[u] = dhg * si;
-              }
-            }
-            out[j] = pack_bf16x2(o2[0], o2[1]);
-          }
-          st.put(2 * q, out[0], out[1], out[2], out[3]);
-          st.put(2 * q + 1, out[4], out[5], out[6], out[7]);
-        }
-        st.flush(tmC, half * p.half_cols + col0 + c0, y);
+      // this row's saved z for the 64 columns (gate and up), loaded before the TMEM reads
+      uint4 za[8], zb[8];
+      #pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        za[i] = reinterpret_cast<const uint4*>(zrow + c0)[i];
+        zb[i] = reinterpret_cast<const uint4*>(zrow + p.half_cols + c0)[i];
       }
+      st.begin_all();
+      #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[16];
+        tmem_ld_x16(t0 + c0 + 16 * q, v);
+        tmem_ld_wait(v);
+        const uint32_t zaw[8] = {za[2 * q].x, za[2 * q].y, za[2 * q].z, za[2 * q].w,
+                                 za[2 * q + 1].x, za[2 * q + 1].y, za[2 * q + 1].z, za[2 * q + 1].w};
+        const uint32_t zbw[8] = {zb[2 * q].x, zb[2 * q].y, zb[2 * q].z, zb[2 * q].w,
+                                 zb[2 * q + 1].x, zb[2 * q + 1].y, zb[2 * q + 1].z, zb[2 * q + 1].w};
+        uint32_t og[8], ou[8];
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float g2[2], u2[2];
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float av = u ? bf16_hi(zaw[j]) : bf16_lo(zaw[j]);
+            const float bv = u ? bf16_hi(zbw[j]) : bf16_lo(zbw[j]);
+            const float dh = no_mma ? 0.f : __uint_as_float(v[2 * j + u]);
+            // sigmoid with the fast exponential and divide (relative error ~1e-6)
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-av));
+            const float si = av * sg;
+            const float dhg = g * dh;
+            dg += dh * si * bv;
+            g2[u] = dhg * bv * sg * (1.0f + av * (1.0f - sg));   // d(gate input)
+            u2[u] = dhg * si;                                  // d(up input)
+          }
+          og[j] = pack_bf16x2(g2[0], g2[1]);
+          ou[j] = pack_bf16x2(u2[0], u2[1]);
+        }
+        st.put(2 * q, og[0], og[1], og[2], og[3]);
+        st.put(2 * q + 1, og[4], og[5], og[6], og[7]);
+        st.put_next(2 * q, ou[0], ou[1], ou[2], ou[3]);
+        st.put_next(2 * q + 1, ou[4], ou[5], ou[6], ou[7]);
+      }
+      st.flush(tmC, col0 + c0, y);                  // gate chunk (current buffer)
+      st.flush(tmC, p.half_cols + col0 + c0, y);    // up chunk (the next buffer)
     }
     if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * p.n_tiles + ti.n] = dg;
   }
