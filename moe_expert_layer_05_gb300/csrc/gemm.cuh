@@ -66,11 +66,14 @@ struct GemmParams {
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
 };
 
-template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false, bool M256_ = false>
+template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false, bool M256_ = false,
+          bool PAIR_ = false>
 struct GemmCfg {
-  static constexpr int BM = 128;                  // M of one MMA instruction
+  static constexpr int BM = 128;                  // rows of A and D per CTA and MMA
   static constexpr bool M256 = M256_;             // 256-row tiles: two MMAs share each B k-block
-  static constexpr int TILE_M = M256 ? 256 : 128;
+  static constexpr bool PAIR = PAIR_;             // 256-row tiles on a CTA pair (cta_group::2)
+  static constexpr bool ROWS256 = M256 || PAIR;   // tiles of 256 rows (pairs of 128-row blocks)
+  static constexpr int TILE_M = ROWS256 ? 256 : 128;
   static constexpr bool MX = MX_;                 // MXFP8 operands (E4M3 + E8M0 1x32 scales)
   static constexpr int BK = MX ? 128 : 64;        // one 128-byte swizzle row per k-block
   static constexpr int KSTEP = MX ? 32 : 16;      // K of one MMA instruction
@@ -79,8 +82,8 @@ struct GemmCfg {
   static constexpr bool B_MN = B_MN_;
   static constexpr Sched S = S_;
   static constexpr Epi EP = EP_;
-  static constexpr int A_BYTES = TILE_M * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int A_BYTES = (M256 ? 256 : 128) * 128;   // this CTA's A rows of one k-block
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * 128;  // this CTA's B rows (a pair splits N)
   static constexpr int SFA_BYTES = MX ? 512 : 0;
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -96,32 +99,40 @@ struct GemmCfg {
   // (barriers, expert offsets, tile prefix).  The ring starts on a 1024-byte
   // boundary; up to 1 KB of slack is kept for that where it fits, and the
   // kernel checks the base it is given before it touches anything.
-  static constexpr int BOOK_BYTES = M256 ? 2432 : 1408;
-  static constexpr int SLACK_MIN = M256 ? 0 : 1024;
+  static constexpr int BOOK_BYTES = ROWS256 ? 2432 : 1408;
+  static constexpr int SLACK_MIN = ROWS256 ? 0 : 1024;
   static constexpr int SMEM_BUDGET = 232448 - BOOK_BYTES - SLACK_MIN;
   static constexpr int RING_IF_TWO = (SMEM_BUDGET - (TMA_OUT ? EPI_WARPS * 2 * 4096 : 0)) / STAGE_BYTES;
-  static constexpr int STAGING_BUFS = (TMA_OUT && RING_IF_TWO < 4) ? 1 : 2;
+  // Weight gradients are bound by their fp32 stores: each epilogue warp keeps
+  // several 4 KB stores in flight (the k-loops are short, so the ring needs
+  // few stages).
+  static constexpr int WGRAD_BUFS = PAIR ? 6 : 4;
+  static constexpr int STAGING_BUFS = (S == Sched::kRoutedK && TMA_OUT) ? WGRAD_BUFS
+                                      : ((TMA_OUT && RING_IF_TWO < 4) ? 1 : 2);
   static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * 4096 : 0;
-  static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES - (MX ? 1024 : 0)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int SMEM_USED = STAGES * STAGE_BYTES + STAGING_BYTES + BOOK_BYTES;
+  // the scale tiles of all stages, padded so the staging buffers after them
+  // start on a 1024-byte boundary (the 128-byte swizzle of the TMA stores)
+  static constexpr int SF_REGION = (STAGES * (SFA_BYTES + SFB_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int SMEM_USED = STAGES * (A_BYTES + B_BYTES) + SF_REGION + STAGING_BYTES + BOOK_BYTES;
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
   static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of one stage's scales
   // TMEM accumulators: two (epilogue of tile i overlaps MMAs of tile i+1),
   // or one where two would not fit next to the scales (MXFP8, N=256) or in
   // 512 columns at all (256-row tiles of N=256: 2 x 256 columns per tile).
-  static constexpr int ACC_COLS = (M256 ? 2 : 1) * BN;
+  static constexpr int ACC_COLS = (M256 ? 2 : 1) * BN;      // a pair: each CTA holds its 128 rows
   static constexpr int ACC_BUFS = ((MX && BN == 256) || 2 * ACC_COLS > 512) ? 1 : 2;
   static constexpr int TMEM_COLS_RAW = ACC_BUFS * ACC_COLS + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
                                    : TMEM_COLS_RAW <= 128 ? 128 : TMEM_COLS_RAW <= 256 ? 256 : 512;
   // Rows of one K-major B box (the SwiGLU tile loads gate and up halves as two boxes).
   // (MXFP8: W1 is stored with gate and up rows interleaved in 128-row blocks, one box.)
-  static constexpr int B_BOX_ROWS = (EP == Epi::kSwiglu && !MX) ? BN / 2 : BN;
+  static constexpr int B_BOX_ROWS = ((EP == Epi::kSwiglu && !MX) || PAIR) ? BN / 2 : BN;
   // Columns of the output a tile covers (SwiGLU: half of the accumulator).
   static constexpr int OUT_COLS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr uint32_t IDESC = MX ? idesc_mxf8_e4m3(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = MX ? idesc_mxf8_e4m3(BM, BN) : idesc_bf16_f32(PAIR ? 256 : BM, BN, A_MN, B_MN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
   static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile: 128 gate + 128 matching up columns");
@@ -129,8 +140,12 @@ struct GemmCfg {
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
   static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
+  static_assert(!PAIR || (!M256 && !MX && TMA_OUT && BN == 256 &&
+                          (S == Sched::kRoutedK ? (A_MN && B_MN && EP == Epi::kStoreF32) : (!A_MN && !B_MN))),
+                "CTA pairs: bf16, N = 256; K-major row-grouped GEMMs or MN-major weight gradients");
   static_assert(SMEM_USED <= SMEM_BYTES && SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(STAGES >= 2, "pipeline depth");
+  static_assert((STAGES * (A_BYTES + B_BYTES) + SF_REGION) % 1024 == 0, "staging buffers 1024-byte aligned");
 };
 
 struct TileInfo {
@@ -168,7 +183,7 @@ __device__ __forceinline__ void build_pair_prefix(const int* s_poff, int E, int 
 template <class C>
 __device__ __forceinline__ int total_tiles(const GemmParams& p, const int* s_poff, const int* s_tpre) {
   if constexpr (C::S == Sched::kRoutedM) {
-    if constexpr (C::M256) return s_tpre[p.E];
+    if constexpr (C::ROWS256) return s_tpre[p.E];
     return (s_poff[p.E] / C::BM) * p.n_tiles;
   } else if constexpr (C::S == Sched::kDenseM) {
     return ((p.m_rows + C::TILE_M - 1) / C::TILE_M) * p.n_tiles;
@@ -181,7 +196,7 @@ template <class C>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* s_poff, const int* s_tpre, int t) {
   TileInfo ti;
   ti.half1 = false;
-  if constexpr (C::S == Sched::kRoutedM && C::M256) {
+  if constexpr (C::S == Sched::kRoutedM && C::ROWS256) {
     int lo = 0, hi = p.E - 1;          // largest e with s_tpre[e] <= t (a non-empty expert)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -215,14 +230,15 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     ti.group = 0;
     ti.n = t / mb;
     ti.m0 = (t % mb) * C::TILE_M;
-    ti.half1 = C::M256 && (ti.m0 + 128 < p.m_rows);
+    ti.half1 = C::ROWS256 && (ti.m0 + 128 < p.m_rows);
     ti.num_kb = p.k_len / C::BK;
     ti.k_row0 = 0;
   } else {
     const int per = p.m_tiles_w * p.n_tiles;
     ti.group = t / per;
     const int r = t % per;
-    ti.m0 = (r / p.n_tiles) * C::BM;
+    ti.m0 = (r / p.n_tiles) * (C::PAIR ? 256 : C::BM);   // a pair covers 256 output rows
+    ti.half1 = C::PAIR;                                  // (both halves always in range)
     ti.n = r % p.n_tiles;
     if (p.poffsets != nullptr) {
       ti.k_row0 = s_poff[ti.group];
@@ -488,7 +504,7 @@ struct Stager {
       tma_store_2d(map, buf + cur * 4096, x, y);
       bulk_commit_group();
     }
-    cur = (NBUF == 1) ? 0 : cur ^ 1;
+    cur = (cur + 1 == NBUF) ? 0 : cur + 1;
   }
   __device__ __forceinline__ void drain() {
     if (lane == 0) bulk_wait_group_all();
@@ -697,7 +713,7 @@ struct GemmBook {
   int bad;
   int sched_tile[kSchedDepth];
   int poff[257];
-  int tpre[C::M256 ? 257 : 1];
+  int tpre[C::ROWS256 ? 257 : 1];
 };
 
 // Called once per CTA after its producer took its last tile index.
@@ -716,6 +732,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                         const GemmParams p) {
   static_assert(sizeof(GemmBook<C>) <= C::BOOK_BYTES, "bookkeeping size");
+  static_assert(!C::PAIR, "CTA-pair tiles run in grouped_gemm_pair_kernel");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   {
     // the ring needs a 1024-byte aligned base inside the allocation
@@ -732,7 +749,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* a_smem = smem;
   uint8_t* b_smem = smem + C::STAGES * C::A_BYTES;
   uint8_t* sf_smem = b_smem + C::STAGES * C::B_BYTES;   // MXFP8 scale tiles (STAGES x (SFA + SFB))
-  uint8_t* stage_smem = sf_smem + C::STAGES * (C::SFA_BYTES + C::SFB_BYTES);   // epilogue staging (1 KB aligned)
+  uint8_t* stage_smem = sf_smem + C::SF_REGION;   // epilogue staging (1 KB aligned)
   GemmBook<C>& bk = *reinterpret_cast<GemmBook<C>*>(stage_smem + C::STAGING_BYTES);
   uint64_t* full_bar = bk.full_bar;
   uint64_t* empty_bar = bk.empty_bar;
@@ -794,7 +811,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (s_bad) {
     if (threadIdx.x == 0) set_status(p.status, kErrBadIndex);
   }
-  if constexpr (C::M256 && C::S == Sched::kRoutedM) {
+  if constexpr (C::ROWS256 && C::S == Sched::kRoutedM) {
     if (warp == 0 && !s_bad) build_pair_prefix(s_poff, p.E, p.n_tiles, s_tpre);
     __syncthreads();
   }
@@ -946,6 +963,236 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+
+// This CTA's share of one k-block of a pair tile: A rows m0 + 128*rank and
+// half of the B rows (SwiGLU: rank 0 the gate rows, rank 1 the matching up
+// rows), both counted on the even CTA's full barrier.
+template <class C>
+__device__ __forceinline__ void issue_loads_pair(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p,
+                                                 const TileInfo& ti, int kb, uint32_t rank, uint8_t* a_dst,
+                                                 uint8_t* b_dst, uint32_t bar_cluster_addr) {
+  const int k0 = kb * C::BK;
+  if constexpr (C::S == Sched::kRoutedK) {
+    // A[m, k] = Abuf[k_row0 + k, m0 + 128*rank + m], B[n, k] = Bbuf[k_row0 + k, n*BN + 128*rank + n]:
+    // MN-major, two 64-wide chunks each
+    const int mr = ti.m0 + 128 * static_cast<int>(rank);
+    const int nr = ti.n * C::BN + 128 * static_cast<int>(rank);
+    tma_load_2d_pair(a_dst, tmA, bar_cluster_addr, mr, ti.k_row0 + k0);
+    tma_load_2d_pair(a_dst + 8192, tmA, bar_cluster_addr, mr + 64, ti.k_row0 + k0);
+    tma_load_2d_pair(b_dst, tmB, bar_cluster_addr, nr, ti.k_row0 + k0);
+    tma_load_2d_pair(b_dst + 8192, tmB, bar_cluster_addr, nr + 64, ti.k_row0 + k0);
+    return;
+  }
+  tma_load_2d_pair(a_dst, tmA, bar_cluster_addr, k0, ti.m0 + 128 * static_cast<int>(rank));
+  int b_row;
+  if constexpr (C::EP == Epi::kSwiglu)
+    b_row = ti.group * p.b_rows_per_group + ti.n * (C::BN / 2) + (rank ? p.b_half_offset : 0);
+  else
+    b_row = ti.group * p.b_rows_per_group + ti.n * C::BN + static_cast<int>(rank) * (C::BN / 2);
+  tma_load_2d_pair(b_dst, tmB, bar_cluster_addr, k0, b_row);
+}
+
+// The grouped GEMM on CTA pairs (clusters of two, one CTA per SM): each
+// 256 x 256 tile is one chain of tcgen05.mma.cta_group::2 (M = 256, N = 256,
+// K = 16) issued by the even CTA.  Each CTA streams 128 rows of A and 128 rows
+// of B per k-block (32 KB per 512 MMA cycles), holds its 128 x 256 fp32
+// accumulator in its own TMEM -- two of them, so the epilogue of one tile
+// overlaps the MMAs of the next -- and writes its own 128 output rows.
+//
+// Pipeline: full[s] lives in the even CTA and counts both CTAs' TMA bytes;
+// the MMA completion of stage s arrives on empty[s] of both CTAs; the
+// accumulator completion arrives on tfull of both; both CTAs' epilogue warps
+// arrive on the even CTA's tempty.  Waits are bounded as in the one-CTA
+// kernel; both CTAs meet in two cluster barriers (after set-up, before TMEM
+// is freed), which every path reaches.
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
+                             const GemmParams p) {
+  static_assert(C::PAIR, "pair configuration");
+  static_assert(sizeof(GemmBook<C>) <= C::BOOK_BYTES, "bookkeeping size");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(num_clusters_x());
+  {
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad + C::SMEM_USED > static_cast<uint32_t>(C::SMEM_BYTES)) {
+      if (threadIdx.x == 0) set_status(p.status, kErrLaunch);
+      cluster_sync();   // the peer meets both cluster barriers whatever it finds
+      cluster_sync();
+      return;
+    }
+  }
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a_smem = smem;
+  uint8_t* b_smem = smem + C::STAGES * C::A_BYTES;
+  uint8_t* stage_smem = b_smem + C::STAGES * C::B_BYTES;   // epilogue staging (1 KB aligned)
+  GemmBook<C>& bk = *reinterpret_cast<GemmBook<C>*>(stage_smem + C::STAGING_BYTES);
+  uint64_t* full_bar = bk.full_bar;
+  uint64_t* empty_bar = bk.empty_bar;
+  uint64_t* tfull_bar = bk.tfull_bar;
+  uint64_t* tempty_bar = bk.tempty_bar;
+  int* s_poff = bk.poff;
+  int* s_tpre = bk.tpre;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);       // even CTA: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < C::ACC_BUFS; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 2 * C::EPI_WARPS);   // even CTA: the epilogue warps of both CTAs
+    }
+    mbar_init(&bk.drain_bar, 1);
+    bk.abort_flag = 0;
+    bk.bad = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  __syncthreads();
+  if (C::S != Sched::kDenseM && p.poffsets != nullptr) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+      const int v = p.poffsets[i];
+      s_poff[i] = v;
+      const int prev = (i == 0) ? 0 : p.poffsets[i - 1];
+      if ((v & (C::BM - 1)) != 0 || v < prev || v > p.rows_cap || (i == 0 && v != 0)) bk.bad = 1;
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&bk.tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();                       // barriers of both CTAs initialised before any cross-CTA signal
+  tc_fence_after_sync();
+  const uint32_t tmem_base = bk.tmem_slot;
+  volatile int* abort_ptr = &bk.abort_flag;
+  const bool bad = bk.bad != 0;          // both CTAs read the same offsets
+  if (bad && leader && threadIdx.x == 0) set_status(p.status, kErrBadIndex);
+  if constexpr (C::S == Sched::kRoutedM) {
+    if (warp == 0 && !bad) build_pair_prefix(s_poff, p.E, p.n_tiles, s_tpre);
+    __syncthreads();
+  }
+  const int ntiles = bad ? 0 : total_tiles<C>(p, s_poff, s_tpre);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[0]), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = cid; t < ntiles && ok; t += ncl) {
+        const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES);
+          issue_loads_pair<C>(&tmA, &tmB, p, ti, kb, rank, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
+                              full_leader + 8u * stage);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        if (leader) {
+          // unwinding: let every stage still counted on this CTA's barriers land
+          for (int s = 0; s < C::STAGES; ++s)
+            if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
+        } else {
+          // this CTA's loads complete on the peer's barriers: give them time to land
+          const unsigned long long t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (even CTA)
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, any = false;
+      for (int t = cid; t < ntiles && ok; t += ncl) {
+        const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
+        if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_ptr)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
+          const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
+          #pragma unroll
+          for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
+            const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
+                                        : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
+                                        : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            mma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          any = true;
+          mma_commit_pair_both(&empty_bar[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit_pair_both(&tfull_bar[acc]);
+        if (++acc == C::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok && any) {
+        mma_commit_pair(&bk.drain_bar);
+        mbar_wait_drain(&bk.drain_bar, 0);
+      }
+    }
+  } else {
+    // -------------------------------------------------- epilogue (warps 2..5 of both CTAs)
+    const int quarter = warp & 3;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty_bar[0]), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    Stager<C::STAGING_BUFS> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * 4096), 0, lane};
+    for (int t = cid; t < ntiles; t += ncl) {
+      const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
+      tc_fence_after_sync();
+      if (leader || ti.half1) {           // a half tile: the odd CTA's rows are not this expert's
+        TileInfo th = ti;
+        th.m0 += 128 * static_cast<int>(rank);
+        epilogue_tile_tma<C>(p, th, tmem_base + acc * C::ACC_COLS, quarter, lane, st, &tmC, &tmC2);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
+      if (++acc == C::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
+    }
+    st.drain();
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();                       // the peer no longer reads this CTA's memory or signals its barriers
+  if (threadIdx.x == 0 && bk.abort_flag) set_status(p.status, kErrTimeout);
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }
 }
 

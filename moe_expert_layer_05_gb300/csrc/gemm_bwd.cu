@@ -99,6 +99,16 @@ cudaError_t wgrad_bn(const void* a, int M, const void* b, int N, int rows_alloc,
   p.status = status;
   CUtensorMap tc;
   if (!make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M)) return cudaErrorInvalidValue;
+  if constexpr (BN == 256) {
+    if (M % 256 == 0) {
+      // 256 x 256 tiles on CTA pairs: each SM loads half of A and half of B
+      // per k-block, so the loads keep up with the MMAs and the fp32 stores
+      // (the bulk of the traffic) set the pace.
+      using C = GemmCfg<BN, true, true, Sched::kRoutedK, Epi::kStoreF32, false, false, true>;
+      p.m_tiles_w = M / 256;
+      return launch_gemm_pair<C>(ta, tb, tc, tc, p, p.E * p.m_tiles_w * p.n_tiles, st);
+    }
+  }
   using C = GemmCfg<BN, true, true, Sched::kRoutedK, Epi::kStoreF32>;
   const int tiles = p.E * p.m_tiles_w * p.n_tiles;
   return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);

@@ -40,6 +40,42 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return cudaGetLastError();
 }
 
+// Launch of the CTA-pair kernel: clusters of two, as many as can be resident
+// at once (queried once per configuration), never more than tiles_upper.
+template <class C>
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                             const CUtensorMap& tc2, const GemmParams& p, int tiles_upper, cudaStream_t st) {
+  static int max_clusters = 0;
+  auto kern = grouped_gemm_pair_kernel<C>;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_clusters = n;
+  }
+  if (tiles_upper <= 0) return cudaSuccess;
+  const int clusters = tiles_upper < max_clusters ? tiles_upper : max_clusters;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tc2, p);
+  count_launches(1);
+  return e;
+}
+
 // Output map for the TMA-store epilogue: boxes of 128 bytes x 32 rows, 128B swizzle.
 inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 64, 32);
