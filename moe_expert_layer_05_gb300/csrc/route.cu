@@ -173,18 +173,29 @@ __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* 
                                                                    int k, int score, int32_t* __restrict__ idx,
                                                                    float* __restrict__ gate,
                                                                    int32_t* __restrict__ hist) {
+  constexpr int kStageFloats = 8192;             // logits of the chunk staged in shared memory (32 KB)
   __shared__ int s_idx[kPairsPerBlock];
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
+  __shared__ float s_logit[kStageFloats];
   const int tpb = kPairsPerBlock / k;            // tokens of this chunk
   const int t0 = blockIdx.x * tpb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The chunk's logits are one contiguous range: read it with the whole block
+  // (many loads in flight) instead of one row at a time per warp.
+  const int nt = min(tpb, T - t0);
+  const bool staged = nt * E <= kStageFloats;
+  if (staged) {
+    const float* src = logits + (long long)t0 * E;
+    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) s_logit[i] = __ldg(src + i);
+    __syncthreads();
+  }
   for (int u = warp; u < tpb; u += 8) {
     const int t = t0 + u;
     if (t >= T) break;
     int id;
     float g;
-    topk_one_token<PER_LANE>(logits + (long long)t * E, bias, E, k, score, lane, id, g);
+    topk_one_token<PER_LANE>(staged ? s_logit + u * E : logits + (long long)t * E, bias, E, k, score, lane, id, g);
     if (lane < k) {
       idx[(long long)t * k + lane] = id;
       gate[(long long)t * k + lane] = g;
@@ -466,45 +477,60 @@ __global__ void __launch_bounds__(128) dgrad_combine_kernel(
   }
 }
 
-// grid (E, H/1024): each thread owns 8 columns, walks the expert's rows.
-__global__ void __launch_bounds__(128) router_wgrad_kernel(const uint4* __restrict__ x_perm,
+// dWr[e] = sum over the rows r of expert e of dl_r * x_perm[r]: grid (E, H/256).
+__global__ void __launch_bounds__(256) router_wgrad_kernel(const uint4* __restrict__ x_perm,
                                                            const float* __restrict__ row_dlogit,
                                                            const int32_t* __restrict__ counts,
                                                            const int32_t* __restrict__ poffsets, int vec_per_row,
                                                            float* __restrict__ dw) {
+  // Block (e, b): 256 columns of dWr[e] (lane = 8 columns); warp w sums the
+  // rows w, w+8, w+16, ... of expert e; the eight partial sums are then added
+  // in warp order, so the result does not depend on scheduling.
+  __shared__ float part[8][256];
   const int e = blockIdx.x;
-  const int v = blockIdx.y * blockDim.x + threadIdx.x;
-  if (v >= vec_per_row) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v = blockIdx.y * 32 + lane;
+  const bool active = v < vec_per_row;
   const int r0 = poffsets[e], n = counts[e];
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  int r = 0;
-  for (; r + 4 <= n; r += 4) {
-    uint4 xv[4];
-    float d[4];
-    #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      xv[u] = __ldg(x_perm + (long long)(r0 + r + u) * vec_per_row + v);
-      d[u] = row_dlogit[r0 + r + u];
+  const uint4* xcol = x_perm + (long long)r0 * vec_per_row + v;
+  int r = warp;
+  if (active) {
+    for (; r + 24 < n; r += 32) {
+      uint4 xv[4];
+      float d[4];
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        xv[u] = __ldg(xcol + (long long)(r + 8 * u) * vec_per_row);
+        d[u] = __ldg(row_dlogit + r0 + r + 8 * u);
+      }
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[0] += d[u] * bf16_lo(xv[u].x); acc[1] += d[u] * bf16_hi(xv[u].x);
+        acc[2] += d[u] * bf16_lo(xv[u].y); acc[3] += d[u] * bf16_hi(xv[u].y);
+        acc[4] += d[u] * bf16_lo(xv[u].z); acc[5] += d[u] * bf16_hi(xv[u].z);
+        acc[6] += d[u] * bf16_lo(xv[u].w); acc[7] += d[u] * bf16_hi(xv[u].w);
+      }
     }
-    #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc[0] += d[u] * bf16_lo(xv[u].x); acc[1] += d[u] * bf16_hi(xv[u].x);
-      acc[2] += d[u] * bf16_lo(xv[u].y); acc[3] += d[u] * bf16_hi(xv[u].y);
-      acc[4] += d[u] * bf16_lo(xv[u].z); acc[5] += d[u] * bf16_hi(xv[u].z);
-      acc[6] += d[u] * bf16_lo(xv[u].w); acc[7] += d[u] * bf16_hi(xv[u].w);
+    for (; r < n; r += 8) {
+      const uint4 xv = __ldg(xcol + (long long)r * vec_per_row);
+      const float d = __ldg(row_dlogit + r0 + r);
+      acc[0] += d * bf16_lo(xv.x); acc[1] += d * bf16_hi(xv.x);
+      acc[2] += d * bf16_lo(xv.y); acc[3] += d * bf16_hi(xv.y);
+      acc[4] += d * bf16_lo(xv.z); acc[5] += d * bf16_hi(xv.z);
+      acc[6] += d * bf16_lo(xv.w); acc[7] += d * bf16_hi(xv.w);
     }
   }
-  for (; r < n; ++r) {
-    const uint4 xv = __ldg(x_perm + (long long)(r0 + r) * vec_per_row + v);
-    const float d = row_dlogit[r0 + r];
-    acc[0] += d * bf16_lo(xv.x); acc[1] += d * bf16_hi(xv.x);
-    acc[2] += d * bf16_lo(xv.y); acc[3] += d * bf16_hi(xv.y);
-    acc[4] += d * bf16_lo(xv.z); acc[5] += d * bf16_hi(xv.z);
-    acc[6] += d * bf16_lo(xv.w); acc[7] += d * bf16_hi(xv.w);
+  #pragma unroll
+  for (int j = 0; j < 8; ++j) part[warp][lane * 8 + j] = acc[j];
+  __syncthreads();
+  const int c = threadIdx.x;                     // column of this block's 256
+  if (blockIdx.y * 256 + c < vec_per_row * 8) {
+    float sum = 0.f;
+    #pragma unroll
+    for (int w = 0; w < 8; ++w) sum += part[w][c];
+    dw[(long long)e * vec_per_row * 8 + blockIdx.y * 256 + c] = sum;
   }
-  float4* out = reinterpret_cast<float4*>(dw + (long long)e * vec_per_row * 8 + (long long)v * 8);
-  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 }  // namespace
@@ -613,8 +639,8 @@ cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, c
 cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, const int32_t* counts,
                                 const int32_t* poffsets, int E, int H, float* dw_router, cudaStream_t st) {
   const int vpr = H / 8;
-  dim3 grid(E, (vpr + 127) / 128);
-  router_wgrad_kernel<<<grid, 128, 0, st>>>(static_cast<const uint4*>(x_perm), row_dlogit, counts, poffsets, vpr,
+  dim3 grid(E, (vpr + 31) / 32);
+  router_wgrad_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x_perm), row_dlogit, counts, poffsets, vpr,
                                             dw_router);
   count_launches(1);
   return cudaGetLastError();
