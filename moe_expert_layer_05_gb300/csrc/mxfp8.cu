@@ -34,6 +34,13 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// 2^-e as a float, e in [-127, 127] (2^-127 is subnormal).  Multiplying by a
+// power of two is exact except where the product is subnormal, and there it
+// rounds once to nearest even, exactly like scaling by 2^-e.
+__device__ __forceinline__ float pow2_neg(int e) {
+  return e < 127 ? __int_as_float((127 - e) << 23) : __int_as_float(0x00400000);
+}
+
 __device__ __forceinline__ size_t sf_offset(int r, int b, int tiles_per_row) {
   return (static_cast<size_t>(r >> 7) * tiles_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 +
          (b & 3);
@@ -45,11 +52,12 @@ __device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst
   #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const int e = mx_exponent(amax);
+  const float sc = pow2_neg(e);
   uint32_t w[8];
   #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint16_t lo = cvt_e4m3x2(ldexpf(v[4 * i + 0], -e), ldexpf(v[4 * i + 1], -e));
-    const uint16_t hi = cvt_e4m3x2(ldexpf(v[4 * i + 2], -e), ldexpf(v[4 * i + 3], -e));
+    const uint16_t lo = cvt_e4m3x2(v[4 * i + 0] * sc, v[4 * i + 1] * sc);
+    const uint16_t hi = cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc);
     w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -70,7 +78,9 @@ __device__ __forceinline__ long long gate_up_row(long long r, int half) {
   return g * 2 * half + (jj / 128) * 256 + up * 128 + (jj % 128);
 }
 
-// Blocks along the row: src [rows, cols] bf16 -> codes [rows, cols], scales tiled.
+// Blocks along the row: src [rows, cols] bf16 -> codes [rows, cols], scales
+// tiled.  One thread per 32-value block: four 16-byte loads, two 16-byte
+// stores of codes, one scale byte.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ src, long long rows, int cols,
                                                             int half, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf) {
@@ -79,16 +89,18 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
   if (i >= rows * nb) return;
   const long long r_in = i / nb;
   const long long r = gate_up_row(r_in, half);
-  const int b = static_cast<int>(i % nb);
-  const uint4* p = src + (r_in * cols + b * 32) / 8;
+  const int b = static_cast<int>(i - r_in * nb);
+  const uint4* p = src + i * 4;
+  uint4 u[4];
+  #pragma unroll
+  for (int q = 0; q < 4; ++q) u[q] = __ldg(p + q);
   float v[32];
   #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 u = p[q];
-    v[8 * q + 0] = bf16_lo(u.x); v[8 * q + 1] = bf16_hi(u.x);
-    v[8 * q + 2] = bf16_lo(u.y); v[8 * q + 3] = bf16_hi(u.y);
-    v[8 * q + 4] = bf16_lo(u.z); v[8 * q + 5] = bf16_hi(u.z);
-    v[8 * q + 6] = bf16_lo(u.w); v[8 * q + 7] = bf16_hi(u.w);
+    v[8 * q + 0] = bf16_lo(u[q].x); v[8 * q + 1] = bf16_hi(u[q].x);
+    v[8 * q + 2] = bf16_lo(u[q].y); v[8 * q + 3] = bf16_hi(u[q].y);
+    v[8 * q + 4] = bf16_lo(u[q].z); v[8 * q + 5] = bf16_hi(u[q].z);
+    v[8 * q + 6] = bf16_lo(u[q].w); v[8 * q + 7] = bf16_hi(u[q].w);
   }
   const uint8_t s = quantize32(v, codes + r * cols + b * 32);
   sf[sf_offset(static_cast<int>(r), b, cols / 128)] = s;
@@ -97,18 +109,33 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // Blocks along the column, output transposed: src [rows, cols] bf16 ->
 // codes [cols, rows] (row c of the output = column c of the input), scales
 // tiled over the [cols, rows] output.  batch: independent matrices one after
-// another (expert weights).
+// another (expert weights).  A block reads a 32-row x 256-column tile with
+// 16-byte loads into shared memory, then thread c quantises column c of it.
+// blockIdx.x runs over the 32-row blocks so that neighbouring blocks write
+// neighbouring 32-byte pieces of the same output rows.
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
                                                             int cols, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  const int rb = blockIdx.y;                 // block of 32 input rows
+  __shared__ uint4 tile[32][32];           // 32 rows x 256 bf16
+  const int rb = blockIdx.x;               // block of 32 input rows
+  const int c0 = blockIdx.y * 256;
   const long long mat = blockIdx.z;
+  const __nv_bfloat16* base = src + mat * rows * cols + static_cast<long long>(rb) * 32 * cols;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  #pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = warp * 4 + k;
+    const int c = c0 + lane * 8;
+    tile[r][lane] = (c < cols) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * cols + c))
+                               : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  const int c = c0 + threadIdx.x;
   if (c >= cols) return;
-  const __nv_bfloat16* s = src + mat * rows * cols + static_cast<long long>(rb) * 32 * cols + c;
+  const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + threadIdx.x;
   float v[32];
   #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(s[static_cast<long long>(i) * cols]);
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(col[i * 256]);
   uint8_t* out = codes + mat * rows * cols + static_cast<long long>(c) * rows + rb * 32;
   const uint8_t e = quantize32(v, out);
   sf[mat * (static_cast<long long>(rows) * cols / 32) + sf_offset(c, rb, rows / 128)] = e;
@@ -129,7 +156,7 @@ cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int 
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
                                  cudaStream_t st) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  dim3 grid((cols + 255) / 256, rows / 32, batch);
+  dim3 grid(rows / 32, (cols + 255) / 256, batch);
   quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, sf);
   count_launches(1);
   return cudaGetLastError();

@@ -77,9 +77,10 @@ def test_quantize_rows(lib, R, C, scale):
     np.testing.assert_array_equal(untile(sf, R, C), os_)
 
 
-@pytest.mark.parametrize("B,R,C", [(1, 256, 384), (3, 128, 256), (2, 512, 128)])
-def test_quantize_cols_transposed(lib, B, R, C):
-    x = to_bf16(_rand((B, R, C), 7 + B))
+@pytest.mark.parametrize("B,R,C,scale", [(1, 256, 384, 1.0), (3, 128, 256, 1.0), (2, 512, 128, 1.0),
+                                         (1, 128, 640, 1e-30), (1, 256, 128, 1e30)])
+def test_quantize_cols_transposed(lib, B, R, C, scale):
+    x = to_bf16(_rand((B, R, C), 7 + B) * np.float32(scale))
     codes, sf = quantize_gpu(x.to(DEV), api.MX_COLS_T, batch=B)
     torch.cuda.synchronize()
     codes = codes.cpu().numpy().reshape(B, C, R)
