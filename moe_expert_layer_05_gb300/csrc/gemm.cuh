@@ -108,6 +108,7 @@ struct GemmCfg {
   // few stages).
   static constexpr int WGRAD_BUFS = PAIR ? 6 : 4;
   static constexpr int STAGING_BUFS = (S == Sched::kRoutedK && TMA_OUT) ? WGRAD_BUFS
+                                      : (EP == Epi::kSwigluBwd) ? 2    // gate and up chunks side by side
                                       : ((TMA_OUT && RING_IF_TWO < 4) ? 1 : 2);
   static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * 4096 : 0;
   static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES - (MX ? 1024 : 0)) / STAGE_BYTES;
@@ -141,8 +142,8 @@ struct GemmCfg {
   static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
   static_assert(!PAIR || (!M256 && !MX && TMA_OUT && BN == 256 &&
-                          (S == Sched::kRoutedK ? (A_MN && B_MN && EP == Epi::kStoreF32) : (!A_MN && !B_MN))),
-                "CTA pairs: bf16, N = 256; K-major row-grouped GEMMs or MN-major weight gradients");
+                          (S == Sched::kRoutedK ? (A_MN && B_MN && EP == Epi::kStoreF32) : !A_MN)),
+                "CTA pairs: bf16, N = 256; row-grouped GEMMs with K-major A, or MN-major weight gradients");
   static_assert(SMEM_USED <= SMEM_BYTES && SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(STAGES >= 2, "pipeline depth");
   static_assert((STAGES * (A_BYTES + B_BYTES) + SF_REGION) % 1024 == 0, "staging buffers 1024-byte aligned");
@@ -637,6 +638,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     const int col0 = ti.n * C::BN;
     const __nv_bfloat16* zrow = p.aux + (long long)(row_ok ? row : 0) * p.ld_aux + col0;
     const int y = ti.m0 + quarter * 32;
+    const int parts = p.n_tiles * (C::BN / 128);   // partials per row: one per 128 columns of dh
     float dg = 0.f;
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN; c0 += 64) {
@@ -684,8 +686,12 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
       }
       st.flush(tmC, col0 + c0, y);                  // gate chunk (current buffer)
       st.flush(tmC, p.half_cols + col0 + c0, y);    // up chunk (the next buffer)
+      if ((c0 & 127) == 64) {                       // one partial <dh, silu(a) b> per 128 columns
+        if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * parts + (col0 + c0) / 128] = dg;
+        dg = 0.f;
+      }
     }
-    if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * p.n_tiles + ti.n] = dg;
+
   }
 }
 
@@ -987,6 +993,13 @@ __device__ __forceinline__ void issue_loads_pair(const CUtensorMap* tmA, const C
     return;
   }
   tma_load_2d_pair(a_dst, tmA, bar_cluster_addr, k0, ti.m0 + 128 * static_cast<int>(rank));
+  if constexpr (C::B_MN) {
+    // B[n, k] = W[group*K + k, n]: this CTA's 128 columns of N, two 64-wide chunks
+    const int nr = ti.n * C::BN + 128 * static_cast<int>(rank);
+    tma_load_2d_pair(b_dst, tmB, bar_cluster_addr, nr, ti.group * p.b_rows_per_group + k0);
+    tma_load_2d_pair(b_dst + 8192, tmB, bar_cluster_addr, nr + 64, ti.group * p.b_rows_per_group + k0);
+    return;
+  }
   int b_row;
   if constexpr (C::EP == Epi::kSwiglu)
     b_row = ti.group * p.b_rows_per_group + ti.n * (C::BN / 2) + (rank ? p.b_half_offset : 0);

@@ -9,12 +9,18 @@
 
 namespace moe {
 
-cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
-                           const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate,
-                           void* dz, float* dgate_part, int* status, cudaStream_t st) {
+namespace {
+template <int BN>
+cudaError_t dgrad_fc2_bn(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
+                         const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate, void* dz,
+                         float* dgate_part, int* status, cudaStream_t st) {
   // B[n=f, k=h] = W2_e[h, f]: W2 seen as [E*H rows, F cols], N contiguous (MN-major).
+  // N = 256: 256 x 256 tiles on CTA pairs (half of A and of B per SM, six
+  // stages, double-buffered accumulators).  N = 128: 256-row tiles on one CTA,
+  // two MMAs sharing each B k-block.
+  constexpr bool PAIR = (BN == 256);
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, dy_perm, H, rows_alloc, 64, 128) ||
+  if (!make_tmap_bf16(&ta, dy_perm, H, rows_alloc, 64, PAIR ? 128 : 256) ||
       !make_tmap_bf16(&tb, w2, F, static_cast<uint64_t>(E) * H, 64, 64))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
@@ -22,7 +28,7 @@ cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const voi
   p.E = E;
   p.m_rows = dense_rows;
   p.k_len = H;
-  p.n_tiles = F / 128;
+  p.n_tiles = F / BN;
   p.b_rows_per_group = H;
   p.c = dz;
   p.ldc = 2 * F;
@@ -36,13 +42,27 @@ cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const voi
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
   if (poffsets != nullptr) {
-    using C = GemmCfg<128, false, true, Sched::kRoutedM, Epi::kSwigluBwd>;
+    using C = GemmCfg<BN, false, true, Sched::kRoutedM, Epi::kSwigluBwd, false, !PAIR, PAIR>;
     const int upper = (rows_alloc / 128) * p.n_tiles;
-    return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
+    if constexpr (PAIR) return launch_gemm_pair<C>(ta, tb, tc, tc, p, upper, st);
+    else return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
   }
-  using C = GemmCfg<128, false, true, Sched::kDenseM, Epi::kSwigluBwd>;
-  const int tiles = ((dense_rows + 127) / 128) * p.n_tiles;
-  return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
+  using C = GemmCfg<BN, false, true, Sched::kDenseM, Epi::kSwigluBwd, false, !PAIR, PAIR>;
+  const int tiles = ((dense_rows + C::TILE_M - 1) / C::TILE_M) * p.n_tiles;
+  if constexpr (PAIR) return launch_gemm_pair<C>(ta, tb, tc, tc, p, tiles, st);
+  else return launch_gemm<C>(ta, tb, tc, tc, p, tiles < num_sms() ? tiles : num_sms(), st);
+}
+}  // namespace
+
+// dgate_part gets one partial sum per 128 columns of dh whatever the tile width.
+cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
+                           const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate,
+                           void* dz, float* dgate_part, int* status, cudaStream_t st) {
+  if (F % 256 == 0)
+    return dgrad_fc2_bn<256>(dy_perm, rows_alloc, H, w2, E, F, poffsets, dense_rows, z, row_gate, dz, dgate_part,
+                             status, st);
+  return dgrad_fc2_bn<128>(dy_perm, rows_alloc, H, w2, E, F, poffsets, dense_rows, z, row_gate, dz, dgate_part,
+                           status, st);
 }
 
 namespace {
