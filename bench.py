@@ -421,6 +421,53 @@ def run_ours(args) -> dict | None:
     return out
 
 
+PROFILE_OPS = ("fc1", "fc2", "dgrad_fc2", "dgrad_fc1", "wgrad_fc1", "wgrad_fc2")
+
+
+def profile_op(args) -> dict:
+    """One untimed step of the workload, then one grouped GEMM of it between
+    cudaProfilerStart and cudaProfilerStop, for `ncu --profile-from-start off`
+    captures.  bf16 workloads only."""
+    from moe_expert_layer_05_gb300 import api
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = dataclasses.replace(w, T=args.tokens)
+    if args.experts is not None:
+        w = dataclasses.replace(w, E=args.experts)
+    if w.dtype != "bf16":
+        raise SystemExit("--profile-op: bf16 workloads only")
+    bwd = args.profile_op not in ("fc1", "fc2")
+    d = make_inputs_on_device(w, dev, seed=0, with_dy=bwd)
+    layer = api.MoELayer(api.config_of(w), d, with_backward=True)
+    layer.forward(d["x"])
+    grads = layer.backward(d["x"], d["dy"])[2] if bwd else None
+    torch.cuda.synchronize()
+    fl, c, ws = layer.fields(), layer.cfg, layer.ws
+    po = fl["poffsets"]
+    calls = {
+        "fc1": lambda: api.moe_grouped_gemm(c, api.GG_FC1_SWIGLU, fl["x_perm"], d["w1"], fl["h"], ws, c2=fl["z"],
+                                            row_gate=fl["row_gate"], poffsets=po),
+        "fc2": lambda: api.moe_grouped_gemm(c, api.GG_FC2, fl["h"], d["w2"], fl["o"], ws, poffsets=po),
+        "dgrad_fc2": lambda: api.moe_grouped_gemm(c, api.GG_DGRAD_FC2, fl["dy_perm"], d["w2"], fl["dz"], ws,
+                                                  aux=fl["z"], row_gate=fl["row_gate"], poffsets=po),
+        "dgrad_fc1": lambda: api.moe_grouped_gemm(c, api.GG_DGRAD_FC1, fl["dz"], d["w1"], fl["dx_perm"], ws,
+                                                  poffsets=po),
+        "wgrad_fc1": lambda: api.moe_grouped_gemm(c, api.GG_WGRAD_FC1, fl["dz"], fl["x_perm"], grads["dw1"], ws,
+                                                  poffsets=po),
+        "wgrad_fc2": lambda: api.moe_grouped_gemm(c, api.GG_WGRAD_FC2, fl["dy_perm"], fl["h"], grads["dw2"], ws,
+                                                  poffsets=po),
+    }
+    torch.cuda.profiler.start()
+    calls[args.profile_op]()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    return {"profile_op": args.profile_op, "workload": args.workload, "T": w.T, "E": w.E,
+            "status": api.moe_read_device_status(ws),
+            "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
+
+
 def e2e_pipelined(api, w, layer, x, y, dy, grads, stream, K, no_graph, dev):
     """K steps through the public API with host buffers: returns (ms for all K
     steps, host->device bytes per step, device->host bytes per step)."""
@@ -579,10 +626,16 @@ def main():
                     help="override T (smaller cases for profiler captures; not a bench line)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller cases for profiler captures; not a bench line)")
+    ap.add_argument("--profile-op", choices=sorted(PROFILE_OPS), default=None,
+                    help="for profiler captures: one untimed step, then this grouped GEMM once inside "
+                         "cudaProfilerStart/Stop (ncu --profile-from-start off); prints one JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.profile_op is not None:
+        out = profile_op(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
     world, _, _ = dist_env()
