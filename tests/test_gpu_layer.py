@@ -238,3 +238,37 @@ def test_few_tiles_long_k_is_deterministic(lib):
     for o in outs[1:]:
         assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
     assert api.moe_read_device_status(layer.ws) == 0
+
+
+def test_router_replay_reproduces_the_layer_permutation(lib):
+    """Router replay: the routing a layer forward recorded (topk_idx, gates) is
+    fed back to moe_permute, which must rebuild the same expert-ordered batch
+    bit for bit (maps, gates per row, x_perm), with no router call."""
+    w = SMALL["dsv3_small"]
+    dinp = _to_dev(make_inputs(w, seed=21))
+    layer = _layer(w, dinp, True)
+    layer.forward(dinp["x"])
+    torch.cuda.synchronize()
+    fl = layer.fields()
+    cfg = layer.cfg
+    cap = api.moe_capacity_rows(cfg)
+    E = w.E
+    got = {"counts": torch.empty(E, dtype=torch.int32, device=DEV),
+           "offsets": torch.empty(E + 1, dtype=torch.int32, device=DEV),
+           "poffsets": torch.empty(E + 1, dtype=torch.int32, device=DEV),
+           "slot_row": torch.empty_like(fl["slot_row"]),
+           "row_src": torch.full((cap,), -7, dtype=torch.int32, device=DEV),
+           "row_gate": torch.empty(cap, dtype=torch.float32, device=DEV),
+           "x_perm": torch.empty((cap, w.H), dtype=torch.bfloat16, device=DEV)}
+    ws = torch.zeros(max(api.moe_workspace_bytes(cfg), 256), dtype=torch.uint8, device=DEV)
+    api.moe_workspace_init(ws)
+    api.moe_permute(cfg, dinp["x"], fl["topk_idx"].clone(), fl["topk_gate"].clone(), got["counts"], got["offsets"],
+                    got["poffsets"], got["slot_row"], got["row_src"], got["row_gate"], got["x_perm"], 1, ws)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(ws) == 0
+    used = int(fl["poffsets"][-1])
+    for name in ("counts", "offsets", "poffsets", "slot_row"):
+        assert torch.equal(got[name], fl[name]), name
+    assert torch.equal(got["row_src"][:used], fl["row_src"][:used])
+    assert torch.equal(got["row_gate"][:used], fl["row_gate"][:used])
+    assert torch.equal(got["x_perm"][:used].view(torch.int16), fl["x_perm"][:used].view(torch.int16))
