@@ -227,13 +227,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
   const bool active = e < E;
   const int per = (NB + G - 1) / G;
   const int b0 = min(NB, g * per), b1 = min(NB, b0 + per);
+  // Both passes over this lane's chunks load 8 entries at a time: the loads of
+  // a batch are independent, so their latencies overlap.
+  constexpr int kBatch = 8;
   int sum = 0;
   if (active) {
     int b = b0;
-    for (; b + 4 <= b1; b += 4) {
-      const int v0 = hist[(long long)b * E + e], v1 = hist[(long long)(b + 1) * E + e];
-      const int v2 = hist[(long long)(b + 2) * E + e], v3 = hist[(long long)(b + 3) * E + e];
-      sum += v0 + v1 + v2 + v3;
+    for (; b + kBatch <= b1; b += kBatch) {
+      int v[kBatch];
+      #pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = hist[(long long)(b + j) * E + e];
+      #pragma unroll
+      for (int j = 0; j < kBatch; ++j) sum += v[j];
     }
     for (; b < b1; ++b) sum += hist[(long long)b * E + e];
   }
@@ -273,7 +278,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
   __syncthreads();
   if (active) {
     int run = s_poff[e] + inc - sum;
-    for (int b = b0; b < b1; ++b) {
+    int b = b0;
+    for (; b + kBatch <= b1; b += kBatch) {
+      int v[kBatch];
+      #pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = hist[(long long)(b + j) * E + e];
+      #pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        hist[(long long)(b + j) * E + e] = run;
+        run += v[j];
+      }
+    }
+    for (; b < b1; ++b) {
       const long long i = (long long)b * E + e;
       const int c = hist[i];
       hist[i] = run;
