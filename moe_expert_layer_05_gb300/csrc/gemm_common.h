@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "gemm.cuh"
@@ -22,15 +23,25 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, u
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, box_inner, box_outer);
 }
 
+// Per-device, per-kernel launch set-up state (function attributes are per
+// device; the cluster occupancy is a property of the device too).
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int d = -1;
+  return (cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices) ? d : -1;
+}
+
 template <class C>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                         const GemmParams& p, int grid, cudaStream_t st) {
-  static bool attr_set = false;
+  static std::atomic<bool> attr_set[kMaxDevices];
   auto kern = grouped_gemm_kernel<C>;
-  if (!attr_set) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   if (grid <= 0) return cudaSuccess;
   GemmParams q = p;
@@ -45,8 +56,11 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 template <class C>
 cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                              const CUtensorMap& tc2, const GemmParams& p, int tiles_upper, cudaStream_t st) {
-  static int max_clusters = 0;
+  static std::atomic<int> max_clusters_of[kMaxDevices];
   auto kern = grouped_gemm_pair_kernel<C>;
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int max_clusters = max_clusters_of[dev].load(std::memory_order_acquire);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -67,6 +81,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
     max_clusters = n;
+    max_clusters_of[dev].store(n, std::memory_order_release);
   }
   if (tiles_upper <= 0) return cudaSuccess;
   const int clusters = tiles_upper < max_clusters ? tiles_upper : max_clusters;
