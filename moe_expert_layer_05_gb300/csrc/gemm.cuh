@@ -526,7 +526,8 @@ template <class C>
 __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
                                                   int quarter, int lane, Stager<C::STAGING_BUFS>& st,
                                                   const CUtensorMap* tmC,
-                                                  const CUtensorMap* tmC2) {
+                                                  const CUtensorMap* tmC2,
+                                                  uint64_t* release_bar = nullptr, bool* released = nullptr) {
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t t0 = tmem_acc + lane_addr;
   const bool no_mma = (ti.num_kb == 0);         // empty group (weight gradients): result is zero
@@ -573,6 +574,53 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
     const int col0 = ti.n * (C::BN / 2);
     const int y = ti.m0 + quarter * 32;
+    if constexpr (C::BN == 256) {
+      if (p.c2 == nullptr && release_bar != nullptr) {
+        // Forward without saved z: compute this row's 128 values of h' into
+        // registers, hand the accumulator back to the MMA warp, then store.
+        uint32_t hp[64];                            // packed bf16 pairs, columns 0..127
+        #pragma unroll
+        for (int qq = 0; qq < 8; qq += 2) {
+          uint32_t av[2][16], bv[2][16];
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            tmem_ld_x16(t0 + 16 * (qq + u), av[u]);
+            tmem_ld_x16(t0 + C::BN / 2 + 16 * (qq + u), bv[u]);
+          }
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            tmem_ld_wait(av[u]);
+            tmem_ld_wait(bv[u]);
+          }
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float a0 = __uint_as_float(av[u][2 * j]), a1 = __uint_as_float(av[u][2 * j + 1]);
+              const float b0 = __uint_as_float(bv[u][2 * j]), b1 = __uint_as_float(bv[u][2 * j + 1]);
+              hp[8 * (qq + u) + j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
+                                                 g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(release_bar);
+        *released = true;
+        #pragma unroll
+        for (int c = 0; c < 2; ++c) {               // two 64-column chunks
+          st.begin();
+          #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t* w = hp + 8 * (4 * c + q);
+            st.put(2 * q, w[0], w[1], w[2], w[3]);
+            st.put(2 * q + 1, w[4], w[5], w[6], w[7]);
+          }
+          st.flush(tmC, col0 + 64 * c, y);
+        }
+        return;
+      }
+    }
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN / 2; c0 += 64) {
       st.begin();
@@ -943,20 +991,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
       tc_fence_after_sync();
+      bool released = false;                 // accumulator already handed back by the epilogue
       if constexpr (C::M256) {
         if (part == 0 || ti.half1) {
           TileInfo th = ti;
           th.m0 += 128 * part;
-          epilogue_tile_tma<C>(p, th, tmem_base + acc * C::ACC_COLS + part * C::BN, quarter, lane, st, &tmC, &tmC2);
+          epilogue_tile_tma<C>(p, th, tmem_base + acc * C::ACC_COLS + part * C::BN, quarter, lane, st, &tmC, &tmC2,
+                               &tempty_bar[acc], &released);
         }
       } else if constexpr (C::TMA_OUT) {
-        epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::ACC_COLS, quarter, lane, st, &tmC, &tmC2);
+        epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::ACC_COLS, quarter, lane, st, &tmC, &tmC2,
+                             &tempty_bar[acc], &released);
       } else {
         epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (lane == 0 && !released) mbar_arrive(&tempty_bar[acc]);
       if (++acc == C::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
     }
     if constexpr (C::TMA_OUT) st.drain();     // every TMA store has finished before the CTA exits
