@@ -1,19 +1,22 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05).
 //
-// One CTA per SM walks a list of 128 x BN output tiles (256 x BN where two
-// 128-row MMAs share each B k-block).  Warp roles:
-//   warp 0      TMA producer: streams A and B k-blocks (64 bf16 = one 128-B
+// One CTA per SM walks a list of output tiles: 128 x BN, or 256 x BN where two
+// 128-row MMAs share each B k-block.  Warp roles:
+//   warp 0      TMA producer: takes tile indices from a counter in global
+//               memory and streams A and B k-blocks (64 bf16 = one 128-B
 //               swizzle row) into a STAGES-deep shared-memory ring;
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
-//               K=16) into one of two TMEM accumulators;
+//               K=16) into a TMEM accumulator (two where they fit, so the
+//               epilogue of one tile overlaps the MMAs of the next);
 //   warps 2..   epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32*(w%4)..+31, i.e. one output row per thread),
-//               apply the fused elementwise step and store to global memory,
-//               while the MMA warp already fills the other accumulator.
+//               apply the fused elementwise step and store through TMA.
+// grouped_gemm_pair_kernel at the end of this file runs 256 x 256 tiles on a
+// pair of CTAs (a cluster of two) with tcgen05.mma.cta_group::2.
 //
 // Group shapes never reach the host.  For routed problems the kernel reads
 // the padded per-expert row offsets (every expert segment is a whole number of
-// 128-row tiles) from device memory and derives its tile list from them: this
+// 128-row blocks) from device memory and derives its tile list from them: this
 // is the grouped GEMM with device-side shapes that the Megatron Core MoE
 // summary describes (technical summary 2.4, grouped GEMM and sync-free
 // kernels).
@@ -317,156 +320,23 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
                                               int quarter, int lane) {
-  const int r = quarter * 32 + lane;            // row inside the tile
+  // Plain stores: only the router logits (fp32, N = E columns, rows not
+  // necessarily 16-byte sized) leave this way; every other epilogue uses TMA.
+  static_assert(C::EP == Epi::kStoreF32 && C::S == Sched::kDenseM, "router epilogue");
+  const int row = ti.m0 + quarter * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-  const bool no_mma = (ti.num_kb == 0);         // empty group: result is zero
-
-  if constexpr (C::S == Sched::kRoutedK) {
-    float* out = reinterpret_cast<float*>(p.c) + (long long)ti.group * p.c_group_stride +
-                 (long long)(ti.m0 + r) * p.ldc + (long long)ti.n * C::BN;
-    #pragma unroll 1
-    for (int c0 = 0; c0 < C::BN; c0 += 16) {
-      uint32_t v[16];
-      tmem_ld_x16(tmem_acc + lane_addr + c0, v);
-      tmem_ld_wait(v);
-      float4* o4 = reinterpret_cast<float4*>(out + c0);
+  const bool row_ok = row < p.m_rows;
+  float* out = reinterpret_cast<float*>(p.c) + (long long)row * p.ldc;
+  #pragma unroll 1
+  for (int c0 = 0; c0 < C::BN; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld_x16(tmem_acc + lane_addr + c0, v);
+    tmem_ld_wait(v);
+    const int colbase = ti.n * C::BN + c0;
+    if (row_ok) {
       #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float4 f;
-        f.x = no_mma ? 0.f : __uint_as_float(v[4 * j + 0]);
-        f.y = no_mma ? 0.f : __uint_as_float(v[4 * j + 1]);
-        f.z = no_mma ? 0.f : __uint_as_float(v[4 * j + 2]);
-        f.w = no_mma ? 0.f : __uint_as_float(v[4 * j + 3]);
-        o4[j] = f;
-      }
-    }
-    return;
-  } else {
-    const int row = ti.m0 + r;
-    const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
-
-    if constexpr (C::EP == Epi::kStoreF32) {
-      float* out = reinterpret_cast<float*>(p.c) + (long long)row * p.ldc;
-      #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(tmem_acc + lane_addr + c0, v);
-        tmem_ld_wait(v);
-        const int colbase = ti.n * C::BN + c0;
-        if (row_ok) {
-          #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (colbase + j < p.valid_cols) out[colbase + j] = __uint_as_float(v[j]);
-        }
-      }
-    } else if constexpr (C::EP == Epi::kStoreBf16) {
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.c) + (long long)row * p.ldc + (long long)ti.n * C::BN;
-      #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(tmem_acc + lane_addr + c0, v);
-        tmem_ld_wait(v);
-        uint4 w0, w1;
-        w0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-        w0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-        w0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-        w0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-        w1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-        w1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-        w1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-        w1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-        if (row_ok) {
-          uint4* o = reinterpret_cast<uint4*>(out + c0);
-          o[0] = w0;
-          o[1] = w1;
-        }
-      }
-    } else if constexpr (C::EP == Epi::kSwiglu) {
-      // accumulator columns [0,128) = gate rows of W1, [128,256) = up rows
-      const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
-      const int col0 = ti.n * (C::BN / 2);
-      __nv_bfloat16* hout = reinterpret_cast<__nv_bfloat16*>(p.c) + (long long)row * p.ldc + col0;
-      __nv_bfloat16* zout = (p.c2 != nullptr)
-                                ? reinterpret_cast<__nv_bfloat16*>(p.c2) + (long long)row * p.ldc2 + col0
-                                : nullptr;
-      #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN / 2; c0 += 16) {
-        uint32_t a[16], b[16];
-        tmem_ld_x16(tmem_acc + lane_addr + c0, a);
-        tmem_ld_x16(tmem_acc + lane_addr + (C::BN / 2) + c0, b);
-        tmem_ld_wait(a);
-        tmem_ld_wait(b);
-        uint32_t hw[8], za[8], zb[8];
-        #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
-          const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
-          const float s0 = a0 / (1.0f + expf(-a0));
-          const float s1 = a1 / (1.0f + expf(-a1));
-          hw[j] = pack_bf16x2(g * s0 * b0, g * s1 * b1);
-          za[j] = pack_bf16x2(a0, a1);
-          zb[j] = pack_bf16x2(b0, b1);
-        }
-        if (row_ok) {
-          uint4* ho = reinterpret_cast<uint4*>(hout + c0);
-          ho[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          ho[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-          if (zout != nullptr) {
-            uint4* zo = reinterpret_cast<uint4*>(zout + c0);
-            zo[0] = make_uint4(za[0], za[1], za[2], za[3]);
-            zo[1] = make_uint4(za[4], za[5], za[6], za[7]);
-            uint4* zo2 = reinterpret_cast<uint4*>(zout + p.half_cols + c0);
-            zo2[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
-            zo2[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
-          }
-        }
-      }
-    } else {  // kSwigluBwd
-      const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
-      const int col0 = ti.n * C::BN;
-      const __nv_bfloat16* zrow = p.aux + (long long)(row_ok ? row : 0) * p.ld_aux + col0;
-      __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(p.c) + (long long)row * p.ldc + col0;
-      float dg = 0.f;
-      #pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += 16) {
-        // rows past the end read row 0 (always present) so the warp stays converged
-        const uint4* pa = reinterpret_cast<const uint4*>(zrow + c0);
-        const uint4* pb = reinterpret_cast<const uint4*>(zrow + p.half_cols + c0);
-        const uint4 za0 = pa[0], za1 = pa[1], zb0 = pb[0], zb1 = pb[1];
-        uint32_t v[16];
-        tmem_ld_x16(tmem_acc + lane_addr + c0, v);
-        tmem_ld_wait(v);
-        const uint32_t zaw[8] = {za0.x, za0.y, za0.z, za0.w, za1.x, za1.y, za1.z, za1.w};
-        const uint32_t zbw[8] = {zb0.x, zb0.y, zb0.z, zb0.w, zb1.x, zb1.y, zb1.z, zb1.w};
-        uint32_t da[8], db[8];
-        #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float av[2] = {bf16_lo(zaw[j]), bf16_hi(zaw[j])};
-          float bv[2] = {bf16_lo(zbw[j]), bf16_hi(zbw[j])};
-          float dav[2], dbv[2];
-          #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float dh = no_mma ? 0.f : __uint_as_float(v[2 * j + u]);
-            const float sg = 1.0f / (1.0f + expf(-av[u]));
-            const float si = av[u] * sg;
-            dg += dh * si * bv[u];
-            const float dhg = g * dh;
-            dav[u] = dhg * bv[u] * sg * (1.0f + av[u] * (1.0f - sg));
-            dbv[u] = dhg * si;
-          }
-          da[j] = pack_bf16x2(dav[0], dav[1]);
-          db[j] = pack_bf16x2(dbv[0], dbv[1]);
-        }
-        if (row_ok) {
-          uint4* o = reinterpret_cast<uint4*>(dz + c0);
-          o[0] = make_uint4(da[0], da[1], da[2], da[3]);
-          o[1] = make_uint4(da[4], da[5], da[6], da[7]);
-          uint4* o2 = reinterpret_cast<uint4*>(dz + p.half_cols + c0);
-          o2[0] = make_uint4(db[0], db[1], db[2], db[3]);
-          o2[1] = make_uint4(db[4], db[5], db[6], db[7]);
-        }
-      }
-      if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * p.n_tiles + ti.n] = dg;
+      for (int j = 0; j < 16; ++j)
+        if (colbase + j < p.valid_cols) out[colbase + j] = __uint_as_float(v[j]);
     }
   }
 }

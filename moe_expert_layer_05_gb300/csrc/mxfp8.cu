@@ -109,36 +109,41 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // Blocks along the column, output transposed: src [rows, cols] bf16 ->
 // codes [cols, rows] (row c of the output = column c of the input), scales
 // tiled over the [cols, rows] output.  batch: independent matrices one after
-// another (expert weights).  A block reads a 32-row x 256-column tile with
-// 16-byte loads into shared memory, then thread c quantises column c of it.
-// blockIdx.x runs over the 32-row blocks so that neighbouring blocks write
-// neighbouring 32-byte pieces of the same output rows.
+// another (expert weights).  A block reads a 128-row x 64-column tile with
+// 16-byte loads into shared memory; thread (c, q) quantises rows 32q..32q+31
+// of column c.  The four threads of a column sit next to each other in a warp,
+// so their 32-byte pieces of one output row form a full 128-byte line.
+// Shared memory: element (r, c) in 16-byte chunk (c / 8) ^ (r / 32) of row r,
+// so the four row blocks read by one warp fall in different banks.
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
                                                             int cols, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf) {
-  __shared__ uint4 tile[32][32];           // 32 rows x 256 bf16
-  const int rb = blockIdx.x;               // block of 32 input rows
-  const int c0 = blockIdx.y * 256;
+  __shared__ uint4 tile[128][8];           // 128 rows x 64 bf16
+  const int rb = blockIdx.x;               // block of 128 input rows
+  const int c0 = blockIdx.y * 64;
   const long long mat = blockIdx.z;
-  const __nv_bfloat16* base = src + mat * rows * cols + static_cast<long long>(rb) * 32 * cols;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const __nv_bfloat16* base = src + mat * rows * cols + static_cast<long long>(rb) * 128 * cols + c0;
   #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int r = warp * 4 + k;
-    const int c = c0 + lane * 8;
-    tile[r][lane] = (c < cols) ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * cols + c))
-                               : make_uint4(0, 0, 0, 0);
+    const int i = threadIdx.x + 256 * k;   // 16-byte piece i: row i / 8, chunk i % 8
+    const int r = i >> 3, j = i & 7;
+    tile[r][j ^ (r >> 5)] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * cols) + j);
   }
   __syncthreads();
-  const int c = c0 + threadIdx.x;
-  if (c >= cols) return;
-  const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cl = warp * 8 + (lane >> 2);   // column inside the tile
+  const int q = lane & 3;                  // block of 32 rows inside the tile
+  const __nv_bfloat16* t = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]);
   float v[32];
   #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(col[i * 256]);
-  uint8_t* out = codes + mat * rows * cols + static_cast<long long>(c) * rows + rb * 32;
+  for (int i = 0; i < 32; ++i) {
+    const int r = 32 * q + i;
+    v[i] = __bfloat162float(t[r * 64 + (((cl >> 3) ^ q) << 3) + (cl & 7)]);
+  }
+  const int c = c0 + cl;
+  uint8_t* out = codes + mat * rows * cols + static_cast<long long>(c) * rows + rb * 128 + 32 * q;
   const uint8_t e = quantize32(v, out);
-  sf[mat * (static_cast<long long>(rows) * cols / 32) + sf_offset(c, rb, rows / 128)] = e;
+  sf[mat * (static_cast<long long>(rows) * cols / 32) + sf_offset(c, rb * 4 + q, rows / 128)] = e;
 }
 
 }  // namespace
@@ -156,7 +161,7 @@ cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int 
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
                                  cudaStream_t st) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  dim3 grid(rows / 32, (cols + 255) / 256, batch);
+  dim3 grid(rows / 128, cols / 64, batch);   // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
   quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, sf);
   count_launches(1);
   return cudaGetLastError();
