@@ -182,11 +182,13 @@ MxWs mx_ws_layout(const moe_config* c) {
     return b;
   };
   auto region = [&]() { end = off > end ? off : end; off = 0; };
-  m.x = buf(cap * H); m.h = buf(cap * F);
-  if (S) { m.xs = buf(T * H); m.hs = buf(T * S); }
+  // xs / dys: x and dy quantised per token (fed to the shared expert, and
+  // gathered into expert order for the routed experts)
+  m.x = buf(cap * H); m.h = buf(cap * F); m.xs = buf(T * H);
+  if (S) m.hs = buf(T * S);
   region();
-  m.dy = buf(cap * H); m.dz = buf(cap * 2 * F);
-  if (S) { m.dys = buf(T * H); m.dzs = buf(T * 2 * S); }
+  m.dy = buf(cap * H); m.dz = buf(cap * 2 * F); m.dys = buf(T * H);
+  if (S) m.dzs = buf(T * 2 * S);
   region();
   m.dzT = buf(2 * F * cap); m.xT = buf(H * cap); m.dyT = buf(H * cap); m.hT = buf(F * cap);
   if (S) { m.dzsT = buf(2 * S * T); m.xsT = buf(H * T); m.dysT = buf(H * T); m.hsT = buf(S * T); }
@@ -497,12 +499,15 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
     auto wq = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
     auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
-    MOE_TRY(launch_quantize_rows(x_perm, cap, H, 0, q(M.x), f(M.x), st));
+    // x is quantised once per token and the codes are permuted like x itself
+    // (blocks lie along H, so quantising before or after the gather is the same)
+    MOE_TRY(launch_quantize_rows(x, T, H, 0, q(M.xs), f(M.xs), st));
+    MOE_TRY(launch_gather_rows_mx(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st));
+    if (with_backward) MOE_TRY(launch_zero_pad_rows_mx(counts, poff, E, H, q(M.x), f(M.x), st));
     MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
     MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st));
     MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st));
     if (S > 0 && T > 0) {
-      MOE_TRY(launch_quantize_rows(x, T, H, 0, q(M.xs), f(M.xs), st));
       MOE_TRY(gemm_mx_fc1(q(M.xs), f(M.xs), T, H, wq(W.s1), wf(W.s1), 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
                           zs, status, st));
       MOE_TRY(launch_quantize_rows(at<void>(act, L.hs), T, S, 0, q(M.hs), f(M.hs), st));
@@ -559,13 +564,14 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
     auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
     auto wq = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
     auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
-    MOE_TRY(launch_quantize_rows(dy_perm, cap, H, 0, q(M.dy), f(M.dy), st));
+    MOE_TRY(launch_quantize_rows(dy, T, H, 0, q(M.dys), f(M.dys), st));
+    MOE_TRY(launch_gather_rows_mx(q(M.dys), f(M.dys), slot_row, T, k, H, q(M.dy), f(M.dy), st));
+    MOE_TRY(launch_zero_pad_rows_mx(counts, poff, E, H, q(M.dy), f(M.dy), st));
     MOE_TRY(gemm_mx_dgrad_fc2(q(M.dy), f(M.dy), cap, H, wq(W.w2t), wf(W.w2t), E, F, poff, 0, at<void>(act, L.z),
                               at<float>(act, L.row_gate), dz, dpart, status, st));
     MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st));
     MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st));
     if (S > 0 && T > 0) {
-      MOE_TRY(launch_quantize_rows(dy, T, H, 0, q(M.dys), f(M.dys), st));
       MOE_TRY(gemm_mx_dgrad_fc2(q(M.dys), f(M.dys), T, H, wq(W.s2t), wf(W.s2t), 1, S, nullptr, T, at<void>(act, L.zs),
                                 nullptr, at<void>(act, L.dzs), nullptr, status, st));
       MOE_TRY(launch_quantize_rows(at<void>(act, L.dzs), T, 2 * S, 0, q(M.dzs), f(M.dzs), st));

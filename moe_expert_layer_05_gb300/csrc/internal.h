@@ -73,9 +73,15 @@ cudaError_t gemm_wgrad(const void* a, int M, const void* b, int N, int rows_allo
 
 // ------------------------------------------------------------ MXFP8 (mxfp8.cu, gemm_mx.cu)
 // Row mode: blocks of 32 along each row; gate_up_half > 0 also interleaves
-// the rows of every [gate; up] group of 2*half rows in 64-row blocks.
+// the rows of every [gate; up] group of 2*half rows in 128-row blocks.
 cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
                                  uint8_t* sf, cudaStream_t st);
+// Row-quantised token rows -> expert order (codes and scale tiles), and the
+// zero codes / scales of the padding rows.
+cudaError_t launch_gather_rows_mx(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
+                                  int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st);
+cudaError_t launch_zero_pad_rows_mx(const int32_t* counts, const int32_t* poffsets, int E, int H, uint8_t* codes,
+                                    uint8_t* sf, cudaStream_t st);
 // Column mode: batch x [rows, cols] -> batch x [cols, rows], blocks along rows.
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
                                  cudaStream_t st);

@@ -146,6 +146,51 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   sf[mat * (static_cast<long long>(rows) * cols / 32) + sf_offset(c, rb * 4 + q, rows / 128)] = e;
 }
 
+// Token-order quantised rows (codes [T, H] and their scale tiles) -> expert
+// order: the same permutation as the bf16 gather, on codes and scales.  Row
+// blocks of 32 lie along H, so a row's codes do not depend on where it goes.
+__global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __restrict__ codes_tok,
+                                                             const uint8_t* __restrict__ sf_tok,
+                                                             const int32_t* __restrict__ slot_row, int k, int H,
+                                                             uint4* __restrict__ codes_perm,
+                                                             uint8_t* __restrict__ sf_perm) {
+  const int t = blockIdx.x;
+  __shared__ int s_rows[kMaxK];
+  if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[static_cast<long long>(t) * k + threadIdx.x];
+  __syncthreads();
+  const int nv = H / 16;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const uint4 c = __ldg(codes_tok + static_cast<long long>(t) * nv + v);
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r >= 0) codes_perm[static_cast<long long>(r) * nv + v] = c;
+    }
+  }
+  const int nb = H / 32, tiles = H / 128;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    const uint8_t e = sf_tok[sf_offset(t, b, tiles)];
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r >= 0) sf_perm[sf_offset(r, b, tiles)] = e;
+    }
+  }
+}
+
+// Padding rows of every expert segment: zero codes and the scale of an
+// all-zero block (byte 0), as quantising zero rows would give.
+__global__ void zero_pad_rows_mx_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ poffsets,
+                                        int H, uint4* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int e = blockIdx.x;
+  const int r0 = poffsets[e] + counts[e], r1 = poffsets[e + 1];
+  const int nv = H / 16, nb = H / 32;
+  const long long n = static_cast<long long>(r1 - r0) * nv;
+  uint4* base = codes + static_cast<long long>(r0) * nv;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
+  const long long m = static_cast<long long>(r1 - r0) * nb;
+  for (long long i = threadIdx.x; i < m; i += blockDim.x)
+    sf[sf_offset(r0 + static_cast<int>(i / nb), static_cast<int>(i % nb), H / 128)] = 0;
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
@@ -167,4 +212,22 @@ cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols,
   return cudaGetLastError();
 }
 
+}  // namespace moe
+
+namespace moe {
+cudaError_t launch_gather_rows_mx(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
+                                  int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  gather_rows_mx_kernel<<<T, 128, 0, st>>>(reinterpret_cast<const uint4*>(codes_tok), sf_tok, slot_row, k, H,
+                                           reinterpret_cast<uint4*>(codes_perm), sf_perm);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_pad_rows_mx(const int32_t* counts, const int32_t* poffsets, int E, int H, uint8_t* codes,
+                                    uint8_t* sf, cudaStream_t st) {
+  zero_pad_rows_mx_kernel<<<E, 256, 0, st>>>(counts, poffsets, H, reinterpret_cast<uint4*>(codes), sf);
+  count_launches(1);
+  return cudaGetLastError();
+}
 }  // namespace moe
