@@ -78,15 +78,21 @@ struct GemmCfg {
   static constexpr bool ROWS256 = M256 || PAIR;   // tiles of 256 rows (pairs of 128-row blocks)
   static constexpr int TILE_M = ROWS256 ? 256 : 128;
   static constexpr bool MX = MX_;                 // MXFP8 operands (E4M3 + E8M0 1x32 scales)
-  static constexpr int BK = MX ? 128 : 64;        // one 128-byte swizzle row per k-block
+  // Contraction elements per k-block: one 128-byte swizzle row (K-major), or
+  // for the weight gradients on CTA pairs (MN-major, short per-expert K) 128
+  // token rows, so each TMA box is 16 KB instead of 8 KB.
+  static constexpr bool WIDE_K = PAIR_ && (S_ == Sched::kRoutedK);
+  static constexpr int BK = MX ? 128 : (WIDE_K ? 128 : 64);
+  static constexpr int MN_CHUNK = BK * 128;       // MN-major: bytes of one 64-wide MN chunk (BK rows of 128 B)
   static constexpr int KSTEP = MX ? 32 : 16;      // K of one MMA instruction
   static constexpr int BN = BN_;
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
   static constexpr Sched S = S_;
   static constexpr Epi EP = EP_;
-  static constexpr int A_BYTES = (M256 ? 256 : 128) * 128;   // this CTA's A rows of one k-block
-  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * 128;  // this CTA's B rows (a pair splits N)
+  static constexpr int ROW_BYTES = MX ? BK : BK * 2;         // bytes of one A / B row of a k-block
+  static constexpr int A_BYTES = (M256 ? 256 : 128) * ROW_BYTES;   // this CTA's A rows of one k-block
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * ROW_BYTES;  // this CTA's B rows (a pair splits N)
   static constexpr int SFA_BYTES = MX ? 512 : 0;
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -109,7 +115,7 @@ struct GemmCfg {
   // Weight gradients are bound by their fp32 stores: each epilogue warp keeps
   // several 4 KB stores in flight (the k-loops are short, so the ring needs
   // few stages).
-  static constexpr int WGRAD_BUFS = PAIR ? 6 : 4;
+  static constexpr int WGRAD_BUFS = WIDE_K ? 2 : 4;
   static constexpr int STAGING_BUFS = (S == Sched::kRoutedK && TMA_OUT) ? WGRAD_BUFS
                                       : (EP == Epi::kSwigluBwd) ? 2    // gate and up chunks side by side
                                       : ((TMA_OUT && RING_IF_TWO < 4) ? 1 : 2);
@@ -144,6 +150,7 @@ struct GemmCfg {
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
   static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
+  static_assert(!WIDE_K || (A_MN && B_MN), "128-row k-blocks only for MN-major operands");
   static_assert(!PAIR || (!M256 && !MX && TMA_OUT && BN == 256 &&
                           (S == Sched::kRoutedK ? (A_MN && B_MN && EP == Epi::kStoreF32) : !A_MN)),
                 "CTA pairs: bf16, N = 256; row-grouped GEMMs with K-major A, or MN-major weight gradients");
@@ -908,9 +915,9 @@ __device__ __forceinline__ void issue_loads_pair(const CUtensorMap* tmA, const C
     const int mr = ti.m0 + 128 * static_cast<int>(rank);
     const int nr = ti.n * C::BN + 128 * static_cast<int>(rank);
     tma_load_2d_pair(a_dst, tmA, bar_cluster_addr, mr, ti.k_row0 + k0);
-    tma_load_2d_pair(a_dst + 8192, tmA, bar_cluster_addr, mr + 64, ti.k_row0 + k0);
+    tma_load_2d_pair(a_dst + C::MN_CHUNK, tmA, bar_cluster_addr, mr + 64, ti.k_row0 + k0);
     tma_load_2d_pair(b_dst, tmB, bar_cluster_addr, nr, ti.k_row0 + k0);
-    tma_load_2d_pair(b_dst + 8192, tmB, bar_cluster_addr, nr + 64, ti.k_row0 + k0);
+    tma_load_2d_pair(b_dst + C::MN_CHUNK, tmB, bar_cluster_addr, nr + 64, ti.k_row0 + k0);
     return;
   }
   tma_load_2d_pair(a_dst, tmA, bar_cluster_addr, k0, ti.m0 + 128 * static_cast<int>(rank));
@@ -1076,9 +1083,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
           #pragma unroll
           for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
-            const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
+            const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, C::MN_CHUNK, 1024)
                                         : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
+            const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, C::MN_CHUNK, 1024)
                                         : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
             mma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }

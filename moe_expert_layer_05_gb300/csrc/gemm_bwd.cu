@@ -103,7 +103,12 @@ cudaError_t wgrad_bn(const void* a, int M, const void* b, int N, int rows_alloc,
                      int dense_rows, float* dw, int* status, cudaStream_t st) {
   // A[m, k] = a[k_row0 + k, m], B[n, k] = b[k_row0 + k, n]: both MN-major.
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, a, M, rows_alloc, 64, 64) || !make_tmap_bf16(&tb, b, N, rows_alloc, 64, 64))
+  // boxes of 64 columns x BK rows (BK = 128 on CTA pairs, 64 otherwise)
+  constexpr bool PAIR_K = (BN == 256);
+  CUtensorMap ta2, tb2;
+  if (!make_tmap_bf16(&ta, a, M, rows_alloc, 64, 64) || !make_tmap_bf16(&tb, b, N, rows_alloc, 64, 64) ||
+      !make_tmap_bf16(&ta2, a, M, rows_alloc, 64, PAIR_K ? 128 : 64) ||
+      !make_tmap_bf16(&tb2, b, N, rows_alloc, 64, PAIR_K ? 128 : 64))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
   p.poffsets = poffsets;
@@ -126,7 +131,7 @@ cudaError_t wgrad_bn(const void* a, int M, const void* b, int N, int rows_alloc,
       // (the bulk of the traffic) set the pace.
       using C = GemmCfg<BN, true, true, Sched::kRoutedK, Epi::kStoreF32, false, false, true>;
       p.m_tiles_w = M / 256;
-      return launch_gemm_pair<C>(ta, tb, tc, tc, p, p.E * p.m_tiles_w * p.n_tiles, st);
+      return launch_gemm_pair<C>(ta2, tb2, tc, tc, p, p.E * p.m_tiles_w * p.n_tiles, st);
     }
   }
   using C = GemmCfg<BN, true, true, Sched::kRoutedK, Epi::kStoreF32>;
