@@ -426,6 +426,41 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     }
   } else if constexpr (C::EP == Epi::kStoreBf16) {
     const int y = ti.m0 + quarter * 32;
+    if constexpr (C::M256 && C::BN == 256) {
+      if (release_bar != nullptr) {
+        // this row's 256 outputs as bf16 pairs in registers, the accumulator
+        // handed back to the MMA warp, then the stores
+        uint32_t pk[128];
+        #pragma unroll
+        for (int h = 0; h < 16; h += 2) {
+          uint32_t v[2][16];
+          tmem_ld_x16(t0 + 16 * h, v[0]);
+          tmem_ld_x16(t0 + 16 * (h + 1), v[1]);
+          tmem_ld_wait(v[0]);
+          tmem_ld_wait(v[1]);
+          #pragma unroll
+          for (int u = 0; u < 2; ++u)
+            #pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pk[8 * (h + u) + j] = pack_bf16x2(__uint_as_float(v[u][2 * j]), __uint_as_float(v[u][2 * j + 1]));
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(release_bar);
+        *released = true;
+        #pragma unroll
+        for (int c = 0; c < 4; ++c) {                // 64-column chunks
+          st.begin();
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* w = pk + 32 * c + 4 * q;
+            st.put(q, w[0], w[1], w[2], w[3]);
+          }
+          st.flush(tmC, ti.n * C::BN + 64 * c, y);
+        }
+        return;
+      }
+    }
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN; c0 += 64) {
       uint32_t v[4][16];                        // 64 columns in one TMEM round trip
