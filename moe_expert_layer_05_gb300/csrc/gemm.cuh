@@ -426,9 +426,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     }
   } else if constexpr (C::EP == Epi::kStoreBf16) {
     const int y = ti.m0 + quarter * 32;
-    if constexpr (C::M256 && C::BN == 256) {
+    if constexpr ((C::M256 || C::ACC_BUFS == 1) && C::BN == 256) {
       if (release_bar != nullptr) {
-        // this row's 256 outputs as bf16 pairs in registers, the accumulator
+        // (single accumulator) this row's 256 outputs as bf16 pairs in registers, the accumulator
         // handed back to the MMA warp, then the stores
         uint32_t pk[128];
         #pragma unroll
