@@ -486,6 +486,54 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
     const int col0 = ti.n * (C::BN / 2);
     const int y = ti.m0 + quarter * 32;
+    if constexpr (C::BN == 256 && C::ACC_BUFS == 1 && !C::M256) {
+      if (p.c2 != nullptr && release_bar != nullptr) {
+        // Single accumulator, z saved: h' and both halves of z for this row's
+        // 128 columns go to registers (bf16 pairs), the accumulator is handed
+        // back, then everything is stored.
+        uint32_t hp[64], zg[64], zu[64];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t a[16], b[16];
+          tmem_ld_x16(t0 + 16 * q, a);
+          tmem_ld_x16(t0 + C::BN / 2 + 16 * q, b);
+          tmem_ld_wait(a);
+          tmem_ld_wait(b);
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
+            const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
+            hp[8 * q + j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
+                                        g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
+            zg[8 * q + j] = pack_bf16x2(a0, a1);
+            zu[8 * q + j] = pack_bf16x2(b0, b1);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(release_bar);
+        *released = true;
+        #pragma unroll
+        for (int c = 0; c < 2; ++c) {               // 64-column chunks: h', z gate, z up
+          st.begin();
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) st.put(q, hp[32 * c + 4 * q], hp[32 * c + 4 * q + 1], hp[32 * c + 4 * q + 2],
+                                            hp[32 * c + 4 * q + 3]);
+          st.flush(tmC, col0 + 64 * c, y);
+          st.begin();
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) st.put(q, zg[32 * c + 4 * q], zg[32 * c + 4 * q + 1], zg[32 * c + 4 * q + 2],
+                                            zg[32 * c + 4 * q + 3]);
+          st.flush(tmC2, col0 + 64 * c, y);
+          st.begin();
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) st.put(q, zu[32 * c + 4 * q], zu[32 * c + 4 * q + 1], zu[32 * c + 4 * q + 2],
+                                            zu[32 * c + 4 * q + 3]);
+          st.flush(tmC2, p.half_cols + col0 + 64 * c, y);
+        }
+        return;
+      }
+    }
     if constexpr (C::BN == 256) {
       if (p.c2 == nullptr && release_bar != nullptr) {
         // Forward without saved z: compute this row's 128 values of h' into
