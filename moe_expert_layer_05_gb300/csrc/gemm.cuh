@@ -411,6 +411,50 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
 
   if constexpr (C::EP == Epi::kStoreF32) {      // weight gradients: [group*M + row, col] fp32
     const int y = ti.group * p.m_rows + ti.m0 + quarter * 32;
+    if constexpr (C::ACC_BUFS == 1 && C::BN == 256 && C::STAGING_BUFS >= 4) {
+      if (release_bar != nullptr) {
+        // Single accumulator: columns 0..127 go straight into the four staging
+        // buffers (their stores start at once), columns 128..255 into
+        // registers; then the accumulator is handed back and the rest stored.
+        #pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t a[16], b[16];
+          load32(t0 + c0, a, b);
+          st.begin();
+          #pragma unroll
+          for (int j = 0; j < 4; ++j) st.put(j, no_mma ? 0u : a[4 * j], no_mma ? 0u : a[4 * j + 1],
+                                            no_mma ? 0u : a[4 * j + 2], no_mma ? 0u : a[4 * j + 3]);
+          #pragma unroll
+          for (int j = 0; j < 4; ++j) st.put(4 + j, no_mma ? 0u : b[4 * j], no_mma ? 0u : b[4 * j + 1],
+                                            no_mma ? 0u : b[4 * j + 2], no_mma ? 0u : b[4 * j + 3]);
+          st.flush(tmC, ti.n * C::BN + c0, y);
+        }
+        uint32_t keep[128];
+        #pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          uint32_t v[16];
+          tmem_ld_x16(t0 + 128 + 16 * h, v);
+          tmem_ld_wait(v);
+          #pragma unroll
+          for (int j = 0; j < 16; ++j) keep[16 * h + j] = no_mma ? 0u : v[j];
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(release_bar);
+        *released = true;
+        #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          st.begin();
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* w = keep + 32 * c + 4 * j;
+            st.put(j, w[0], w[1], w[2], w[3]);
+          }
+          st.flush(tmC, ti.n * C::BN + 128 + 32 * c, y);
+        }
+        return;
+      }
+    }
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN; c0 += 32) {
       uint32_t a[16], b[16];
