@@ -57,14 +57,14 @@ cudaError_t router_bn(const void* x, const void* wr, int T, int H, int E, float*
   p.E = 1;
   p.m_rows = T;
   p.k_len = H;
-  p.n_tiles = 1;
+  p.n_tiles = (E + BN - 1) / BN;
   p.b_rows_per_group = 0;
   p.c = logits;
   p.ldc = E;
   p.valid_cols = E;
   p.rows_cap = T;
   p.status = status;
-  const int tiles = (T + 127) / 128;
+  const int tiles = ((T + 127) / 128) * p.n_tiles;
   return launch_gemm<C>(ta, tb, ta, ta, p, tiles < num_sms() ? tiles : num_sms(), st);   // plain stores
 }
 
@@ -76,8 +76,9 @@ cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, floa
   if (E <= 16) return router_bn<16>(x, wr, T, H, E, logits, status, st);
   if (E <= 32) return router_bn<32>(x, wr, T, H, E, logits, status, st);
   if (E <= 64) return router_bn<64>(x, wr, T, H, E, logits, status, st);
-  if (E <= 128) return router_bn<128>(x, wr, T, H, E, logits, status, st);
-  return router_bn<256>(x, wr, T, H, E, logits, status, st);
+  // E > 128: two 128-wide N tiles per row block, twice as many CTAs busy as
+  // one 256-wide tile (the router has only T/128 row blocks)
+  return router_bn<128>(x, wr, T, H, E, logits, status, st);
 }
 
 cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E, int F, const int32_t* poffsets,
