@@ -20,11 +20,13 @@ Source: "Scalable Training of Mixture-of-Experts Models with Megatron Core"
 * routing weight applied before the activation computation so backward keeps
   no extra intermediate: technical summary section 2.2 (memory-efficient
   permutation);
-* MXFP8 expert GEMMs on Blackwell: technical summary section 2.5.
+* MXFP8 expert GEMMs on Blackwell: technical summary section 2.5;
+* NVFP4 expert GEMMs, named beside MXFP8 in the same section (forward only;
+  the format's own definition is the reading, see the NVFP4 section below).
 
 The pages give no formula for any of these.  The readings taken where they are
 silent (gate formulas, selection key, tie rule, SwiGLU layout, where the gate
-multiplies, the MX scale rule) are listed with the design notes of the
+multiplies, the MX scale rule, the NVFP4 tensor scale) are listed with the design notes of the
 repository; each function below states the reading it implements.
 
 Every function here is pinned by a test in tests/test_oracle_*.py against
@@ -683,3 +685,168 @@ def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None,
     out["dWr"] = dl.T @ x
     out["dx"] = dx
     return out
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 expert GEMMs (technical summary 2.5: NVFP4 named beside MXFP8 as a
+# Blackwell quantisation recipe for the expert GEMMs and activations).  The
+# pages give no recipe; the reading taken is the NVFP4 format itself:
+#   * elements FP4 E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit:
+#     0, 0.5, 1, 1.5, 2, 3, 4, 6), rounded to nearest even, saturated to +-6;
+#   * one unsigned E4M3 scale per block of 16 consecutive values along the
+#     contraction;
+#   * one fp32 scale per tensor from its largest magnitude, so the block scales
+#     land in E4M3's range: S = 2688 / amax (2688 = 6 * 448, the E2M1 and E4M3
+#     maxima).
+# The encoding decisions (scale byte, element codes) are taken in fp32 in the
+# order written below, the precision the GPU quantiser works in, so both sides
+# make the same decisions from the same bf16 inputs:
+#   s_f  = fp32(fp32(amax_b / 6) * S)       block scale before rounding
+#   s    = e4m3(s_f)                        (round to nearest even, satfinite)
+#   r    = fp32(S / s)  (0 when s == 0)     multiplier of the block's values
+#   code = e2m1(fp32(v * r))
+# and a value is decoded as e2m1(code) * s / S.  S and r are capped at the
+# largest finite fp32 (only reached for tensors with amax below ~1e-33).
+# ---------------------------------------------------------------------------
+
+E2M1_MAX = 6.0
+NV_BLOCK = 16
+NV_TENSOR_RANGE = 2688.0     # E2M1 max * E4M3 max
+_F32_MAX = float(np.finfo(np.float32).max)
+
+
+def e2m1_decode(code) -> np.ndarray:
+    """Value of each 4-bit E2M1 pattern (low nibble of the input) as fp64."""
+    c = np.asarray(code, np.int64) & 0xF
+    s = np.where(c & 0x8, -1.0, 1.0)
+    ex = (c >> 1) & 0x3
+    m = c & 0x1
+    val = np.where(ex == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(ex.astype(np.float64) - 1.0))
+    return s * val
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """Round fp64 values to E2M1, nearest-even, saturating to +-6.  Returns the
+    4-bit patterns as uint8.  Inputs must be finite."""
+    v = np.asarray(v, np.float64)
+    sign = np.signbit(v)
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    # quantisation step: 0.5 below 2, 1 in [2, 4), 2 in [4, 6]
+    step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    q = np.minimum(_round_half_even(a / step) * step, E2M1_MAX)
+    # encode q (exactly representable): subnormal 0.5 -> 0b001, else exponent/mantissa
+    _, qp1 = np.frexp(q)
+    qp = qp1 - 1
+    normal = q >= 1.0
+    ex = np.where(normal, qp + 1, 0)
+    mant = np.where(normal, q / np.exp2(qp.astype(np.float64)) * 2.0 - 2.0, q / 0.5)
+    code = (ex.astype(np.int64) << 1) | mant.astype(np.int64)
+    code = np.where(q == 0, 0, code) | np.where(sign, 0x8, 0)
+    return code.astype(np.uint8)
+
+
+def nvfp4_tensor_scale(amax) -> np.float32:
+    """S = 2688 / amax in fp32 (1 for an all-zero tensor), capped at the largest fp32."""
+    amax = np.float32(amax)
+    if not amax > 0:
+        return np.float32(1.0)
+    with np.errstate(over="ignore"):
+        s = np.float32(NV_TENSOR_RANGE) / amax
+    return np.float32(min(float(s), _F32_MAX))
+
+
+def nvfp4_quantize(v, amax=None, axis=-1):
+    """Quantise along ``axis`` in blocks of 16 with the tensor scale of ``amax``
+    (default: max |v| over the whole array).  Returns (codes uint8 holding one
+    E2M1 pattern each, same shape as v; scales uint8 E4M3 with the blocked
+    axis divided by 16).  v is taken in fp32 (bf16 inputs are exact there)."""
+    v32 = np.moveaxis(np.asarray(v, np.float32), axis, -1)
+    if amax is None:
+        amax = np.abs(v32).max() if v32.size else 0.0
+    S = nvfp4_tensor_scale(amax)
+    shp = v32.shape
+    if shp[-1] % NV_BLOCK:
+        raise ValueError("blocked axis must be a multiple of 16")
+    blocks = v32.reshape(shp[:-1] + (shp[-1] // NV_BLOCK, NV_BLOCK))
+    amax_b = np.abs(blocks).max(axis=-1)
+    s_f = (amax_b / np.float32(6.0)).astype(np.float32) * S           # fp32 divide, fp32 multiply
+    s_code = e4m3_encode(s_f.astype(np.float64))
+    s_val = e4m3_decode(s_code).astype(np.float32)
+    with np.errstate(divide="ignore", over="ignore"):
+        r = np.where(s_val > 0, S / np.where(s_val > 0, s_val, np.float32(1.0)), np.float32(0.0)).astype(np.float32)
+    r = np.minimum(r, np.float32(_F32_MAX))
+    scaled = (blocks * r[..., None]).astype(np.float32)
+    codes = e2m1_encode(scaled.astype(np.float64)).reshape(shp)
+    return np.moveaxis(codes, -1, axis), np.moveaxis(s_code, -1, axis), S
+
+
+def nvfp4_dequantize(codes, scales, S, axis=-1):
+    """value = e2m1(code) * e4m3(scale) / S, one scale per 16 along axis."""
+    c = np.moveaxis(np.asarray(codes), axis, -1)
+    s = np.moveaxis(np.asarray(scales), axis, -1)
+    rep = np.repeat(e4m3_decode(s), NV_BLOCK, axis=-1)
+    return np.moveaxis(e2m1_decode(c) * rep / np.float64(S), -1, axis)
+
+
+def nvfp4_roundtrip(v, amax=None, axis=-1):
+    """dequantize(quantize(v)): the operand an NVFP4 GEMM multiplies."""
+    c, s, S = nvfp4_quantize(v, amax, axis)
+    return nvfp4_dequantize(c, s, S, axis)
+
+
+def bf16_round(v) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even), returned as fp64: the
+    storage type of the activations the quantiser reads."""
+    f = np.ascontiguousarray(np.asarray(v, np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=None, w2_shared=None,
+                      routing=None, weight_cache=None, quant=nvfp4_roundtrip, store=bf16_round):
+    """Forward with NVFP4 expert GEMMs.  Each quantised tensor has its own
+    tensor scale: x (all tokens), W1 and W2 (all experts), h' (the gated
+    activation of every expert row, rounded to bf16 as it is stored), and the
+    shared expert's W1s, W2s and h.  Everything else as moe_forward.
+    ``quant(v, amax, axis)`` and ``store(v)`` are the quantise-dequantise map
+    and the activation storage rounding; identities give back the unquantised
+    layer (tests/test_oracle_nvfp4.py pins that)."""
+    x = np.asarray(x, np.float64)
+    E = _shape(w1)[0]
+    F = _shape(w1)[1] // 2
+    cache = weight_cache if weight_cache is not None else {}
+
+    def wq(name, W):
+        if name not in cache:
+            cache[name] = quant(np.asarray(W, np.float64), None, -1)
+        return cache[name]
+
+    logits = None
+    if routing is None:
+        logits = router_logits(x, w_router)
+        idx, gate = route(logits, k, score, bias)
+    else:
+        idx = np.asarray(routing[0], np.int64)
+        gate = np.asarray(routing[1], np.float64)
+    xq = quant(x, None, -1)
+    W1q, W2q = wq("w1", w1), wq("w2", w2)
+    rows = []
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        z = xq[tok] @ W1q[e].T
+        hp = store(gate[tok, slot][:, None] * silu(z[:, :F]) * z[:, F:])
+        rows.append((e, tok, hp))
+    amax_h = max((np.abs(hp).max() for _, _, hp in rows), default=0.0)
+    y = np.zeros_like(x)
+    for e, tok, hp in rows:
+        np.add.at(y, tok, quant(hp, amax_h, -1) @ W2q[e].T)
+    if w1_shared is not None:
+        W1s, W2s = wq("w1s", w1_shared), wq("w2s", w2_shared)
+        S = W1s.shape[0] // 2
+        z = xq @ W1s.T
+        hs = store(silu(z[:, :S]) * z[:, S:])
+        y += quant(hs, None, -1) @ W2s.T
+    return {"y": y, "logits": logits, "topk_idx": idx.astype(np.int32), "gates": gate}
