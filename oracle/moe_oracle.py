@@ -803,6 +803,24 @@ def bf16_round(v) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def nvfp4_weight(cache, name, W, e=None, quant=nvfp4_roundtrip):
+    """Quantise-dequantise expert e of the weight tensor W (or all of a 2-D W
+    when e is None) with the tensor amax over every expert, memoised in
+    ``cache`` (a dict): the recipe quantises each weight once.  W may be any
+    object whose W[e] gives expert e as an array."""
+    key = (name, e)
+    if key not in cache:
+        akey = (name, "amax")
+        if akey not in cache:
+            if e is None:
+                cache[akey] = float(np.abs(np.asarray(W, np.float32)).max())
+            else:
+                cache[akey] = max(float(np.abs(np.asarray(W[i], np.float32)).max()) for i in range(_shape(W)[0]))
+        Wi = W if e is None else W[e]
+        cache[key] = quant(np.asarray(Wi, np.float64), cache[akey], -1)
+    return cache[key]
+
+
 def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=None, w2_shared=None,
                       routing=None, weight_cache=None, quant=nvfp4_roundtrip, store=bf16_round):
     """Forward with NVFP4 expert GEMMs.  Each quantised tensor has its own
@@ -817,10 +835,8 @@ def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_share
     F = _shape(w1)[1] // 2
     cache = weight_cache if weight_cache is not None else {}
 
-    def wq(name, W):
-        if name not in cache:
-            cache[name] = quant(np.asarray(W, np.float64), None, -1)
-        return cache[name]
+    def wq(name, W, e):
+        return nvfp4_weight(cache, name, W, e, quant)
 
     logits = None
     if routing is None:
@@ -830,21 +846,20 @@ def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_share
         idx = np.asarray(routing[0], np.int64)
         gate = np.asarray(routing[1], np.float64)
     xq = quant(x, None, -1)
-    W1q, W2q = wq("w1", w1), wq("w2", w2)
     rows = []
     for e in range(E):
         tok, slot = np.nonzero(idx == e)
         if tok.size == 0:
             continue
-        z = xq[tok] @ W1q[e].T
+        z = xq[tok] @ wq("w1", w1, e).T
         hp = store(gate[tok, slot][:, None] * silu(z[:, :F]) * z[:, F:])
         rows.append((e, tok, hp))
     amax_h = max((np.abs(hp).max() for _, _, hp in rows), default=0.0)
     y = np.zeros_like(x)
     for e, tok, hp in rows:
-        np.add.at(y, tok, quant(hp, amax_h, -1) @ W2q[e].T)
+        np.add.at(y, tok, quant(hp, amax_h, -1) @ wq("w2", w2, e).T)
     if w1_shared is not None:
-        W1s, W2s = wq("w1s", w1_shared), wq("w2s", w2_shared)
+        W1s, W2s = wq("w1s", w1_shared, None), wq("w2s", w2_shared, None)
         S = W1s.shape[0] // 2
         z = xq @ W1s.T
         hs = store(silu(z[:, :S]) * z[:, S:])

@@ -161,9 +161,9 @@ def test_quantised_layer_deviation_matches_the_format():
 
 def test_h_scale_is_shared_by_all_experts():
     """The h' quantiser calls (one per expert with rows) all get the same
-    tensor amax, the largest |h'| over every expert's rows; x and the weights
-    are quantised with their own amax (None: the whole tensor's)."""
-    x, wr, w1, w2, _, _ = _case(4, T=128, H=64, F=64)
+    tensor amax, the largest |h'| over every expert's rows; each weight is
+    quantised with the amax of the whole tensor (all experts), x with its own."""
+    x, wr, w1, w2, _, _ = _case(4, T=128, H=128, F=64)
     calls = []
 
     def rec(v, amax, axis):
@@ -171,9 +171,20 @@ def test_h_scale_is_shared_by_all_experts():
         return O.nvfp4_roundtrip(v, amax, axis)
 
     O.moe_forward_nvfp4(x, wr, w1, w2, k=2, quant=rec)
-    h_calls = [(v, a) for v, a in calls if a is not None]
-    assert len(h_calls) == len({e for e in O.route(O.router_logits(x, wr), 2, O.SOFTMAX)[0].ravel()})
+    used = sorted({int(e) for e in O.route(O.router_logits(x, wr), 2, O.SOFTMAX)[0].ravel()})
+
+    def is_expert_of(v, W):
+        return any(v.shape == W[e].shape and np.array_equal(v, W[e]) for e in range(W.shape[0]))
+
+    w1_calls = [a for v, a in calls if is_expert_of(v, w1)]
+    w2_calls = [a for v, a in calls if is_expert_of(v, w2)]
+    x_calls = [a for v, a in calls if v.shape == x.shape and np.array_equal(v, x)]
+    h_calls = [(v, a) for v, a in calls if not (is_expert_of(v, w1) or is_expert_of(v, w2) or
+                                                (v.shape == x.shape and np.array_equal(v, x)))]
+    assert len(w1_calls) == len(w2_calls) == len(h_calls) == len(used)
+    assert set(w1_calls) == {float(np.abs(w1).astype(np.float32).max())}
+    assert set(w2_calls) == {float(np.abs(w2).astype(np.float32).max())}
+    assert x_calls == [None]
     amaxes = {float(a) for _, a in h_calls}
     assert len(amaxes) == 1
     assert amaxes.pop() == max(np.abs(v).max() for v, _ in h_calls)
-    assert sum(1 for _, a in calls if a is None) == 3        # x, W1, W2
