@@ -173,6 +173,8 @@ def _oracle_fns(w):
     from oracle import moe_oracle as O
     if w.dtype == "mxfp8":
         return O.moe_forward_mx, O.moe_backward_mx
+    if w.dtype == "nvfp4":
+        return O.moe_forward_nvfp4, None         # forward-only workloads
     return O.moe_forward, O.moe_backward
 
 
@@ -182,7 +184,7 @@ def oracle_step_timed(w, inp_cpu, tokens: np.ndarray) -> float:
     fwd_fn, bwd_fn = _oracle_fns(w)
     x = inp_cpu["x_np"][tokens]
     sh = dict(w1_shared=inp_cpu["w1s_np"], w2_shared=inp_cpu["w2s_np"])
-    if w.dtype == "mxfp8":
+    if w.dtype != "bf16":
         sh["weight_cache"] = inp_cpu["wcache"]      # weights quantised once, as the recipe does
     t0 = time.perf_counter()
     fwd = fwd_fn(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], k=w.k, score=w.score, bias=inp_cpu["bias_np"],
@@ -209,6 +211,9 @@ def warm_experts(w, inp, tokens):
     for e in np.unique(idx):
         inp["w1"][e]
         inp["w2"][e]
+        if w.dtype == "nvfp4":
+            O.nvfp4_weight(inp["wcache"], "w1", inp["w1"], int(e))
+            O.nvfp4_weight(inp["wcache"], "w2", inp["w2"], int(e))
         if quantised:
             # the recipe quantises weights once; do it here, outside the timed oracle call
             for name, W in (("w1", inp["w1"][e]), ("w2", inp["w2"][e])):
@@ -335,7 +340,25 @@ def run_ours(args) -> dict | None:
     e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
     z = fl["z"] if w.backward else None
     mx = w.dtype == "mxfp8"
-    if mx:
+    nv = w.dtype == "nvfp4"
+    if nv:
+        # the NVFP4 layer permutes quantised codes and leaves x_perm unwritten:
+        # permute x (padding rows zeroed), then quantise it and W1 with the
+        # library's own quantiser into bench-owned buffers
+        cap = layer.layout.cap
+        api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"], fl["poffsets"],
+                        fl["slot_row"], fl["row_src"], fl["row_gate"], fl["x_perm"], 1, layer.ws)
+        xq = torch.empty(cap * w.H // 2, dtype=torch.uint8, device=dev)
+        xsf = torch.empty(cap * w.H // 16, dtype=torch.uint8, device=dev)
+        w1q = torch.empty(dinp["w1"].numel() // 2, dtype=torch.uint8, device=dev)
+        w1sf = torch.empty(dinp["w1"].numel() // 16, dtype=torch.uint8, device=dev)
+        amax = torch.empty(2, dtype=torch.float32, device=dev)
+        api.moe_quantize_nvfp4(fl["x_perm"], 1, cap, w.H, api.MX_ROWS, xq, xsf, amax[0:1])
+        api.moe_quantize_nvfp4(dinp["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP, w1q, w1sf, amax[1:2])
+        fc1_args = (xq, w1q, fl["h"], layer.ws)
+        fc1_kw = dict(c2=None, row_gate=fl["row_gate"], poffsets=fl["poffsets"], a_scales=xsf, b_scales=w1sf,
+                      a_amax=amax[0:1], b_amax=amax[1:2])
+    elif mx:
         # operands quantised by the library's own quantiser into bench-owned buffers
         cap = layer.layout.cap
         xq = torch.empty(cap * w.H, dtype=torch.uint8, device=dev)
@@ -357,7 +380,7 @@ def run_ours(args) -> dict | None:
     torch.cuda.synchronize()
     fc1_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(s_ev, e_ev))
     # the rest of the forward chain, one stage at a time (context for the line)
-    stages = {} if mx else stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, Kk)
+    stages = {} if (mx or nv) else stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, Kk)
     stages["fc1_grouped_gemm"] = fc1_ms
 
     # ---- end to end: host buffers, copies inside the timed region.  Two sets
@@ -379,6 +402,9 @@ def run_ours(args) -> dict | None:
     if mx:
         peak *= 2.0   # dense fp8 / bf16 nominal ratio (4.5 / 2.25 PFLOP/s)
         peak_note = f"2 x bf16_tflops of {peak_src} peaks (fp8:bf16 nominal ratio; burst)"
+    if nv:
+        peak *= 6.0   # dense fp4 / bf16 nominal ratio on GB300 (13.5 / 2.25 PFLOP/s)
+        peak_note = f"6 x bf16_tflops of {peak_src} peaks (fp4:bf16 nominal ratio on GB300; burst)"
     fwd_flop = 6.0 * R * w.H * w.F + 6.0 * w.T * w.H * w.S
     step_flop = fwd_flop * (3 if w.backward else 1)
     out = {
@@ -392,7 +418,7 @@ def run_ours(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp8" if mx else "bf16",
+        "dtype": w.dtype,
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
                    "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
@@ -402,6 +428,7 @@ def run_ours(args) -> dict | None:
         "expert_gemm_tflops_per_gpu": step_flop / (total_ms / K / 1e3) / 1e12,
         "roofline": {"bound": "tensor",
                      "kernel": "fc1 grouped GEMM (tcgen05" + (" mxf8f6f4 block-scaled" if mx else "") +
+                               (" mxf4nvf4 block-scaled" if nv else "") +
                                ", fused gated SwiGLU)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": peak_note,

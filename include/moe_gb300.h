@@ -53,7 +53,7 @@ typedef enum {
 } moe_status;
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
-typedef enum { MOE_GEMM_BF16 = 0, MOE_GEMM_MXFP8 = 1 } moe_gemm_dtype;
+typedef enum { MOE_GEMM_BF16 = 0, MOE_GEMM_MXFP8 = 1, MOE_GEMM_NVFP4 = 2 } moe_gemm_dtype;
 
 /* Layer shape.
  *   T tokens, H hidden, E routed experts, k experts per token, F routed expert
@@ -68,7 +68,8 @@ typedef enum { MOE_GEMM_BF16 = 0, MOE_GEMM_MXFP8 = 1 } moe_gemm_dtype;
 typedef struct {
   int32_t T, H, E, k, F, S;
   int32_t score;   /* moe_score_fn */
-  int32_t dtype;   /* moe_gemm_dtype; MOE_GEMM_MXFP8 also needs T % 128 == 0 */
+  int32_t dtype;   /* moe_gemm_dtype; MXFP8 and NVFP4 also need T % 128 == 0, NVFP4
+                      H, F, S multiples of 256 (NVFP4 layers run forward only) */
 } moe_config;
 
 /* Weights (device, bf16 unless noted).
@@ -82,8 +83,8 @@ typedef struct {
   const void* w2;
   const void* w1_shared;
   const void* w2_shared;
-  /* MOE_GEMM_MXFP8 only: the buffer moe_prepare_mxfp8_weights filled from the
-   * weights above (NULL for bf16). */
+  /* MOE_GEMM_MXFP8 / MOE_GEMM_NVFP4 only: the buffer moe_prepare_mxfp8_weights
+   * or moe_prepare_nvfp4_weights filled from the weights above (NULL for bf16). */
   const void* mx;
 } moe_weights;
 
@@ -250,7 +251,14 @@ typedef enum {
  *   DGRAD_FC1:  a = dz [cap,2F]; b = W1^T [E,H,2F] (MOE_MX_COLS_T of w1).
  *   WGRAD_FC1:  a = dz^T [2F,cap], b = x_perm^T [H,cap] (MOE_MX_COLS_T).
  *   WGRAD_FC2:  a = dy_perm^T [H,cap], b = h^T [F,cap] (MOE_MX_COLS_T).
- * Dense calls need dense_rows % 128 == 0. */
+ * Dense calls need dense_rows % 128 == 0.
+ * NVFP4 (dtype == MOE_GEMM_NVFP4; forward ops only, the others return
+ * MOE_ERR_UNSUPPORTED): a and b are E2M1 codes (see moe_quantize_nvfp4),
+ * a_scales / b_scales their E4M3 scale tiles and a_amax / b_amax (device, one
+ * fp32 each) the tensor amaxes they were quantised with.
+ *   FC1_SWIGLU: a = x_perm codes [cap,H/2]; b = W1 codes, gate/up interleaved
+ *               (MOE_MX_ROWS_GATE_UP of w1).
+ *   FC2:        a = h codes [cap,F/2]; b = W2 codes [E*H,F/2] (MOE_MX_ROWS). */
 typedef struct {
   int32_t op;             /* moe_gg_op */
   int32_t dense_rows;     /* 0: routed; >0: one dense group of this many rows */
@@ -262,8 +270,10 @@ typedef struct {
   const float* row_gate;
   float* dgate_part;
   const int32_t* poffsets;
-  const void* a_scales;   /* MXFP8 only */
-  const void* b_scales;   /* MXFP8 only */
+  const void* a_scales;   /* MXFP8 / NVFP4 only */
+  const void* b_scales;   /* MXFP8 / NVFP4 only */
+  const float* a_amax;    /* NVFP4 only */
+  const float* b_amax;    /* NVFP4 only */
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For
@@ -318,13 +328,49 @@ moe_status moe_prepare_mxfp8_weights(const moe_config* cfg, const moe_weights* w
                                      void* stream);
 
 /* --------------------------------------------------------------------------
+ * NVFP4 (technical summary 2.5 names NVFP4 beside MXFP8 for the expert GEMMs;
+ * the format's own definition is taken as the recipe; forward GEMMs only).
+ * Element type E2M1 (0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives), two codes per
+ * byte with the lower-indexed element in the low nibble; one unsigned E4M3
+ * scale per block of 16 values along the contraction; one fp32 tensor scale
+ * S = 2688 / amax (1 if amax == 0).  With d = fp32(amax_b / 6), all in fp32:
+ * s = e4m3(d * S) (nearest even, saturated to 448), r = S / s (0 if s == 0),
+ * code = e2m1(v * r) (nearest even, saturated to +-6); value = e2m1 * s / S.
+ * Scale tiles: for codes of a [R, C] matrix (R % 128 == 0, C % 64 == 0) the
+ * R*C/16 scale bytes form 512-byte tiles, tile (i, j) covering rows
+ * 128i..128i+127 and blocks 4j..4j+3 (columns 64j..64j+63) at byte
+ * (i*(C/64) + j)*512; inside a tile the scale of row r, block b is at
+ * (r%32)*16 + (r/32)*4 + b.
+ * ----------------------------------------------------------------------- */
+
+/* Quantise a bf16 tensor [batch*rows, cols] to NVFP4 along its rows (mode
+ * MOE_MX_ROWS, or MOE_MX_ROWS_GATE_UP as for MXFP8).  Writes the tensor's
+ * amax (fp32) to *amax (device) first, then codes (batch*rows*cols/2 bytes)
+ * and scales (batch*rows*cols/16 bytes).  cols % 64 == 0, batch*rows % 128 == 0;
+ * ROWS_GATE_UP: rows % 256 == 0.  Inputs must be finite. */
+moe_status moe_quantize_nvfp4(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t mode,
+                              uint8_t* codes, uint8_t* scales, float* amax, void* stream);
+
+/* Bytes of the quantised-weight buffer an NVFP4 layer needs (moe_weights.mx);
+ * 0 unless cfg->dtype == MOE_GEMM_NVFP4. */
+size_t moe_nvfp4_weights_bytes(const moe_config* cfg);
+
+/* Quantise w1 (gate/up interleaved), w2 and the shared expert once into the
+ * buffer, each with its own tensor amax.  Call again after every weight update. */
+moe_status moe_prepare_nvfp4_weights(const moe_config* cfg, const moe_weights* w, void* buf, size_t bytes,
+                                     void* stream);
+
+/* --------------------------------------------------------------------------
  * Whole layer
  * ----------------------------------------------------------------------- */
 
 /* Forward: y = sum_i g_i SwiGLU_{e_i}(x) (+ SharedSwiGLU(x)).
  * x [T,H] bf16, y [T,H] bf16.  `act` holds everything backward needs (layout
  * from moe_activation_layout(cfg, with_backward)); with_backward = 1 also
- * zeroes the padding rows.  Fixed number of launches; no host sync. */
+ * zeroes the padding rows.  Fixed number of launches; no host sync.
+ * NVFP4 layers: with_backward must be 0 (MOE_ERR_UNSUPPORTED otherwise); x is
+ * quantised per token and its codes permuted, so x_perm is left unwritten.
+ * The backward calls return MOE_ERR_UNSUPPORTED for NVFP4 layers. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, void* act,
                              size_t act_bytes, int32_t with_backward, void* ws, size_t ws_bytes, void* stream);
 

@@ -17,6 +17,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error", -4: "workspace too small",
                 -5: "bad expert index", -6: "device wait timed out"}
 SCORE = {"softmax": 0, "sigmoid": 1}
+GEMM_DTYPE = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
 
 GG_FC1_SWIGLU, GG_FC2, GG_DGRAD_FC2, GG_DGRAD_FC1, GG_WGRAD_FC1, GG_WGRAD_FC2 = range(6)
 MX_ROWS, MX_COLS_T, MX_ROWS_GATE_UP = range(3)
@@ -52,7 +53,7 @@ class MoeActLayout(ctypes.Structure):
 class MoeGemmArgs(ctypes.Structure):
     _fields_ = [("op", c_i32), ("dense_rows", c_i32), ("a", c_vp), ("b", c_vp), ("c", c_vp), ("c2", c_vp),
                 ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp),
-                ("a_scales", c_vp), ("b_scales", c_vp)]
+                ("a_scales", c_vp), ("b_scales", c_vp), ("a_amax", c_vp), ("b_amax", c_vp)]
 
 
 _P = ctypes.POINTER
@@ -76,6 +77,9 @@ _SIGS = {
     "moe_quantize_mxfp8": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "moe_mxfp8_weights_bytes": (c_sz, [_P(MoeConfig)]),
     "moe_prepare_mxfp8_weights": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_sz, c_vp]),
+    "moe_quantize_nvfp4": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
+    "moe_nvfp4_weights_bytes": (c_sz, [_P(MoeConfig)]),
+    "moe_prepare_nvfp4_weights": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_sz, c_vp]),
     "moe_layer_forward": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_sz, c_i32, c_vp, c_sz,
                                   c_vp]),
     "moe_layer_backward_dgrad": (c_i32, [_P(MoeConfig), _P(MoeWeights), c_vp, c_vp, c_vp, c_vp, c_vp, c_sz,
@@ -138,7 +142,7 @@ def stream_ptr(stream=None) -> int | None:
 
 def make_config(T, H, E, k, F, S=0, score="softmax", dtype="bf16") -> MoeConfig:
     return MoeConfig(T, H, E, k, F, S, SCORE[score] if isinstance(score, str) else int(score),
-                     0 if dtype == "bf16" else 1)
+                     GEMM_DTYPE[dtype] if isinstance(dtype, str) else int(dtype))
 
 
 def config_of(workload, tokens: int | None = None) -> MoeConfig:
@@ -200,9 +204,9 @@ def moe_permute_noalloc(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, 
 
 
 def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
-                     dense_rows=0, a_scales=None, b_scales=None, stream=None) -> None:
+                     dense_rows=0, a_scales=None, b_scales=None, a_amax=None, b_amax=None, stream=None) -> None:
     args = MoeGemmArgs(op, dense_rows, ptr(a), ptr(b), ptr(c), ptr(c2), ptr(aux), ptr(row_gate), ptr(dgate_part),
-                       ptr(poffsets), ptr(a_scales), ptr(b_scales))
+                       ptr(poffsets), ptr(a_scales), ptr(b_scales), ptr(a_amax), ptr(b_amax))
     check(load().moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), ptr(ws), stream_ptr(stream)),
           "moe_grouped_gemm")
 
@@ -220,6 +224,21 @@ def moe_prepare_mxfp8_weights(cfg, weights: MoeWeights, mx, stream=None) -> None
     check(load().moe_prepare_mxfp8_weights(ctypes.byref(cfg), ctypes.byref(weights), ptr(mx),
                                            mx.numel() * mx.element_size(), stream_ptr(stream)),
           "moe_prepare_mxfp8_weights")
+
+
+def moe_quantize_nvfp4(src, batch, rows, cols, mode, codes, scales, amax, stream=None) -> None:
+    check(load().moe_quantize_nvfp4(ptr(src), batch, rows, cols, mode, ptr(codes), ptr(scales), ptr(amax),
+                                    stream_ptr(stream)), "moe_quantize_nvfp4")
+
+
+def moe_nvfp4_weights_bytes(cfg) -> int:
+    return int(load().moe_nvfp4_weights_bytes(ctypes.byref(cfg)))
+
+
+def moe_prepare_nvfp4_weights(cfg, weights: MoeWeights, buf, stream=None) -> None:
+    check(load().moe_prepare_nvfp4_weights(ctypes.byref(cfg), ctypes.byref(weights), ptr(buf),
+                                           buf.numel() * buf.element_size(), stream_ptr(stream)),
+          "moe_prepare_nvfp4_weights")
 
 
 def moe_unpermute(cfg, o_perm, slot_row, shared_out, y, stream=None) -> None:
@@ -267,14 +286,20 @@ class MoELayer:
                              ptr(weights["w2"]), ptr(weights.get("w1_shared")), ptr(weights.get("w2_shared")),
                              None)
         self.mx = None
-        if cfg.dtype == 1:
+        if cfg.dtype == GEMM_DTYPE["mxfp8"]:
             self.mx = torch.empty(moe_mxfp8_weights_bytes(cfg), dtype=torch.uint8, device=device)
+        elif cfg.dtype == GEMM_DTYPE["nvfp4"]:
+            self.mx = torch.empty(moe_nvfp4_weights_bytes(cfg), dtype=torch.uint8, device=device)
+        if self.mx is not None:
             self.cw.mx = ptr(self.mx)
             self.prepare_weights()
 
     def prepare_weights(self, stream=None) -> None:
-        """(MXFP8) quantise the weights into the layer's buffer; call after a weight update."""
-        moe_prepare_mxfp8_weights(self.cfg, self.cw, self.mx, stream)
+        """(MXFP8 / NVFP4) quantise the weights into the layer's buffer; call after a weight update."""
+        if self.cfg.dtype == GEMM_DTYPE["nvfp4"]:
+            moe_prepare_nvfp4_weights(self.cfg, self.cw, self.mx, stream)
+        else:
+            moe_prepare_mxfp8_weights(self.cfg, self.cw, self.mx, stream)
 
     def view(self, name: str, dtype, shape) -> torch.Tensor:
         off = getattr(self.layout, name)

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
-SOURCES = ["api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_mx.cu", "mxfp8.cu", "permute_noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_mx.cu", "mxfp8.cu", "nvfp4.cu", "permute_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-Xptxas", "-warn-spills"]

@@ -68,8 +68,10 @@ bool config_ok(const moe_config* c) {
   if (c->k > kMaxK || c->k > c->E || c->E > kMaxE) return false;
   if (c->H % 128 || c->F % 128 || c->S % 128) return false;
   if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return false;
-  if (c->dtype != MOE_GEMM_BF16 && c->dtype != MOE_GEMM_MXFP8) return false;
-  if (c->dtype == MOE_GEMM_MXFP8 && c->T % 128 != 0) return false;   // whole 128-row scale tiles
+  if (c->dtype != MOE_GEMM_BF16 && c->dtype != MOE_GEMM_MXFP8 && c->dtype != MOE_GEMM_NVFP4) return false;
+  if (c->dtype != MOE_GEMM_BF16 && c->T % 128 != 0) return false;   // whole 128-row scale tiles
+  // NVFP4: 256-element k-blocks along H, F and S
+  if (c->dtype == MOE_GEMM_NVFP4 && (c->H % 256 || c->F % 256 || c->S % 256)) return false;
   const long long pairs = static_cast<long long>(c->T) * c->k;
   if (pairs + 128LL * c->E >= (1LL << 31)) return false;
   return true;
@@ -82,6 +84,7 @@ int cap_rows(const moe_config* c) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dev_ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+bool f32_ptr_ok(const float* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -228,6 +231,66 @@ MxW mx_weight_layout(const moe_config* c) {
 
 size_t mx_ws_base(const moe_config* c) { return kStatusBytes + align_up(hist_bytes(c)); }
 
+// ---------------------------------------------------------------- NVFP4 buffers
+// E2M1 codes (elems / 2 bytes) and E4M3 scale tiles (elems / 16 bytes), and
+// one fp32 amax per quantised tensor.
+struct Nv4Buf {
+  size_t q = kNone, sf = kNone;
+};
+
+Nv4Buf nv4_buf(size_t& off, size_t elems) {
+  Nv4Buf b;
+  b.q = off;
+  off = align_up(off + (elems / 2 ? elems / 2 : 1));
+  b.sf = off;
+  off = align_up(off + (elems / 16 ? elems / 16 : 1));
+  return b;
+}
+
+// Forward activations: x quantised per token (xs) and gathered into expert
+// order (x), h (expert order), hs (shared expert); amax slots x, h, hs.
+struct Nv4Ws {
+  Nv4Buf x, h, xs, hs;
+  size_t amax = kNone;
+  size_t total = 0;
+};
+
+Nv4Ws nv4_ws_layout(const moe_config* c) {
+  Nv4Ws m;
+  const size_t T = c->T, H = c->H, F = c->F, S = c->S, cap = static_cast<size_t>(cap_rows(c));
+  size_t off = 0;
+  m.amax = off;
+  off = align_up(off + 4 * sizeof(float));
+  m.x = nv4_buf(off, cap * H);
+  m.h = nv4_buf(off, cap * F);
+  m.xs = nv4_buf(off, T * H);
+  if (S) m.hs = nv4_buf(off, T * S);
+  m.total = off;
+  return m;
+}
+
+// Weights, prepared once by moe_prepare_nvfp4_weights: w1 (gate/up rows
+// interleaved in 128-row blocks), w2, and the shared expert's; amax slots w1,
+// w2, s1, s2.
+struct Nv4W {
+  Nv4Buf w1, w2, s1, s2;
+  size_t amax = kNone;
+  size_t total = 0;
+};
+
+Nv4W nv4_weight_layout(const moe_config* c) {
+  Nv4W m;
+  const size_t H = c->H, E = c->E, F = c->F, S = c->S;
+  size_t off = 0;
+  m.amax = off;
+  off = align_up(off + 4 * sizeof(float));
+  m.w1 = nv4_buf(off, E * 2 * F * H);
+  m.w2 = nv4_buf(off, E * H * F);
+  if (S) { m.s1 = nv4_buf(off, 2 * S * H); m.s2 = nv4_buf(off, H * S); }
+  m.total = off;
+  return m;
+}
+
 moe_status check_device() { return device_is_gb300() ? MOE_OK : MOE_ERR_UNSUPPORTED; }
 
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
@@ -264,6 +327,7 @@ size_t moe_workspace_bytes(const moe_config* cfg) {
   if (!config_ok(cfg)) return 0;
   size_t b = kStatusBytes + align_up(hist_bytes(cfg));
   if (cfg->dtype == MOE_GEMM_MXFP8) b += mx_ws_layout(cfg).total;
+  if (cfg->dtype == MOE_GEMM_NVFP4) b += nv4_ws_layout(cfg).total;
   return b;
 }
 
@@ -318,6 +382,58 @@ moe_status moe_prepare_mxfp8_weights(const moe_config* cfg, const moe_weights* w
     MOE_TRY(launch_quantize_rows(w->w2_shared, H, S, 0, q(L.s2), f(L.s2), st));
     MOE_TRY(launch_quantize_cols(w->w1_shared, 1, 2 * S, H, q(L.s1t), f(L.s1t), st));
     MOE_TRY(launch_quantize_cols(w->w2_shared, 1, H, S, q(L.s2t), f(L.s2t), st));
+  }
+  return MOE_OK;
+}
+
+size_t moe_nvfp4_weights_bytes(const moe_config* cfg) {
+  if (!config_ok(cfg) || cfg->dtype != MOE_GEMM_NVFP4) return 0;
+  return nv4_weight_layout(cfg).total;
+}
+
+moe_status moe_quantize_nvfp4(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t mode,
+                              uint8_t* codes, uint8_t* scales, float* amax, void* stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  if (!f32_ptr_ok(amax)) return MOE_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(batch) * rows * cols;
+  if (n > 0 && (!dev_ptr_ok(src) || !dev_ptr_ok(codes) || !dev_ptr_ok(scales))) return MOE_ERR_INVALID_ARG;
+  if (cols % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if ((static_cast<long long>(batch) * rows) % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (mode == MOE_MX_ROWS_GATE_UP && rows % 256 != 0) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_MX_ROWS && mode != MOE_MX_ROWS_GATE_UP) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long R = static_cast<long long>(batch) * rows;
+  MOE_TRY(launch_amax_bf16(src, R, cols, nullptr, nullptr, amax, st));
+  return cuda_status(
+      launch_quantize_rows_nv4(src, R, cols, mode == MOE_MX_ROWS_GATE_UP ? rows / 2 : 0, amax, codes, scales, st));
+}
+
+moe_status moe_prepare_nvfp4_weights(const moe_config* cfg, const moe_weights* w, void* buf, size_t bytes,
+                                     void* stream) {
+  if (!config_ok(cfg) || cfg->dtype != MOE_GEMM_NVFP4 || w == nullptr || !dev_ptr_ok(buf) || !dev_ptr_ok(w->w1) ||
+      !dev_ptr_ok(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
+  const Nv4W L = nv4_weight_layout(cfg);
+  if (bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (moe_status s = check_device(); s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long H = cfg->H, E = cfg->E, F = cfg->F, S = cfg->S;
+  float* amax = at<float>(buf, L.amax);
+  auto q = [&](const Nv4Buf& b) { return at<uint8_t>(buf, b.q); };
+  auto f = [&](const Nv4Buf& b) { return at<uint8_t>(buf, b.sf); };
+  MOE_TRY(launch_amax_bf16(w->w1, E * 2 * F, static_cast<int>(H), nullptr, nullptr, amax + 0, st));
+  MOE_TRY(launch_quantize_rows_nv4(w->w1, E * 2 * F, static_cast<int>(H), static_cast<int>(F), amax + 0, q(L.w1),
+                                   f(L.w1), st));
+  MOE_TRY(launch_amax_bf16(w->w2, E * H, static_cast<int>(F), nullptr, nullptr, amax + 1, st));
+  MOE_TRY(launch_quantize_rows_nv4(w->w2, E * H, static_cast<int>(F), 0, amax + 1, q(L.w2), f(L.w2), st));
+  if (S > 0) {
+    MOE_TRY(launch_amax_bf16(w->w1_shared, 2 * S, static_cast<int>(H), nullptr, nullptr, amax + 2, st));
+    MOE_TRY(launch_quantize_rows_nv4(w->w1_shared, 2 * S, static_cast<int>(H), static_cast<int>(S), amax + 2,
+                                     q(L.s1), f(L.s1), st));
+    MOE_TRY(launch_amax_bf16(w->w2_shared, H, static_cast<int>(S), nullptr, nullptr, amax + 3, st));
+    MOE_TRY(launch_quantize_rows_nv4(w->w2_shared, H, static_cast<int>(S), 0, amax + 3, q(L.s2), f(L.s2), st));
   }
   return MOE_OK;
 }
@@ -390,6 +506,27 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
   const int rows = dense ? a->dense_rows : cap_rows(cfg);
   const int32_t* po = dense ? nullptr : a->poffsets;
   int* status = status_ptr(ws);
+  if (cfg->dtype == MOE_GEMM_NVFP4) {
+    if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales) || !f32_ptr_ok(a->a_amax) || !f32_ptr_ok(a->b_amax))
+      return MOE_ERR_INVALID_ARG;
+    if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+    switch (a->op) {
+      case MOE_GG_FC1_SWIGLU:
+        if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
+        return cuda_status(gemm_nv4_fc1(a->a, a->a_scales, a->a_amax, rows, H, a->b, a->b_scales, a->b_amax, E, F, po,
+                                        a->dense_rows, a->row_gate, a->c, a->c2, status, st));
+      case MOE_GG_FC2:
+        return cuda_status(gemm_nv4_nt_bf16(a->a, a->a_scales, a->a_amax, rows, F, a->b, a->b_scales, a->b_amax, E, H,
+                                            po, a->dense_rows, a->c, status, st));
+      case MOE_GG_DGRAD_FC2:
+      case MOE_GG_DGRAD_FC1:
+      case MOE_GG_WGRAD_FC1:
+      case MOE_GG_WGRAD_FC2:
+        return MOE_ERR_UNSUPPORTED;            // NVFP4: forward GEMMs only
+      default:
+        return MOE_ERR_INVALID_ARG;
+    }
+  }
   if (cfg->dtype == MOE_GEMM_MXFP8) {
     if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
     if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
@@ -460,7 +597,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(y))) return MOE_ERR_INVALID_ARG;
   if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
   if (w->router_bias != nullptr && !aligned16(w->router_bias)) return MOE_ERR_INVALID_ARG;
-  if (cfg->dtype == MOE_GEMM_MXFP8 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype != MOE_GEMM_BF16 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_NVFP4 && with_backward) return MOE_ERR_UNSUPPORTED;   // NVFP4: forward only
   if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (moe_status s = check_device(); s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -483,13 +621,47 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   MOE_TRY(launch_topk_permute_maps(logits, cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr, T, E, k,
                                    cfg->score, idx, gate, hist_ptr(ws), counts, at<int32_t>(act, L.offsets), poff,
                                    slot_row, at<int32_t>(act, L.row_src), row_gate, st));
-  MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
+  // (NVFP4 layers permute the quantised codes instead; x_perm stays unwritten)
+  if (cfg->dtype != MOE_GEMM_NVFP4) MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
   if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
   // 5-6: grouped expert GEMMs; the gate multiplies the SwiGLU output inside fc1
   void* z = with_backward ? at<void>(act, L.z) : nullptr;
   void* zs = with_backward && S > 0 ? at<void>(act, L.zs) : nullptr;
   const void* shared_out = nullptr;
-  if (cfg->dtype == MOE_GEMM_MXFP8) {
+  if (cfg->dtype == MOE_GEMM_NVFP4) {
+    // NVFP4 expert GEMMs (forward): x quantised once per token with the tensor
+    // scale of all of x, codes permuted into expert order; h quantised with
+    // the tensor scale of its valid rows (row_src >= 0); weights prepared once.
+    const Nv4Ws M = nv4_ws_layout(cfg);
+    const Nv4W W = nv4_weight_layout(cfg);
+    char* mb = static_cast<char*>(ws) + mx_ws_base(cfg);
+    auto q = [&](const Nv4Buf& b) { return reinterpret_cast<uint8_t*>(mb + b.q); };
+    auto f = [&](const Nv4Buf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
+    auto wq = [&](const Nv4Buf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
+    auto wf = [&](const Nv4Buf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
+    float* amax = reinterpret_cast<float*>(mb + M.amax);
+    const float* wamax = at<const float>(const_cast<void*>(w->mx), W.amax);
+    MOE_TRY(launch_amax_bf16(x, T, H, nullptr, nullptr, amax + 0, st));
+    MOE_TRY(launch_quantize_rows_nv4(x, T, H, 0, amax + 0, q(M.xs), f(M.xs), st));
+    MOE_TRY(launch_gather_rows_nv4(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st));
+    MOE_TRY(gemm_nv4_fc1(q(M.x), f(M.x), amax + 0, cap, H, wq(W.w1), wf(W.w1), wamax + 0, E, F, poff, 0, row_gate, h,
+                         nullptr, status, st));
+    // rows past the last expert's segment are never written: bounded by poffsets[E]
+    MOE_TRY(launch_amax_bf16(h, cap, F, at<int32_t>(act, L.row_src), poff + E, amax + 1, st));
+    MOE_TRY(launch_quantize_rows_nv4(h, cap, F, 0, amax + 1, q(M.h), f(M.h), st));
+    MOE_TRY(gemm_nv4_nt_bf16(q(M.h), f(M.h), amax + 1, cap, F, wq(W.w2), wf(W.w2), wamax + 1, E, H, poff, 0, o, status,
+                             st));
+    if (S > 0 && T > 0) {
+      void* hs = at<void>(act, L.hs);
+      MOE_TRY(gemm_nv4_fc1(q(M.xs), f(M.xs), amax + 0, T, H, wq(W.s1), wf(W.s1), wamax + 2, 1, S, nullptr, T, nullptr,
+                           hs, nullptr, status, st));
+      MOE_TRY(launch_amax_bf16(hs, T, S, nullptr, nullptr, amax + 2, st));
+      MOE_TRY(launch_quantize_rows_nv4(hs, T, S, 0, amax + 2, q(M.hs), f(M.hs), st));
+      MOE_TRY(gemm_nv4_nt_bf16(q(M.hs), f(M.hs), amax + 2, T, S, wq(W.s2), wf(W.s2), wamax + 3, 1, H, nullptr, T,
+                               at<void>(act, L.os), status, st));
+      shared_out = at<void>(act, L.os);
+    }
+  } else if (cfg->dtype == MOE_GEMM_MXFP8) {
     // MXFP8 expert GEMMs: activations quantised (blocks of 32 along K) on the
     // way in, weights prepared once; router, gates and combine stay fp32/bf16.
     const MxWs M = mx_ws_layout(cfg);
@@ -539,6 +711,7 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
   if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(dy) || !dev_ptr_ok(dx))) return MOE_ERR_INVALID_ARG;
   if (cfg->S > 0 && (!dev_ptr_ok(w->w1_shared) || !dev_ptr_ok(w->w2_shared))) return MOE_ERR_INVALID_ARG;
   if (dgate != nullptr && !aligned16(dgate)) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_NVFP4) return MOE_ERR_UNSUPPORTED;   // NVFP4: forward only
   if (cfg->dtype == MOE_GEMM_MXFP8 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
   if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (moe_status s = check_device(); s != MOE_OK) return s;
@@ -607,6 +780,7 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!dev_ptr_ok(x) || !dev_ptr_ok(dy))) return MOE_ERR_INVALID_ARG;
   if (cfg->S > 0 && (!dev_ptr_ok(g->dw1_shared) || !dev_ptr_ok(g->dw2_shared))) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_NVFP4) return MOE_ERR_UNSUPPORTED;   // NVFP4: forward only
   if (cfg->dtype == MOE_GEMM_MXFP8 && !dev_ptr_ok(w->mx)) return MOE_ERR_INVALID_ARG;
   if (act_bytes < L.total || ws_bytes < moe_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (moe_status s = check_device(); s != MOE_OK) return s;

@@ -21,6 +21,7 @@
 // summary describes (technical summary 2.4, grouped GEMM and sync-free
 // kernels).
 #pragma once
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -59,17 +60,22 @@ struct GemmParams {
   float* dgate_part;       // kSwigluBwd: [rows, n_tiles] partial dot products
   int valid_cols;          // kStoreF32: store only columns < valid_cols
   int rows_cap;            // rows allocated in the expert-ordered buffers (routed modes)
-  // MXFP8 only: E8M0 scale tiles of A and B (512 B per 128 rows x 128 K, see
-  // mxfp8.cu) and the number of tiles along K in one 128-row band of each.
+  // MXFP8 / NVFP4: scale tiles of A and B (512 B per 128 rows x 128 K of
+  // E8M0, or x 64 K of E4M3; see mxfp8.cu, nvfp4.cu) and the number of tiles
+  // along K in one 128-row band of each.
   const uint8_t* sfa;
   const uint8_t* sfb;
   int sfa_tiles_k;
   int sfb_tiles_k;
+  // NVFP4: the tensor amax of A and of B (device); the accumulator is
+  // multiplied by 1 / (S_a * S_b) before the epilogue's arithmetic.
+  const float* amax_a;
+  const float* amax_b;
   int* status;             // device status word (first error wins)
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
 };
 
-template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, bool MX_ = false, bool M256_ = false,
+template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, int MX_ = 0, bool M256_ = false,
           bool PAIR_ = false>
 struct GemmCfg {
   static constexpr int BM = 128;                  // rows of A and D per CTA and MMA
@@ -77,24 +83,28 @@ struct GemmCfg {
   static constexpr bool PAIR = PAIR_;             // 256-row tiles on a CTA pair (cta_group::2)
   static constexpr bool ROWS256 = M256 || PAIR;   // tiles of 256 rows (pairs of 128-row blocks)
   static constexpr int TILE_M = ROWS256 ? 256 : 128;
-  static constexpr bool MX = MX_;                 // MXFP8 operands (E4M3 + E8M0 1x32 scales)
+  static constexpr bool MX = MX_ != 0;            // block-scaled operands: 1 MXFP8, 2 NVFP4
+  static constexpr bool NV4 = MX_ == 2;           // NVFP4 (E2M1 + E4M3 1x16 scales + tensor scale)
   // Contraction elements per k-block: one 128-byte swizzle row (K-major), or
   // for the weight gradients on CTA pairs (MN-major, short per-expert K) 128
   // token rows, so each TMA box is 16 KB instead of 8 KB.
   static constexpr bool WIDE_K = PAIR_ && (S_ == Sched::kRoutedK);
-  static constexpr int BK = MX ? 128 : (WIDE_K ? 128 : 64);
+  static constexpr int BK = NV4 ? 256 : MX ? 128 : (WIDE_K ? 128 : 64);   // elements (128 B K-major rows)
   static constexpr int MN_CHUNK = BK * 128;       // MN-major: bytes of one 64-wide MN chunk (BK rows of 128 B)
-  static constexpr int KSTEP = MX ? 32 : 16;      // K of one MMA instruction
+  static constexpr int KSTEP = NV4 ? 64 : MX ? 32 : 16;   // K of one MMA instruction (32 bytes)
   static constexpr int BN = BN_;
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
   static constexpr Sched S = S_;
   static constexpr Epi EP = EP_;
-  static constexpr int ROW_BYTES = MX ? BK : BK * 2;         // bytes of one A / B row of a k-block
+  static constexpr int ROW_BYTES = NV4 ? BK / 2 : MX ? BK : BK * 2;   // bytes of one A / B row of a k-block
   static constexpr int A_BYTES = (M256 ? 256 : 128) * ROW_BYTES;   // this CTA's A rows of one k-block
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * ROW_BYTES;  // this CTA's B rows (a pair splits N)
-  static constexpr int SFA_BYTES = MX ? 512 : 0;
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  // scale tiles of one k-block: one 512-byte tile per 128 rows (MXFP8), four
+  // (one per MMA of K = 64) for NVFP4
+  static constexpr int SF_TILES_KB = NV4 ? 4 : 1;
+  static constexpr int SFA_BYTES = MX ? 512 * SF_TILES_KB : 0;
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 * SF_TILES_KB : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   // Outputs leave through TMA stores staged in shared memory (every epilogue
   // but the router's narrow fp32 logits, whose rows need not be 16-byte sized).
@@ -127,7 +137,8 @@ struct GemmCfg {
   static constexpr int SF_REGION = (STAGES * (SFA_BYTES + SFB_BYTES) + 1023) / 1024 * 1024;
   static constexpr int SMEM_USED = STAGES * (A_BYTES + B_BYTES) + SF_REGION + STAGING_BYTES + BOOK_BYTES;
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
-  static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;   // TMEM columns of one stage's scales
+  // TMEM columns of one stage's scales (4 per 128 rows and scale tile)
+  static constexpr int SF_COLS = MX ? SF_TILES_KB * (4 + 4 * (BN / 128)) : 0;
   // TMEM accumulators: two (epilogue of tile i overlaps MMAs of tile i+1),
   // or one where two would not fit next to the scales (MXFP8, N=256) or in
   // 512 columns at all (256-row tiles of N=256: 2 x 256 columns per tile).
@@ -142,11 +153,15 @@ struct GemmCfg {
   // Columns of the output a tile covers (SwiGLU: half of the accumulator).
   static constexpr int OUT_COLS = (EP == Epi::kSwiglu) ? BN / 2 : BN;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr uint32_t IDESC = MX ? idesc_mxf8_e4m3(BM, BN) : idesc_bf16_f32(PAIR ? 256 : BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = NV4  ? idesc_nvf4_e2m1(BM, BN)
+                                    : MX  ? idesc_mxf8_e4m3(BM, BN)
+                                          : idesc_bf16_f32(PAIR ? 256 : BM, BN, A_MN, B_MN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
   static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile: 128 gate + 128 matching up columns");
   static_assert(!MX || (BN % 128 == 0 && !A_MN && !B_MN), "MXFP8 operands are K-major, 128-row scale tiles");
+  static_assert(!NV4 || (S != Sched::kRoutedK && EP != Epi::kSwigluBwd && EP != Epi::kStoreF32),
+                "NVFP4: forward GEMMs (bf16 or SwiGLU epilogue)");
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
   static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
@@ -279,14 +294,17 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
       b_row = ti.group * p.b_rows_per_group + ti.n * C::BN;
       k_col = k0;
     }
-    tma_load_2d(a_dst, tmA, bar, k_col, a_row);
-    tma_load_2d(b_dst, tmB, bar, k_col, b_row);
-    const int kt = k_col / 128;
-    bulk_load(sf_dst, p.sfa + ((long long)(a_row / 128) * p.sfa_tiles_k + kt) * 512, 512, bar);
+    // the TMA maps count bytes along K: two E2M1 codes per byte for NVFP4
+    const int k_byte = C::NV4 ? k_col / 2 : k_col;
+    tma_load_2d(a_dst, tmA, bar, k_byte, a_row);
+    tma_load_2d(b_dst, tmB, bar, k_byte, b_row);
+    // scale tiles of this k-block: contiguous along K within a 128-row band
+    constexpr int TB = 512 * C::SF_TILES_KB;
+    const int kt = k_col / (C::NV4 ? 64 : 128);
+    bulk_load(sf_dst, p.sfa + ((long long)(a_row / 128) * p.sfa_tiles_k + kt) * 512, TB, bar);
     #pragma unroll
     for (int i = 0; i < C::BN / 128; ++i)
-      bulk_load(sf_dst + 512 * (i + 1), p.sfb + ((long long)(b_row / 128 + i) * p.sfb_tiles_k + kt) * 512, 512,
-                bar);
+      bulk_load(sf_dst + TB * (i + 1), p.sfb + ((long long)(b_row / 128 + i) * p.sfb_tiles_k + kt) * 512, TB, bar);
     return;
   }
   // ---- A
@@ -397,6 +415,18 @@ __device__ __forceinline__ void load32(uint32_t taddr, uint32_t (&a)[16], uint32
   tmem_ld_wait(b);
 }
 
+// Factor `al` the epilogue applies to the accumulator before its arithmetic:
+// NVFP4 GEMMs multiply the block-scaled codes, so the tensor scales 1/S_a and
+// 1/S_b are still owed; 1 otherwise.  Computed once per CTA.
+template <class C>
+__device__ __forceinline__ float acc_scale(const GemmParams& p) {
+  if constexpr (C::NV4) {
+    return (1.0f / nv4_tensor_scale(*p.amax_a)) * (1.0f / nv4_tensor_scale(*p.amax_b));
+  } else {
+    return 1.0f;
+  }
+}
+
 // Epilogue with TMA stores.  Rows of the tile: warp quarter q owns rows
 // 32q..32q+31, lane = row.  Dense tiles past the last row are clipped by TMA.
 template <class C>
@@ -404,7 +434,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
                                                   int quarter, int lane, Stager<C::STAGING_BUFS>& st,
                                                   const CUtensorMap* tmC,
                                                   const CUtensorMap* tmC2,
-                                                  uint64_t* release_bar = nullptr, bool* released = nullptr) {
+                                                  uint64_t* release_bar = nullptr, bool* released = nullptr,
+                                                  const float al = 1.0f) {
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t t0 = tmem_acc + lane_addr;
   const bool no_mma = (ti.num_kb == 0);         // empty group (weight gradients): result is zero
@@ -486,7 +517,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           for (int u = 0; u < 2; ++u)
             #pragma unroll
             for (int j = 0; j < 8; ++j)
-              pk[8 * (h + u) + j] = pack_bf16x2(__uint_as_float(v[u][2 * j]), __uint_as_float(v[u][2 * j + 1]));
+              pk[8 * (h + u) + j] = pack_bf16x2(__uint_as_float(v[u][2 * j]) * al,
+                                                __uint_as_float(v[u][2 * j + 1]) * al);
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -517,7 +549,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
       for (int h = 0; h < 4; ++h) {
         uint32_t w[8];
         #pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(v[h][2 * j]), __uint_as_float(v[h][2 * j + 1]));
+        for (int j = 0; j < 8; ++j)
+          w[j] = pack_bf16x2(__uint_as_float(v[h][2 * j]) * al, __uint_as_float(v[h][2 * j + 1]) * al);
         st.put(2 * h, w[0], w[1], w[2], w[3]);
         st.put(2 * h + 1, w[4], w[5], w[6], w[7]);
       }
@@ -545,8 +578,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           tmem_ld_wait(b);
           #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
-            const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
+            const float a0 = __uint_as_float(a[2 * j]) * al, a1 = __uint_as_float(a[2 * j + 1]) * al;
+            const float b0 = __uint_as_float(b[2 * j]) * al, b1 = __uint_as_float(b[2 * j + 1]) * al;
             hp[8 * q + j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
                                         g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
             zg[8 * q + j] = pack_bf16x2(a0, a1);
@@ -600,8 +633,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           for (int u = 0; u < 2; ++u) {
             #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float a0 = __uint_as_float(av[u][2 * j]), a1 = __uint_as_float(av[u][2 * j + 1]);
-              const float b0 = __uint_as_float(bv[u][2 * j]), b1 = __uint_as_float(bv[u][2 * j + 1]);
+              const float a0 = __uint_as_float(av[u][2 * j]) * al, a1 = __uint_as_float(av[u][2 * j + 1]) * al;
+              const float b0 = __uint_as_float(bv[u][2 * j]) * al, b1 = __uint_as_float(bv[u][2 * j + 1]) * al;
               hp[8 * (qq + u) + j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
                                                  g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
             }
@@ -649,8 +682,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         uint32_t hw[8];
         #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float a0 = __uint_as_float(a[2 * j]), a1 = __uint_as_float(a[2 * j + 1]);
-          const float b0 = __uint_as_float(b[2 * j]), b1 = __uint_as_float(b[2 * j + 1]);
+          const float a0 = __uint_as_float(a[2 * j]) * al, a1 = __uint_as_float(a[2 * j + 1]) * al;
+          const float b0 = __uint_as_float(b[2 * j]) * al, b1 = __uint_as_float(b[2 * j + 1]) * al;
           // silu(a) = a / (1 + e^-a) with the fast exponential and divide: their
           // relative error (~1e-6) is far below the bf16 rounding of h
           hw[j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
@@ -671,10 +704,11 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
             load32(t0 + half * (C::BN / 2) + c0 + 32 * h2, a, b);
             uint32_t w[16];
             #pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+            for (int j = 0; j < 8; ++j)
+              w[j] = pack_bf16x2(__uint_as_float(a[2 * j]) * al, __uint_as_float(a[2 * j + 1]) * al);
             #pragma unroll
             for (int j = 0; j < 8; ++j)
-              w[8 + j] = pack_bf16x2(__uint_as_float(b[2 * j]), __uint_as_float(b[2 * j + 1]));
+              w[8 + j] = pack_bf16x2(__uint_as_float(b[2 * j]) * al, __uint_as_float(b[2 * j + 1]) * al);
             #pragma unroll
             for (int j = 0; j < 4; ++j) st.put(4 * h2 + j, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
           }
@@ -933,7 +967,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
           const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
-          if constexpr (C::MX) {
+          if constexpr (C::NV4) {
+            // scale tiles of this stage -> TMEM (tile kk of A: 4 columns; of B: 4 per
+            // 128 rows), then 4 MMAs of K = 64; each TMEM cell holds the four E4M3
+            // scales of one row for one MMA (16 values each)
+            const uint32_t sf_addr = smem_u32(sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES));
+            const uint32_t sfa_t = tmem_base + C::ACC_BUFS * C::ACC_COLS + stage * C::SF_COLS;
+            const uint32_t sfb_t = sfa_t + 16;
+            #pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              tmem_cp_32x128b_warpx4(sfa_t + 4 * kk, smem_desc_plain16(sf_addr + 512 * kk));
+              #pragma unroll
+              for (int i = 0; i < C::BN / 128; ++i)
+                tmem_cp_32x128b_warpx4(sfb_t + (C::BN / 32) * kk + 4 * i,
+                                       smem_desc_plain16(sf_addr + 2048 * (i + 1) + 512 * kk));
+            }
+            #pragma unroll
+            for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
+              const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+              mma_nvf4_ss(d_tmem, ad, bd, C::IDESC, sfa_t + 4 * kk, sfb_t + (C::BN / 32) * kk,
+                          (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else if constexpr (C::MX) {
             // scale tiles of this stage -> TMEM, then 4 MMAs of K=32; MMA kk reads byte kk
             const uint32_t sf_addr = smem_u32(sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES));
             const uint32_t sfa_t = tmem_base + C::ACC_BUFS * C::ACC_COLS + stage * C::SF_COLS;
@@ -985,6 +1041,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     Stager<C::STAGING_BUFS> st{stage_smem + ew * (C::STAGING_BUFS * 4096), 0, lane};
+    const float al = acc_scale<C>(p);
     for (int j = 0;; ++j) {
       const int slot = j % kSchedDepth;
       if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr)) break;
@@ -1001,11 +1058,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           TileInfo th = ti;
           th.m0 += 128 * part;
           epilogue_tile_tma<C>(p, th, tmem_base + acc * C::ACC_COLS + part * C::BN, quarter, lane, st, &tmC, &tmC2,
-                               &tempty_bar[acc], &released);
+                               &tempty_bar[acc], &released, al);
         }
       } else if constexpr (C::TMA_OUT) {
         epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::ACC_COLS, quarter, lane, st, &tmC, &tmC2,
-                             &tempty_bar[acc], &released);
+                             &tempty_bar[acc], &released, al);
       } else {
         epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
       }

@@ -190,4 +190,97 @@ cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* 
   return mx_wgrad_bn<128>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
 }
 
+// ---------------------------------------------------------------- NVFP4
+// The same kernel with E2M1 operands (two codes per byte, so a 128-byte
+// K-major row holds 256 elements), one E4M3 scale per 16 along K (four 512-byte
+// tiles per k-block and 128 rows), kind::mxf4nvf4 MMAs of K = 64, and the
+// tensor scales applied to the accumulator in the epilogue (see nvfp4.cu).
+
+cudaError_t gemm_nv4_fc1(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int H,
+                         const void* w1q, const void* w1sf, const float* amax_w, int E, int F,
+                         const int32_t* poffsets, int dense_rows, const float* row_gate, void* h, void* z,
+                         int* status, cudaStream_t st) {
+  // w1q rows of one expert are [gate 0..127, up 0..127, gate 128..255, up 128..255, ...]
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, aq, H / 2, rows_alloc, 128) ||
+      !make_tmap_u8(&tb, w1q, H / 2, static_cast<uint64_t>(E) * 2 * F, 256))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.m_rows = dense_rows;
+  p.k_len = H;
+  p.n_tiles = F / 128;
+  p.b_rows_per_group = 2 * F;
+  p.c = h;
+  p.ldc = F;
+  p.c2 = z;
+  p.ldc2 = 2 * F;
+  p.half_cols = F;
+  p.row_gate = row_gate;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(asf);
+  p.sfb = static_cast<const uint8_t*>(w1sf);
+  p.sfa_tiles_k = H / 64;
+  p.sfb_tiles_k = H / 64;
+  p.amax_a = amax_a;
+  p.amax_b = amax_w;
+  CUtensorMap tc, tz;
+  if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
+    return cudaErrorInvalidValue;
+  if (z == nullptr) tz = tc;
+  if (poffsets != nullptr)
+    return launch_mx<GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwiglu, 2>>(ta, tb, tc, tz, p, rows_alloc,
+                                                                                   dense_rows, st);
+  return launch_mx<GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwiglu, 2>>(ta, tb, tc, tz, p, rows_alloc,
+                                                                                dense_rows, st);
+}
+
+namespace {
+template <int BN>
+cudaError_t nv4_nt_bf16_bn(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int K,
+                           const void* bq, const void* bsf, const float* amax_b, int E, int N,
+                           const int32_t* poffsets, int dense_rows, void* c, int* status, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, aq, K / 2, rows_alloc, 128) || !make_tmap_u8(&tb, bq, K / 2, static_cast<uint64_t>(E) * N, BN))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.m_rows = dense_rows;
+  p.k_len = K;
+  p.n_tiles = N / BN;
+  p.b_rows_per_group = N;
+  p.c = c;
+  p.ldc = N;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(asf);
+  p.sfb = static_cast<const uint8_t*>(bsf);
+  p.sfa_tiles_k = K / 64;
+  p.sfb_tiles_k = K / 64;
+  p.amax_a = amax_a;
+  p.amax_b = amax_b;
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, c, N, rows_alloc)) return cudaErrorInvalidValue;
+  if (poffsets != nullptr)
+    return launch_mx<GemmCfg<BN, false, false, Sched::kRoutedM, Epi::kStoreBf16, 2>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                     dense_rows, st);
+  return launch_mx<GemmCfg<BN, false, false, Sched::kDenseM, Epi::kStoreBf16, 2>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                  dense_rows, st);
+}
+}  // namespace
+
+// c [rows, N] bf16 = A [rows, K] x B_e [N, K]^T, both NVFP4.
+cudaError_t gemm_nv4_nt_bf16(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int K,
+                             const void* bq, const void* bsf, const float* amax_b, int E, int N,
+                             const int32_t* poffsets, int dense_rows, void* c, int* status, cudaStream_t st) {
+  if (N % 256 == 0)
+    return nv4_nt_bf16_bn<256>(aq, asf, amax_a, rows_alloc, K, bq, bsf, amax_b, E, N, poffsets, dense_rows, c, status,
+                               st);
+  return nv4_nt_bf16_bn<128>(aq, asf, amax_a, rows_alloc, K, bq, bsf, amax_b, E, N, poffsets, dense_rows, c, status,
+                             st);
+}
+
 }  // namespace moe

@@ -98,4 +98,25 @@ cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* 
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
                           cudaStream_t st);
 
+// ------------------------------------------------------------ NVFP4 (nvfp4.cu, gemm_mx.cu)
+// *amax = max |v| over a bf16 [rows, cols] tensor (rows with row_src < 0 skipped
+// when row_src is given, rows from *rows_end on when rows_end is given); zeroes
+// *amax first.
+cudaError_t launch_amax_bf16(const void* src, long long rows, int cols, const int32_t* row_src,
+                             const int32_t* rows_end, float* amax, cudaStream_t st);
+// Blocks of 16 along each row with the tensor scale of *amax; codes [rows, cols/2].
+cudaError_t launch_quantize_rows_nv4(const void* src, long long rows, int cols, int gate_up_half,
+                                     const float* amax, uint8_t* codes, uint8_t* sf, cudaStream_t st);
+cudaError_t launch_gather_rows_nv4(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
+                                   int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st);
+// NVFP4 GEMMs: A [rows, K] and B_e [N, K] E2M1 codes with scale tiles; amax_a,
+// amax_b their tensor amaxes (device).
+cudaError_t gemm_nv4_fc1(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int H,
+                         const void* w1q, const void* w1sf, const float* amax_w, int E, int F,
+                         const int32_t* poffsets, int dense_rows, const float* row_gate, void* h, void* z,
+                         int* status, cudaStream_t st);
+cudaError_t gemm_nv4_nt_bf16(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int K,
+                             const void* bq, const void* bsf, const float* amax_b, int E, int N,
+                             const int32_t* poffsets, int dense_rows, void* c, int* status, cudaStream_t st);
+
 }  // namespace moe

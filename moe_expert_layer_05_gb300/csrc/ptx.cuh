@@ -169,6 +169,19 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= (A * sfa) * (B * sfb)^T with E2M1 A and B (two codes per
+// byte, K-major) and one unsigned E4M3 scale per 16 elements along K (NVFP4);
+// K = 64 per instruction, so each row needs four scales: the four bytes of
+// its 32-bit TMEM cell.
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P;\n setp.ne.b32 P, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], P;\n}\n"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copy 32 rows x 16 bytes from shared memory into TMEM, replicated into the
 // four 32-lane quarters: lane i (of every quarter), column c receives bytes
 // [4c, 4c+4) of row i.  Used for the MXFP8 scale factors.
@@ -260,6 +273,17 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
          | (0u << 10)                                // B format E4M3
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (1u << 23)                                // scale factor format E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor, kind::mxf4nvf4 with block scaling: E2M1 A and B
+// (format code 1 of that kind), fp32 D, unsigned E4M3 scale factors (bit 23
+// clear), K-major operands, scale-factor ids 0 (each MMA uses whole cells).
+__host__ __device__ constexpr uint32_t idesc_nvf4_e2m1(int M, int N) {
+  return (1u << 7)                                   // A format E2M1
+         | (1u << 10)                                // B format E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (0u << 23)                                // scale factor format UE4M3
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 

@@ -29,7 +29,7 @@ class Workload:
     S: int = 0       # shared expert ffn size (0: no shared expert)
     score: str = "softmax"   # "softmax" or "sigmoid"
     zipf_s: float = 0.0      # >0: router bias ~ Zipf(s) over experts (sigmoid only)
-    dtype: str = "bf16"      # expert GEMM operand type: "bf16" or "mxfp8"
+    dtype: str = "bf16"      # expert GEMM operand type: "bf16", "mxfp8" or "nvfp4" (forward only)
     backward: bool = False
 
     def as_dict(self) -> dict:
@@ -44,6 +44,9 @@ WORKLOADS = {
                      score="sigmoid", zipf_s=1.2),
     "dsv3_mxfp8": Workload("dsv3_mxfp8", T=16384, H=7168, E=256, k=8, F=2048, S=2048,
                            score="sigmoid", zipf_s=1.2, dtype="mxfp8", backward=True),
+    # NVFP4 expert GEMMs (forward): the Mixtral-like layer, and a small case for the oracle
+    "mixtral_nvfp4": Workload("mixtral_nvfp4", T=4096, H=4096, E=8, k=2, F=14336, dtype="nvfp4"),
+    "tiny_nvfp4": Workload("tiny_nvfp4", T=256, H=256, E=8, k=2, F=512, dtype="nvfp4"),
 }
 
 # Weight of the router bias: b_e = ZIPF_C * ln(E * p_e), p_e ∝ rank_e^(-s).

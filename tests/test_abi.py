@@ -83,3 +83,34 @@ def test_null_and_misaligned_pointers_rejected_before_launch():
     args = api.MoeGemmArgs(9, 16, 16, 16, 16, None, None, None, None, None)
     st = lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), 16, None)
     assert st in (-1, -2)      # unknown op (or no GB300 here)
+
+
+def test_nvfp4_config_rules_and_sizes():
+    """NVFP4 layers: T % 128, H/F/S % 256; their workspace holds the E2M1 codes
+    (half a byte per element) and E4M3 scales (one byte per 16); the weight
+    buffer likewise; backward calls and NVFP4 backward GEMM ops are refused
+    before any launch."""
+    lib = api.load()
+    ok = api.make_config(256, 256, 8, 2, 512, 0, dtype="nvfp4")
+    assert api.moe_capacity_rows(ok) > 0
+    for bad in (dict(H=128), dict(F=384), dict(S=128), dict(T=100)):
+        kw = dict(T=256, H=256, E=8, k=2, F=512, S=0)
+        kw.update(bad)
+        assert api.moe_capacity_rows(api.make_config(dtype="nvfp4", **kw)) == -1, bad
+    bf = api.make_config(256, 256, 8, 2, 512, 0)
+    cap = api.moe_capacity_rows(ok)
+    extra = api.moe_workspace_bytes(ok) - api.moe_workspace_bytes(bf)
+    assert extra >= (cap * 256 + cap * 512 + 256 * 256) * (1 / 2 + 1 / 16)
+    wb = api.moe_nvfp4_weights_bytes(ok)
+    assert wb >= 8 * (2 * 512 * 256 + 256 * 512) * (1 / 2 + 1 / 16)
+    assert api.moe_nvfp4_weights_bytes(bf) == 0
+    w = api.MoeWeights(16, None, 16, 16, None, None, 16)
+    assert lib.moe_layer_forward(ctypes.byref(ok), ctypes.byref(w), 16, 16, 16, 1 << 40, 1, 16, 1 << 40,
+                                 None) == -2
+    assert lib.moe_layer_backward_dgrad(ctypes.byref(ok), ctypes.byref(w), 16, 16, 16, None, 16, 1 << 40, 16,
+                                        1 << 40, None) == -2
+    # quantiser argument checks: cols % 64, rows % 128, known mode, amax pointer
+    assert lib.moe_quantize_nvfp4(16, 1, 128, 96, 0, 16, 16, 16, None) == -1
+    assert lib.moe_quantize_nvfp4(16, 1, 100, 64, 0, 16, 16, 16, None) == -1
+    assert lib.moe_quantize_nvfp4(16, 1, 128, 64, 1, 16, 16, 16, None) == -1
+    assert lib.moe_quantize_nvfp4(16, 1, 128, 64, 0, 16, 16, None, None) == -1

@@ -41,7 +41,9 @@ def _to_dev(inp):
 
 def _layer(w: Workload, dev_inp, with_backward):
     cfg = api.config_of(w, tokens=dev_inp["x"].shape[0])
-    return api.MoELayer(cfg, dev_inp, with_backward=with_backward)
+    layer = api.MoELayer(cfg, dev_inp, with_backward=with_backward)
+    layer.act.fill_(0x7F)      # large finite garbage: the layer must not read memory it did not write
+    return layer
 
 
 def _oracle_fwd(w, inp_cpu, tokens=None):

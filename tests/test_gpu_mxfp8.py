@@ -243,6 +243,7 @@ def test_mx_layer_against_mxfp8_oracle(lib, name):
     inp = make_inputs(w, seed=2)
     dinp = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     layer = api.MoELayer(api.config_of(w), dinp, with_backward=True)
+    layer.act.fill_(0x7F)      # large finite garbage: the layer must not read memory it did not write
     y = layer.forward(dinp["x"])
     dx, dgate, grads = layer.backward(dinp["x"], dinp["dy"])
     torch.cuda.synchronize()
