@@ -111,7 +111,11 @@ struct GemmCfg {
   static constexpr bool TMA_OUT = !(EP == Epi::kStoreF32 && S == Sched::kDenseM);
   // Epilogue warps: four (one per TMEM lane quarter), or eight for 256-row
   // tiles, where the second four write rows 128..255 at the same time.
-  static constexpr int EPI_WARPS = M256 ? 8 : 4;
+  // NVFP4 SwiGLU tiles (one accumulator, MMAs fast enough that the MMA warp
+  // waits for it): eight warps too, the second four taking the upper half of
+  // the h' columns, so the accumulator is read and handed back in half the time.
+  static constexpr bool SPLIT_COLS = NV4 && EP == Epi::kSwiglu && BN == 256;
+  static constexpr int EPI_WARPS = (M256 || SPLIT_COLS) ? 8 : 4;
   // Shared memory (all of it dynamic): the k-block ring, 4 KB staging buffers
   // (32 rows x 128 B, 128B-swizzled) per epilogue warp -- two each, or one
   // where two would cost the ring its fourth stage -- and the bookkeeping
@@ -435,7 +439,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
                                                   const CUtensorMap* tmC,
                                                   const CUtensorMap* tmC2,
                                                   uint64_t* release_bar = nullptr, bool* released = nullptr,
-                                                  const float al = 1.0f) {
+                                                  const float al = 1.0f, const int cpart = 0) {
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t t0 = tmem_acc + lane_addr;
   const bool no_mma = (ti.num_kb == 0);         // empty group (weight gradients): result is zero
@@ -566,14 +570,17 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     if constexpr (C::BN == 256 && C::ACC_BUFS == 1 && !C::M256) {
       if (p.c2 != nullptr && release_bar != nullptr) {
         // Single accumulator, z saved: h' and both halves of z for this row's
-        // 128 columns go to registers (bf16 pairs), the accumulator is handed
-        // back, then everything is stored.
-        uint32_t hp[64], zg[64], zu[64];
+        // 128 columns (64 when the columns are split over two warps) go to
+        // registers (bf16 pairs), the accumulator is handed back, then
+        // everything is stored.
+        constexpr int NQ = C::SPLIT_COLS ? 4 : 8;   // 16-column groups of h' this warp owns
+        const int q0 = C::SPLIT_COLS ? 4 * cpart : 0;
+        uint32_t hp[8 * NQ], zg[8 * NQ], zu[8 * NQ];
         #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < NQ; ++q) {
           uint32_t a[16], b[16];
-          tmem_ld_x16(t0 + 16 * q, a);
-          tmem_ld_x16(t0 + C::BN / 2 + 16 * q, b);
+          tmem_ld_x16(t0 + 16 * (q0 + q), a);
+          tmem_ld_x16(t0 + C::BN / 2 + 16 * (q0 + q), b);
           tmem_ld_wait(a);
           tmem_ld_wait(b);
           #pragma unroll
@@ -591,22 +598,23 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         if (lane == 0) mbar_arrive(release_bar);
         *released = true;
         #pragma unroll
-        for (int c = 0; c < 2; ++c) {               // 64-column chunks: h', z gate, z up
+        for (int c = 0; c < NQ / 4; ++c) {          // 64-column chunks: h', z gate, z up
+          const int cc = q0 / 4 + c;
           st.begin();
           #pragma unroll
           for (int q = 0; q < 8; ++q) st.put(q, hp[32 * c + 4 * q], hp[32 * c + 4 * q + 1], hp[32 * c + 4 * q + 2],
                                             hp[32 * c + 4 * q + 3]);
-          st.flush(tmC, col0 + 64 * c, y);
+          st.flush(tmC, col0 + 64 * cc, y);
           st.begin();
           #pragma unroll
           for (int q = 0; q < 8; ++q) st.put(q, zg[32 * c + 4 * q], zg[32 * c + 4 * q + 1], zg[32 * c + 4 * q + 2],
                                             zg[32 * c + 4 * q + 3]);
-          st.flush(tmC2, col0 + 64 * c, y);
+          st.flush(tmC2, col0 + 64 * cc, y);
           st.begin();
           #pragma unroll
           for (int q = 0; q < 8; ++q) st.put(q, zu[32 * c + 4 * q], zu[32 * c + 4 * q + 1], zu[32 * c + 4 * q + 2],
                                             zu[32 * c + 4 * q + 3]);
-          st.flush(tmC2, p.half_cols + col0 + 64 * c, y);
+          st.flush(tmC2, p.half_cols + col0 + 64 * cc, y);
         }
         return;
       }
@@ -615,14 +623,16 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
       if (p.c2 == nullptr && release_bar != nullptr) {
         // Forward without saved z: compute this row's 128 values of h' into
         // registers, hand the accumulator back to the MMA warp, then store.
-        uint32_t hp[64];                            // packed bf16 pairs, columns 0..127
+        constexpr int NQ = C::SPLIT_COLS ? 4 : 8;   // 16-column groups of h' this warp owns
+        const int q0 = C::SPLIT_COLS ? 4 * cpart : 0;
+        uint32_t hp[8 * NQ];                        // packed bf16 pairs
         #pragma unroll
-        for (int qq = 0; qq < 8; qq += 2) {
+        for (int qq = 0; qq < NQ; qq += 2) {
           uint32_t av[2][16], bv[2][16];
           #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            tmem_ld_x16(t0 + 16 * (qq + u), av[u]);
-            tmem_ld_x16(t0 + C::BN / 2 + 16 * (qq + u), bv[u]);
+            tmem_ld_x16(t0 + 16 * (q0 + qq + u), av[u]);
+            tmem_ld_x16(t0 + C::BN / 2 + 16 * (q0 + qq + u), bv[u]);
           }
           #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -645,7 +655,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         if (lane == 0) mbar_arrive(release_bar);
         *released = true;
         #pragma unroll
-        for (int c = 0; c < 2; ++c) {               // two 64-column chunks
+        for (int c = 0; c < NQ / 4; ++c) {          // 64-column chunks
           st.begin();
           #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -653,13 +663,14 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
             st.put(2 * q, w[0], w[1], w[2], w[3]);
             st.put(2 * q + 1, w[4], w[5], w[6], w[7]);
           }
-          st.flush(tmC, col0 + 64 * c, y);
+          st.flush(tmC, col0 + 64 * (q0 / 4 + c), y);
         }
         return;
       }
     }
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN / 2; c0 += 64) {
+      if (C::SPLIT_COLS && c0 != 64 * cpart) continue;   // the other warp of this lane quarter has it
       st.begin();
       #pragma unroll 1
       for (int qq = 0; qq < 4; qq += 2) {
@@ -1038,6 +1049,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int ew = warp - 2;
     const int quarter = warp & 3;          // TMEM lanes a warp may read: 32 * (warp % 4) onwards
     const int part = ew >> 2;              // 256-row tiles: which 128-row half this warp writes
+                                           // (split-column tiles: which half of the h' columns)
     int acc = 0;
     uint32_t acc_phase = 0;
     Stager<C::STAGING_BUFS> st{stage_smem + ew * (C::STAGING_BUFS * 4096), 0, lane};
@@ -1062,7 +1074,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       } else if constexpr (C::TMA_OUT) {
         epilogue_tile_tma<C>(p, ti, tmem_base + acc * C::ACC_COLS, quarter, lane, st, &tmC, &tmC2,
-                             &tempty_bar[acc], &released, al);
+                             &tempty_bar[acc], &released, al, C::SPLIT_COLS ? part : 0);
       } else {
         epilogue_tile<C>(p, ti, tmem_base + acc * C::BN, quarter, lane);
       }
