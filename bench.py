@@ -451,10 +451,54 @@ def run_ours(args) -> dict | None:
 PROFILE_OPS = ("fc1", "fc2", "dgrad_fc2", "dgrad_fc1", "wgrad_fc1", "wgrad_fc2")
 
 
+def profile_op_nvfp4(args, w, dev) -> dict:
+    """--profile-op for an NVFP4 workload: the NVFP4 forward once, then x_perm
+    (permuted, padding zeroed), h and the weights quantised by the library into
+    bench-owned buffers, and the chosen NVFP4 GEMM once inside the profiler range."""
+    from moe_expert_layer_05_gb300 import api
+    if args.profile_op not in ("fc1", "fc2"):
+        raise SystemExit("--profile-op: NVFP4 workloads have fc1 and fc2 only")
+    d = make_inputs_on_device(w, dev, seed=0, with_dy=False)
+    cfg = api.config_of(w)
+    layer = api.MoELayer(cfg, d, with_backward=False)
+    x = d["x"]
+    layer.forward(x)
+    fl, ws, cap = layer.fields(), layer.ws, layer.layout.cap
+    api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"], fl["poffsets"],
+                    fl["slot_row"], fl["row_src"], fl["row_gate"], fl["x_perm"], 1, ws)
+
+    def q(t, batch, rows, cols, mode):
+        c = torch.empty(t.numel() // 2, dtype=torch.uint8, device=dev)
+        sf = torch.empty(t.numel() // 16, dtype=torch.uint8, device=dev)
+        a = torch.empty(1, dtype=torch.float32, device=dev)
+        api.moe_quantize_nvfp4(t, batch, rows, cols, mode, c, sf, a)
+        return c, sf, a
+
+    po = fl["poffsets"]
+    if args.profile_op == "fc1":
+        (aq, asf, aa), (bq, bsf, ba) = q(fl["x_perm"], 1, cap, w.H, api.MX_ROWS), \
+            q(d["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP)
+        call = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, aq, bq, fl["h"], ws, row_gate=fl["row_gate"],
+                                            poffsets=po, a_scales=asf, b_scales=bsf, a_amax=aa, b_amax=ba)
+    else:
+        (aq, asf, aa), (bq, bsf, ba) = q(fl["h"], 1, cap, w.F, api.MX_ROWS), q(d["w2"], 1, w.E * w.H, w.F, api.MX_ROWS)
+        call = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, aq, bq, fl["o"], ws, poffsets=po, a_scales=asf,
+                                            b_scales=bsf, a_amax=aa, b_amax=ba)
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    return {"profile_op": args.profile_op, "workload": args.workload, "T": w.T, "E": w.E,
+            "status": api.moe_read_device_status(ws),
+            "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
+
+
 def profile_op(args) -> dict:
     """One untimed step of the workload, then one grouped GEMM of it between
     cudaProfilerStart and cudaProfilerStop, for `ncu --profile-from-start off`
-    captures.  bf16 workloads only."""
+    captures.  bf16 workloads (every op) and NVFP4 workloads (fc1, fc2)."""
     from moe_expert_layer_05_gb300 import api
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -463,8 +507,10 @@ def profile_op(args) -> dict:
         w = dataclasses.replace(w, T=args.tokens)
     if args.experts is not None:
         w = dataclasses.replace(w, E=args.experts)
+    if w.dtype == "nvfp4":
+        return profile_op_nvfp4(args, w, dev)
     if w.dtype != "bf16":
-        raise SystemExit("--profile-op: bf16 workloads only")
+        raise SystemExit("--profile-op: bf16 and NVFP4 workloads only")
     bwd = args.profile_op not in ("fc1", "fc2")
     d = make_inputs_on_device(w, dev, seed=0, with_dy=bwd)
     layer = api.MoELayer(api.config_of(w), d, with_backward=True)

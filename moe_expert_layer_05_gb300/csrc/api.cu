@@ -514,7 +514,7 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
       case MOE_GG_FC1_SWIGLU:
         if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
         return cuda_status(gemm_nv4_fc1(a->a, a->a_scales, a->a_amax, rows, H, a->b, a->b_scales, a->b_amax, E, F, po,
-                                        a->dense_rows, a->row_gate, a->c, a->c2, status, st));
+                                        a->dense_rows, a->row_gate, a->c, a->c2, nullptr, status, st));
       case MOE_GG_FC2:
         return cuda_status(gemm_nv4_nt_bf16(a->a, a->a_scales, a->a_amax, rows, F, a->b, a->b_scales, a->b_amax, E, H,
                                             po, a->dense_rows, a->c, status, st));
@@ -644,18 +644,19 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     MOE_TRY(launch_amax_bf16(x, T, H, nullptr, nullptr, amax + 0, st));
     MOE_TRY(launch_quantize_rows_nv4(x, T, H, 0, amax + 0, q(M.xs), f(M.xs), st));
     MOE_TRY(launch_gather_rows_nv4(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st));
+    // fc1 writes h' and its amax (padding rows have gate 0, so h' = 0 there;
+    // rows past the last expert's segment are never computed)
+    MOE_TRY(cudaMemsetAsync(amax + 1, 0, sizeof(float), st));
     MOE_TRY(gemm_nv4_fc1(q(M.x), f(M.x), amax + 0, cap, H, wq(W.w1), wf(W.w1), wamax + 0, E, F, poff, 0, row_gate, h,
-                         nullptr, status, st));
-    // rows past the last expert's segment are never written: bounded by poffsets[E]
-    MOE_TRY(launch_amax_bf16(h, cap, F, at<int32_t>(act, L.row_src), poff + E, amax + 1, st));
+                         nullptr, amax + 1, status, st));
     MOE_TRY(launch_quantize_rows_nv4(h, cap, F, 0, amax + 1, q(M.h), f(M.h), st));
     MOE_TRY(gemm_nv4_nt_bf16(q(M.h), f(M.h), amax + 1, cap, F, wq(W.w2), wf(W.w2), wamax + 1, E, H, poff, 0, o, status,
                              st));
     if (S > 0 && T > 0) {
       void* hs = at<void>(act, L.hs);
+      MOE_TRY(cudaMemsetAsync(amax + 2, 0, sizeof(float), st));
       MOE_TRY(gemm_nv4_fc1(q(M.xs), f(M.xs), amax + 0, T, H, wq(W.s1), wf(W.s1), wamax + 2, 1, S, nullptr, T, nullptr,
-                           hs, nullptr, status, st));
-      MOE_TRY(launch_amax_bf16(hs, T, S, nullptr, nullptr, amax + 2, st));
+                           hs, nullptr, amax + 2, status, st));
       MOE_TRY(launch_quantize_rows_nv4(hs, T, S, 0, amax + 2, q(M.hs), f(M.hs), st));
       MOE_TRY(gemm_nv4_nt_bf16(q(M.hs), f(M.hs), amax + 2, T, S, wq(W.s2), wf(W.s2), wamax + 3, 1, H, nullptr, T,
                                at<void>(act, L.os), status, st));

@@ -71,6 +71,10 @@ struct GemmParams {
   // multiplied by 1 / (S_a * S_b) before the epilogue's arithmetic.
   const float* amax_a;
   const float* amax_b;
+  // kSwiglu (nullable): atomicMax of |h'| as stored (bf16 values, fp32 bit
+  // patterns, non-negative so they order as unsigned) -- the tensor amax the
+  // NVFP4 quantiser of h' needs, taken without another pass over h'.
+  unsigned* amax_out;
   int* status;             // device status word (first error wins)
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
 };
@@ -431,6 +435,16 @@ __device__ __forceinline__ float acc_scale(const GemmParams& p) {
   }
 }
 
+// |h'| maximum of packed bf16 pairs, folded into a warp maximum and one
+// atomicMax per warp (NaN inputs are ignored by fmaxf).
+__device__ __forceinline__ float amax_bf16x2(float m, uint32_t w) {
+  return fmaxf(m, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+}
+__device__ __forceinline__ void amax_flush(unsigned* out, float m, int lane) {
+  const unsigned u = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+  if (lane == 0) atomicMax(out, u);
+}
+
 // Epilogue with TMA stores.  Rows of the tile: warp quarter q owns rows
 // 32q..32q+31, lane = row.  Dense tiles past the last row are clipped by TMA.
 template <class C>
@@ -597,6 +611,12 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         __syncwarp();
         if (lane == 0) mbar_arrive(release_bar);
         *released = true;
+        if (p.amax_out != nullptr) {
+          float m = 0.f;
+          #pragma unroll
+          for (int i = 0; i < 8 * NQ; ++i) m = amax_bf16x2(m, hp[i]);
+          amax_flush(p.amax_out, m, lane);
+        }
         #pragma unroll
         for (int c = 0; c < NQ / 4; ++c) {          // 64-column chunks: h', z gate, z up
           const int cc = q0 / 4 + c;
@@ -654,6 +674,12 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         __syncwarp();
         if (lane == 0) mbar_arrive(release_bar);
         *released = true;
+        if (p.amax_out != nullptr) {
+          float m = 0.f;
+          #pragma unroll
+          for (int i = 0; i < 8 * NQ; ++i) m = amax_bf16x2(m, hp[i]);
+          amax_flush(p.amax_out, m, lane);
+        }
         #pragma unroll
         for (int c = 0; c < NQ / 4; ++c) {          // 64-column chunks
           st.begin();
@@ -668,6 +694,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         return;
       }
     }
+    float hmax = 0.f;
     #pragma unroll 1
     for (int c0 = 0; c0 < C::BN / 2; c0 += 64) {
       if (C::SPLIT_COLS && c0 != 64 * cpart) continue;   // the other warp of this lane quarter has it
@@ -700,6 +727,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           hw[j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
                               g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
         }
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) hmax = amax_bf16x2(hmax, hw[j]);
         st.put(2 * q, hw[0], hw[1], hw[2], hw[3]);
         st.put(2 * q + 1, hw[4], hw[5], hw[6], hw[7]);
        }
@@ -727,6 +756,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         }
       }
     }
+    if (p.amax_out != nullptr) amax_flush(p.amax_out, hmax, lane);
   } else {  // kSwigluBwd: dz gate and up chunks of each 64 columns in one pass
     static_assert(C::STAGING_BUFS == 2, "the gate and up chunks are staged side by side");
     const int row = ti.m0 + quarter * 32 + lane;

@@ -199,7 +199,7 @@ cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* 
 cudaError_t gemm_nv4_fc1(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int H,
                          const void* w1q, const void* w1sf, const float* amax_w, int E, int F,
                          const int32_t* poffsets, int dense_rows, const float* row_gate, void* h, void* z,
-                         int* status, cudaStream_t st) {
+                         float* amax_h, int* status, cudaStream_t st) {
   // w1q rows of one expert are [gate 0..127, up 0..127, gate 128..255, up 128..255, ...]
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, aq, H / 2, rows_alloc, 128) ||
@@ -226,6 +226,7 @@ cudaError_t gemm_nv4_fc1(const void* aq, const void* asf, const float* amax_a, i
   p.sfb_tiles_k = H / 64;
   p.amax_a = amax_a;
   p.amax_b = amax_w;
+  p.amax_out = reinterpret_cast<unsigned*>(amax_h);
   CUtensorMap tc, tz;
   if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
     return cudaErrorInvalidValue;

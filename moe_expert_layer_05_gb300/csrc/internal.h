@@ -110,11 +110,12 @@ cudaError_t launch_quantize_rows_nv4(const void* src, long long rows, int cols, 
 cudaError_t launch_gather_rows_nv4(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
                                    int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st);
 // NVFP4 GEMMs: A [rows, K] and B_e [N, K] E2M1 codes with scale tiles; amax_a,
-// amax_b their tensor amaxes (device).
+// amax_b their tensor amaxes (device).  amax_h (nullable, zeroed by the caller):
+// receives max |h'| over the rows fc1 computes.
 cudaError_t gemm_nv4_fc1(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int H,
                          const void* w1q, const void* w1sf, const float* amax_w, int E, int F,
                          const int32_t* poffsets, int dense_rows, const float* row_gate, void* h, void* z,
-                         int* status, cudaStream_t st);
+                         float* amax_h, int* status, cudaStream_t st);
 cudaError_t gemm_nv4_nt_bf16(const void* aq, const void* asf, const float* amax_a, int rows_alloc, int K,
                              const void* bq, const void* bsf, const float* amax_b, int E, int N,
                              const int32_t* poffsets, int dense_rows, void* c, int* status, cudaStream_t st);
