@@ -46,6 +46,10 @@ FLUSH_BYTES = 512 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one fc1 launch, from the ncu
 # capture summarised in profiles/ (None until captured for the current kernel).
 FC1_TRAFFIC_BYTES = 2.342e9   # profiles/fc1_grouped_gemm_mixtral_full.md (bf16 Mixtral-like fc1, DRAM read + write)
+# NVFP4 Mixtral-like fc1: captured at T=2048, E=4 (the same 1024 rows per
+# expert), 374.1 MB; the traffic grows with the experts, so x2 for E=8
+# (profiles/fc1_grouped_gemm_mixtral_nvfp4.md)
+FC1_NV4_TRAFFIC_BYTES = 2 * 374.1e6
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -432,7 +436,8 @@ def run_ours(args) -> dict | None:
                                ", fused gated SwiGLU)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": peak_note,
-                     "traffic": (FC1_TRAFFIC_BYTES if (w.name == "mixtral" and not mx) else None),
+                     "traffic": (FC1_TRAFFIC_BYTES if w.name == "mixtral" else
+                                 FC1_NV4_TRAFFIC_BYTES if w.name == "mixtral_nvfp4" else None),
                      "flop_per_launch": fc1_flop, "ms_per_launch": fc1_ms},
         "stages_ms": stages,
         "e2e": {"value": aggregate(w.T, K, world, e2e_total), "unit": "tokens/s",

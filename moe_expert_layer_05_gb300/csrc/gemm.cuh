@@ -71,9 +71,9 @@ struct GemmParams {
   // multiplied by 1 / (S_a * S_b) before the epilogue's arithmetic.
   const float* amax_a;
   const float* amax_b;
-  // kSwiglu (nullable): atomicMax of |h'| as stored (bf16 values, fp32 bit
-  // patterns, non-negative so they order as unsigned) -- the tensor amax the
-  // NVFP4 quantiser of h' needs, taken without another pass over h'.
+  // NVFP4 kSwiglu (nullable): atomicMax of |h'| as stored (bf16 values, fp32
+  // bit patterns, non-negative so they order as unsigned) -- the tensor amax
+  // the NVFP4 quantiser of h' needs, taken without another pass over h'.
   unsigned* amax_out;
   int* status;             // device status word (first error wins)
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
@@ -611,11 +611,13 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         __syncwarp();
         if (lane == 0) mbar_arrive(release_bar);
         *released = true;
-        if (p.amax_out != nullptr) {
-          float m = 0.f;
-          #pragma unroll
-          for (int i = 0; i < 8 * NQ; ++i) m = amax_bf16x2(m, hp[i]);
-          amax_flush(p.amax_out, m, lane);
+        if constexpr (C::NV4) {
+          if (p.amax_out != nullptr) {
+            float m = 0.f;
+            #pragma unroll
+            for (int i = 0; i < 8 * NQ; ++i) m = amax_bf16x2(m, hp[i]);
+            amax_flush(p.amax_out, m, lane);
+          }
         }
         #pragma unroll
         for (int c = 0; c < NQ / 4; ++c) {          // 64-column chunks: h', z gate, z up
@@ -674,11 +676,13 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         __syncwarp();
         if (lane == 0) mbar_arrive(release_bar);
         *released = true;
-        if (p.amax_out != nullptr) {
-          float m = 0.f;
-          #pragma unroll
-          for (int i = 0; i < 8 * NQ; ++i) m = amax_bf16x2(m, hp[i]);
-          amax_flush(p.amax_out, m, lane);
+        if constexpr (C::NV4) {
+          if (p.amax_out != nullptr) {
+            float m = 0.f;
+            #pragma unroll
+            for (int i = 0; i < 8 * NQ; ++i) m = amax_bf16x2(m, hp[i]);
+            amax_flush(p.amax_out, m, lane);
+          }
         }
         #pragma unroll
         for (int c = 0; c < NQ / 4; ++c) {          // 64-column chunks
@@ -727,8 +731,10 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           hw[j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0,
                               g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
         }
-        #pragma unroll
-        for (int j = 0; j < 8; ++j) hmax = amax_bf16x2(hmax, hw[j]);
+        if constexpr (C::NV4) {
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) hmax = amax_bf16x2(hmax, hw[j]);
+        }
         st.put(2 * q, hw[0], hw[1], hw[2], hw[3]);
         st.put(2 * q + 1, hw[4], hw[5], hw[6], hw[7]);
        }
@@ -756,7 +762,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         }
       }
     }
-    if (p.amax_out != nullptr) amax_flush(p.amax_out, hmax, lane);
+    if constexpr (C::NV4) {
+      if (p.amax_out != nullptr) amax_flush(p.amax_out, hmax, lane);
+    }
   } else {  // kSwigluBwd: dz gate and up chunks of each 64 columns in one pass
     static_assert(C::STAGING_BUFS == 2, "the gate and up chunks are staged side by side");
     const int row = ti.m0 + quarter * 32 + lane;
