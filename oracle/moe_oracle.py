@@ -822,14 +822,18 @@ def nvfp4_weight(cache, name, W, e=None, quant=nvfp4_roundtrip):
 
 
 def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=None, w2_shared=None,
-                      routing=None, weight_cache=None, quant=nvfp4_roundtrip, store=bf16_round):
+                      routing=None, weight_cache=None, quant=nvfp4_roundtrip, store=bf16_round,
+                      x_amax=None, h_amax=None):
     """Forward with NVFP4 expert GEMMs.  Each quantised tensor has its own
     tensor scale: x (all tokens), W1 and W2 (all experts), h' (the gated
     activation of every expert row, rounded to bf16 as it is stored), and the
     shared expert's W1s, W2s and h.  Everything else as moe_forward.
     ``quant(v, amax, axis)`` and ``store(v)`` are the quantise-dequantise map
     and the activation storage rounding; identities give back the unquantised
-    layer (tests/test_oracle_nvfp4.py pins that)."""
+    layer (tests/test_oracle_nvfp4.py pins that).  ``x_amax`` / ``h_amax``
+    replace the tensor amaxes of x and h' when x holds only some of the
+    tokens (every other step is row-local, so those rows then come out as in
+    the forward of all tokens)."""
     x = np.asarray(x, np.float64)
     E = _shape(w1)[0]
     F = _shape(w1)[1] // 2
@@ -845,7 +849,7 @@ def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_share
     else:
         idx = np.asarray(routing[0], np.int64)
         gate = np.asarray(routing[1], np.float64)
-    xq = quant(x, None, -1)
+    xq = quant(x, x_amax, -1)
     rows = []
     for e in range(E):
         tok, slot = np.nonzero(idx == e)
@@ -854,7 +858,7 @@ def moe_forward_nvfp4(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_share
         z = xq[tok] @ wq("w1", w1, e).T
         hp = store(gate[tok, slot][:, None] * silu(z[:, :F]) * z[:, F:])
         rows.append((e, tok, hp))
-    amax_h = max((np.abs(hp).max() for _, _, hp in rows), default=0.0)
+    amax_h = max((np.abs(hp).max() for _, _, hp in rows), default=0.0) if h_amax is None else h_amax
     y = np.zeros_like(x)
     for e, tok, hp in rows:
         np.add.at(y, tok, quant(hp, amax_h, -1) @ wq("w2", w2, e).T)

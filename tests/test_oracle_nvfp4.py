@@ -188,3 +188,29 @@ def test_h_scale_is_shared_by_all_experts():
     amaxes = {float(a) for _, a in h_calls}
     assert len(amaxes) == 1
     assert amaxes.pop() == max(np.abs(v).max() for v, _ in h_calls)
+
+
+def test_sampled_tokens_with_full_tensor_amaxes_match_the_full_forward():
+    """Rows of a token sample, given the full tensors' amaxes of x and h',
+    equal those rows of the forward over all tokens (everything else is
+    row-local) -- the form the full-size GPU test uses."""
+    x, wr, w1, w2, _, _ = _case(6, T=96, H=64, F=64)
+    full = O.moe_forward_nvfp4(x, wr, w1, w2, k=2)
+    h_amaxes = set()
+
+    def rec(v, amax, axis):
+        v = np.asarray(v)
+        weight = any(v.shape == W[e].shape and np.array_equal(v, W[e]) for W in (w1, w2) for e in range(4))
+        if amax is not None and not weight:
+            h_amaxes.add(float(amax))                   # h' calls: the shared tensor amax
+        return O.nvfp4_roundtrip(v, amax, axis)
+
+    O.moe_forward_nvfp4(x, wr, w1, w2, k=2, quant=rec)
+    assert len(h_amaxes) == 1
+    h_amax = h_amaxes.pop()
+    tokens = np.array([3, 17, 40, 41, 95])
+    part = O.moe_forward_nvfp4(x[tokens], wr, w1, w2, k=2, x_amax=np.abs(x).max(), h_amax=h_amax)
+    # equal up to the fp64 summation order of the matmuls (a code flip would be ~1e-2)
+    np.testing.assert_allclose(part["y"], full["y"][tokens], rtol=1e-12, atol=1e-13)
+    wrong = O.moe_forward_nvfp4(x[tokens], wr, w1, w2, k=2)  # the sample's own amaxes: other codes
+    assert np.abs(wrong["y"] - full["y"][tokens]).max() > 1e-4
