@@ -272,3 +272,49 @@ def test_mx_layer_against_mxfp8_oracle(lib, name):
         for gname, oname in (("dw1_shared", "dW1_shared"), ("dw2_shared", "dW2_shared")):
             r = rel_l2(f64(grads[gname]), bwd[oname])
             assert r <= 3e-2, (gname, r)
+
+
+def test_mx_full_size_sampled(lib):
+    """The DeepSeek-like MXFP8 training layer at full size (T=16384, E=256,
+    shared expert), forward as the benchmark runs it: routing properties at any
+    size; for the expert with the most rows, seeded sample rows of z, h' and o
+    recomputed by the oracle (blocks of 32 are row-local, so sampled rows need
+    no other tokens); the shared expert's output rows likewise; the combine on
+    the sampled tokens."""
+    from gpu_helpers import i64
+    from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs_on_device
+    w = WORKLOADS["dsv3_mxfp8"]
+    dinp = make_inputs_on_device(w, DEV, seed=0, with_dy=False)
+    layer = api.MoELayer(api.config_of(w), dinp, with_backward=True)
+    layer.act.fill_(0x7F)
+    y = layer.forward(dinp["x"])
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(layer.ws) == 0
+    fl = layer.fields()
+    counts, po = i64(fl["counts"]), i64(fl["poffsets"])
+    assert counts.sum() == w.T * w.k
+    slot = i64(fl["slot_row"])
+    src = i64(fl["row_src"])
+    assert np.all(src[slot] == np.arange(w.T)[:, None])
+    e = int(np.argmax(counts))
+    rng = np.random.default_rng(13)
+    rows = np.sort(po[e] + rng.choice(counts[e], size=6, replace=False))
+    toks = src[rows]
+    rows_t, toks_t = torch.from_numpy(rows).to(DEV), torch.from_numpy(toks).to(DEV)
+    F = w.F
+    z = deq(dinp["x"][toks_t], -1) @ deq(dinp["w1"][e], -1).T
+    assert_bf16_close(f64(fl["z"][rows_t]), z, "z (mxfp8, full size)")
+    g = f64(fl["row_gate"][rows_t])
+    assert_bf16_close(f64(fl["h"][rows_t]), g[:, None] * O.silu(z[:, :F]) * z[:, F:], "h (mxfp8, full size)")
+    o_ref = deq(fl["h"][rows_t], -1) @ deq(dinp["w2"][e], -1).T
+    assert_bf16_close(f64(fl["o"][rows_t]), o_ref, "o (mxfp8, full size)")
+    # shared expert on the sampled tokens: os = q(hs) q(W2s)^T, hs = silu(a) b of q(x) q(W1s)^T
+    S = w.S
+    zs = deq(dinp["x"][toks_t], -1) @ deq(dinp["w1_shared"], -1).T
+    hs = layer.view("hs", torch.bfloat16, (w.T, S))[toks_t]
+    assert_bf16_close(f64(hs), O.silu(zs[:, :S]) * zs[:, S:], "hs (mxfp8, full size)")
+    os_ = layer.view("os", torch.bfloat16, (w.T, w.H))[toks_t]
+    assert_bf16_close(f64(os_), deq(hs, -1) @ deq(dinp["w2_shared"], -1).T, "os (mxfp8, full size)")
+    # combine: y[t] = bf16(sum of the token's k expert rows + shared row)
+    o_rows = f64(fl["o"][torch.from_numpy(slot[toks].ravel()).to(DEV)]).reshape(len(toks), w.k, w.H)
+    assert_bf16_close(f64(y[toks_t]), o_rows.sum(1) + f64(os_), "y (mxfp8 combine, full size)")

@@ -252,3 +252,84 @@ def test_nv4_layer_against_nvfp4_oracle(lib, name):
     assert rel_l2(f64(y)[stable], plain["y"][stable]) < 0.3
     with pytest.raises(api.MoeError):
         api.MoELayer(api.config_of(w), dinp, with_backward=True).forward(dinp["x"])
+
+
+def test_nv4_full_size_sampled(lib):
+    """The Mixtral-like NVFP4 forward at full size, as the benchmark runs it.
+    Tensor amaxes are read from the device tensors with torch (exact maxima
+    of bf16 values); for the expert with the most rows, seeded sample rows of
+    h' and o are recomputed by the oracle from those amaxes (fc1 from x and
+    W1, fc2 from the stored h' rows and W2); the combine is checked on the
+    sampled tokens; the routing properties hold at any size; and the layer
+    stays within the format's error of the bf16 layer."""
+    from gpu_helpers import i64
+    from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs_on_device
+    w = WORKLOADS["mixtral_nvfp4"]
+    dinp = make_inputs_on_device(w, DEV, seed=0)
+    layer = api.MoELayer(api.config_of(w), dinp, with_backward=False)
+    layer.act.fill_(0x7F)
+    y = layer.forward(dinp["x"])
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(layer.ws) == 0
+    fl = layer.fields()
+    cap = layer.layout.cap
+    counts, po = i64(fl["counts"]), i64(fl["poffsets"])
+    assert counts.sum() == w.T * w.k
+    slot = i64(fl["slot_row"])
+    src = i64(fl["row_src"])
+    assert np.all(src[slot] == np.arange(w.T)[:, None])
+    valid = torch.from_numpy((np.arange(cap) < po[-1]) & (src >= 0)).to(DEV)
+    x_amax = float(dinp["x"].abs().max())
+    h_amax = float(fl["h"][valid].abs().max())
+    w1_amax, w2_amax = float(dinp["w1"].abs().max()), float(dinp["w2"].abs().max())
+    e = int(np.argmax(counts))
+    rng = np.random.default_rng(11)
+    rows = np.sort(po[e] + rng.choice(counts[e], size=6, replace=False))
+    toks = src[rows]
+    rows_t = torch.from_numpy(rows).to(DEV)
+    F = w.F
+    xq = O.nvfp4_roundtrip(f64(dinp["x"][torch.from_numpy(toks).to(DEV)]), x_amax)
+    z = xq @ O.nvfp4_roundtrip(f64(dinp["w1"][e]), w1_amax).T
+    g = f64(fl["row_gate"][rows_t])
+    assert_bf16_close(f64(fl["h"][rows_t]), g[:, None] * O.silu(z[:, :F]) * z[:, F:], "h (nvfp4, full size)")
+    hq = O.nvfp4_roundtrip(f64(fl["h"][rows_t]), h_amax)
+    o_ref = hq @ O.nvfp4_roundtrip(f64(dinp["w2"][e]), w2_amax).T
+    assert_bf16_close(f64(fl["o"][rows_t]), o_ref, "o (nvfp4, full size)")
+    # combine on the sampled tokens: y[t] = bf16(sum over the token's k rows of o)
+    o_rows = f64(fl["o"][torch.from_numpy(slot[toks].ravel()).to(DEV)]).reshape(len(toks), w.k, w.H)
+    assert_bf16_close(f64(y[torch.from_numpy(toks).to(DEV)]), o_rows.sum(1), "y (nvfp4 combine, full size)")
+    # the whole layer against the bf16 layer: the format's own error, not a gross one
+    ref = api.MoELayer(api.config_of(WORKLOADS["mixtral"]), dinp, with_backward=False).forward(dinp["x"])
+    torch.cuda.synchronize()
+    r = rel_l2(f64(y), f64(ref))
+    assert 0.02 < r < 0.3, r
+
+
+def test_nv4_layer_graph_replay_is_bit_identical(lib):
+    """The NVFP4 forward (amax reductions, quantisers, code gather, GEMMs with
+    the fused h' amax) issues no host sync: it captures into one CUDA graph,
+    and replays are bit-identical to the eager run (the amaxes are maxima, so
+    the atomics' order does not matter)."""
+    w = NV_LAYERS["dsv3_nv_small"]
+    inp = make_inputs(w, seed=4)
+    dinp = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    layer = api.MoELayer(api.config_of(w), dinp, with_backward=False)
+    x = dinp["x"]
+    y0 = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, y)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, y)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    assert api.moe_read_device_status(layer.ws) == 0
