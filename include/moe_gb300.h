@@ -232,7 +232,12 @@ typedef enum {
    * c = dw1 [E,2F,H] fp32 (zero for experts with no rows). */
   MOE_GG_WGRAD_FC1 = 4,
   /* dW2_e = A_e^T B_e: a = dy_perm [cap,H], b = h [cap,F]; c = dw2 [E,H,F] fp32. */
-  MOE_GG_WGRAD_FC2 = 5
+  MOE_GG_WGRAD_FC2 = 5,
+  /* FC1_SWIGLU with the permutation fused into the A load (bf16, routed only):
+   * a = x [T,H] in token order, a_rows = row_src [cap] (token of each padded
+   * row, -1 for padding: a zero row); A row r is x[a_rows[r]].  b, c, c2,
+   * row_gate, poffsets as FC1_SWIGLU.  x_perm is neither read nor written. */
+  MOE_GG_FC1_SWIGLU_GATHERED = 6
 } moe_gg_op;
 
 /* Arguments of one grouped GEMM.  `poffsets` [E+1] (device) gives each expert's
@@ -274,6 +279,7 @@ typedef struct {
   const void* b_scales;   /* MXFP8 / NVFP4 only */
   const float* a_amax;    /* NVFP4 only */
   const float* b_amax;    /* NVFP4 only */
+  const int32_t* a_rows;  /* FC1_SWIGLU_GATHERED only */
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For

@@ -559,6 +559,11 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
     case MOE_GG_FC1_SWIGLU:
       if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
       return cuda_status(gemm_fc1(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->row_gate, a->c, a->c2, status, st));
+    case MOE_GG_FC1_SWIGLU_GATHERED:
+      if (dense || !dev_ptr_ok(a->a_rows) || (a->c2 != nullptr && !aligned16(a->c2))) return MOE_ERR_INVALID_ARG;
+      if (cfg->F % 128 != 0) return MOE_ERR_INVALID_ARG;
+      return cuda_status(gemm_fc1_gather(a->a, cfg->T, a->a_rows, rows, H, a->b, E, F, po, a->row_gate, a->c, a->c2,
+                                         status, st));
     case MOE_GG_FC2:
       return cuda_status(gemm_fc2(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st));
     case MOE_GG_DGRAD_FC2:

@@ -75,12 +75,18 @@ struct GemmParams {
   // bit patterns, non-negative so they order as unsigned) -- the tensor amax
   // the NVFP4 quantiser of h' needs, taken without another pass over h'.
   unsigned* amax_out;
+  // Gathered A (fc1 with the permutation fused into its A load): row r of the
+  // tile is row a_row_src[r] of a_tok [a_rows, k_len] (token order), or zeros
+  // where a_row_src[r] < 0 (padding).
+  const __nv_bfloat16* a_tok;
+  const int32_t* a_row_src;
+  int a_rows;
   int* status;             // device status word (first error wins)
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
 };
 
 template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, int MX_ = 0, bool M256_ = false,
-          bool PAIR_ = false>
+          bool PAIR_ = false, bool GATHER_ = false>
 struct GemmCfg {
   static constexpr int BM = 128;                  // rows of A and D per CTA and MMA
   static constexpr bool M256 = M256_;             // 256-row tiles: two MMAs share each B k-block
@@ -88,6 +94,12 @@ struct GemmCfg {
   static constexpr bool ROWS256 = M256 || PAIR;   // tiles of 256 rows (pairs of 128-row blocks)
   static constexpr int TILE_M = ROWS256 ? 256 : 128;
   static constexpr bool MX = MX_ != 0;            // block-scaled operands: 1 MXFP8, 2 NVFP4
+  // A rows gathered by the producer warp from the token-order input with
+  // 16-byte cp.async copies (the permutation fused into fc1's A load)
+  static constexpr bool GATHER = GATHER_;
+  // arrivals that complete a full barrier: the TMA producer's, plus one per
+  // gathering lane
+  static constexpr int FULL_COUNT = GATHER ? 33 : 1;
   static constexpr bool NV4 = MX_ == 2;           // NVFP4 (E2M1 + E4M3 1x16 scales + tensor scale)
   // Contraction elements per k-block: one 128-byte swizzle row (K-major), or
   // for the weight gradients on CTA pairs (MN-major, short per-expert K) 128
@@ -173,6 +185,8 @@ struct GemmCfg {
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
   static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
+  static_assert(!GATHER || (M256 && !MX && !A_MN && S == Sched::kRoutedM && BK == 64),
+                "gathered A: bf16 256-row row-grouped tiles");
   static_assert(!WIDE_K || (A_MN && B_MN), "128-row k-blocks only for MN-major operands");
   static_assert(!PAIR || (!M256 && !MX && TMA_OUT && BN == 256 &&
                           (S == Sched::kRoutedK ? (A_MN && B_MN && EP == Epi::kStoreF32) : !A_MN)),
@@ -315,12 +329,12 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
       bulk_load(sf_dst + TB * (i + 1), p.sfb + ((long long)(b_row / 128 + i) * p.sfb_tiles_k + kt) * 512, TB, bar);
     return;
   }
-  // ---- A
+  // ---- A (gathered tiles: the producer warp copies A itself)
   if constexpr (C::S == Sched::kRoutedK) {
     // A[m, k] = Abuf[k_row0 + k, m0 + m]  (MN-major, two 64-wide chunks)
     tma_load_2d(a_dst, tmA, bar, ti.m0, ti.k_row0 + k0);
     tma_load_2d(a_dst + 8192, tmA, bar, ti.m0 + 64, ti.k_row0 + k0);
-  } else {
+  } else if constexpr (!C::GATHER) {
     tma_load_2d(a_dst, tmA, bar, k0, ti.m0);
   }
   // ---- B
@@ -908,7 +922,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], C::FULL_COUNT);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < C::ACC_BUFS; ++a) {
@@ -959,6 +973,90 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int ntiles = s_bad ? 0 : total_tiles<C>(p, s_poff, s_tpre);
 
   if (warp == 0) {
+    if constexpr (C::GATHER) {
+      // -------------------------------- gathering producer (all 32 lanes)
+      // Lane 0 runs the schedule and the B TMA loads; every lane copies 8 rows
+      // of each A k-block (rows lane + 32 i) from the token-order input with
+      // 16-byte cp.async into the 128B-swizzled layout TMA would have written
+      // (chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16)).  A stage is
+      // signalled once its copies have landed: after the next stage's copies are
+      // issued, each lane waits for its older group, fences the writes for the
+      // tensor cores' (async) proxy and arrives on the stage's full barrier.
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      int pending = -1;
+      bool ok = true;
+      int next = 0;
+      if (lane == 0) next = (p.sched != nullptr) ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      const uint32_t a_base = smem_u32(a_smem);
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kSchedDepth;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&bk.sched_empty[slot], ((j / kSchedDepth) & 1) ^ 1u, abort_ptr) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        const int t = (next < ntiles) ? next : -1;
+        if (lane == 0) {
+          bk.sched_tile[slot] = t;
+          mbar_arrive(&bk.sched_full[slot]);
+          if (t >= 0) next = (p.sched != nullptr) ? atomicAdd(p.sched, 1) : t + static_cast<int>(gridDim.x);
+        }
+        if (t < 0) break;
+        next = __shfl_sync(0xffffffffu, next, 0);
+        const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
+        const __nv_bfloat16* src[8];
+        uint32_t live = 0;                   // rows with a token (the rest are zero rows)
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = ti.m0 + lane + 32 * i;
+          int tok = (r < p.rows_cap) ? p.a_row_src[r] : -1;
+          if (tok >= p.a_rows) tok = -1;
+          src[i] = p.a_tok + (tok >= 0 ? static_cast<long long>(tok) * p.k_len : 0);
+          live |= (tok >= 0 ? 1u : 0u) << i;
+        }
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          int e = 1;
+          if (lane == 0) e = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, e, 0)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full_bar[stage], C::B_BYTES);
+            issue_loads<C>(&tmA, &tmB, p, ti, kb, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
+                           sf_smem, &full_bar[stage]);
+          }
+          const int k0 = kb * C::BK;
+          const uint32_t dst0 = a_base + stage * C::A_BYTES;
+          #pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = lane + 32 * i;
+            const uint32_t rb = dst0 + r * 128;
+            const uint32_t nbytes = ((live >> i) & 1u) ? 16u : 0u;
+            #pragma unroll
+            for (int c = 0; c < 8; ++c) cp_async_16(rb + ((c ^ (r & 7)) << 4), src[i] + k0 + 8 * c, nbytes);
+          }
+          cp_async_commit();
+          if (pending >= 0) {
+            cp_async_wait<1>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full_bar[pending]);
+          }
+          pending = stage;
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (pending >= 0) mbar_arrive(&full_bar[pending]);
+      if (lane == 0) {
+        sched_finish(p.sched);
+        if (!ok) {
+          for (int s = 0; s < C::STAGES; ++s)
+            if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
+        }
+      }
+    } else {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       int stage = 0;
@@ -992,6 +1090,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int s = 0; s < C::STAGES; ++s)
           if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
       }
+    }
     }
   } else if (warp == 1) {
     if (lane == 0) {

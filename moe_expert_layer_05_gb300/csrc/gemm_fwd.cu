@@ -117,6 +117,40 @@ cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E
   return launch_gemm<C>(ta, tb, tc, tz, p, tiles < num_sms() ? tiles : num_sms(), st);
 }
 
+cudaError_t gemm_fc1_gather(const void* x, int T, const int32_t* row_src, int rows_alloc, int H, const void* w1,
+                            int E, int F, const int32_t* poffsets, const float* row_gate, void* h, void* z, int* status,
+                            cudaStream_t st) {
+  // A rows are copied by the kernel's producer warp from x [T, H] (token order)
+  // through row_src; only W1 goes through TMA
+  CUtensorMap tb;
+  if (!make_tmap_bf16(&tb, w1, H, static_cast<uint64_t>(E) * 2 * F, 64, 128)) return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.k_len = H;
+  p.n_tiles = F / 128;
+  p.b_rows_per_group = 2 * F;
+  p.b_half_offset = F;
+  p.c = h;
+  p.ldc = F;
+  p.c2 = z;
+  p.ldc2 = 2 * F;
+  p.half_cols = F;
+  p.row_gate = row_gate;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.a_tok = static_cast<const __nv_bfloat16*>(x);
+  p.a_row_src = row_src;
+  p.a_rows = T;
+  CUtensorMap tc, tz;
+  if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
+    return cudaErrorInvalidValue;
+  if (z == nullptr) tz = tc;
+  using C = GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwiglu, 0, true, false, true>;
+  const int upper = (rows_alloc / 128) * p.n_tiles;
+  return launch_gemm<C>(tb, tb, tc, tz, p, upper < num_sms() ? upper : num_sms(), st);
+}
+
 namespace {
 template <int BN>
 cudaError_t fc2_bn(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,

@@ -56,6 +56,11 @@ cudaError_t gemm_router(const void* x, const void* wr, int T, int H, int E, floa
 // poffsets == nullptr: dense, rows = dense_rows, one group.
 cudaError_t gemm_fc1(const void* a, int rows_alloc, int H, const void* w1, int E, int F, const int32_t* poffsets,
                      int dense_rows, const float* row_gate, void* h, void* z, int* status, cudaStream_t st);
+// fc1 with the permutation fused into its A load: row r of A is x[row_src[r]]
+// (zeros where row_src[r] < 0); x [T,H] in token order.
+cudaError_t gemm_fc1_gather(const void* x, int T, const int32_t* row_src, int rows_alloc, int H, const void* w1,
+                            int E, int F, const int32_t* poffsets, const float* row_gate, void* h, void* z, int* status,
+                            cudaStream_t st);
 // o[cap,H] = A[cap,F] * W2_e[H,F]^T
 cudaError_t gemm_fc2(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
                      int dense_rows, void* o, int* status, cudaStream_t st);

@@ -241,6 +241,41 @@ def test_gemm_fc1_fc2(lib, T, H, E, k, F, skew):
     assert_bf16_close(f64(o)[:used], or_, "o", rel_l2_tol=8e-3, elem_rel=2.0 ** -6, elem_abs_frac=2e-2)
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", GEMM_CASES)
+def test_gemm_fc1_gathered(lib, T, H, E, k, F, skew):
+    """fc1 with the permutation fused into its A load (rows gathered from x in
+    token order by row_src, zero rows for padding) gives z and h bit-identical
+    to fc1 on the explicitly permuted x_perm (same operand bytes, same MMA
+    order), and both match the oracle.  Rows past the last segment of row_src
+    hold garbage that no tile may read."""
+    cfg, m, cap, used, valid = _routed_case(T, H, E, k, F, skew, 31)
+    x = to_bf16(_rand((T, H), 32))
+    w1 = to_bf16(_rand((E, 2 * F, H), 33, 0.05)).to(DEV)
+    rg = np.where(valid, np.abs(_rand((cap,), 34)), 0).astype(np.float32)
+    rs = np.full(cap, 0x7F7F7F7F, np.int32)
+    rs[:used] = m["row_src"]
+    xp = np.zeros((cap, H), np.float32)
+    xp[:used][m["row_src"] >= 0] = x.float().numpy()[m["row_src"][m["row_src"] >= 0]]
+    x_perm = to_bf16(xp).to(DEV)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    rgd = torch.from_numpy(rg).to(DEV)
+    ws = _ws(cfg)
+    outs = []
+    for op, a, extra in ((api.GG_FC1_SWIGLU, x_perm, {}),
+                         (api.GG_FC1_SWIGLU_GATHERED, x.to(DEV), {"a_rows": torch.from_numpy(rs).to(DEV)})):
+        z = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=DEV)
+        h = torch.zeros((cap, F), dtype=torch.bfloat16, device=DEV)
+        api.moe_grouped_gemm(cfg, op, a, w1, h, ws, c2=z, row_gate=rgd, poffsets=po, **extra)
+        outs.append((z, h))
+    torch.cuda.synchronize()
+    assert _status(ws) == 0
+    (z0, h0), (z1, h1) = outs
+    assert torch.equal(z0[:used].view(torch.int16), z1[:used].view(torch.int16))
+    assert torch.equal(h0[:used].view(torch.int16), h1[:used].view(torch.int16))
+    zr, hr = O.expert_fc1(f64(x_perm)[:used], LazyW(w1), m["poffsets"], rg[:used])
+    assert_bf16_close(f64(h1)[:used], hr, "h (gathered)")
+
+
 class LazyW:
     def __init__(self, t):
         self.t, self.shape, self.c = t, tuple(t.shape), {}
