@@ -114,3 +114,19 @@ def test_nvfp4_config_rules_and_sizes():
     assert lib.moe_quantize_nvfp4(16, 1, 100, 64, 0, 16, 16, 16, None) == -1
     assert lib.moe_quantize_nvfp4(16, 1, 128, 64, 1, 16, 16, 16, None) == -1
     assert lib.moe_quantize_nvfp4(16, 1, 128, 64, 0, 16, 16, None, None) == -1
+
+
+def test_gathered_fc1_arguments_checked_before_launch():
+    """MOE_GG_FC1_SWIGLU_GATHERED needs the row map (a_rows) and a routed call;
+    MXFP8 / NVFP4 layers do not offer it."""
+    lib = api.load()
+    cfg = api.make_config(256, 128, 8, 2, 256)
+    no_rows = api.MoeGemmArgs(api.GG_FC1_SWIGLU_GATHERED, 0, 16, 16, 16, None, None, None, None, 16)
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(no_rows), 16, None) in (-1, -2)   # -2: no GB300
+    dense = api.MoeGemmArgs(api.GG_FC1_SWIGLU_GATHERED, 128, 16, 16, 16, None, None, None, None, 16)
+    dense.a_rows = 16
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(dense), 16, None) in (-1, -2)
+    for dt in ("mxfp8", "nvfp4"):
+        c = api.make_config(256, 256, 8, 2, 256, dtype=dt)
+        a = api.MoeGemmArgs(api.GG_FC1_SWIGLU_GATHERED, 0, 16, 16, 16, None, None, None, None, 16, 16, 16, 16, 16, 16)
+        assert lib.moe_grouped_gemm(ctypes.byref(c), ctypes.byref(a), 16, None) in (-1, -2)
