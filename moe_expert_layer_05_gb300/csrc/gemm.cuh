@@ -3,11 +3,14 @@
 // One CTA per SM walks a list of output tiles: 128 x BN, or 256 x BN where two
 // 128-row MMAs share each B k-block.  Warp roles:
 //   warp 0      TMA producer: takes tile indices from a counter in global
-//               memory and streams A and B k-blocks (64 bf16 = one 128-B
-//               swizzle row) into a STAGES-deep shared-memory ring;
-//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
-//               K=16) into a TMEM accumulator (two where they fit, so the
-//               epilogue of one tile overlaps the MMAs of the next);
+//               memory and streams A and B k-blocks (one 128-B swizzle row:
+//               64 bf16, 128 E4M3 or 256 E2M1 values, plus their scale tiles
+//               for MXFP8 / NVFP4) into a STAGES-deep shared-memory ring; for
+//               the gathered fc1 all 32 lanes copy A rows with cp.async;
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN;
+//               kind::f16, mxf8f6f4 or mxf4nvf4 block-scaled) into a TMEM
+//               accumulator (two where they fit, so the epilogue of one tile
+//               overlaps the MMAs of the next);
 //   warps 2..   epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32*(w%4)..+31, i.e. one output row per thread),
 //               apply the fused elementwise step and store through TMA.
