@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FLUSH_BYTES = 512 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one fc1 launch, from the ncu
 # capture summarised in profiles/ (None until captured for the current kernel).
-FC1_TRAFFIC_BYTES = 2.342e9   # profiles/fc1_grouped_gemm_mixtral_full.md (bf16 Mixtral-like fc1, DRAM read + write)
+FC1_TRAFFIC_BYTES = 2.295e9   # profiles/fc1_grouped_gemm_mixtral_full.md (bf16 Mixtral-like fc1, DRAM read + write)
 # NVFP4 Mixtral-like fc1: captured at T=2048, E=4 (the same 1024 rows per
 # expert), 374.1 MB; the traffic grows with the experts, so x2 for E=8
 # (profiles/fc1_grouped_gemm_mixtral_nvfp4.md)
