@@ -214,3 +214,15 @@ def test_sampled_tokens_with_full_tensor_amaxes_match_the_full_forward():
     np.testing.assert_allclose(part["y"], full["y"][tokens], rtol=1e-12, atol=1e-13)
     wrong = O.moe_forward_nvfp4(x[tokens], wr, w1, w2, k=2)  # the sample's own amaxes: other codes
     assert np.abs(wrong["y"] - full["y"][tokens]).max() > 1e-4
+
+
+def test_bf16_round_matches_torch_cast():
+    """The oracle's bf16 storage rounding equals torch's round-to-nearest-even
+    cast (a library routine), ties included."""
+    import torch
+    rng = np.random.default_rng(12)
+    v = np.concatenate([rng.standard_normal(100000) * np.exp2(rng.integers(-30, 30, 100000)),
+                        1.0 + np.arange(-64, 64) * 2.0 ** -8,          # exact ties between bf16 neighbours
+                        [0.0, -0.0, 65504.0, -3.0e38]])
+    want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(v), want)
