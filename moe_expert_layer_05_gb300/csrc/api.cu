@@ -647,8 +647,9 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     float* amax = reinterpret_cast<float*>(mb + M.amax);
     const float* wamax = at<const float>(const_cast<void*>(w->mx), W.amax);
     MOE_TRY(launch_amax_bf16(x, T, H, nullptr, nullptr, amax + 0, st));
-    MOE_TRY(launch_quantize_rows_nv4(x, T, H, 0, amax + 0, q(M.xs), f(M.xs), st));
-    MOE_TRY(launch_gather_rows_nv4(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st));
+    // straight into expert order; the token-order copy only for the shared expert
+    MOE_TRY(launch_quantize_gather_nv4(x, T, H, slot_row, k, amax + 0, q(M.x), f(M.x), S > 0 ? q(M.xs) : nullptr,
+                                       S > 0 ? f(M.xs) : nullptr, st));
     // fc1 writes h' and its amax (padding rows have gate 0, so h' = 0 there;
     // rows past the last expert's segment are never computed)
     MOE_TRY(cudaMemsetAsync(amax + 1, 0, sizeof(float), st));

@@ -112,8 +112,11 @@ cudaError_t launch_amax_bf16(const void* src, long long rows, int cols, const in
 // Blocks of 16 along each row with the tensor scale of *amax; codes [rows, cols/2].
 cudaError_t launch_quantize_rows_nv4(const void* src, long long rows, int cols, int gate_up_half,
                                      const float* amax, uint8_t* codes, uint8_t* sf, cudaStream_t st);
-cudaError_t launch_gather_rows_nv4(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
-                                   int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st);
+// x [T,H] quantised straight into its k expert-ordered rows (and into token
+// order as well when codes_tok is given).
+cudaError_t launch_quantize_gather_nv4(const void* x, int T, int H, const int32_t* slot_row, int k,
+                                      const float* amax, uint8_t* codes_perm, uint8_t* sf_perm, uint8_t* codes_tok,
+                                      uint8_t* sf_tok, cudaStream_t st);
 // NVFP4 GEMMs: A [rows, K] and B_e [N, K] E2M1 codes with scale tiles; amax_a,
 // amax_b their tensor amaxes (device).  amax_h (nullable, zeroed by the caller):
 // receives max |h'| over the rows fc1 computes.

@@ -78,6 +78,28 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict_
   }
 }
 
+// One block of 16 values (two 16-byte loads of bf16) -> eight code bytes
+// (w[0], w[1]) and the scale byte, with the tensor scale S.
+__device__ __forceinline__ uint32_t quantize16(const uint4* p, float S, uint32_t (&w)[2]) {
+  const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+  const float v[16] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y),
+                       bf16_lo(u0.z), bf16_hi(u0.z), bf16_lo(u0.w), bf16_hi(u0.w),
+                       bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
+                       bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
+  float amax_b = 0.f;
+  #pragma unroll
+  for (int j = 0; j < 16; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
+  const float d = amax_b / 6.0f;
+  const uint32_t s = cvt_e4m3(d * S);
+  const float sv = e4m3_to_f32(s);
+  float rr = sv > 0.f ? S / sv : 0.f;
+  if (!(rr <= FLT_MAX)) rr = FLT_MAX;
+  w[0] = w[1] = 0u;
+  #pragma unroll
+  for (int j = 0; j < 8; ++j) w[j >> 2] |= cvt_e2m1x2(v[2 * j] * rr, v[2 * j + 1] * rr) << (8 * (j & 3));
+  return s;
+}
+
 // Blocks of 16 along each row: src [rows, cols] bf16 -> codes [rows, cols/2]
 // bytes, scale tiles.  One thread per block: two 16-byte loads, one 8-byte
 // store of codes, one scale byte.
@@ -91,53 +113,40 @@ __global__ void __launch_bounds__(256) quantize_rows_nv4_kernel(const uint4* __r
   const long long r_in = i / nb;
   const long long r = gate_up_row16(r_in, half);
   const int b = static_cast<int>(i - r_in * nb);
-  const uint4 u0 = __ldg(src + 2 * i), u1 = __ldg(src + 2 * i + 1);
-  const float v[16] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y),
-                       bf16_lo(u0.z), bf16_hi(u0.z), bf16_lo(u0.w), bf16_hi(u0.w),
-                       bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
-                       bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
-  float amax_b = 0.f;
-  #pragma unroll
-  for (int j = 0; j < 16; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
-  const float S = nv4_tensor_scale(__ldg(amax_p));
-  const float d = amax_b / 6.0f;
-  const uint32_t s = cvt_e4m3(d * S);
-  const float sv = e4m3_to_f32(s);
-  float rr = sv > 0.f ? S / sv : 0.f;
-  if (!(rr <= FLT_MAX)) rr = FLT_MAX;
-  uint32_t w[2] = {0u, 0u};
-  #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j >> 2] |= cvt_e2m1x2(v[2 * j] * rr, v[2 * j + 1] * rr) << (8 * (j & 3));
+  uint32_t w[2];
+  const uint32_t s = quantize16(src + 2 * i, nv4_tensor_scale(__ldg(amax_p)), w);
   *reinterpret_cast<uint2*>(codes + r * (cols / 2) + b * 8) = make_uint2(w[0], w[1]);
   sf[sf_offset16(r, b, cols / 64)] = static_cast<uint8_t>(s);
 }
 
-// Token-order codes [T, H/2] and scale tiles -> expert order (the bf16
-// gather's permutation on codes and scales).
-__global__ void __launch_bounds__(128) gather_rows_nv4_kernel(const uint4* __restrict__ codes_tok,
-                                                              const uint8_t* __restrict__ sf_tok,
-                                                              const int32_t* __restrict__ slot_row, int k, int H,
-                                                              uint4* __restrict__ codes_perm,
-                                                              uint8_t* __restrict__ sf_perm) {
-  const int t = blockIdx.x;
-  __shared__ int s_rows[kMaxK];
-  if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[static_cast<long long>(t) * k + threadIdx.x];
-  __syncthreads();
-  const int nv = H / 32;                     // 16-byte pieces of a row of codes
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    const uint4 c = __ldg(codes_tok + static_cast<long long>(t) * nv + v);
-    for (int i = 0; i < k; ++i) {
-      const int r = s_rows[i];
-      if (r >= 0) codes_perm[static_cast<long long>(r) * nv + v] = c;
-    }
+// Token rows of x [T, H] quantised straight into expert order: block b of
+// token t goes to each of its k padded rows (slot_row), and to row t of the
+// token-order copy when one is asked for (the shared expert reads it).  The
+// codes of a row do not depend on where the row goes (blocks lie along H).
+__global__ void __launch_bounds__(256) quantize_gather_nv4_kernel(const uint4* __restrict__ src, int T, int H,
+                                                                  const int32_t* __restrict__ slot_row, int k,
+                                                                  const float* __restrict__ amax_p,
+                                                                  uint8_t* __restrict__ codes_perm,
+                                                                  uint8_t* __restrict__ sf_perm,
+                                                                  uint8_t* __restrict__ codes_tok,
+                                                                  uint8_t* __restrict__ sf_tok) {
+  const int nb = H / 16;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(T) * nb) return;
+  const int t = static_cast<int>(i / nb);
+  const int b = static_cast<int>(i - static_cast<long long>(t) * nb);
+  uint32_t w[2];
+  const uint32_t s = quantize16(src + 2 * i, nv4_tensor_scale(__ldg(amax_p)), w);
+  const uint2 c = make_uint2(w[0], w[1]);
+  for (int j = 0; j < k; ++j) {
+    const int r = __ldg(slot_row + static_cast<long long>(t) * k + j);
+    if (r < 0) continue;
+    *reinterpret_cast<uint2*>(codes_perm + static_cast<long long>(r) * (H / 2) + b * 8) = c;
+    sf_perm[sf_offset16(r, b, H / 64)] = static_cast<uint8_t>(s);
   }
-  const int nb = H / 16, tiles = H / 64;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    const uint8_t e = sf_tok[sf_offset16(t, b, tiles)];
-    for (int i = 0; i < k; ++i) {
-      const int r = s_rows[i];
-      if (r >= 0) sf_perm[sf_offset16(r, b, tiles)] = e;
-    }
+  if (codes_tok != nullptr) {
+    *reinterpret_cast<uint2*>(codes_tok + static_cast<long long>(t) * (H / 2) + b * 8) = c;
+    sf_tok[sf_offset16(t, b, H / 64)] = static_cast<uint8_t>(s);
   }
 }
 
@@ -167,13 +176,16 @@ cudaError_t launch_quantize_rows_nv4(const void* src, long long rows, int cols, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows_nv4(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
-                                   int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st) {
-  if (T == 0) return cudaSuccess;
-  gather_rows_nv4_kernel<<<T, 128, 0, st>>>(reinterpret_cast<const uint4*>(codes_tok), sf_tok, slot_row, k, H,
-                                            reinterpret_cast<uint4*>(codes_perm), sf_perm);
+cudaError_t launch_quantize_gather_nv4(const void* x, int T, int H, const int32_t* slot_row, int k,
+                                      const float* amax, uint8_t* codes_perm, uint8_t* sf_perm, uint8_t* codes_tok,
+                                      uint8_t* sf_tok, cudaStream_t st) {
+  const long long n = static_cast<long long>(T) * (H / 16);
+  if (n == 0) return cudaSuccess;
+  quantize_gather_nv4_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+      static_cast<const uint4*>(x), T, H, slot_row, k, amax, codes_perm, sf_perm, codes_tok, sf_tok);
   count_launches(1);
   return cudaGetLastError();
 }
+
 
 }  // namespace moe
