@@ -298,6 +298,31 @@ int32_t* hist_ptr(void* ws) { return at<int32_t>(ws, kStatusBytes); }
 
 }  // namespace
 
+namespace {
+// The host-side checks of one grouped-GEMM call that depend on the op and
+// the operand type, all before the device check so that a bad argument
+// reads as MOE_ERR_INVALID_ARG (or an op the type does not offer as
+// MOE_ERR_UNSUPPORTED) on any machine.
+moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool dense) {
+  const bool fc1 = a->op == MOE_GG_FC1_SWIGLU || a->op == MOE_GG_FC1_SWIGLU_GATHERED;
+  if (fc1 && a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
+  if (a->op == MOE_GG_DGRAD_FC2 && !dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
+  if (a->op < MOE_GG_FC1_SWIGLU || a->op > MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_BF16) {
+    if (a->op == MOE_GG_FC1_SWIGLU_GATHERED && (dense || !dev_ptr_ok(a->a_rows))) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+  }
+  if (a->op == MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;     // bf16 only
+  if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
+  if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_GEMM_NVFP4) {
+    if (!f32_ptr_ok(a->a_amax) || !f32_ptr_ok(a->b_amax)) return MOE_ERR_INVALID_ARG;
+    if (a->op != MOE_GG_FC1_SWIGLU && a->op != MOE_GG_FC2) return MOE_ERR_UNSUPPORTED;   // forward GEMMs only
+  }
+  return MOE_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* moe_status_string(moe_status s) {
@@ -498,6 +523,7 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
   const bool dense = a->dense_rows > 0;
   if (!dense && !dev_ptr_ok(a->poffsets)) return MOE_ERR_INVALID_ARG;
   if (a->dense_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (moe_status s = gemm_args_check(cfg, a, dense); s != MOE_OK) return s;
   if (moe_status s = check_device(); s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int H = cfg->H;

@@ -81,8 +81,7 @@ def test_null_and_misaligned_pointers_rejected_before_launch():
     args = api.MoeGemmArgs(0, 0, 16, 16, 16, None, None, None, None, None)  # routed without offsets
     assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), 16, None) == -1
     args = api.MoeGemmArgs(9, 16, 16, 16, 16, None, None, None, None, None)
-    st = lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), 16, None)
-    assert st in (-1, -2)      # unknown op (or no GB300 here)
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), 16, None) == -1   # unknown op
 
 
 def test_nvfp4_config_rules_and_sizes():
@@ -122,11 +121,32 @@ def test_gathered_fc1_arguments_checked_before_launch():
     lib = api.load()
     cfg = api.make_config(256, 128, 8, 2, 256)
     no_rows = api.MoeGemmArgs(api.GG_FC1_SWIGLU_GATHERED, 0, 16, 16, 16, None, None, None, None, 16)
-    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(no_rows), 16, None) in (-1, -2)   # -2: no GB300
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(no_rows), 16, None) == -1
     dense = api.MoeGemmArgs(api.GG_FC1_SWIGLU_GATHERED, 128, 16, 16, 16, None, None, None, None, 16)
     dense.a_rows = 16
-    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(dense), 16, None) in (-1, -2)
+    assert lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(dense), 16, None) == -1
     for dt in ("mxfp8", "nvfp4"):
         c = api.make_config(256, 256, 8, 2, 256, dtype=dt)
         a = api.MoeGemmArgs(api.GG_FC1_SWIGLU_GATHERED, 0, 16, 16, 16, None, None, None, None, 16, 16, 16, 16, 16, 16)
-        assert lib.moe_grouped_gemm(ctypes.byref(c), ctypes.byref(a), 16, None) in (-1, -2)
+        assert lib.moe_grouped_gemm(ctypes.byref(c), ctypes.byref(a), 16, None) == -1
+
+
+def test_low_precision_gemm_arguments_checked_before_launch():
+    """MXFP8 / NVFP4 grouped GEMMs need their scale tiles (and NVFP4 the tensor
+    amaxes); NVFP4 offers the forward ops only (MOE_ERR_UNSUPPORTED for the
+    rest); dense calls need whole 128-row scale tiles."""
+    lib = api.load()
+    nv = api.make_config(256, 256, 8, 2, 256, dtype="nvfp4")
+    mx = api.make_config(256, 256, 8, 2, 256, dtype="mxfp8")
+
+    def call(cfg, op, dense_rows=0, scales=16, amax=16):
+        a = api.MoeGemmArgs(op, dense_rows, 16, 16, 16, None, 16, None, None, 16, scales, scales, amax, amax)
+        return lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(a), 16, None)
+
+    assert call(nv, api.GG_FC1_SWIGLU, scales=None) == -1
+    assert call(nv, api.GG_FC2, amax=None) == -1
+    assert call(nv, api.GG_FC2, amax=18) == -1                 # misaligned fp32
+    for op in (api.GG_DGRAD_FC2, api.GG_DGRAD_FC1, api.GG_WGRAD_FC1, api.GG_WGRAD_FC2):
+        assert call(nv, op) == -2
+    assert call(mx, api.GG_FC2, scales=None) == -1
+    assert call(mx, api.GG_FC1_SWIGLU, dense_rows=100) == -1
