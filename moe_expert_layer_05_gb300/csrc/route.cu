@@ -92,6 +92,61 @@ __device__ __forceinline__ void topk_one_token(const float* __restrict__ row, co
   out_gate = w / sum;
 }
 
+// Route one token in one thread (few experts: E <= kThreadTopkE): the same
+// keys, tie rule, slot order and gate arithmetic as topk_one_token, so the
+// result is identical; a warp then routes 32 tokens at once instead of one.
+constexpr int kThreadTopkE = 16;
+__device__ __forceinline__ void topk_one_token_thread(const float* __restrict__ row, const float* __restrict__ bias,
+                                                      int E, int k, int score, int32_t* __restrict__ idx_out,
+                                                      float* __restrict__ gate_out, int* __restrict__ s_idx_out) {
+  float lg[kThreadTopkE], key[kThreadTopkE];
+  #pragma unroll
+  for (int e = 0; e < kThreadTopkE; ++e) {
+    lg[e] = (e < E) ? row[e] : 0.f;
+    if (score == 0) {
+      key[e] = lg[e];
+    } else {
+      key[e] = 1.0f / (1.0f + expf(-lg[e]));
+      if (bias != nullptr && e < E) key[e] += bias[e];
+    }
+  }
+  // slots unrolled to the bound and guarded by k, so every array stays in registers
+  uint32_t taken = 0;
+  float slot_logit[kThreadTopkE];
+  int slot_id[kThreadTopkE];
+  #pragma unroll
+  for (int s = 0; s < kThreadTopkE; ++s) {
+    if (s < k) {
+      Cand best{0.f, 0.f, INT_MAX};
+      #pragma unroll
+      for (int e = 0; e < kThreadTopkE; ++e) {
+        Cand c{key[e], lg[e], (e < E && !((taken >> e) & 1u)) ? e : INT_MAX};
+        if (better(c, best)) best = c;
+      }
+      taken |= 1u << best.id;
+      slot_logit[s] = best.logit;
+      slot_id[s] = best.id;
+    }
+  }
+  float w[kThreadTopkE];
+  float sum = 0.f;                                        // slot order, as the warp version
+  #pragma unroll
+  for (int s = 0; s < kThreadTopkE; ++s) {
+    if (s < k) {
+      w[s] = (score == 0) ? expf(slot_logit[s] - slot_logit[0]) : 1.0f / (1.0f + expf(-slot_logit[s]));
+      sum += w[s];
+    }
+  }
+  #pragma unroll
+  for (int s = 0; s < kThreadTopkE; ++s) {
+    if (s < k) {
+      idx_out[s] = slot_id[s];
+      gate_out[s] = w[s] / sum;
+      s_idx_out[s] = slot_id[s];
+    }
+  }
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                    int T, int E, int k, int score, int32_t* __restrict__ idx,
@@ -166,7 +221,8 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __
 }
 
 // Top-k gating fused with the chunk histogram: block b routes the tokens of
-// chunk b (one warp per token, as topk_kernel) and then counts its pairs.
+// chunk b (one warp per token, as topk_kernel; one thread per token when
+// E <= kThreadTopkE) and then counts its pairs.
 template <int PER_LANE>
 __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* __restrict__ logits,
                                                                    const float* __restrict__ bias, int T, int E,
@@ -190,16 +246,25 @@ __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* 
     for (int i = threadIdx.x; i < nt * E; i += blockDim.x) s_logit[i] = __ldg(src + i);
     __syncthreads();
   }
-  for (int u = warp; u < tpb; u += 8) {
-    const int t = t0 + u;
-    if (t >= T) break;
-    int id;
-    float g;
-    topk_one_token<PER_LANE>(staged ? s_logit + u * E : logits + (long long)t * E, bias, E, k, score, lane, id, g);
-    if (lane < k) {
-      idx[(long long)t * k + lane] = id;
-      gate[(long long)t * k + lane] = g;
-      s_idx[u * k + lane] = id;
+  if constexpr (PER_LANE == 0) {
+    // few experts (E <= kThreadTopkE): one thread per token
+    for (int u = threadIdx.x; u < nt; u += blockDim.x) {
+      const long long t = t0 + u;
+      topk_one_token_thread(staged ? s_logit + u * E : logits + t * E, bias, E, k, score, idx + t * k, gate + t * k,
+                            s_idx + u * k);
+    }
+  } else {
+    for (int u = warp; u < tpb; u += 8) {
+      const int t = t0 + u;
+      if (t >= T) break;
+      int id;
+      float g;
+      topk_one_token<PER_LANE>(staged ? s_logit + u * E : logits + (long long)t * E, bias, E, k, score, lane, id, g);
+      if (lane < k) {
+        idx[(long long)t * k + lane] = id;
+        gate[(long long)t * k + lane] = g;
+        s_idx[u * k + lane] = id;
+      }
     }
   }
   __syncthreads();
@@ -605,7 +670,9 @@ cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int
                                      cudaStream_t st) {
   const int NB = chunks_of(T, k);
   if (NB > 0) {
-    if (E <= 32) topk_hist_kernel<1><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    if (E <= kThreadTopkE)
+      topk_hist_kernel<0><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    else if (E <= 32) topk_hist_kernel<1><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
     else if (E <= 64) topk_hist_kernel<2><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
     else if (E <= 128) topk_hist_kernel<4><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
     else topk_hist_kernel<8><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);

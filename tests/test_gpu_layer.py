@@ -274,3 +274,22 @@ def test_router_replay_reproduces_the_layer_permutation(lib):
     assert torch.equal(got["row_src"][:used], fl["row_src"][:used])
     assert torch.equal(got["row_gate"][:used], fl["row_gate"][:used])
     assert torch.equal(got["x_perm"][:used].view(torch.int16), fl["x_perm"][:used].view(torch.int16))
+
+
+@pytest.mark.parametrize("E,k,score", [(8, 2, "softmax"), (16, 3, "sigmoid"), (16, 16, "softmax"), (32, 4, "softmax"),
+                                       (64, 8, "sigmoid")])
+def test_fused_topk_matches_the_standalone_gating(lib, E, k, score):
+    """The layer's top-k (fused with the counting-sort histogram: one thread
+    per token for E <= 16, one warp per token above) gives indices and gates
+    bit-identical to the standalone gating kernel on the same logits."""
+    w = Workload("topk", T=640, H=128, E=E, k=k, F=128, score=score, zipf_s=1.2 if score == "sigmoid" else 0.0)
+    dinp = _to_dev(make_inputs(w, seed=9))
+    layer = _layer(w, dinp, False)
+    layer.forward(dinp["x"])
+    fl = layer.fields()
+    idx = torch.empty_like(fl["topk_idx"])
+    gate = torch.empty_like(fl["topk_gate"])
+    api.moe_topk_gating(layer.cfg, fl["logits"], dinp["bias"], idx, gate)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, fl["topk_idx"])
+    assert torch.equal(gate.view(torch.int32), fl["topk_gate"].view(torch.int32))
