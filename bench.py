@@ -3,18 +3,27 @@
 
 A step is one pass of the layer over one batch: router GEMM, top-k gating,
 sync-free permutation, grouped-GEMM SwiGLU experts with the gate applied at the
-activation, combine (plus dgrad + wgrad for workloads that train).  The default
-workload is the Mixtral-like forward layer (T=4096, H=4096, E=8, k=2,
-F=14336, bf16), seeded synthetic inputs.
+activation, combine, plus the data and weight gradients for the workloads that
+train.  Seeded synthetic inputs of the layer shapes the Megatron Core MoE
+summary trains (Mixtral-, Qwen3- and DeepSeek-V3-like layers).
+
+With no --workload the run measures all five configurations one after the
+other (tiny, Mixtral-like, Qwen3-like training, DeepSeek-like bf16 forward,
+DeepSeek-like MXFP8 training) and prints one line whose headline is the
+largest, the DeepSeek-like MXFP8 training layer (T=16384, H=7168, E=256 + one
+shared expert, k=8, F=2048); the other four are complete sub-records under
+"configs".  Under torchrun (N>1) every rank runs the headline only.
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on
 the launching stream, with L2 flushed (a 512 MB write) before every step outside
-the events; barrier + synchronize on both sides; the max over ranks.  With
---gpus N under torchrun every rank runs its own tokens through replicated
-experts (no data-path collective): weak scaling.  The end-to-end figure (e2e)
-streams K batches from pinned host memory and reads every result back, on two
-copy streams with double-buffered device inputs, so the copies of one step
-overlap the compute of its neighbours.
+the events; barrier + synchronize on both sides; the max over ranks.  Every rank
+runs its own tokens through replicated experts (no data-path collective): weak
+scaling.  The end-to-end figure (e2e) streams K batches from pinned host memory
+and reads every result back, on two copy streams with double-buffered device
+inputs.  Each grouped GEMM of the step is then timed alone on the same inputs
+and set against its roofline: max(flops / tensor peak, algorithmic bytes / HBM
+bandwidth), both terms reported.  nvidia-smi samples the clocks from the first
+warm-up step to the end of the end-to-end leg.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -22,7 +31,9 @@ overlap the compute of its neighbours.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import dataclasses
+import gc
 import json
 import os
 import statistics
@@ -38,18 +49,17 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs, make_inputs_on_device  # noqa: E402
+from moe_expert_layer_05_gb300.inputs import (WORKLOADS, make_inputs, make_inputs_on_device,  # noqa: E402
+                                              make_router_inputs_on_device)
 
 METRIC = "MoE layer tokens/s on 1 GB300; grouped-GEMM TFLOPS as % of tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum of one fc1 launch, from the ncu
-# capture summarised in profiles/ (None until captured for the current kernel).
-FC1_TRAFFIC_BYTES = 2.295e9   # profiles/fc1_grouped_gemm_mixtral_full.md (bf16 Mixtral-like fc1, DRAM read + write)
-# NVFP4 Mixtral-like fc1: captured at T=2048, E=4 (the same 1024 rows per
-# expert), 374.1 MB; the traffic grows with the experts, so x2 for E=8
-# (profiles/fc1_grouped_gemm_mixtral_nvfp4.md)
-FC1_NV4_TRAFFIC_BYTES = 2 * 374.1e6
+HEADLINE = "dsv3_mxfp8"
+SUITE = ("tiny", "mixtral", "qwen3", "dsv3", HEADLINE)
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of a grouped GEMM,
+# from an ncu capture of the current kernel: (workload, op) -> (bytes, how taken).
+TRAFFIC = {}
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -85,11 +95,13 @@ def aggregate(tokens_per_rank: int, steps: int, world: int, max_total_ms: float)
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms.  A sample is 'under load' when the
+    board draws at least 1.5x the lowest power seen in the run."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -107,10 +119,6 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
-        t0 = time.time()
-        while not self.lines and time.time() - t0 < 5:
-            time.sleep(0.01)
-        self.lines.clear()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -125,22 +133,26 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]),
+                             {n for n, v in zip(self.REASONS, parts[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
+        p_min = min(r[2] for r in rows)
+        load = [r for r in rows if r[2] >= 1.5 * p_min] or rows
+        reasons = set()
+        for r in load:
+            reasons |= r[3]
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": sorted(reasons), "samples": len(rows),
+                "samples_under_load": len(load)}
 
 
 def read_peaks() -> tuple[dict, str]:
@@ -153,24 +165,29 @@ def read_peaks() -> tuple[dict, str]:
 
 
 # ---------------------------------------------------------------- oracle timing (CPU)
-class _F32Experts:
-    """Expert weights as fp32 numpy (exact bf16 values), per expert on demand."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class _HostExperts:
+    """Expert weights as fp64 numpy (exact bf16 values), filled for the experts
+    a sample needs before any timing, so the timed oracle call converts nothing."""
 
     def __init__(self, t: torch.Tensor):
         self.t = t
         self.shape = tuple(t.shape)
         self.c = {}
 
-    def __getitem__(self, e):
-        e = int(e)
+    def fill(self, e: int):
         if e not in self.c:
-            self.c[e] = self.t[e].to("cpu", torch.float32).numpy()
+            self.c[e] = self.t[e].to("cpu", torch.float32).numpy().astype(np.float64)
         return self.c[e]
 
-    def warm(self):
-        for e in range(self.shape[0]):
-            self[e]
-        return self
+    def __getitem__(self, e):
+        return self.c[int(e)] if int(e) in self.c else self.fill(int(e))
 
 
 def _oracle_fns(w):
@@ -182,368 +199,273 @@ def _oracle_fns(w):
     return O.moe_forward, O.moe_backward
 
 
-def oracle_step_timed(w, inp_cpu, tokens: np.ndarray) -> float:
-    """One step of the oracle (forward, plus backward for training workloads)
-    on the given tokens; returns seconds."""
-    fwd_fn, bwd_fn = _oracle_fns(w)
-    x = inp_cpu["x_np"][tokens]
-    sh = dict(w1_shared=inp_cpu["w1s_np"], w2_shared=inp_cpu["w2s_np"])
-    if w.dtype != "bf16":
-        sh["weight_cache"] = inp_cpu["wcache"]      # weights quantised once, as the recipe does
-    t0 = time.perf_counter()
-    fwd = fwd_fn(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], k=w.k, score=w.score, bias=inp_cpu["bias_np"],
-                 **sh)
-    if w.backward:
-        bwd_fn(x, inp_cpu["wr_np"], inp_cpu["w1"], inp_cpu["w2"], fwd, inp_cpu["dy_np"][tokens], score=w.score, **sh)
-    return time.perf_counter() - t0
-
-
 def oracle_inputs(w, dinp) -> dict:
     def npf(t):
         return None if t is None else t.to("cpu", torch.float32).numpy().astype(np.float64)
     return {"x_np": npf(dinp["x"]), "wr_np": npf(dinp["w_router"]), "bias_np": npf(dinp["bias"]),
             "w1s_np": npf(dinp["w1_shared"]), "w2s_np": npf(dinp["w2_shared"]), "dy_np": npf(dinp["dy"]),
-            "w1": _F32Experts(dinp["w1"]), "w2": _F32Experts(dinp["w2"]), "wcache": {}}
+            "w1": _HostExperts(dinp["w1"]), "w2": _HostExperts(dinp["w2"]), "wcache": {}}
 
 
-def warm_experts(w, inp, tokens):
-    """Copy to host (untimed) the experts the given tokens route to."""
+def sample_experts(w, inp, tokens) -> np.ndarray:
     from oracle import moe_oracle as O
     logits = O.router_logits(inp["x_np"][tokens], inp["wr_np"])
     idx, _ = O.route(logits, w.k, w.score, inp["bias_np"])
-    quantised = w.dtype == "mxfp8"
-    for e in np.unique(idx):
-        inp["w1"][e]
-        inp["w2"][e]
-        if w.dtype == "nvfp4":
+    return np.unique(idx)
+
+
+def warm_experts(w, inp, experts, threads: int | None = None):
+    """Untimed preparation of what the timed oracle call reads: fp64 host
+    copies of the given experts' weights, and for the quantised recipes the
+    weights quantised once (as the recipe does), in parallel threads."""
+    from oracle import moe_oracle as O
+    for e in experts:
+        inp["w1"].fill(int(e))
+        inp["w2"].fill(int(e))
+    jobs = []
+    if w.dtype == "mxfp8":
+        for e in experts:
+            for name in ("w1", "w2"):
+                for axis in (-1, 0):
+                    if (name, int(e), axis) not in inp["wcache"]:
+                        jobs.append((name, int(e), axis, inp[name][int(e)]))
+        if inp["w1s_np"] is not None:
+            for name, W in (("w1s", inp["w1s_np"]), ("w2s", inp["w2s_np"])):
+                for axis in (-1, 0):
+                    if (name, 0, axis) not in inp["wcache"]:
+                        jobs.append((name, 0, axis, W))
+
+        def run(j):
+            return (j[0], j[1], j[2]), O.mxfp8_roundtrip(j[3], j[2])
+
+        with cf.ThreadPoolExecutor(max_workers=threads or min(8, host_cores())) as ex:
+            inp["wcache"].update(dict(ex.map(run, jobs)))
+    elif w.dtype == "nvfp4":
+        for e in experts:
             O.nvfp4_weight(inp["wcache"], "w1", inp["w1"], int(e))
             O.nvfp4_weight(inp["wcache"], "w2", inp["w2"], int(e))
-        if quantised:
-            # the recipe quantises weights once; do it here, outside the timed oracle call
-            for name, W in (("w1", inp["w1"][e]), ("w2", inp["w2"][e])):
-                for axis in (-1, 0):
-                    key = (name, int(e), axis)
-                    if key not in inp["wcache"]:
-                        inp["wcache"][key] = O.mxfp8_roundtrip(W, axis)
-    if quantised and inp["w1s_np"] is not None:
-        for name, W in (("w1s", inp["w1s_np"]), ("w2s", inp["w2s_np"])):
-            for axis in (-1, 0):
-                inp["wcache"].setdefault((name, 0, axis), O.mxfp8_roundtrip(W, axis))
 
 
-def host_cores() -> int:
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
+def oracle_step_timed(w, inp, tokens: np.ndarray) -> float:
+    """One step of the oracle (forward, plus backward for training workloads)
+    on the given tokens, with everything it reads already on the host; seconds."""
+    fwd_fn, bwd_fn = _oracle_fns(w)
+    x = inp["x_np"][tokens]
+    sh = dict(w1_shared=inp["w1s_np"], w2_shared=inp["w2s_np"])
+    if w.dtype != "bf16":
+        sh["weight_cache"] = inp["wcache"]      # weights quantised once, as the recipe does
+    t0 = time.perf_counter()
+    fwd = fwd_fn(x, inp["wr_np"], inp["w1"], inp["w2"], k=w.k, score=w.score, bias=inp["bias_np"], **sh)
+    if w.backward:
+        bwd_fn(x, inp["wr_np"], inp["w1"], inp["w2"], fwd, inp["dy_np"][tokens], score=w.score, **sh)
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w, inp, target_s: float, max_experts: int) -> tuple[np.ndarray, float]:
+    """The first n tokens, n doubled from 1 while one oracle step stays under
+    target_s and the experts the sample reaches stay within max_experts (their
+    host copies and quantised weights are prepared untimed).  Returns the
+    tokens and the last step's seconds."""
+    n = 1
+    while True:
+        toks = np.arange(n)
+        warm_experts(w, inp, sample_experts(w, inp, toks))
+        t = oracle_step_timed(w, inp, toks)
+        nxt = min(w.T, 2 * n)
+        if t >= 0.5 * target_s or n >= w.T or len(sample_experts(w, inp, np.arange(nxt))) > max_experts:
+            return toks, t
+        n = nxt
+
+
+def _max_experts(w) -> int:
+    # bound the untimed preparation: host copies (and quantised copies) of the experts a sample reaches
+    per_expert = 3 * w.F * w.H * 8 * (3 if w.dtype == "mxfp8" else 1)
+    return max(w.k, min(w.E, int(24e9 // per_expert)))
 
 
 def cpu_baseline(w, dinp, target_s: float = 10.0) -> dict:
-    """The oracle, as it stands, on the first n tokens; n grows until one run
-    takes about target_s seconds (or covers all tokens)."""
+    """The oracle, as it stands, timed on a bounded sample of the workload's tokens."""
     inp = oracle_inputs(w, dinp)
-    n = 8
-    while True:
-        warm_experts(w, inp, np.arange(n))
-        t = oracle_step_timed(w, inp, np.arange(n))
-        if t >= 0.7 * target_s or n >= w.T:
-            break
-        n = min(w.T, max(n * 2, int(n * target_s / max(t, 1e-3))))
+    toks, _ = oracle_sample(w, inp, target_s, _max_experts(w))
+    t = oracle_step_timed(w, inp, toks)
     what = "forward + backward" if w.backward else "forward"
+    n = len(toks)
     return {"value": n / t, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"first {n} of {w.T} tokens, {what} (fp64 numpy), {t:.1f} s"}
+            "sample": f"first {n} of {w.T} tokens ({len(sample_experts(w, inp, toks))} experts reached), {what}, "
+                      f"fp64 numpy, {t:.2f} s; weights copied to the host and (quantised recipes) quantised "
+                      f"before timing"}
 
 
-# ---------------------------------------------------------------- our arm
-def run_ours(args) -> dict | None:
-    from moe_expert_layer_05_gb300 import api
+# ---------------------------------------------------------------- algorithmic work of each grouped GEMM
+GEMM_OPS = ("fc1", "fc2", "dgrad_fc2", "dgrad_fc1", "wgrad_fc1", "wgrad_fc2")
 
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA GPU (GB300); there is no CPU path")
-    torch.cuda.set_device(local)
-    dist_init(world, True)
-    dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
-    if args.tokens is not None:
-        w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
-    if args.experts is not None:
-        w = dataclasses.replace(w, E=args.experts, name=f"{w.name}_E{args.experts}")
-    dinp = make_inputs_on_device(w, dev, seed=rank)
-    cfg = api.config_of(w)
-    layer = api.MoELayer(cfg, dinp, with_backward=w.backward, device=dev)
-    x = dinp["x"]
-    y = torch.empty_like(x)
-    dy = dinp["dy"]
-    grads = None
-    if w.backward:
-        layer.forward(x, y)
-        _, _, grads = layer.backward(x, dy)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    def step():
-        layer.forward(x, y)
+def op_work(w, op: str, n_active: int) -> tuple[float, float]:
+    """(flops, algorithmic HBM bytes) of one routed grouped-GEMM launch: R = T*k
+    rows (padding not counted), n_active experts with rows read their weights
+    once, every expert's weight gradient is written (zero where empty)."""
+    R, H, F, E = w.T * w.k, w.H, w.F, w.E
+    # operand bytes per element: bf16 2; MXFP8 codes + an E8M0 scale per 32; NVFP4 half a byte + an E4M3 per 16
+    bw = ba = {"bf16": 2.0, "mxfp8": 1 + 1 / 32, "nvfp4": 0.5 + 1 / 16}[w.dtype]
+    z_saved = w.backward
+    if op == "fc1":
+        return 4.0 * R * H * F, n_active * 2 * F * H * bw + R * H * ba + R * F * 2 + (R * 2 * F * 2 if z_saved else 0)
+    if op == "fc2":
+        return 2.0 * R * H * F, n_active * H * F * bw + R * F * ba + R * H * 2
+    if op == "dgrad_fc2":
+        return 2.0 * R * H * F, n_active * H * F * bw + R * H * ba + R * 2 * F * 2 * 2
+    if op == "dgrad_fc1":
+        return 4.0 * R * H * F, n_active * 2 * F * H * bw + R * 2 * F * ba + R * H * 2
+    if op == "wgrad_fc1":
+        return 4.0 * R * H * F, E * 2 * F * H * 4 + R * 2 * F * ba + R * H * ba
+    if op == "wgrad_fc2":
+        return 2.0 * R * H * F, E * H * F * 4 + R * H * ba + R * F * ba
+    raise ValueError(op)
+
+
+def roofline_of(w, op, ms, n_active, peaks, peak_src) -> dict:
+    flop, nbytes = op_work(w, op, n_active)
+    p_tensor = float(peaks["bf16_tflops"]) * (2.0 if w.dtype == "mxfp8" else 6.0 if w.dtype == "nvfp4" else 1.0)
+    bw = float(peaks["hbm_gbs"])
+    t_tensor = flop / (p_tensor * 1e12) * 1e3
+    t_hbm = nbytes / (bw * 1e9) * 1e3
+    tensor = t_tensor >= t_hbm
+    tflops = flop / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    note = {"bf16": "bf16_tflops", "mxfp8": "2 x bf16_tflops (fp8:bf16 nominal ratio)",
+            "nvfp4": "6 x bf16_tflops (fp4:bf16 nominal ratio on GB300)"}[w.dtype]
+    return {"bound": "tensor" if tensor else "hbm",
+            "achieved": tflops if tensor else gbs, "peak": p_tensor if tensor else bw,
+            "unit": "TFLOP/s" if tensor else "GB/s", "frac": max(t_tensor, t_hbm) / ms,
+            "peak_source": (f"{note} of {peak_src} peaks (burst; kernel timed alone)" if tensor
+                            else f"hbm_gbs of {peak_src} peaks"),
+            "ms_per_launch": ms, "flop_per_launch": flop, "bytes_per_launch": nbytes,
+            "tflops": tflops, "gbs": gbs, "t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm,
+            "tensor_frac": t_tensor / ms, "hbm_frac": t_hbm / ms,
+            "traffic": TRAFFIC.get((w.name, op), (None, None))[0],
+            "traffic_note": TRAFFIC.get((w.name, op), (None, None))[1]}
+
+
+def _timed(fn, n, flush, stream) -> float:
+    s = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        s[i].record(stream)
+        fn()
+        e[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in zip(s, e))
+
+
+def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
+    """One closure per grouped GEMM of the step, on the layer's own saved
+    tensors; quantised operands (MXFP8) are made by the library's quantiser
+    into buffers owned here."""
+    cfg, fl, ws = layer.cfg, layer.fields(), layer.ws
+    po, cap, H, F, E = fl["poffsets"], layer.layout.cap, w.H, w.F, w.E
+    calls = {}
+    if w.dtype == "bf16":
+        calls["fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, fl["x_perm"], dinp["w1"], fl["h"], ws,
+                                                    c2=fl["z"] if w.backward else None, row_gate=fl["row_gate"],
+                                                    poffsets=po)
+        calls["fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, fl["h"], dinp["w2"], fl["o"], ws, poffsets=po)
         if w.backward:
-            layer.backward(x, dy, grads)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
-    # One step as a CUDA graph (the layer issues a fixed launch sequence and no
-    # host sync, so it captures whole); --no-graph launches it eagerly.
-    run = step
-    launches_per_step = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step()                      # warm the capture stream's first use
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
-        l0 = api.moe_kernel_launches()
-        with torch.cuda.graph(graph):
-            step()
-        launches_per_step = api.moe_kernel_launches() - l0
-        run = graph.replay
-        for _ in range(args.warmup):
-            run()
-        torch.cuda.synchronize()
-
-    # ---- timed region
-    K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    l0 = api.moe_kernel_launches()
-    for i in range(K):
-        flush.zero_()
-        starts[i].record(stream)
-        run()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    launches = api.moe_kernel_launches() - l0
-    if launches_per_step is not None:
-        launches = launches_per_step * K      # graph replays: the library's kernels, counted at capture
-    barrier(world)
-    clk = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    value = aggregate(w.T, K, world, total_ms)
-    assert api.moe_read_device_status(layer.ws) == 0, "device status not ok"
-
-    # ---- the dominant kernel (fc1 grouped GEMM) alone, same inputs, same stream
-    fl = layer.fields()
-    Kk = max(10, min(K, 200))
-    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
-    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kk)]
-    z = fl["z"] if w.backward else None
-    mx = w.dtype == "mxfp8"
-    nv = w.dtype == "nvfp4"
-    if nv:
+            dpart = layer.view("dgate_part", torch.float32, (cap, F // 128))
+            calls["dgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC2, fl["dy_perm"], dinp["w2"],
+                                                              fl["dz"], ws, aux=fl["z"], row_gate=fl["row_gate"],
+                                                              dgate_part=dpart, poffsets=po)
+            calls["dgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC1, fl["dz"], dinp["w1"],
+                                                              fl["dx_perm"], ws, poffsets=po)
+            calls["wgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, fl["dz"], fl["x_perm"],
+                                                              grads["dw1"], ws, poffsets=po)
+            calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, fl["dy_perm"], fl["h"],
+                                                              grads["dw2"], ws, poffsets=po)
+        return calls
+    if w.dtype == "nvfp4":
         # the NVFP4 layer permutes quantised codes and leaves x_perm unwritten:
-        # permute x (padding rows zeroed), then quantise it and W1 with the
-        # library's own quantiser into bench-owned buffers
-        cap = layer.layout.cap
-        api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"], fl["poffsets"],
-                        fl["slot_row"], fl["row_src"], fl["row_gate"], fl["x_perm"], 1, layer.ws)
-        xq = torch.empty(cap * w.H // 2, dtype=torch.uint8, device=dev)
-        xsf = torch.empty(cap * w.H // 16, dtype=torch.uint8, device=dev)
-        w1q = torch.empty(dinp["w1"].numel() // 2, dtype=torch.uint8, device=dev)
-        w1sf = torch.empty(dinp["w1"].numel() // 16, dtype=torch.uint8, device=dev)
-        amax = torch.empty(2, dtype=torch.float32, device=dev)
-        api.moe_quantize_nvfp4(fl["x_perm"], 1, cap, w.H, api.MX_ROWS, xq, xsf, amax[0:1])
-        api.moe_quantize_nvfp4(dinp["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP, w1q, w1sf, amax[1:2])
-        fc1_args = (xq, w1q, fl["h"], layer.ws)
-        fc1_kw = dict(c2=None, row_gate=fl["row_gate"], poffsets=fl["poffsets"], a_scales=xsf, b_scales=w1sf,
-                      a_amax=amax[0:1], b_amax=amax[1:2])
-    elif mx:
-        # operands quantised by the library's own quantiser into bench-owned buffers
-        cap = layer.layout.cap
-        xq = torch.empty(cap * w.H, dtype=torch.uint8, device=dev)
-        xsf = torch.empty(cap * w.H // 32, dtype=torch.uint8, device=dev)
-        w1q = torch.empty(dinp["w1"].numel(), dtype=torch.uint8, device=dev)
-        w1sf = torch.empty(dinp["w1"].numel() // 32, dtype=torch.uint8, device=dev)
-        api.moe_quantize_mxfp8(fl["x_perm"], 1, cap, w.H, api.MX_ROWS, xq, xsf)
-        api.moe_quantize_mxfp8(dinp["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP, w1q, w1sf)
-        fc1_args = (xq, w1q, fl["h"], layer.ws)
-        fc1_kw = dict(c2=z, row_gate=fl["row_gate"], poffsets=fl["poffsets"], a_scales=xsf, b_scales=w1sf)
-    else:
-        fc1_args = (fl["x_perm"], dinp["w1"], fl["h"], layer.ws)
-        fc1_kw = dict(c2=z, row_gate=fl["row_gate"], poffsets=fl["poffsets"])
-    for i in range(Kk):
-        flush.zero_()
-        s_ev[i].record(stream)
-        api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, *fc1_args, **fc1_kw)
-        e_ev[i].record(stream)
-    torch.cuda.synchronize()
-    fc1_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(s_ev, e_ev))
-    # the rest of the forward chain, one stage at a time (context for the line)
-    stages = {} if (mx or nv) else stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, Kk)
-    stages["fc1_grouped_gemm"] = fc1_ms
+        # permute x (padding rows zeroed), then quantise it, h and the weights
+        # with the library's own quantiser
+        api.moe_permute(cfg, dinp["x"], fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"], po,
+                        fl["slot_row"], fl["row_src"], fl["row_gate"], fl["x_perm"], 1, ws)
 
-    # ---- end to end: host buffers, copies inside the timed region.  Two sets
-    # of device inputs/outputs: step i's host->device copy (copy stream) and
-    # step i-1's device->host read (a second copy stream) overlap step i-1's /
-    # step i's compute, the way a user streams batches through the layer.
-    e2e_total, e2e_in, e2e_out = e2e_pipelined(api, w, layer, x, y, dy, grads, stream, K, args.no_graph, dev)
-    barrier(world)
-    e2e_total = max_over_ranks(e2e_total, world, dev)
+        def q4(t, batch, rows, cols, mode):
+            c = torch.empty(batch * rows * cols // 2, dtype=torch.uint8, device=dev)
+            sf = torch.empty(batch * rows * cols // 16, dtype=torch.uint8, device=dev)
+            a = torch.empty(1, dtype=torch.float32, device=dev)
+            api.moe_quantize_nvfp4(t, batch, rows, cols, mode, c, sf, a)
+            return c, sf, a
 
-    if rank != 0:
-        return None
-    peaks, peak_src = read_peaks()
-    R = w.T * w.k
-    fc1_flop = 4.0 * R * w.H * w.F
-    achieved = fc1_flop / (fc1_ms / 1e3) / 1e12
-    peak = float(peaks["bf16_tflops"])
-    peak_note = f"bf16_tflops of {peak_src} peaks (burst; kernel timed alone)"
-    if mx:
-        peak *= 2.0   # dense fp8 / bf16 nominal ratio (4.5 / 2.25 PFLOP/s)
-        peak_note = f"2 x bf16_tflops of {peak_src} peaks (fp8:bf16 nominal ratio; burst)"
-    if nv:
-        peak *= 6.0   # dense fp4 / bf16 nominal ratio on GB300 (13.5 / 2.25 PFLOP/s)
-        peak_note = f"6 x bf16_tflops of {peak_src} peaks (fp4:bf16 nominal ratio on GB300; burst)"
-    fwd_flop = 6.0 * R * w.H * w.F + 6.0 * w.T * w.H * w.S
-    step_flop = fwd_flop * (3 if w.backward else 1)
-    out = {
-        "metric": METRIC,
-        "value": value,
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": total_ms / K,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": w.dtype,
-        "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
-                   "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
-                   "l2": "flushed (512 MB write) before every timed step, outside the events",
-                   "parallelism": f"replicas x{world}",
-                   "cuda_graph": not args.no_graph},
-        "expert_gemm_tflops_per_gpu": step_flop / (total_ms / K / 1e3) / 1e12,
-        "roofline": {"bound": "tensor",
-                     "kernel": "fc1 grouped GEMM (tcgen05" + (" mxf8f6f4 block-scaled" if mx else "") +
-                               (" mxf4nvf4 block-scaled" if nv else "") +
-                               ", fused gated SwiGLU)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": peak_note,
-                     "traffic": (FC1_TRAFFIC_BYTES if w.name == "mixtral" else
-                                 FC1_NV4_TRAFFIC_BYTES if w.name == "mixtral_nvfp4" else None),
-                     "flop_per_launch": fc1_flop, "ms_per_launch": fc1_ms},
-        "stages_ms": stages,
-        "e2e": {"value": aggregate(w.T, K, world, e2e_total), "unit": "tokens/s",
-                "h2d_bytes_per_step": e2e_in, "d2h_bytes_per_step": e2e_out,
-                "how": "pinned host x (and dy) -> device and y -> pinned host every step on two copy "
-                       "streams, double-buffered so copies overlap the neighbouring steps' compute; "
-                       "no L2 flush (the expert weights exceed L2); first copy to last read back"},
-        "gpu_launches": int(launches),
-        "clocks": clk,
-    }
-    if not args.no_cpu_baseline and world == 1:
-        out["cpu_baseline"] = cpu_baseline(w, dinp)
-    return out
-
-
-PROFILE_OPS = ("fc1", "fc2", "dgrad_fc2", "dgrad_fc1", "wgrad_fc1", "wgrad_fc2")
-
-
-def profile_op_nvfp4(args, w, dev) -> dict:
-    """--profile-op for an NVFP4 workload: the NVFP4 forward once, then x_perm
-    (permuted, padding zeroed), h and the weights quantised by the library into
-    bench-owned buffers, and the chosen NVFP4 GEMM once inside the profiler range."""
-    from moe_expert_layer_05_gb300 import api
-    if args.profile_op not in ("fc1", "fc2"):
-        raise SystemExit("--profile-op: NVFP4 workloads have fc1 and fc2 only")
-    d = make_inputs_on_device(w, dev, seed=0, with_dy=False)
-    cfg = api.config_of(w)
-    layer = api.MoELayer(cfg, d, with_backward=False)
-    x = d["x"]
-    layer.forward(x)
-    fl, ws, cap = layer.fields(), layer.ws, layer.layout.cap
-    api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"], fl["poffsets"],
-                    fl["slot_row"], fl["row_src"], fl["row_gate"], fl["x_perm"], 1, ws)
+        (xq, xsf, xa), (w1q, w1sf, w1a) = q4(fl["x_perm"], 1, cap, H, api.MX_ROWS), \
+            q4(dinp["w1"], E, 2 * F, H, api.MX_ROWS_GATE_UP)
+        calls["fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, fl["h"], ws,
+                                                    row_gate=fl["row_gate"], poffsets=po, a_scales=xsf,
+                                                    b_scales=w1sf, a_amax=xa, b_amax=w1a)
+        (hq, hsf, ha), (w2q, w2sf, w2a) = q4(fl["h"], 1, cap, F, api.MX_ROWS), \
+            q4(dinp["w2"], 1, E * H, F, api.MX_ROWS)
+        calls["fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, hq, w2q, fl["o"], ws, poffsets=po,
+                                                    a_scales=hsf, b_scales=w2sf, a_amax=ha, b_amax=w2a)
+        return calls
+    if w.dtype != "mxfp8":
+        return calls
 
     def q(t, batch, rows, cols, mode):
-        c = torch.empty(t.numel() // 2, dtype=torch.uint8, device=dev)
-        sf = torch.empty(t.numel() // 16, dtype=torch.uint8, device=dev)
-        a = torch.empty(1, dtype=torch.float32, device=dev)
-        api.moe_quantize_nvfp4(t, batch, rows, cols, mode, c, sf, a)
-        return c, sf, a
+        c = torch.empty(batch * rows * cols, dtype=torch.uint8, device=dev)
+        sf = torch.empty(batch * rows * cols // 32, dtype=torch.uint8, device=dev)
+        api.moe_quantize_mxfp8(t, batch, rows, cols, mode, c, sf)
+        return c, sf
 
-    po = fl["poffsets"]
-    if args.profile_op == "fc1":
-        (aq, asf, aa), (bq, bsf, ba) = q(fl["x_perm"], 1, cap, w.H, api.MX_ROWS), \
-            q(d["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP)
-        call = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, aq, bq, fl["h"], ws, row_gate=fl["row_gate"],
-                                            poffsets=po, a_scales=asf, b_scales=bsf, a_amax=aa, b_amax=ba)
-    else:
-        (aq, asf, aa), (bq, bsf, ba) = q(fl["h"], 1, cap, w.F, api.MX_ROWS), q(d["w2"], 1, w.E * w.H, w.F, api.MX_ROWS)
-        call = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, aq, bq, fl["o"], ws, poffsets=po, a_scales=asf,
-                                            b_scales=bsf, a_amax=aa, b_amax=ba)
-    call()
-    torch.cuda.synchronize()
-    torch.cuda.profiler.start()
-    call()
-    torch.cuda.synchronize()
-    torch.cuda.profiler.stop()
-    return {"profile_op": args.profile_op, "workload": args.workload, "T": w.T, "E": w.E,
-            "status": api.moe_read_device_status(ws),
-            "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
+    xq, xsf = q(fl["x_perm"], 1, cap, H, api.MX_ROWS)
+    w1q, w1sf = q(dinp["w1"], E, 2 * F, H, api.MX_ROWS_GATE_UP)
+    calls["fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, fl["h"], ws,
+                                                c2=fl["z"] if w.backward else None, row_gate=fl["row_gate"],
+                                                poffsets=po, a_scales=xsf, b_scales=w1sf)
+    hq, hsf = q(fl["h"], 1, cap, F, api.MX_ROWS)
+    w2q, w2sf = q(dinp["w2"], 1, E * H, F, api.MX_ROWS)
+    calls["fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, hq, w2q, fl["o"], ws, poffsets=po, a_scales=hsf,
+                                                b_scales=w2sf)
+    if w.backward:
+        dpart = layer.view("dgate_part", torch.float32, (cap, F // 128))
+        dyq, dysf = q(fl["dy_perm"], 1, cap, H, api.MX_ROWS)
+        w2tq, w2tsf = q(dinp["w2"], E, H, F, api.MX_COLS_T)
+        calls["dgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC2, dyq, w2tq, fl["dz"], ws,
+                                                          aux=fl["z"], row_gate=fl["row_gate"], dgate_part=dpart,
+                                                          poffsets=po, a_scales=dysf, b_scales=w2tsf)
+        dzq, dzsf = q(fl["dz"], 1, cap, 2 * F, api.MX_ROWS)
+        w1tq, w1tsf = q(dinp["w1"], E, 2 * F, H, api.MX_COLS_T)
+        calls["dgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC1, dzq, w1tq, fl["dx_perm"], ws,
+                                                          poffsets=po, a_scales=dzsf, b_scales=w1tsf)
+        dzt, dztsf = q(fl["dz"], 1, cap, 2 * F, api.MX_COLS_T)
+        xt, xtsf = q(fl["x_perm"], 1, cap, H, api.MX_COLS_T)
+        calls["wgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, dzt, xt, grads["dw1"], ws,
+                                                          poffsets=po, a_scales=dztsf, b_scales=xtsf)
+        dyt, dytsf = q(fl["dy_perm"], 1, cap, H, api.MX_COLS_T)
+        ht, htsf = q(fl["h"], 1, cap, F, api.MX_COLS_T)
+        calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, dyt, ht, grads["dw2"], ws,
+                                                          poffsets=po, a_scales=dytsf, b_scales=htsf)
+    return calls
 
 
-def profile_op(args) -> dict:
-    """One untimed step of the workload, then one grouped GEMM of it between
-    cudaProfilerStart and cudaProfilerStop, for `ncu --profile-from-start off`
-    captures.  bf16 workloads (every op) and NVFP4 workloads (fc1, fc2)."""
-    from moe_expert_layer_05_gb300 import api
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    w = WORKLOADS[args.workload]
-    if args.tokens is not None:
-        w = dataclasses.replace(w, T=args.tokens)
-    if args.experts is not None:
-        w = dataclasses.replace(w, E=args.experts)
-    if w.dtype == "nvfp4":
-        return profile_op_nvfp4(args, w, dev)
-    if w.dtype != "bf16":
-        raise SystemExit("--profile-op: bf16 and NVFP4 workloads only")
-    bwd = args.profile_op not in ("fc1", "fc2")
-    d = make_inputs_on_device(w, dev, seed=0, with_dy=bwd)
-    layer = api.MoELayer(api.config_of(w), d, with_backward=True)
-    layer.forward(d["x"])
-    grads = layer.backward(d["x"], d["dy"])[2] if bwd else None
-    torch.cuda.synchronize()
-    fl, c, ws = layer.fields(), layer.cfg, layer.ws
-    po = fl["poffsets"]
-    calls = {
-        "fc1": lambda: api.moe_grouped_gemm(c, api.GG_FC1_SWIGLU, fl["x_perm"], d["w1"], fl["h"], ws, c2=fl["z"],
-                                            row_gate=fl["row_gate"], poffsets=po),
-        "fc2": lambda: api.moe_grouped_gemm(c, api.GG_FC2, fl["h"], d["w2"], fl["o"], ws, poffsets=po),
-        "dgrad_fc2": lambda: api.moe_grouped_gemm(c, api.GG_DGRAD_FC2, fl["dy_perm"], d["w2"], fl["dz"], ws,
-                                                  aux=fl["z"], row_gate=fl["row_gate"], poffsets=po),
-        "dgrad_fc1": lambda: api.moe_grouped_gemm(c, api.GG_DGRAD_FC1, fl["dz"], d["w1"], fl["dx_perm"], ws,
-                                                  poffsets=po),
-        "wgrad_fc1": lambda: api.moe_grouped_gemm(c, api.GG_WGRAD_FC1, fl["dz"], fl["x_perm"], grads["dw1"], ws,
-                                                  poffsets=po),
-        "wgrad_fc2": lambda: api.moe_grouped_gemm(c, api.GG_WGRAD_FC2, fl["dy_perm"], fl["h"], grads["dw2"], ws,
-                                                  poffsets=po),
-    }
-    torch.cuda.profiler.start()
-    calls[args.profile_op]()
-    torch.cuda.synchronize()
-    torch.cuda.profiler.stop()
-    return {"profile_op": args.profile_op, "workload": args.workload, "T": w.T, "E": w.E,
-            "status": api.moe_read_device_status(ws),
-            "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
+def stage_breakdown(api, w, layer, dinp, x, y, flush, stream, n) -> dict:
+    """The HBM-bound steps alone (CUDA events, L2 flushed), with their
+    algorithmic bytes: permute (1+k)*T*H*2, combine (k+1)*T*H*2 (+T*H*2 shared)."""
+    cfg, fl = layer.cfg, layer.fields()
+    T, H, k = w.T, w.H, w.k
+    shared = layer.view("os", torch.bfloat16, (T, H)) if w.S > 0 else None
+    out = {}
+    out["router_topk"] = _timed(lambda: api.moe_router_topk(cfg, x, dinp["w_router"], dinp["bias"], fl["logits"],
+                                                             fl["topk_idx"], fl["topk_gate"], layer.ws),
+                                n, flush, stream)
+    out["permute"] = _timed(lambda: api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"],
+                                                    fl["offsets"], fl["poffsets"], fl["slot_row"], fl["row_src"],
+                                                    fl["row_gate"], fl["x_perm"], int(w.backward), layer.ws),
+                            n, flush, stream)
+    out["combine"] = _timed(lambda: api.moe_unpermute(cfg, fl["o"], fl["slot_row"], shared, y), n, flush, stream)
+    pbytes = (1 + k) * T * H * 2
+    cbytes = (k + 1) * T * H * 2 + (T * H * 2 if w.S > 0 else 0)
+    out["permute_gbs"] = pbytes / (out["permute"] / 1e3) / 1e9
+    out["combine_gbs"] = cbytes / (out["combine"] / 1e3) / 1e9
+    return out
 
 
 def e2e_pipelined(api, w, layer, x, y, dy, grads, stream, K, no_graph, dev):
@@ -618,73 +540,322 @@ def e2e_pipelined(api, w, layer, x, y, dy, grads, stream, K, no_graph, dev):
     return start.elapsed_time(end), h2d, y.numel() * y.element_size()
 
 
-def stage_breakdown(api, cfg, layer, dinp, x, y, flush, stream, n) -> dict:
-    fl = layer.fields()
-    lay = layer.layout
-    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+# ---------------------------------------------------------------- our arm
+def bench_workload(args, w, world, rank, local, dev, cpu_target_s: float | None) -> dict | None:
+    from moe_expert_layer_05_gb300 import api
 
-    def timed(fn):
-        s = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for i in range(n):
-            flush.zero_()
-            s[i].record(stream)
-            fn()
-            e[i].record(stream)
+    dinp = make_inputs_on_device(w, dev, seed=rank)
+    cfg = api.config_of(w)
+    layer = api.MoELayer(cfg, dinp, with_backward=w.backward, device=dev)
+    x = dinp["x"]
+    y = torch.empty_like(x)
+    dy = dinp["dy"]
+    grads = None
+    clocks = ClockSampler(local)
+    clocks.start()
+    if w.backward:
+        layer.forward(x, y)
+        _, _, grads = layer.backward(x, dy)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.forward(x, y)
+        if w.backward:
+            layer.backward(x, dy, grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # One step as a CUDA graph (the layer issues a fixed launch sequence and no
+    # host sync, so it captures whole); --no-graph launches it eagerly.
+    run = step
+    launches_per_step = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()                      # warm the capture stream's first use
+        stream.wait_stream(side)
         torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in zip(s, e))
+        l0 = api.moe_kernel_launches()
+        with torch.cuda.graph(graph):
+            step()
+        launches_per_step = api.moe_kernel_launches() - l0
+        run = graph.replay
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
 
-    out = {}
-    out["router_topk"] = timed(lambda: api.moe_router_topk(cfg, x, dinp["w_router"], dinp["bias"], fl["logits"],
-                                                            fl["topk_idx"], fl["topk_gate"], layer.ws))
-    row_src = fl["row_src"]
-    out["permute"] = timed(lambda: api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"],
-                                                   fl["offsets"], fl["poffsets"], fl["slot_row"], row_src,
-                                                   fl["row_gate"], fl["x_perm"], 0, layer.ws))
-    out["fc2_grouped_gemm"] = timed(lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, fl["h"], dinp["w2"], fl["o"],
-                                                                 layer.ws, poffsets=fl["poffsets"]))
-    out["combine"] = timed(lambda: api.moe_unpermute(cfg, fl["o"], fl["slot_row"], None, y))
-    # algorithmic bytes of the two HBM-bound copies: (1+k)*T*H*2 each
-    nbytes = (1 + k) * T * H * 2
-    out["permute_gbs"] = nbytes / (out["permute"] / 1e3) / 1e9
-    out["combine_gbs"] = nbytes / (out["combine"] / 1e3) / 1e9
+    # ---- timed region
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = api.moe_kernel_launches()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        run()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = api.moe_kernel_launches() - l0
+    if launches_per_step is not None:
+        launches = launches_per_step * K      # graph replays: the library's kernels, counted at capture
+    barrier(world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = aggregate(w.T, K, world, total_ms)
+    assert api.moe_read_device_status(layer.ws) == 0, "device status not ok"
+
+    # ---- each grouped GEMM alone, same inputs, same stream
+    Kk = max(10, min(K, 200))
+    n_active = int((layer.fields()["counts"] > 0).sum())
+    calls = gemm_op_calls(api, w, layer, dinp, grads, dev)
+    op_ms = {op: _timed(fn, Kk, flush, stream) for op, fn in calls.items()}
+    del calls
+    stages = stage_breakdown(api, w, layer, dinp, x, y, flush, stream, Kk) if w.dtype != "nvfp4" else {}
+    assert api.moe_read_device_status(layer.ws) == 0, "device status not ok"
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    e2e_total, e2e_in, e2e_out = e2e_pipelined(api, w, layer, x, y, dy, grads, stream, K, args.no_graph, dev)
+    barrier(world)
+    e2e_total = max_over_ranks(e2e_total, world, dev)
+    clk = clocks.stop()
+
+    if rank != 0:
+        return None
+    peaks, peak_src = read_peaks()
+    R = w.T * w.k
+    fwd_flop = 6.0 * R * w.H * w.F + 6.0 * w.T * w.H * w.S
+    step_flop = fwd_flop * (3 if w.backward else 1)
+    ops = {op: roofline_of(w, op, ms, n_active, peaks, peak_src) for op, ms in op_ms.items()}
+    for r in ops.values():
+        if clk.get("sm_mhz"):
+            r["ms_x_sm_mhz"] = r["ms_per_launch"] * clk["sm_mhz"]
+    dominant = max(ops, key=lambda o: ops[o]["ms_per_launch"])
+    roof = dict(ops[dominant])
+    roof["kernel"] = f"{dominant} grouped GEMM (tcgen05" + \
+        (", mxf8f6f4 block-scaled" if w.dtype == "mxfp8" else "") + ")"
+    roof["why_this_kernel"] = "the longest grouped GEMM of the step, timed alone"
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
+                   "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
+                   "l2": "flushed (512 MB write) before every timed step, outside the events",
+                   "parallelism": f"replicas x{world}",
+                   "cuda_graph": not args.no_graph},
+        "expert_gemm_tflops_per_gpu": step_flop / (total_ms / K / 1e3) / 1e12,
+        "expert_gemm_frac_of_bf16_peak": step_flop / (total_ms / K / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
+        "roofline": roof,
+        "gemm_ops": ops,
+        "experts_with_rows": n_active,
+        "stages_ms": stages,
+        "e2e": {"value": aggregate(w.T, K, world, e2e_total), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e_in, "d2h_bytes_per_step": e2e_out,
+                "how": "pinned host x (and dy) -> device and y -> pinned host every step on two copy "
+                       "streams, double-buffered so copies overlap the neighbouring steps' compute; "
+                       "no L2 flush (the expert weights exceed L2); first copy to last read back"},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if cpu_target_s is not None and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w, dinp, cpu_target_s)
+    del layer, grads, dinp, flush
+    gc.collect()
+    torch.cuda.empty_cache()
     return out
+
+
+def run_ours(args) -> dict | None:
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (GB300); there is no CPU path")
+    torch.cuda.set_device(local)
+    dist_init(world, True)
+    dev = torch.device("cuda", local)
+    cpu = None if args.no_cpu_baseline else 10.0
+    if args.workload is not None:
+        w = WORKLOADS[args.workload]
+        if args.tokens is not None:
+            w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
+        if args.experts is not None:
+            w = dataclasses.replace(w, E=args.experts, name=f"{w.name}_E{args.experts}")
+        return bench_workload(args, w, world, rank, local, dev, cpu)
+    if world > 1:
+        return bench_workload(args, WORKLOADS[HEADLINE], world, rank, local, dev, cpu)
+    sub = {}
+    for name in SUITE[:-1]:
+        sub[name] = bench_workload(args, WORKLOADS[name], world, rank, local, dev, None if cpu is None else 5.0)
+    out = bench_workload(args, WORKLOADS[HEADLINE], world, rank, local, dev, cpu)
+    out["configs"] = sub
+    out["headline"] = ("the largest configuration: DeepSeek-V3-like layer, fwd+bwd, MXFP8 expert GEMMs, "
+                       "T=16384; the other four configurations are under 'configs'")
+    return out
+
+
+# ---------------------------------------------------------------- profiler captures
+PROFILE_OPS = GEMM_OPS + ("permute", "combine")
+
+
+def profile_op(args) -> dict:
+    """For `ncu --profile-from-start off` captures: set up once, then exactly one
+    launch of the chosen op between cudaProfilerStart and cudaProfilerStop.
+    permute / combine allocate only x, the routing and the expert-ordered rows
+    (and y); the grouped GEMMs run one untimed layer step first."""
+    from moe_expert_layer_05_gb300 import api
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.tokens is not None:
+        w = dataclasses.replace(w, T=args.tokens)
+    if args.experts is not None:
+        w = dataclasses.replace(w, E=args.experts)
+    cfg = api.config_of(w)
+    if args.profile_op in ("permute", "combine"):
+        d = make_router_inputs_on_device(w, dev, seed=0)
+        T, E, k, H = w.T, w.E, w.k, w.H
+        cap = api.moe_capacity_rows(cfg)
+        ws = torch.zeros(max(api.moe_workspace_bytes(cfg), 256), dtype=torch.uint8, device=dev)
+        api.moe_workspace_init(ws)
+        i32 = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+        idx, gate = i32(T, k), torch.empty((T, k), dtype=torch.float32, device=dev)
+        counts, offs, poffs, slot_row, row_src = i32(E), i32(E + 1), i32(E + 1), i32(T, k), i32(cap)
+        row_gate = torch.empty(cap, dtype=torch.float32, device=dev)
+        rows = torch.empty((cap, H), dtype=torch.bfloat16, device=dev)
+        bias = d["bias"] if w.score == "sigmoid" else None
+        api.moe_router_topk(cfg, d["x"], d["w_router"], bias, logits, idx, gate, ws)
+        perm = lambda: api.moe_permute(cfg, d["x"], idx, gate, counts, offs, poffs, slot_row, row_src, row_gate, rows,
+                                       0, ws)
+        perm()
+        y = torch.empty_like(d["x"])
+        call = perm if args.profile_op == "permute" else (lambda: api.moe_unpermute(cfg, rows, slot_row, None, y))
+        call()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        call()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        return {"profile_op": args.profile_op, "workload": w.name, "T": T, "E": E,
+                "algorithmic_bytes": (1 + k) * T * H * 2, "status": api.moe_read_device_status(ws),
+                "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
+    if w.dtype == "nvfp4":
+        return profile_op_nvfp4(args, w, dev)
+    bwd = args.profile_op not in ("fc1", "fc2") or w.backward
+    w = dataclasses.replace(w, backward=bwd)
+    d = make_inputs_on_device(w, dev, seed=0, with_dy=bwd)
+    layer = api.MoELayer(api.config_of(w), d, with_backward=bwd)
+    layer.forward(d["x"])
+    grads = layer.backward(d["x"], d["dy"])[2] if bwd else None
+    torch.cuda.synchronize()
+    call = gemm_op_calls(api, w, layer, d, grads, dev)[args.profile_op]
+    n_active = int((layer.fields()["counts"] > 0).sum())
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    flop, nbytes = op_work(w, args.profile_op, n_active)
+    return {"profile_op": args.profile_op, "workload": w.name, "T": w.T, "E": w.E, "experts_with_rows": n_active,
+            "flop": flop, "algorithmic_bytes": nbytes, "status": api.moe_read_device_status(layer.ws),
+            "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
+
+
+def profile_op_nvfp4(args, w, dev) -> dict:
+    """--profile-op for an NVFP4 workload: the NVFP4 forward once, then x_perm
+    (permuted, padding zeroed), h and the weights quantised by the library into
+    bench-owned buffers, and the chosen NVFP4 GEMM once inside the profiler range."""
+    from moe_expert_layer_05_gb300 import api
+    if args.profile_op not in ("fc1", "fc2"):
+        raise SystemExit("--profile-op: NVFP4 workloads have fc1 and fc2 only")
+    d = make_inputs_on_device(w, dev, seed=0, with_dy=False)
+    cfg = api.config_of(w)
+    layer = api.MoELayer(cfg, d, with_backward=False)
+    x = d["x"]
+    layer.forward(x)
+    fl, ws, cap = layer.fields(), layer.ws, layer.layout.cap
+    api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"], fl["poffsets"],
+                    fl["slot_row"], fl["row_src"], fl["row_gate"], fl["x_perm"], 1, ws)
+
+    def q(t, batch, rows, cols, mode):
+        c = torch.empty(t.numel() // 2, dtype=torch.uint8, device=dev)
+        sf = torch.empty(t.numel() // 16, dtype=torch.uint8, device=dev)
+        a = torch.empty(1, dtype=torch.float32, device=dev)
+        api.moe_quantize_nvfp4(t, batch, rows, cols, mode, c, sf, a)
+        return c, sf, a
+
+    po = fl["poffsets"]
+    if args.profile_op == "fc1":
+        (aq, asf, aa), (bq, bsf, ba) = q(fl["x_perm"], 1, cap, w.H, api.MX_ROWS), \
+            q(d["w1"], w.E, 2 * w.F, w.H, api.MX_ROWS_GATE_UP)
+        call = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, aq, bq, fl["h"], ws, row_gate=fl["row_gate"],
+                                            poffsets=po, a_scales=asf, b_scales=bsf, a_amax=aa, b_amax=ba)
+    else:
+        (aq, asf, aa), (bq, bsf, ba) = q(fl["h"], 1, cap, w.F, api.MX_ROWS), q(d["w2"], 1, w.E * w.H, w.F, api.MX_ROWS)
+        call = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, aq, bq, fl["o"], ws, poffsets=po, a_scales=asf,
+                                            b_scales=bsf, a_amax=aa, b_amax=ba)
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    return {"profile_op": args.profile_op, "workload": args.workload, "T": w.T, "E": w.E,
+            "status": api.moe_read_device_status(ws),
+            "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
 
 
 # ---------------------------------------------------------------- reference arm
 def run_reference(args) -> dict | None:
+    """The fp64 oracle on the host cores, on our arm's workload, metric and
+    unit: every step runs the same bounded sample of the workload's tokens,
+    with the weights it reads copied (and, for the quantised recipes,
+    quantised) once before the first step."""
     world, rank, local = dist_env()
     if rank != 0:
         return None
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload or HEADLINE]
     if torch.cuda.is_available():
         torch.cuda.set_device(local)
         dinp = make_inputs_on_device(w, torch.device("cuda", local), seed=0)
     else:
         dinp = make_inputs(w, seed=0)
     inp = oracle_inputs(w, dinp)
-    warm_experts(w, inp, np.arange(4))
-    # size the per-step sample so that W + K steps end within ~2 minutes
-    t1 = oracle_step_timed(w, inp, np.arange(4)) / 4
-    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(w.T, per_step_budget / max(t1, 1e-6))))
-    rng = np.random.default_rng(0)
-    samples = [np.sort(rng.choice(w.T, n, replace=False)) for _ in range(args.warmup + args.steps)]
-    warm_experts(w, inp, np.unique(np.concatenate(samples)))   # host copies of the weights, untimed
-    for smp in samples[:args.warmup]:
-        oracle_step_timed(w, inp, smp)
+    per_step = min(10.0, 100.0 / max(1, args.steps + args.warmup))
+    toks, _ = oracle_sample(w, inp, per_step, _max_experts(w))
+    for _ in range(args.warmup):
+        oracle_step_timed(w, inp, toks)
     total = 0.0
-    for smp in samples[args.warmup:]:
-        total += oracle_step_timed(w, inp, smp)
+    for _ in range(args.steps):
+        total += oracle_step_timed(w, inp, toks)
+    n = len(toks)
     value = n * args.steps / total
-    sample = (f"{n} random tokens of {w.T} per step (fp64 numpy oracle, "
-              f"{'forward + backward' if w.backward else 'forward'})")
+    sample = (f"first {n} of {w.T} tokens every step ({len(sample_experts(w, inp, toks))} experts reached), "
+              f"{'forward + backward' if w.backward else 'forward'}, fp64 numpy; weights copied to the host and "
+              f"(quantised recipes) quantised before the first step")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "F": w.F, "S": w.S,
-                   "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd"},
+                   "score": w.score, "pass": "fwd+bwd" if w.backward else "fwd",
+                   "l2": "flushed (512 MB write) before every timed step, outside the events",
+                   "parallelism": f"replicas x{world}", "cuda_graph": True},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -694,10 +865,11 @@ def run_reference(args) -> dict | None:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=None,
+                    help="one workload only (default: all five configurations, headline the largest)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each timed step eagerly, not as a CUDA graph")
     ap.add_argument("--tokens", type=int, default=None,
@@ -705,8 +877,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller cases for profiler captures; not a bench line)")
     ap.add_argument("--profile-op", choices=sorted(PROFILE_OPS), default=None,
-                    help="for profiler captures: one untimed step, then this grouped GEMM once inside "
-                         "cudaProfilerStart/Stop (ncu --profile-from-start off); prints one JSON line")
+                    help="for profiler captures: set up, then this op once inside cudaProfilerStart/Stop "
+                         "(ncu --profile-from-start off); prints one JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -165,6 +165,7 @@ moe_status moe_read_device_status(const void* ws, int32_t* code, void* stream);
  *   logits[t,e] = sum_h x[t,h] * w_router[e,h]  (bf16 in, fp32 accumulate, fp32 out)
  *   topk_idx[t,:] = the k experts with the largest key (key = logit for softmax,
  *   sigmoid(logit) + bias[e] for sigmoid), by key descending, lower id first on ties;
+ *   a NaN key ranks as -infinity (after every finite key);
  *   topk_gate[t,:] = the normalised gates of those experts (fp32, sum to 1).
  * x [T,H] bf16; w_router [E,H] bf16; bias [E] fp32 or NULL.
  * Outputs: logits [T,E] fp32, topk_idx [T,k] int32, topk_gate [T,k] fp32. */
@@ -205,8 +206,12 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
  * divides 256 (e.g. T*k up to 262144 pairs with
  * E = 256); larger shapes return MOE_ERR_WORKSPACE before any launch.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array: calls whose
+ * (cudaGetSymbolAddress, with that device current) and keeps it for that
+ * device's current context; make that first call before any stream capture.
+ * A call from another context on the same device (made with the driver API)
+ * looks the address up again.  Not supported: calling it again after a
+ * device reset (cudaDeviceReset) of a device it already ran on in this
+ * process, where a new context may reuse the old handle.  All calls share the one array: calls whose
  * work overlaps on the GPU (other streams, other threads) race and must be
  * ordered by the caller.  The array's old contents are never read.
  * Device-side errors are not recorded (there is no status word): a pair with

@@ -14,6 +14,7 @@
 // address is looked up once per device with cudaGetSymbolAddress (with that
 // device current) during the first call on that device, and passed to the
 // kernels as a plain pointer.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,19 +32,49 @@ static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-int32_t* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  CUcontext ctx = nullptr;     // context the address belongs to
+  int32_t* addr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of g_permute_scratch on the current device (set up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link-time libcuda).
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_permute_scratch in the current device's current context,
+// looked up with cudaGetSymbolAddress the first time this device (in this
+// context) calls, then reused.  A different current context on the same
+// device (one made with the driver API) gets its own lookup.
 int32_t* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CUcontext ctx = nullptr;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& s = g_scratch[dev];
+  if (s.addr == nullptr || ctx == nullptr || s.ctx != ctx) {
     void* p = nullptr;
+    // (binds the device's primary context if no context was current yet)
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    if (ctx == nullptr && (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)) return nullptr;
+    s.ctx = ctx;
+    s.addr = static_cast<int32_t*>(p);
   }
-  return g_scratch_addr[dev];
+  return s.addr;
 }
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

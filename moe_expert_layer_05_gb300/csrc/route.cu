@@ -29,6 +29,8 @@ struct Cand {
   int id;  // INT_MAX = none
 };
 
+// Keys are never NaN here (a NaN key is replaced by -inf before ranking), so
+// this is a strict total order: key descending, then expert id ascending.
 __device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
   if (a.id == INT_MAX) return false;
   if (b.id == INT_MAX) return true;
@@ -59,6 +61,7 @@ __device__ __forceinline__ void topk_one_token(const float* __restrict__ row, co
       key[j] = 1.0f / (1.0f + expf(-lg[j]));
       if (bias != nullptr && e < E) key[j] += bias[e];
     }
+    if (key[j] != key[j]) key[j] = -INFINITY;   // NaN ranks last: the order stays total
     if (e >= E) taken |= 1u << j;
   }
   float my_logit = 0.f;  // lane s keeps slot s
@@ -109,6 +112,7 @@ __device__ __forceinline__ void topk_one_token_thread(const float* __restrict__ 
       key[e] = 1.0f / (1.0f + expf(-lg[e]));
       if (bias != nullptr && e < E) key[e] += bias[e];
     }
+    if (key[e] != key[e]) key[e] = -INFINITY;   // as in topk_one_token
   }
   // slots unrolled to the bound and guarded by k, so every array stays in registers
   uint32_t taken = 0;

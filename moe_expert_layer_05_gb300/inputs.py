@@ -139,6 +139,22 @@ def make_inputs_on_device(w: Workload, device, seed: int = 0, with_dy: bool | No
     return out
 
 
+def make_router_inputs_on_device(w: Workload, device, seed: int = 0) -> dict:
+    """x, the router weight and (sigmoid workloads) the router bias of
+    make_inputs_on_device, without the expert weights: for runs that time the
+    routing and permutation alone."""
+    gen = torch.Generator(device=device)
+
+    def normal(slot, shape, std):
+        gen.manual_seed(seed * 64 + _SLOTS[slot])
+        t = torch.empty(shape, dtype=torch.float32, device=device)
+        t.normal_(0.0, std, generator=gen)
+        return t.to(torch.bfloat16)
+
+    return {"x": normal("x", (w.T, w.H), 1.0), "w_router": normal("w_router", (w.E, w.H), 0.02),
+            "bias": torch.from_numpy(zipf_router_bias(w.E, w.zipf_s)).to(device) if w.zipf_s > 0 else None}
+
+
 def random_topk_indices(T: int, E: int, k: int, seed: int = 0, skew: float = 0.0) -> np.ndarray:
     """Routing indices drawn directly (no router): k distinct experts per token.
 

@@ -307,7 +307,7 @@ def router_backward(logits, sel, gates, dgate, score):
 
 
 def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
-                 w1_shared=None, w2_shared=None, with_router=True):
+                 w1_shared=None, w2_shared=None, with_router=True, weight_grads=True):
     """Gradients of L = <dy, y> with the routing held fixed (top-k is piecewise
     constant), by the chain rule, in fp64.
 
@@ -317,6 +317,8 @@ def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
       dx_t += W1_e^T [da, db];  dW1_e += [da, db] x_t^T;  dW2_e += dy_t (g h)^T
     Router: dlogits = router_backward(...); dx_t += Wr^T dl_t; dWr += dl_t x_t^T.
     Shared expert: the same with g = 1 and no gate gradient.
+    weight_grads=False leaves out dW1, dW2, dWr and the shared expert's
+    weight gradients (for large layers evaluated on a few tokens).
     """
     x = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
@@ -327,8 +329,8 @@ def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
     gate = np.asarray(fwd["gates"], np.float64)
     k = idx.shape[1]
     dx = np.zeros_like(x)
-    dW1 = np.zeros((E, 2 * F, H))
-    dW2 = np.zeros((E, H, F))
+    dW1 = np.zeros((E, 2 * F, H)) if weight_grads else None
+    dW2 = np.zeros((E, H, F)) if weight_grads else None
     dgate = np.zeros((T, k))
     for e in range(E):
         tok, slot = np.nonzero(idx == e)
@@ -348,9 +350,12 @@ def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
         db = dh * silu(a)
         dz = np.concatenate([da, db], axis=1)
         np.add.at(dx, tok, dz @ W1)
-        dW1[e] = dz.T @ xe
-        dW2[e] = dye.T @ (g * h)
-    out = {"dx": dx, "dW1": dW1, "dW2": dW2, "dgate": dgate}
+        if weight_grads:
+            dW1[e] = dz.T @ xe
+            dW2[e] = dye.T @ (g * h)
+    out = {"dx": dx, "dgate": dgate}
+    if weight_grads:
+        out.update(dW1=dW1, dW2=dW2)
     if w1_shared is not None:
         W1 = np.asarray(w1_shared, np.float64)
         W2 = np.asarray(w2_shared, np.float64)
@@ -361,14 +366,16 @@ def moe_backward(x, w_router, w1, w2, fwd, dy, score=SOFTMAX,
         dh = dy @ W2
         dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
         dx += dz @ W1
-        out["dW1_shared"] = dz.T @ x
-        out["dW2_shared"] = dy.T @ h
+        if weight_grads:
+            out["dW1_shared"] = dz.T @ x
+            out["dW2_shared"] = dy.T @ h
     if with_router:
         logits = fwd["logits"] if fwd.get("logits") is not None else router_logits(x, w_router)
         dl = router_backward(logits, idx, gate, dgate, score)
         dx += dl @ np.asarray(w_router, np.float64)
         out["dlogits"] = dl
-        out["dWr"] = dl.T @ x
+        if weight_grads:
+            out["dWr"] = dl.T @ x
     out["dx"] = dx
     return out
 
@@ -629,10 +636,11 @@ def moe_forward_mx(x, w_router, w1, w2, k, score=SOFTMAX, bias=None, w1_shared=N
 
 
 def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None, w2_shared=None,
-                    quant=mxfp8_roundtrip, weight_cache=None):
+                    quant=mxfp8_roundtrip, weight_cache=None, weight_grads=True):
     """Gradients as the MXFP8 recipe computes them: the chain rule of the
     unquantised layer, with every expert-GEMM operand quantised along its
-    contraction axis (straight through the quantiser)."""
+    contraction axis (straight through the quantiser).  weight_grads=False
+    leaves out the weight gradients, as in moe_backward."""
     qw = _weight_quantiser(quant, weight_cache)
     x = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
@@ -643,8 +651,8 @@ def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None,
     gate = np.asarray(fwd["gates"], np.float64)
     k = idx.shape[1]
     dx = np.zeros_like(x)
-    dW1 = np.zeros((E, 2 * F, H))
-    dW2 = np.zeros((E, H, F))
+    dW1 = np.zeros((E, 2 * F, H)) if weight_grads else None
+    dW2 = np.zeros((E, H, F)) if weight_grads else None
     dgate = np.zeros((T, k))
     for e in range(E):
         tok, slot = np.nonzero(idx == e)          # ascending token: the expert's row order
@@ -663,9 +671,12 @@ def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None,
         dh = g * dhp
         dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
         np.add.at(dx, tok, quant(dz, -1) @ qw("w1", e, W1, 0))  # contraction over 2F
-        dW1[e] = _q_tokens(dz, quant).T @ _q_tokens(xe, quant)
-        dW2[e] = _q_tokens(dye, quant).T @ _q_tokens(g * h, quant)
-    out = {"dW1": dW1, "dW2": dW2, "dgate": dgate}
+        if weight_grads:
+            dW1[e] = _q_tokens(dz, quant).T @ _q_tokens(xe, quant)
+            dW2[e] = _q_tokens(dye, quant).T @ _q_tokens(g * h, quant)
+    out = {"dgate": dgate}
+    if weight_grads:
+        out.update(dW1=dW1, dW2=dW2)
     if w1_shared is not None:
         W1 = np.asarray(w1_shared, np.float64)
         W2 = np.asarray(w2_shared, np.float64)
@@ -676,13 +687,15 @@ def moe_backward_mx(x, w_router, w1, w2, fwd, dy, score=SOFTMAX, w1_shared=None,
         dh = quant(dy, -1) @ qw("w2s", 0, W2, 0)
         dz = np.concatenate([dh * b * silu_grad(a), dh * silu(a)], axis=1)
         dx += quant(dz, -1) @ qw("w1s", 0, W1, 0)
-        out["dW1_shared"] = _q_tokens(dz, quant).T @ _q_tokens(x, quant)
-        out["dW2_shared"] = _q_tokens(dy, quant).T @ _q_tokens(h, quant)
+        if weight_grads:
+            out["dW1_shared"] = _q_tokens(dz, quant).T @ _q_tokens(x, quant)
+            out["dW2_shared"] = _q_tokens(dy, quant).T @ _q_tokens(h, quant)
     logits = fwd["logits"] if fwd.get("logits") is not None else router_logits(x, w_router)
     dl = router_backward(logits, idx, gate, dgate, score)
     dx += dl @ np.asarray(w_router, np.float64)
     out["dlogits"] = dl
-    out["dWr"] = dl.T @ x
+    if weight_grads:
+        out["dWr"] = dl.T @ x
     out["dx"] = dx
     return out
 

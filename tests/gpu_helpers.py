@@ -1,8 +1,12 @@
 """Shared helpers of the GPU parity tests (comparison metrics, host copies)."""
 from __future__ import annotations
 
+import concurrent.futures as cf
+
 import numpy as np
 import torch
+
+from oracle import moe_oracle as O
 
 
 def f64(t) -> np.ndarray:
@@ -60,3 +64,67 @@ class LazyExperts:
         if e not in self._cache:
             self._cache[e] = f64(self.t[e])
         return self._cache[e]
+
+
+class StreamExperts:
+    """Per-expert view of a [E, ...] device tensor, copied to the host (fp32,
+    exact for bf16) on every access and never kept: for oracle runs over many
+    large experts."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, e):
+        return self.t[int(e)].to("cpu", torch.float32).numpy()
+
+
+def mx_weight_cache(w1: torch.Tensor, w2: torch.Tensor, experts, w1s=None, w2s=None, threads: int = 8) -> dict:
+    """The oracle's MX weight cache ((name, expert, axis) -> quantise-dequantise
+    of that weight along axis) for the given experts and the shared expert,
+    each entry made by the oracle's own quantiser; the entries are independent,
+    so they are made in parallel threads (numpy releases the GIL in its loops)."""
+    jobs = []
+    for e in sorted({int(e) for e in experts}):
+        for axis in (-1, 0):
+            jobs += [("w1", e, w1, axis), ("w2", e, w2, axis)]
+    if w1s is not None:
+        for axis in (-1, 0):
+            jobs += [("w1s", 0, w1s, axis), ("w2s", 0, w2s, axis)]
+
+    def run(job):
+        name, e, t, axis = job
+        src = t if name in ("w1s", "w2s") else t[e]
+        return (name, e, axis), O.mxfp8_roundtrip(f64(src), axis)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        return dict(ex.map(run, jobs))
+
+
+def check_full_permutation(w, fl, x, n_rows=4096, seed=0):
+    """The layer's permutation at its full T against the oracle's counting sort
+    run on the GPU's own routing: counts, offsets, padded offsets, slot_row,
+    row_src and row_gate bit for bit over every pair; x_perm bit for bit on a
+    seeded sample of rows (every padding row of the sample must be zero when
+    the layer trains)."""
+    idx = i64(fl["topk_idx"])
+    m = O.permutation_maps(idx, w.E, 128)
+    for name in ("counts", "offsets", "poffsets", "slot_row"):
+        np.testing.assert_array_equal(i64(fl[name]), m[name], err_msg=name)
+    used = int(m["poffsets"][-1])
+    np.testing.assert_array_equal(i64(fl["row_src"][:used]), m["row_src"])
+    valid = m["row_src"] >= 0
+    rg = fl["row_gate"][:used].view(torch.int32).cpu().numpy()
+    tg = fl["topk_gate"].view(torch.int32).cpu().numpy()
+    np.testing.assert_array_equal(rg[valid], tg[m["row_src"][valid], m["row_slot"][valid]])
+    assert np.all(rg[~valid] == 0)
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(used, size=min(n_rows, used), replace=False))
+    rows_t = torch.from_numpy(rows).to(x.device)
+    xp = fl["x_perm"][rows_t].view(torch.int16).cpu().numpy()
+    v = valid[rows]
+    src = torch.from_numpy(m["row_src"][rows][v]).to(x.device)
+    np.testing.assert_array_equal(xp[v], x[src].view(torch.int16).cpu().numpy())
+    return m
+
+

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import LazyExperts, f64, i64, rel_l2
+from gpu_helpers import LazyExperts, check_full_permutation, f64, i64, rel_l2
 from moe_expert_layer_05_gb300 import api
 from moe_expert_layer_05_gb300.inputs import WORKLOADS, Workload, make_inputs, make_inputs_on_device
 from oracle import moe_oracle as O
@@ -70,6 +70,22 @@ def check_e2e(got, ref, what):
     return r
 
 
+def check_dlogits(w, fl, dgate, bwd_dlogits, stable, tol):
+    """dlogits of the layer: against the oracle's router backward (end to end,
+    on the stable tokens), and as a step against the router-backward formula
+    applied to the GPU's own fp32 logits, gates and gate gradients."""
+    got = f64(fl["dlogits"])
+    r = rel_l2(got[stable], bwd_dlogits[stable])
+    assert r <= tol, f"dlogits rel-L2 {r:.3e}"
+    dg = f64(dgate)
+    step = O.router_backward(f64(fl["logits"]), i64(fl["topk_idx"]), f64(fl["topk_gate"]), dg, w.score)
+    # fp32 evaluation of the same formula: a few ulps of the row's gate gradients
+    row_scale = np.abs(dg).max(axis=1, keepdims=True) + np.abs(step).max(axis=1, keepdims=True)
+    assert np.all(np.abs(got - step) <= 1e-5 * np.abs(step) + 1e-6 * row_scale)
+    assert rel_l2(got, step) <= 1e-5
+    assert np.all(got[step == 0] == 0)           # only the chosen experts' logits get gradient
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 def test_layer_small(lib, name):
     w = SMALL[name]
@@ -88,6 +104,7 @@ def test_layer_small(lib, name):
     np.testing.assert_array_equal(i64(fl["topk_idx"])[stable], fwd["topk_idx"][stable])
     check_e2e(f64(y)[stable], fwd["y"][stable], f"{name} y")
     assert (~stable).sum() <= max(1, w.T // 100)
+    check_full_permutation(w, fl, dinp["x"])
     if not w.backward:
         return
     dy = dinp["dy"]
@@ -102,6 +119,7 @@ def test_layer_small(lib, name):
     assert r <= 1e-2, f"dx rel-L2 {r:.3e}"
     assert np.all(np.abs(f64(dx)[stable] - dxr) <= 2e-2 * max(1.0, np.abs(dxr).max()) + 2.0 ** -7 * np.abs(dxr))
     assert rel_l2(f64(dgate)[stable], bwd["dgate"][stable]) <= 1e-2
+    check_dlogits(w, layer.fields(), dgate, bwd["dlogits"], stable, 1e-2)
     touched = np.zeros(w.E, bool)
     touched[fwd["topk_idx"][~stable].ravel()] = True
     for gname, oname in (("dw1", "dW1"), ("dw2", "dW2"), ("dw_router", "dWr")):
@@ -181,12 +199,8 @@ def test_layer_full_size_forward_sampled(lib, name, n_sample):
     torch.cuda.synchronize()
     assert api.moe_read_device_status(layer.ws) == 0
     fl = layer.fields()
-    # properties that hold at any size
-    counts = i64(fl["counts"])
-    assert counts.sum() == w.T * w.k
-    slot = i64(fl["slot_row"])
-    src = i64(fl["row_src"])
-    assert np.all(src[slot] == np.arange(w.T)[:, None])
+    # the permutation at full T, bit for bit against the oracle's counting sort
+    check_full_permutation(w, fl, dinp["x"])
     fwd = _oracle_fwd(w, inp, tokens)
     stable = _stable_tokens(w, fwd["logits"], inp["bias"])
     np.testing.assert_array_equal(i64(fl["topk_idx"])[tokens][stable], fwd["topk_idx"][stable])
@@ -204,13 +218,16 @@ def test_layer_full_size_qwen3_fwd_bwd_sampled(lib):
     fwd = _oracle_fwd(w, inp, tokens)
     stable = _stable_tokens(w, fwd["logits"], None)
     check_e2e(f64(y[torch.from_numpy(tokens).to(DEV)])[stable], fwd["y"][stable], "qwen3 y")
-    bwd = O.moe_backward(f64(inp["x"])[tokens], f64(inp["w_router"]), inp["w1_np"], inp["w2_np"], fwd,
-                         f64(inp["dy"])[tokens], score=w.score)
-    got_dx = f64(dx[torch.from_numpy(tokens).to(DEV)])[stable]
-    assert rel_l2(got_dx, bwd["dx"][stable]) <= 1e-2
-    assert rel_l2(f64(dgate[torch.from_numpy(tokens).to(DEV)])[stable], bwd["dgate"][stable]) <= 1e-2
-    # one expert's weight gradients in full: all tokens routed to it
     fl = layer.fields()
+    check_full_permutation(w, fl, dinp["x"])
+    bwd = O.moe_backward(f64(inp["x"])[tokens], f64(inp["w_router"]), inp["w1_np"], inp["w2_np"], fwd,
+                         f64(inp["dy"])[tokens], score=w.score, weight_grads=False)
+    tok_t = torch.from_numpy(tokens).to(DEV)
+    got_dx = f64(dx[tok_t])[stable]
+    assert rel_l2(got_dx, bwd["dx"][stable]) <= 1e-2
+    assert rel_l2(f64(dgate[tok_t])[stable], bwd["dgate"][stable]) <= 1e-2
+    assert rel_l2(f64(fl["dlogits"][tok_t])[stable], bwd["dlogits"][stable]) <= 1e-2
+    # one expert's weight gradients in full: all tokens routed to it
     idx_gpu = i64(fl["topk_idx"])
     order = np.argsort(np.bincount(idx_gpu.ravel(), minlength=w.E))
     for e_star in [int(order[w.E // 2 + j]) for j in range(8)]:
@@ -276,14 +293,21 @@ def test_router_replay_reproduces_the_layer_permutation(lib):
     assert torch.equal(got["x_perm"][:used].view(torch.int16), fl["x_perm"][:used].view(torch.int16))
 
 
+@pytest.mark.parametrize("nan", [False, True])
 @pytest.mark.parametrize("E,k,score", [(8, 2, "softmax"), (16, 3, "sigmoid"), (16, 16, "softmax"), (32, 4, "softmax"),
                                        (64, 8, "sigmoid")])
-def test_fused_topk_matches_the_standalone_gating(lib, E, k, score):
+def test_fused_topk_matches_the_standalone_gating(lib, E, k, score, nan):
     """The layer's top-k (fused with the counting-sort histogram: one thread
     per token for E <= 16, one warp per token above) gives indices and gates
-    bit-identical to the standalone gating kernel on the same logits."""
+    bit-identical to the standalone gating kernel on the same logits.  With
+    nan: one expert's router row and two tokens are NaN, so NaN logits reach
+    both paths (a NaN key ranks last in both)."""
     w = Workload("topk", T=640, H=128, E=E, k=k, F=128, score=score, zipf_s=1.2 if score == "sigmoid" else 0.0)
     dinp = _to_dev(make_inputs(w, seed=9))
+    if nan:
+        dinp["w_router"][min(3, E - 1)] = float("nan")
+        dinp["x"][5] = float("nan")
+        dinp["x"][300] = float("nan")
     layer = _layer(w, dinp, False)
     layer.forward(dinp["x"])
     fl = layer.fields()
@@ -293,3 +317,16 @@ def test_fused_topk_matches_the_standalone_gating(lib, E, k, score):
     torch.cuda.synchronize()
     assert torch.equal(idx, fl["topk_idx"])
     assert torch.equal(gate.view(torch.int32), fl["topk_gate"].view(torch.int32))
+    if nan:
+        lg = fl["logits"].cpu().numpy()
+        bias = None if dinp["bias"] is None else dinp["bias"].cpu().numpy()
+        want = O.topk_select(O.selection_keys_f32(lg, score, bias), k)
+        got = i64(idx)
+        assert all(len(set(r)) == k for r in got)
+        np.testing.assert_array_equal(got[5], np.arange(k))
+        rows = np.ones(len(got), bool)
+        rows[[5, 300]] = False                     # every logit NaN: experts 0..k-1
+        if k < E:
+            assert not (got[rows] == min(3, E - 1)).any()     # the NaN expert is never chosen
+        if score == "softmax":
+            np.testing.assert_array_equal(got, want)

@@ -274,47 +274,100 @@ def test_mx_layer_against_mxfp8_oracle(lib, name):
             assert r <= 3e-2, (gname, r)
 
 
-def test_mx_full_size_sampled(lib):
+def _stable_expert_tokens(w, x64, wr64, bias64, idx_gpu, counts):
+    """A mid-sized expert all of whose tokens are routed away from near ties
+    (fp64 top-k key gaps >= 1e-5), with its tokens and their oracle routing."""
+    order = np.argsort(counts, kind="stable")
+    nz = order[counts[order] > 0]
+    for j in range(len(nz) // 2, len(nz)):
+        e = int(nz[j])
+        toks = np.nonzero((idx_gpu == e).any(1))[0]
+        logits = O.router_logits(x64[toks], wr64)
+        keys = O.selection_keys(logits, w.score, bias64)
+        if np.all(O.topk_gap(keys, w.k) >= 1e-5):
+            idx, gate = O.route(logits, w.k, w.score, bias64)
+            return e, toks, idx, gate
+    raise AssertionError("no expert with only stable tokens")
+
+
+def test_mx_full_size_training_sampled(lib):
     """The DeepSeek-like MXFP8 training layer at full size (T=16384, E=256,
-    shared expert), forward as the benchmark runs it: routing properties at any
-    size; for the expert with the most rows, seeded sample rows of z, h' and o
-    recomputed by the oracle (blocks of 32 are row-local, so sampled rows need
-    no other tokens); the shared expert's output rows likewise; the combine on
-    the sampled tokens."""
-    from gpu_helpers import i64
+    shared expert), forward and backward as the benchmark runs them:
+    * the permutation at full T bit for bit against the oracle's counting sort
+      on the GPU's routing;
+    * two sampled tokens end to end against the oracle alone (fp64 router,
+      every expert they reach and the shared expert quantised by the oracle):
+      y, dx, dgate and dlogits within rel-L2 3e-2;
+    * a mid-sized expert e, over all of its tokens, against the oracle
+      restricted to that expert (its gates given, as router replay does):
+      dW1[e] and dW2[e] in full, the gate gradients of its slots, and sampled
+      rows of z, h', o, dz and dx_perm from the oracle's own step functions;
+    * dWr[e] as the router weight-gradient step on the layer's own dlogits."""
+    from gpu_helpers import StreamExperts, check_full_permutation, i64, mx_weight_cache
     from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs_on_device
     w = WORKLOADS["dsv3_mxfp8"]
-    dinp = make_inputs_on_device(w, DEV, seed=0, with_dy=False)
+    dinp = make_inputs_on_device(w, DEV, seed=0)
     layer = api.MoELayer(api.config_of(w), dinp, with_backward=True)
     layer.act.fill_(0x7F)
     y = layer.forward(dinp["x"])
+    dx, dgate, grads = layer.backward(dinp["x"], dinp["dy"])
     torch.cuda.synchronize()
     assert api.moe_read_device_status(layer.ws) == 0
     fl = layer.fields()
-    counts, po = i64(fl["counts"]), i64(fl["poffsets"])
-    assert counts.sum() == w.T * w.k
-    slot = i64(fl["slot_row"])
-    src = i64(fl["row_src"])
-    assert np.all(src[slot] == np.arange(w.T)[:, None])
-    e = int(np.argmax(counts))
+    check_full_permutation(w, fl, dinp["x"])
+    counts, po, src = i64(fl["counts"]), i64(fl["poffsets"]), i64(fl["row_src"])
+    idx_gpu = i64(fl["topk_idx"])
+    x64, dy64 = f64(dinp["x"]), f64(dinp["dy"])
+    wr64, bias64 = f64(dinp["w_router"]), f64(dinp["bias"])
+    e, toks, idx_o, gate_o = _stable_expert_tokens(w, x64, wr64, bias64, idx_gpu, counts)
+    np.testing.assert_array_equal(idx_o, idx_gpu[toks])
     rng = np.random.default_rng(13)
-    rows = np.sort(po[e] + rng.choice(counts[e], size=6, replace=False))
-    toks = src[rows]
-    rows_t, toks_t = torch.from_numpy(rows).to(DEV), torch.from_numpy(toks).to(DEV)
-    F = w.F
-    z = deq(dinp["x"][toks_t], -1) @ deq(dinp["w1"][e], -1).T
-    assert_bf16_close(f64(fl["z"][rows_t]), z, "z (mxfp8, full size)")
-    g = f64(fl["row_gate"][rows_t])
-    assert_bf16_close(f64(fl["h"][rows_t]), g[:, None] * O.silu(z[:, :F]) * z[:, F:], "h (mxfp8, full size)")
-    o_ref = deq(fl["h"][rows_t], -1) @ deq(dinp["w2"][e], -1).T
-    assert_bf16_close(f64(fl["o"][rows_t]), o_ref, "o (mxfp8, full size)")
-    # shared expert on the sampled tokens: os = q(hs) q(W2s)^T, hs = silu(a) b of q(x) q(W1s)^T
-    S = w.S
-    zs = deq(dinp["x"][toks_t], -1) @ deq(dinp["w1_shared"], -1).T
-    hs = layer.view("hs", torch.bfloat16, (w.T, S))[toks_t]
-    assert_bf16_close(f64(hs), O.silu(zs[:, :S]) * zs[:, S:], "hs (mxfp8, full size)")
-    os_ = layer.view("os", torch.bfloat16, (w.T, w.H))[toks_t]
-    assert_bf16_close(f64(os_), deq(hs, -1) @ deq(dinp["w2_shared"], -1).T, "os (mxfp8, full size)")
-    # combine: y[t] = bf16(sum of the token's k expert rows + shared row)
-    o_rows = f64(fl["o"][torch.from_numpy(slot[toks].ravel()).to(DEV)]).reshape(len(toks), w.k, w.H)
-    assert_bf16_close(f64(y[toks_t]), o_rows.sum(1) + f64(os_), "y (mxfp8 combine, full size)")
+    sample = np.sort(rng.choice(len(toks), size=2, replace=False))
+    ts = toks[sample]
+    cache = mx_weight_cache(dinp["w1"], dinp["w2"], np.unique(idx_o[sample]), dinp["w1_shared"], dinp["w2_shared"])
+
+    # two tokens end to end, the oracle alone
+    W1, W2 = StreamExperts(dinp["w1"]), StreamExperts(dinp["w2"])
+    sh = dict(w1_shared=f64(dinp["w1_shared"]), w2_shared=f64(dinp["w2_shared"]), weight_cache=cache)
+    fwd = O.moe_forward_mx(x64[ts], wr64, W1, W2, k=w.k, score=w.score, bias=bias64, **sh)
+    np.testing.assert_array_equal(fwd["topk_idx"], idx_gpu[ts])
+    bwd = O.moe_backward_mx(x64[ts], wr64, W1, W2, fwd, dy64[ts], score=w.score, weight_grads=False, **sh)
+    ts_t = torch.from_numpy(ts).to(DEV)
+    for what, got, ref in (("y", y[ts_t], fwd["y"]), ("dx", dx[ts_t], bwd["dx"]), ("dgate", dgate[ts_t], bwd["dgate"]),
+                           ("dlogits", fl["dlogits"][ts_t], bwd["dlogits"])):
+        r = rel_l2(f64(got), ref)
+        assert r <= 3e-2, (what, r)
+
+    # expert e over all of its tokens, the oracle restricted to it
+    n = len(toks)
+    slot_o = np.argmax(idx_o == e, axis=1)
+    g_e = gate_o[np.arange(n), slot_o]
+    ce = {("w1", 0, a): cache[("w1", e, a)] for a in (-1, 0) if ("w1", e, a) in cache}
+    ce.update({("w2", 0, a): cache[("w2", e, a)] for a in (-1, 0) if ("w2", e, a) in cache})
+    w1e, w2e = f64(dinp["w1"][e])[None], f64(dinp["w2"][e])[None]
+    fwd_e = O.moe_forward_mx(x64[toks], wr64[e:e + 1], w1e, w2e, k=1, score=w.score,
+                             routing=(np.zeros((n, 1), np.int64), g_e[:, None]), weight_cache=ce)
+    bwd_e = O.moe_backward_mx(x64[toks], wr64[e:e + 1], w1e, w2e, fwd_e, dy64[toks], score=w.score, weight_cache=ce)
+    for what, got, ref in (("dW1[e]", grads["dw1"][e], bwd_e["dW1"][0]), ("dW2[e]", grads["dw2"][e], bwd_e["dW2"][0])):
+        r = rel_l2(f64(got), ref)
+        assert r <= 3e-2, (what, r)
+    slot_g = np.argmax(idx_gpu[toks] == e, axis=1)
+    r = rel_l2(f64(dgate)[toks, slot_g], bwd_e["dgate"][:, 0])
+    assert r <= 3e-2, ("dgate of expert e", r)
+    # sampled rows of expert e: z, h', o, dz, dx_perm by the oracle's step functions
+    rows = np.sort(po[e] + rng.choice(counts[e], size=8, replace=False))
+    rt = src[rows]
+    assert np.all(np.isin(rt, toks))
+    g_rows = g_e[np.searchsorted(toks, rt)]
+    seg = np.array([0, len(rows)])
+    z, hp = O.expert_fc1(O.mxfp8_roundtrip(x64[rt], -1), ce[("w1", 0, -1)][None], seg, g_rows)
+    o = O.expert_fc2(O.mxfp8_roundtrip(hp, -1), ce[("w2", 0, -1)][None], seg)
+    dz, _ = O.expert_dgrad_fc2(O.mxfp8_roundtrip(dy64[rt], -1), ce[("w2", 0, 0)][None], z, seg, g_rows)
+    dxp = O.expert_dgrad_fc1(O.mxfp8_roundtrip(dz, -1), ce[("w1", 0, 0)][None], seg)
+    rows_t = torch.from_numpy(rows).to(DEV)
+    for what, name, ref in (("z", "z", z), ("h'", "h", hp), ("o", "o", o), ("dz", "dz", dz), ("dx_perm", "dx_perm", dxp)):
+        r = rel_l2(f64(fl[name][rows_t]), ref)
+        assert r <= 3e-2, (what, r)
+    # dWr[e] = sum over the tokens of e of dlogits[t, e] x[t] (the step, on the layer's dlogits)
+    ref = f64(fl["dlogits"])[:, e] @ x64
+    assert rel_l2(f64(grads["dw_router"][e]), ref) <= 1e-4

@@ -89,6 +89,40 @@ def test_topk_gating(lib, score, T, E, k, grid):
     np.testing.assert_allclose(f64(gate).sum(1), 1.0, atol=2e-6)
 
 
+@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("T,E,k", [(96, 8, 2), (96, 64, 8), (40, 16, 16)])
+def test_topk_nan_logits_rank_last(lib, score, T, E, k):
+    """A NaN key ranks after every finite key (ties among them by lower id),
+    as numpy's sort orders NaN: the order stays total, so every lane of the
+    warp agrees and no expert is picked twice."""
+    lg = _rand((T, E), T + E, 1.0)
+    rng = np.random.default_rng(E + k)
+    lg[rng.random((T, E)) < 0.2] = np.nan
+    lg[7] = np.nan                              # a token with no finite logit
+    bias = (_rand((E,), 6, 0.05) if score == "sigmoid" else None)
+    cfg = api.make_config(T, 128, E, k, 128, score=score)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    api.moe_topk_gating(cfg, torch.from_numpy(lg).to(DEV),
+                        None if bias is None else torch.from_numpy(bias).to(DEV), idx, gate)
+    torch.cuda.synchronize()
+    got = i64(idx)
+    want = O.topk_select(O.selection_keys_f32(lg, score, bias), k)
+    for t in range(T):
+        assert len(set(got[t])) == k, t
+    if score == "softmax":
+        np.testing.assert_array_equal(got, want)
+    else:
+        keys32 = O.selection_keys_f32(lg, score, bias).astype(np.float64)
+        fin = np.where(np.isnan(keys32), -np.inf, keys32)
+        ok = O.topk_gap(np.nan_to_num(fin, neginf=-1e30), k) > 1e-6
+        np.testing.assert_array_equal(got[ok], want[ok])
+    np.testing.assert_array_equal(got[7], np.arange(k))
+    finite_rows = np.isfinite(np.take_along_axis(lg, got, axis=1)).all(1)
+    g_ref = O.gates_from_logits(lg.astype(np.float64), got, score)
+    np.testing.assert_allclose(f64(gate)[finite_rows], g_ref[finite_rows], rtol=2e-6, atol=2e-7)
+
+
 # ------------------------------------------------------------------ permutation
 PERM_CASES = [
     # T, E, k, skew, H

@@ -175,3 +175,18 @@ def test_mx_recipe_equals_block_scaled_gemms_on_contraction_axes(score):
     # and the quantisation is not a no-op here: the unquantised layer is several percent away
     plain = O.moe_forward(x, wr, w1, w2, k=k, score=score, **kw)
     assert np.linalg.norm(plain["y"] - y) > 1e-3 * np.linalg.norm(y)
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_backward_without_weight_grads_changes_nothing_else(mx):
+    """weight_grads=False only leaves outputs out: dx, dgate and dlogits are
+    bit-identical to the full backward's."""
+    x, wr, w1, w2, w1s, w2s, dy = _case(5, S=64)
+    kw = dict(w1_shared=w1s, w2_shared=w2s)
+    fwd_fn, bwd_fn = (O.moe_forward_mx, O.moe_backward_mx) if mx else (O.moe_forward, O.moe_backward)
+    fwd = fwd_fn(x, wr, w1, w2, k=2, score=O.SIGMOID, **kw)
+    full = bwd_fn(x, wr, w1, w2, fwd, dy, score=O.SIGMOID, **kw)
+    part = bwd_fn(x, wr, w1, w2, fwd, dy, score=O.SIGMOID, weight_grads=False, **kw)
+    for n in ("dx", "dgate", "dlogits"):
+        np.testing.assert_array_equal(part[n], full[n])
+    assert not {"dW1", "dW2", "dWr", "dW1_shared", "dW2_shared"} & set(part)
