@@ -57,9 +57,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FLUSH_BYTES = 512 << 20
 HEADLINE = "dsv3_mxfp8"
 SUITE = ("tiny", "mixtral", "qwen3", "dsv3", HEADLINE)
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of a grouped GEMM,
-# from an ncu capture of the current kernel: (workload, op) -> (bytes, how taken).
-TRAFFIC = {}
+# DRAM traffic of one launch of a grouped GEMM (dram__bytes_read.sum +
+# dram__bytes_write.sum, one ncu pass) over its algorithmic bytes, captured on
+# a case with the workload's rows per expert and fewer experts, so the ratio
+# carries to the full launch (traffic grows with the experts):
+# (workload, op) -> (ratio, capture).
+_CAP_MX = "ncu 2026-12-03, T=4096 E=64 (512 rows per expert, as at full size)"
+TRAFFIC = {
+    ("dsv3_mxfp8", "fc1"): (1.0806, _CAP_MX),
+    ("dsv3_mxfp8", "fc2"): (1.0332, _CAP_MX),
+    ("dsv3_mxfp8", "dgrad_fc2"): (1.0577, _CAP_MX),
+    ("dsv3_mxfp8", "dgrad_fc1"): (1.0268, _CAP_MX),
+    ("dsv3_mxfp8", "wgrad_fc1"): (1.0046, _CAP_MX),
+    ("dsv3_mxfp8", "wgrad_fc2"): (0.9958, _CAP_MX),
+    ("qwen3", "wgrad_fc1"): (0.9829, "ncu 2026-12-03, T=2048 E=32 (512 rows per expert, as at full size)"),
+    ("dsv3", "fc1"): (1.0633, "ncu 2026-12-03, T=2048 E=64 (256 rows per expert, as at full size)"),
+    ("mixtral", "fc1"): (1.0679, "ncu 2026-12-03, T=2048 E=4 (1024 rows per expert, as at full size)"),
+}
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -342,8 +356,10 @@ def roofline_of(w, op, ms, n_active, peaks, peak_src) -> dict:
             "ms_per_launch": ms, "flop_per_launch": flop, "bytes_per_launch": nbytes,
             "tflops": tflops, "gbs": gbs, "t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm,
             "tensor_frac": t_tensor / ms, "hbm_frac": t_hbm / ms,
-            "traffic": TRAFFIC.get((w.name, op), (None, None))[0],
-            "traffic_note": TRAFFIC.get((w.name, op), (None, None))[1]}
+            "traffic": (TRAFFIC[(w.name, op)][0] * nbytes) if (w.name, op) in TRAFFIC else None,
+            "traffic_note": (f"measured DRAM bytes / algorithmic bytes = {TRAFFIC[(w.name, op)][0]:.4f} "
+                             f"({TRAFFIC[(w.name, op)][1]}) x this launch's algorithmic bytes"
+                             if (w.name, op) in TRAFFIC else None)}
 
 
 def _timed(fn, n, flush, stream) -> float:
@@ -727,6 +743,7 @@ def profile_op(args) -> dict:
         w = dataclasses.replace(w, E=args.experts)
     cfg = api.config_of(w)
     if args.profile_op in ("permute", "combine"):
+        cfg = api.make_config(w.T, w.H, w.E, w.k, w.F, 0, w.score, "bf16")   # the routing and row copies only
         d = make_router_inputs_on_device(w, dev, seed=0)
         T, E, k, H = w.T, w.E, w.k, w.H
         cap = api.moe_capacity_rows(cfg)
