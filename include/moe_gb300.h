@@ -148,8 +148,8 @@ moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, m
  * workspace must not overlap on the GPU (issue them on one stream). */
 size_t moe_workspace_bytes(const moe_config* cfg);
 
-/* Clear the device status word and the tile counter of `ws` (its first 256
- * bytes).  Stream-ordered, does not block. */
+/* Zero the whole workspace (the device status word, the GEMM tile counter,
+ * the fused combine's counters).  Stream-ordered, does not block. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, then copy the device status word to *code
@@ -242,7 +242,21 @@ typedef enum {
    * a = x [T,H] in token order, a_rows = row_src [cap] (token of each padded
    * row, -1 for padding: a zero row); A row r is x[a_rows[r]].  b, c, c2,
    * row_gate, poffsets as FC1_SWIGLU.  x_perm is neither read nor written. */
-  MOE_GG_FC1_SWIGLU_GATHERED = 6
+  MOE_GG_FC1_SWIGLU_GATHERED = 6,
+  /* FC2 with the combine fused into its epilogue (bf16 or MXFP8, routed only,
+   * H % 256 == 0): c = o [cap,H] as FC2, and c2 = y [T,H] with
+   * y[t] = sum_i o[slot_row[t,i]] (+ aux[t]) summed in slot order in fp32 and
+   * rounded once -- the same bits as moe_unpermute.  a_rows = row_src [cap],
+   * slot_row [T,k] (rows -1 are skipped), aux = the shared expert's output
+   * [T,H] or NULL.  Once a tile's rows of o are stored it counts them per
+   * (token, 256 columns) in the workspace; the tile that completes a token's
+   * slots sums them, so the order never depends on timing.  The counters must
+   * be zero before the call (moe_workspace_init) and are zero after it; after
+   * a device error (status word set) call moe_workspace_init again.  A token
+   * none of whose slots is valid gets no y row.  Technical summary 2.2 of the
+   * Megatron Core MoE summary (memory-efficient permutation: the combine is an
+   * unweighted sum because the gate was applied before the activation). */
+  MOE_GG_FC2_COMBINE = 7
 } moe_gg_op;
 
 /* Arguments of one grouped GEMM.  `poffsets` [E+1] (device) gives each expert's
@@ -284,7 +298,8 @@ typedef struct {
   const void* b_scales;   /* MXFP8 / NVFP4 only */
   const float* a_amax;    /* NVFP4 only */
   const float* b_amax;    /* NVFP4 only */
-  const int32_t* a_rows;  /* FC1_SWIGLU_GATHERED only */
+  const int32_t* a_rows;  /* FC1_SWIGLU_GATHERED, FC2_COMBINE */
+  const int32_t* slot_row;/* FC2_COMBINE only */
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For

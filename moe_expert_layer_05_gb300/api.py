@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA er
 SCORE = {"softmax": 0, "sigmoid": 1}
 GEMM_DTYPE = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
 
-GG_FC1_SWIGLU, GG_FC2, GG_DGRAD_FC2, GG_DGRAD_FC1, GG_WGRAD_FC1, GG_WGRAD_FC2, GG_FC1_SWIGLU_GATHERED = range(7)
+(GG_FC1_SWIGLU, GG_FC2, GG_DGRAD_FC2, GG_DGRAD_FC1, GG_WGRAD_FC1, GG_WGRAD_FC2, GG_FC1_SWIGLU_GATHERED,
+ GG_FC2_COMBINE) = range(8)
 MX_ROWS, MX_COLS_T, MX_ROWS_GATE_UP = range(3)
 
 c_i32 = ctypes.c_int32
@@ -53,7 +54,8 @@ class MoeActLayout(ctypes.Structure):
 class MoeGemmArgs(ctypes.Structure):
     _fields_ = [("op", c_i32), ("dense_rows", c_i32), ("a", c_vp), ("b", c_vp), ("c", c_vp), ("c2", c_vp),
                 ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp),
-                ("a_scales", c_vp), ("b_scales", c_vp), ("a_amax", c_vp), ("b_amax", c_vp), ("a_rows", c_vp)]
+                ("a_scales", c_vp), ("b_scales", c_vp), ("a_amax", c_vp), ("b_amax", c_vp), ("a_rows", c_vp),
+                ("slot_row", c_vp)]
 
 
 _P = ctypes.POINTER
@@ -205,9 +207,10 @@ def moe_permute_noalloc(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, 
 
 def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
                      dense_rows=0, a_scales=None, b_scales=None, a_amax=None, b_amax=None, a_rows=None,
-                     stream=None) -> None:
+                     slot_row=None, stream=None) -> None:
     args = MoeGemmArgs(op, dense_rows, ptr(a), ptr(b), ptr(c), ptr(c2), ptr(aux), ptr(row_gate), ptr(dgate_part),
-                       ptr(poffsets), ptr(a_scales), ptr(b_scales), ptr(a_amax), ptr(b_amax), ptr(a_rows))
+                       ptr(poffsets), ptr(a_scales), ptr(b_scales), ptr(a_amax), ptr(b_amax), ptr(a_rows),
+                       ptr(slot_row))
     check(load().moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), ptr(ws), stream_ptr(stream)),
           "moe_grouped_gemm")
 

@@ -57,6 +57,14 @@ using namespace moe;
 namespace {
 
 constexpr size_t kAlign = 256;
+// Whether the layer forward fuses the combine into fc2 (where H % 256 == 0).
+// Off: measured on GB300 the fused epilogue costs fc2 more than the separate
+// combine kernel takes (DeepSeek-like: 2.17 ms against 1.86 + 0.19 ms), since
+// that kernel already streams at the HBM rate.  MOE_GG_FC2_COMBINE offers it.
+#ifndef MOE_FUSE_COMBINE
+#define MOE_FUSE_COMBINE 0
+#endif
+constexpr bool kFuseCombine = MOE_FUSE_COMBINE != 0;
 constexpr size_t kStatusBytes = 256;   // status word region at the start of the workspace
 constexpr size_t kNone = SIZE_MAX;
 
@@ -291,6 +299,29 @@ Nv4W nv4_weight_layout(const moe_config* c) {
   return m;
 }
 
+// Counters of the combine fused into fc2 (one int per token and 256-column
+// tile of y), after the quantised activations; zero between launches.
+size_t combine_count_bytes(const moe_config* c) {
+  return c->H % 256 == 0 ? static_cast<size_t>(c->T) * (c->H / 256) * sizeof(int32_t) : 0;
+}
+size_t combine_count_offset(const moe_config* c) {
+  size_t b = kStatusBytes + align_up(hist_bytes(c));
+  if (c->dtype == MOE_GEMM_MXFP8) b += mx_ws_layout(c).total;
+  if (c->dtype == MOE_GEMM_NVFP4) b += nv4_ws_layout(c).total;
+  return b;
+}
+
+CombineArgs combine_args(const moe_config* c, const moe_gemm_args* a, void* ws) {
+  CombineArgs r;
+  r.row_src = a->a_rows;
+  r.slot_row = a->slot_row;
+  r.k = c->k;
+  r.count = at<int32_t>(ws, combine_count_offset(c));
+  r.shared = a->aux;
+  r.y = a->c2;
+  return r;
+}
+
 moe_status check_device() { return device_is_gb300() ? MOE_OK : MOE_ERR_UNSUPPORTED; }
 
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
@@ -307,7 +338,13 @@ moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool d
   const bool fc1 = a->op == MOE_GG_FC1_SWIGLU || a->op == MOE_GG_FC1_SWIGLU_GATHERED;
   if (fc1 && a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
   if (a->op == MOE_GG_DGRAD_FC2 && !dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
-  if (a->op < MOE_GG_FC1_SWIGLU || a->op > MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;
+  if (a->op < MOE_GG_FC1_SWIGLU || a->op > MOE_GG_FC2_COMBINE) return MOE_ERR_INVALID_ARG;
+  if (a->op == MOE_GG_FC2_COMBINE) {
+    if (dense || cfg->dtype == MOE_GEMM_NVFP4 || cfg->H % 256 != 0) return MOE_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!dev_ptr_ok(a->c2) || !dev_ptr_ok(a->a_rows) || !dev_ptr_ok(a->slot_row)))
+      return MOE_ERR_INVALID_ARG;
+    if (a->aux != nullptr && !aligned16(a->aux)) return MOE_ERR_INVALID_ARG;
+  }
   if (cfg->dtype == MOE_GEMM_BF16) {
     if (a->op == MOE_GG_FC1_SWIGLU_GATHERED && (dense || !dev_ptr_ok(a->a_rows))) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -350,10 +387,7 @@ moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, m
 
 size_t moe_workspace_bytes(const moe_config* cfg) {
   if (!config_ok(cfg)) return 0;
-  size_t b = kStatusBytes + align_up(hist_bytes(cfg));
-  if (cfg->dtype == MOE_GEMM_MXFP8) b += mx_ws_layout(cfg).total;
-  if (cfg->dtype == MOE_GEMM_NVFP4) b += nv4_ws_layout(cfg).total;
-  return b;
+  return combine_count_offset(cfg) + align_up(combine_count_bytes(cfg));
 }
 
 size_t moe_mxfp8_weights_bytes(const moe_config* cfg) {
@@ -465,7 +499,7 @@ moe_status moe_prepare_nvfp4_weights(const moe_config* cfg, const moe_weights* w
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!dev_ptr_ok(ws) || ws_bytes < kStatusBytes) return MOE_ERR_INVALID_ARG;
-  return cuda_status(cudaMemsetAsync(ws, 0, kStatusBytes, static_cast<cudaStream_t>(stream)));
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_read_device_status(const void* ws, int32_t* code, void* stream) {
@@ -564,6 +598,9 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
       case MOE_GG_FC2:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->dense_rows,
                                            a->c, status, st));
+      case MOE_GG_FC2_COMBINE:
+        return cuda_status(gemm_mx_fc2_combine(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->c,
+                                               combine_args(cfg, a, ws), status, st));
       case MOE_GG_DGRAD_FC2:
         if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
         return cuda_status(gemm_mx_dgrad_fc2(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
@@ -592,6 +629,8 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
                                          status, st));
     case MOE_GG_FC2:
       return cuda_status(gemm_fc2(a->a, rows, F, a->b, E, H, po, a->dense_rows, a->c, status, st));
+    case MOE_GG_FC2_COMBINE:
+      return cuda_status(gemm_fc2_combine(a->a, rows, F, a->b, E, H, po, a->c, combine_args(cfg, a, ws), status, st));
     case MOE_GG_DGRAD_FC2:
       if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
       return cuda_status(gemm_dgrad_fc2(a->a, rows, H, a->b, E, F, po, a->dense_rows, a->aux, a->row_gate, a->c,
@@ -659,6 +698,20 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   void* z = with_backward ? at<void>(act, L.z) : nullptr;
   void* zs = with_backward && S > 0 ? at<void>(act, L.zs) : nullptr;
   const void* shared_out = nullptr;
+  // 7 fused into fc2's epilogue where its 256-column tiles cover H: each
+  // token's y is summed by the tile that completes it (same bits as the
+  // separate combine kernel); otherwise a combine kernel after fc2
+  const bool fused_combine = kFuseCombine && H % 256 == 0 && T > 0;
+  CombineArgs cmb{};
+  if (fused_combine) {
+    cmb.row_src = at<int32_t>(act, L.row_src);
+    cmb.slot_row = slot_row;
+    cmb.k = k;
+    cmb.count = at<int32_t>(ws, combine_count_offset(cfg));
+    cmb.y = y;
+  }
+  // (the shared expert's output, when there is one, is set below before fc2)
+  auto with_shared = [&]() { cmb.shared = shared_out; };
   if (cfg->dtype == MOE_GEMM_NVFP4) {
     // NVFP4 expert GEMMs (forward): x quantised once per token with the tensor
     // scale of all of x, codes permuted into expert order; h quantised with
@@ -709,9 +762,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     MOE_TRY(launch_quantize_rows(x, T, H, 0, q(M.xs), f(M.xs), st));
     MOE_TRY(launch_gather_rows_mx(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st));
     if (with_backward) MOE_TRY(launch_zero_pad_rows_mx(counts, poff, E, H, q(M.x), f(M.x), st));
-    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
-    MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st));
-    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st));
+    // the shared expert first: with the combine fused into fc2 its rows must exist
     if (S > 0 && T > 0) {
       MOE_TRY(gemm_mx_fc1(q(M.xs), f(M.xs), T, H, wq(W.s1), wf(W.s1), 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
                           zs, status, st));
@@ -720,14 +771,27 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
                               status, st));
       shared_out = at<void>(act, L.os);
     }
+    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
+    MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st));
+    with_shared();
+    if (fused_combine) {
+      MOE_TRY(gemm_mx_fc2_combine(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, o, cmb, status, st));
+      return MOE_OK;
+    }
+    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st));
   } else {
-    MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, z, status, st));
-    MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st));
     if (S > 0 && T > 0) {
       MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs), zs, status, st));
       MOE_TRY(gemm_fc2(at<void>(act, L.hs), T, S, w->w2_shared, 1, H, nullptr, T, at<void>(act, L.os), status, st));
       shared_out = at<void>(act, L.os);
     }
+    MOE_TRY(gemm_fc1(x_perm, cap, H, w->w1, E, F, poff, 0, row_gate, h, z, status, st));
+    with_shared();
+    if (fused_combine) {
+      MOE_TRY(gemm_fc2_combine(h, cap, F, w->w2, E, H, poff, o, cmb, status, st));
+      return MOE_OK;
+    }
+    MOE_TRY(gemm_fc2(h, cap, F, w->w2, E, H, poff, 0, o, status, st));
   }
   // 7: unweighted combine
   MOE_TRY(launch_combine(o, slot_row, shared_out, T, k, H, y, st));

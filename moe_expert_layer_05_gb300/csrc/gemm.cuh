@@ -86,6 +86,18 @@ struct GemmParams {
   int a_rows;
   int* status;             // device status word (first error wins)
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
+  // fc2 with the combine fused into its epilogue (kStoreBf16, BN = 256, routed;
+  // cmb_y == nullptr: off).  After a tile's rows of o are stored, each row adds
+  // one to the counter of (its token, this N tile); the arrival that completes
+  // the token's valid slots sums the token's k rows of those columns in slot
+  // order (fp32, plus the shared expert's row), writes y once and puts the
+  // counter back to zero.
+  const int32_t* cmb_row_src;      // [rows_cap] token of each row, -1 padding
+  const int32_t* cmb_slot_row;     // [T, k] row of each (token, slot), -1 dropped
+  int cmb_k;
+  int* cmb_count;                  // [T, n_tiles], zero between launches
+  const __nv_bfloat16* cmb_shared; // [T, ldc] or nullptr
+  __nv_bfloat16* cmb_y;            // [T, ldc]
 };
 
 template <int BN_, bool A_MN_, bool B_MN_, Sched S_, Epi EP_, int MX_ = 0, bool M256_ = false,
@@ -462,6 +474,70 @@ __device__ __forceinline__ void amax_flush(unsigned* out, float m, int lane) {
   if (lane == 0) atomicMax(out, u);
 }
 
+__device__ __forceinline__ void add8_bf16(float (&acc)[8], const uint4& v) {
+  acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+  acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+  acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+  acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+}
+
+// The combine fused into fc2's epilogue (GemmParams::cmb_*), for this warp's
+// 32 rows (y0 .. y0+31) of N tile n, once their TMA stores have been issued.
+// Every row of a tile belongs to a different token (a token picks an expert at
+// most once), so a lane's counter is its own.  The sum runs in slot order
+// whichever tile arrives last, so y is the same bits on every run.
+template <int NBUF>
+__device__ __forceinline__ void fused_combine_rows(const GemmParams& p, int y0, int n, int lane, Stager<NBUF>& st) {
+  st.drain();                                   // lane 0: this warp's stores of o are complete
+  if (lane == 0) fence_proxy_async_global();
+  __syncwarp();
+  const int r = y0 + lane;
+  const int t = (r < p.rows_cap) ? p.cmb_row_src[r] : -1;
+  const int k = p.cmb_k;
+  bool last = false;
+  if (t >= 0) {
+    int valid = 0;
+    for (int i = 0; i < k; ++i) valid += p.cmb_slot_row[(long long)t * k + i] >= 0 ? 1 : 0;
+    __threadfence();                            // o's rows before the count others act on
+    last = atomicAdd(p.cmb_count + (long long)t * p.n_tiles + n, 1) + 1 == valid;
+  }
+  unsigned todo = __ballot_sync(0xffffffffu, last);
+  if (todo == 0) return;
+  __threadfence();                              // the other tiles' rows after their counts
+  const long long ld = p.ldc;
+  const int col = n * 256 + 8 * lane;           // 8 columns (16 bytes) per lane
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.c);
+  while (todo != 0) {
+    const int src = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const int tt = __shfl_sync(0xffffffffu, t, src);
+    // lane i < k holds slot i's row; the rows are loaded 8 at a time (all in
+    // flight together) and added in slot order
+    const int my_row = (lane < k) ? p.cmb_slot_row[(long long)tt * k + lane] : -1;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint4 sv = make_uint4(0, 0, 0, 0);
+    if (p.cmb_shared != nullptr) sv = __ldg(reinterpret_cast<const uint4*>(p.cmb_shared + tt * ld + col));
+    for (int i0 = 0; i0 < k; i0 += 8) {
+      uint4 v[8];
+      int rr[8];
+      #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        rr[j] = __shfl_sync(0xffffffffu, my_row, (i0 + j) & 31);
+        if (i0 + j >= k) rr[j] = -1;
+        v[j] = rr[j] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(o + rr[j] * ld + col)) : make_uint4(0, 0, 0, 0);
+      }
+      #pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (rr[j] >= 0) add8_bf16(acc, v[j]);
+    }
+    if (p.cmb_shared != nullptr) add8_bf16(acc, sv);
+    *reinterpret_cast<uint4*>(p.cmb_y + tt * ld + col) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+    if (lane == src) p.cmb_count[(long long)tt * p.n_tiles + n] = 0;   // ready for the next launch
+  }
+}
+
 // Epilogue with TMA stores.  Rows of the tile: warp quarter q owns rows
 // 32q..32q+31, lane = row.  Dense tiles past the last row are clipped by TMA.
 template <class C>
@@ -569,6 +645,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
           }
           st.flush(tmC, ti.n * C::BN + 64 * c, y);
         }
+        if constexpr (C::S == Sched::kRoutedM) {
+          if (p.cmb_y != nullptr) fused_combine_rows(p, y, ti.n, lane, st);
+        }
         return;
       }
     }
@@ -590,6 +669,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         st.put(2 * h + 1, w[4], w[5], w[6], w[7]);
       }
       st.flush(tmC, ti.n * C::BN + c0, y);
+    }
+    if constexpr (C::S == Sched::kRoutedM && C::BN == 256) {
+      if (p.cmb_y != nullptr) fused_combine_rows(p, y, ti.n, lane, st);
     }
   } else if constexpr (C::EP == Epi::kSwiglu) {
     // accumulator columns [0, BN/2) = gate rows of W1, [BN/2, BN) = the matching up rows

@@ -99,6 +99,15 @@ inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, uint64_t cols,
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32);
 }
 
+inline void set_combine(GemmParams& p, const CombineArgs& c) {
+  p.cmb_row_src = c.row_src;
+  p.cmb_slot_row = c.slot_row;
+  p.cmb_k = c.k;
+  p.cmb_count = c.count;
+  p.cmb_shared = static_cast<const __nv_bfloat16*>(c.shared);
+  p.cmb_y = static_cast<__nv_bfloat16*>(c.y);
+}
+
 inline GemmParams gemm_params_zero() {
   GemmParams p{};
   p.valid_cols = 1 << 30;

@@ -190,4 +190,29 @@ cudaError_t gemm_fc2(const void* a, int rows_alloc, int F, const void* w2, int E
   return fc2_bn<128>(a, rows_alloc, F, w2, E, H, poffsets, dense_rows, o, status, st);
 }
 
+cudaError_t gemm_fc2_combine(const void* a, int rows_alloc, int F, const void* w2, int E, int H,
+                             const int32_t* poffsets, void* o, const CombineArgs& cmb, int* status, cudaStream_t st) {
+  if (H % 256 != 0 || poffsets == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, a, F, rows_alloc, 64, 256) ||
+      !make_tmap_bf16(&tb, w2, F, static_cast<uint64_t>(E) * H, 64, 256))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.k_len = F;
+  p.n_tiles = H / 256;
+  p.b_rows_per_group = H;
+  p.c = o;
+  p.ldc = H;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  set_combine(p, cmb);
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, o, H, rows_alloc)) return cudaErrorInvalidValue;
+  using C = GemmCfg<256, false, false, Sched::kRoutedM, Epi::kStoreBf16, false, true>;
+  const int upper = (rows_alloc / 128) * p.n_tiles;
+  return launch_gemm<C>(ta, tb, tc, tc, p, upper < num_sms() ? upper : num_sms(), st);
+}
+
 }  // namespace moe

@@ -114,6 +114,34 @@ cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int
   return mx_nt_bf16_bn<128>(aq, asf, rows_alloc, K, bq, bsf, E, N, poffsets, dense_rows, c, status, st);
 }
 
+cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc, int F, const void* bq,
+                                const void* bsf, int E, int H, const int32_t* poffsets, void* o,
+                                const CombineArgs& cmb, int* status, cudaStream_t st) {
+  if (H % 256 != 0 || poffsets == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, aq, F, rows_alloc, 128) || !make_tmap_u8(&tb, bq, F, static_cast<uint64_t>(E) * H, 256))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = E;
+  p.k_len = F;
+  p.n_tiles = H / 256;
+  p.b_rows_per_group = H;
+  p.c = o;
+  p.ldc = H;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(asf);
+  p.sfb = static_cast<const uint8_t*>(bsf);
+  p.sfa_tiles_k = F / 128;
+  p.sfb_tiles_k = F / 128;
+  set_combine(p, cmb);
+  CUtensorMap tc;
+  if (!make_tmap_out_bf16(&tc, o, H, rows_alloc)) return cudaErrorInvalidValue;
+  return launch_mx<GemmCfg<256, false, false, Sched::kRoutedM, Epi::kStoreBf16, true>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                      0, st);
+}
+
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
                               const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st) {

@@ -64,6 +64,19 @@ cudaError_t gemm_fc1_gather(const void* x, int T, const int32_t* row_src, int ro
 // o[cap,H] = A[cap,F] * W2_e[H,F]^T
 cudaError_t gemm_fc2(const void* a, int rows_alloc, int F, const void* w2, int E, int H, const int32_t* poffsets,
                      int dense_rows, void* o, int* status, cudaStream_t st);
+// The combine fused into fc2's epilogue: besides o, y[t] = sum_i o[slot_row[t,i]]
+// (+ shared[t]) in slot order, fp32, one rounding -- the bits of launch_combine.
+// count: [T, H/256] ints, zero before the launch and after it.  H % 256 == 0.
+struct CombineArgs {
+  const int32_t* row_src;
+  const int32_t* slot_row;
+  int k;
+  int* count;
+  const void* shared;   // nullable
+  void* y;
+};
+cudaError_t gemm_fc2_combine(const void* a, int rows_alloc, int F, const void* w2, int E, int H,
+                             const int32_t* poffsets, void* o, const CombineArgs& cmb, int* status, cudaStream_t st);
 // dz[cap,2F] from dh = A[cap,H] * W2_e ([H,F]) with SwiGLU backward epilogue.
 cudaError_t gemm_dgrad_fc2(const void* dy_perm, int rows_alloc, int H, const void* w2, int E, int F,
                            const int32_t* poffsets, int dense_rows, const void* z, const float* row_gate,
@@ -96,6 +109,10 @@ cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, 
 cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
                             int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
                             cudaStream_t st);
+// MXFP8 fc2 (N = H, H % 256 == 0) with the combine fused into its epilogue.
+cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc, int F, const void* bq,
+                                const void* bsf, int E, int H, const int32_t* poffsets, void* o,
+                                const CombineArgs& cmb, int* status, cudaStream_t st);
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
                               const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st);

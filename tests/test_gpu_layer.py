@@ -70,6 +70,18 @@ def check_e2e(got, ref, what):
     return r
 
 
+def check_combine_bits(layer, w, y):
+    """y of the layer (the combine fused into fc2 where H % 256 == 0, the
+    combine kernel otherwise) is bit-identical to moe_unpermute of the layer's
+    own o and shared-expert rows."""
+    fl = layer.fields()
+    sh = layer.view("os", torch.bfloat16, (w.T, w.H)) if w.S else None
+    ref = torch.empty_like(y)
+    api.moe_unpermute(layer.cfg, fl["o"], fl["slot_row"], sh, ref)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
 def check_dlogits(w, fl, dgate, bwd_dlogits, stable, tol):
     """dlogits of the layer: against the oracle's router backward (end to end,
     on the stable tokens), and as a step against the router-backward formula
@@ -105,6 +117,7 @@ def test_layer_small(lib, name):
     check_e2e(f64(y)[stable], fwd["y"][stable], f"{name} y")
     assert (~stable).sum() <= max(1, w.T // 100)
     check_full_permutation(w, fl, dinp["x"])
+    check_combine_bits(layer, w, y)
     if not w.backward:
         return
     dy = dinp["dy"]
@@ -201,6 +214,7 @@ def test_layer_full_size_forward_sampled(lib, name, n_sample):
     fl = layer.fields()
     # the permutation at full T, bit for bit against the oracle's counting sort
     check_full_permutation(w, fl, dinp["x"])
+    check_combine_bits(layer, w, y)
     fwd = _oracle_fwd(w, inp, tokens)
     stable = _stable_tokens(w, fwd["logits"], inp["bias"])
     np.testing.assert_array_equal(i64(fl["topk_idx"])[tokens][stable], fwd["topk_idx"][stable])

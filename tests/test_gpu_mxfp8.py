@@ -171,6 +171,36 @@ def test_mx_gemm_forward(lib, T, H, E, k, F, skew):
     assert_bf16_close(f64(o)[:used], O.expert_fc2(deq(h_in, -1)[:used], deq(w2, -1), m["poffsets"]), "o (mxfp8)")
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(256, 256, 8, 2, 256, 0.0), (640, 512, 16, 4, 384, 1.5)])
+def test_mx_gemm_fc2_combine(lib, T, H, E, k, F, skew):
+    """MXFP8 fc2 with the combine fused into its epilogue: o bit-identical to
+    the plain MXFP8 fc2 and y to moe_unpermute of it, two calls in a row."""
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 51)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    h_in = _rows(cap, F, valid, 52)
+    w2 = to_bf16(_rand((E, H, F), 53, 0.05))
+    hq, hsf = quantize_gpu(h_in.to(DEV), api.MX_ROWS)
+    w2q, w2sf = quantize_gpu(w2.to(DEV).reshape(E * H, F), api.MX_ROWS)
+    slot = torch.from_numpy(m["slot_row"].astype(np.int32)).to(DEV)
+    src = torch.full((cap,), -1, dtype=torch.int32, device=DEV)
+    src[:used] = torch.from_numpy(m["row_src"].astype(np.int32)).to(DEV)
+    sh = to_bf16(_rand((T, H), 54)).to(DEV)
+    ws = _ws(cfg)
+    o_ref = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+    api.moe_grouped_gemm(cfg, api.GG_FC2, hq, w2q, o_ref, ws, poffsets=po, a_scales=hsf, b_scales=w2sf)
+    y_ref = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    api.moe_unpermute(cfg, o_ref, slot, sh, y_ref)
+    for rep in range(2):
+        o = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+        y = torch.full((T, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        api.moe_grouped_gemm(cfg, api.GG_FC2_COMBINE, hq, w2q, o, ws, c2=y, aux=sh, poffsets=po, a_scales=hsf,
+                             b_scales=w2sf, a_rows=src, slot_row=slot)
+        torch.cuda.synchronize()
+        assert api.moe_read_device_status(ws) == 0
+        assert torch.equal(o[:used].view(torch.int16), o_ref[:used].view(torch.int16)), rep
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), rep
+
+
 @pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
 def test_mx_gemm_dgrad(lib, T, H, E, k, F, skew):
     cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 13)
@@ -258,6 +288,13 @@ def test_mx_layer_against_mxfp8_oracle(lib, name):
     np.testing.assert_array_equal(layer.fields()["topk_idx"].cpu().numpy()[stable], fwd["topk_idx"][stable])
     r_y = rel_l2(f64(y)[stable], fwd["y"][stable])
     assert r_y <= 3e-2, r_y
+    # y (combine fused into fc2 where H % 256 == 0) = moe_unpermute of the layer's own o, bit for bit
+    fl = layer.fields()
+    os_rows = layer.view("os", torch.bfloat16, (w.T, w.H)) if w.S else None
+    y_cmb = torch.empty_like(y)
+    api.moe_unpermute(layer.cfg, fl["o"], fl["slot_row"], os_rows, y_cmb)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_cmb.view(torch.int16))
     plain = O.moe_forward(*args, k=w.k, score=w.score, bias=bias, **sh)
     assert rel_l2(f64(y)[stable], plain["y"][stable]) < 0.15
     bwd = O.moe_backward_mx(*args, fwd, f64(inp["dy"]), score=w.score, **sh)

@@ -333,6 +333,57 @@ def test_gemm_fc2_alone(lib, T, H, E, k, F, skew):
     assert_bf16_close(f64(o)[:used], O.expert_fc2(f64(hin)[:used], LazyW(w2), m["poffsets"]), "o")
 
 
+@pytest.mark.parametrize("shared,dropped", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(700, 256, 16, 4, 384, 1.5), (300, 512, 128, 8, 128, 1.0),
+                                            (256, 768, 8, 2, 256, 0.0)])
+def test_gemm_fc2_combine(lib, T, H, E, k, F, skew, shared, dropped):
+    """fc2 with the combine fused into its epilogue: o bit-identical to the
+    plain fc2, y bit-identical to moe_unpermute of that o (same slot-order fp32
+    sum, one rounding) and within the oracle's combine bound; two calls in a
+    row (the counters go back to zero).  With dropped: some pairs have
+    slot_row -1 (and their rows row_src -1), as after an out-of-range id."""
+    cfg, m, cap, used, valid = _routed_case(T, H, E, k, F, skew, 41)
+    hin = _rows(cap, F, valid, 42)
+    w2 = to_bf16(_rand((E, H, F), 43, 0.05)).to(DEV)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    slot = m["slot_row"].astype(np.int32).copy()
+    src = np.full(cap, -1, np.int32)
+    src[:used] = m["row_src"]
+    if dropped:
+        rng = np.random.default_rng(44)
+        for t in rng.choice(T, size=max(1, T // 20), replace=False):
+            i = int(rng.integers(k))
+            src[slot[t, i]] = -1
+            slot[t, i] = -1
+    slot_t, src_t = torch.from_numpy(slot).to(DEV), torch.from_numpy(src).to(DEV)
+    sh = to_bf16(_rand((T, H), 45)).to(DEV) if shared else None
+    ws = _ws(cfg)
+    o_ref = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+    api.moe_grouped_gemm(cfg, api.GG_FC2, hin.to(DEV), w2, o_ref, ws, poffsets=po)
+    y_ref = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    api.moe_unpermute(cfg, o_ref, slot_t, sh, y_ref)
+    for rep in range(2):
+        o = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+        y = torch.full((T, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        api.moe_grouped_gemm(cfg, api.GG_FC2_COMBINE, hin.to(DEV), w2, o, ws, c2=y, aux=sh, poffsets=po,
+                             a_rows=src_t, slot_row=slot_t)
+        torch.cuda.synchronize()
+        assert _status(ws) == 0
+        assert torch.equal(o[:used].view(torch.int16), o_ref[:used].view(torch.int16)), rep
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), rep
+    # and against the oracle's combine of the same o (the plain fc2 is pinned by test_gemm_fc2_alone);
+    # dropped pairs leave the sum, as moe_unpermute skips them
+    o64 = f64(o_ref)
+    if not dropped:
+        ref = O.unpermute_sum(o64, m, None if sh is None else f64(sh))
+    else:
+        ref = np.where((slot >= 0)[..., None], o64[np.where(slot >= 0, slot, 0)], 0.0).sum(1)
+        ref = ref + (f64(sh) if shared else 0.0)
+    absum = np.where((slot >= 0)[..., None], np.abs(o64)[np.where(slot >= 0, slot, 0)], 0.0).sum(1)
+    absum = absum + (np.abs(f64(sh)) if shared else 0.0)
+    assert np.all(np.abs(f64(y) - ref) <= 2.0 ** -8 * np.abs(ref) + 2.0 ** -19 * absum + 1e-30)
+
+
 @pytest.mark.parametrize("T,H,E,k,F,skew", GEMM_CASES)
 def test_gemm_dgrad(lib, T, H, E, k, F, skew):
     cfg, m, cap, used, valid = _routed_case(T, H, E, k, F, skew, 31)
