@@ -478,21 +478,44 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
     return calls
 
 
-def stage_breakdown(api, w, layer, dinp, x, y, flush, stream, n) -> dict:
-    """The HBM-bound steps alone (CUDA events, L2 flushed), with their
-    algorithmic bytes: permute (1+k)*T*H*2, combine (k+1)*T*H*2 (+T*H*2 shared)."""
+def _as_graph(fn, stream, dev):
+    """fn's launches captured once into a CUDA graph (as the layer's step runs
+    them), returned as its replay: the stage is then timed without the host's
+    per-launch overhead between its kernels."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g.replay, g
+
+
+def stage_breakdown(api, w, layer, dinp, x, y, flush, stream, n, dev=None) -> dict:
+    """The HBM-bound steps alone (CUDA events, L2 flushed; each stage replayed
+    as a CUDA graph, as in the layer's step), with their algorithmic bytes:
+    permute (1+k)*T*H*2, combine (k+1)*T*H*2 (+T*H*2 shared)."""
     cfg, fl = layer.cfg, layer.fields()
     T, H, k = w.T, w.H, w.k
+    dev = x.device if dev is None else dev
     shared = layer.view("os", torch.bfloat16, (T, H)) if w.S > 0 else None
+    graphs = []
+
+    def timed(fn):
+        run, g = _as_graph(fn, stream, dev)
+        graphs.append(g)
+        return _timed(run, n, flush, stream)
+
     out = {}
-    out["router_topk"] = _timed(lambda: api.moe_router_topk(cfg, x, dinp["w_router"], dinp["bias"], fl["logits"],
-                                                             fl["topk_idx"], fl["topk_gate"], layer.ws),
-                                n, flush, stream)
-    out["permute"] = _timed(lambda: api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"],
-                                                    fl["offsets"], fl["poffsets"], fl["slot_row"], fl["row_src"],
-                                                    fl["row_gate"], fl["x_perm"], int(w.backward), layer.ws),
-                            n, flush, stream)
-    out["combine"] = _timed(lambda: api.moe_unpermute(cfg, fl["o"], fl["slot_row"], shared, y), n, flush, stream)
+    out["router_topk"] = timed(lambda: api.moe_router_topk(cfg, x, dinp["w_router"], dinp["bias"], fl["logits"],
+                                                            fl["topk_idx"], fl["topk_gate"], layer.ws))
+    out["permute"] = timed(lambda: api.moe_permute(cfg, x, fl["topk_idx"], fl["topk_gate"], fl["counts"],
+                                                   fl["offsets"], fl["poffsets"], fl["slot_row"], fl["row_src"],
+                                                   fl["row_gate"], fl["x_perm"], int(w.backward), layer.ws))
+    out["combine"] = timed(lambda: api.moe_unpermute(cfg, fl["o"], fl["slot_row"], shared, y))
     pbytes = (1 + k) * T * H * 2
     cbytes = (k + 1) * T * H * 2 + (T * H * 2 if w.S > 0 else 0)
     out["permute_gbs"] = pbytes / (out["permute"] / 1e3) / 1e9

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __
   __shared__ int s_tot[kMaxE];
   const int e = load_pair_expert(idx, npairs, pb, E, status);
   block_stable_rank(e, E, s_cnt, s_tot);
-  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)blockIdx.x * E + x] = s_tot[x];
+  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)x * gridDim.x + blockIdx.x] = s_tot[x];
 }
 
 // Top-k gating fused with the chunk histogram: block b routes the tokens of
@@ -277,57 +277,59 @@ __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* 
   const long long p = (long long)blockIdx.x * pb + threadIdx.x;
   const int e = (threadIdx.x < pb && p < npairs) ? s_idx[threadIdx.x] : -1;
   block_stable_rank(e, E, s_cnt, s_tot);
-  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)blockIdx.x * E + x] = s_tot[x];
+  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)x * gridDim.x + blockIdx.x] = s_tot[x];
 }
 
-// One block.  hist [NB][E] -> counts, offsets, poffsets, and in place
-// base[b][e] = poffsets[e] + sum_{b'<b} hist[b'][e].  Also marks padding rows.
-// Thread (e, g): expert e, group g of G lanes (G a power of two <= 32, G*E <=
-// 1024) owning a contiguous range of chunks; sums and prefixes across the G
-// lanes of one expert are warp shuffles.
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int NB, int E, int G,
-                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                    int32_t* __restrict__ poffsets, int32_t* __restrict__ row_src,
-                                                    float* __restrict__ row_gate) {
-  __shared__ int s_cnt[kMaxE];
-  __shared__ int s_poff[kMaxE + 1];
-  const int tid = threadIdx.x;
-  const int e = tid / G, g = tid % G;
-  const bool active = e < E;
-  const int per = (NB + G - 1) / G;
-  const int b0 = min(NB, g * per), b1 = min(NB, b0 + per);
-  // Both passes over this lane's chunks load 8 entries at a time: the loads of
-  // a batch are independent, so their latencies overlap.
+// The chunk histograms are laid out per expert: hist[e * NB + b] = pairs of
+// chunk b routed to expert e.  One warp per expert scans its column in place:
+// hist[e][b] becomes the number of expert-e pairs in the chunks before b, and
+// counts[e] the column total.  All of a lane's loads of a batch are issued
+// before the first is used.
+__global__ void __launch_bounds__(256) scan_cols_kernel(int32_t* __restrict__ hist, int NB, int E,
+                                                        int32_t* __restrict__ counts) {
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (e >= E) return;
+  int32_t* col = hist + (long long)e * NB;
   constexpr int kBatch = 8;
-  int sum = 0;
-  if (active) {
-    int b = b0;
-    for (; b + kBatch <= b1; b += kBatch) {
-      int v[kBatch];
-      #pragma unroll
-      for (int j = 0; j < kBatch; ++j) v[j] = hist[(long long)(b + j) * E + e];
-      #pragma unroll
-      for (int j = 0; j < kBatch; ++j) sum += v[j];
+  int run = 0;
+  for (int b0 = 0; b0 < NB; b0 += 32 * kBatch) {
+    int v[kBatch];
+    #pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int b = b0 + 32 * j + lane;
+      v[j] = (b < NB) ? col[b] : 0;
     }
-    for (; b < b1; ++b) sum += hist[(long long)b * E + e];
+    #pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      int inc = v[j];
+      #pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(kFull, inc, d);
+        if (lane >= d) inc += u;
+      }
+      const int b = b0 + 32 * j + lane;
+      if (b < NB) col[b] = run + inc - v[j];
+      run += __shfl_sync(kFull, inc, 31);
+    }
   }
-  // inclusive prefix over the G lanes of this expert (lanes g of a group are consecutive)
-  int inc = sum;
-  for (int d = 1; d < G; d <<= 1) {
-    const int v = __shfl_up_sync(kFull, inc, d);
-    if (g >= d) inc += v;
-  }
-  const int total = __shfl_sync(kFull, inc, (tid & 31) | (G - 1));   // last lane of the group
-  if (active && g == 0) {
-    s_cnt[e] = total;
-    counts[e] = total;
-  }
-  __syncthreads();
+  if (lane == 0) counts[e] = run;
+}
+
+// Exclusive scans over the experts of counts and of counts rounded up to
+// whole 128-row blocks, by the first warp of a block, into s_off / s_poff
+// (E + 1 entries each).
+__device__ __forceinline__ void expert_offsets(const int32_t* __restrict__ counts, int E, int* s_off, int* s_poff) {
+  const int tid = threadIdx.x;
   if (tid < 32) {
     const int per_lane = (E + 31) / 32;
     const int e0 = tid * per_lane, e1 = min(E, e0 + per_lane);
     int cs = 0, ps = 0;
-    for (int x = e0; x < e1; ++x) { cs += s_cnt[x]; ps += (s_cnt[x] + kPadRows - 1) / kPadRows * kPadRows; }
+    for (int x = e0; x < e1; ++x) {
+      const int c = counts[x];
+      cs += c;
+      ps += (c + kPadRows - 1) / kPadRows * kPadRows;
+    }
     int ci = cs, pi = ps;
     #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -336,64 +338,58 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
     }
     int c_ex = ci - cs, p_ex = pi - ps;
     for (int x = e0; x < e1; ++x) {
-      offsets[x] = c_ex;
-      poffsets[x] = p_ex;
+      const int c = counts[x];
+      s_off[x] = c_ex;
       s_poff[x] = p_ex;
-      c_ex += s_cnt[x];
-      p_ex += (s_cnt[x] + kPadRows - 1) / kPadRows * kPadRows;
+      c_ex += c;
+      p_ex += (c + kPadRows - 1) / kPadRows * kPadRows;
     }
-    if (tid == 31) { offsets[E] = ci; poffsets[E] = pi; s_poff[E] = pi; }
-  }
-  __syncthreads();
-  if (active) {
-    int run = s_poff[e] + inc - sum;
-    int b = b0;
-    for (; b + kBatch <= b1; b += kBatch) {
-      int v[kBatch];
-      #pragma unroll
-      for (int j = 0; j < kBatch; ++j) v[j] = hist[(long long)(b + j) * E + e];
-      #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        hist[(long long)(b + j) * E + e] = run;
-        run += v[j];
-      }
-    }
-    for (; b < b1; ++b) {
-      const long long i = (long long)b * E + e;
-      const int c = hist[i];
-      hist[i] = run;
-      run += c;
-    }
-  }
-  // padding rows of every segment
-  for (int i = tid; i < E * kPadRows; i += blockDim.x) {
-    const int x = i / kPadRows, j = i % kPadRows;
-    const int r = s_poff[x] + s_cnt[x] + j;
-    if (r < s_poff[x + 1]) {
-      row_src[r] = -1;
-      if (row_gate != nullptr) row_gate[r] = 0.f;
-    }
+    if (tid == 31) { s_off[E] = ci; s_poff[E] = pi; }
   }
 }
 
+// Block b: the maps of chunk b's pairs.  Row of a pair = poffsets[e] + pairs
+// of expert e in earlier chunks (the scanned column) + its stable rank inside
+// the chunk.  Block 0 also writes offsets and poffsets and marks the padding
+// rows of every segment (row_src -1, row_gate 0).
 __global__ void __launch_bounds__(kPairsPerBlock) scatter_kernel(const int32_t* __restrict__ idx,
                                                                  const float* __restrict__ gate, long long npairs,
-                                                                 int pb, int E, int k,
+                                                                 int pb, int E, int k, int NB,
                                                                  const int32_t* __restrict__ base,
+                                                                 const int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ offsets,
+                                                                 int32_t* __restrict__ poffsets,
                                                                  int32_t* __restrict__ slot_row,
                                                                  int32_t* __restrict__ row_src,
                                                                  float* __restrict__ row_gate) {
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_poff[kMaxE + 1];
+  expert_offsets(counts, E, s_off, s_poff);
   const int e = load_pair_expert(idx, npairs, pb, E, nullptr);
-  const int r = block_stable_rank(e, E, s_cnt, s_tot);
+  const int r = block_stable_rank(e, E, s_cnt, s_tot);   // (its barriers also publish s_off, s_poff)
+  if (blockIdx.x == 0) {
+    for (int x = threadIdx.x; x <= E; x += blockDim.x) {
+      offsets[x] = s_off[x];
+      poffsets[x] = s_poff[x];
+    }
+    for (int i = threadIdx.x; i < E * kPadRows; i += blockDim.x) {
+      const int x = i / kPadRows, j = i % kPadRows;
+      const int rr = s_poff[x] + counts[x] + j;
+      if (rr < s_poff[x + 1]) {
+        row_src[rr] = -1;
+        if (row_gate != nullptr) row_gate[rr] = 0.f;
+      }
+    }
+  }
   const long long p = (long long)blockIdx.x * pb + threadIdx.x;
   if (threadIdx.x >= pb || p >= npairs) return;
   if (e < 0) {
     slot_row[p] = -1;
     return;
   }
-  const int row = base[(long long)blockIdx.x * E + e] + r;
+  const int row = s_poff[e] + base[(long long)e * NB + blockIdx.x] + r;
   slot_row[p] = row;
   row_src[row] = static_cast<int32_t>(p / k);
   if (row_gate != nullptr) row_gate[row] = gate[p];
@@ -636,22 +632,17 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 namespace {
 int chunks_of(int T, int k) { return (T + kPairsPerBlock / k - 1) / (kPairsPerBlock / k); }
 
-int scan_groups(int E) {
-  int G = 32;
-  while (G > 1 && G * E > 1024) G >>= 1;
-  return G;
-}
-
 cudaError_t launch_scan_scatter(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
                                 int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
                                 int32_t* row_src, float* row_gate, cudaStream_t st) {
   const long long npairs = (long long)T * k;
   const int NB = chunks_of(T, k);
-  scan_kernel<<<1, 1024, 0, st>>>(hist, NB, E, scan_groups(E), counts, offsets, poffsets, row_src, row_gate);
-  if (NB > 0)
-    scatter_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, gate, npairs, pairs_per_chunk(k), E, k, hist, slot_row,
-                                                  row_src, gate != nullptr ? row_gate : nullptr);
-  count_launches(NB > 0 ? 2 : 1);
+  scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, NB, E, counts);
+  // (with no tokens one block still writes the offsets)
+  scatter_kernel<<<NB > 0 ? NB : 1, kPairsPerBlock, 0, st>>>(idx, gate, npairs, pairs_per_chunk(k), E, k, NB, hist,
+                                                             counts, offsets, poffsets, slot_row, row_src,
+                                                             gate != nullptr ? row_gate : nullptr);
+  count_launches(2);
   return cudaGetLastError();
 }
 }  // namespace
