@@ -152,6 +152,16 @@ size_t moe_workspace_bytes(const moe_config* cfg);
  * the fused combine's counters).  Stream-ordered, does not block. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
+/* For tests of the failure path: every pipeline wait inside the grouped
+ * GEMMs launched after this call gives up after `ns` nanoseconds instead of
+ * the default 2 s (0 restores the default).  A wait that gives up makes its
+ * kernel raise a flag that ends the other waits of its CTA, let every copy and
+ * MMA already issued finish (bounded drains), free its TMEM and set
+ * MOE_ERR_TIMEOUT in the status word; the outputs of that launch are then
+ * incomplete.  Process-wide; not meant for production use.  No counterpart on
+ * the pages: a library-side check of the bounded waits. */
+void moe_debug_set_wait_limit_ns(uint64_t ns);
+
 /* Synchronise `stream`, then copy the device status word to *code
  * (MOE_OK or the first device error since the last moe_workspace_init).
  * The only call that blocks; keep it out of the hot path. */

@@ -63,6 +63,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [c_i32]),
     "moe_version": (c_i32, []),
     "moe_kernel_launches": (ctypes.c_uint64, []),
+    "moe_debug_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "moe_capacity_rows": (c_i32, [_P(MoeConfig)]),
     "moe_activation_layout": (c_i32, [_P(MoeConfig), c_i32, _P(MoeActLayout)]),
     "moe_workspace_bytes": (c_sz, [_P(MoeConfig)]),
@@ -365,6 +366,11 @@ class MoELayer:
                      ptr(grads.get("dw2_shared")))
         moe_layer_backward_wgrad(c, self.cw, x, dy, g, self.act, self.ws, stream)
         return dx, dgate, grads
+
+
+def moe_debug_set_wait_limit_ns(ns: int) -> None:
+    """Test hook: the grouped GEMMs' pipeline waits give up after ns (0: 2 s)."""
+    load().moe_debug_set_wait_limit_ns(int(ns))
 
 
 def moe_kernel_launches() -> int:

@@ -48,6 +48,11 @@ std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n), std::memory_order_relaxed); }
 
 int num_sms() { return dev_info().sms; }
+
+namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+}  // namespace
+unsigned long long gemm_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 bool device_is_gb300() { return dev_info().gb300; }
 
 }  // namespace moe
@@ -376,6 +381,8 @@ const char* moe_status_string(moe_status s) {
 }
 
 int32_t moe_version(void) { return 0x000100; }
+
+void moe_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 
 uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 

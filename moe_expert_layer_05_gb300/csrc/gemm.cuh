@@ -86,6 +86,7 @@ struct GemmParams {
   int a_rows;
   int* status;             // device status word (first error wins)
   int* sched;              // [0] next tile, [1] CTAs finished: the dynamic schedule (nullptr: static)
+  unsigned long long wait_ns;  // limit of a pipeline wait before the kernel gives up (0: kWaitLimitNs)
   // fc2 with the combine fused into its epilogue (kStoreBf16, BN = 256, routed;
   // cmb_y == nullptr: off).  After a tile's rows of o are stored, each row adds
   // one to the counter of (its token, this N tile); the arrival that completes
@@ -1047,6 +1048,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
+  const unsigned long long wait_lim = p.wait_ns != 0 ? p.wait_ns : kWaitLimitNs;
 
   if (s_bad) {
     if (threadIdx.x == 0) set_status(p.status, kErrBadIndex);
@@ -1079,7 +1081,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int j = 0; ok; ++j) {
         const int slot = j % kSchedDepth;
         int w = 1;
-        if (lane == 0) w = mbar_wait(&bk.sched_empty[slot], ((j / kSchedDepth) & 1) ^ 1u, abort_ptr) ? 1 : 0;
+        if (lane == 0) w = mbar_wait(&bk.sched_empty[slot], ((j / kSchedDepth) & 1) ^ 1u, abort_ptr, wait_lim) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
         const int t = (next < ntiles) ? next : -1;
         if (lane == 0) {
@@ -1102,7 +1104,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           int e = 1;
-          if (lane == 0) e = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr) ? 1 : 0;
+          if (lane == 0) e = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr, wait_lim) ? 1 : 0;
           if (!__shfl_sync(0xffffffffu, e, 0)) { ok = false; break; }
           if (lane == 0) {
             mbar_arrive_expect_tx(&full_bar[stage], C::B_BYTES);
@@ -1151,7 +1153,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       int next = (p.sched != nullptr) ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x);
       for (int j = 0; ok; ++j) {
         const int slot = j % kSchedDepth;
-        if (!mbar_wait(&bk.sched_empty[slot], ((j / kSchedDepth) & 1) ^ 1u, abort_ptr)) { ok = false; break; }
+        if (!mbar_wait(&bk.sched_empty[slot], ((j / kSchedDepth) & 1) ^ 1u, abort_ptr, wait_lim)) { ok = false; break; }
         const int t = (next < ntiles) ? next : -1;
         bk.sched_tile[slot] = t;
         mbar_arrive(&bk.sched_full[slot]);
@@ -1160,7 +1162,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         next = (p.sched != nullptr) ? atomicAdd(p.sched, 1) : t + static_cast<int>(gridDim.x);
         const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
         for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr, wait_lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
           issue_loads<C>(&tmA, &tmB, p, ti, kb, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
                          sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES), &full_bar[stage]);
@@ -1187,16 +1189,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       bool ok = true, any = false;
       for (int j = 0; ok; ++j) {
         const int slot = j % kSchedDepth;
-        if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr)) { ok = false; break; }
+        if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr, wait_lim)) { ok = false; break; }
         const int t = bk.sched_tile[slot];
         mbar_arrive(&bk.sched_empty[slot]);
         if (t < 0) break;
         const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr, wait_lim)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_ptr)) { ok = false; break; }
+          if (!mbar_wait(&full_bar[stage], phase, abort_ptr, wait_lim)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
           const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
@@ -1278,13 +1280,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const float al = acc_scale<C>(p);
     for (int j = 0;; ++j) {
       const int slot = j % kSchedDepth;
-      if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr)) break;
+      if (!mbar_wait(&bk.sched_full[slot], (j / kSchedDepth) & 1, abort_ptr, wait_lim)) break;
       const int t = bk.sched_tile[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bk.sched_empty[slot]);
       if (t < 0) break;
       const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
-      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr, wait_lim)) break;
       tc_fence_after_sync();
       bool released = false;                 // accumulator already handed back by the epilogue
       if constexpr (C::M256) {
@@ -1440,6 +1442,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = bk.tmem_slot;
   volatile int* abort_ptr = &bk.abort_flag;
+  const unsigned long long wait_lim = p.wait_ns != 0 ? p.wait_ns : kWaitLimitNs;
   const bool bad = bk.bad != 0;          // both CTAs read the same offsets
   if (bad && leader && threadIdx.x == 0) set_status(p.status, kErrBadIndex);
   if constexpr (C::S == Sched::kRoutedM) {
@@ -1459,7 +1462,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int t = cid; t < ntiles && ok; t += ncl) {
         const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
         for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr)) { ok = false; break; }
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_ptr, wait_lim)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES);
           issue_loads_pair<C>(&tmA, &tmB, p, ti, kb, rank, a_smem + stage * C::A_BYTES, b_smem + stage * C::B_BYTES,
                               full_leader + 8u * stage);
@@ -1491,11 +1494,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       bool ok = true, any = false;
       for (int t = cid; t < ntiles && ok; t += ncl) {
         const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
-        if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr)) { ok = false; break; }
+        if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_ptr, wait_lim)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_ptr)) { ok = false; break; }
+          if (!mbar_wait(&full_bar[stage], phase, abort_ptr, wait_lim)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(a_smem + stage * C::A_BYTES);
           const uint32_t b_addr = smem_u32(b_smem + stage * C::B_BYTES);
@@ -1529,7 +1532,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     Stager<C::STAGING_BUFS> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * 4096), 0, lane};
     for (int t = cid; t < ntiles; t += ncl) {
       const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
-      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr)) break;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr, wait_lim)) break;
       tc_fence_after_sync();
       if (leader || ti.half1) {           // a half tile: the odd CTA's rows are not this expert's
         TileInfo th = ti;

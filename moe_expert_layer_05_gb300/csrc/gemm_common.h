@@ -46,6 +46,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   if (grid <= 0) return cudaSuccess;
   GemmParams q = p;
   q.sched = (p.status != nullptr) ? p.status + kSchedCounterWord : nullptr;
+  q.wait_ns = gemm_wait_limit_ns();
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, tc, tc2, q);
   count_launches(1);
   return cudaGetLastError();
@@ -86,7 +87,9 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
   if (tiles_upper <= 0) return cudaSuccess;
   const int clusters = tiles_upper < max_clusters ? tiles_upper : max_clusters;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tc2, p);
+  GemmParams q = p;
+  q.wait_ns = gemm_wait_limit_ns();
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tc2, q);
   count_launches(1);
   return e;
 }

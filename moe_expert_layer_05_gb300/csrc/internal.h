@@ -14,6 +14,9 @@ constexpr int kMaxK = 32;
 
 int num_sms();
 bool device_is_gb300();
+// Limit of one pipeline wait inside the grouped GEMMs (0: the kernels' 2 s
+// default); set through moe_debug_set_wait_limit_ns.
+unsigned long long gemm_wait_limit_ns();
 // Counts kernel launches issued by the library (process-wide).
 void count_launches(int n);
 

@@ -72,17 +72,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with an explicit suspend-time hint (ns): the thread is suspended at
+// most about that long before the test returns (the plain form's limit is the
+// system's own and may outlast a short wait limit).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n selp.b32 %0, 1, 0, P;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this (set for tests of the failure path) use the hinted test.
+constexpr unsigned long long kShortWaitNs = 1000000ull;
+
 // Wait until the phase with the given parity has completed.  Gives up when
-// *abort is raised by another warp or after kWaitLimitNs; then raises *abort
+// *abort is raised by another warp or after limit_ns; then raises *abort
 // itself and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns < kShortWaitNs) {
+    // short limits (tests of the failure path): short suspensions, the clock
+    // read after every unsuccessful test
+    const unsigned long long ts = global_timer_ns();
+    for (;;) {
+      if (mbar_try_wait_hint(bar, parity, 100u)) return true;
+      if (*abort) return false;
+      if (global_timer_ns() - ts > limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }
@@ -354,14 +384,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 // mbar_wait for a barrier that the peer CTA also arrives on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((n & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }
