@@ -163,7 +163,9 @@ struct GemmCfg {
   // few stages).
   static constexpr int WGRAD_BUFS = WIDE_K ? 2 : 4;
   static constexpr int STAGING_BUFS = (S == Sched::kRoutedK && TMA_OUT) ? WGRAD_BUFS
-                                      : (EP == Epi::kSwigluBwd) ? 2    // gate and up chunks side by side
+                                      // gate and up chunks side by side; one buffer (the up chunk
+                                      // waits in registers) where two would cost the ring a stage
+                                      : (EP == Epi::kSwigluBwd) ? ((MX && BN == 256) ? 1 : 2)
                                       : ((TMA_OUT && RING_IF_TWO < 4) ? 1 : 2);
   static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * 4096 : 0;
   static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES - (MX ? 1024 : 0)) / STAGE_BYTES;
@@ -866,7 +868,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
       if (p.amax_out != nullptr) amax_flush(p.amax_out, hmax, lane);
     }
   } else {  // kSwigluBwd: dz gate and up chunks of each 64 columns in one pass
-    static_assert(C::STAGING_BUFS == 2, "the gate and up chunks are staged side by side");
+    static_assert(C::STAGING_BUFS == 2 || C::STAGING_BUFS == 1, "gate and up chunks: two buffers, or one");
     const int row = ti.m0 + quarter * 32 + lane;
     const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
     const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
@@ -885,6 +887,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         zb[i] = reinterpret_cast<const uint4*>(zrow + p.half_cols + c0)[i];
       }
       st.begin_all();
+      uint32_t up_keep[C::STAGING_BUFS == 1 ? 32 : 1];   // one buffer: the up chunk waits here
       #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[16];
@@ -916,11 +919,24 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         }
         st.put(2 * q, og[0], og[1], og[2], og[3]);
         st.put(2 * q + 1, og[4], og[5], og[6], og[7]);
-        st.put_next(2 * q, ou[0], ou[1], ou[2], ou[3]);
-        st.put_next(2 * q + 1, ou[4], ou[5], ou[6], ou[7]);
+        if constexpr (C::STAGING_BUFS == 2) {
+          st.put_next(2 * q, ou[0], ou[1], ou[2], ou[3]);
+          st.put_next(2 * q + 1, ou[4], ou[5], ou[6], ou[7]);
+        } else {
+          #pragma unroll
+          for (int j = 0; j < 8; ++j) up_keep[8 * q + j] = ou[j];
+        }
       }
       st.flush(tmC, col0 + c0, y);                  // gate chunk (current buffer)
-      st.flush(tmC, p.half_cols + col0 + c0, y);    // up chunk (the next buffer)
+      if constexpr (C::STAGING_BUFS == 1) {
+        st.begin();                                 // the gate chunk's store has read the buffer
+        #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          st.put(2 * q, up_keep[8 * q], up_keep[8 * q + 1], up_keep[8 * q + 2], up_keep[8 * q + 3]);
+          st.put(2 * q + 1, up_keep[8 * q + 4], up_keep[8 * q + 5], up_keep[8 * q + 6], up_keep[8 * q + 7]);
+        }
+      }
+      st.flush(tmC, p.half_cols + col0 + c0, y);    // up chunk (the next buffer, or the same one again)
       if ((c0 & 127) == 64) {                       // one partial <dh, silu(a) b> per 128 columns
         if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * parts + (col0 + c0) / 128] = dg;
         dg = 0.f;

@@ -142,12 +142,19 @@ cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc,
                                                                                       0, st);
 }
 
+#ifndef MOE_MX_DGRAD_FC2_BN
+#define MOE_MX_DGRAD_FC2_BN 256
+#endif
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
                               const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st) {
-  // B_e = W2_e^T [F, H], quantised along H
+  // B_e = W2_e^T [F, H], quantised along H.  256-column tiles where F allows:
+  // one accumulator (256 columns beside the scale columns), 48 KB per k-block
+  // of 128 x 256 x 128 instead of 32 KB per 128 x 128 x 128.
+  const bool wide = MOE_MX_DGRAD_FC2_BN == 256 && F % 256 == 0;
   CUtensorMap ta, tb;
-  if (!make_tmap_u8(&ta, dyq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w2tq, H, static_cast<uint64_t>(E) * F, 128))
+  if (!make_tmap_u8(&ta, dyq, H, rows_alloc, 128) ||
+      !make_tmap_u8(&tb, w2tq, H, static_cast<uint64_t>(E) * F, wide ? 256 : 128))
     return cudaErrorInvalidValue;
   GemmParams p = gemm_params_zero();
   p.poffsets = poffsets;
@@ -171,6 +178,14 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
   p.sfb_tiles_k = H / 128;
   CUtensorMap tc;
   if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
+  if (wide) {
+    p.n_tiles = F / 256;
+    if (poffsets != nullptr)
+      return launch_mx<GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p,
+                                                                                           rows_alloc, dense_rows, st);
+    return launch_mx<GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p, rows_alloc,
+                                                                                        dense_rows, st);
+  }
   if (poffsets != nullptr)
     return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p, rows_alloc,
                                                                                          dense_rows, st);
