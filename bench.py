@@ -441,6 +441,14 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
         api.moe_quantize_mxfp8(t, batch, rows, cols, mode, c, sf)
         return c, sf
 
+    # the MXFP8 layer keeps x and dy in token order (x_perm, dy_perm unwritten):
+    # expert-ordered bf16 copies for the operands here, by the permutation entry point
+    perm = lambda src, dst: api.moe_permute(cfg, src, fl["topk_idx"], fl["topk_gate"], fl["counts"], fl["offsets"],
+                                            po, fl["slot_row"], fl["row_src"], fl["row_gate"], dst, 1, ws)
+    perm(dinp["x"], fl["x_perm"])
+    if w.backward:
+        perm(dinp["dy"], fl["dy_perm"])
+
     xq, xsf = q(fl["x_perm"], 1, cap, H, api.MX_ROWS)
     w1q, w1sf = q(dinp["w1"], E, 2 * F, H, api.MX_ROWS_GATE_UP)
     calls["fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, fl["h"], ws,

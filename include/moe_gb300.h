@@ -406,6 +406,9 @@ moe_status moe_prepare_nvfp4_weights(const moe_config* cfg, const moe_weights* w
  * zeroes the padding rows.  Fixed number of launches; no host sync.
  * NVFP4 layers: with_backward must be 0 (MOE_ERR_UNSUPPORTED otherwise); x is
  * quantised per token and its codes permuted, so x_perm is left unwritten.
+ * MXFP8 layers likewise permute x's quantised codes and leave x_perm (and, in
+ * the backward, dy_perm) unwritten: their weight gradients and the router's
+ * read x and dy through row_src. 
  * The backward calls return MOE_ERR_UNSUPPORTED for NVFP4 layers. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, void* act,
                              size_t act_bytes, int32_t with_backward, void* ws, size_t ws_bytes, void* stream);

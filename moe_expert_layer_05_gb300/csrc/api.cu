@@ -698,9 +698,12 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   MOE_TRY(launch_topk_permute_maps(logits, cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr, T, E, k,
                                    cfg->score, idx, gate, hist_ptr(ws), counts, at<int32_t>(act, L.offsets), poff,
                                    slot_row, at<int32_t>(act, L.row_src), row_gate, st));
-  // (NVFP4 layers permute the quantised codes instead; x_perm stays unwritten)
-  if (cfg->dtype != MOE_GEMM_NVFP4) MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
-  if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
+  // (MXFP8 and NVFP4 layers permute the quantised codes instead and read x
+  // through row_src where its rows are needed again; x_perm stays unwritten)
+  if (cfg->dtype == MOE_GEMM_BF16) {
+    MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
+    if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
+  }
   // 5-6: grouped expert GEMMs; the gate multiplies the SwiGLU output inside fc1
   void* z = with_backward ? at<void>(act, L.z) : nullptr;
   void* zs = with_backward && S > 0 ? at<void>(act, L.zs) : nullptr;
@@ -830,8 +833,10 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
   void* dx_perm = at<void>(act, L.dx_perm);
   float* dpart = at<float>(act, L.dgate_part);
 
-  MOE_TRY(launch_gather_rows(dy, slot_row, T, k, H, dy_perm, st));
-  MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, dy_perm, st));
+  if (cfg->dtype == MOE_GEMM_BF16) {
+    MOE_TRY(launch_gather_rows(dy, slot_row, T, k, H, dy_perm, st));
+    MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, dy_perm, st));
+  }
   const void* dxs = nullptr;
   if (cfg->dtype == MOE_GEMM_MXFP8) {
     const MxWs M = mx_ws_layout(cfg);
@@ -899,10 +904,12 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     char* mb = static_cast<char*>(ws) + mx_ws_base(cfg);
     auto q = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.q); };
     auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
+    // x and dy in expert order are read straight from token order through row_src
+    const int32_t* row_src = at<int32_t>(act, L.row_src);
     MOE_TRY(launch_quantize_cols(at<void>(act, L.dz), 1, cap, 2 * F, q(M.dzT), f(M.dzT), st));
-    MOE_TRY(launch_quantize_cols(at<void>(act, L.x_perm), 1, cap, H, q(M.xT), f(M.xT), st));
+    MOE_TRY(launch_quantize_cols_gather(x, T, row_src, cap, H, q(M.xT), f(M.xT), st));
     MOE_TRY(gemm_mx_wgrad(q(M.dzT), f(M.dzT), 2 * F, q(M.xT), f(M.xT), H, cap, E, poff, 0, g->dw1, status, st));
-    MOE_TRY(launch_quantize_cols(at<void>(act, L.dy_perm), 1, cap, H, q(M.dyT), f(M.dyT), st));
+    MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st));
     MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st));
     MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, q(M.hT), f(M.hT), F, cap, E, poff, 0, g->dw2, status, st));
     if (S > 0 && T > 0) {
@@ -923,8 +930,12 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
       MOE_TRY(gemm_wgrad(dy, H, at<void>(act, L.hs), S, T, 1, nullptr, T, g->dw2_shared, status, st));
     }
   }
-  MOE_TRY(launch_router_wgrad(at<void>(act, L.x_perm), at<float>(act, L.row_dlogit), counts, poff, E, H,
-                              g->dw_router, st));
+  if (cfg->dtype == MOE_GEMM_MXFP8)
+    MOE_TRY(launch_router_wgrad(x, at<int32_t>(act, L.row_src), at<float>(act, L.row_dlogit), counts, poff, E, H,
+                                g->dw_router, st));
+  else
+    MOE_TRY(launch_router_wgrad(at<void>(act, L.x_perm), nullptr, at<float>(act, L.row_dlogit), counts, poff, E, H,
+                                g->dw_router, st));
   if (S > 0 && T == 0) {
     MOE_TRY(cudaMemsetAsync(g->dw1_shared, 0, sizeof(float) * 2 * S * H, st));
     MOE_TRY(cudaMemsetAsync(g->dw2_shared, 0, sizeof(float) * S * H, st));

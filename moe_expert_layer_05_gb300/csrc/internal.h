@@ -47,9 +47,11 @@ cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, c
                                  int n_part, const void* w_router, const void* dx_shared, int T, int E, int k,
                                  int H, int score, void* dx, float* dgate, float* dlogits, float* row_dlogit,
                                  cudaStream_t st);
-// dWr[e] = sum over expert e's rows of row_dlogit[r] * x_perm[r]  (fp32)
-cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, const int32_t* counts,
-                                const int32_t* poffsets, int E, int H, float* dw_router, cudaStream_t st);
+// dWr[e] = sum over expert e's rows of row_dlogit[r] * x_perm[r]  (fp32);
+// with row_src given, x_perm is x in token order, read through row_src.
+cudaError_t launch_router_wgrad(const void* x_perm, const int32_t* row_src, const float* row_dlogit,
+                                const int32_t* counts, const int32_t* poffsets, int E, int H, float* dw_router,
+                                cudaStream_t st);
 
 // ------------------------------------------------------------ GEMMs (gemm_*.cu)
 // logits[T,E] (fp32) = x[T,H] * Wr[E,H]^T
@@ -106,6 +108,10 @@ cudaError_t launch_zero_pad_rows_mx(const int32_t* counts, const int32_t* poffse
 // Column mode: batch x [rows, cols] -> batch x [cols, rows], blocks along rows.
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
                                  cudaStream_t st);
+// Column mode on rows gathered through row_map: row r of the [rows, cols]
+// input is src row row_map[r] (a zero row where it is outside [0, src_rows)).
+cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
+                                        uint8_t* codes, uint8_t* sf, cudaStream_t st);
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
                         void* z, int* status, cudaStream_t st);

@@ -115,8 +115,12 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // so their 32-byte pieces of one output row form a full 128-byte line.
 // Shared memory: element (r, c) in 16-byte chunk (c / 8) ^ (r / 32) of row r,
 // so the four row blocks read by one warp fall in different banks.
+// row_map (nullable, batch 1 only): input row r is src row row_map[r], or a
+// zero row where row_map[r] is outside [0, src_rows) -- the expert-ordered
+// rows read straight from token order through row_src, padding rows zero.
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
-                                                            int cols, uint8_t* __restrict__ codes,
+                                                            int cols, const int32_t* __restrict__ row_map,
+                                                            int src_rows, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf) {
   __shared__ uint4 tile[128][8];           // 128 rows x 64 bf16
   const int rb = blockIdx.x;               // block of 128 input rows
@@ -127,7 +131,16 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   for (int k = 0; k < 4; ++k) {
     const int i = threadIdx.x + 256 * k;   // 16-byte piece i: row i / 8, chunk i % 8
     const int r = i >> 3, j = i & 7;
-    tile[r][j ^ (r >> 5)] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * cols) + j);
+    uint4 v;
+    if (row_map != nullptr) {
+      const int t = row_map[rb * 128 + r];
+      v = (t >= 0 && t < src_rows)
+              ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(t) * cols + c0) + j)
+              : make_uint4(0, 0, 0, 0);
+    } else {
+      v = __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * cols) + j);
+    }
+    tile[r][j ^ (r >> 5)] = v;
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -207,7 +220,18 @@ cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols,
                                  cudaStream_t st) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
   dim3 grid(rows / 128, cols / 64, batch);   // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
-  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, sf);
+  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, nullptr, 0, codes,
+                                             sf);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
+                                        uint8_t* codes, uint8_t* sf, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  dim3 grid(rows / 128, cols / 64, 1);
+  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, row_map, src_rows,
+                                             codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }

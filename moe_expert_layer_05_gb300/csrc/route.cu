@@ -559,7 +559,10 @@ __global__ void __launch_bounds__(128) dgrad_combine_kernel(
 }
 
 // dWr[e] = sum over the rows r of expert e of dl_r * x_perm[r]: grid (E, H/256).
+// With row_src given, x_perm is x in token order and row r of expert e is
+// x[row_src[r]] (the expert-ordered copy need not exist).
 __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint4* __restrict__ x_perm,
+                                                           const int32_t* __restrict__ row_src,
                                                            const float* __restrict__ row_dlogit,
                                                            const int32_t* __restrict__ counts,
                                                            const int32_t* __restrict__ poffsets, int vec_per_row,
@@ -574,7 +577,9 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint4* __restri
   const bool active = v < vec_per_row;
   const int r0 = poffsets[e], n = counts[e];
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const uint4* xcol = x_perm + (long long)r0 * vec_per_row + v;
+  const uint4* xcol = x_perm + (row_src != nullptr ? 0 : (long long)r0 * vec_per_row) + v;
+  // row index within x_perm's view: the expert's row, or its token
+  auto xrow = [&](int rr) -> long long { return row_src != nullptr ? (long long)__ldg(row_src + r0 + rr) : rr; };
   int r = warp;
   if (active) {
     for (; r + 24 < n; r += 32) {
@@ -582,7 +587,7 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint4* __restri
       float d[4];
       #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        xv[u] = __ldg(xcol + (long long)(r + 8 * u) * vec_per_row);
+        xv[u] = __ldg(xcol + xrow(r + 8 * u) * vec_per_row);
         d[u] = __ldg(row_dlogit + r0 + r + 8 * u);
       }
       #pragma unroll
@@ -594,7 +599,7 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint4* __restri
       }
     }
     for (; r < n; r += 8) {
-      const uint4 xv = __ldg(xcol + (long long)r * vec_per_row);
+      const uint4 xv = __ldg(xcol + xrow(r) * vec_per_row);
       const float d = __ldg(row_dlogit + r0 + r);
       acc[0] += d * bf16_lo(xv.x); acc[1] += d * bf16_hi(xv.x);
       acc[2] += d * bf16_lo(xv.y); acc[3] += d * bf16_hi(xv.y);
@@ -714,12 +719,13 @@ cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_wgrad(const void* x_perm, const float* row_dlogit, const int32_t* counts,
-                                const int32_t* poffsets, int E, int H, float* dw_router, cudaStream_t st) {
+cudaError_t launch_router_wgrad(const void* x_perm, const int32_t* row_src, const float* row_dlogit,
+                                const int32_t* counts, const int32_t* poffsets, int E, int H, float* dw_router,
+                                cudaStream_t st) {
   const int vpr = H / 8;
   dim3 grid(E, (vpr + 31) / 32);
-  router_wgrad_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x_perm), row_dlogit, counts, poffsets, vpr,
-                                            dw_router);
+  router_wgrad_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x_perm), row_src, row_dlogit, counts, poffsets,
+                                            vpr, dw_router);
   count_launches(1);
   return cudaGetLastError();
 }

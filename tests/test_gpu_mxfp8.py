@@ -351,7 +351,7 @@ def test_mx_full_size_training_sampled(lib):
     torch.cuda.synchronize()
     assert api.moe_read_device_status(layer.ws) == 0
     fl = layer.fields()
-    check_full_permutation(w, fl, dinp["x"])
+    check_full_permutation(w, fl, dinp["x"], rows=False)
     counts, po, src = i64(fl["counts"]), i64(fl["poffsets"]), i64(fl["row_src"])
     idx_gpu = i64(fl["topk_idx"])
     x64, dy64 = f64(dinp["x"]), f64(dinp["dy"])
