@@ -437,7 +437,7 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
 
     def q(t, batch, rows, cols, mode):
         c = torch.empty(batch * rows * cols, dtype=torch.uint8, device=dev)
-        sf = torch.empty(batch * rows * cols // 32, dtype=torch.uint8, device=dev)
+        sf = torch.empty(batch * rows * cols // 28 + 512, dtype=torch.uint8, device=dev)   # room for G224 layouts
         api.moe_quantize_mxfp8(t, batch, rows, cols, mode, c, sf)
         return c, sf
 
@@ -456,8 +456,11 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
                                                 poffsets=po, a_scales=xsf, b_scales=w1sf)
     hq, hsf = q(fl["h"], 1, cap, F, api.MX_ROWS)
     w2q, w2sf = q(dinp["w2"], 1, E * H, F, api.MX_ROWS)
-    calls["fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, hq, w2q, fl["o"], ws, poffsets=po, a_scales=hsf,
-                                                b_scales=w2sf)
+    # the layer runs fc2 and the fc1 data gradient on 256 x 224 tiles where H allows (B scales grouped by 224)
+    g224 = 224 if H % 224 == 0 else 0
+    w2g, w2gsf = q(dinp["w2"], 1, E * H, F, api.MX_ROWS_G224) if g224 else (w2q, w2sf)
+    calls["fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC2, hq, w2g, fl["o"], ws, poffsets=po, a_scales=hsf,
+                                                b_scales=w2gsf, b_scale_group=g224)
     if H % 256 == 0:
         y_c = torch.empty((w.T, H), dtype=torch.bfloat16, device=dev)
         sh = layer.view("os", torch.bfloat16, (w.T, H)) if w.S else None
@@ -472,9 +475,10 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
                                                           aux=fl["z"], row_gate=fl["row_gate"], dgate_part=dpart,
                                                           poffsets=po, a_scales=dysf, b_scales=w2tsf)
         dzq, dzsf = q(fl["dz"], 1, cap, 2 * F, api.MX_ROWS)
-        w1tq, w1tsf = q(dinp["w1"], E, 2 * F, H, api.MX_COLS_T)
+        w1tq, w1tsf = q(dinp["w1"], E, 2 * F, H, api.MX_COLS_T_G224 if g224 else api.MX_COLS_T)
         calls["dgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC1, dzq, w1tq, fl["dx_perm"], ws,
-                                                          poffsets=po, a_scales=dzsf, b_scales=w1tsf)
+                                                          poffsets=po, a_scales=dzsf, b_scales=w1tsf,
+                                                          b_scale_group=g224)
         dzt, dztsf = q(fl["dz"], 1, cap, 2 * F, api.MX_COLS_T)
         xt, xtsf = q(fl["x_perm"], 1, cap, H, api.MX_COLS_T)
         calls["wgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, dzt, xt, grads["dw1"], ws,

@@ -280,9 +280,11 @@ typedef enum {
  * contraction: a and b are codes and a_scales / b_scales their scale tiles.
  *   FC1_SWIGLU: a = x_perm [cap,H]; b = W1 rows gate/up interleaved
  *               (MOE_MX_ROWS_GATE_UP of w1 [E,2F,H]).
- *   FC2:        a = h [cap,F]; b = W2 [E*H,F] (MOE_MX_ROWS).
+ *   FC2:        a = h [cap,F]; b = W2 [E*H,F] (MOE_MX_ROWS, or MOE_MX_ROWS_G224 with
+ *               b_scale_group = 224).
  *   DGRAD_FC2:  a = dy_perm [cap,H]; b = W2^T [E,F,H] (MOE_MX_COLS_T of w2); aux = z (bf16).
- *   DGRAD_FC1:  a = dz [cap,2F]; b = W1^T [E,H,2F] (MOE_MX_COLS_T of w1).
+ *   DGRAD_FC1:  a = dz [cap,2F]; b = W1^T [E,H,2F] (MOE_MX_COLS_T of w1, or MOE_MX_COLS_T_G224
+ *               with b_scale_group = 224).
  *   WGRAD_FC1:  a = dz^T [2F,cap], b = x_perm^T [H,cap] (MOE_MX_COLS_T).
  *   WGRAD_FC2:  a = dy_perm^T [H,cap], b = h^T [F,cap] (MOE_MX_COLS_T).
  * Dense calls need dense_rows % 128 == 0.
@@ -310,6 +312,9 @@ typedef struct {
   const float* b_amax;    /* NVFP4 only */
   const int32_t* a_rows;  /* FC1_SWIGLU_GATHERED, FC2_COMBINE */
   const int32_t* slot_row;/* FC2_COMBINE only */
+  int32_t b_scale_group;  /* MXFP8 FC2 / DGRAD_FC1 (routed, H % 224 == 0): 224 when b's scales
+                             were written by MOE_MX_ROWS_G224 / MOE_MX_COLS_T_G224 (the GEMM then
+                             runs 256 x 224 tiles); 0 (or 128) otherwise and for every other op */
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For
@@ -343,14 +348,23 @@ typedef enum {
   MOE_MX_ROWS = 0,          /* src [batch*rows, cols] -> codes [batch*rows, cols], blocks along each row */
   MOE_MX_COLS_T = 1,        /* src batch x [rows, cols] -> codes batch x [cols, rows], blocks along rows
                                (each matrix transposed; scale tiles per matrix) */
-  MOE_MX_ROWS_GATE_UP = 2   /* as ROWS, rows of every [gate; up] matrix of `rows` rows reordered as
+  MOE_MX_ROWS_GATE_UP = 2,  /* as ROWS, rows of every [gate; up] matrix of `rows` rows reordered as
                                gate 0..127, up 0..127, gate 128..255, up 128..255, ... (fc1 weights;
                                rows % 256 == 0) */
+  MOE_MX_ROWS_G224 = 3,     /* as ROWS, codes identical, but the scale tiles take the rows in groups
+                               of 224: group g's rows 0..127 are tile row 2g, its rows 128..223 the
+                               first 96 rows of tile row 2g+1 (the other 32 rows of that tile are
+                               never written nor read); batch*rows % 224 == 0.  For the B operand of
+                               the 256 x 224 GEMM tiles (moe_gemm_args.b_scale_group). */
+  MOE_MX_COLS_T_G224 = 4    /* as COLS_T with the output rows (the input columns) grouped by 224 the
+                               same way, per matrix; cols % 224 == 0 */
 } moe_mx_mode;
 
 /* Quantise a bf16 tensor to MXFP8.  codes: batch*rows*cols bytes; scales:
- * batch*rows*cols/32 bytes.  cols % 128 == 0; ROWS: batch*rows % 128 == 0;
- * COLS_T: rows % 128 == 0; ROWS_GATE_UP: rows % 256 == 0. */
+ * batch*rows*cols/32 bytes (the G224 modes: 8/7 of that, R/224 * 2 tile rows
+ * for R grouped rows).  cols % 128 == 0; ROWS: batch*rows % 128 == 0;
+ * COLS_T: rows % 128 == 0; ROWS_GATE_UP: rows % 256 == 0; ROWS_G224:
+ * batch*rows % 224 == 0; COLS_T_G224: rows % 128 == 0, cols % 224 == 0. */
 moe_status moe_quantize_mxfp8(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t mode,
                               uint8_t* codes, uint8_t* scales, void* stream);
 

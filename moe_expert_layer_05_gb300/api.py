@@ -21,7 +21,7 @@ GEMM_DTYPE = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
 
 (GG_FC1_SWIGLU, GG_FC2, GG_DGRAD_FC2, GG_DGRAD_FC1, GG_WGRAD_FC1, GG_WGRAD_FC2, GG_FC1_SWIGLU_GATHERED,
  GG_FC2_COMBINE) = range(8)
-MX_ROWS, MX_COLS_T, MX_ROWS_GATE_UP = range(3)
+MX_ROWS, MX_COLS_T, MX_ROWS_GATE_UP, MX_ROWS_G224, MX_COLS_T_G224 = range(5)
 
 c_i32 = ctypes.c_int32
 c_vp = ctypes.c_void_p
@@ -55,7 +55,7 @@ class MoeGemmArgs(ctypes.Structure):
     _fields_ = [("op", c_i32), ("dense_rows", c_i32), ("a", c_vp), ("b", c_vp), ("c", c_vp), ("c2", c_vp),
                 ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp),
                 ("a_scales", c_vp), ("b_scales", c_vp), ("a_amax", c_vp), ("b_amax", c_vp), ("a_rows", c_vp),
-                ("slot_row", c_vp)]
+                ("slot_row", c_vp), ("b_scale_group", c_i32)]
 
 
 _P = ctypes.POINTER
@@ -208,10 +208,10 @@ def moe_permute_noalloc(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, 
 
 def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
                      dense_rows=0, a_scales=None, b_scales=None, a_amax=None, b_amax=None, a_rows=None,
-                     slot_row=None, stream=None) -> None:
+                     slot_row=None, b_scale_group=0, stream=None) -> None:
     args = MoeGemmArgs(op, dense_rows, ptr(a), ptr(b), ptr(c), ptr(c2), ptr(aux), ptr(row_gate), ptr(dgate_part),
                        ptr(poffsets), ptr(a_scales), ptr(b_scales), ptr(a_amax), ptr(b_amax), ptr(a_rows),
-                       ptr(slot_row))
+                       ptr(slot_row), int(b_scale_group))
     check(load().moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), ptr(ws), stream_ptr(stream)),
           "moe_grouped_gemm")
 

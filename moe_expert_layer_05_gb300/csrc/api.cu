@@ -219,24 +219,31 @@ struct MxW {
   size_t total = 0;
 };
 
+// The routed fc2 and fc1 data gradient (N = H) run on 256 x 224 tiles when H
+// allows: their B operands (W2, W1^T) then keep scale tiles per 224 rows.
+// (The fused fc2 + combine keeps 256-wide tiles and W2's 128-row tiles.)
+bool mx_b224(const moe_config* c) { return c->H % 224 == 0 && !kFuseCombine; }
+
 MxW mx_weight_layout(const moe_config* c) {
   MxW m;
   const size_t H = c->H, E = c->E, F = c->F, S = c->S;
+  const int g = mx_b224(c) ? kMxScaleGroup224 : 128;
   size_t off = 0;
-  auto buf = [&](size_t elems) {
+  auto buf = [&](size_t elems, size_t sf_bytes) {
     MxBuf b;
     b.q = off;
     off = align_up(off + elems);
     b.sf = off;
-    off = align_up(off + elems / 32);
+    off = align_up(off + sf_bytes);
     return b;
   };
-  m.w1 = buf(E * 2 * F * H);    // [E*2F, H], gate/up interleaved in 128-row blocks (fc1)
-  m.w2 = buf(E * H * F);        // [E*H, F]  (fc2)
-  m.w1t = buf(E * H * 2 * F);   // [E, H, 2F] = W1_e^T, blocks along 2F (fc1 dgrad)
-  m.w2t = buf(E * F * H);       // [E, F, H]  = W2_e^T, blocks along H  (fc2 dgrad)
+  m.w1 = buf(E * 2 * F * H, E * 2 * F * H / 32);                 // [E*2F, H], gate/up interleaved (fc1)
+  m.w2 = buf(E * H * F, mx_scale_bytes(E * H, F, g));            // [E*H, F]  (fc2)
+  m.w1t = buf(E * H * 2 * F, E * mx_scale_bytes(H, 2 * F, g));   // [E, H, 2F] = W1_e^T, blocks along 2F (fc1 dgrad)
+  m.w2t = buf(E * F * H, E * F * H / 32);                       // [E, F, H] = W2_e^T, blocks along H (fc2 dgrad)
   if (S) {
-    m.s1 = buf(2 * S * H); m.s2 = buf(H * S); m.s1t = buf(H * 2 * S); m.s2t = buf(S * H);
+    m.s1 = buf(2 * S * H, 2 * S * H / 32); m.s2 = buf(H * S, H * S / 32);
+    m.s1t = buf(H * 2 * S, H * 2 * S / 32); m.s2t = buf(S * H, S * H / 32);
   }
   m.total = off;
   return m;
@@ -352,10 +359,16 @@ moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool d
   }
   if (cfg->dtype == MOE_GEMM_BF16) {
     if (a->op == MOE_GG_FC1_SWIGLU_GATHERED && (dense || !dev_ptr_ok(a->a_rows))) return MOE_ERR_INVALID_ARG;
-    return MOE_OK;
+    return (a->b_scale_group == 0 || a->b_scale_group == 128) ? MOE_OK : MOE_ERR_INVALID_ARG;
   }
   if (a->op == MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;     // bf16 only
   if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
+  // B's scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1, routed, H % 224 == 0
+  if (a->b_scale_group != 0 && a->b_scale_group != 128) {
+    if (a->b_scale_group != kMxScaleGroup224 || cfg->dtype != MOE_GEMM_MXFP8 || dense || cfg->H % 224 != 0 ||
+        (a->op != MOE_GG_FC2 && a->op != MOE_GG_DGRAD_FC1))
+      return MOE_ERR_INVALID_ARG;
+  }
   if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->dtype == MOE_GEMM_NVFP4) {
     if (!f32_ptr_ok(a->a_amax) || !f32_ptr_ok(a->b_amax)) return MOE_ERR_INVALID_ARG;
@@ -409,21 +422,30 @@ moe_status moe_quantize_mxfp8(const void* src, int32_t batch, int32_t rows, int3
   if (n == 0) return MOE_OK;
   if (!dev_ptr_ok(src) || !dev_ptr_ok(codes) || !dev_ptr_ok(scales)) return MOE_ERR_INVALID_ARG;
   if (cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  const long long R = static_cast<long long>(batch) * rows;
+  bool shape_ok = false;
+  switch (mode) {
+    case MOE_MX_ROWS: shape_ok = R % 128 == 0; break;
+    case MOE_MX_ROWS_GATE_UP: shape_ok = rows % 256 == 0; break;
+    case MOE_MX_COLS_T: shape_ok = rows % 128 == 0; break;
+    case MOE_MX_ROWS_G224: shape_ok = R % 224 == 0; break;
+    case MOE_MX_COLS_T_G224: shape_ok = rows % 128 == 0 && cols % 224 == 0; break;
+    default: break;
+  }
+  if (!shape_ok) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (moe_status s = check_device(); s != MOE_OK) return s;
   switch (mode) {
     case MOE_MX_ROWS:
-      if ((static_cast<long long>(batch) * rows) % 128 != 0) return MOE_ERR_INVALID_ARG;
-      return cuda_status(launch_quantize_rows(src, static_cast<long long>(batch) * rows, cols, 0, codes, scales, st));
+      return cuda_status(launch_quantize_rows(src, R, cols, 0, codes, scales, st));
     case MOE_MX_ROWS_GATE_UP:
-      if (rows % 256 != 0) return MOE_ERR_INVALID_ARG;
-      return cuda_status(
-          launch_quantize_rows(src, static_cast<long long>(batch) * rows, cols, rows / 2, codes, scales, st));
+      return cuda_status(launch_quantize_rows(src, R, cols, rows / 2, codes, scales, st));
     case MOE_MX_COLS_T:
-      if (rows % 128 != 0) return MOE_ERR_INVALID_ARG;
       return cuda_status(launch_quantize_cols(src, batch, rows, cols, codes, scales, st));
-    default:
-      return MOE_ERR_INVALID_ARG;
+    case MOE_MX_ROWS_G224:
+      return cuda_status(launch_quantize_rows(src, R, cols, 0, codes, scales, st, kMxScaleGroup224));
+    default:   // MOE_MX_COLS_T_G224
+      return cuda_status(launch_quantize_cols(src, batch, rows, cols, codes, scales, st, kMxScaleGroup224));
   }
 }
 
@@ -440,8 +462,9 @@ moe_status moe_prepare_mxfp8_weights(const moe_config* cfg, const moe_weights* w
   auto q = [&](const MxBuf& b) { return at<uint8_t>(mx, b.q); };
   auto f = [&](const MxBuf& b) { return at<uint8_t>(mx, b.sf); };
   MOE_TRY(launch_quantize_rows(w->w1, static_cast<long long>(E) * 2 * F, H, F, q(L.w1), f(L.w1), st));
-  MOE_TRY(launch_quantize_rows(w->w2, static_cast<long long>(E) * H, F, 0, q(L.w2), f(L.w2), st));
-  MOE_TRY(launch_quantize_cols(w->w1, E, 2 * F, H, q(L.w1t), f(L.w1t), st));
+  const int g = mx_b224(cfg) ? kMxScaleGroup224 : 128;
+  MOE_TRY(launch_quantize_rows(w->w2, static_cast<long long>(E) * H, F, 0, q(L.w2), f(L.w2), st, g));
+  MOE_TRY(launch_quantize_cols(w->w1, E, 2 * F, H, q(L.w1t), f(L.w1t), st, g));
   MOE_TRY(launch_quantize_cols(w->w2, E, H, F, q(L.w2t), f(L.w2t), st));
   if (S > 0) {
     MOE_TRY(launch_quantize_rows(w->w1_shared, 2 * S, H, S, q(L.s1), f(L.s1), st));
@@ -604,7 +627,7 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
                                        a->row_gate, a->c, a->c2, status, st));
       case MOE_GG_FC2:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->dense_rows,
-                                           a->c, status, st));
+                                           a->c, status, st, a->b_scale_group == 0 ? 128 : a->b_scale_group));
       case MOE_GG_FC2_COMBINE:
         return cuda_status(gemm_mx_fc2_combine(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->c,
                                                combine_args(cfg, a, ws), status, st));
@@ -614,7 +637,8 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
                                              a->aux, a->row_gate, a->c, a->dgate_part, status, st));
       case MOE_GG_DGRAD_FC1:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, 2 * F, a->b, a->b_scales, E, H, po,
-                                           a->dense_rows, a->c, status, st));
+                                           a->dense_rows, a->c, status, st,
+                                           a->b_scale_group == 0 ? 128 : a->b_scale_group));
       case MOE_GG_WGRAD_FC1:
         return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, 2 * F, a->b, a->b_scales, H, rows, E, po, a->dense_rows,
                                          static_cast<float*>(a->c), status, st));
@@ -788,7 +812,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
       MOE_TRY(gemm_mx_fc2_combine(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, o, cmb, status, st));
       return MOE_OK;
     }
-    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st));
+    MOE_TRY(gemm_mx_nt_bf16(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, 0, o, status, st,
+                            mx_b224(cfg) ? kMxScaleGroup224 : 128));
   } else {
     if (S > 0 && T > 0) {
       MOE_TRY(gemm_fc1(x, T, H, w->w1_shared, 1, S, nullptr, T, nullptr, at<void>(act, L.hs), zs, status, st));
@@ -852,7 +877,8 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
     MOE_TRY(gemm_mx_dgrad_fc2(q(M.dy), f(M.dy), cap, H, wq(W.w2t), wf(W.w2t), E, F, poff, 0, at<void>(act, L.z),
                               at<float>(act, L.row_gate), dz, dpart, status, st));
     MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st));
-    MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st));
+    MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st,
+                            mx_b224(cfg) ? kMxScaleGroup224 : 128));
     if (S > 0 && T > 0) {
       MOE_TRY(gemm_mx_dgrad_fc2(q(M.dys), f(M.dys), T, H, wq(W.s2t), wf(W.s2t), 1, S, nullptr, T, at<void>(act, L.zs),
                                 nullptr, at<void>(act, L.dzs), nullptr, status, st));

@@ -135,8 +135,14 @@ struct GemmCfg {
   // scale tiles of one k-block: one 512-byte tile per 128 rows (MXFP8), four
   // (one per MMA of K = 64) for NVFP4
   static constexpr int SF_TILES_KB = NV4 ? 4 : 1;
-  static constexpr int SFA_BYTES = MX ? 512 * SF_TILES_KB : 0;
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 * SF_TILES_KB : 0;
+  // scale tiles of A (one per 128 rows of the tile) and of B (one per 128
+  // rows, rounded up: a 224-row B tile takes two, from the layout that groups
+  // B's rows by 224 -- the tile's rows 128..223 fill 96 rows of the second)
+  static constexpr int SFA_TILES = M256 ? 2 : 1;
+  static constexpr int SFB_TILES = (BN + 127) / 128;
+  static constexpr int SFB_GROUP = (MX && BN % 128 != 0) ? BN : 128;
+  static constexpr int SFA_BYTES = MX ? 512 * SF_TILES_KB * SFA_TILES : 0;
+  static constexpr int SFB_BYTES = MX ? SFB_TILES * 512 * SF_TILES_KB : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   // Outputs leave through TMA stores staged in shared memory (every epilogue
   // but the router's narrow fp32 logits, whose rows need not be 16-byte sized).
@@ -176,7 +182,7 @@ struct GemmCfg {
   static constexpr int SMEM_USED = STAGES * (A_BYTES + B_BYTES) + SF_REGION + STAGING_BYTES + BOOK_BYTES;
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 <= 232448) ? SMEM_USED + 1024 : 232448;
   // TMEM columns of one stage's scales (4 per 128 rows and scale tile)
-  static constexpr int SF_COLS = MX ? SF_TILES_KB * (4 + 4 * (BN / 128)) : 0;
+  static constexpr int SF_COLS = MX ? SF_TILES_KB * 4 * (SFA_TILES + SFB_TILES) : 0;
   // TMEM accumulators: two (epilogue of tile i overlaps MMAs of tile i+1),
   // or one where two would not fit next to the scales (MXFP8, N=256) or in
   // 512 columns at all (256-row tiles of N=256: 2 x 256 columns per tile).
@@ -197,11 +203,13 @@ struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N of one MMA");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column chunks");
   static_assert(EP != Epi::kSwiglu || BN == 256, "SwiGLU tile: 128 gate + 128 matching up columns");
-  static_assert(!MX || (BN % 128 == 0 && !A_MN && !B_MN), "MXFP8 operands are K-major, 128-row scale tiles");
+  static_assert(!MX || ((BN % 128 == 0 || (BN == 224 && M256)) && !A_MN && !B_MN),
+                "MXFP8 operands are K-major, 128-row scale tiles (224-row B tiles: 256 x 224 tiles)");
   static_assert(!NV4 || (S != Sched::kRoutedK && EP != Epi::kSwigluBwd && EP != Epi::kStoreF32),
                 "NVFP4: forward GEMMs (bf16 or SwiGLU epilogue)");
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
-  static_assert(!M256 || (!MX && !A_MN && S != Sched::kRoutedK), "256-row tiles: K-major bf16 A, row-grouped");
+  static_assert(!M256 || ((!MX || (!NV4 && BN == 224 && EP == Epi::kStoreBf16)) && !A_MN && S != Sched::kRoutedK),
+                "256-row tiles: K-major A, row-grouped; MXFP8 ones 256 x 224 with bf16 stores");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
   static_assert(!GATHER || (M256 && !MX && !A_MN && S == Sched::kRoutedM && BK == 64),
                 "gathered A: bf16 256-row row-grouped tiles");
@@ -342,9 +350,19 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
     constexpr int TB = 512 * C::SF_TILES_KB;
     const int kt = k_col / (C::NV4 ? 64 : 128);
     bulk_load(sf_dst, p.sfa + ((long long)(a_row / 128) * p.sfa_tiles_k + kt) * 512, TB, bar);
+    if constexpr (C::SFA_TILES == 2) {
+      // rows 128..255 of a 256-row tile; a tile without them (the last of an
+      // expert with an odd number of 128-row blocks) loads its first tile again,
+      // so the byte count stays fixed and nothing past the buffer is read
+      const int a_tile1 = a_row / 128 + (ti.half1 ? 1 : 0);
+      bulk_load(sf_dst + TB, p.sfa + ((long long)a_tile1 * p.sfa_tiles_k + kt) * 512, TB, bar);
+    }
+    // B rows grouped by SFB_GROUP (128: one tile per 128 rows; 224: two tiles a group)
+    const int b_tile0 = (C::SFB_GROUP == 128) ? b_row / 128 : (b_row / C::SFB_GROUP) * C::SFB_TILES;
     #pragma unroll
-    for (int i = 0; i < C::BN / 128; ++i)
-      bulk_load(sf_dst + TB * (i + 1), p.sfb + ((long long)(b_row / 128 + i) * p.sfb_tiles_k + kt) * 512, TB, bar);
+    for (int i = 0; i < C::SFB_TILES; ++i)
+      bulk_load(sf_dst + TB * (C::SFA_TILES + i), p.sfb + ((long long)(b_tile0 + i) * p.sfb_tiles_k + kt) * 512, TB,
+                bar);
     return;
   }
   // ---- A (gathered tiles: the producer warp copies A itself)
@@ -427,6 +445,12 @@ struct Stager {
   __device__ __forceinline__ void put(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
     const uint32_t base = smem_u32(buf + cur * 4096);
     st_shared_v4(base + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, cc, d);
+  }
+  // 16-byte chunk c of this lane's row in a buffer of 64-byte rows without
+  // swizzle (for a 32-column bf16 box)
+  __device__ __forceinline__ void put_rows64(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
+    const uint32_t base = smem_u32(buf + cur * 4096);
+    st_shared_v4(base + lane * 64 + (c << 4), a, b, cc, d);
   }
   // into the buffer after the current one (two buffers filled in one pass)
   __device__ __forceinline__ void put_next(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
@@ -615,6 +639,50 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     }
   } else if constexpr (C::EP == Epi::kStoreBf16) {
     const int y = ti.m0 + quarter * 32;
+    if constexpr (C::BN == 224) {
+      // 256 x 224 tiles (one accumulator): this row's 224 outputs as bf16 pairs
+      // in registers, the accumulator handed back, then three 64-column stores
+      // through the swizzled staging and the last 32 columns through tmC2
+      // (64-byte rows, no swizzle)
+      uint32_t pk[112];
+      #pragma unroll
+      for (int h = 0; h < 14; h += 2) {
+        uint32_t v[2][16];
+        tmem_ld_x16(t0 + 16 * h, v[0]);
+        tmem_ld_x16(t0 + 16 * (h + 1), v[1]);
+        tmem_ld_wait(v[0]);
+        tmem_ld_wait(v[1]);
+        #pragma unroll
+        for (int u = 0; u < 2; ++u)
+          #pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[8 * (h + u) + j] = pack_bf16x2(__uint_as_float(v[u][2 * j]) * al,
+                                              __uint_as_float(v[u][2 * j + 1]) * al);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (release_bar != nullptr) {
+        if (lane == 0) mbar_arrive(release_bar);
+        *released = true;
+      }
+      #pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        st.begin();
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* w = pk + 32 * c + 4 * q;
+          st.put(q, w[0], w[1], w[2], w[3]);
+        }
+        st.flush(tmC, ti.n * C::BN + 64 * c, y);
+      }
+      st.begin();
+      #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t* w = pk + 96 + 4 * q;
+        st.put_rows64(q, w[0], w[1], w[2], w[3]);
+      }
+      st.flush(tmC2, ti.n * C::BN + 192, y);
+    } else {
     if constexpr ((C::M256 || C::ACC_BUFS == 1) && C::BN == 256) {
       if (release_bar != nullptr) {
         // (single accumulator) this row's 256 outputs as bf16 pairs in registers, the accumulator
@@ -675,6 +743,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     }
     if constexpr (C::S == Sched::kRoutedM && C::BN == 256) {
       if (p.cmb_y != nullptr) fused_combine_rows(p, y, ti.n, lane, st);
+    }
     }
   } else if constexpr (C::EP == Epi::kSwiglu) {
     // accumulator columns [0, BN/2) = gate rows of W1, [BN/2, BN) = the matching up rows
@@ -1242,18 +1311,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
           } else if constexpr (C::MX) {
             // scale tiles of this stage -> TMEM, then 4 MMAs of K=32; MMA kk reads byte kk
+            // (256-row tiles: A's two scale tiles in 4 columns each, then B's; the
+            // second MMA takes A rows 128..255, 16 KB further on, into the
+            // accumulator's second half)
             const uint32_t sf_addr = smem_u32(sf_smem + stage * (C::SFA_BYTES + C::SFB_BYTES));
             const uint32_t sfa_t = tmem_base + C::ACC_BUFS * C::ACC_COLS + stage * C::SF_COLS;
-            const uint32_t sfb_t = sfa_t + 4;
-            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_plain16(sf_addr));
+            const uint32_t sfb_t = sfa_t + 4 * C::SFA_TILES;
             #pragma unroll
-            for (int i = 0; i < C::BN / 128; ++i)
-              tmem_cp_32x128b_warpx4(sfb_t + 4 * i, smem_desc_plain16(sf_addr + 512 * (i + 1)));
+            for (int i = 0; i < C::SFA_TILES; ++i)
+              tmem_cp_32x128b_warpx4(sfa_t + 4 * i, smem_desc_plain16(sf_addr + 512 * i));
+            #pragma unroll
+            for (int i = 0; i < C::SFB_TILES; ++i)
+              tmem_cp_32x128b_warpx4(sfb_t + 4 * i, smem_desc_plain16(sf_addr + 512 * (C::SFA_TILES + i)));
             #pragma unroll
             for (int kk = 0; kk < C::BK / C::KSTEP; ++kk) {
               const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
               mma_mxf8_ss(d_tmem, ad, bd, C::IDESC | idesc_sf_ids(kk, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (C::M256) {
+                if (ti.half1)
+                  mma_mxf8_ss(d_tmem + C::BN, smem_desc_sw128(a_addr + 16384 + kk * 32, 16, 1024), bd,
+                              C::IDESC | idesc_sf_ids(kk, kk), sfa_t + 4, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+              }
             }
           } else {
             #pragma unroll

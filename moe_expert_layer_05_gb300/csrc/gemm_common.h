@@ -13,10 +13,11 @@
 
 namespace moe {
 
-// Encode a 2-D row-major tensor map with 128-byte swizzle.  inner = elements
-// per row, outer = rows, box = {box_inner, box_outer} elements.
+// Encode a 2-D row-major tensor map (128-byte swizzle unless told otherwise).
+// inner = elements per row, outer = rows, box = {box_inner, box_outer} elements.
 bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, uint64_t inner,
-                  uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+                  uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 inline bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                            uint32_t box_outer) {
@@ -97,6 +98,10 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
 // Output map for the TMA-store epilogue: boxes of 128 bytes x 32 rows, 128B swizzle.
 inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 64, 32);
+}
+// 32-column bf16 boxes (64-byte rows, no swizzle): the last columns of a 224-wide tile
+inline bool make_tmap_out_bf16_32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32);

@@ -46,6 +46,17 @@ __device__ __forceinline__ size_t sf_offset(int r, int b, int tiles_per_row) {
          (b & 3);
 }
 
+// The same with the rows taken in groups of `group` (128, or 224 for the B
+// operand of 224-wide GEMM tiles): group g starts a new tile row, its rows
+// 0..127 fill tile row 2g and rows 128..223 the first 96 rows of tile row
+// 2g + 1 (the other 32 rows of that tile are never read).
+__device__ __forceinline__ size_t sf_offset_g(int r, int b, int tiles_per_row, int group) {
+  if (group == 128) return sf_offset(r, b, tiles_per_row);
+  const int g = r / group, i = r - g * group;
+  const int tr = 2 * g + (i >> 7), rr = i & 127;
+  return (static_cast<size_t>(tr) * tiles_per_row + (b >> 2)) * 512 + (rr & 31) * 16 + ((rr >> 5) & 3) * 4 + (b & 3);
+}
+
 // Quantise 32 values held by this thread; writes 32 code bytes and returns the scale byte.
 __device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst) {
   float amax = 0.f;
@@ -82,7 +93,7 @@ __device__ __forceinline__ long long gate_up_row(long long r, int half) {
 // tiled.  One thread per 32-value block: four 16-byte loads, two 16-byte
 // stores of codes, one scale byte.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ src, long long rows, int cols,
-                                                            int half, uint8_t* __restrict__ codes,
+                                                            int half, int group, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf) {
   const int nb = cols / 32;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -103,7 +114,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
     v[8 * q + 6] = bf16_lo(u[q].w); v[8 * q + 7] = bf16_hi(u[q].w);
   }
   const uint8_t s = quantize32(v, codes + r * cols + b * 32);
-  sf[sf_offset(static_cast<int>(r), b, cols / 128)] = s;
+  sf[sf_offset_g(static_cast<int>(r), b, cols / 128, group)] = s;
 }
 
 // Blocks along the column, output transposed: src [rows, cols] bf16 ->
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // rows read straight from token order through row_src, padding rows zero.
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
                                                             int cols, const int32_t* __restrict__ row_map,
-                                                            int src_rows, uint8_t* __restrict__ codes,
+                                                            int src_rows, int group, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ sf) {
   __shared__ uint4 tile[128][8];           // 128 rows x 64 bf16
   const int rb = blockIdx.x;               // block of 128 input rows
@@ -156,7 +167,9 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   const int c = c0 + cl;
   uint8_t* out = codes + mat * rows * cols + static_cast<long long>(c) * rows + rb * 128 + 32 * q;
   const uint8_t e = quantize32(v, out);
-  sf[mat * (static_cast<long long>(rows) * cols / 32) + sf_offset(c, rb * 4 + q, rows / 128)] = e;
+  // scale bytes of one matrix: its output rows (the input columns) in groups
+  const long long mat_sf = static_cast<long long>(group == 128 ? cols / 128 : 2 * (cols / group)) * rows * 4;
+  sf[mat * mat_sf + sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
 }
 
 // Token-order quantised rows (codes [T, H] and their scale tiles) -> expert
@@ -207,21 +220,21 @@ __global__ void zero_pad_rows_mx_kernel(const int32_t* __restrict__ counts, cons
 }  // namespace
 
 cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
-                                 uint8_t* sf, cudaStream_t st) {
+                                 uint8_t* sf, cudaStream_t st, int group) {
   const long long n = rows * (cols / 32);
   if (n == 0) return cudaSuccess;
-  quantize_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(static_cast<const uint4*>(src), rows,
-                                                                               cols, gate_up_half, codes, sf);
+  quantize_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+      static_cast<const uint4*>(src), rows, cols, gate_up_half, group, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, int group) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
   dim3 grid(rows / 128, cols / 64, batch);   // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
-  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, nullptr, 0, codes,
-                                             sf);
+  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, nullptr, 0, group,
+                                             codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -231,7 +244,7 @@ cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int
   if (rows == 0 || cols == 0) return cudaSuccess;
   dim3 grid(rows / 128, cols / 64, 1);
   quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, row_map, src_rows,
-                                             codes, sf);
+                                             128, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -150,3 +150,22 @@ def test_low_precision_gemm_arguments_checked_before_launch():
         assert call(nv, op) == -2
     assert call(mx, api.GG_FC2, scales=None) == -1
     assert call(mx, api.GG_FC1_SWIGLU, dense_rows=100) == -1
+    # B scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1, routed, H % 224 == 0 only
+    mx224 = api.make_config(256, 896, 8, 2, 256, dtype="mxfp8")
+    bf224 = api.make_config(256, 896, 8, 2, 256)
+
+    def call_g(cfg, op, group, dense_rows=0):
+        a = api.MoeGemmArgs(op, dense_rows, 16, 16, 16, None, 16, None, None, 16, 16, 16, 16, 16)
+        a.b_scale_group = group
+        return lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(a), 16, None)
+
+    assert call_g(mx, api.GG_FC2, 224) == -1                   # H = 256
+    assert call_g(mx224, api.GG_FC2, 100) == -1
+    assert call_g(mx224, api.GG_FC1_SWIGLU, 224) == -1
+    assert call_g(mx224, api.GG_WGRAD_FC1, 224) == -1
+    assert call_g(mx224, api.GG_FC2, 224, dense_rows=128) == -1
+    assert call_g(bf224, api.GG_FC2, 224) == -1
+    for op in (api.GG_FC2, api.GG_DGRAD_FC1):                  # accepted: only the device check is left
+        assert call_g(mx224, op, 224) != -1
+    assert lib.moe_quantize_mxfp8(16, 1, 200, 128, api.MX_ROWS_G224, 16, 16, None) == -1
+    assert lib.moe_quantize_mxfp8(16, 1, 128, 256, api.MX_COLS_T_G224, 16, 16, None) == -1

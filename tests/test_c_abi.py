@@ -2,6 +2,7 @@
 -pedantic -Werror, links against the library and calls its host-side entry
 points, getting the same sizes and layouts as the Python binding (no GPU,
 no Python or torch types across the boundary)."""
+import ctypes
 import os
 import shutil
 import subprocess
@@ -13,6 +14,7 @@ from moe_expert_layer_05_gb300 import api
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 C_SRC = r"""
+#include <stddef.h>
 #include <stdio.h>
 #include "moe_gb300.h"
 
@@ -24,9 +26,10 @@ int main(void) {
   n.dtype = MOE_GEMM_NVFP4;
   moe_config bad = c;
   bad.H = 100;
-  printf("%d %d %zu %zu %zu %zu %d %s\n", (int)moe_version(), (int)moe_capacity_rows(&c), L.total,
+  printf("%d %d %zu %zu %zu %zu %d %zu %zu %s\n", (int)moe_version(), (int)moe_capacity_rows(&c), L.total,
          moe_workspace_bytes(&c), moe_nvfp4_weights_bytes(&n), moe_mxfp8_weights_bytes(&c),
-         (int)moe_capacity_rows(&bad), moe_status_string(MOE_ERR_WORKSPACE));
+         (int)moe_capacity_rows(&bad), sizeof(moe_gemm_args), offsetof(moe_gemm_args, b_scale_group),
+         moe_status_string(MOE_ERR_WORKSPACE));
   return 0;
 }
 """
@@ -55,4 +58,6 @@ def test_header_is_plain_c_and_links():
     assert int(res[4]) == api.moe_nvfp4_weights_bytes(nv) > 0
     assert int(res[5]) == api.moe_mxfp8_weights_bytes(cfg) > 0
     assert int(res[6]) == -1
-    assert " ".join(res[7:]) == api.moe_status_string(-4)
+    assert int(res[7]) == ctypes.sizeof(api.MoeGemmArgs)             # the binding's struct matches the header's
+    assert int(res[8]) == api.MoeGemmArgs.b_scale_group.offset
+    assert " ".join(res[9:]) == api.moe_status_string(-4)

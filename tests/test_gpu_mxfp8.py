@@ -24,22 +24,36 @@ DEV = "cuda"
 
 def untile(sf: torch.Tensor, R: int, C: int) -> np.ndarray:
     """Scale tiles (512 B per 128 rows x 4 blocks) -> plain [R, C/32]."""
-    t = sf.cpu().numpy().reshape(R // 128, C // 128, 512)
+    t = sf.cpu().numpy()[: R * C // 32].reshape(R // 128, C // 128, 512)
     r = np.arange(128)[:, None]
     b = np.arange(4)[None, :]
     idx = (r % 32) * 16 + (r // 32) * 4 + b
     return t[:, :, idx].transpose(0, 2, 1, 3).reshape(R, C // 32)
 
 
+def untile_g224(sf: torch.Tensor, R: int, C: int) -> np.ndarray:
+    """Scale tiles with the rows in groups of 224 (rows 0..127 of group g in
+    tile row 2g, rows 128..223 in the first 96 rows of tile row 2g+1) -> [R, C/32]."""
+    t = sf.cpu().numpy()[: (R // 224) * 2 * (C // 128) * 512].reshape(R // 224 * 2, C // 128, 512)
+    r = np.arange(R)
+    g, i = r // 224, r % 224
+    tr, rr = 2 * g + i // 128, i % 128
+    b = np.arange(C // 32)
+    return t[tr[:, None], (b // 4)[None, :], ((rr % 32) * 16 + (rr // 32) * 4)[:, None] + (b % 4)[None, :]]
+
+
 def quantize_gpu(x: torch.Tensor, mode: int, batch=1):
     n = x.numel()
     codes = torch.empty(n, dtype=torch.uint8, device=DEV)
-    sf = torch.empty(n // 32, dtype=torch.uint8, device=DEV)
-    if mode == api.MX_ROWS:
+    if mode in (api.MX_ROWS, api.MX_ROWS_G224):
         rows, cols = x.numel() // x.shape[-1], x.shape[-1]
+        nsf = n // 32 if mode == api.MX_ROWS else rows // 224 * 2 * (cols // 128) * 512
+        sf = torch.empty(nsf, dtype=torch.uint8, device=DEV)
         api.moe_quantize_mxfp8(x, 1, rows, cols, mode, codes, sf)
     else:
         rows, cols = x.shape[-2], x.shape[-1]
+        nsf = n // 32 if mode != api.MX_COLS_T_G224 else batch * (cols // 224) * 2 * (rows // 128) * 512
+        sf = torch.empty(nsf, dtype=torch.uint8, device=DEV)
         api.moe_quantize_mxfp8(x, batch, rows, cols, mode, codes, sf)
     return codes, sf
 
@@ -105,6 +119,25 @@ def test_quantize_gate_up_interleave(lib):
             r = (jj // 128) * 256 + up * 128 + jj % 128
             np.testing.assert_array_equal(got[e, r], oc[e, j])
             np.testing.assert_array_equal(gsf[e, r], os_[e, j])
+
+
+def test_quantize_g224_scale_layout(lib):
+    """The 224-row grouping changes where each scale byte sits, nothing else:
+    codes identical, scales equal after both layouts are undone (row and
+    transposed-column modes, several matrices)."""
+    E, R, C = 2, 896, 1792          # rows (E*R) and output rows (C) multiples of 128 and 224
+    x = to_bf16(_rand((E, R, C), 71) * np.float32(3.0)).to(DEV)
+    c0, s0 = quantize_gpu(x.reshape(E * R, C), api.MX_ROWS)
+    c1, s1 = quantize_gpu(x.reshape(E * R, C), api.MX_ROWS_G224)
+    assert torch.equal(c0, c1)
+    np.testing.assert_array_equal(untile(s0[: E * R * C // 32], E * R, C), untile_g224(s1, E * R, C))
+    t0, u0 = quantize_gpu(x, api.MX_COLS_T, batch=E)             # [E, C, R], blocks along R
+    t1, u1 = quantize_gpu(x, api.MX_COLS_T_G224, batch=E)
+    assert torch.equal(t0, t1)
+    per0, per1 = C * R // 32, (C // 224) * 2 * (R // 128) * 512
+    for e in range(E):
+        np.testing.assert_array_equal(untile(u0[e * per0:(e + 1) * per0], C, R),
+                                      untile_g224(u1[e * per1:(e + 1) * per1], C, R))
 
 
 # ------------------------------------------------------------------ grouped GEMMs
@@ -235,6 +268,45 @@ def test_mx_gemm_dgrad(lib, T, H, E, k, F, skew):
     assert_bf16_close(f64(dx)[:used], O.expert_dgrad_fc1(deq(dz_in, -1)[:used], w1_deq, m["poffsets"]), "dx (mxfp8)")
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(512, 896, 8, 2, 256, 0.0), (640, 896, 16, 4, 384, 1.5),
+                                             (384, 1792, 64, 8, 128, 1.0)])
+def test_mx_gemm_256x224_tiles(lib, T, H, E, k, F, skew):
+    """fc2 and the fc1 data gradient on 256 x 224 tiles (B's scale tiles grouped
+    by 224 rows): against the oracle on the same quantised operands, and bit
+    for bit against the 128 x 256 tiles (same products, same K order), with
+    experts whose last 256-row tile is half empty."""
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 81)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    h_in = _rows(cap, F, valid, 82)
+    dz_in = _rows(cap, 2 * F, valid, 83)
+    w1 = to_bf16(_rand((E, 2 * F, H), 84, 0.05))
+    w2 = to_bf16(_rand((E, H, F), 85, 0.05))
+    hq, hsf = quantize_gpu(h_in.to(DEV), api.MX_ROWS)
+    dzq, dzsf = quantize_gpu(dz_in.to(DEV), api.MX_ROWS)
+    w2q, w2sf = quantize_gpu(w2.to(DEV).reshape(E * H, F), api.MX_ROWS)
+    w2g, w2gsf = quantize_gpu(w2.to(DEV).reshape(E * H, F), api.MX_ROWS_G224)
+    w1tq, w1tsf = quantize_gpu(w1.to(DEV), api.MX_COLS_T, batch=E)
+    w1tg, w1tgsf = quantize_gpu(w1.to(DEV), api.MX_COLS_T_G224, batch=E)
+    ws = _ws(cfg)
+    out = {}
+    for tag, (b2, s2, b1, s1, g) in {"128": (w2q, w2sf, w1tq, w1tsf, 0), "224": (w2g, w2gsf, w1tg, w1tgsf, 224)}.items():
+        o = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+        dx = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+        api.moe_grouped_gemm(cfg, api.GG_FC2, hq, b2, o, ws, poffsets=po, a_scales=hsf, b_scales=s2,
+                             b_scale_group=g)
+        api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC1, dzq, b1, dx, ws, poffsets=po, a_scales=dzsf, b_scales=s1,
+                             b_scale_group=g)
+        torch.cuda.synchronize()
+        assert api.moe_read_device_status(ws) == 0
+        out[tag] = (o, dx)
+    o, dx = out["224"]
+    assert_bf16_close(f64(o)[:used], O.expert_fc2(deq(h_in, -1)[:used], deq(w2, -1), m["poffsets"]), "o (224)")
+    w1_deq = O.mxfp8_roundtrip(f64(w1), axis=1)
+    assert_bf16_close(f64(dx)[:used], O.expert_dgrad_fc1(deq(dz_in, -1)[:used], w1_deq, m["poffsets"]), "dx (224)")
+    for a, b in zip(out["224"], out["128"]):
+        assert torch.equal(a[:used].view(torch.int16), b[:used].view(torch.int16))
+
+
 @pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
 def test_mx_gemm_wgrad(lib, T, H, E, k, F, skew):
     cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 23)
@@ -262,6 +334,9 @@ MX_LAYERS = {
                               dtype="mxfp8", backward=True),
     "mixtral_mx_small": Workload("mixtral_mx_small", T=256, H=512, E=8, k=2, F=768, dtype="mxfp8", backward=True),
     "wide_mx": Workload("wide_mx", T=256, H=256, E=8, k=2, F=2048, dtype="mxfp8", backward=True),   # few tiles, long K
+    # H % 224 == 0: fc2 and the fc1 data gradient on 256 x 224 tiles
+    "h896_mx": Workload("h896_mx", T=384, H=896, E=16, k=4, F=256, S=256, score="sigmoid", zipf_s=1.2,
+                        dtype="mxfp8", backward=True),
 }
 
 
