@@ -152,7 +152,12 @@ struct GemmCfg {
   // NVFP4 SwiGLU tiles (one accumulator, MMAs fast enough that the MMA warp
   // waits for it): eight warps too, the second four taking the upper half of
   // the h' columns, so the accumulator is read and handed back in half the time.
-  static constexpr bool SPLIT_COLS = NV4 && EP == Epi::kSwiglu && BN == 256;
+  // MXFP8 SwiGLU-backward tiles of N = 256 likewise: each warp loads its 128
+  // columns of dh into registers and hands the accumulator back at once (the
+  // elementwise backward is the long part of that epilogue), then stores dz in
+  // 32-column chunks through 2 KB staging buffers, so the ring keeps 4 stages.
+  static constexpr bool SPLIT_BWD = MX && !NV4 && EP == Epi::kSwigluBwd && BN == 256;
+  static constexpr bool SPLIT_COLS = (NV4 && EP == Epi::kSwiglu && BN == 256) || SPLIT_BWD;
   static constexpr int EPI_WARPS = (M256 || SPLIT_COLS) ? 8 : 4;
   // Shared memory (all of it dynamic): the k-block ring, 4 KB staging buffers
   // (32 rows x 128 B, 128B-swizzled) per epilogue warp -- two each, or one
@@ -173,7 +178,8 @@ struct GemmCfg {
                                       // waits in registers) where two would cost the ring a stage
                                       : (EP == Epi::kSwigluBwd) ? ((MX && BN == 256) ? 1 : 2)
                                       : ((TMA_OUT && RING_IF_TWO < 4) ? 1 : 2);
-  static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * 4096 : 0;
+  static constexpr int STAGING_BUF = SPLIT_BWD ? 2048 : 4096;   // bytes of one staging buffer
+  static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * STAGING_BUF : 0;
   static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES - (MX ? 1024 : 0)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   // the scale tiles of all stages, padded so the staging buffers after them
@@ -428,7 +434,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 // 32 rows (one per lane) x 128 bytes in the 128-byte swizzled order (16-byte
 // chunk c of row r sits at chunk c ^ (r % 8)), so a warp's 16-byte stores hit
 // distinct banks.  Lane 0 issues the stores and owns the bulk groups.
-template <int NBUF>
+template <int NBUF, int BUF = 4096>
 struct Stager {
   uint8_t* buf;
   int cur;
@@ -443,25 +449,32 @@ struct Stager {
     __syncwarp();
   }
   __device__ __forceinline__ void put(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
-    const uint32_t base = smem_u32(buf + cur * 4096);
+    const uint32_t base = smem_u32(buf + cur * BUF);
     st_shared_v4(base + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, cc, d);
   }
   // 16-byte chunk c of this lane's row in a buffer of 64-byte rows without
   // swizzle (for a 32-column bf16 box)
   __device__ __forceinline__ void put_rows64(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
-    const uint32_t base = smem_u32(buf + cur * 4096);
+    const uint32_t base = smem_u32(buf + cur * BUF);
     st_shared_v4(base + lane * 64 + (c << 4), a, b, cc, d);
+  }
+  // 16-byte chunk c of this lane's 64-byte row in the 64-byte swizzled order
+  // (chunk c of row r at chunk c ^ ((r / 2) % 4)): 32-column bf16 boxes, with
+  // eight consecutive lanes' stores in distinct banks
+  __device__ __forceinline__ void put_rows64_sw(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
+    const uint32_t base = smem_u32(buf + cur * BUF);
+    st_shared_v4(base + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), a, b, cc, d);
   }
   // into the buffer after the current one (two buffers filled in one pass)
   __device__ __forceinline__ void put_next(int c, uint32_t a, uint32_t b, uint32_t cc, uint32_t d) {
-    const uint32_t base = smem_u32(buf + (cur ^ 1) * 4096);
+    const uint32_t base = smem_u32(buf + (cur ^ 1) * BUF);
     st_shared_v4(base + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, cc, d);
   }
   __device__ __forceinline__ void flush(const CUtensorMap* map, int x, int y) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(map, buf + cur * 4096, x, y);
+      tma_store_2d(map, buf + cur * BUF, x, y);
       bulk_commit_group();
     }
     cur = (cur + 1 == NBUF) ? 0 : cur + 1;
@@ -514,7 +527,8 @@ __device__ __forceinline__ void add8_bf16(float (&acc)[8], const uint4& v) {
 // most once), so a lane's counter is its own.  The sum runs in slot order
 // whichever tile arrives last, so y is the same bits on every run.
 template <int NBUF>
-__device__ __forceinline__ void fused_combine_rows(const GemmParams& p, int y0, int n, int lane, Stager<NBUF>& st) {
+__device__ __forceinline__ void fused_combine_rows(const GemmParams& p, int y0, int n, int lane,
+                                                   Stager<NBUF, 4096>& st) {
   st.drain();                                   // lane 0: this warp's stores of o are complete
   if (lane == 0) fence_proxy_async_global();
   __syncwarp();
@@ -569,7 +583,8 @@ __device__ __forceinline__ void fused_combine_rows(const GemmParams& p, int y0, 
 // 32q..32q+31, lane = row.  Dense tiles past the last row are clipped by TMA.
 template <class C>
 __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const TileInfo& ti, uint32_t tmem_acc,
-                                                  int quarter, int lane, Stager<C::STAGING_BUFS>& st,
+                                                  int quarter, int lane,
+                                                  Stager<C::STAGING_BUFS, C::STAGING_BUF>& st,
                                                   const CUtensorMap* tmC,
                                                   const CUtensorMap* tmC2,
                                                   uint64_t* release_bar = nullptr, bool* released = nullptr,
@@ -936,6 +951,81 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     if constexpr (C::NV4) {
       if (p.amax_out != nullptr) amax_flush(p.amax_out, hmax, lane);
     }
+  } else if constexpr (C::SPLIT_BWD) {
+    // kSwigluBwd on 8 warps: this warp's 128 columns of dh (half cpart of the
+    // tile) to registers, the accumulator handed back, then per 32 columns the
+    // saved z, the SwiGLU backward and the dz gate and up chunks through the
+    // 2 KB staging (tmC2: 32-column boxes, 64-byte swizzle); one partial
+    // <dh, silu(a) b> per warp (its 128 columns)
+    const int row = ti.m0 + quarter * 32 + lane;
+    const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
+    const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
+    const int colw = ti.n * C::BN + 128 * cpart;
+    const int y = ti.m0 + quarter * 32;
+    const int parts = p.n_tiles * (C::BN / 128);
+    uint32_t dh[128];
+    #pragma unroll
+    for (int h = 0; h < 8; h += 2) {
+      uint32_t v[2][16];
+      tmem_ld_x16(t0 + 128 * cpart + 16 * h, v[0]);
+      tmem_ld_x16(t0 + 128 * cpart + 16 * (h + 1), v[1]);
+      tmem_ld_wait(v[0]);
+      tmem_ld_wait(v[1]);
+      #pragma unroll
+      for (int u = 0; u < 2; ++u)
+        #pragma unroll
+        for (int j = 0; j < 16; ++j) dh[16 * (h + u) + j] = no_mma ? 0u : v[u][j];
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (release_bar != nullptr) {
+      if (lane == 0) mbar_arrive(release_bar);
+      *released = true;
+    }
+    const __nv_bfloat16* zrow = p.aux + (long long)(row_ok ? row : 0) * p.ld_aux + colw;
+    float dg = 0.f;
+    #pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 za[4], zb[4];
+      #pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        za[i] = reinterpret_cast<const uint4*>(zrow + 32 * c)[i];
+        zb[i] = reinterpret_cast<const uint4*>(zrow + p.half_cols + 32 * c)[i];
+      }
+      uint32_t og[16], ou[16];
+      #pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint4& a4 = za[j >> 2];
+        const uint4& b4 = zb[j >> 2];
+        const uint32_t zaw = (j & 3) == 0 ? a4.x : (j & 3) == 1 ? a4.y : (j & 3) == 2 ? a4.z : a4.w;
+        const uint32_t zbw = (j & 3) == 0 ? b4.x : (j & 3) == 1 ? b4.y : (j & 3) == 2 ? b4.z : b4.w;
+        float g2[2], u2[2];
+        #pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float av = u ? bf16_hi(zaw) : bf16_lo(zaw);
+          const float bv = u ? bf16_hi(zbw) : bf16_lo(zbw);
+          const float dhv = __uint_as_float(dh[32 * c + 2 * j + u]);
+          // sigmoid with the fast exponential and divide (relative error ~1e-6)
+          const float sg = __fdividef(1.0f, 1.0f + __expf(-av));
+          const float si = av * sg;
+          const float dhg = g * dhv;
+          dg += dhv * si * bv;
+          g2[u] = dhg * bv * sg * (1.0f + av * (1.0f - sg));   // d(gate input)
+          u2[u] = dhg * si;                                  // d(up input)
+        }
+        og[j] = pack_bf16x2(g2[0], g2[1]);
+        ou[j] = pack_bf16x2(u2[0], u2[1]);
+      }
+      st.begin();
+      #pragma unroll
+      for (int q = 0; q < 4; ++q) st.put_rows64_sw(q, og[4 * q], og[4 * q + 1], og[4 * q + 2], og[4 * q + 3]);
+      st.flush(tmC2, colw + 32 * c, y);
+      st.begin();
+      #pragma unroll
+      for (int q = 0; q < 4; ++q) st.put_rows64_sw(q, ou[4 * q], ou[4 * q + 1], ou[4 * q + 2], ou[4 * q + 3]);
+      st.flush(tmC2, p.half_cols + colw + 32 * c, y);
+    }
+    if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * parts + colw / 128] = dg;
   } else {  // kSwigluBwd: dz gate and up chunks of each 64 columns in one pass
     static_assert(C::STAGING_BUFS == 2 || C::STAGING_BUFS == 1, "gate and up chunks: two buffers, or one");
     const int row = ti.m0 + quarter * 32 + lane;
@@ -1371,7 +1461,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                            // (split-column tiles: which half of the h' columns)
     int acc = 0;
     uint32_t acc_phase = 0;
-    Stager<C::STAGING_BUFS> st{stage_smem + ew * (C::STAGING_BUFS * 4096), 0, lane};
+    Stager<C::STAGING_BUFS, C::STAGING_BUF> st{stage_smem + ew * (C::STAGING_BUFS * C::STAGING_BUF), 0, lane};
     const float al = acc_scale<C>(p);
     for (int j = 0;; ++j) {
       const int slot = j % kSchedDepth;
@@ -1624,7 +1714,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    Stager<C::STAGING_BUFS> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * 4096), 0, lane};
+    Stager<C::STAGING_BUFS, C::STAGING_BUF> st{stage_smem + (warp - 2) * (C::STAGING_BUFS * C::STAGING_BUF), 0,
+                                               lane};
     for (int t = cid; t < ntiles; t += ncl) {
       const TileInfo ti = decode_tile<C>(p, s_poff, s_tpre, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_ptr, wait_lim)) break;

@@ -103,6 +103,10 @@ inline bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t cols
 inline bool make_tmap_out_bf16_32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
+// 32-column bf16 boxes with 64-byte swizzle (the split SwiGLU-backward epilogue)
+inline bool make_tmap_out_bf16_32_sw64(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
 inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
   return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32);
 }

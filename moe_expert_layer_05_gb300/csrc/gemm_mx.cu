@@ -210,15 +210,17 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
   p.sfb = static_cast<const uint8_t*>(w2tsf);
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
-  CUtensorMap tc;
-  if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc)) return cudaErrorInvalidValue;
+  CUtensorMap tc, tc32;
+  if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc) || !make_tmap_out_bf16_32_sw64(&tc32, dz, 2 * F, rows_alloc))
+    return cudaErrorInvalidValue;
   if (wide) {
+    // (eight epilogue warps storing 32-column chunks through tc32)
     p.n_tiles = F / 256;
     if (poffsets != nullptr)
-      return launch_mx<GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p,
+      return launch_mx<GemmCfg<256, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc32, p,
                                                                                            rows_alloc, dense_rows, st);
-    return launch_mx<GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p, rows_alloc,
-                                                                                        dense_rows, st);
+    return launch_mx<GemmCfg<256, false, false, Sched::kDenseM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc32, p,
+                                                                                        rows_alloc, dense_rows, st);
   }
   if (poffsets != nullptr)
     return launch_mx<GemmCfg<128, false, false, Sched::kRoutedM, Epi::kSwigluBwd, true>>(ta, tb, tc, tc, p, rows_alloc,
