@@ -480,9 +480,10 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
                                                           poffsets=po, a_scales=dzsf, b_scales=w1tsf,
                                                           b_scale_group=g224)
         dzt, dztsf = q(fl["dz"], 1, cap, 2 * F, api.MX_COLS_T)
-        xt, xtsf = q(fl["x_perm"], 1, cap, H, api.MX_COLS_T)
+        xt, xtsf = q(fl["x_perm"], 1, cap, H, api.MX_COLS_T_G224 if g224 else api.MX_COLS_T)
         calls["wgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, dzt, xt, grads["dw1"], ws,
-                                                          poffsets=po, a_scales=dztsf, b_scales=xtsf)
+                                                          poffsets=po, a_scales=dztsf, b_scales=xtsf,
+                                                          b_scale_group=g224)
         dyt, dytsf = q(fl["dy_perm"], 1, cap, H, api.MX_COLS_T)
         ht, htsf = q(fl["h"], 1, cap, F, api.MX_COLS_T)
         calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, dyt, ht, grads["dw2"], ws,

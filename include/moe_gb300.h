@@ -285,7 +285,8 @@ typedef enum {
  *   DGRAD_FC2:  a = dy_perm [cap,H]; b = W2^T [E,F,H] (MOE_MX_COLS_T of w2); aux = z (bf16).
  *   DGRAD_FC1:  a = dz [cap,2F]; b = W1^T [E,H,2F] (MOE_MX_COLS_T of w1, or MOE_MX_COLS_T_G224
  *               with b_scale_group = 224).
- *   WGRAD_FC1:  a = dz^T [2F,cap], b = x_perm^T [H,cap] (MOE_MX_COLS_T).
+ *   WGRAD_FC1:  a = dz^T [2F,cap], b = x_perm^T [H,cap] (MOE_MX_COLS_T, or MOE_MX_COLS_T_G224
+ *               with b_scale_group = 224).
  *   WGRAD_FC2:  a = dy_perm^T [H,cap], b = h^T [F,cap] (MOE_MX_COLS_T).
  * Dense calls need dense_rows % 128 == 0.
  * NVFP4 (dtype == MOE_GEMM_NVFP4; forward ops only, the others return
@@ -312,9 +313,10 @@ typedef struct {
   const float* b_amax;    /* NVFP4 only */
   const int32_t* a_rows;  /* FC1_SWIGLU_GATHERED, FC2_COMBINE */
   const int32_t* slot_row;/* FC2_COMBINE only */
-  int32_t b_scale_group;  /* MXFP8 FC2 / DGRAD_FC1 (routed, H % 224 == 0): 224 when b's scales
-                             were written by MOE_MX_ROWS_G224 / MOE_MX_COLS_T_G224 (the GEMM then
-                             runs 256 x 224 tiles); 0 (or 128) otherwise and for every other op */
+  int32_t b_scale_group;  /* MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 (routed, H % 224 == 0): 224 when
+                             b's scales were written by MOE_MX_ROWS_G224 / MOE_MX_COLS_T_G224 (the
+                             GEMM then runs 256 x 224 tiles); 0 (or 128) otherwise and for every
+                             other op */
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For

@@ -175,6 +175,13 @@ struct MxBuf {
   size_t q = kNone, sf = kNone;   // E4M3 codes, E8M0 scale tiles (codes / 32 bytes)
 };
 
+// The routed fc2 and fc1 data gradient (N = H) run on 256 x 224 tiles when H
+// allows: their B operands (W2, W1^T) then keep scale tiles per 224 rows.
+// (The fused fc2 + combine keeps 256-wide tiles and W2's 128-row tiles.)
+bool mx_b224(const moe_config* c) { return c->H % 224 == 0 && !kFuseCombine; }
+// x^T, the B operand of the routed fc1 weight gradient (N = H), likewise.
+int mx_xt_group(const moe_config* c) { return c->H % 224 == 0 ? kMxScaleGroup224 : 128; }
+
 // Transient quantised activations, placed in the workspace after the
 // histograms.  The forward, dgrad and wgrad calls each use their own set; the
 // region is the largest of the three.
@@ -189,12 +196,13 @@ MxWs mx_ws_layout(const moe_config* c) {
   MxWs m;
   const size_t T = c->T, H = c->H, F = c->F, S = c->S, cap = static_cast<size_t>(cap_rows(c));
   size_t off = 0, end = 0;
-  auto buf = [&](size_t elems) {
+  auto buf = [&](size_t elems, size_t sf_bytes = 0) {
     MxBuf b;
     b.q = off;
     off = align_up(off + (elems ? elems : 1));
     b.sf = off;
-    off = align_up(off + (elems / 32 ? elems / 32 : 1));
+    if (sf_bytes == 0) sf_bytes = elems / 32;
+    off = align_up(off + (sf_bytes ? sf_bytes : 1));
     return b;
   };
   auto region = [&]() { end = off > end ? off : end; off = 0; };
@@ -206,7 +214,8 @@ MxWs mx_ws_layout(const moe_config* c) {
   m.dy = buf(cap * H); m.dz = buf(cap * 2 * F); m.dys = buf(T * H);
   if (S) m.dzs = buf(T * 2 * S);
   region();
-  m.dzT = buf(2 * F * cap); m.xT = buf(H * cap); m.dyT = buf(H * cap); m.hT = buf(F * cap);
+  m.dzT = buf(2 * F * cap); m.dyT = buf(H * cap); m.hT = buf(F * cap);
+  m.xT = buf(H * cap, mx_scale_bytes(H, cap, mx_xt_group(c)));   // rows grouped by 224 for the 256 x 224 tiles
   if (S) { m.dzsT = buf(2 * S * T); m.xsT = buf(H * T); m.dysT = buf(H * T); m.hsT = buf(S * T); }
   region();
   m.total = end;
@@ -219,10 +228,6 @@ struct MxW {
   size_t total = 0;
 };
 
-// The routed fc2 and fc1 data gradient (N = H) run on 256 x 224 tiles when H
-// allows: their B operands (W2, W1^T) then keep scale tiles per 224 rows.
-// (The fused fc2 + combine keeps 256-wide tiles and W2's 128-row tiles.)
-bool mx_b224(const moe_config* c) { return c->H % 224 == 0 && !kFuseCombine; }
 
 MxW mx_weight_layout(const moe_config* c) {
   MxW m;
@@ -363,10 +368,11 @@ moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool d
   }
   if (a->op == MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;     // bf16 only
   if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
-  // B's scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1, routed, H % 224 == 0
+  // B's scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 (the GEMMs
+  // whose N is H), routed, H % 224 == 0
   if (a->b_scale_group != 0 && a->b_scale_group != 128) {
     if (a->b_scale_group != kMxScaleGroup224 || cfg->dtype != MOE_GEMM_MXFP8 || dense || cfg->H % 224 != 0 ||
-        (a->op != MOE_GG_FC2 && a->op != MOE_GG_DGRAD_FC1))
+        (a->op != MOE_GG_FC2 && a->op != MOE_GG_DGRAD_FC1 && a->op != MOE_GG_WGRAD_FC1))
       return MOE_ERR_INVALID_ARG;
   }
   if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
@@ -641,7 +647,8 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
                                            a->b_scale_group == 0 ? 128 : a->b_scale_group));
       case MOE_GG_WGRAD_FC1:
         return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, 2 * F, a->b, a->b_scales, H, rows, E, po, a->dense_rows,
-                                         static_cast<float*>(a->c), status, st));
+                                         static_cast<float*>(a->c), status, st,
+                                         a->b_scale_group == 0 ? 128 : a->b_scale_group));
       case MOE_GG_WGRAD_FC2:
         return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, H, a->b, a->b_scales, F, rows, E, po, a->dense_rows,
                                          static_cast<float*>(a->c), status, st));
@@ -933,8 +940,9 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     // x and dy in expert order are read straight from token order through row_src
     const int32_t* row_src = at<int32_t>(act, L.row_src);
     MOE_TRY(launch_quantize_cols(at<void>(act, L.dz), 1, cap, 2 * F, q(M.dzT), f(M.dzT), st));
-    MOE_TRY(launch_quantize_cols_gather(x, T, row_src, cap, H, q(M.xT), f(M.xT), st));
-    MOE_TRY(gemm_mx_wgrad(q(M.dzT), f(M.dzT), 2 * F, q(M.xT), f(M.xT), H, cap, E, poff, 0, g->dw1, status, st));
+    MOE_TRY(launch_quantize_cols_gather(x, T, row_src, cap, H, q(M.xT), f(M.xT), st, mx_xt_group(cfg)));
+    MOE_TRY(gemm_mx_wgrad(q(M.dzT), f(M.dzT), 2 * F, q(M.xT), f(M.xT), H, cap, E, poff, 0, g->dw1, status, st,
+                          mx_xt_group(cfg)));
     MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st));
     MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st));
     MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, q(M.hT), f(M.hT), F, cap, E, poff, 0, g->dw2, status, st));

@@ -172,7 +172,9 @@ struct GemmCfg {
   // Weight gradients are bound by their fp32 stores: each epilogue warp keeps
   // several 4 KB stores in flight (the k-loops are short, so the ring needs
   // few stages).
-  static constexpr int WGRAD_BUFS = WIDE_K ? 2 : 4;
+  // (256 x 224 MXFP8 weight-gradient tiles: eight warps, one buffer each, so
+  // the ring keeps three 62 KB stages)
+  static constexpr int WGRAD_BUFS = WIDE_K ? 2 : (M256 ? 1 : 4);
   static constexpr int STAGING_BUFS = (S == Sched::kRoutedK && TMA_OUT) ? WGRAD_BUFS
                                       // gate and up chunks side by side; one buffer (the up chunk
                                       // waits in registers) where two would cost the ring a stage
@@ -214,8 +216,11 @@ struct GemmCfg {
   static_assert(!NV4 || (S != Sched::kRoutedK && EP != Epi::kSwigluBwd && EP != Epi::kStoreF32),
                 "NVFP4: forward GEMMs (bf16 or SwiGLU epilogue)");
   static_assert(TMEM_COLS_RAW <= 512, "TMEM columns");
-  static_assert(!M256 || ((!MX || (!NV4 && BN == 224 && EP == Epi::kStoreBf16)) && !A_MN && S != Sched::kRoutedK),
-                "256-row tiles: K-major A, row-grouped; MXFP8 ones 256 x 224 with bf16 stores");
+  static_assert(!M256 || (!A_MN && (MX ? (!NV4 && BN == 224 &&
+                                           (S == Sched::kRoutedK ? EP == Epi::kStoreF32 : EP == Epi::kStoreBf16))
+                                        : S != Sched::kRoutedK)),
+                "256-row tiles: K-major A; bf16 ones row-grouped, MXFP8 ones 256 x 224 (bf16 stores, or fp32 "
+                "weight gradients)");
   static_assert(!M256 || TMA_OUT, "256-row tiles store through TMA");
   static_assert(!GATHER || (M256 && !MX && !A_MN && S == Sched::kRoutedM && BK == 64),
                 "gathered A: bf16 256-row row-grouped tiles");
@@ -317,8 +322,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const int* 
     const int per = p.m_tiles_w * p.n_tiles;
     ti.group = t / per;
     const int r = t % per;
-    ti.m0 = (r / p.n_tiles) * (C::PAIR ? 256 : C::BM);   // a pair covers 256 output rows
-    ti.half1 = C::PAIR;                                  // (both halves always in range)
+    ti.m0 = (r / p.n_tiles) * (C::ROWS256 ? 256 : C::BM);   // a pair or a 256-row tile covers 256 output rows
+    ti.half1 = C::ROWS256;                                  // (both halves always in range)
     ti.n = r % p.n_tiles;
     if (p.poffsets != nullptr) {
       ti.k_row0 = s_poff[ti.group];

@@ -261,9 +261,46 @@ cudaError_t mx_wgrad_bn(const void* atq, const void* atsf, int M, const void* bt
 }
 }  // namespace
 
+namespace {
+// 256 x 224 weight-gradient tiles (B's scale tiles grouped by 224 rows): two
+// 128 x 224 MMAs share each B k-block, 60 KB of operands per k-block for
+// 256 x 224 outputs instead of 48 KB for 128 x 256, and eight epilogue warps.
+cudaError_t mx_wgrad_224(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
+                         int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
+                         cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, atq, rows_alloc, M, 256) || !make_tmap_u8(&tb, btq, rows_alloc, N, 224))
+    return cudaErrorInvalidValue;
+  GemmParams p = gemm_params_zero();
+  p.poffsets = poffsets;
+  p.E = (poffsets != nullptr) ? E : 1;
+  p.m_rows = M;
+  p.k_len = dense_rows;
+  p.m_tiles_w = M / 256;
+  p.n_tiles = N / 224;
+  p.c = dw;
+  p.ldc = N;
+  p.c_group_stride = static_cast<long long>(M) * N;
+  p.rows_cap = rows_alloc;
+  p.status = status;
+  p.sfa = static_cast<const uint8_t*>(atsf);
+  p.sfb = static_cast<const uint8_t*>(btsf);
+  p.sfa_tiles_k = rows_alloc / 128;
+  p.sfb_tiles_k = rows_alloc / 128;
+  CUtensorMap tc;
+  if (!make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M)) return cudaErrorInvalidValue;
+  return launch_mx<GemmCfg<224, false, false, Sched::kRoutedK, Epi::kStoreF32, true, true>>(ta, tb, tc, tc, p,
+                                                                                           rows_alloc, dense_rows, st);
+}
+}  // namespace
+
 cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
-                          cudaStream_t st) {
+                          cudaStream_t st, int b_group) {
+  if (b_group == kMxScaleGroup224) {
+    if (N % 224 != 0 || M % 256 != 0) return cudaErrorInvalidValue;
+    return mx_wgrad_224(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
+  }
   if (N % 256 == 0)
     return mx_wgrad_bn<256>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
   return mx_wgrad_bn<128>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);

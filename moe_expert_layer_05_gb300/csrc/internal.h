@@ -121,7 +121,7 @@ constexpr int kMxScaleGroup224 = 224;
 // Column mode on rows gathered through row_map: row r of the [rows, cols]
 // input is src row row_map[r] (a zero row where it is outside [0, src_rows)).
 cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
-                                        uint8_t* codes, uint8_t* sf, cudaStream_t st);
+                                        uint8_t* codes, uint8_t* sf, cudaStream_t st, int group = 128);
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
                         void* z, int* status, cudaStream_t st);
@@ -137,9 +137,10 @@ cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc,
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
                               const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st);
+// b_group 224: B's scale tiles grouped by 224 rows (256 x 224 tiles; N % 224 == 0, M % 256 == 0).
 cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
-                          cudaStream_t st);
+                          cudaStream_t st, int b_group = 128);
 
 // ------------------------------------------------------------ NVFP4 (nvfp4.cu, gemm_mx.cu)
 // *amax = max |v| over a bf16 [rows, cols] tensor (rows with row_src < 0 skipped

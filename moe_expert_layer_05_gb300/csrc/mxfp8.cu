@@ -240,11 +240,11 @@ cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols,
 }
 
 cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
-                                        uint8_t* codes, uint8_t* sf, cudaStream_t st) {
+                                        uint8_t* codes, uint8_t* sf, cudaStream_t st, int group) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   dim3 grid(rows / 128, cols / 64, 1);
   quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, row_map, src_rows,
-                                             128, codes, sf);
+                                             group, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }

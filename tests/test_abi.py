@@ -162,10 +162,10 @@ def test_low_precision_gemm_arguments_checked_before_launch():
     assert call_g(mx, api.GG_FC2, 224) == -1                   # H = 256
     assert call_g(mx224, api.GG_FC2, 100) == -1
     assert call_g(mx224, api.GG_FC1_SWIGLU, 224) == -1
-    assert call_g(mx224, api.GG_WGRAD_FC1, 224) == -1
+    assert call_g(mx224, api.GG_WGRAD_FC2, 224) == -1
     assert call_g(mx224, api.GG_FC2, 224, dense_rows=128) == -1
     assert call_g(bf224, api.GG_FC2, 224) == -1
-    for op in (api.GG_FC2, api.GG_DGRAD_FC1):                  # accepted: only the device check is left
+    for op in (api.GG_FC2, api.GG_DGRAD_FC1, api.GG_WGRAD_FC1):   # accepted: only the device check is left
         assert call_g(mx224, op, 224) != -1
     assert lib.moe_quantize_mxfp8(16, 1, 200, 128, api.MX_ROWS_G224, 16, 16, None) == -1
     assert lib.moe_quantize_mxfp8(16, 1, 128, 256, api.MX_COLS_T_G224, 16, 16, None) == -1

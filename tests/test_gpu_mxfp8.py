@@ -328,6 +328,36 @@ def test_mx_gemm_wgrad(lib, T, H, E, k, F, skew):
     assert np.all(f64(dw1)[m["counts"] == 0] == 0)
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(512, 896, 8, 2, 256, 0.0), (640, 896, 16, 4, 384, 1.5)])
+def test_mx_gemm_wgrad_256x224_tiles(lib, T, H, E, k, F, skew):
+    """The fc1 weight gradient on 256 x 224 tiles (x^T's scale tiles grouped by
+    224 rows): against the oracle, zero for empty experts, and bit for bit
+    against the 128 x 256 tiles."""
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 91)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    dz = _rows(cap, 2 * F, valid, 92)
+    xp = _rows(cap, H, valid, 93)
+    dzT, dzTs = quantize_gpu(dz.to(DEV), api.MX_COLS_T)          # [2F, cap]
+    xT, xTs = quantize_gpu(xp.to(DEV), api.MX_COLS_T)            # [H, cap]
+    xTg, xTgs = quantize_gpu(xp.to(DEV), api.MX_COLS_T_G224)
+    ws = _ws(cfg)
+    out = []
+    for b, bs, g in ((xT, xTs, 0), (xTg, xTgs, 224)):
+        dw1 = torch.full((E, 2 * F, H), 7.0, dtype=torch.float32, device=DEV)
+        api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, dzT, b, dw1, ws, poffsets=po, a_scales=dzTs, b_scales=bs,
+                             b_scale_group=g)
+        torch.cuda.synchronize()
+        assert api.moe_read_device_status(ws) == 0
+        out.append(dw1)
+    a = O.mxfp8_roundtrip(f64(dz), axis=0)[:used]
+    bq = O.mxfp8_roundtrip(f64(xp), axis=0)[:used]
+    ref = O.expert_wgrad(a, bq, m["poffsets"])
+    scale = np.einsum("rm,rn->mn", np.abs(a), np.abs(bq))
+    assert np.all(np.abs(f64(out[1]) - ref) <= 2.0 ** -14 * scale[None] + 1e-6)
+    assert np.all(f64(out[1])[m["counts"] == 0] == 0)
+    assert torch.equal(out[0], out[1])
+
+
 # ------------------------------------------------------------------ layer
 MX_LAYERS = {
     "dsv3_mx_small": Workload("dsv3_mx_small", T=384, H=256, E=64, k=8, F=128, S=256, score="sigmoid", zipf_s=1.2,
