@@ -801,8 +801,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     // x is quantised once per token and the codes are permuted like x itself
     // (blocks lie along H, so quantising before or after the gather is the same)
     MOE_TRY(launch_quantize_rows(x, T, H, 0, q(M.xs), f(M.xs), st));
-    MOE_TRY(launch_gather_rows_mx(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st));
-    if (with_backward) MOE_TRY(launch_zero_pad_rows_mx(counts, poff, E, H, q(M.x), f(M.x), st));
+    MOE_TRY(launch_gather_rows_mx(q(M.xs), f(M.xs), slot_row, T, k, H, q(M.x), f(M.x), st, counts, poff,
+                                  with_backward ? E : 0));
     // the shared expert first: with the combine fused into fc2 its rows must exist
     if (S > 0 && T > 0) {
       MOE_TRY(gemm_mx_fc1(q(M.xs), f(M.xs), T, H, wq(W.s1), wf(W.s1), 1, S, nullptr, T, nullptr, at<void>(act, L.hs),
@@ -813,7 +813,7 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
       shared_out = at<void>(act, L.os);
     }
     MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
-    MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st));
+    MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st, 128, poff + E));
     with_shared();
     if (fused_combine) {
       MOE_TRY(gemm_mx_fc2_combine(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, o, cmb, status, st));
@@ -879,11 +879,10 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
     auto wq = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.q); };
     auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
     MOE_TRY(launch_quantize_rows(dy, T, H, 0, q(M.dys), f(M.dys), st));
-    MOE_TRY(launch_gather_rows_mx(q(M.dys), f(M.dys), slot_row, T, k, H, q(M.dy), f(M.dy), st));
-    MOE_TRY(launch_zero_pad_rows_mx(counts, poff, E, H, q(M.dy), f(M.dy), st));
+    MOE_TRY(launch_gather_rows_mx(q(M.dys), f(M.dys), slot_row, T, k, H, q(M.dy), f(M.dy), st, counts, poff, E));
     MOE_TRY(gemm_mx_dgrad_fc2(q(M.dy), f(M.dy), cap, H, wq(W.w2t), wf(W.w2t), E, F, poff, 0, at<void>(act, L.z),
                               at<float>(act, L.row_gate), dz, dpart, status, st));
-    MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st));
+    MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st, 128, poff + E));
     MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st,
                             mx_b224(cfg) ? kMxScaleGroup224 : 128));
     if (S > 0 && T > 0) {
@@ -939,12 +938,13 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     auto f = [&](const MxBuf& b) { return reinterpret_cast<uint8_t*>(mb + b.sf); };
     // x and dy in expert order are read straight from token order through row_src
     const int32_t* row_src = at<int32_t>(act, L.row_src);
-    MOE_TRY(launch_quantize_cols(at<void>(act, L.dz), 1, cap, 2 * F, q(M.dzT), f(M.dzT), st));
-    MOE_TRY(launch_quantize_cols_gather(x, T, row_src, cap, H, q(M.xT), f(M.xT), st, mx_xt_group(cfg)));
+    // (rows past the last expert's padded end are skipped: no GEMM reads them)
+    MOE_TRY(launch_quantize_cols(at<void>(act, L.dz), 1, cap, 2 * F, q(M.dzT), f(M.dzT), st, 128, poff + E));
+    MOE_TRY(launch_quantize_cols_gather(x, T, row_src, cap, H, q(M.xT), f(M.xT), st, mx_xt_group(cfg), poff + E));
     MOE_TRY(gemm_mx_wgrad(q(M.dzT), f(M.dzT), 2 * F, q(M.xT), f(M.xT), H, cap, E, poff, 0, g->dw1, status, st,
                           mx_xt_group(cfg)));
-    MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st));
-    MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st));
+    MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st, 128, poff + E));
+    MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st, 128, poff + E));
     MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, q(M.hT), f(M.hT), F, cap, E, poff, 0, g->dw2, status, st));
     if (S > 0 && T > 0) {
       MOE_TRY(launch_quantize_cols(at<void>(act, L.dzs), 1, T, 2 * S, q(M.dzsT), f(M.dzsT), st));

@@ -95,23 +95,27 @@ cudaError_t gemm_wgrad(const void* a, int M, const void* b, int N, int rows_allo
                        int dense_rows, float* dw, int* status, cudaStream_t st);
 
 // ------------------------------------------------------------ MXFP8 (mxfp8.cu, gemm_mx.cu)
+// row_limit (device, nullable; the quantisers below take it too): rows from
+// *row_limit on are skipped -- the capacity rows past the last expert, which
+// no GEMM reads.
 // Row mode: blocks of 32 along each row; gate_up_half > 0 also interleaves
 // the rows of every [gate; up] group of 2*half rows in 128-row blocks.
 // group: scale tiles per 128 rows (128), or per group of 224 rows (two tiles
 // a group, the second one's last 32 rows unused; rows % 224 == 0): the B
 // operand layout of the 224-wide GEMM tiles (kMxScaleGroup224).
 cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
-                                 uint8_t* sf, cudaStream_t st, int group = 128);
+                                 uint8_t* sf, cudaStream_t st, int group = 128, const int32_t* row_limit = nullptr);
 // Row-quantised token rows -> expert order (codes and scale tiles), and the
 // zero codes / scales of the padding rows.
+// E_pad > 0: the same launch zeroes the padding rows (codes and scales) of
+// experts 0 .. E_pad-1 (counts, poffsets [E+1]).
 cudaError_t launch_gather_rows_mx(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
-                                  int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st);
-cudaError_t launch_zero_pad_rows_mx(const int32_t* counts, const int32_t* poffsets, int E, int H, uint8_t* codes,
-                                    uint8_t* sf, cudaStream_t st);
+                                  int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st,
+                                  const int32_t* counts = nullptr, const int32_t* poffsets = nullptr, int E_pad = 0);
 // Column mode: batch x [rows, cols] -> batch x [cols, rows], blocks along rows
 // (group: as for the row mode, over the output rows; cols % 224 == 0 for 224).
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
-                                 cudaStream_t st, int group = 128);
+                                 cudaStream_t st, int group = 128, const int32_t* row_limit = nullptr);
 // Scale bytes of a [rows, cols] codes matrix (blocks along cols) with its
 // rows' scale tiles in groups of `group` rows.
 inline size_t mx_scale_bytes(size_t rows, size_t cols, int group) {
@@ -121,7 +125,8 @@ constexpr int kMxScaleGroup224 = 224;
 // Column mode on rows gathered through row_map: row r of the [rows, cols]
 // input is src row row_map[r] (a zero row where it is outside [0, src_rows)).
 cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
-                                        uint8_t* codes, uint8_t* sf, cudaStream_t st, int group = 128);
+                                        uint8_t* codes, uint8_t* sf, cudaStream_t st, int group = 128,
+                                        const int32_t* row_limit = nullptr);
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
                         void* z, int* status, cudaStream_t st);

@@ -93,12 +93,13 @@ __device__ __forceinline__ long long gate_up_row(long long r, int half) {
 // tiled.  One thread per 32-value block: four 16-byte loads, two 16-byte
 // stores of codes, one scale byte.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ src, long long rows, int cols,
-                                                            int half, int group, uint8_t* __restrict__ codes,
-                                                            uint8_t* __restrict__ sf) {
+                                                            int half, int group, const int32_t* __restrict__ row_limit,
+                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int nb = cols / 32;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= rows * nb) return;
   const long long r_in = i / nb;
+  if (row_limit != nullptr && r_in >= __ldg(row_limit)) return;   // rows past the last expert: never read
   const long long r = gate_up_row(r_in, half);
   const int b = static_cast<int>(i - r_in * nb);
   const uint4* p = src + i * 4;
@@ -131,10 +132,12 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // rows read straight from token order through row_src, padding rows zero.
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
                                                             int cols, const int32_t* __restrict__ row_map,
-                                                            int src_rows, int group, uint8_t* __restrict__ codes,
-                                                            uint8_t* __restrict__ sf) {
+                                                            int src_rows, int group,
+                                                            const int32_t* __restrict__ row_limit,
+                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   __shared__ uint4 tile[128][8];           // 128 rows x 64 bf16
   const int rb = blockIdx.x;               // block of 128 input rows
+  if (row_limit != nullptr && rb * 128 >= __ldg(row_limit)) return;   // past the last expert: never read
   const int c0 = blockIdx.y * 64;
   const long long mat = blockIdx.z;
   const __nv_bfloat16* base = src + mat * rows * cols + static_cast<long long>(rb) * 128 * cols + c0;
@@ -172,15 +175,38 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   sf[mat * mat_sf + sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
 }
 
+// Padding rows of expert e's segment: zero codes and the scale of an
+// all-zero block (byte 0), as quantising zero rows would give.
+__device__ __forceinline__ void zero_pad_rows_mx(const int32_t* __restrict__ counts,
+                                                 const int32_t* __restrict__ poffsets, int e, int H,
+                                                 uint4* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int r0 = poffsets[e] + counts[e], r1 = poffsets[e + 1];
+  const int nv = H / 16, nb = H / 32;
+  const long long n = static_cast<long long>(r1 - r0) * nv;
+  uint4* base = codes + static_cast<long long>(r0) * nv;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
+  const long long m = static_cast<long long>(r1 - r0) * nb;
+  for (long long i = threadIdx.x; i < m; i += blockDim.x)
+    sf[sf_offset(r0 + static_cast<int>(i / nb), static_cast<int>(i % nb), H / 128)] = 0;
+}
+
 // Token-order quantised rows (codes [T, H] and their scale tiles) -> expert
 // order: the same permutation as the bf16 gather, on codes and scales.  Row
 // blocks of 32 lie along H, so a row's codes do not depend on where it goes.
+// Blocks 0 .. E_pad - 1 zero the padding rows of expert `block` in the same
+// launch (first, so they overlap the gathers rather than trail them).
 __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __restrict__ codes_tok,
                                                              const uint8_t* __restrict__ sf_tok,
-                                                             const int32_t* __restrict__ slot_row, int k, int H,
+                                                             const int32_t* __restrict__ slot_row, int E_pad, int k,
+                                                             int H, const int32_t* __restrict__ counts,
+                                                             const int32_t* __restrict__ poffsets,
                                                              uint4* __restrict__ codes_perm,
                                                              uint8_t* __restrict__ sf_perm) {
-  const int t = blockIdx.x;
+  if (static_cast<int>(blockIdx.x) < E_pad) {
+    zero_pad_rows_mx(counts, poffsets, blockIdx.x, H, codes_perm, sf_perm);
+    return;
+  }
+  const int t = blockIdx.x - E_pad;
   __shared__ int s_rows[kMaxK];
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[static_cast<long long>(t) * k + threadIdx.x];
   __syncthreads();
@@ -202,49 +228,35 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __rest
   }
 }
 
-// Padding rows of every expert segment: zero codes and the scale of an
-// all-zero block (byte 0), as quantising zero rows would give.
-__global__ void zero_pad_rows_mx_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ poffsets,
-                                        int H, uint4* __restrict__ codes, uint8_t* __restrict__ sf) {
-  const int e = blockIdx.x;
-  const int r0 = poffsets[e] + counts[e], r1 = poffsets[e + 1];
-  const int nv = H / 16, nb = H / 32;
-  const long long n = static_cast<long long>(r1 - r0) * nv;
-  uint4* base = codes + static_cast<long long>(r0) * nv;
-  for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
-  const long long m = static_cast<long long>(r1 - r0) * nb;
-  for (long long i = threadIdx.x; i < m; i += blockDim.x)
-    sf[sf_offset(r0 + static_cast<int>(i / nb), static_cast<int>(i % nb), H / 128)] = 0;
-}
-
 }  // namespace
 
 cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int gate_up_half, uint8_t* codes,
-                                 uint8_t* sf, cudaStream_t st, int group) {
+                                 uint8_t* sf, cudaStream_t st, int group, const int32_t* row_limit) {
   const long long n = rows * (cols / 32);
   if (n == 0) return cudaSuccess;
   quantize_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-      static_cast<const uint4*>(src), rows, cols, gate_up_half, group, codes, sf);
+      static_cast<const uint4*>(src), rows, cols, gate_up_half, group, row_limit, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
-                                 cudaStream_t st, int group) {
+                                 cudaStream_t st, int group, const int32_t* row_limit) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
   dim3 grid(rows / 128, cols / 64, batch);   // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
   quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, nullptr, 0, group,
-                                             codes, sf);
+                                             row_limit, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
-                                        uint8_t* codes, uint8_t* sf, cudaStream_t st, int group) {
+                                        uint8_t* codes, uint8_t* sf, cudaStream_t st, int group,
+                                        const int32_t* row_limit) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   dim3 grid(rows / 128, cols / 64, 1);
   quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, row_map, src_rows,
-                                             group, codes, sf);
+                                             group, row_limit, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -253,17 +265,12 @@ cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int
 
 namespace moe {
 cudaError_t launch_gather_rows_mx(const uint8_t* codes_tok, const uint8_t* sf_tok, const int32_t* slot_row, int T,
-                                  int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st) {
-  if (T == 0) return cudaSuccess;
-  gather_rows_mx_kernel<<<T, 128, 0, st>>>(reinterpret_cast<const uint4*>(codes_tok), sf_tok, slot_row, k, H,
-                                           reinterpret_cast<uint4*>(codes_perm), sf_perm);
-  count_launches(1);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_zero_pad_rows_mx(const int32_t* counts, const int32_t* poffsets, int E, int H, uint8_t* codes,
-                                    uint8_t* sf, cudaStream_t st) {
-  zero_pad_rows_mx_kernel<<<E, 256, 0, st>>>(counts, poffsets, H, reinterpret_cast<uint4*>(codes), sf);
+                                  int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st,
+                                  const int32_t* counts, const int32_t* poffsets, int E_pad) {
+  if (T + E_pad == 0) return cudaSuccess;
+  gather_rows_mx_kernel<<<T + E_pad, 128, 0, st>>>(reinterpret_cast<const uint4*>(codes_tok), sf_tok, slot_row,
+                                                   E_pad, k, H, counts, poffsets,
+                                                   reinterpret_cast<uint4*>(codes_perm), sf_perm);
   count_launches(1);
   return cudaGetLastError();
 }
