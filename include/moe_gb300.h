@@ -109,14 +109,21 @@ typedef struct {
  *   x_perm bf16 [cap,H]; z bf16 [cap,2F] (fc1 output); h bf16 [cap,F] (gate *
  *   SwiGLU output); o bf16 [cap,H] (fc2 output);
  *   zs bf16 [T,2S], hs bf16 [T,S], os bf16 [T,H] (shared expert, if S > 0);
- *   backward only: dy_perm bf16 [cap,H]; dz bf16 [cap,2F]; dx_perm bf16 [cap,H];
+ *   backward only: dy_perm bf16 [cap,H]; dz bf16 [cap,2F] (MXFP8 layers with F %
+ *   256 == 0 leave it unwritten: their fc2 data gradient writes dz in MXFP8
+ *   only); dx_perm bf16 [cap,H];
  *   dgate_part fp32 [cap, F/128]; dlogits fp32 [T,E]; row_dlogit fp32 [cap];
- *   dzs bf16 [T,2S]; dxs bf16 [T,H].
+ *   dzs bf16 [T,2S]; dxs bf16 [T,H];
+ *   MXFP8 layers, backward only: dz_qt u8 [2F,cap] (dz quantised along the
+ *   rows, 32-row blocks, and transposed: the fc1 weight gradient's A operand,
+ *   written by moe_layer_backward_dgrad) and dz_qt_sf its scale tiles (cap/128
+ *   tiles per tile row of 128 of the 2F rows).
  * Fields that do not apply have offset SIZE_MAX. */
 typedef struct {
   size_t logits, topk_idx, topk_gate, counts, offsets, poffsets, slot_row, row_src, row_gate;
   size_t x_perm, z, h, o, zs, hs, os;
   size_t dy_perm, dz, dx_perm, dgate_part, dlogits, row_dlogit, dzs, dxs;
+  size_t dz_qt, dz_qt_sf;
   size_t total;          /* bytes the activation buffer needs */
   int32_t cap;           /* rows of the expert-ordered buffers */
   int32_t backward;      /* 1 if the backward fields are present */
@@ -317,6 +324,16 @@ typedef struct {
                              b's scales were written by MOE_MX_ROWS_G224 / MOE_MX_COLS_T_G224 (the
                              GEMM then runs 256 x 224 tiles); 0 (or 128) otherwise and for every
                              other op */
+  /* MXFP8 DGRAD_FC2 only (routed, F % 256 == 0; NULL pairs: not written): dz
+   * also written in MXFP8 by the epilogue, for the GEMMs that read it next --
+   * q_codes [cap,2F] with q_scales (blocks along the row, as MOE_MX_ROWS) and
+   * qt_codes [2F,cap] with qt_scales (blocks of 32 rows, transposed, as
+   * MOE_MX_COLS_T), bit-identical to quantising the bf16 dz, rows < the last
+   * expert's padded end. */
+  void* q_codes;
+  void* q_scales;
+  void* qt_codes;
+  void* qt_scales;
 } moe_gemm_args;
 
 /* One grouped GEMM on the tensor cores (tcgen05, TMA-fed, persistent).  For

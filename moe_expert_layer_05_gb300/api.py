@@ -44,7 +44,7 @@ class MoeGrads(ctypes.Structure):
 
 _LAYOUT_FIELDS = ["logits", "topk_idx", "topk_gate", "counts", "offsets", "poffsets", "slot_row", "row_src",
                   "row_gate", "x_perm", "z", "h", "o", "zs", "hs", "os", "dy_perm", "dz", "dx_perm",
-                  "dgate_part", "dlogits", "row_dlogit", "dzs", "dxs"]
+                  "dgate_part", "dlogits", "row_dlogit", "dzs", "dxs", "dz_qt", "dz_qt_sf"]
 
 
 class MoeActLayout(ctypes.Structure):
@@ -55,7 +55,8 @@ class MoeGemmArgs(ctypes.Structure):
     _fields_ = [("op", c_i32), ("dense_rows", c_i32), ("a", c_vp), ("b", c_vp), ("c", c_vp), ("c2", c_vp),
                 ("aux", c_vp), ("row_gate", c_vp), ("dgate_part", c_vp), ("poffsets", c_vp),
                 ("a_scales", c_vp), ("b_scales", c_vp), ("a_amax", c_vp), ("b_amax", c_vp), ("a_rows", c_vp),
-                ("slot_row", c_vp), ("b_scale_group", c_i32)]
+                ("slot_row", c_vp), ("b_scale_group", c_i32), ("q_codes", c_vp), ("q_scales", c_vp),
+                ("qt_codes", c_vp), ("qt_scales", c_vp)]
 
 
 _P = ctypes.POINTER
@@ -208,10 +209,11 @@ def moe_permute_noalloc(cfg, x, topk_idx, topk_gate, counts, offsets, poffsets, 
 
 def moe_grouped_gemm(cfg, op, a, b, c, ws, c2=None, aux=None, row_gate=None, dgate_part=None, poffsets=None,
                      dense_rows=0, a_scales=None, b_scales=None, a_amax=None, b_amax=None, a_rows=None,
-                     slot_row=None, b_scale_group=0, stream=None) -> None:
+                     slot_row=None, b_scale_group=0, q_codes=None, q_scales=None, qt_codes=None, qt_scales=None,
+                     stream=None) -> None:
     args = MoeGemmArgs(op, dense_rows, ptr(a), ptr(b), ptr(c), ptr(c2), ptr(aux), ptr(row_gate), ptr(dgate_part),
                        ptr(poffsets), ptr(a_scales), ptr(b_scales), ptr(a_amax), ptr(b_amax), ptr(a_rows),
-                       ptr(slot_row), int(b_scale_group))
+                       ptr(slot_row), int(b_scale_group), ptr(q_codes), ptr(q_scales), ptr(qt_codes), ptr(qt_scales))
     check(load().moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(args), ptr(ws), stream_ptr(stream)),
           "moe_grouped_gemm")
 

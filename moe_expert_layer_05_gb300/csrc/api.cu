@@ -163,8 +163,15 @@ moe_status compute_layout(const moe_config* c, int with_bwd, moe_act_layout* L) 
     } else {
       L->dzs = L->dxs = kNone;
     }
+    if (c->dtype == MOE_GEMM_MXFP8) {   // dz^T as the fc1 weight gradient reads it, left by the data gradient
+      L->dz_qt = take(2 * F * cap);
+      L->dz_qt_sf = take(2 * F * cap / 32);
+    } else {
+      L->dz_qt = L->dz_qt_sf = kNone;
+    }
   } else {
     L->dy_perm = L->dz = L->dx_perm = L->dgate_part = L->dlogits = L->row_dlogit = L->dzs = L->dxs = kNone;
+    L->dz_qt = L->dz_qt_sf = kNone;
   }
   L->total = off;
   return MOE_OK;
@@ -188,7 +195,7 @@ int mx_xt_group(const moe_config* c) { return c->H % 224 == 0 ? kMxScaleGroup224
 struct MxWs {
   MxBuf x, h, xs, hs;                             // forward
   MxBuf dy, dz, dys, dzs;                         // dgrad
-  MxBuf dzT, xT, dyT, hT, dzsT, xsT, dysT, hsT;   // wgrad (transposed: blocks along tokens)
+  MxBuf xT, dyT, hT, dzsT, xsT, dysT, hsT;        // wgrad (transposed: blocks along tokens; dz^T is in act)
   size_t total = 0;
 };
 
@@ -214,7 +221,7 @@ MxWs mx_ws_layout(const moe_config* c) {
   m.dy = buf(cap * H); m.dz = buf(cap * 2 * F); m.dys = buf(T * H);
   if (S) m.dzs = buf(T * 2 * S);
   region();
-  m.dzT = buf(2 * F * cap); m.dyT = buf(H * cap); m.hT = buf(F * cap);
+  m.dyT = buf(H * cap); m.hT = buf(F * cap);
   m.xT = buf(H * cap, mx_scale_bytes(H, cap, mx_xt_group(c)));   // rows grouped by 224 for the 256 x 224 tiles
   if (S) { m.dzsT = buf(2 * S * T); m.xsT = buf(H * T); m.dysT = buf(H * T); m.hsT = buf(S * T); }
   region();
@@ -364,9 +371,19 @@ moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool d
   }
   if (cfg->dtype == MOE_GEMM_BF16) {
     if (a->op == MOE_GG_FC1_SWIGLU_GATHERED && (dense || !dev_ptr_ok(a->a_rows))) return MOE_ERR_INVALID_ARG;
+    if (a->q_codes || a->q_scales || a->qt_codes || a->qt_scales) return MOE_ERR_INVALID_ARG;
     return (a->b_scale_group == 0 || a->b_scale_group == 128) ? MOE_OK : MOE_ERR_INVALID_ARG;
   }
   if (a->op == MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;     // bf16 only
+  // dz's MXFP8 copies from the fc2 data gradient's epilogue
+  const bool want_q = a->q_codes != nullptr || a->q_scales != nullptr;
+  const bool want_qt = a->qt_codes != nullptr || a->qt_scales != nullptr;
+  if (want_q || want_qt) {
+    if (cfg->dtype != MOE_GEMM_MXFP8 || a->op != MOE_GG_DGRAD_FC2 || dense || !gemm_mx_dgrad_fc2_quantises(cfg->F))
+      return MOE_ERR_INVALID_ARG;
+    if (want_q && (!dev_ptr_ok(a->q_codes) || !dev_ptr_ok(a->q_scales))) return MOE_ERR_INVALID_ARG;
+    if (want_qt && (!dev_ptr_ok(a->qt_codes) || !dev_ptr_ok(a->qt_scales))) return MOE_ERR_INVALID_ARG;
+  }
   if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
   // B's scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 (the GEMMs
   // whose N is H), routed, H % 224 == 0
@@ -637,10 +654,15 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
       case MOE_GG_FC2_COMBINE:
         return cuda_status(gemm_mx_fc2_combine(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->c,
                                                combine_args(cfg, a, ws), status, st));
-      case MOE_GG_DGRAD_FC2:
+      case MOE_GG_DGRAD_FC2: {
         if (!dev_ptr_ok(a->aux)) return MOE_ERR_INVALID_ARG;
+        const MxOutQ q{static_cast<uint8_t*>(a->q_codes), static_cast<uint8_t*>(a->q_scales),
+                       static_cast<uint8_t*>(a->qt_codes), static_cast<uint8_t*>(a->qt_scales)};
+        const bool any_q = q.codes != nullptr || q.codes_t != nullptr;
         return cuda_status(gemm_mx_dgrad_fc2(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
-                                             a->aux, a->row_gate, a->c, a->dgate_part, status, st));
+                                             a->aux, a->row_gate, a->c, a->dgate_part, status, st,
+                                             any_q ? &q : nullptr));
+      }
       case MOE_GG_DGRAD_FC1:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, 2 * F, a->b, a->b_scales, E, H, po,
                                            a->dense_rows, a->c, status, st,
@@ -880,9 +902,20 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
     auto wf = [&](const MxBuf& b) { return at<const uint8_t>(const_cast<void*>(w->mx), b.sf); };
     MOE_TRY(launch_quantize_rows(dy, T, H, 0, q(M.dys), f(M.dys), st));
     MOE_TRY(launch_gather_rows_mx(q(M.dys), f(M.dys), slot_row, T, k, H, q(M.dy), f(M.dy), st, counts, poff, E));
+    // dz's MXFP8 copies for the fc1 data gradient (rows, workspace) and the fc1
+    // weight gradient (transposed, act): from the epilogue where it can, else
+    // quantised from the bf16 dz
+    uint8_t* dz_qt = at<uint8_t>(act, L.dz_qt);
+    uint8_t* dz_qt_sf = at<uint8_t>(act, L.dz_qt_sf);
+    const MxOutQ dzq{q(M.dz), f(M.dz), dz_qt, dz_qt_sf};
+    const bool fused_q = gemm_mx_dgrad_fc2_quantises(F);
     MOE_TRY(gemm_mx_dgrad_fc2(q(M.dy), f(M.dy), cap, H, wq(W.w2t), wf(W.w2t), E, F, poff, 0, at<void>(act, L.z),
-                              at<float>(act, L.row_gate), dz, dpart, status, st));
-    MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st, 128, poff + E));
+                              at<float>(act, L.row_gate), fused_q ? nullptr : dz, dpart, status, st,
+                              fused_q ? &dzq : nullptr));
+    if (!fused_q) {
+      MOE_TRY(launch_quantize_rows(dz, cap, 2 * F, 0, q(M.dz), f(M.dz), st, 128, poff + E));
+      MOE_TRY(launch_quantize_cols(dz, 1, cap, 2 * F, dz_qt, dz_qt_sf, st, 128, poff + E));
+    }
     MOE_TRY(gemm_mx_nt_bf16(q(M.dz), f(M.dz), cap, 2 * F, wq(W.w1t), wf(W.w1t), E, H, poff, 0, dx_perm, status, st,
                             mx_b224(cfg) ? kMxScaleGroup224 : 128));
     if (S > 0 && T > 0) {
@@ -939,9 +972,10 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     // x and dy in expert order are read straight from token order through row_src
     const int32_t* row_src = at<int32_t>(act, L.row_src);
     // (rows past the last expert's padded end are skipped: no GEMM reads them)
-    MOE_TRY(launch_quantize_cols(at<void>(act, L.dz), 1, cap, 2 * F, q(M.dzT), f(M.dzT), st, 128, poff + E));
     MOE_TRY(launch_quantize_cols_gather(x, T, row_src, cap, H, q(M.xT), f(M.xT), st, mx_xt_group(cfg), poff + E));
-    MOE_TRY(gemm_mx_wgrad(q(M.dzT), f(M.dzT), 2 * F, q(M.xT), f(M.xT), H, cap, E, poff, 0, g->dw1, status, st,
+    // dz^T: left in act by the data gradient
+    MOE_TRY(gemm_mx_wgrad(at<uint8_t>(act, L.dz_qt), at<uint8_t>(act, L.dz_qt_sf), 2 * F, q(M.xT), f(M.xT), H, cap, E,
+                          poff, 0, g->dw1, status, st,
                           mx_xt_group(cfg)));
     MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st, 128, poff + E));
     MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st, 128, poff + E));

@@ -25,6 +25,7 @@
 // kernels).
 #pragma once
 #include "nvfp4.cuh"
+#include "mx_quant.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -93,6 +94,18 @@ struct GemmParams {
   // the token's valid slots sums the token's k rows of those columns in slot
   // order (fp32, plus the shared expert's row), writes y once and puts the
   // counter back to zero.
+  // MXFP8 copies of the output quantised in the epilogue for the GEMMs that
+  // read it next (the split SwiGLU-backward tiles; nullptr: none): q = rows
+  // quantised along the row, [rows_cap, ld_q] codes with ld_q / 128 scale
+  // tiles per tile row; qt = quantised along the rows (32-row blocks, one per
+  // epilogue warp) and transposed, [ld_q, rows_cap] codes with rows_cap / 128
+  // scale tiles per tile row.  Bit-identical to the standalone quantisers
+  // applied to the bf16 output.
+  uint8_t* q_codes;
+  uint8_t* q_sf;
+  uint8_t* qt_codes;
+  uint8_t* qt_sf;
+  int ld_q;
   const int32_t* cmb_row_src;      // [rows_cap] token of each row, -1 padding
   const int32_t* cmb_slot_row;     // [T, k] row of each (token, slot), -1 dropped
   int cmb_k;
@@ -489,6 +502,67 @@ struct Stager {
     __syncwarp();
   }
 };
+
+// One 32-column chunk of a bf16 output held by a warp, lane = row y + lane, o
+// = the row's 32 values as packed pairs, first column ocol.  The chunk goes
+// to the 64-byte-swizzled staging buffer; from there it is stored through tm
+// (nullptr: not stored) and, as p asks, quantised: q = this row's 32 values
+// as one MX block (from the registers); qt = column ocol + lane's 32 rows as
+// one block, transposed (the lane reads its column back from the staging, two
+// short loops, so the code stays small).
+template <int NBUF, int BUF>
+__device__ __forceinline__ void emit_chunk32(const GemmParams& p, Stager<NBUF, BUF>& st, const uint32_t (&o)[16],
+                                             int ocol, int y, int lane, const CUtensorMap* tm) {
+  st.begin();
+  #pragma unroll
+  for (int q = 0; q < 4; ++q) st.put_rows64_sw(q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  const bool want_qt = p.qt_codes != nullptr, want_q = p.q_codes != nullptr;
+  const uint32_t sbase = smem_u32(st.buf + st.cur * BUF);
+  if (want_qt) {
+    uint32_t t[8];
+    __syncwarp();                               // every row of the chunk is in the staging
+    // element (r, lane): 16-byte chunk lane/8 of row r, swizzled, element lane%8
+    const uint32_t col_off = static_cast<uint32_t>((lane & 7) * 2);
+    const uint32_t cj = static_cast<uint32_t>(lane >> 3);
+    auto elem = [&](int r) {
+      const uint32_t a = sbase + r * 64 + ((cj ^ ((r >> 1) & 3)) << 4) + col_off;
+      return __uint_as_float(ld_shared_u16(a) << 16);
+    };
+    float amax = 0.f;
+    #pragma unroll 4
+    for (int r = 0; r < 32; ++r) amax = fmaxf(amax, fabsf(elem(r)));
+    const int et = mx_exponent(amax);
+    const float sc = pow2_neg(et);
+    #pragma unroll
+    for (int r4 = 0; r4 < 8; ++r4)
+      t[r4] = e4m3_pack4(elem(4 * r4) * sc, elem(4 * r4 + 1) * sc, elem(4 * r4 + 2) * sc, elem(4 * r4 + 3) * sc);
+    // (transposed copy: this lane's column, 32 bytes, straight to its row of qt)
+    uint4* dst = reinterpret_cast<uint4*>(p.qt_codes + (long long)(ocol + lane) * p.rows_cap + y);
+    dst[0] = make_uint4(t[0], t[1], t[2], t[3]);
+    dst[1] = make_uint4(t[4], t[5], t[6], t[7]);
+    p.qt_sf[mx_sf_offset(ocol + lane, y >> 5, p.rows_cap >> 7)] = static_cast<uint8_t>(et + 127);
+  }
+  if (want_q) {
+    // (row copy: this lane's 32 bytes straight to its row)
+    float v[32];
+    #pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[2 * i] = bf16_lo(o[i]);
+      v[2 * i + 1] = bf16_hi(o[i]);
+    }
+    float amax = 0.f;
+    #pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int eq = mx_exponent(amax);
+    uint32_t w[8];
+    e4m3_pack32(v, pow2_neg(eq), w);
+    uint4* d = reinterpret_cast<uint4*>(p.q_codes + (long long)(y + lane) * p.ld_q + ocol);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    p.q_sf[mx_sf_offset(y + lane, ocol >> 5, p.ld_q >> 7)] = static_cast<uint8_t>(eq + 127);
+  }
+  if (tm != nullptr) st.flush(tm, ocol, y);     // the bf16 chunk
+}
 
 __device__ __forceinline__ void load32(uint32_t taddr, uint32_t (&a)[16], uint32_t (&b)[16]) {
   tmem_ld_x16(taddr, a);
@@ -1021,14 +1095,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
         og[j] = pack_bf16x2(g2[0], g2[1]);
         ou[j] = pack_bf16x2(u2[0], u2[1]);
       }
-      st.begin();
-      #pragma unroll
-      for (int q = 0; q < 4; ++q) st.put_rows64_sw(q, og[4 * q], og[4 * q + 1], og[4 * q + 2], og[4 * q + 3]);
-      st.flush(tmC2, colw + 32 * c, y);
-      st.begin();
-      #pragma unroll
-      for (int q = 0; q < 4; ++q) st.put_rows64_sw(q, ou[4 * q], ou[4 * q + 1], ou[4 * q + 2], ou[4 * q + 3]);
-      st.flush(tmC2, p.half_cols + colw + 32 * c, y);
+      const CUtensorMap* tm = (p.c != nullptr) ? tmC2 : nullptr;
+      emit_chunk32(p, st, og, colw + 32 * c, y, lane, tm);
+      emit_chunk32(p, st, ou, p.half_cols + colw + 32 * c, y, lane, tm);
     }
     if (row_ok && p.dgate_part != nullptr) p.dgate_part[(long long)row * parts + colw / 128] = dg;
   } else {  // kSwigluBwd: dz gate and up chunks of each 64 columns in one pass

@@ -179,9 +179,14 @@ cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc,
 #ifndef MOE_MX_DGRAD_FC2_BN
 #define MOE_MX_DGRAD_FC2_BN 256
 #endif
+bool gemm_mx_dgrad_fc2_quantises(int F) { return MOE_MX_DGRAD_FC2_BN == 256 && F % 256 == 0; }
+
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
-                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st) {
+                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st,
+                              const MxOutQ* q) {
+  if (q != nullptr && (!gemm_mx_dgrad_fc2_quantises(F) || poffsets == nullptr)) return cudaErrorInvalidValue;
+  if (q == nullptr && dz == nullptr) return cudaErrorInvalidValue;
   // B_e = W2_e^T [F, H], quantised along H.  256-column tiles where F allows:
   // one accumulator (256 columns beside the scale columns), 48 KB per k-block
   // of 128 x 256 x 128 instead of 32 KB per 128 x 128 x 128.
@@ -204,6 +209,13 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
   p.ld_aux = 2 * F;
   p.row_gate = row_gate;
   p.dgate_part = dgate_part;
+  if (q != nullptr) {                   // (the split 256-column epilogue writes them)
+    p.q_codes = q->codes;
+    p.q_sf = q->sf;
+    p.qt_codes = q->codes_t;
+    p.qt_sf = q->sf_t;
+    p.ld_q = 2 * F;
+  }
   p.rows_cap = rows_alloc;
   p.status = status;
   p.sfa = static_cast<const uint8_t*>(dysf);
@@ -211,7 +223,10 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
   CUtensorMap tc, tc32;
-  if (!make_tmap_out_bf16(&tc, dz, 2 * F, rows_alloc) || !make_tmap_out_bf16_32_sw64(&tc32, dz, 2 * F, rows_alloc))
+  // (no bf16 dz: the maps are encoded on the codes buffer and never used)
+  const void* dz_map = dz != nullptr ? dz : (q->codes != nullptr ? static_cast<const void*>(q->codes) : q->codes_t);
+  if (!make_tmap_out_bf16(&tc, dz_map, 2 * F, rows_alloc) ||
+      !make_tmap_out_bf16_32_sw64(&tc32, dz_map, 2 * F, rows_alloc))
     return cudaErrorInvalidValue;
   if (wide) {
     // (eight epilogue warps storing 32-column chunks through tc32)

@@ -139,9 +139,22 @@ cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int
 cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc, int F, const void* bq,
                                 const void* bsf, int E, int H, const int32_t* poffsets, void* o,
                                 const CombineArgs& cmb, int* status, cudaStream_t st);
+// MXFP8 copies of a GEMM output written by its epilogue: codes / sf = rows
+// quantised along the row, codes_t / sf_t = quantised along the rows and
+// transposed (nullptr: that copy is not written).
+struct MxOutQ {
+  uint8_t* codes;
+  uint8_t* sf;
+  uint8_t* codes_t;
+  uint8_t* sf_t;
+};
+// q (nullable): dz's MXFP8 copies ([cap, 2F] and [2F, cap]) from the epilogue;
+// only where gemm_mx_dgrad_fc2_quantises(F).  dz (bf16) may then be nullptr.
+bool gemm_mx_dgrad_fc2_quantises(int F);
 cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc, int H, const void* w2tq,
                               const void* w2tsf, int E, int F, const int32_t* poffsets, int dense_rows, const void* z,
-                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st);
+                              const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st,
+                              const MxOutQ* q = nullptr);
 // b_group 224: B's scale tiles grouped by 224 rows (256 x 224 tiles; N % 224 == 0, M % 256 == 0).
 cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,

@@ -15,67 +15,11 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "mx_quant.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
-
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t d;
-  // d[15:8] = e4m3(first source), d[7:0] = e4m3(second source)
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-// E8M0 exponent of a block whose largest magnitude is amax.
-__device__ __forceinline__ int mx_exponent(float amax) {
-  if (!(amax > 0.f)) return -127;
-  int e = ilogbf(amax) - 8;
-  return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
-
-// 2^-e as a float, e in [-127, 127] (2^-127 is subnormal).  Multiplying by a
-// power of two is exact except where the product is subnormal, and there it
-// rounds once to nearest even, exactly like scaling by 2^-e.
-__device__ __forceinline__ float pow2_neg(int e) {
-  return e < 127 ? __int_as_float((127 - e) << 23) : __int_as_float(0x00400000);
-}
-
-__device__ __forceinline__ size_t sf_offset(int r, int b, int tiles_per_row) {
-  return (static_cast<size_t>(r >> 7) * tiles_per_row + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 +
-         (b & 3);
-}
-
-// The same with the rows taken in groups of `group` (128, or 224 for the B
-// operand of 224-wide GEMM tiles): group g starts a new tile row, its rows
-// 0..127 fill tile row 2g and rows 128..223 the first 96 rows of tile row
-// 2g + 1 (the other 32 rows of that tile are never read).
-__device__ __forceinline__ size_t sf_offset_g(int r, int b, int tiles_per_row, int group) {
-  if (group == 128) return sf_offset(r, b, tiles_per_row);
-  const int g = r / group, i = r - g * group;
-  const int tr = 2 * g + (i >> 7), rr = i & 127;
-  return (static_cast<size_t>(tr) * tiles_per_row + (b >> 2)) * 512 + (rr & 31) * 16 + ((rr >> 5) & 3) * 4 + (b & 3);
-}
-
-// Quantise 32 values held by this thread; writes 32 code bytes and returns the scale byte.
-__device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst) {
-  float amax = 0.f;
-  #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int e = mx_exponent(amax);
-  const float sc = pow2_neg(e);
-  uint32_t w[8];
-  #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint16_t lo = cvt_e4m3x2(v[4 * i + 0] * sc, v[4 * i + 1] * sc);
-    const uint16_t hi = cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc);
-    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  return static_cast<uint8_t>(e + 127);
-}
 
 // Output row of input row r when the rows come in groups of 2*half (an
 // expert's [gate; up] projection) and are interleaved in 128-row blocks:
@@ -115,7 +59,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
     v[8 * q + 6] = bf16_lo(u[q].w); v[8 * q + 7] = bf16_hi(u[q].w);
   }
   const uint8_t s = quantize32(v, codes + r * cols + b * 32);
-  sf[sf_offset_g(static_cast<int>(r), b, cols / 128, group)] = s;
+  sf[mx_sf_offset_g(static_cast<int>(r), b, cols / 128, group)] = s;
 }
 
 // Blocks along the column, output transposed: src [rows, cols] bf16 ->
@@ -172,7 +116,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   const uint8_t e = quantize32(v, out);
   // scale bytes of one matrix: its output rows (the input columns) in groups
   const long long mat_sf = static_cast<long long>(group == 128 ? cols / 128 : 2 * (cols / group)) * rows * 4;
-  sf[mat * mat_sf + sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
+  sf[mat * mat_sf + mx_sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
 }
 
 // Padding rows of expert e's segment: zero codes and the scale of an
@@ -187,7 +131,7 @@ __device__ __forceinline__ void zero_pad_rows_mx(const int32_t* __restrict__ cou
   for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
   const long long m = static_cast<long long>(r1 - r0) * nb;
   for (long long i = threadIdx.x; i < m; i += blockDim.x)
-    sf[sf_offset(r0 + static_cast<int>(i / nb), static_cast<int>(i % nb), H / 128)] = 0;
+    sf[mx_sf_offset(r0 + static_cast<int>(i / nb), static_cast<int>(i % nb), H / 128)] = 0;
 }
 
 // Token-order quantised rows (codes [T, H] and their scale tiles) -> expert
@@ -220,10 +164,10 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __rest
   }
   const int nb = H / 32, tiles = H / 128;
   for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    const uint8_t e = sf_tok[sf_offset(t, b, tiles)];
+    const uint8_t e = sf_tok[mx_sf_offset(t, b, tiles)];
     for (int i = 0; i < k; ++i) {
       const int r = s_rows[i];
-      if (r >= 0) sf_perm[sf_offset(r, b, tiles)] = e;
+      if (r >= 0) sf_perm[mx_sf_offset(r, b, tiles)] = e;
     }
   }
 }

@@ -167,5 +167,19 @@ def test_low_precision_gemm_arguments_checked_before_launch():
     assert call_g(bf224, api.GG_FC2, 224) == -1
     for op in (api.GG_FC2, api.GG_DGRAD_FC1, api.GG_WGRAD_FC1):   # accepted: only the device check is left
         assert call_g(mx224, op, 224) != -1
+    # dz's MXFP8 copies: MXFP8 DGRAD_FC2 only, routed, F % 256 == 0, both pointers of a pair
+    def call_q(cfg, op, dense_rows=0, **kw):
+        a = api.MoeGemmArgs(op, dense_rows, 16, 16, 16, None, 16, None, None, 16, 16, 16, 16, 16)
+        for k_, v in kw.items():
+            setattr(a, k_, v)
+        return lib.moe_grouped_gemm(ctypes.byref(cfg), ctypes.byref(a), 16, None)
+
+    both = dict(q_codes=16, q_scales=16, qt_codes=16, qt_scales=16)
+    assert call_q(mx, api.GG_DGRAD_FC2, **both) != -1                 # F = 256: accepted
+    assert call_q(mx, api.GG_DGRAD_FC2, q_codes=16) == -1             # half a pair
+    assert call_q(mx, api.GG_FC2, **both) == -1
+    assert call_q(mx, api.GG_DGRAD_FC2, dense_rows=128, **both) == -1
+    assert call_q(api.make_config(256, 256, 8, 2, 256), api.GG_DGRAD_FC2, **both) == -1
+    assert call_q(api.make_config(256, 256, 8, 2, 384, dtype="mxfp8"), api.GG_DGRAD_FC2, **both) == -1
     assert lib.moe_quantize_mxfp8(16, 1, 200, 128, api.MX_ROWS_G224, 16, 16, None) == -1
     assert lib.moe_quantize_mxfp8(16, 1, 128, 256, api.MX_COLS_T_G224, 16, 16, None) == -1

@@ -307,6 +307,48 @@ def test_mx_gemm_256x224_tiles(lib, T, H, E, k, F, skew):
         assert torch.equal(a[:used].view(torch.int16), b[:used].view(torch.int16))
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(512, 256, 8, 2, 256, 0.0), (640, 512, 16, 4, 512, 1.5),
+                                             (384, 256, 64, 8, 256, 1.0)])
+def test_mx_gemm_dgrad_fc2_mxfp8_copies(lib, T, H, E, k, F, skew):
+    """The fc2 data gradient's epilogue also writing dz in MXFP8 (F % 256 ==
+    0): the row copy equals the row quantiser applied to the bf16 dz of the
+    same call, the transposed copy the column quantiser, codes and scales bit
+    for bit over every expert's padded rows; dz and the gate partials are the
+    same as without the copies."""
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 101)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    dy = _rows(cap, H, valid, 102)
+    z = _rows(cap, 2 * F, valid, 103).to(DEV)
+    w2 = to_bf16(_rand((E, H, F), 104, 0.05))
+    rg = torch.from_numpy(np.where(valid, np.abs(_rand((cap,), 105)), 0).astype(np.float32)).to(DEV)
+    dyq, dysf = quantize_gpu(dy.to(DEV), api.MX_ROWS)
+    w2tq, w2tsf = quantize_gpu(w2.to(DEV), api.MX_COLS_T, batch=E)
+    ws = _ws(cfg)
+    outs = []
+    for with_q in (False, True):
+        dz = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=DEV)
+        dpart = torch.zeros((cap, F // 128), dtype=torch.float32, device=DEV)
+        q = dict(q_codes=torch.full((cap * 2 * F,), 0xAB, dtype=torch.uint8, device=DEV),
+                 q_scales=torch.full((cap * 2 * F // 32,), 0xAB, dtype=torch.uint8, device=DEV),
+                 qt_codes=torch.full((cap * 2 * F,), 0xAB, dtype=torch.uint8, device=DEV),
+                 qt_scales=torch.full((cap * 2 * F // 32,), 0xAB, dtype=torch.uint8, device=DEV)) if with_q else {}
+        api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC2, dyq, w2tq, dz, ws, aux=z, row_gate=rg, dgate_part=dpart,
+                             poffsets=po, a_scales=dysf, b_scales=w2tsf, **q)
+        torch.cuda.synchronize()
+        assert api.moe_read_device_status(ws) == 0
+        outs.append((dz, dpart, q))
+    (dz0, dp0, _), (dz1, dp1, q) = outs
+    assert torch.equal(dz0[:used].view(torch.int16), dz1[:used].view(torch.int16))
+    assert torch.equal(dp0[:used], dp1[:used])
+    rc, rs = quantize_gpu(dz1[:used].contiguous(), api.MX_ROWS)
+    assert torch.equal(q["q_codes"][: used * 2 * F], rc)
+    np.testing.assert_array_equal(untile(q["q_scales"], cap, 2 * F)[:used], untile(rs, used, 2 * F))
+    tc, ts = quantize_gpu(dz1[:used].contiguous(), api.MX_COLS_T)          # [2F, used]
+    got_t = q["qt_codes"].view(2 * F, cap)[:, :used].contiguous().view(-1)
+    assert torch.equal(got_t, tc)
+    np.testing.assert_array_equal(untile(q["qt_scales"], 2 * F, cap)[:, : used // 32], untile(ts, 2 * F, used))
+
+
 @pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
 def test_mx_gemm_wgrad(lib, T, H, E, k, F, skew):
     cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 23)
@@ -416,6 +458,45 @@ def test_mx_layer_against_mxfp8_oracle(lib, name):
             assert r <= 3e-2, (gname, r)
 
 
+def test_mx_layer_dz_copies_without_the_fused_epilogue(lib):
+    """Where F % 256 != 0 the fc2 data gradient stores bf16 dz and the layer
+    quantises it: the transposed codes and scales left in act equal the column
+    quantiser applied to that dz, and the fc1 data gradient the layer computed
+    from the row copy equals, bit for bit, the same GEMM fed by the row
+    quantiser.  (Where F % 256 == 0 the epilogue writes both copies; see
+    test_mx_gemm_dgrad_fc2_mxfp8_copies.)"""
+    w = MX_LAYERS["dsv3_mx_small"]
+    inp = make_inputs(w, seed=4)
+    dinp = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    layer = api.MoELayer(api.config_of(w), dinp, with_backward=True)
+    layer.act.fill_(0x7F)
+    layer.forward(dinp["x"])
+    layer.backward(dinp["x"], dinp["dy"])
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(layer.ws) == 0
+    fl = layer.fields()
+    cap, F2, H, E = layer.layout.cap, 2 * w.F, w.H, w.E
+    used = int(fl["poffsets"][-1])
+    dz = fl["dz"]
+    # transposed copy: [2F, cap] codes, blocks along the rows
+    ref_t, ref_ts = quantize_gpu(dz[:used].contiguous(), api.MX_COLS_T)          # [2F, used]
+    got_t = layer.view("dz_qt", torch.uint8, (F2, cap))[:, :used]
+    assert torch.equal(got_t.contiguous().view(-1), ref_t)
+    got_ts = untile(layer.view("dz_qt_sf", torch.uint8, (F2 * cap // 32,)), F2, cap)[:, : used // 32]
+    np.testing.assert_array_equal(got_ts, untile(ref_ts, F2, used))
+    # row copy, through the fc1 data gradient
+    g = 224 if H % 224 == 0 else 0
+    dzq, dzsf = quantize_gpu(dz, api.MX_ROWS)
+    w1tq, w1tsf = quantize_gpu(dinp["w1"], api.MX_COLS_T_G224 if g else api.MX_COLS_T, batch=E)
+    dx = torch.zeros((cap, H), dtype=torch.bfloat16, device=DEV)
+    ws = _ws(layer.cfg)
+    api.moe_grouped_gemm(layer.cfg, api.GG_DGRAD_FC1, dzq, w1tq, dx, ws, poffsets=fl["poffsets"], a_scales=dzsf,
+                         b_scales=w1tsf, b_scale_group=g)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(ws) == 0
+    assert torch.equal(dx[:used].view(torch.int16), fl["dx_perm"][:used].view(torch.int16))
+
+
 def _stable_expert_tokens(w, x64, wr64, bias64, idx_gpu, counts):
     """A mid-sized expert all of whose tokens are routed away from near ties
     (fp64 top-k key gaps >= 1e-5), with its tokens and their oracle routing."""
@@ -443,7 +524,8 @@ def test_mx_full_size_training_sampled(lib):
     * a mid-sized expert e, over all of its tokens, against the oracle
       restricted to that expert (its gates given, as router replay does):
       dW1[e] and dW2[e] in full, the gate gradients of its slots, and sampled
-      rows of z, h', o, dz and dx_perm from the oracle's own step functions;
+      rows of z, h', o and dx_perm from the oracle's own step functions (dz
+      only in MXFP8, through dx_perm and dW1[e]);
     * dWr[e] as the router weight-gradient step on the layer's own dlogits."""
     from gpu_helpers import StreamExperts, check_full_permutation, i64, mx_weight_cache
     from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs_on_device
@@ -507,7 +589,8 @@ def test_mx_full_size_training_sampled(lib):
     dz, _ = O.expert_dgrad_fc2(O.mxfp8_roundtrip(dy64[rt], -1), ce[("w2", 0, 0)][None], z, seg, g_rows)
     dxp = O.expert_dgrad_fc1(O.mxfp8_roundtrip(dz, -1), ce[("w1", 0, 0)][None], seg)
     rows_t = torch.from_numpy(rows).to(DEV)
-    for what, name, ref in (("z", "z", z), ("h'", "h", hp), ("o", "o", o), ("dz", "dz", dz), ("dx_perm", "dx_perm", dxp)):
+    # (dz itself stays in MXFP8: its row copy feeds dx_perm, its transposed copy dW1[e], both checked)
+    for what, name, ref in (("z", "z", z), ("h'", "h", hp), ("o", "o", o), ("dx_perm", "dx_perm", dxp)):
         r = rel_l2(f64(fl[name][rows_t]), ref)
         assert r <= 3e-2, (what, r)
     # dWr[e] = sum over the tokens of e of dlogits[t, e] x[t] (the step, on the layer's dlogits)
