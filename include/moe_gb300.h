@@ -329,7 +329,8 @@ typedef struct {
    * q_codes [cap,2F] with q_scales (blocks along the row, as MOE_MX_ROWS) and
    * qt_codes [2F,cap] with qt_scales (blocks of 32 rows, transposed, as
    * MOE_MX_COLS_T), bit-identical to quantising the bf16 dz, rows < the last
-   * expert's padded end. */
+   * expert's padded end.  With both copies requested c may be NULL (no bf16
+   * dz is written). */
   void* q_codes;
   void* q_scales;
   void* qt_codes;

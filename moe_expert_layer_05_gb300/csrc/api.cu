@@ -606,7 +606,10 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
 
 moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void* ws, void* stream) {
   if (!config_ok(cfg) || a == nullptr || !dev_ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
-  if (!dev_ptr_ok(a->a) || !dev_ptr_ok(a->b) || !dev_ptr_ok(a->c)) return MOE_ERR_INVALID_ARG;
+  // (DGRAD_FC2 writing both MXFP8 copies of dz may leave the bf16 dz out)
+  const bool c_optional = a->op == MOE_GG_DGRAD_FC2 && a->c == nullptr && a->q_codes != nullptr &&
+                          a->qt_codes != nullptr;
+  if (!dev_ptr_ok(a->a) || !dev_ptr_ok(a->b) || (!c_optional && !dev_ptr_ok(a->c))) return MOE_ERR_INVALID_ARG;
   const bool dense = a->dense_rows > 0;
   if (!dense && !dev_ptr_ok(a->poffsets)) return MOE_ERR_INVALID_ARG;
   if (a->dense_rows < 0) return MOE_ERR_INVALID_ARG;

@@ -347,6 +347,16 @@ def test_mx_gemm_dgrad_fc2_mxfp8_copies(lib, T, H, E, k, F, skew):
     got_t = q["qt_codes"].view(2 * F, cap)[:, :used].contiguous().view(-1)
     assert torch.equal(got_t, tc)
     np.testing.assert_array_equal(untile(q["qt_scales"], 2 * F, cap)[:, : used // 32], untile(ts, 2 * F, used))
+    # without the bf16 dz (c = NULL), as the layer runs it: the same copies
+    q2 = {k_: torch.zeros_like(v) for k_, v in q.items()}
+    dpart2 = torch.zeros_like(dp1)
+    api.moe_grouped_gemm(cfg, api.GG_DGRAD_FC2, dyq, w2tq, None, ws, aux=z, row_gate=rg, dgate_part=dpart2,
+                         poffsets=po, a_scales=dysf, b_scales=w2tsf, **q2)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status(ws) == 0
+    assert torch.equal(dpart2[:used], dp1[:used])
+    assert torch.equal(q2["q_codes"][: used * 2 * F], q["q_codes"][: used * 2 * F])
+    assert torch.equal(q2["qt_codes"].view(2 * F, cap)[:, :used], q["qt_codes"].view(2 * F, cap)[:, :used])
 
 
 @pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
