@@ -794,7 +794,7 @@ def run_ours(args) -> dict | None:
 
 
 # ---------------------------------------------------------------- profiler captures
-PROFILE_OPS = GEMM_OPS + ("permute", "combine")
+PROFILE_OPS = GEMM_OPS + ("permute", "combine", "step")
 
 
 def profile_op(args) -> dict:
@@ -811,6 +811,31 @@ def profile_op(args) -> dict:
     if args.experts is not None:
         w = dataclasses.replace(w, E=args.experts)
     cfg = api.config_of(w)
+    if args.profile_op == "step":
+        # one whole step of the layer (forward, and backward where the workload
+        # trains) after three warm-up steps, launched eagerly
+        d = make_inputs_on_device(w, dev, seed=0, with_dy=w.backward)
+        layer = api.MoELayer(api.config_of(w), d, with_backward=w.backward, device=dev)
+        x, dy = d["x"], d["dy"]
+        y = torch.empty_like(x)
+        layer.forward(x, y)
+        grads = layer.backward(x, dy)[2] if w.backward else None
+
+        def one():
+            layer.forward(x, y)
+            if w.backward:
+                layer.backward(x, dy, grads)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        l0 = api.moe_kernel_launches()
+        torch.cuda.profiler.start()
+        one()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        return {"profile_op": "step", "workload": w.name, "T": w.T, "E": w.E,
+                "launches": api.moe_kernel_launches() - l0, "status": api.moe_read_device_status(layer.ws)}
     if args.profile_op in ("permute", "combine"):
         cfg = api.make_config(w.T, w.H, w.E, w.k, w.F, 0, w.score, "bf16")   # the routing and row copies only
         d = make_router_inputs_on_device(w, dev, seed=0)
