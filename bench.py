@@ -323,6 +323,10 @@ def op_work(w, op: str, n_active: int) -> tuple[float, float]:
     bw = ba = {"bf16": 2.0, "mxfp8": 1 + 1 / 32, "nvfp4": 0.5 + 1 / 16}[w.dtype]
     z_saved = w.backward
     if op == "fc1":
+        if w.dtype == "mxfp8":
+            # h' written only as its MXFP8 copies (rows; transposed too when training), as the layer runs it
+            return 4.0 * R * H * F, (n_active * 2 * F * H * bw + R * H * ba + R * F * ba * (2 if z_saved else 1)
+                                     + (R * 2 * F * 2 if z_saved else 0))
         return 4.0 * R * H * F, n_active * 2 * F * H * bw + R * H * ba + R * F * 2 + (R * 2 * F * 2 if z_saved else 0)
     if op == "fc2":
         return 2.0 * R * H * F, n_active * H * F * bw + R * F * ba + R * H * 2
@@ -454,10 +458,17 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
 
     xq, xsf = q(fl["x_perm"], 1, cap, H, api.MX_ROWS)
     w1q, w1sf = q(dinp["w1"], E, 2 * F, H, api.MX_ROWS_GATE_UP)
-    calls["fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, fl["h"], ws,
+    # as the layer runs it: h' only as its MXFP8 copies (the transposed one when training)
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+    hc = dict(q_codes=u8(cap * F), q_scales=u8(cap * F // 32))
+    if w.backward:
+        hc.update(qt_codes=u8(cap * F), qt_scales=u8(cap * F // 32))
+    calls["fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, None, ws,
                                                 c2=fl["z"] if w.backward else None, row_gate=fl["row_gate"],
-                                                poffsets=po, a_scales=xsf, b_scales=w1sf)
-    hq, hsf = q(fl["h"], 1, cap, F, api.MX_ROWS)
+                                                poffsets=po, a_scales=xsf, b_scales=w1sf, **hc)
+    calls["fc1"]()
+    torch.cuda.synchronize()
+    hq, hsf = hc["q_codes"], hc["q_scales"]
     w2q, w2sf = q(dinp["w2"], 1, E * H, F, api.MX_ROWS)
     # the layer runs fc2 and the fc1 data gradient on 256 x 224 tiles where H allows (B scales grouped by 224)
     g224 = 224 if H % 224 == 0 else 0
@@ -500,7 +511,7 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
                                                           poffsets=po, a_scales=dztsf, b_scales=xtsf,
                                                           b_scale_group=g224)
         dyt, dytsf = q(fl["dy_perm"], 1, cap, H, api.MX_COLS_T)
-        ht, htsf = q(fl["h"], 1, cap, F, api.MX_COLS_T)
+        ht, htsf = hc["qt_codes"], hc["qt_scales"]
         calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, dyt, ht, grads["dw2"], ws,
                                                           poffsets=po, a_scales=dytsf, b_scales=htsf)
     return calls

@@ -117,13 +117,15 @@ typedef struct {
  *   MXFP8 layers, backward only: dz_qt u8 [2F,cap] (dz quantised along the
  *   rows, 32-row blocks, and transposed: the fc1 weight gradient's A operand,
  *   written by moe_layer_backward_dgrad) and dz_qt_sf its scale tiles (cap/128
- *   tiles per tile row of 128 of the 2F rows).
+ *   tiles per tile row of 128 of the 2F rows); h_qt u8 [F,cap] and h_qt_sf,
+ *   h' the same way (the fc2 weight gradient's B operand, written by the
+ *   forward).  MXFP8 layers write h' only in MXFP8: h stays unwritten.
  * Fields that do not apply have offset SIZE_MAX. */
 typedef struct {
   size_t logits, topk_idx, topk_gate, counts, offsets, poffsets, slot_row, row_src, row_gate;
   size_t x_perm, z, h, o, zs, hs, os;
   size_t dy_perm, dz, dx_perm, dgate_part, dlogits, row_dlogit, dzs, dxs;
-  size_t dz_qt, dz_qt_sf;
+  size_t dz_qt, dz_qt_sf, h_qt, h_qt_sf;
   size_t total;          /* bytes the activation buffer needs */
   int32_t cap;           /* rows of the expert-ordered buffers */
   int32_t backward;      /* 1 if the backward fields are present */
@@ -324,13 +326,14 @@ typedef struct {
                              b's scales were written by MOE_MX_ROWS_G224 / MOE_MX_COLS_T_G224 (the
                              GEMM then runs 256 x 224 tiles); 0 (or 128) otherwise and for every
                              other op */
-  /* MXFP8 DGRAD_FC2 only (routed, F % 256 == 0; NULL pairs: not written): dz
-   * also written in MXFP8 by the epilogue, for the GEMMs that read it next --
-   * q_codes [cap,2F] with q_scales (blocks along the row, as MOE_MX_ROWS) and
-   * qt_codes [2F,cap] with qt_scales (blocks of 32 rows, transposed, as
-   * MOE_MX_COLS_T), bit-identical to quantising the bf16 dz, rows < the last
-   * expert's padded end.  With both copies requested c may be NULL (no bf16
-   * dz is written). */
+  /* MXFP8 DGRAD_FC2 (routed, F % 256 == 0) and FC1_SWIGLU (routed); NULL
+   * pairs: not written.  The output (dz, resp. h') also written in MXFP8 by
+   * the epilogue, for the GEMMs that read it next -- q_codes [cap,N] with
+   * q_scales (blocks along the row, as MOE_MX_ROWS) and qt_codes [N,cap] with
+   * qt_scales (blocks of 32 rows, transposed, as MOE_MX_COLS_T), N = 2F for
+   * dz and F for h'; bit-identical to quantising the bf16 output, rows < the
+   * last expert's padded end.  c may be NULL (no bf16 output written) for
+   * DGRAD_FC2 with both copies requested and for FC1_SWIGLU with the row copy. */
   void* q_codes;
   void* q_scales;
   void* qt_codes;

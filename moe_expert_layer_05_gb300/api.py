@@ -44,7 +44,8 @@ class MoeGrads(ctypes.Structure):
 
 _LAYOUT_FIELDS = ["logits", "topk_idx", "topk_gate", "counts", "offsets", "poffsets", "slot_row", "row_src",
                   "row_gate", "x_perm", "z", "h", "o", "zs", "hs", "os", "dy_perm", "dz", "dx_perm",
-                  "dgate_part", "dlogits", "row_dlogit", "dzs", "dxs", "dz_qt", "dz_qt_sf"]
+                  "dgate_part", "dlogits", "row_dlogit", "dzs", "dxs", "dz_qt", "dz_qt_sf", "h_qt",
+                  "h_qt_sf"]
 
 
 class MoeActLayout(ctypes.Structure):

@@ -163,15 +163,17 @@ moe_status compute_layout(const moe_config* c, int with_bwd, moe_act_layout* L) 
     } else {
       L->dzs = L->dxs = kNone;
     }
-    if (c->dtype == MOE_GEMM_MXFP8) {   // dz^T as the fc1 weight gradient reads it, left by the data gradient
+    if (c->dtype == MOE_GEMM_MXFP8) {   // dz^T and h'^T as the weight gradients read them
       L->dz_qt = take(2 * F * cap);
       L->dz_qt_sf = take(2 * F * cap / 32);
+      L->h_qt = take(F * cap);
+      L->h_qt_sf = take(F * cap / 32);
     } else {
-      L->dz_qt = L->dz_qt_sf = kNone;
+      L->dz_qt = L->dz_qt_sf = L->h_qt = L->h_qt_sf = kNone;
     }
   } else {
     L->dy_perm = L->dz = L->dx_perm = L->dgate_part = L->dlogits = L->row_dlogit = L->dzs = L->dxs = kNone;
-    L->dz_qt = L->dz_qt_sf = kNone;
+    L->dz_qt = L->dz_qt_sf = L->h_qt = L->h_qt_sf = kNone;
   }
   L->total = off;
   return MOE_OK;
@@ -195,7 +197,7 @@ int mx_xt_group(const moe_config* c) { return c->H % 224 == 0 ? kMxScaleGroup224
 struct MxWs {
   MxBuf x, h, xs, hs;                             // forward
   MxBuf dy, dz, dys, dzs;                         // dgrad
-  MxBuf xT, dyT, hT, dzsT, xsT, dysT, hsT;        // wgrad (transposed: blocks along tokens; dz^T is in act)
+  MxBuf xT, dyT, dzsT, xsT, dysT, hsT;            // wgrad (transposed: blocks along tokens; dz^T, h'^T in act)
   size_t total = 0;
 };
 
@@ -221,7 +223,7 @@ MxWs mx_ws_layout(const moe_config* c) {
   m.dy = buf(cap * H); m.dz = buf(cap * 2 * F); m.dys = buf(T * H);
   if (S) m.dzs = buf(T * 2 * S);
   region();
-  m.dyT = buf(H * cap); m.hT = buf(F * cap);
+  m.dyT = buf(H * cap);
   m.xT = buf(H * cap, mx_scale_bytes(H, cap, mx_xt_group(c)));   // rows grouped by 224 for the 256 x 224 tiles
   if (S) { m.dzsT = buf(2 * S * T); m.xsT = buf(H * T); m.dysT = buf(H * T); m.hsT = buf(S * T); }
   region();
@@ -375,12 +377,13 @@ moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool d
     return (a->b_scale_group == 0 || a->b_scale_group == 128) ? MOE_OK : MOE_ERR_INVALID_ARG;
   }
   if (a->op == MOE_GG_FC1_SWIGLU_GATHERED) return MOE_ERR_INVALID_ARG;     // bf16 only
-  // dz's MXFP8 copies from the fc2 data gradient's epilogue
+  // MXFP8 copies of the output from the epilogue: dz (fc2 data gradient) or h' (fc1)
   const bool want_q = a->q_codes != nullptr || a->q_scales != nullptr;
   const bool want_qt = a->qt_codes != nullptr || a->qt_scales != nullptr;
   if (want_q || want_qt) {
-    if (cfg->dtype != MOE_GEMM_MXFP8 || a->op != MOE_GG_DGRAD_FC2 || dense || !gemm_mx_dgrad_fc2_quantises(cfg->F))
-      return MOE_ERR_INVALID_ARG;
+    const bool op_ok = (a->op == MOE_GG_DGRAD_FC2 && gemm_mx_dgrad_fc2_quantises(cfg->F)) ||
+                       a->op == MOE_GG_FC1_SWIGLU;
+    if (cfg->dtype != MOE_GEMM_MXFP8 || !op_ok || dense) return MOE_ERR_INVALID_ARG;
     if (want_q && (!dev_ptr_ok(a->q_codes) || !dev_ptr_ok(a->q_scales))) return MOE_ERR_INVALID_ARG;
     if (want_qt && (!dev_ptr_ok(a->qt_codes) || !dev_ptr_ok(a->qt_scales))) return MOE_ERR_INVALID_ARG;
   }
@@ -606,9 +609,11 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
 
 moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void* ws, void* stream) {
   if (!config_ok(cfg) || a == nullptr || !dev_ptr_ok(ws)) return MOE_ERR_INVALID_ARG;
-  // (DGRAD_FC2 writing both MXFP8 copies of dz may leave the bf16 dz out)
-  const bool c_optional = a->op == MOE_GG_DGRAD_FC2 && a->c == nullptr && a->q_codes != nullptr &&
-                          a->qt_codes != nullptr;
+  // (DGRAD_FC2 writing both MXFP8 copies of dz may leave the bf16 dz out, FC1
+  // writing the row copy of h' the bf16 h')
+  const bool c_optional = a->c == nullptr && ((a->op == MOE_GG_DGRAD_FC2 && a->q_codes != nullptr &&
+                                               a->qt_codes != nullptr) ||
+                                              (a->op == MOE_GG_FC1_SWIGLU && a->q_codes != nullptr));
   if (!dev_ptr_ok(a->a) || !dev_ptr_ok(a->b) || (!c_optional && !dev_ptr_ok(a->c))) return MOE_ERR_INVALID_ARG;
   const bool dense = a->dense_rows > 0;
   if (!dense && !dev_ptr_ok(a->poffsets)) return MOE_ERR_INVALID_ARG;
@@ -647,10 +652,14 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
     if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
     if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
     switch (a->op) {
-      case MOE_GG_FC1_SWIGLU:
+      case MOE_GG_FC1_SWIGLU: {
         if (a->c2 != nullptr && !aligned16(a->c2)) return MOE_ERR_INVALID_ARG;
+        const MxOutQ q{static_cast<uint8_t*>(a->q_codes), static_cast<uint8_t*>(a->q_scales),
+                       static_cast<uint8_t*>(a->qt_codes), static_cast<uint8_t*>(a->qt_scales)};
+        const bool any_q = q.codes != nullptr || q.codes_t != nullptr;
         return cuda_status(gemm_mx_fc1(a->a, a->a_scales, rows, H, a->b, a->b_scales, E, F, po, a->dense_rows,
-                                       a->row_gate, a->c, a->c2, status, st));
+                                       a->row_gate, a->c, a->c2, status, st, any_q ? &q : nullptr));
+      }
       case MOE_GG_FC2:
         return cuda_status(gemm_mx_nt_bf16(a->a, a->a_scales, rows, F, a->b, a->b_scales, E, H, po, a->dense_rows,
                                            a->c, status, st, a->b_scale_group == 0 ? 128 : a->b_scale_group));
@@ -837,8 +846,12 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
                               status, st));
       shared_out = at<void>(act, L.os);
     }
-    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, h, z, status, st));
-    MOE_TRY(launch_quantize_rows(h, cap, F, 0, q(M.h), f(M.h), st, 128, poff + E));
+    // h' only in MXFP8, from fc1's epilogue: the row copy for fc2 (workspace) and,
+    // for training, the transposed copy for the fc2 weight gradient (act)
+    const MxOutQ hq{q(M.h), f(M.h), with_backward ? at<uint8_t>(act, L.h_qt) : nullptr,
+                    with_backward ? at<uint8_t>(act, L.h_qt_sf) : nullptr};
+    MOE_TRY(gemm_mx_fc1(q(M.x), f(M.x), cap, H, wq(W.w1), wf(W.w1), E, F, poff, 0, row_gate, nullptr, z, status, st,
+                        &hq));
     with_shared();
     if (fused_combine) {
       MOE_TRY(gemm_mx_fc2_combine(q(M.h), f(M.h), cap, F, wq(W.w2), wf(W.w2), E, H, poff, o, cmb, status, st));
@@ -981,8 +994,9 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
                           poff, 0, g->dw1, status, st,
                           mx_xt_group(cfg)));
     MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st, 128, poff + E));
-    MOE_TRY(launch_quantize_cols(at<void>(act, L.h), 1, cap, F, q(M.hT), f(M.hT), st, 128, poff + E));
-    MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, q(M.hT), f(M.hT), F, cap, E, poff, 0, g->dw2, status, st));
+    // h'^T: left in act by fc1
+    MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, at<uint8_t>(act, L.h_qt), at<uint8_t>(act, L.h_qt_sf), F, cap, E,
+                          poff, 0, g->dw2, status, st));
     if (S > 0 && T > 0) {
       MOE_TRY(launch_quantize_cols(at<void>(act, L.dzs), 1, T, 2 * S, q(M.dzsT), f(M.dzsT), st));
       MOE_TRY(launch_quantize_cols(x, 1, T, H, q(M.xsT), f(M.xsT), st));

@@ -170,7 +170,11 @@ struct GemmCfg {
   // elementwise backward is the long part of that epilogue), then stores dz in
   // 32-column chunks through 2 KB staging buffers, so the ring keeps 4 stages.
   static constexpr bool SPLIT_BWD = MX && !NV4 && EP == Epi::kSwigluBwd && BN == 256;
-  static constexpr bool SPLIT_COLS = (NV4 && EP == Epi::kSwiglu && BN == 256) || SPLIT_BWD;
+  // MXFP8 gated-SwiGLU tiles likewise: each warp takes 64 columns of h' (its
+  // 64 gate and 64 up accumulator columns), then writes z and h' (or h''s
+  // MXFP8 copies) in 32-column chunks through the same 2 KB staging.
+  static constexpr bool SPLIT_FWD = MX && !NV4 && EP == Epi::kSwiglu && BN == 256;
+  static constexpr bool SPLIT_COLS = (NV4 && EP == Epi::kSwiglu && BN == 256) || SPLIT_BWD || SPLIT_FWD;
   static constexpr int EPI_WARPS = (M256 || SPLIT_COLS) ? 8 : 4;
   // Shared memory (all of it dynamic): the k-block ring, 4 KB staging buffers
   // (32 rows x 128 B, 128B-swizzled) per epilogue warp -- two each, or one
@@ -193,7 +197,7 @@ struct GemmCfg {
                                       // waits in registers) where two would cost the ring a stage
                                       : (EP == Epi::kSwigluBwd) ? ((MX && BN == 256) ? 1 : 2)
                                       : ((TMA_OUT && RING_IF_TWO < 4) ? 1 : 2);
-  static constexpr int STAGING_BUF = SPLIT_BWD ? 2048 : 4096;   // bytes of one staging buffer
+  static constexpr int STAGING_BUF = (SPLIT_BWD || SPLIT_FWD) ? 2048 : 4096;   // bytes of one staging buffer
   static constexpr int STAGING_BYTES = TMA_OUT ? EPI_WARPS * STAGING_BUFS * STAGING_BUF : 0;
   static constexpr int STAGES_RAW = (SMEM_BUDGET - STAGING_BYTES - (MX ? 1024 : 0)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -512,11 +516,11 @@ struct Stager {
 // short loops, so the code stays small).
 template <int NBUF, int BUF>
 __device__ __forceinline__ void emit_chunk32(const GemmParams& p, Stager<NBUF, BUF>& st, const uint32_t (&o)[16],
-                                             int ocol, int y, int lane, const CUtensorMap* tm) {
+                                             int ocol, int y, int lane, const CUtensorMap* tm, bool quant = true) {
   st.begin();
   #pragma unroll
   for (int q = 0; q < 4; ++q) st.put_rows64_sw(q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-  const bool want_qt = p.qt_codes != nullptr, want_q = p.q_codes != nullptr;
+  const bool want_qt = quant && p.qt_codes != nullptr, want_q = quant && p.q_codes != nullptr;
   const uint32_t sbase = smem_u32(st.buf + st.cur * BUF);
   if (want_qt) {
     uint32_t t[8];
@@ -838,6 +842,55 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
     if constexpr (C::S == Sched::kRoutedM && C::BN == 256) {
       if (p.cmb_y != nullptr) fused_combine_rows(p, y, ti.n, lane, st);
     }
+    }
+  } else if constexpr (C::EP == Epi::kSwiglu && C::SPLIT_FWD) {
+    // gated SwiGLU on 8 warps: this warp's 64 columns of h' (half cpart of the
+    // tile's 128) -- its 64 gate and 64 up accumulator columns -- to
+    // registers, the accumulator handed back, then per 32 columns:
+    // h' = g * silu(a) * b, the saved z chunks (gate, up) and h' itself (bf16
+    // through tmC, and/or its MXFP8 copies) through the 2 KB staging
+    // (32-column boxes, 64-byte swizzle)
+    const int row = ti.m0 + quarter * 32 + lane;
+    const bool row_ok = (C::S != Sched::kDenseM) || (row < p.m_rows);
+    const float g = (p.row_gate != nullptr && row_ok) ? p.row_gate[row] : 1.0f;
+    const int colh = ti.n * (C::BN / 2) + 64 * cpart;
+    const int y = ti.m0 + quarter * 32;
+    uint32_t ga[64], ua[64];
+    #pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t a[16], b[16];
+      tmem_ld_x16(t0 + 64 * cpart + 16 * h, a);
+      tmem_ld_x16(t0 + C::BN / 2 + 64 * cpart + 16 * h, b);
+      tmem_ld_wait(a);
+      tmem_ld_wait(b);
+      #pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        ga[16 * h + j] = a[j];
+        ua[16 * h + j] = b[j];
+      }
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (release_bar != nullptr) {
+      if (lane == 0) mbar_arrive(release_bar);
+      *released = true;
+    }
+    #pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t hp[16], zg[16], zu[16];
+      #pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float a0 = __uint_as_float(ga[32 * c + 2 * j]) * al, a1 = __uint_as_float(ga[32 * c + 2 * j + 1]) * al;
+        const float b0 = __uint_as_float(ua[32 * c + 2 * j]) * al, b1 = __uint_as_float(ua[32 * c + 2 * j + 1]) * al;
+        hp[j] = pack_bf16x2(g * __fdividef(a0, 1.0f + __expf(-a0)) * b0, g * __fdividef(a1, 1.0f + __expf(-a1)) * b1);
+        zg[j] = pack_bf16x2(a0, a1);
+        zu[j] = pack_bf16x2(b0, b1);
+      }
+      if (p.c2 != nullptr) {
+        emit_chunk32(p, st, zg, colh + 32 * c, y, lane, tmC2, false);
+        emit_chunk32(p, st, zu, p.half_cols + colh + 32 * c, y, lane, tmC2, false);
+      }
+      emit_chunk32(p, st, hp, colh + 32 * c, y, lane, p.c != nullptr ? tmC : nullptr, true);
     }
   } else if constexpr (C::EP == Epi::kSwiglu) {
     // accumulator columns [0, BN/2) = gate rows of W1, [BN/2, BN) = the matching up rows

@@ -37,8 +37,10 @@ cudaError_t launch_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 
 cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
                         int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
-                        void* z, int* status, cudaStream_t st) {
+                        void* z, int* status, cudaStream_t st, const MxOutQ* q) {
   // w1q rows of one expert are [gate 0..127, up 0..127, gate 128..255, up 128..255, ...]
+  if (q != nullptr && poffsets == nullptr) return cudaErrorInvalidValue;
+  if (h == nullptr && (q == nullptr || q->codes == nullptr)) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, aq, H, rows_alloc, 128) || !make_tmap_u8(&tb, w1q, H, static_cast<uint64_t>(E) * 2 * F, 256))
     return cudaErrorInvalidValue;
@@ -61,8 +63,19 @@ cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, 
   p.sfb = static_cast<const uint8_t*>(w1sf);
   p.sfa_tiles_k = H / 128;
   p.sfb_tiles_k = H / 128;
+  if (q != nullptr) {                   // (the split SwiGLU epilogue writes them)
+    p.q_codes = q->codes;
+    p.q_sf = q->sf;
+    p.qt_codes = q->codes_t;
+    p.qt_sf = q->sf_t;
+    p.ld_q = F;
+  }
+  // 32-column boxes (eight split-column epilogue warps, 2 KB staging); without a
+  // bf16 h the map is encoded on the codes buffer and never used
   CUtensorMap tc, tz;
-  if (!make_tmap_out_bf16(&tc, h, F, rows_alloc) || (z != nullptr && !make_tmap_out_bf16(&tz, z, 2 * F, rows_alloc)))
+  const void* h_map = h != nullptr ? h : static_cast<const void*>(q->codes);
+  if (!make_tmap_out_bf16_32_sw64(&tc, h_map, F, rows_alloc) ||
+      (z != nullptr && !make_tmap_out_bf16_32_sw64(&tz, z, 2 * F, rows_alloc)))
     return cudaErrorInvalidValue;
   if (z == nullptr) tz = tc;
   if (poffsets != nullptr)

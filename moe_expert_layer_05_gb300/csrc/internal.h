@@ -127,18 +127,6 @@ constexpr int kMxScaleGroup224 = 224;
 cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
                                         uint8_t* codes, uint8_t* sf, cudaStream_t st, int group = 128,
                                         const int32_t* row_limit = nullptr);
-cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
-                        int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
-                        void* z, int* status, cudaStream_t st);
-// b_group: the row grouping of B's scale tiles (128, or 224: 256 x 224 tiles,
-// routed calls with N % 224 == 0).
-cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
-                            int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
-                            cudaStream_t st, int b_group = 128);
-// MXFP8 fc2 (N = H, H % 256 == 0) with the combine fused into its epilogue.
-cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc, int F, const void* bq,
-                                const void* bsf, int E, int H, const int32_t* poffsets, void* o,
-                                const CombineArgs& cmb, int* status, cudaStream_t st);
 // MXFP8 copies of a GEMM output written by its epilogue: codes / sf = rows
 // quantised along the row, codes_t / sf_t = quantised along the rows and
 // transposed (nullptr: that copy is not written).
@@ -148,6 +136,20 @@ struct MxOutQ {
   uint8_t* codes_t;
   uint8_t* sf_t;
 };
+// q (nullable; routed only): h''s MXFP8 copies ([cap, F] and [F, cap]) from
+// the epilogue; h (bf16) may then be nullptr if q->codes is given.
+cudaError_t gemm_mx_fc1(const void* aq, const void* asf, int rows_alloc, int H, const void* w1q, const void* w1sf,
+                        int E, int F, const int32_t* poffsets, int dense_rows, const float* row_gate, void* h,
+                        void* z, int* status, cudaStream_t st, const MxOutQ* q = nullptr);
+// b_group: the row grouping of B's scale tiles (128, or 224: 256 x 224 tiles,
+// routed calls with N % 224 == 0).
+cudaError_t gemm_mx_nt_bf16(const void* aq, const void* asf, int rows_alloc, int K, const void* bq, const void* bsf,
+                            int E, int N, const int32_t* poffsets, int dense_rows, void* c, int* status,
+                            cudaStream_t st, int b_group = 128);
+// MXFP8 fc2 (N = H, H % 256 == 0) with the combine fused into its epilogue.
+cudaError_t gemm_mx_fc2_combine(const void* aq, const void* asf, int rows_alloc, int F, const void* bq,
+                                const void* bsf, int E, int H, const int32_t* poffsets, void* o,
+                                const CombineArgs& cmb, int* status, cudaStream_t st);
 // q (nullable): dz's MXFP8 copies ([cap, 2F] and [2F, cap]) from the epilogue;
 // only where gemm_mx_dgrad_fc2_quantises(F).  dz (bf16) may then be nullptr.
 bool gemm_mx_dgrad_fc2_quantises(int F);

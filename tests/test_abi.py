@@ -188,6 +188,11 @@ def test_low_precision_gemm_arguments_checked_before_launch():
     assert call_q(mx, api.GG_DGRAD_FC2, q_codes=16) == -1             # half a pair
     assert call_q(mx, api.GG_DGRAD_FC2, c=None, q_codes=16, q_scales=16) == -1
     assert call_q(mx, api.GG_FC2, **both) == -1
+    assert call_q(mx, api.GG_FC1_SWIGLU, dense_rows=128, **both) == -1     # routed only
+    assert call_q(api.make_config(256, 256, 8, 2, 256), api.GG_FC1_SWIGLU, **both) == -1
+    if NO_GPU:
+        assert call_q(mx, api.GG_FC1_SWIGLU, **both) != -1                  # h''s copies: accepted
+        assert call_q(mx, api.GG_FC1_SWIGLU, c=None, q_codes=16, q_scales=16) != -1
     assert call_q(mx, api.GG_DGRAD_FC2, dense_rows=128, **both) == -1
     assert call_q(api.make_config(256, 256, 8, 2, 256), api.GG_DGRAD_FC2, **both) == -1
     assert call_q(api.make_config(256, 256, 8, 2, 384, dtype="mxfp8"), api.GG_DGRAD_FC2, **both) == -1

@@ -359,6 +359,48 @@ def test_mx_gemm_dgrad_fc2_mxfp8_copies(lib, T, H, E, k, F, skew):
     assert torch.equal(q2["qt_codes"].view(2 * F, cap)[:, :used], q["qt_codes"].view(2 * F, cap)[:, :used])
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(512, 256, 8, 2, 256, 0.0), (640, 512, 16, 4, 384, 1.5)])
+def test_mx_gemm_fc1_mxfp8_copies(lib, T, H, E, k, F, skew):
+    """fc1's epilogue also writing h' in MXFP8: the row copy equals the row
+    quantiser applied to the bf16 h' of the same call, the transposed copy the
+    column quantiser, codes and scales bit for bit over every expert's padded
+    rows; z and h' are the same as without the copies, and the copies are the
+    same without the bf16 h' (c = NULL)."""
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 111)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    x = _rows(cap, H, valid, 112)
+    w1 = to_bf16(_rand((E, 2 * F, H), 113, 0.05))
+    rg = torch.from_numpy(np.where(valid, np.abs(_rand((cap,), 114)), 0).astype(np.float32)).to(DEV)
+    xq, xsf = quantize_gpu(x.to(DEV), api.MX_ROWS)
+    w1q, w1sf = quantize_gpu(w1.to(DEV), api.MX_ROWS_GATE_UP, batch=E)
+    ws = _ws(cfg)
+    u8 = lambda n: torch.full((n,), 0xAB, dtype=torch.uint8, device=DEV)
+    outs = []
+    for mode in ("plain", "copies", "copies_only"):
+        h = torch.zeros((cap, F), dtype=torch.bfloat16, device=DEV) if mode != "copies_only" else None
+        z = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=DEV)
+        q = dict(q_codes=u8(cap * F), q_scales=u8(cap * F // 32), qt_codes=u8(cap * F),
+                 qt_scales=u8(cap * F // 32)) if mode != "plain" else {}
+        api.moe_grouped_gemm(cfg, api.GG_FC1_SWIGLU, xq, w1q, h, ws, c2=z, row_gate=rg, poffsets=po, a_scales=xsf,
+                             b_scales=w1sf, **q)
+        torch.cuda.synchronize()
+        assert api.moe_read_device_status(ws) == 0
+        outs.append((h, z, q))
+    (h0, z0, _), (h1, z1, q1), (_, z2, q2) = outs
+    for a, b in ((h0, h1), (z0, z1), (z0, z2)):
+        assert torch.equal(a[:used].view(torch.int16), b[:used].view(torch.int16))
+    rc, rs = quantize_gpu(h1[:used].contiguous(), api.MX_ROWS)
+    assert torch.equal(q1["q_codes"][: used * F], rc)
+    np.testing.assert_array_equal(untile(q1["q_scales"], cap, F)[:used], untile(rs, used, F))
+    tc, ts = quantize_gpu(h1[:used].contiguous(), api.MX_COLS_T)          # [F, used]
+    assert torch.equal(q1["qt_codes"].view(F, cap)[:, :used].contiguous().view(-1), tc)
+    np.testing.assert_array_equal(untile(q1["qt_scales"], F, cap)[:, : used // 32], untile(ts, F, used))
+    for k_ in ("q_codes", "q_scales"):
+        assert torch.equal(q2[k_][: used * F // (32 if "scales" in k_ else 1)],
+                           q1[k_][: used * F // (32 if "scales" in k_ else 1)])
+    assert torch.equal(q2["qt_codes"].view(F, cap)[:, :used], q1["qt_codes"].view(F, cap)[:, :used])
+
+
 @pytest.mark.parametrize("T,H,E,k,F,skew", MX_CASES)
 def test_mx_gemm_wgrad(lib, T, H, E, k, F, skew):
     cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 23)
@@ -534,8 +576,8 @@ def test_mx_full_size_training_sampled(lib):
     * a mid-sized expert e, over all of its tokens, against the oracle
       restricted to that expert (its gates given, as router replay does):
       dW1[e] and dW2[e] in full, the gate gradients of its slots, and sampled
-      rows of z, h', o and dx_perm from the oracle's own step functions (dz
-      only in MXFP8, through dx_perm and dW1[e]);
+      rows of z, o and dx_perm from the oracle's own step functions (h' and
+      dz only in MXFP8: through o, dx_perm, dW1[e] and dW2[e]);
     * dWr[e] as the router weight-gradient step on the layer's own dlogits."""
     from gpu_helpers import StreamExperts, check_full_permutation, i64, mx_weight_cache
     from moe_expert_layer_05_gb300.inputs import WORKLOADS, make_inputs_on_device
@@ -599,8 +641,9 @@ def test_mx_full_size_training_sampled(lib):
     dz, _ = O.expert_dgrad_fc2(O.mxfp8_roundtrip(dy64[rt], -1), ce[("w2", 0, 0)][None], z, seg, g_rows)
     dxp = O.expert_dgrad_fc1(O.mxfp8_roundtrip(dz, -1), ce[("w1", 0, 0)][None], seg)
     rows_t = torch.from_numpy(rows).to(DEV)
-    # (dz itself stays in MXFP8: its row copy feeds dx_perm, its transposed copy dW1[e], both checked)
-    for what, name, ref in (("z", "z", z), ("h'", "h", hp), ("o", "o", o), ("dx_perm", "dx_perm", dxp)):
+    # (h' and dz stay in MXFP8: h''s row copy feeds o and its transposed copy dW2[e], dz's feed
+    # dx_perm and dW1[e], all checked)
+    for what, name, ref in (("z", "z", z), ("o", "o", o), ("dx_perm", "dx_perm", dxp)):
         r = rel_l2(f64(fl[name][rows_t]), ref)
         assert r <= 3e-2, (what, r)
     # dWr[e] = sum over the tokens of e of dlogits[t, e] x[t] (the step, on the layer's dlogits)
