@@ -510,10 +510,16 @@ def gemm_op_calls(api, w, layer, dinp, grads, dev) -> dict:
         calls["wgrad_fc1"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC1, dzt, xt, grads["dw1"], ws,
                                                           poffsets=po, a_scales=dztsf, b_scales=xtsf,
                                                           b_scale_group=g224)
-        dyt, dytsf = q(fl["dy_perm"], 1, cap, H, api.MX_COLS_T)
         ht, htsf = hc["qt_codes"], hc["qt_scales"]
-        calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, dyt, ht, grads["dw2"], ws,
-                                                          poffsets=po, a_scales=dytsf, b_scales=htsf)
+        if g224 and F % 256 == 0:               # dW2^T on 256 x 224 tiles, stored transposed (operands swapped)
+            dyt, dytsf = q(fl["dy_perm"], 1, cap, H, api.MX_COLS_T_G224)
+            calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, ht, dyt, grads["dw2"], ws,
+                                                              poffsets=po, a_scales=htsf, b_scales=dytsf,
+                                                              b_scale_group=224)
+        else:
+            dyt, dytsf = q(fl["dy_perm"], 1, cap, H, api.MX_COLS_T)
+            calls["wgrad_fc2"] = lambda: api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, dyt, ht, grads["dw2"], ws,
+                                                              poffsets=po, a_scales=dytsf, b_scales=htsf)
     return calls
 
 

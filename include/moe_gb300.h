@@ -296,7 +296,11 @@ typedef enum {
  *               with b_scale_group = 224).
  *   WGRAD_FC1:  a = dz^T [2F,cap], b = x_perm^T [H,cap] (MOE_MX_COLS_T, or MOE_MX_COLS_T_G224
  *               with b_scale_group = 224).
- *   WGRAD_FC2:  a = dy_perm^T [H,cap], b = h^T [F,cap] (MOE_MX_COLS_T).
+ *   WGRAD_FC2:  a = dy_perm^T [H,cap], b = h^T [F,cap] (MOE_MX_COLS_T); or, with
+ *               b_scale_group = 224 (F % 256 == 0), the operands swapped: a = h^T
+ *               [F,cap] (MOE_MX_COLS_T), b = dy_perm^T [H,cap] (MOE_MX_COLS_T_G224),
+ *               the GEMM computing dW2^T on 256 x 224 tiles and storing them
+ *               transposed, so c is dW2 [E,H,F] either way.
  * Dense calls need dense_rows % 128 == 0.
  * NVFP4 (dtype == MOE_GEMM_NVFP4; forward ops only, the others return
  * MOE_ERR_UNSUPPORTED): a and b are E2M1 codes (see moe_quantize_nvfp4),
@@ -322,7 +326,8 @@ typedef struct {
   const float* b_amax;    /* NVFP4 only */
   const int32_t* a_rows;  /* FC1_SWIGLU_GATHERED, FC2_COMBINE */
   const int32_t* slot_row;/* FC2_COMBINE only */
-  int32_t b_scale_group;  /* MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 (routed, H % 224 == 0): 224 when
+  int32_t b_scale_group;  /* MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 / WGRAD_FC2 (routed, H % 224 == 0;
+                             WGRAD_FC2 also F % 256 == 0, operands swapped as above): 224 when
                              b's scales were written by MOE_MX_ROWS_G224 / MOE_MX_COLS_T_G224 (the
                              GEMM then runs 256 x 224 tiles); 0 (or 128) otherwise and for every
                              other op */

@@ -190,6 +190,9 @@ struct MxBuf {
 bool mx_b224(const moe_config* c) { return c->H % 224 == 0 && !kFuseCombine; }
 // x^T, the B operand of the routed fc1 weight gradient (N = H), likewise.
 int mx_xt_group(const moe_config* c) { return c->H % 224 == 0 ? kMxScaleGroup224 : 128; }
+// The routed fc2 weight gradient as dW2^T = h'^T-rows x dy^T (M = F, N = H)
+// on 256 x 224 tiles stored transposed: dy^T then keeps 224-row scale groups.
+bool mx_dw2_trans(const moe_config* c) { return c->H % 224 == 0 && c->F % 256 == 0; }
 
 // Transient quantised activations, placed in the workspace after the
 // histograms.  The forward, dgrad and wgrad calls each use their own set; the
@@ -223,7 +226,7 @@ MxWs mx_ws_layout(const moe_config* c) {
   m.dy = buf(cap * H); m.dz = buf(cap * 2 * F); m.dys = buf(T * H);
   if (S) m.dzs = buf(T * 2 * S);
   region();
-  m.dyT = buf(H * cap);
+  m.dyT = buf(H * cap, mx_scale_bytes(H, cap, mx_dw2_trans(c) ? kMxScaleGroup224 : 128));
   m.xT = buf(H * cap, mx_scale_bytes(H, cap, mx_xt_group(c)));   // rows grouped by 224 for the 256 x 224 tiles
   if (S) { m.dzsT = buf(2 * S * T); m.xsT = buf(H * T); m.dysT = buf(H * T); m.hsT = buf(S * T); }
   region();
@@ -389,10 +392,13 @@ moe_status gemm_args_check(const moe_config* cfg, const moe_gemm_args* a, bool d
   }
   if (!dev_ptr_ok(a->a_scales) || !dev_ptr_ok(a->b_scales)) return MOE_ERR_INVALID_ARG;
   // B's scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 (the GEMMs
-  // whose N is H), routed, H % 224 == 0
+  // whose N is H) and WGRAD_FC2 with its operands swapped (F % 256 == 0), routed,
+  // H % 224 == 0
   if (a->b_scale_group != 0 && a->b_scale_group != 128) {
     if (a->b_scale_group != kMxScaleGroup224 || cfg->dtype != MOE_GEMM_MXFP8 || dense || cfg->H % 224 != 0 ||
-        (a->op != MOE_GG_FC2 && a->op != MOE_GG_DGRAD_FC1 && a->op != MOE_GG_WGRAD_FC1))
+        (a->op != MOE_GG_FC2 && a->op != MOE_GG_DGRAD_FC1 && a->op != MOE_GG_WGRAD_FC1 &&
+         a->op != MOE_GG_WGRAD_FC2) ||
+        (a->op == MOE_GG_WGRAD_FC2 && cfg->F % 256 != 0))
       return MOE_ERR_INVALID_ARG;
   }
   if (dense && a->dense_rows % 128 != 0) return MOE_ERR_INVALID_ARG;
@@ -684,6 +690,9 @@ moe_status moe_grouped_gemm(const moe_config* cfg, const moe_gemm_args* a, void*
                                          static_cast<float*>(a->c), status, st,
                                          a->b_scale_group == 0 ? 128 : a->b_scale_group));
       case MOE_GG_WGRAD_FC2:
+        if (a->b_scale_group == kMxScaleGroup224)   // operands swapped: a = h'^T, b = dy^T; c still [E, H, F]
+          return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, F, a->b, a->b_scales, H, rows, E, po, a->dense_rows,
+                                           static_cast<float*>(a->c), status, st, kMxScaleGroup224, true));
         return cuda_status(gemm_mx_wgrad(a->a, a->a_scales, H, a->b, a->b_scales, F, rows, E, po, a->dense_rows,
                                          static_cast<float*>(a->c), status, st));
       default:
@@ -993,10 +1002,17 @@ moe_status moe_layer_backward_wgrad(const moe_config* cfg, const moe_weights* w,
     MOE_TRY(gemm_mx_wgrad(at<uint8_t>(act, L.dz_qt), at<uint8_t>(act, L.dz_qt_sf), 2 * F, q(M.xT), f(M.xT), H, cap, E,
                           poff, 0, g->dw1, status, st,
                           mx_xt_group(cfg)));
-    MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st, 128, poff + E));
     // h'^T: left in act by fc1
-    MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, at<uint8_t>(act, L.h_qt), at<uint8_t>(act, L.h_qt_sf), F, cap, E,
-                          poff, 0, g->dw2, status, st));
+    if (mx_dw2_trans(cfg)) {
+      MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st, kMxScaleGroup224,
+                                          poff + E));
+      MOE_TRY(gemm_mx_wgrad(at<uint8_t>(act, L.h_qt), at<uint8_t>(act, L.h_qt_sf), F, q(M.dyT), f(M.dyT), H, cap, E,
+                            poff, 0, g->dw2, status, st, kMxScaleGroup224, true));
+    } else {
+      MOE_TRY(launch_quantize_cols_gather(dy, T, row_src, cap, H, q(M.dyT), f(M.dyT), st, 128, poff + E));
+      MOE_TRY(gemm_mx_wgrad(q(M.dyT), f(M.dyT), H, at<uint8_t>(act, L.h_qt), at<uint8_t>(act, L.h_qt_sf), F, cap, E,
+                            poff, 0, g->dw2, status, st));
+    }
     if (S > 0 && T > 0) {
       MOE_TRY(launch_quantize_cols(at<void>(act, L.dzs), 1, T, 2 * S, q(M.dzsT), f(M.dzsT), st));
       MOE_TRY(launch_quantize_cols(x, 1, T, H, q(M.xsT), f(M.xsT), st));

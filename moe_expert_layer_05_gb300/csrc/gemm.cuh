@@ -63,6 +63,8 @@ struct GemmParams {
   const float* row_gate;   // per output row gate (nullptr: 1.0)
   float* dgate_part;       // kSwigluBwd: [rows, n_tiles] partial dot products
   int valid_cols;          // kStoreF32: store only columns < valid_cols
+  int c_trans;             // kStoreF32, kRoutedK: output stored transposed, element (m, n) of group g
+                           // at c[g * c_group_stride + n * m_rows + m]
   int rows_cap;            // rows allocated in the expert-ordered buffers (routed modes)
   // MXFP8 / NVFP4: scale tiles of A and B (512 B per 128 rows x 128 K of
   // E8M0, or x 64 K of E4M3; see mxfp8.cu, nvfp4.cu) and the number of tiles
@@ -718,6 +720,32 @@ __device__ __forceinline__ void epilogue_tile_tma(const GemmParams& p, const Til
             st.put(j, w[0], w[1], w[2], w[3]);
           }
           st.flush(tmC, ti.n * C::BN + 128 + 32 * c, y);
+        }
+        return;
+      }
+    }
+    if constexpr (C::S == Sched::kRoutedK) {
+      if (p.c_trans) {
+        // transposed: the 32 x 32 block (rows y.., columns c0..) goes to the
+        // staging as 32 rows of one column each (row j = column c0 + j, 128
+        // bytes, 16-byte chunks in the 128-byte swizzled order; lane = element
+        // within the row, so each store of the warp hits 32 distinct banks)
+        // and from there to rows group * N + n0 + c0.. of the [E * N, M] output
+        const uint32_t lane_off = static_cast<uint32_t>((lane & 3) * 4);
+        const uint32_t lane_chunk = static_cast<uint32_t>(lane >> 2);
+        #pragma unroll 1
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          uint32_t a[16], b[16];
+          load32(t0 + c0, a, b);
+          st.begin();
+          const uint32_t base = smem_u32(st.buf + st.cur * C::STAGING_BUF);
+          #pragma unroll
+          for (int j = 0; j < 16; ++j)
+            st_shared_u32(base + j * 128 + ((lane_chunk ^ (j & 7)) << 4) + lane_off, no_mma ? 0u : a[j]);
+          #pragma unroll
+          for (int j = 0; j < 16; ++j)
+            st_shared_u32(base + (16 + j) * 128 + ((lane_chunk ^ (j & 7)) << 4) + lane_off, no_mma ? 0u : b[j]);
+          st.flush(tmC, ti.m0 + quarter * 32, ti.group * p.n_tiles * C::BN + ti.n * C::BN + c0);
         }
         return;
       }

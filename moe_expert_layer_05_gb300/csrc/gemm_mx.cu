@@ -295,7 +295,7 @@ namespace {
 // 256 x 224 outputs instead of 48 KB for 128 x 256, and eight epilogue warps.
 cudaError_t mx_wgrad_224(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                          int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool c_trans) {
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, atq, rows_alloc, M, 256) || !make_tmap_u8(&tb, btq, rows_alloc, N, 224))
     return cudaErrorInvalidValue;
@@ -315,8 +315,11 @@ cudaError_t mx_wgrad_224(const void* atq, const void* atsf, int M, const void* b
   p.sfb = static_cast<const uint8_t*>(btsf);
   p.sfa_tiles_k = rows_alloc / 128;
   p.sfb_tiles_k = rows_alloc / 128;
+  p.c_trans = c_trans ? 1 : 0;
   CUtensorMap tc;
-  if (!make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M)) return cudaErrorInvalidValue;
+  const bool map_ok = c_trans ? make_tmap_out_f32(&tc, dw, M, static_cast<uint64_t>(p.E) * N)
+                              : make_tmap_out_f32(&tc, dw, N, static_cast<uint64_t>(p.E) * M);
+  if (!map_ok) return cudaErrorInvalidValue;
   return launch_mx<GemmCfg<224, false, false, Sched::kRoutedK, Epi::kStoreF32, true, true>>(ta, tb, tc, tc, p,
                                                                                            rows_alloc, dense_rows, st);
 }
@@ -324,11 +327,12 @@ cudaError_t mx_wgrad_224(const void* atq, const void* atsf, int M, const void* b
 
 cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
-                          cudaStream_t st, int b_group) {
+                          cudaStream_t st, int b_group, bool c_trans) {
   if (b_group == kMxScaleGroup224) {
     if (N % 224 != 0 || M % 256 != 0) return cudaErrorInvalidValue;
-    return mx_wgrad_224(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
+    return mx_wgrad_224(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st, c_trans);
   }
+  if (c_trans) return cudaErrorInvalidValue;
   if (N % 256 == 0)
     return mx_wgrad_bn<256>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);
   return mx_wgrad_bn<128>(atq, atsf, M, btq, btsf, N, rows_alloc, E, poffsets, dense_rows, dw, status, st);

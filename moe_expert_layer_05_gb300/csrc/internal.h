@@ -158,9 +158,10 @@ cudaError_t gemm_mx_dgrad_fc2(const void* dyq, const void* dysf, int rows_alloc,
                               const float* row_gate, void* dz, float* dgate_part, int* status, cudaStream_t st,
                               const MxOutQ* q = nullptr);
 // b_group 224: B's scale tiles grouped by 224 rows (256 x 224 tiles; N % 224 == 0, M % 256 == 0).
+// c_trans (b_group 224 only): dw is [E, N, M], the tiles stored transposed.
 cudaError_t gemm_mx_wgrad(const void* atq, const void* atsf, int M, const void* btq, const void* btsf, int N,
                           int rows_alloc, int E, const int32_t* poffsets, int dense_rows, float* dw, int* status,
-                          cudaStream_t st, int b_group = 128);
+                          cudaStream_t st, int b_group = 128, bool c_trans = false);
 
 // ------------------------------------------------------------ NVFP4 (nvfp4.cu, gemm_mx.cu)
 // *amax = max |v| over a bf16 [rows, cols] tensor (rows with row_src < 0 skipped

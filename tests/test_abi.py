@@ -156,7 +156,8 @@ def test_low_precision_gemm_arguments_checked_before_launch():
         assert call(nv, op) == -2
     assert call(mx, api.GG_FC2, scales=None) == -1
     assert call(mx, api.GG_FC1_SWIGLU, dense_rows=100) == -1
-    # B scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1, routed, H % 224 == 0 only
+    # B scale tiles grouped by 224 rows: MXFP8 FC2 / DGRAD_FC1 / WGRAD_FC1 / WGRAD_FC2 (F % 256 == 0),
+    # routed, H % 224 == 0 only
     mx224 = api.make_config(256, 896, 8, 2, 256, dtype="mxfp8")
     bf224 = api.make_config(256, 896, 8, 2, 256)
 
@@ -168,11 +169,11 @@ def test_low_precision_gemm_arguments_checked_before_launch():
     assert call_g(mx, api.GG_FC2, 224) == -1                   # H = 256
     assert call_g(mx224, api.GG_FC2, 100) == -1
     assert call_g(mx224, api.GG_FC1_SWIGLU, 224) == -1
-    assert call_g(mx224, api.GG_WGRAD_FC2, 224) == -1
+    assert call_g(api.make_config(256, 896, 8, 2, 384, dtype="mxfp8"), api.GG_WGRAD_FC2, 224) == -1   # F % 256
     assert call_g(mx224, api.GG_FC2, 224, dense_rows=128) == -1
     assert call_g(bf224, api.GG_FC2, 224) == -1
     if NO_GPU:
-        for op in (api.GG_FC2, api.GG_DGRAD_FC1, api.GG_WGRAD_FC1):   # accepted: only the device check is left
+        for op in (api.GG_FC2, api.GG_DGRAD_FC1, api.GG_WGRAD_FC1, api.GG_WGRAD_FC2):   # accepted: device check left
             assert call_g(mx224, op, 224) != -1
     # dz's MXFP8 copies: MXFP8 DGRAD_FC2 only, routed, F % 256 == 0, both pointers of a pair
     def call_q(cfg, op, dense_rows=0, **kw):

@@ -452,6 +452,37 @@ def test_mx_gemm_wgrad_256x224_tiles(lib, T, H, E, k, F, skew):
     assert torch.equal(out[0], out[1])
 
 
+@pytest.mark.parametrize("T,H,E,k,F,skew", [(512, 896, 8, 2, 256, 0.0), (640, 896, 16, 4, 512, 1.5)])
+def test_mx_gemm_wgrad_fc2_transposed_tiles(lib, T, H, E, k, F, skew):
+    """The fc2 weight gradient with its operands swapped (dW2^T = h'^T x dy^T
+    on 256 x 224 tiles, dy^T's scales grouped by 224 rows, tiles stored
+    transposed): dW2 [E, H, F] against the oracle, zero for empty experts, and
+    against the unswapped GEMM."""
+    cfg, m, cap, used, valid = _routed(T, H, E, k, F, skew, 95)
+    po = torch.from_numpy(m["poffsets"].astype(np.int32)).to(DEV)
+    dy = _rows(cap, H, valid, 96)
+    hp = _rows(cap, F, valid, 97)
+    dyT, dyTs = quantize_gpu(dy.to(DEV), api.MX_COLS_T)          # [H, cap]
+    dyTg, dyTgs = quantize_gpu(dy.to(DEV), api.MX_COLS_T_G224)
+    hT, hTs = quantize_gpu(hp.to(DEV), api.MX_COLS_T)            # [F, cap]
+    ws = _ws(cfg)
+    out = []
+    for a_, as_, b_, bs_, g in ((dyT, dyTs, hT, hTs, 0), (hT, hTs, dyTg, dyTgs, 224)):
+        dw2 = torch.full((E, H, F), 7.0, dtype=torch.float32, device=DEV)
+        api.moe_grouped_gemm(cfg, api.GG_WGRAD_FC2, a_, b_, dw2, ws, poffsets=po, a_scales=as_, b_scales=bs_,
+                             b_scale_group=g)
+        torch.cuda.synchronize()
+        assert api.moe_read_device_status(ws) == 0
+        out.append(dw2)
+    a = O.mxfp8_roundtrip(f64(dy), axis=0)[:used]
+    bq = O.mxfp8_roundtrip(f64(hp), axis=0)[:used]
+    ref = O.expert_wgrad(a, bq, m["poffsets"])
+    scale = np.einsum("rm,rn->mn", np.abs(a), np.abs(bq))
+    assert np.all(np.abs(f64(out[1]) - ref) <= 2.0 ** -14 * scale[None] + 1e-6)
+    assert np.all(f64(out[1])[m["counts"] == 0] == 0)
+    assert np.all(np.abs(f64(out[1]) - f64(out[0])) <= 2.0 ** -20 * scale[None] + 1e-7)
+
+
 # ------------------------------------------------------------------ layer
 MX_LAYERS = {
     "dsv3_mx_small": Workload("dsv3_mx_small", T=384, H=256, E=64, k=8, F=128, S=256, score="sigmoid", zipf_s=1.2,
