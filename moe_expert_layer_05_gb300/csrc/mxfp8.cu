@@ -65,58 +65,98 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // Blocks along the column, output transposed: src [rows, cols] bf16 ->
 // codes [cols, rows] (row c of the output = column c of the input), scales
 // tiled over the [cols, rows] output.  batch: independent matrices one after
-// another (expert weights).  A block reads a 128-row x 64-column tile with
-// 16-byte loads into shared memory; thread (c, q) quantises rows 32q..32q+31
-// of column c.  The four threads of a column sit next to each other in a warp,
-// so their 32-byte pieces of one output row form a full 128-byte line.
-// Shared memory: element (r, c) in 16-byte chunk (c / 8) ^ (r / 32) of row r,
-// so the four row blocks read by one warp fall in different banks.
+// another (expert weights).  Tiles of 128 rows x 64 columns; thread (c, q)
+// quantises rows 32q..32q+31 of column c.  The four threads of a column sit
+// next to each other in a warp, so their 32-byte pieces of one output row form
+// a full 128-byte line.  Shared memory: element (r, c) in 16-byte chunk
+// (c / 8) ^ (r / 32) of row r, so the four row blocks read by one warp fall in
+// different banks.
+// Persistent: a block walks tiles blockIdx.x, + gridDim.x, ... (row blocks
+// fastest, then column blocks, then matrices, so the blocks in flight share
+// one 64-column slice of the source), quantising one tile while the next
+// one's rows land in the other half of a double buffer (cp.async, 16-byte
+// pieces, zero-filled for zero rows) and the row indices of the one after are
+// read.  The tile walk steps without divisions (with 64-bit divisions per tile
+// the kernel was slower than the one-shot version it replaced).
 // row_map (nullable, batch 1 only): input row r is src row row_map[r], or a
 // zero row where row_map[r] is outside [0, src_rows) -- the expert-ordered
 // rows read straight from token order through row_src, padding rows zero.
-__global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows,
-                                                            int cols, const int32_t* __restrict__ row_map,
-                                                            int src_rows, int group,
-                                                            const int32_t* __restrict__ row_limit,
+// row_limit (nullable): row blocks from row_limit[0] on are neither read nor
+// written (rows past the last expert).
+__global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int batch,
+                                                            int rows, int cols,
+                                                            const int32_t* __restrict__ row_map, int src_rows,
+                                                            int group, const int32_t* __restrict__ row_limit,
                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
-  __shared__ uint4 tile[128][8];           // 128 rows x 64 bf16
-  const int rb = blockIdx.x;               // block of 128 input rows
-  if (row_limit != nullptr && rb * 128 >= __ldg(row_limit)) return;   // past the last expert: never read
-  const int c0 = blockIdx.y * 64;
-  const long long mat = blockIdx.z;
-  const __nv_bfloat16* base = src + mat * rows * cols + static_cast<long long>(rb) * 128 * cols + c0;
-  #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = threadIdx.x + 256 * k;   // 16-byte piece i: row i / 8, chunk i % 8
-    const int r = i >> 3, j = i & 7;
-    uint4 v;
-    if (row_map != nullptr) {
-      const int t = row_map[rb * 128 + r];
-      v = (t >= 0 && t < src_rows)
-              ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(t) * cols + c0) + j)
-              : make_uint4(0, 0, 0, 0);
-    } else {
-      v = __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * cols) + j);
+  __shared__ uint4 tile[2][128 * 8];       // two 128-row x 64-column tiles
+  int nrb = rows / 128;
+  if (row_limit != nullptr) nrb = min(nrb, (__ldg(row_limit) + 127) / 128);
+  const int ncb = cols / 64;
+  const int total = nrb * ncb * batch;
+  const int G = static_cast<int>(gridDim.x);
+  int t = static_cast<int>(blockIdx.x);
+  if (t >= total) return;
+  const int j = threadIdx.x & 7, r0 = threadIdx.x >> 3;   // pieces: rows r0 + 32 k, chunk j
+  const int lim = row_map != nullptr ? src_rows : rows;
+  int idx[4];
+  auto rows_of = [&](int rb) {
+    #pragma unroll
+    for (int k = 0; k < 4; ++k)
+      idx[k] = row_map != nullptr ? __ldg(row_map + rb * 128 + r0 + 32 * k) : rb * 128 + r0 + 32 * k;
+  };
+  auto issue = [&](int rb, int cb, int mat, int buf) {
+    const __nv_bfloat16* m = src + static_cast<long long>(mat) * rows * cols + cb * 64 + 8 * j;
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = r0 + 32 * k;
+      const bool ok = idx[k] >= 0 && idx[k] < lim;
+      cp_async_16(smem_u32(&tile[buf][r * 8 + (j ^ (r >> 5))]), ok ? m + static_cast<long long>(idx[k]) * cols : src,
+                  ok ? 16u : 0u);
     }
-    tile[r][j ^ (r >> 5)] = v;
-  }
-  __syncthreads();
+  };
+  const int g_cb = G / nrb, g_rb = G - g_cb * nrb;   // one step of G tiles: column blocks and rows blocks
+  auto advance = [&](int& rb, int& cb, int& mat) {
+    rb += g_rb;
+    cb += g_cb;
+    if (rb >= nrb) { rb -= nrb; ++cb; }
+    if (batch > 1) { mat += cb / ncb; cb %= ncb; }   // (batch 1: t < total keeps cb < ncb)
+  };
+  int rb = t % nrb, cb = (t / nrb) % ncb, mat = t / (nrb * ncb);
+  rows_of(rb);
+  issue(rb, cb, mat, 0);
+  cp_async_commit();
+  int rbn = rb, cbn = cb, matn = mat;
+  advance(rbn, cbn, matn);
+  if (t + G < total) rows_of(rbn);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cl = warp * 8 + (lane >> 2);   // column inside the tile
   const int q = lane & 3;                  // block of 32 rows inside the tile
-  const __nv_bfloat16* t = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]);
-  float v[32];
-  #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int r = 32 * q + i;
-    v[i] = __bfloat162float(t[r * 64 + (((cl >> 3) ^ q) << 3) + (cl & 7)]);
-  }
-  const int c = c0 + cl;
-  uint8_t* out = codes + mat * rows * cols + static_cast<long long>(c) * rows + rb * 128 + 32 * q;
-  const uint8_t e = quantize32(v, out);
   // scale bytes of one matrix: its output rows (the input columns) in groups
   const long long mat_sf = static_cast<long long>(group == 128 ? cols / 128 : 2 * (cols / group)) * rows * 4;
-  sf[mat * mat_sf + mx_sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
+  for (int buf = 0; t < total; t += G, buf ^= 1) {
+    if (t + G < total) issue(rbn, cbn, matn, buf ^ 1);
+    cp_async_commit();
+    int rb2 = rbn, cb2 = cbn, mat2 = matn;
+    advance(rb2, cb2, mat2);
+    if (t + 2 * G < total) rows_of(rb2);   // (read while this tile is quantised)
+    cp_async_wait<1>();                    // this thread's pieces of tile t have landed
+    __syncthreads();
+    const __nv_bfloat16* tb = reinterpret_cast<const __nv_bfloat16*>(&tile[buf][0]);
+    float v[32];
+    #pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * q + i;
+      v[i] = __bfloat162float(tb[r * 64 + (((cl >> 3) ^ q) << 3) + (cl & 7)]);
+    }
+    __syncthreads();                       // the buffer may be refilled (two tiles on)
+    const int c = cb * 64 + cl;
+    uint8_t* out = codes + static_cast<long long>(mat) * rows * cols + static_cast<long long>(c) * rows + rb * 128 +
+                   32 * q;
+    const uint8_t e = quantize32(v, out);
+    sf[mat * mat_sf + mx_sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
+    rb = rbn; cb = cbn; mat = matn;
+    rbn = rb2; cbn = cb2; matn = mat2;
+  }
 }
 
 // Padding rows of expert e's segment: zero codes and the scale of an
@@ -125,13 +165,15 @@ __device__ __forceinline__ void zero_pad_rows_mx(const int32_t* __restrict__ cou
                                                  const int32_t* __restrict__ poffsets, int e, int H,
                                                  uint4* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int r0 = poffsets[e] + counts[e], r1 = poffsets[e + 1];
-  const int nv = H / 16, nb = H / 32;
+  const int nv = H / 16;
   const long long n = static_cast<long long>(r1 - r0) * nv;
   uint4* base = codes + static_cast<long long>(r0) * nv;
   for (long long i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
-  const long long m = static_cast<long long>(r1 - r0) * nb;
+  const int tiles = H / 128;                  // a row's four scales of a tile: one 32-bit word
+  const long long m = static_cast<long long>(r1 - r0) * tiles;
   for (long long i = threadIdx.x; i < m; i += blockDim.x)
-    sf[mx_sf_offset(r0 + static_cast<int>(i / nb), static_cast<int>(i % nb), H / 128)] = 0;
+    *reinterpret_cast<uint32_t*>(sf + mx_sf_offset(r0 + static_cast<int>(i / tiles),
+                                                   4 * static_cast<int>(i % tiles), tiles)) = 0u;
 }
 
 // Token-order quantised rows (codes [T, H] and their scale tiles) -> expert
@@ -162,12 +204,14 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __rest
       if (r >= 0) codes_perm[static_cast<long long>(r) * nv + v] = c;
     }
   }
-  const int nb = H / 32, tiles = H / 128;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    const uint8_t e = sf_tok[mx_sf_offset(t, b, tiles)];
+  // scales: a row's four blocks of one 128-column tile are four adjacent
+  // bytes in the tiled layout, so they move as one 32-bit word
+  const int tiles = H / 128;
+  for (int j = threadIdx.x; j < tiles; j += blockDim.x) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(sf_tok + mx_sf_offset(t, 4 * j, tiles));
     for (int i = 0; i < k; ++i) {
       const int r = s_rows[i];
-      if (r >= 0) sf_perm[mx_sf_offset(r, b, tiles)] = e;
+      if (r >= 0) *reinterpret_cast<uint32_t*>(sf_perm + mx_sf_offset(r, 4 * j, tiles)) = w;
     }
   }
 }
@@ -184,12 +228,27 @@ cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int 
   return cudaGetLastError();
 }
 
+namespace {
+// Blocks of the persistent column quantiser: as many as are resident on the
+// GPU at once, at most one per tile.
+unsigned quantize_cols_grid(long long tiles) {
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_cols_kernel, 256, 0) != cudaSuccess)
+    per_sm = 1;
+  const long long cap = static_cast<long long>(per_sm < 1 ? 1 : per_sm) * num_sms();
+  return static_cast<unsigned>(tiles < cap ? tiles : cap);
+}
+}  // namespace
+
 cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* sf,
                                  cudaStream_t st, int group, const int32_t* row_limit) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  dim3 grid(rows / 128, cols / 64, batch);   // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
-  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, nullptr, 0, group,
-                                             row_limit, codes, sf);
+  // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
+  const long long tiles = static_cast<long long>(batch) * (rows / 128) * (cols / 64);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  quantize_cols_kernel<<<quantize_cols_grid(tiles), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), batch, rows,
+                                                                  cols, nullptr, 0, group, row_limit, codes, sf);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -198,9 +257,11 @@ cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int
                                         uint8_t* codes, uint8_t* sf, cudaStream_t st, int group,
                                         const int32_t* row_limit) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  dim3 grid(rows / 128, cols / 64, 1);
-  quantize_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, row_map, src_rows,
-                                             group, row_limit, codes, sf);
+  const long long tiles = static_cast<long long>(rows / 128) * (cols / 64);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  quantize_cols_kernel<<<quantize_cols_grid(tiles), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), 1, rows,
+                                                                  cols, row_map, src_rows, group, row_limit, codes,
+                                                                  sf);
   count_launches(1);
   return cudaGetLastError();
 }
