@@ -556,10 +556,7 @@ __device__ __forceinline__ void emit_chunk32(const GemmParams& p, Stager<NBUF, B
       v[2 * i] = bf16_lo(o[i]);
       v[2 * i + 1] = bf16_hi(o[i]);
     }
-    float amax = 0.f;
-    #pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const int eq = mx_exponent(amax);
+    const int eq = mx_exponent(amax32(v));
     uint32_t w[8];
     e4m3_pack32(v, pow2_neg(eq), w);
     uint4* d = reinterpret_cast<uint4*>(p.q_codes + (long long)(y + lane) * p.ld_q + ocol);

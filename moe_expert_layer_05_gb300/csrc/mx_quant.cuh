@@ -50,20 +50,49 @@ __device__ __forceinline__ size_t mx_sf_offset_g(int r, int b, int tiles_per_row
   return (static_cast<size_t>(tr) * tiles_per_row + (b >> 2)) * 512 + (rr & 31) * 16 + ((rr >> 5) & 3) * 4 + (b & 3);
 }
 
-// Quantise 32 values held by this thread; writes 32 code bytes and returns the scale byte.
-__device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst) {
+// max(a, |b|, |c|) in one three-input maximum
+__device__ __forceinline__ float max_abs2(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(fabsf(b)), "f"(fabsf(c)));
+  return d;
+}
+
+// The largest magnitude of 32 values (exact: a maximum rounds nothing).
+__device__ __forceinline__ float amax32(const float (&v)[32]) {
   float amax = 0.f;
   #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int e = mx_exponent(amax);
-  const float sc = pow2_neg(e);
-  uint32_t w[8];
+  for (int i = 0; i < 16; ++i) amax = max_abs2(amax, v[2 * i], v[2 * i + 1]);
+  return amax;
+}
+
+// (a * s, b * s), each rounded to nearest as a plain fp32 product, in one
+// packed two-lane multiply
+__device__ __forceinline__ void mul2(float a, float b, float s, float& x, float& y) {
+  asm("{\n\t.reg .b64 p, q, r;\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mov.b64 q, {%4, %4};\n\t"
+      "mul.rn.f32x2 r, p, q;\n\t"
+      "mov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "f"(s));
+}
+
+// Pack 32 values (scaled by sc) into 8 words of E4M3 codes, value i in byte i.
+__device__ __forceinline__ void e4m3_pack32(const float (&v)[32], float sc, uint32_t (&w)[8]) {
   #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint16_t lo = cvt_e4m3x2(v[4 * i + 0] * sc, v[4 * i + 1] * sc);
-    const uint16_t hi = cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc);
-    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    float a, b, c, d;
+    mul2(v[4 * i + 0], v[4 * i + 1], sc, a, b);
+    mul2(v[4 * i + 2], v[4 * i + 3], sc, c, d);
+    w[i] = static_cast<uint32_t>(cvt_e4m3x2(a, b)) | (static_cast<uint32_t>(cvt_e4m3x2(c, d)) << 16);
   }
+}
+
+// Quantise 32 values held by this thread; writes 32 code bytes and returns the scale byte.
+__device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst) {
+  const int e = mx_exponent(amax32(v));
+  uint32_t w[8];
+  e4m3_pack32(v, pow2_neg(e), w);
   uint4* d = reinterpret_cast<uint4*>(dst);
   d[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -73,16 +102,6 @@ __device__ __forceinline__ uint8_t quantize32(const float (&v)[32], uint8_t* dst
 // Four values to four E4M3 codes, value i in byte i.
 __device__ __forceinline__ uint32_t e4m3_pack4(float a, float b, float c, float d) {
   return static_cast<uint32_t>(cvt_e4m3x2(a, b)) | (static_cast<uint32_t>(cvt_e4m3x2(c, d)) << 16);
-}
-
-// Pack 32 values (scaled by sc) into 8 words of E4M3 codes, value i in byte i.
-__device__ __forceinline__ void e4m3_pack32(const float (&v)[32], float sc, uint32_t (&w)[8]) {
-  #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint16_t lo = cvt_e4m3x2(v[4 * i + 0] * sc, v[4 * i + 1] * sc);
-    const uint16_t hi = cvt_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc);
-    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
 }
 
 }  // namespace moe

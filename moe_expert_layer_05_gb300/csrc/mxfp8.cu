@@ -83,10 +83,11 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 // rows read straight from token order through row_src, padding rows zero.
 // row_limit (nullable): row blocks from row_limit[0] on are neither read nor
 // written (rows past the last expert).
+template <int GROUP>
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ src, int batch,
                                                             int rows, int cols,
                                                             const int32_t* __restrict__ row_map, int src_rows,
-                                                            int group, const int32_t* __restrict__ row_limit,
+                                                            const int32_t* __restrict__ row_limit,
                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   __shared__ uint4 tile[2][128 * 8];       // two 128-row x 64-column tiles
   int nrb = rows / 128;
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   const int cl = warp * 8 + (lane >> 2);   // column inside the tile
   const int q = lane & 3;                  // block of 32 rows inside the tile
   // scale bytes of one matrix: its output rows (the input columns) in groups
-  const long long mat_sf = static_cast<long long>(group == 128 ? cols / 128 : 2 * (cols / group)) * rows * 4;
+  const long long mat_sf = static_cast<long long>(GROUP == 128 ? cols / 128 : 2 * (cols / GROUP)) * rows * 4;
   for (int buf = 0; t < total; t += G, buf ^= 1) {
     if (t + G < total) issue(rbn, cbn, matn, buf ^ 1);
     cp_async_commit();
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
     uint8_t* out = codes + static_cast<long long>(mat) * rows * cols + static_cast<long long>(c) * rows + rb * 128 +
                    32 * q;
     const uint8_t e = quantize32(v, out);
-    sf[mat * mat_sf + mx_sf_offset_g(c, rb * 4 + q, rows / 128, group)] = e;
+    sf[mat * mat_sf + mx_sf_offset_g(c, rb * 4 + q, rows / 128, GROUP)] = e;
     rb = rbn; cb = cbn; mat = matn;
     rbn = rb2; cbn = cb2; matn = mat2;
   }
@@ -229,15 +230,23 @@ cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int 
 }
 
 namespace {
-// Blocks of the persistent column quantiser: as many as are resident on the
-// GPU at once, at most one per tile.
-unsigned quantize_cols_grid(long long tiles) {
+// The persistent column quantiser with as many blocks as are resident on the
+// GPU at once, at most one per tile; the scale grouping (128 or 224 rows) is
+// a template argument so that its row-group division is a constant one.
+template <int GROUP>
+cudaError_t launch_cols(const void* src, int batch, int rows, int cols, const int32_t* row_map, int src_rows,
+                        const int32_t* row_limit, uint8_t* codes, uint8_t* sf, cudaStream_t st) {
+  const long long tiles = static_cast<long long>(batch) * (rows / 128) * (cols / 64);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
   static int per_sm = 0;
   if (per_sm == 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_cols_kernel, 256, 0) != cudaSuccess)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_cols_kernel<GROUP>, 256, 0) != cudaSuccess)
     per_sm = 1;
   const long long cap = static_cast<long long>(per_sm < 1 ? 1 : per_sm) * num_sms();
-  return static_cast<unsigned>(tiles < cap ? tiles : cap);
+  quantize_cols_kernel<GROUP><<<static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(src), batch, rows, cols, row_map, src_rows, row_limit, codes, sf);
+  count_launches(1);
+  return cudaGetLastError();
 }
 }  // namespace
 
@@ -245,25 +254,20 @@ cudaError_t launch_quantize_cols(const void* src, int batch, int rows, int cols,
                                  cudaStream_t st, int group, const int32_t* row_limit) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
   // rows % 128 == 0 and cols % 128 == 0 (checked by the callers)
-  const long long tiles = static_cast<long long>(batch) * (rows / 128) * (cols / 64);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  quantize_cols_kernel<<<quantize_cols_grid(tiles), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), batch, rows,
-                                                                  cols, nullptr, 0, group, row_limit, codes, sf);
-  count_launches(1);
-  return cudaGetLastError();
+  if (group == kMxScaleGroup224)
+    return launch_cols<kMxScaleGroup224>(src, batch, rows, cols, nullptr, 0, row_limit, codes, sf, st);
+  if (group != 128) return cudaErrorInvalidValue;
+  return launch_cols<128>(src, batch, rows, cols, nullptr, 0, row_limit, codes, sf, st);
 }
 
 cudaError_t launch_quantize_cols_gather(const void* src, int src_rows, const int32_t* row_map, int rows, int cols,
                                         uint8_t* codes, uint8_t* sf, cudaStream_t st, int group,
                                         const int32_t* row_limit) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  const long long tiles = static_cast<long long>(rows / 128) * (cols / 64);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  quantize_cols_kernel<<<quantize_cols_grid(tiles), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), 1, rows,
-                                                                  cols, row_map, src_rows, group, row_limit, codes,
-                                                                  sf);
-  count_launches(1);
-  return cudaGetLastError();
+  if (group == kMxScaleGroup224)
+    return launch_cols<kMxScaleGroup224>(src, 1, rows, cols, row_map, src_rows, row_limit, codes, sf, st);
+  if (group != 128) return cudaErrorInvalidValue;
+  return launch_cols<128>(src, 1, rows, cols, row_map, src_rows, row_limit, codes, sf, st);
 }
 
 }  // namespace moe
