@@ -542,7 +542,11 @@ def _as_graph(fn, stream, dev):
 def stage_breakdown(api, w, layer, dinp, x, y, flush, stream, n, dev=None) -> dict:
     """The HBM-bound steps alone (CUDA events, L2 flushed; each stage replayed
     as a CUDA graph, as in the layer's step), with their algorithmic bytes:
-    permute (1+k)*T*H*2, combine (k+1)*T*H*2 (+T*H*2 shared)."""
+    permute (1+k)*T*H*2, combine (k+1)*T*H*2 (+T*H*2 shared).  A graph of one
+    trivial kernel, timed the same way, gives the fixed cost of a graph launch
+    between two events (`graph_launch`, about 7 us), which the layer's step
+    pays once, not per stage; the `*_gbs` rates are taken over each stage's
+    time less that cost, the `*_gbs_raw` ones over the whole time."""
     cfg, fl = layer.cfg, layer.fields()
     T, H, k = w.T, w.H, w.k
     dev = x.device if dev is None else dev
@@ -563,8 +567,13 @@ def stage_breakdown(api, w, layer, dinp, x, y, flush, stream, n, dev=None) -> di
     out["combine"] = timed(lambda: api.moe_unpermute(cfg, fl["o"], fl["slot_row"], shared, y))
     pbytes = (1 + k) * T * H * 2
     cbytes = (k + 1) * T * H * 2 + (T * H * 2 if w.S > 0 else 0)
-    out["permute_gbs"] = pbytes / (out["permute"] / 1e3) / 1e9
-    out["combine_gbs"] = cbytes / (out["combine"] / 1e3) / 1e9
+    tiny = torch.zeros(16, device=dev)
+    out["graph_launch"] = timed(lambda: tiny.add_(1.0))
+    net = lambda ms: max(ms - out["graph_launch"], 1e-6)
+    out["permute_gbs"] = pbytes / (net(out["permute"]) / 1e3) / 1e9
+    out["combine_gbs"] = cbytes / (net(out["combine"]) / 1e3) / 1e9
+    out["permute_gbs_raw"] = pbytes / (out["permute"] / 1e3) / 1e9
+    out["combine_gbs_raw"] = cbytes / (out["combine"] / 1e3) / 1e9
     return out
 
 

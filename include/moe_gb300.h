@@ -150,9 +150,11 @@ int32_t moe_capacity_rows(const moe_config* cfg);
 moe_status moe_activation_layout(const moe_config* cfg, int32_t with_backward, moe_act_layout* out);
 
 /* Bytes of scratch workspace every compute call below needs.  Host only.
- * The first 256 bytes of the workspace hold the device status word and the
+ * The first 256 bytes of the workspace hold the device status word, the
  * grouped GEMMs' tile counter (ints 32 and 33), which hands out output tiles
- * in order and is back at zero after every GEMM launch.  Initialise them
+ * in order and is back at zero after every GEMM launch, and the permutation's
+ * count of finished histogram blocks (int 40, back at zero after each
+ * moe_permute / bf16 moe_layer_forward).  Initialise them
  * once with moe_workspace_init before first use.  Calls that share one
  * workspace must not overlap on the GPU (issue them on one stream). */
 size_t moe_workspace_bytes(const moe_config* cfg);

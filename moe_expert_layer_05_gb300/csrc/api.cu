@@ -606,9 +606,9 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   if (topk_gate != nullptr && !dev_ptr_ok(row_gate)) return MOE_ERR_INVALID_ARG;
   if (moe_status s = check_device(); s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_TRY(launch_permute_maps(topk_idx, topk_gate, cfg->T, cfg->E, cfg->k, hist_ptr(ws), counts, offsets, poffsets,
-                              slot_row, row_src, topk_gate != nullptr ? row_gate : nullptr, status_ptr(ws), st));
-  MOE_TRY(launch_gather_rows(x, slot_row, cfg->T, cfg->k, cfg->H, x_perm, st));
+  MOE_TRY(launch_permute_gather(topk_idx, topk_gate, cfg->T, cfg->E, cfg->k, hist_ptr(ws),
+                                status_ptr(ws) + kMapsDoneWord, counts, offsets, poffsets, slot_row, row_src,
+                                topk_gate != nullptr ? row_gate : nullptr, x, cfg->H, x_perm, status_ptr(ws), st));
   if (zero_pad) MOE_TRY(launch_zero_pad_rows(counts, poffsets, cfg->E, cfg->H, x_perm, st));
   return MOE_OK;
 }
@@ -769,14 +769,19 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   // 1-2: router GEMM + top-k gating
   MOE_TRY(gemm_router(x, w->w_router, T, H, E, logits, status, st));
   // 2-4: top-k gating fused with the counting-sort histograms, scan, scatter (sync-free)
-  MOE_TRY(launch_topk_permute_maps(logits, cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr, T, E, k,
-                                   cfg->score, idx, gate, hist_ptr(ws), counts, at<int32_t>(act, L.offsets), poff,
-                                   slot_row, at<int32_t>(act, L.row_src), row_gate, st));
-  // (MXFP8 and NVFP4 layers permute the quantised codes instead and read x
-  // through row_src where its rows are needed again; x_perm stays unwritten)
+  const float* rbias = cfg->score == MOE_SCORE_SIGMOID ? w->router_bias : nullptr;
   if (cfg->dtype == MOE_GEMM_BF16) {
-    MOE_TRY(launch_gather_rows(x, slot_row, T, k, H, x_perm, st));
+    // the maps and the row copy of x: two launches where the histograms are small
+    MOE_TRY(launch_topk_permute_gather(logits, rbias, T, E, k, cfg->score, idx, gate, hist_ptr(ws),
+                                       status + kMapsDoneWord, counts, at<int32_t>(act, L.offsets), poff, slot_row,
+                                       at<int32_t>(act, L.row_src), row_gate, x, H, x_perm, status, st));
     if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
+  } else {
+    // (MXFP8 and NVFP4 layers permute the quantised codes instead and read x
+    // through row_src where its rows are needed again; x_perm stays unwritten)
+    MOE_TRY(launch_topk_permute_maps(logits, rbias, T, E, k, cfg->score, idx, gate, hist_ptr(ws), counts,
+                                     at<int32_t>(act, L.offsets), poff, slot_row, at<int32_t>(act, L.row_src),
+                                     row_gate, st));
   }
   // 5-6: grouped expert GEMMs; the gate multiplies the SwiGLU output inside fc1
   void* z = with_backward ? at<void>(act, L.z) : nullptr;

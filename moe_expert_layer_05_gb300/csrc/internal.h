@@ -11,6 +11,9 @@ constexpr int kPadRows = 128;      // expert segments start at multiples of this
 constexpr int kPairsPerBlock = 256;  // (token, slot) pairs per counting-sort block
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 32;
+// Int of the workspace's 256-byte status region that counts the finished
+// blocks of the permutation's histogram launch (zero between launches).
+constexpr int kMapsDoneWord = 40;
 
 int num_sms();
 bool device_is_gb300();
@@ -34,6 +37,20 @@ cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int
                                      int32_t* idx, float* gate, int32_t* hist, int32_t* counts, int32_t* offsets,
                                      int32_t* poffsets, int32_t* slot_row, int32_t* row_src, float* row_gate,
                                      cudaStream_t st);
+// The same maps plus the row copy of x into x_perm, in two launches where
+// NB * E is small (histograms, ranks and the scan in the first; the maps and
+// the copy in the second), three otherwise.  done: a workspace int, zero
+// between launches.
+cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
+                                  int* done, int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
+                                  int32_t* row_src, float* row_gate, const void* x, int H, void* x_perm, int* status,
+                                  cudaStream_t st);
+// Top-k gating fused into the first launch of launch_permute_gather.
+cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, int T, int E, int k, int score,
+                                       int32_t* idx, float* gate, int32_t* hist, int* done, int32_t* counts,
+                                       int32_t* offsets, int32_t* poffsets, int32_t* slot_row, int32_t* row_src,
+                                       float* row_gate, const void* x, int H, void* x_perm, int* status,
+                                       cudaStream_t st);
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
                                cudaStream_t st);
 cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,

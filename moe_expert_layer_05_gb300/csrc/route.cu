@@ -214,6 +214,69 @@ __device__ __forceinline__ int load_pair_expert(const int32_t* __restrict__ idx,
   return e;
 }
 
+// One warp scans column col[0..NB) in place (exclusive) and returns its total.
+// The loads go through L2 (another block may have written the column).
+__device__ __forceinline__ int scan_column(int32_t* __restrict__ col, int NB, int lane) {
+  constexpr int kBatch = 8;
+  int run = 0;
+  for (int b0 = 0; b0 < NB; b0 += 32 * kBatch) {
+    int v[kBatch];
+    #pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int b = b0 + 32 * j + lane;
+      v[j] = (b < NB) ? __ldcg(col + b) : 0;
+    }
+    #pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      int inc = v[j];
+      #pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(kFull, inc, d);
+        if (lane >= d) inc += u;
+      }
+      const int b = b0 + 32 * j + lane;
+      if (b < NB) col[b] = run + inc - v[j];
+      run += __shfl_sync(kFull, inc, 31);
+    }
+  }
+  return run;
+}
+
+// ------------------------------------------- permutation in two launches
+// The histogram launch (count_rank_kernel, or topk_hist_kernel with RANKS)
+// also leaves each pair's stable rank inside its chunk in slot_row (-1 for a
+// dropped pair).  With LAST_SCAN (small problems: NB * E <= kLastScanEntries)
+// the last of its blocks to finish -- found by an atomic count of finished
+// blocks, no block waits for another -- scans the histogram columns and
+// writes counts, so the scan needs no launch of its own; otherwise
+// scan_cols_kernel runs between the two launches.  gather_scatter_kernel then
+// turns the ranks into rows and copies the token rows in the same launch.
+constexpr int kLastScanEntries = 8192;
+
+template <bool LAST_SCAN>
+__device__ __forceinline__ void hist_rank_tail(int e, long long p, bool has_pair, int E, int32_t* __restrict__ hist,
+                                               int32_t* __restrict__ slot_row, int* __restrict__ done,
+                                               int32_t* __restrict__ counts, int* s_cnt, int* s_tot) {
+  const int r = block_stable_rank(e, E, s_cnt, s_tot);
+  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)x * gridDim.x + blockIdx.x] = s_tot[x];
+  if (has_pair) slot_row[p] = r;                   // (-1 where e < 0)
+  if constexpr (LAST_SCAN) {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(done, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int x = warp; x < E; x += blockDim.x / 32) {
+      const int tot = scan_column(hist + (long long)x * gridDim.x, gridDim.x, lane);
+      if (lane == 0) counts[x] = tot;
+    }
+    if (threadIdx.x == 0) atomicExch(done, 0);   // zero for the next launch
+  }
+}
+
 __global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __restrict__ idx, long long npairs,
                                                                int pb, int E, int32_t* __restrict__ hist,
                                                                int* status) {
@@ -227,12 +290,17 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __
 // Top-k gating fused with the chunk histogram: block b routes the tokens of
 // chunk b (one warp per token, as topk_kernel; one thread per token when
 // E <= kThreadTopkE) and then counts its pairs.
-template <int PER_LANE>
+// MODE 0: the histograms only; 1: also the ranks in slot_row; 2: also the
+// last block's column scan (see hist_rank_tail).
+template <int PER_LANE, int MODE>
 __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* __restrict__ logits,
                                                                    const float* __restrict__ bias, int T, int E,
                                                                    int k, int score, int32_t* __restrict__ idx,
                                                                    float* __restrict__ gate,
-                                                                   int32_t* __restrict__ hist) {
+                                                                   int32_t* __restrict__ hist,
+                                                                   int32_t* __restrict__ slot_row,
+                                                                   int* __restrict__ done,
+                                                                   int32_t* __restrict__ counts) {
   constexpr int kStageFloats = 8192;             // logits of the chunk staged in shared memory (32 KB)
   __shared__ int s_idx[kPairsPerBlock];
   __shared__ int s_cnt[8 * kMaxE];
@@ -276,8 +344,12 @@ __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* 
   const long long npairs = (long long)T * k;
   const long long p = (long long)blockIdx.x * pb + threadIdx.x;
   const int e = (threadIdx.x < pb && p < npairs) ? s_idx[threadIdx.x] : -1;
-  block_stable_rank(e, E, s_cnt, s_tot);
-  for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)x * gridDim.x + blockIdx.x] = s_tot[x];
+  if constexpr (MODE == 0) {
+    block_stable_rank(e, E, s_cnt, s_tot);
+    for (int x = threadIdx.x; x < E; x += blockDim.x) hist[(long long)x * gridDim.x + blockIdx.x] = s_tot[x];
+  } else {
+    hist_rank_tail<MODE == 2>(e, p, threadIdx.x < pb && p < npairs, E, hist, slot_row, done, counts, s_cnt, s_tot);
+  }
 }
 
 // The chunk histograms are laid out per expert: hist[e * NB + b] = pairs of
@@ -393,6 +465,103 @@ __global__ void __launch_bounds__(kPairsPerBlock) scatter_kernel(const int32_t* 
   slot_row[p] = row;
   row_src[row] = static_cast<int32_t>(p / k);
   if (row_gate != nullptr) row_gate[row] = gate[p];
+}
+
+template <bool LAST_SCAN>
+__global__ void __launch_bounds__(kPairsPerBlock) count_rank_kernel(const int32_t* __restrict__ idx,
+                                                                    long long npairs, int pb, int E,
+                                                                    int32_t* __restrict__ hist,
+                                                                    int32_t* __restrict__ slot_row,
+                                                                    int* __restrict__ done,
+                                                                    int32_t* __restrict__ counts, int* status) {
+  __shared__ int s_cnt[8 * kMaxE];
+  __shared__ int s_tot[kMaxE];
+  const int e = load_pair_expert(idx, npairs, pb, E, status);
+  const long long p = (long long)blockIdx.x * pb + threadIdx.x;
+  hist_rank_tail<LAST_SCAN>(e, p, threadIdx.x < pb && p < npairs, E, hist, slot_row, done, counts, s_cnt, s_tot);
+}
+
+// Block t (128 threads): token t's k pairs get their rows, row = padded
+// offset of the expert + its pairs in earlier chunks (the scanned column) +
+// the rank the histogram launch left in slot_row; then x[t] is copied to
+// them.  Every block derives the expert offsets from counts (E <= 256);
+// block 0 also writes offsets, poffsets and marks the padding rows.  Launched
+// with max(T, 1) blocks.
+__global__ void __launch_bounds__(128) gather_scatter_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int E,
+    int k, int NB, int pb, int vec_per_row, const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ poffsets, int32_t* __restrict__ slot_row,
+    int32_t* __restrict__ row_src, float* __restrict__ row_gate, uint4* __restrict__ x_perm, int* status) {
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_poff[kMaxE + 1];
+  __shared__ int s_rows[kMaxK];
+  const int t = blockIdx.x;
+  // the first batch of x[t]'s loads is issued before the maps are worked
+  // out, so their latency overlaps
+  const uint4* src = x + (long long)min(t, max(T - 1, 0)) * vec_per_row;
+  uint4 val[4];
+  #pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int v = threadIdx.x + u * blockDim.x;
+    if (t < T && v < vec_per_row) val[u] = __ldg(src + v);
+  }
+  expert_offsets(counts, E, s_off, s_poff);
+  __syncthreads();
+  if (t == 0) {
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+      offsets[i] = s_off[i];
+      poffsets[i] = s_poff[i];
+    }
+    for (int i = threadIdx.x; i < E * kPadRows; i += blockDim.x) {
+      const int e = i / kPadRows, j = i % kPadRows;
+      const int rr = s_poff[e] + counts[e] + j;
+      if (rr < s_poff[e + 1]) {
+        row_src[rr] = -1;
+        if (row_gate != nullptr) row_gate[rr] = 0.f;
+      }
+    }
+  }
+  if (t >= T) return;
+  if (threadIdx.x < k) {
+    const long long p = (long long)t * k + threadIdx.x;
+    const int e = idx[p];
+    int row = -1;
+    if (e >= 0 && e < E) {
+      const int chunk = static_cast<int>(p / pb);
+      row = s_poff[e] + base[(long long)e * NB + chunk] + slot_row[p];
+      if (row < s_poff[e] || row >= s_poff[e] + counts[e]) {
+        // only reachable if the histogram launch's results are inconsistent
+        // (a workspace not initialised, or shared by overlapping calls)
+        set_status(status, kErrBadIndex);
+        row = -1;
+      } else {
+        row_src[row] = t;
+        if (row_gate != nullptr) row_gate[row] = gate[p];
+      }
+    }
+    slot_row[p] = row;
+    s_rows[threadIdx.x] = row;
+  }
+  __syncthreads();
+  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += 4 * blockDim.x) {
+    if (v0 != threadIdx.x) {
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < vec_per_row) val[u] = __ldg(src + v);
+      }
+    }
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r < 0) continue;
+      uint4* dst = x_perm + (long long)r * vec_per_row;
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < vec_per_row) dst[v] = val[u];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- row copies
@@ -664,21 +833,97 @@ cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, in
   return launch_scan_scatter(idx, gate, T, E, k, hist, counts, offsets, poffsets, slot_row, row_src, row_gate, st);
 }
 
+namespace {
+template <int MODE>
+void topk_hist(const float* logits, const float* bias, int T, int E, int k, int score, int32_t* idx, float* gate,
+               int32_t* hist, int32_t* slot_row, int* done, int32_t* counts, int NB, cudaStream_t st) {
+  if (E <= kThreadTopkE)
+    topk_hist_kernel<0, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+                                                             done, counts);
+  else if (E <= 32)
+    topk_hist_kernel<1, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+                                                             done, counts);
+  else if (E <= 64)
+    topk_hist_kernel<2, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+                                                             done, counts);
+  else if (E <= 128)
+    topk_hist_kernel<4, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+                                                             done, counts);
+  else
+    topk_hist_kernel<8, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+                                                             done, counts);
+  count_launches(1);
+}
+
+// The second launch (after the histograms and ranks, and scan_cols_kernel
+// where the histogram launch did not scan).
+cudaError_t launch_gather_scatter(const void* x, const int32_t* idx, const float* gate, int T, int E, int k, int H,
+                                  const int32_t* hist, const int32_t* counts, int32_t* offsets, int32_t* poffsets,
+                                  int32_t* slot_row, int32_t* row_src, float* row_gate, void* x_perm, int* status,
+                                  cudaStream_t st) {
+  gather_scatter_kernel<<<T > 0 ? T : 1, 128, 0, st>>>(
+      static_cast<const uint4*>(x), idx, gate, T, E, k, chunks_of(T, k), pairs_per_chunk(k), H / 8, hist, counts,
+      offsets, poffsets, slot_row, row_src, gate != nullptr ? row_gate : nullptr, static_cast<uint4*>(x_perm),
+      status);
+  count_launches(1);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int T, int E, int k, int score,
                                      int32_t* idx, float* gate, int32_t* hist, int32_t* counts, int32_t* offsets,
                                      int32_t* poffsets, int32_t* slot_row, int32_t* row_src, float* row_gate,
                                      cudaStream_t st) {
   const int NB = chunks_of(T, k);
+  if (NB > 0) topk_hist<0>(logits, bias, T, E, k, score, idx, gate, hist, nullptr, nullptr, nullptr, NB, st);
+  return launch_scan_scatter(idx, gate, T, E, k, hist, counts, offsets, poffsets, slot_row, row_src, row_gate, st);
+}
+
+cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, int T, int E, int k, int score,
+                                       int32_t* idx, float* gate, int32_t* hist, int* done, int32_t* counts,
+                                       int32_t* offsets, int32_t* poffsets, int32_t* slot_row, int32_t* row_src,
+                                       float* row_gate, const void* x, int H, void* x_perm, int* status,
+                                       cudaStream_t st) {
+  const int NB = chunks_of(T, k);
   if (NB > 0) {
-    if (E <= kThreadTopkE)
-      topk_hist_kernel<0><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
-    else if (E <= 32) topk_hist_kernel<1><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
-    else if (E <= 64) topk_hist_kernel<2><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
-    else if (E <= 128) topk_hist_kernel<4><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
-    else topk_hist_kernel<8><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist);
+    if ((long long)NB * E <= kLastScanEntries) {
+      topk_hist<2>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
+    } else {
+      topk_hist<1>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
+      scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, NB, E, counts);
+      count_launches(1);
+    }
+  } else {
+    scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, 0, E, counts);   // counts = 0
     count_launches(1);
   }
-  return launch_scan_scatter(idx, gate, T, E, k, hist, counts, offsets, poffsets, slot_row, row_src, row_gate, st);
+  return launch_gather_scatter(x, idx, gate, T, E, k, H, hist, counts, offsets, poffsets, slot_row, row_src, row_gate,
+                               x_perm, status, st);
+}
+
+cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
+                                  int* done, int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
+                                  int32_t* row_src, float* row_gate, const void* x, int H, void* x_perm, int* status,
+                                  cudaStream_t st) {
+  const long long npairs = (long long)T * k;
+  const int NB = chunks_of(T, k);
+  if (NB > 0) {
+    if ((long long)NB * E <= kLastScanEntries) {
+      count_rank_kernel<true><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
+                                                             counts, status);
+      count_launches(1);
+    } else {
+      count_rank_kernel<false><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row,
+                                                              done, counts, status);
+      scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, NB, E, counts);
+      count_launches(2);
+    }
+  } else {
+    scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, 0, E, counts);   // counts = 0
+    count_launches(1);
+  }
+  return launch_gather_scatter(x, idx, gate, T, E, k, H, hist, counts, offsets, poffsets, slot_row, row_src, row_gate,
+                               x_perm, status, st);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
