@@ -252,6 +252,12 @@ __device__ __forceinline__ int scan_column(int32_t* __restrict__ col, int NB, in
 // scan_cols_kernel runs between the two launches.  gather_scatter_kernel then
 // turns the ranks into rows and copies the token rows in the same launch.
 constexpr int kLastScanEntries = 8192;
+// gather_scatter_kernel: a block per token, warp 0 deriving the expert
+// offsets while warp 1 fetches the pairs' maps.  Where all blocks fit on the
+// GPU at once (T <= kGsSmallT) two warps, each thread with 8 16-byte loads of
+// the row in flight (a 4096-wide bf16 row in one batch); otherwise four
+// warps with 4 loads each (measured faster for the larger batches).
+constexpr int kGsSmallT = 4864;   // 152 SMs x 32 blocks
 
 template <bool LAST_SCAN>
 __device__ __forceinline__ void hist_rank_tail(int e, long long p, bool has_pair, int E, int32_t* __restrict__ hist,
@@ -481,13 +487,14 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_rank_kernel(const int32_
   hist_rank_tail<LAST_SCAN>(e, p, threadIdx.x < pb && p < npairs, E, hist, slot_row, done, counts, s_cnt, s_tot);
 }
 
-// Block t (128 threads): token t's k pairs get their rows, row = padded
+// Block t: token t's k pairs get their rows, row = padded
 // offset of the expert + its pairs in earlier chunks (the scanned column) +
 // the rank the histogram launch left in slot_row; then x[t] is copied to
 // them.  Every block derives the expert offsets from counts (E <= 256);
 // block 0 also writes offsets, poffsets and marks the padding rows.  Launched
 // with max(T, 1) blocks.
-__global__ void __launch_bounds__(128) gather_scatter_kernel(
+template <int kGsThreads, int kGsBatch>
+__global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int E,
     int k, int NB, int pb, int vec_per_row, const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ poffsets, int32_t* __restrict__ slot_row,
@@ -495,27 +502,39 @@ __global__ void __launch_bounds__(128) gather_scatter_kernel(
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_poff[kMaxE + 1];
   __shared__ int s_rows[kMaxK];
+  __shared__ int s_e[kMaxK];
+  __shared__ int s_in[kMaxK];
   const int t = blockIdx.x;
   // the first batch of x[t]'s loads is issued before the maps are worked
-  // out, so their latency overlaps
+  // out, and warp 1 fetches the pairs' experts, scanned columns and ranks
+  // while warp 0 derives the expert offsets, so the latencies overlap
   const uint4* src = x + (long long)min(t, max(T - 1, 0)) * vec_per_row;
-  uint4 val[4];
+  uint4 val[kGsBatch];
   #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int v = threadIdx.x + u * blockDim.x;
+  for (int u = 0; u < kGsBatch; ++u) {
+    const int v = threadIdx.x + u * kGsThreads;
     if (t < T && v < vec_per_row) val[u] = __ldg(src + v);
+  }
+  const int i1 = threadIdx.x - 32;
+  if (t < T && i1 >= 0 && i1 < k) {
+    const long long p = (long long)t * k + i1;
+    int e = idx[p];
+    int in_e = 0;                                  // pairs of expert e before this one
+    if (e >= 0 && e < E) in_e = base[(long long)e * NB + static_cast<int>(p / pb)] + slot_row[p];
+    else e = -1;
+    s_e[i1] = e;
+    s_in[i1] = in_e;
   }
   expert_offsets(counts, E, s_off, s_poff);
   __syncthreads();
   if (t == 0) {
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    for (int i = threadIdx.x; i <= E; i += kGsThreads) {
       offsets[i] = s_off[i];
       poffsets[i] = s_poff[i];
     }
-    for (int i = threadIdx.x; i < E * kPadRows; i += blockDim.x) {
-      const int e = i / kPadRows, j = i % kPadRows;
-      const int rr = s_poff[e] + counts[e] + j;
-      if (rr < s_poff[e + 1]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = warp; e < E; e += kGsThreads / 32) {
+      for (int rr = s_poff[e] + (s_off[e + 1] - s_off[e]) + lane; rr < s_poff[e + 1]; rr += 32) {
         row_src[rr] = -1;
         if (row_gate != nullptr) row_gate[rr] = 0.f;
       }
@@ -524,12 +543,12 @@ __global__ void __launch_bounds__(128) gather_scatter_kernel(
   if (t >= T) return;
   if (threadIdx.x < k) {
     const long long p = (long long)t * k + threadIdx.x;
-    const int e = idx[p];
+    const int e = s_e[threadIdx.x];
     int row = -1;
-    if (e >= 0 && e < E) {
-      const int chunk = static_cast<int>(p / pb);
-      row = s_poff[e] + base[(long long)e * NB + chunk] + slot_row[p];
-      if (row < s_poff[e] || row >= s_poff[e] + counts[e]) {
+    if (e >= 0) {
+      const int in_e = s_in[threadIdx.x];
+      row = s_poff[e] + in_e;
+      if (in_e < 0 || in_e >= s_off[e + 1] - s_off[e]) {
         // only reachable if the histogram launch's results are inconsistent
         // (a workspace not initialised, or shared by overlapping calls)
         set_status(status, kErrBadIndex);
@@ -543,11 +562,11 @@ __global__ void __launch_bounds__(128) gather_scatter_kernel(
     s_rows[threadIdx.x] = row;
   }
   __syncthreads();
-  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += 4 * blockDim.x) {
+  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += kGsBatch * kGsThreads) {
     if (v0 != threadIdx.x) {
       #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = v0 + u * blockDim.x;
+      for (int u = 0; u < kGsBatch; ++u) {
+        const int v = v0 + u * kGsThreads;
         if (v < vec_per_row) val[u] = __ldg(src + v);
       }
     }
@@ -556,8 +575,8 @@ __global__ void __launch_bounds__(128) gather_scatter_kernel(
       if (r < 0) continue;
       uint4* dst = x_perm + (long long)r * vec_per_row;
       #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = v0 + u * blockDim.x;
+      for (int u = 0; u < kGsBatch; ++u) {
+        const int v = v0 + u * kGsThreads;
         if (v < vec_per_row) dst[v] = val[u];
       }
     }
@@ -861,7 +880,8 @@ cudaError_t launch_gather_scatter(const void* x, const int32_t* idx, const float
                                   const int32_t* hist, const int32_t* counts, int32_t* offsets, int32_t* poffsets,
                                   int32_t* slot_row, int32_t* row_src, float* row_gate, void* x_perm, int* status,
                                   cudaStream_t st) {
-  gather_scatter_kernel<<<T > 0 ? T : 1, 128, 0, st>>>(
+  auto kern = (T <= kGsSmallT) ? gather_scatter_kernel<64, 8> : gather_scatter_kernel<128, 4>;
+  kern<<<T > 0 ? T : 1, (T <= kGsSmallT) ? 64 : 128, 0, st>>>(
       static_cast<const uint4*>(x), idx, gate, T, E, k, chunks_of(T, k), pairs_per_chunk(k), H / 8, hist, counts,
       offsets, poffsets, slot_row, row_src, gate != nullptr ? row_gate : nullptr, static_cast<uint4*>(x_perm),
       status);
