@@ -493,10 +493,14 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_rank_kernel(const int32_
 // them.  Every block derives the expert offsets from counts (E <= 256);
 // block 0 also writes offsets, poffsets and marks the padding rows.  Launched
 // with max(T, 1) blocks.
-template <int kGsThreads, int kGsBatch>
+// RAW (at most 32 chunks and 32 experts): base holds the chunk histograms
+// as counted, not scanned, and counts is not written yet; each block sums the
+// columns it needs itself (one coalesced load per expert and per pair) and
+// block 0 also writes counts -- no scan between the two launches.
+template <int kGsThreads, int kGsBatch, bool RAW>
 __global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int E,
-    int k, int NB, int pb, int vec_per_row, const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    int k, int NB, int pb, int vec_per_row, const int32_t* __restrict__ base, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ poffsets, int32_t* __restrict__ slot_row,
     int32_t* __restrict__ row_src, float* __restrict__ row_gate, uint4* __restrict__ x_perm, int* status) {
   __shared__ int s_off[kMaxE + 1];
@@ -516,21 +520,83 @@ __global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
     if (t < T && v < vec_per_row) val[u] = __ldg(src + v);
   }
   const int i1 = threadIdx.x - 32;
-  if (t < T && i1 >= 0 && i1 < k) {
-    const long long p = (long long)t * k + i1;
-    int e = idx[p];
-    int in_e = 0;                                  // pairs of expert e before this one
-    if (e >= 0 && e < E) in_e = base[(long long)e * NB + static_cast<int>(p / pb)] + slot_row[p];
-    else e = -1;
-    s_e[i1] = e;
-    s_in[i1] = in_e;
+  if constexpr (RAW) {
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+      // warp 0: counts[e] = sum over the chunks of column e (lane e keeps it),
+      // then the exclusive scans over the experts
+      int col[32];
+      #pragma unroll
+      for (int e = 0; e < 32; ++e) col[e] = (e < E && lane < NB) ? base[e * NB + lane] : 0;
+      int c = 0;
+      #pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int tot = __reduce_add_sync(kFull, col[e]);
+        if (lane == e) c = tot;
+      }
+      const int pc = (c + kPadRows - 1) / kPadRows * kPadRows;
+      int ci = c, pi = pc;
+      #pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int a = __shfl_up_sync(kFull, ci, d), b = __shfl_up_sync(kFull, pi, d);
+        if (lane >= d) { ci += a; pi += b; }
+      }
+      if (lane < E) {
+        s_off[lane] = ci - c;
+        s_poff[lane] = pi - pc;
+      }
+      if (lane == 31) {                               // lanes >= E add nothing
+        s_off[E] = ci;
+        s_poff[E] = pi;
+      }
+    } else if (threadIdx.x < 64 && t < T) {
+      // warp 1: lane i < k holds pair i; pairs of its expert in the chunks
+      // before this token's = sum of that column's first `chunk` entries
+      const long long p0 = (long long)t * k;
+      const int chunk = static_cast<int>(p0 / pb);
+      int e = -1, r = 0;
+      if (lane < k) {
+        e = idx[p0 + lane];
+        if (e < 0 || e >= E) e = -1;
+        else r = slot_row[p0 + lane];
+      }
+      int in_e = r;
+      for (int g = 0; g < k; g += 8) {
+        int v[8];
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int ej = __shfl_sync(kFull, e, (g + j) & 31);
+          v[j] = (g + j < k && ej >= 0 && lane < chunk) ? base[ej * NB + lane] : 0;
+        }
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int sum = __reduce_add_sync(kFull, v[j]);
+          if (lane == g + j) in_e += sum;
+        }
+      }
+      if (lane < k) {
+        s_e[lane] = e;
+        s_in[lane] = in_e;
+      }
+    }
+  } else {
+    if (t < T && i1 >= 0 && i1 < k) {
+      const long long p = (long long)t * k + i1;
+      int e = idx[p];
+      int in_e = 0;                                  // pairs of expert e before this one
+      if (e >= 0 && e < E) in_e = base[(long long)e * NB + static_cast<int>(p / pb)] + slot_row[p];
+      else e = -1;
+      s_e[i1] = e;
+      s_in[i1] = in_e;
+    }
+    expert_offsets(counts, E, s_off, s_poff);
   }
-  expert_offsets(counts, E, s_off, s_poff);
   __syncthreads();
   if (t == 0) {
     for (int i = threadIdx.x; i <= E; i += kGsThreads) {
       offsets[i] = s_off[i];
       poffsets[i] = s_poff[i];
+      if (RAW && i < E) counts[i] = s_off[i + 1] - s_off[i];
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int e = warp; e < E; e += kGsThreads / 32) {
@@ -876,12 +942,22 @@ void topk_hist(const float* logits, const float* bias, int T, int E, int k, int 
 
 // The second launch (after the histograms and ranks, and scan_cols_kernel
 // where the histogram launch did not scan).
+// At most 32 chunks and 32 experts: the row copy sums the raw histogram
+// columns itself (gather_scatter_kernel RAW), so nothing runs between the
+// two launches.
+bool raw_histograms(int T, int E, int k) {
+  const int NB = chunks_of(T, k);
+  return NB >= 1 && NB <= 32 && E <= 32;
+}
+
 cudaError_t launch_gather_scatter(const void* x, const int32_t* idx, const float* gate, int T, int E, int k, int H,
-                                  const int32_t* hist, const int32_t* counts, int32_t* offsets, int32_t* poffsets,
+                                  const int32_t* hist, int32_t* counts, int32_t* offsets, int32_t* poffsets,
                                   int32_t* slot_row, int32_t* row_src, float* row_gate, void* x_perm, int* status,
                                   cudaStream_t st) {
-  auto kern = (T <= kGsSmallT) ? gather_scatter_kernel<64, 8> : gather_scatter_kernel<128, 4>;
-  kern<<<T > 0 ? T : 1, (T <= kGsSmallT) ? 64 : 128, 0, st>>>(
+  const bool raw = raw_histograms(T, E, k);
+  auto kern = raw ? gather_scatter_kernel<64, 8, true>
+                  : (T <= kGsSmallT) ? gather_scatter_kernel<64, 8, false> : gather_scatter_kernel<128, 4, false>;
+  kern<<<T > 0 ? T : 1, (raw || T <= kGsSmallT) ? 64 : 128, 0, st>>>(
       static_cast<const uint4*>(x), idx, gate, T, E, k, chunks_of(T, k), pairs_per_chunk(k), H / 8, hist, counts,
       offsets, poffsets, slot_row, row_src, gate != nullptr ? row_gate : nullptr, static_cast<uint4*>(x_perm),
       status);
@@ -905,7 +981,9 @@ cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, i
                                        float* row_gate, const void* x, int H, void* x_perm, int* status,
                                        cudaStream_t st) {
   const int NB = chunks_of(T, k);
-  if (NB > 0) {
+  if (raw_histograms(T, E, k)) {
+    topk_hist<1>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
+  } else if (NB > 0) {
     if ((long long)NB * E <= kLastScanEntries) {
       topk_hist<2>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
     } else {
@@ -927,7 +1005,11 @@ cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, 
                                   cudaStream_t st) {
   const long long npairs = (long long)T * k;
   const int NB = chunks_of(T, k);
-  if (NB > 0) {
+  if (raw_histograms(T, E, k)) {
+    count_rank_kernel<false><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
+                                                            counts, status);
+    count_launches(1);
+  } else if (NB > 0) {
     if ((long long)NB * E <= kLastScanEntries) {
       count_rank_kernel<true><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
                                                              counts, status);
