@@ -136,6 +136,8 @@ PERM_CASES = [
     (0, 8, 2, 0.0, 128),
     (500, 16, 3, 0.5, 128),     # k does not divide the 256-pair chunk
     (300, 32, 6, 1.0, 128),
+    (300, 33, 2, 0.5, 128),     # one expert past the row copy's own column sums (last-block scan)
+    (2100, 128, 8, 1.0, 128),   # histograms past the last-block scan (scan launch between)
 ]
 
 
@@ -186,19 +188,29 @@ def test_permute_bit_exact(lib, T, E, k, skew, H):
     np.testing.assert_array_equal(got_bits, want_bits)
 
 
-def test_permute_is_deterministic(lib):
-    T, E, k, H = 4096, 64, 8, 128
+@pytest.mark.parametrize("T,E", [(1024, 8), (4096, 64), (4096, 128)])
+def test_permute_is_deterministic(lib, T, E):
+    """Three calls on one workspace give the same bits (32 chunks of 8
+    experts: the row copy sums the raw histograms; 128 chunks of 64: the
+    histogram launch's last block scans them and puts its counter back to
+    zero; 128 of 128: a scan launch between)."""
+    k, H = 8, 128
     idx = torch.from_numpy(random_topk_indices(T, E, k, seed=1, skew=1.0)).to(DEV)
     x = to_bf16(_rand((T, H), 9)).to(DEV)
     cfg = api.make_config(T, H, E, k, 128)
+    ws = _ws(cfg)
     outs = []
     for _ in range(3):
         cap, b = _perm_buffers(cfg)
         api.moe_permute(cfg, x, idx, None, b["counts"], b["offsets"], b["poffsets"], b["slot_row"],
-                        b["row_src"], None, b["x_perm"], 1, _ws(cfg))
-        outs.append((b["slot_row"].cpu(), b["x_perm"].view(torch.int16).cpu()))
+                        b["row_src"], None, b["x_perm"], 1, ws)
+        outs.append((b["slot_row"].cpu(), b["x_perm"].view(torch.int16).cpu(), b["counts"].cpu()))
+    assert _status(ws) == 0
+    m = O.permutation_maps(idx.cpu().numpy(), E, 128)
+    np.testing.assert_array_equal(outs[0][0].numpy(), m["slot_row"])
+    np.testing.assert_array_equal(outs[0][2].numpy(), m["counts"])
     for o in outs[1:]:
-        assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1])
+        assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1]) and torch.equal(o[2], outs[0][2])
 
 
 def test_permute_bad_index_sets_status(lib):
