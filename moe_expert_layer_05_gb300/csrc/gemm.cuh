@@ -1299,6 +1299,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                         const GemmParams p) {
+  pdl_wait();
   static_assert(sizeof(GemmBook<C>) <= C::BOOK_BYTES, "bookkeeping size");
   static_assert(!C::PAIR, "CTA-pair tiles run in grouped_gemm_pair_kernel");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1650,6 +1651,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
+  pdl_launch_next();
   if (threadIdx.x == 0 && abort_flag) set_status(p.status, kErrTimeout);
   if (warp == 1) {
     tc_fence_after_sync();
@@ -1711,6 +1713,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                              const GemmParams p) {
+  pdl_wait();
   static_assert(C::PAIR, "pair configuration");
   static_assert(sizeof(GemmBook<C>) <= C::BOOK_BYTES, "bookkeeping size");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1889,6 +1892,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();                       // the peer no longer reads this CTA's memory or signals its barriers
+  pdl_launch_next();
   if (threadIdx.x == 0 && bk.abort_flag) set_status(p.status, kErrTimeout);
   if (warp == 1) {
     tc_fence_after_sync();

@@ -48,7 +48,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   GemmParams q = p;
   q.sched = (p.status != nullptr) ? p.status + kSchedCounterWord : nullptr;
   q.wait_ns = gemm_wait_limit_ns();
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, tc, tc2, q);
+  launch_k(kern, grid, C::THREADS, C::SMEM_BYTES, st, ta, tb, tc, tc2, q);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -63,17 +63,19 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   int max_clusters = max_clusters_of[dev].load(std::memory_order_acquire);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // (see launch_k)
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;                       // (the occupancy query takes the cluster shape alone)
   if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -90,6 +92,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   GemmParams q = p;
   q.wait_ns = gemm_wait_limit_ns();
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tc2, q);
   count_launches(1);
   return e;

@@ -17,6 +17,25 @@ constexpr int kMapsDoneWord = 40;
 
 int num_sms();
 bool device_is_gb300();
+
+// Launch of one of the library's kernels (each begins with pdl_entry()) with
+// programmatic stream serialization, so that its launch overlaps the tail of
+// the kernel before it in the stream.  Errors are also left for
+// cudaGetLastError, as with <<<>>>.
+template <class... KArgs, class... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 // Limit of one pipeline wait inside the grouped GEMMs (0: the kernels' 2 s
 // default); set through moe_debug_set_wait_limit_ns.
 unsigned long long gemm_wait_limit_ns();

@@ -39,6 +39,7 @@ __device__ __forceinline__ long long gate_up_row(long long r, int half) {
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ src, long long rows, int cols,
                                                             int half, int group, const int32_t* __restrict__ row_limit,
                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  pdl_entry();
   const int nb = cols / 32;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= rows * nb) return;
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
                                                             const int32_t* __restrict__ row_map, int src_rows,
                                                             const int32_t* __restrict__ row_limit,
                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  pdl_entry();
   __shared__ uint4 tile[2][128 * 8];       // two 128-row x 64-column tiles
   int nrb = rows / 128;
   if (row_limit != nullptr) nrb = min(nrb, (__ldg(row_limit) + 127) / 128);
@@ -189,6 +191,7 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __rest
                                                              const int32_t* __restrict__ poffsets,
                                                              uint4* __restrict__ codes_perm,
                                                              uint8_t* __restrict__ sf_perm) {
+  pdl_entry();
   if (static_cast<int>(blockIdx.x) < E_pad) {
     zero_pad_rows_mx(counts, poffsets, blockIdx.x, H, codes_perm, sf_perm);
     return;
@@ -223,7 +226,7 @@ cudaError_t launch_quantize_rows(const void* src, long long rows, int cols, int 
                                  uint8_t* sf, cudaStream_t st, int group, const int32_t* row_limit) {
   const long long n = rows * (cols / 32);
   if (n == 0) return cudaSuccess;
-  quantize_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+  launch_k(quantize_rows_kernel, static_cast<unsigned>((n + 255) / 256), 256, 0, st, 
       static_cast<const uint4*>(src), rows, cols, gate_up_half, group, row_limit, codes, sf);
   count_launches(1);
   return cudaGetLastError();
@@ -243,7 +246,7 @@ cudaError_t launch_cols(const void* src, int batch, int rows, int cols, const in
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_cols_kernel<GROUP>, 256, 0) != cudaSuccess)
     per_sm = 1;
   const long long cap = static_cast<long long>(per_sm < 1 ? 1 : per_sm) * num_sms();
-  quantize_cols_kernel<GROUP><<<static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0, st>>>(
+  launch_k(quantize_cols_kernel<GROUP>, static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0, st, 
       static_cast<const __nv_bfloat16*>(src), batch, rows, cols, row_map, src_rows, row_limit, codes, sf);
   count_launches(1);
   return cudaGetLastError();
@@ -277,7 +280,7 @@ cudaError_t launch_gather_rows_mx(const uint8_t* codes_tok, const uint8_t* sf_to
                                   int k, int H, uint8_t* codes_perm, uint8_t* sf_perm, cudaStream_t st,
                                   const int32_t* counts, const int32_t* poffsets, int E_pad) {
   if (T + E_pad == 0) return cudaSuccess;
-  gather_rows_mx_kernel<<<T + E_pad, 128, 0, st>>>(reinterpret_cast<const uint4*>(codes_tok), sf_tok, slot_row,
+  launch_k(gather_rows_mx_kernel, T + E_pad, 128, 0, st, reinterpret_cast<const uint4*>(codes_tok), sf_tok, slot_row,
                                                    E_pad, k, H, counts, poffsets,
                                                    reinterpret_cast<uint4*>(codes_perm), sf_perm);
   count_launches(1);

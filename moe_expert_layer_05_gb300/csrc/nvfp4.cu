@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict_
                                                         int vec_per_row, const int32_t* __restrict__ row_src,
                                                         const int32_t* __restrict__ rows_end,
                                                         unsigned* __restrict__ out) {
+  pdl_entry();
   float m = 0.f;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   if (rows_end != nullptr) {
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(256) quantize_rows_nv4_kernel(const uint4* __r
                                                                 int cols, int half, const float* __restrict__ amax_p,
                                                                 uint8_t* __restrict__ codes,
                                                                 uint8_t* __restrict__ sf) {
+  pdl_entry();
   const int nb = cols / 16;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= rows * nb) return;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(256) quantize_gather_nv4_kernel(const uint4* _
                                                                   uint8_t* __restrict__ sf_perm,
                                                                   uint8_t* __restrict__ codes_tok,
                                                                   uint8_t* __restrict__ sf_tok) {
+  pdl_entry();
   const int nb = H / 16;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<long long>(T) * nb) return;
@@ -160,7 +163,7 @@ cudaError_t launch_amax_bf16(const void* src, long long rows, int cols, const in
   long long blocks = (nvec + 255) / 256;
   const long long cap = 4LL * num_sms();
   if (blocks > cap) blocks = cap;
-  amax_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint4*>(src), nvec, cols / 8,
+  launch_k(amax_bf16_kernel, static_cast<unsigned>(blocks), 256, 0, st, static_cast<const uint4*>(src), nvec, cols / 8,
                                                                    row_src, rows_end, reinterpret_cast<unsigned*>(amax));
   count_launches(1);
   return cudaGetLastError();
@@ -170,7 +173,7 @@ cudaError_t launch_quantize_rows_nv4(const void* src, long long rows, int cols, 
                                      const float* amax, uint8_t* codes, uint8_t* sf, cudaStream_t st) {
   const long long n = rows * (cols / 16);
   if (n == 0) return cudaSuccess;
-  quantize_rows_nv4_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+  launch_k(quantize_rows_nv4_kernel, static_cast<unsigned>((n + 255) / 256), 256, 0, st, 
       static_cast<const uint4*>(src), rows, cols, gate_up_half, amax, codes, sf);
   count_launches(1);
   return cudaGetLastError();
@@ -181,7 +184,7 @@ cudaError_t launch_quantize_gather_nv4(const void* x, int T, int H, const int32_
                                       uint8_t* sf_tok, cudaStream_t st) {
   const long long n = static_cast<long long>(T) * (H / 16);
   if (n == 0) return cudaSuccess;
-  quantize_gather_nv4_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+  launch_k(quantize_gather_nv4_kernel, static_cast<unsigned>((n + 255) / 256), 256, 0, st, 
       static_cast<const uint4*>(x), T, H, slot_row, k, amax, codes_perm, sf_perm, codes_tok, sf_tok);
   count_launches(1);
   return cudaGetLastError();

@@ -22,6 +22,23 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // region are the grouped GEMMs' tile counter (zero between launches).
 constexpr int kSchedCounterWord = 32;
 
+// Launch chaining.  Every kernel of the library begins with griddepcontrol
+// .wait and is launched with programmatic stream serialization (launch_k in
+// internal.h): it may be scheduled before the kernel ahead of it in the
+// stream has finished, but touches no global memory before that grid has
+// completed and its writes are visible.  The routing, copy and quantiser
+// kernels then let the next grid launch at once (pdl_entry); the persistent
+// GEMMs only once their tiles are done (pdl_wait first, pdl_launch_next at
+// their teardown) -- a GEMM that released its dependents at its start ran
+// the long layers about 0.5 % slower.  (A kernel whose predecessor was
+// launched without the attribute simply starts after it, as usual.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_entry() {
+  pdl_wait();
+  pdl_launch_next();
+}
+
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }

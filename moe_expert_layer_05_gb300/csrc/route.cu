@@ -155,6 +155,7 @@ template <int PER_LANE>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                    int T, int E, int k, int score, int32_t* __restrict__ idx,
                                                    float* __restrict__ gate) {
+  pdl_entry();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -286,6 +287,7 @@ __device__ __forceinline__ void hist_rank_tail(int e, long long p, bool has_pair
 __global__ void __launch_bounds__(kPairsPerBlock) count_kernel(const int32_t* __restrict__ idx, long long npairs,
                                                                int pb, int E, int32_t* __restrict__ hist,
                                                                int* status) {
+  pdl_entry();
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
   const int e = load_pair_expert(idx, npairs, pb, E, status);
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* 
                                                                    int32_t* __restrict__ slot_row,
                                                                    int* __restrict__ done,
                                                                    int32_t* __restrict__ counts) {
+  pdl_entry();
   constexpr int kStageFloats = 8192;             // logits of the chunk staged in shared memory (32 KB)
   __shared__ int s_idx[kPairsPerBlock];
   __shared__ int s_cnt[8 * kMaxE];
@@ -365,6 +368,7 @@ __global__ void __launch_bounds__(kPairsPerBlock) topk_hist_kernel(const float* 
 // before the first is used.
 __global__ void __launch_bounds__(256) scan_cols_kernel(int32_t* __restrict__ hist, int NB, int E,
                                                         int32_t* __restrict__ counts) {
+  pdl_entry();
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (e >= E) return;
@@ -440,6 +444,7 @@ __global__ void __launch_bounds__(kPairsPerBlock) scatter_kernel(const int32_t* 
                                                                  int32_t* __restrict__ slot_row,
                                                                  int32_t* __restrict__ row_src,
                                                                  float* __restrict__ row_gate) {
+  pdl_entry();
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
   __shared__ int s_off[kMaxE + 1];
@@ -480,6 +485,7 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_rank_kernel(const int32_
                                                                     int32_t* __restrict__ slot_row,
                                                                     int* __restrict__ done,
                                                                     int32_t* __restrict__ counts, int* status) {
+  pdl_entry();
   __shared__ int s_cnt[8 * kMaxE];
   __shared__ int s_tot[kMaxE];
   const int e = load_pair_expert(idx, npairs, pb, E, status);
@@ -503,6 +509,7 @@ __global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
     int k, int NB, int pb, int vec_per_row, const int32_t* __restrict__ base, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ poffsets, int32_t* __restrict__ slot_row,
     int32_t* __restrict__ row_src, float* __restrict__ row_gate, uint4* __restrict__ x_perm, int* status) {
+  pdl_entry();
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_poff[kMaxE + 1];
   __shared__ int s_rows[kMaxK];
@@ -654,6 +661,7 @@ __global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
 // keeps up to 4 16-byte loads in flight before storing.
 __global__ void __launch_bounds__(128) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ slot_row,
                                                      int k, int vec_per_row, uint4* __restrict__ x_perm) {
+  pdl_entry();
   const int t = blockIdx.x;
   __shared__ int s_rows[kMaxK];
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
@@ -681,6 +689,7 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4* __restrict__ x
 
 __global__ void zero_pad_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ poffsets,
                                 int vec_per_row, uint4* __restrict__ buf) {
+  pdl_entry();
   const int e = blockIdx.x;
   const int r0 = poffsets[e] + counts[e], r1 = poffsets[e + 1];
   const long long n = (long long)(r1 - r0) * vec_per_row;
@@ -705,6 +714,7 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
 __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ o, const int32_t* __restrict__ slot_row,
                                                       const uint4* __restrict__ shared, int k, int vec_per_row,
                                                       uint4* __restrict__ y) {
+  pdl_entry();
   const int t = blockIdx.x;
   __shared__ int s_rows[kMaxK];
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
@@ -744,6 +754,7 @@ __global__ void __launch_bounds__(128) dgrad_combine_kernel(
     int n_part, const uint4* __restrict__ w_router, const uint4* __restrict__ dx_shared, int E, int k,
     int vec_per_row, int score, uint4* __restrict__ dx, float* __restrict__ dgate, float* __restrict__ dlogits,
     float* __restrict__ row_dlogit) {
+  pdl_entry();
   const int t = blockIdx.x;
   __shared__ int s_rows[kMaxK];
   __shared__ int s_ids[kMaxK];
@@ -821,6 +832,7 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint4* __restri
                                                            const int32_t* __restrict__ counts,
                                                            const int32_t* __restrict__ poffsets, int vec_per_row,
                                                            float* __restrict__ dw) {
+  pdl_entry();
   // Block (e, b): 256 columns of dWr[e] (lane = 8 columns); warp w sums the
   // rows w, w+8, w+16, ... of expert e; the eight partial sums are then added
   // in warp order, so the result does not depend on scheduling.
@@ -880,10 +892,10 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         float* gate, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + 7) / 8;
-  if (E <= 32) topk_kernel<1><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
-  else if (E <= 64) topk_kernel<2><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
-  else if (E <= 128) topk_kernel<4><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
-  else topk_kernel<8><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, score, idx, gate);
+  if (E <= 32) launch_k(topk_kernel<1>, blocks, 256, 0, st, logits, bias, T, E, k, score, idx, gate);
+  else if (E <= 64) launch_k(topk_kernel<2>, blocks, 256, 0, st, logits, bias, T, E, k, score, idx, gate);
+  else if (E <= 128) launch_k(topk_kernel<4>, blocks, 256, 0, st, logits, bias, T, E, k, score, idx, gate);
+  else launch_k(topk_kernel<8>, blocks, 256, 0, st, logits, bias, T, E, k, score, idx, gate);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -896,9 +908,9 @@ cudaError_t launch_scan_scatter(const int32_t* idx, const float* gate, int T, in
                                 int32_t* row_src, float* row_gate, cudaStream_t st) {
   const long long npairs = (long long)T * k;
   const int NB = chunks_of(T, k);
-  scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, NB, E, counts);
+  launch_k(scan_cols_kernel, (E + 7) / 8, 256, 0, st, hist, NB, E, counts);
   // (with no tokens one block still writes the offsets)
-  scatter_kernel<<<NB > 0 ? NB : 1, kPairsPerBlock, 0, st>>>(idx, gate, npairs, pairs_per_chunk(k), E, k, NB, hist,
+  launch_k(scatter_kernel, NB > 0 ? NB : 1, kPairsPerBlock, 0, st, idx, gate, npairs, pairs_per_chunk(k), E, k, NB, hist,
                                                              counts, offsets, poffsets, slot_row, row_src,
                                                              gate != nullptr ? row_gate : nullptr);
   count_launches(2);
@@ -912,7 +924,7 @@ cudaError_t launch_permute_maps(const int32_t* idx, const float* gate, int T, in
   const long long npairs = (long long)T * k;
   const int NB = chunks_of(T, k);
   if (NB > 0) {
-    count_kernel<<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, status);
+    launch_k(count_kernel, NB, kPairsPerBlock, 0, st, idx, npairs, pairs_per_chunk(k), E, hist, status);
     count_launches(1);
   }
   return launch_scan_scatter(idx, gate, T, E, k, hist, counts, offsets, poffsets, slot_row, row_src, row_gate, st);
@@ -923,19 +935,19 @@ template <int MODE>
 void topk_hist(const float* logits, const float* bias, int T, int E, int k, int score, int32_t* idx, float* gate,
                int32_t* hist, int32_t* slot_row, int* done, int32_t* counts, int NB, cudaStream_t st) {
   if (E <= kThreadTopkE)
-    topk_hist_kernel<0, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+    launch_k(topk_hist_kernel<0, MODE>, NB, kPairsPerBlock, 0, st, logits, bias, T, E, k, score, idx, gate, hist, slot_row,
                                                              done, counts);
   else if (E <= 32)
-    topk_hist_kernel<1, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+    launch_k(topk_hist_kernel<1, MODE>, NB, kPairsPerBlock, 0, st, logits, bias, T, E, k, score, idx, gate, hist, slot_row,
                                                              done, counts);
   else if (E <= 64)
-    topk_hist_kernel<2, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+    launch_k(topk_hist_kernel<2, MODE>, NB, kPairsPerBlock, 0, st, logits, bias, T, E, k, score, idx, gate, hist, slot_row,
                                                              done, counts);
   else if (E <= 128)
-    topk_hist_kernel<4, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+    launch_k(topk_hist_kernel<4, MODE>, NB, kPairsPerBlock, 0, st, logits, bias, T, E, k, score, idx, gate, hist, slot_row,
                                                              done, counts);
   else
-    topk_hist_kernel<8, MODE><<<NB, kPairsPerBlock, 0, st>>>(logits, bias, T, E, k, score, idx, gate, hist, slot_row,
+    launch_k(topk_hist_kernel<8, MODE>, NB, kPairsPerBlock, 0, st, logits, bias, T, E, k, score, idx, gate, hist, slot_row,
                                                              done, counts);
   count_launches(1);
 }
@@ -957,7 +969,7 @@ cudaError_t launch_gather_scatter(const void* x, const int32_t* idx, const float
   const bool raw = raw_histograms(T, E, k);
   auto kern = raw ? gather_scatter_kernel<64, 8, true>
                   : (T <= kGsSmallT) ? gather_scatter_kernel<64, 8, false> : gather_scatter_kernel<128, 4, false>;
-  kern<<<T > 0 ? T : 1, (raw || T <= kGsSmallT) ? 64 : 128, 0, st>>>(
+  launch_k(kern, T > 0 ? T : 1, (raw || T <= kGsSmallT) ? 64 : 128, 0, st, 
       static_cast<const uint4*>(x), idx, gate, T, E, k, chunks_of(T, k), pairs_per_chunk(k), H / 8, hist, counts,
       offsets, poffsets, slot_row, row_src, gate != nullptr ? row_gate : nullptr, static_cast<uint4*>(x_perm),
       status);
@@ -988,11 +1000,11 @@ cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, i
       topk_hist<2>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
     } else {
       topk_hist<1>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
-      scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, NB, E, counts);
+      launch_k(scan_cols_kernel, (E + 7) / 8, 256, 0, st, hist, NB, E, counts);
       count_launches(1);
     }
   } else {
-    scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, 0, E, counts);   // counts = 0
+    launch_k(scan_cols_kernel, (E + 7) / 8, 256, 0, st, hist, 0, E, counts);   // counts = 0
     count_launches(1);
   }
   return launch_gather_scatter(x, idx, gate, T, E, k, H, hist, counts, offsets, poffsets, slot_row, row_src, row_gate,
@@ -1006,22 +1018,22 @@ cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, 
   const long long npairs = (long long)T * k;
   const int NB = chunks_of(T, k);
   if (raw_histograms(T, E, k)) {
-    count_rank_kernel<false><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
+    launch_k(count_rank_kernel<false>, NB, kPairsPerBlock, 0, st, idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
                                                             counts, status);
     count_launches(1);
   } else if (NB > 0) {
     if ((long long)NB * E <= kLastScanEntries) {
-      count_rank_kernel<true><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
+      launch_k(count_rank_kernel<true>, NB, kPairsPerBlock, 0, st, idx, npairs, pairs_per_chunk(k), E, hist, slot_row, done,
                                                              counts, status);
       count_launches(1);
     } else {
-      count_rank_kernel<false><<<NB, kPairsPerBlock, 0, st>>>(idx, npairs, pairs_per_chunk(k), E, hist, slot_row,
+      launch_k(count_rank_kernel<false>, NB, kPairsPerBlock, 0, st, idx, npairs, pairs_per_chunk(k), E, hist, slot_row,
                                                               done, counts, status);
-      scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, NB, E, counts);
+      launch_k(scan_cols_kernel, (E + 7) / 8, 256, 0, st, hist, NB, E, counts);
       count_launches(2);
     }
   } else {
-    scan_cols_kernel<<<(E + 7) / 8, 256, 0, st>>>(hist, 0, E, counts);   // counts = 0
+    launch_k(scan_cols_kernel, (E + 7) / 8, 256, 0, st, hist, 0, E, counts);   // counts = 0
     count_launches(1);
   }
   return launch_gather_scatter(x, idx, gate, T, E, k, H, hist, counts, offsets, poffsets, slot_row, row_src, row_gate,
@@ -1031,14 +1043,14 @@ cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, 
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
                                cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  gather_kernel<<<T, 128, 0, st>>>(static_cast<const uint4*>(x), slot_row, k, H / 8, static_cast<uint4*>(x_perm));
+  launch_k(gather_kernel, T, 128, 0, st, static_cast<const uint4*>(x), slot_row, k, H / 8, static_cast<uint4*>(x_perm));
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,
                                  cudaStream_t st) {
-  zero_pad_kernel<<<E, 256, 0, st>>>(counts, poffsets, H / 8, static_cast<uint4*>(buf));
+  launch_k(zero_pad_kernel, E, 256, 0, st, counts, poffsets, H / 8, static_cast<uint4*>(buf));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -1046,7 +1058,7 @@ cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets,
 cudaError_t launch_combine(const void* o_perm, const int32_t* slot_row, const void* shared, int T, int k, int H,
                            void* y, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 128, 0, st>>>(static_cast<const uint4*>(o_perm), slot_row, static_cast<const uint4*>(shared),
+  launch_k(combine_kernel, T, 128, 0, st, static_cast<const uint4*>(o_perm), slot_row, static_cast<const uint4*>(shared),
                                     k, H / 8, static_cast<uint4*>(y));
   count_launches(1);
   return cudaGetLastError();
@@ -1058,7 +1070,7 @@ cudaError_t launch_dgrad_combine(const void* dx_perm, const int32_t* slot_row, c
                                  int H, int score, void* dx, float* dgate, float* dlogits, float* row_dlogit,
                                  cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  dgrad_combine_kernel<<<T, 128, 0, st>>>(
+  launch_k(dgrad_combine_kernel, T, 128, 0, st, 
       static_cast<const uint4*>(dx_perm), slot_row, topk_idx, topk_gate, logits, dgate_part, n_part,
       static_cast<const uint4*>(w_router), static_cast<const uint4*>(dx_shared), E, k, H / 8, score,
       static_cast<uint4*>(dx), dgate, dlogits, row_dlogit);
@@ -1071,7 +1083,7 @@ cudaError_t launch_router_wgrad(const void* x_perm, const int32_t* row_src, cons
                                 cudaStream_t st) {
   const int vpr = H / 8;
   dim3 grid(E, (vpr + 31) / 32);
-  router_wgrad_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x_perm), row_src, row_dlogit, counts, poffsets,
+  launch_k(router_wgrad_kernel, grid, 256, 0, st, static_cast<const uint4*>(x_perm), row_src, row_dlogit, counts, poffsets,
                                             vpr, dw_router);
   count_launches(1);
   return cudaGetLastError();
