@@ -608,8 +608,8 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_TRY(launch_permute_gather(topk_idx, topk_gate, cfg->T, cfg->E, cfg->k, hist_ptr(ws),
                                 status_ptr(ws) + kMapsDoneWord, counts, offsets, poffsets, slot_row, row_src,
-                                topk_gate != nullptr ? row_gate : nullptr, x, cfg->H, x_perm, status_ptr(ws), st));
-  if (zero_pad) MOE_TRY(launch_zero_pad_rows(counts, poffsets, cfg->E, cfg->H, x_perm, st));
+                                topk_gate != nullptr ? row_gate : nullptr, x, cfg->H, x_perm, zero_pad ? 1 : 0,
+                                status_ptr(ws), st));
   return MOE_OK;
 }
 
@@ -774,8 +774,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     // the maps and the row copy of x: two launches where the histograms are small
     MOE_TRY(launch_topk_permute_gather(logits, rbias, T, E, k, cfg->score, idx, gate, hist_ptr(ws),
                                        status + kMapsDoneWord, counts, at<int32_t>(act, L.offsets), poff, slot_row,
-                                       at<int32_t>(act, L.row_src), row_gate, x, H, x_perm, status, st));
-    if (with_backward) MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, x_perm, st));
+                                       at<int32_t>(act, L.row_src), row_gate, x, H, x_perm, with_backward ? 1 : 0,
+                                       status, st));
   } else {
     // (MXFP8 and NVFP4 layers permute the quantised codes instead and read x
     // through row_src where its rows are needed again; x_perm stays unwritten)
@@ -918,8 +918,7 @@ moe_status moe_layer_backward_dgrad(const moe_config* cfg, const moe_weights* w,
   float* dpart = at<float>(act, L.dgate_part);
 
   if (cfg->dtype == MOE_GEMM_BF16) {
-    MOE_TRY(launch_gather_rows(dy, slot_row, T, k, H, dy_perm, st));
-    MOE_TRY(launch_zero_pad_rows(counts, poff, E, H, dy_perm, st));
+    MOE_TRY(launch_gather_rows_zero(dy, slot_row, T, k, E, counts, H, dy_perm, st));
   }
   const void* dxs = nullptr;
   if (cfg->dtype == MOE_GEMM_MXFP8) {

@@ -56,22 +56,26 @@ cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int
                                      int32_t* idx, float* gate, int32_t* hist, int32_t* counts, int32_t* offsets,
                                      int32_t* poffsets, int32_t* slot_row, int32_t* row_src, float* row_gate,
                                      cudaStream_t st);
-// The same maps plus the row copy of x into x_perm, in two launches where
-// NB * E is small (histograms, ranks and the scan in the first; the maps and
-// the copy in the second), three otherwise.  done: a workspace int, zero
-// between launches.
+// The same maps plus the row copy of x into x_perm (and, with zero_pad, zeros
+// in the segments' padding rows), in two launches where NB * E is small
+// (histograms, ranks and the scan in the first; the maps and the copy in the
+// second), three otherwise.  done: a workspace int, zero between launches.
 cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
                                   int* done, int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
-                                  int32_t* row_src, float* row_gate, const void* x, int H, void* x_perm, int* status,
-                                  cudaStream_t st);
+                                  int32_t* row_src, float* row_gate, const void* x, int H, void* x_perm, int zero_pad,
+                                  int* status, cudaStream_t st);
 // Top-k gating fused into the first launch of launch_permute_gather.
 cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, int T, int E, int k, int score,
                                        int32_t* idx, float* gate, int32_t* hist, int* done, int32_t* counts,
                                        int32_t* offsets, int32_t* poffsets, int32_t* slot_row, int32_t* row_src,
-                                       float* row_gate, const void* x, int H, void* x_perm, int* status,
-                                       cudaStream_t st);
+                                       float* row_gate, const void* x, int H, void* x_perm, int zero_pad,
+                                       int* status, cudaStream_t st);
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
                                cudaStream_t st);
+// The row copy of an input whose maps exist (dy), zeroing the segments'
+// padding rows in the same launch.
+cudaError_t launch_gather_rows_zero(const void* x, const int32_t* slot_row, int T, int k, int E,
+                                   const int32_t* counts, int H, void* x_perm, cudaStream_t st);
 cudaError_t launch_zero_pad_rows(const int32_t* counts, const int32_t* poffsets, int E, int H, void* buf,
                                  cudaStream_t st);
 cudaError_t launch_combine(const void* o_perm, const int32_t* slot_row, const void* shared, int T, int k, int H,

@@ -499,6 +499,28 @@ __global__ void __launch_bounds__(kPairsPerBlock) count_rank_kernel(const int32_
 // them.  Every block derives the expert offsets from counts (E <= 256);
 // block 0 also writes offsets, poffsets and marks the padding rows.  Launched
 // with max(T, 1) blocks.
+// Zero the padding rows of the expert segments, spread over the blocks of a
+// row-copy launch: block b takes padding rows b, b + nblocks, ... of the
+// concatenation of every expert's padding (s_off / s_poff: the expert
+// offsets and padded offsets in shared memory; expert e's padding starts
+// after its counts and has s_poff[e+1] - s_poff[e] - (s_off[e+1] - s_off[e])
+// rows).
+template <int THREADS>
+__device__ __forceinline__ void zero_padding_rows(int b, int nblocks, const int* s_off, const int* s_poff, int E,
+                                                  int vec_per_row, uint4* __restrict__ buf) {
+  const int total = (s_poff[E] - s_off[E]);       // padding rows before expert E
+  for (int j = b; j < total; j += nblocks) {
+    int lo = 0, hi = E - 1;                       // largest e with padding-before(e) <= j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_poff[mid] - s_off[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    const int row = s_off[lo + 1] - s_off[lo] + s_poff[lo] + (j - (s_poff[lo] - s_off[lo]));
+    uint4* dst = buf + (long long)row * vec_per_row;
+    for (int v = threadIdx.x; v < vec_per_row; v += THREADS) dst[v] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // RAW (at most 32 chunks and 32 experts): base holds the chunk histograms
 // as counted, not scanned, and counts is not written yet; each block sums the
 // columns it needs itself (one coalesced load per expert and per pair) and
@@ -508,7 +530,8 @@ __global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int E,
     int k, int NB, int pb, int vec_per_row, const int32_t* __restrict__ base, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ poffsets, int32_t* __restrict__ slot_row,
-    int32_t* __restrict__ row_src, float* __restrict__ row_gate, uint4* __restrict__ x_perm, int* status) {
+    int32_t* __restrict__ row_src, float* __restrict__ row_gate, uint4* __restrict__ x_perm, int zero_pad,
+    int* status) {
   pdl_entry();
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_poff[kMaxE + 1];
@@ -613,6 +636,7 @@ __global__ void __launch_bounds__(kGsThreads) gather_scatter_kernel(
       }
     }
   }
+  if (zero_pad) zero_padding_rows<kGsThreads>(t, gridDim.x, s_off, s_poff, E, vec_per_row, x_perm);
   if (t >= T) return;
   if (threadIdx.x < k) {
     const long long p = (long long)t * k + threadIdx.x;
@@ -666,6 +690,45 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint4* __restrict__ x
   __shared__ int s_rows[kMaxK];
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
   __syncthreads();
+  const uint4* src = x + (long long)t * vec_per_row;
+  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += 4 * blockDim.x) {
+    uint4 val[4];
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * blockDim.x;
+      if (v < vec_per_row) val[u] = __ldg(src + v);
+    }
+    for (int i = 0; i < k; ++i) {
+      const int r = s_rows[i];
+      if (r < 0) continue;
+      uint4* dst = x_perm + (long long)r * vec_per_row;
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < vec_per_row) dst[v] = val[u];
+      }
+    }
+  }
+}
+
+// The row copy of an input whose maps exist already (dy in the backward),
+// with the segments' padding rows zeroed in the same launch (block t copies
+// token t and zeroes padding rows t, t + T, ...; every block derives the
+// expert offsets from counts).
+__global__ void __launch_bounds__(128) gather_zero_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ slot_row, int T, int k, int E,
+                                                          const int32_t* __restrict__ counts, int vec_per_row,
+                                                          uint4* __restrict__ x_perm) {
+  pdl_entry();
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_poff[kMaxE + 1];
+  __shared__ int s_rows[kMaxK];
+  const int t = blockIdx.x;
+  if (t < T && threadIdx.x < k) s_rows[threadIdx.x] = slot_row[(long long)t * k + threadIdx.x];
+  expert_offsets(counts, E, s_off, s_poff);
+  __syncthreads();
+  zero_padding_rows<128>(t, gridDim.x, s_off, s_poff, E, vec_per_row, x_perm);
+  if (t >= T) return;
   const uint4* src = x + (long long)t * vec_per_row;
   for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += 4 * blockDim.x) {
     uint4 val[4];
@@ -964,15 +1027,15 @@ bool raw_histograms(int T, int E, int k) {
 
 cudaError_t launch_gather_scatter(const void* x, const int32_t* idx, const float* gate, int T, int E, int k, int H,
                                   const int32_t* hist, int32_t* counts, int32_t* offsets, int32_t* poffsets,
-                                  int32_t* slot_row, int32_t* row_src, float* row_gate, void* x_perm, int* status,
-                                  cudaStream_t st) {
+                                  int32_t* slot_row, int32_t* row_src, float* row_gate, void* x_perm, int zero_pad,
+                                  int* status, cudaStream_t st) {
   const bool raw = raw_histograms(T, E, k);
   auto kern = raw ? gather_scatter_kernel<64, 8, true>
                   : (T <= kGsSmallT) ? gather_scatter_kernel<64, 8, false> : gather_scatter_kernel<128, 4, false>;
   launch_k(kern, T > 0 ? T : 1, (raw || T <= kGsSmallT) ? 64 : 128, 0, st, 
       static_cast<const uint4*>(x), idx, gate, T, E, k, chunks_of(T, k), pairs_per_chunk(k), H / 8, hist, counts,
       offsets, poffsets, slot_row, row_src, gate != nullptr ? row_gate : nullptr, static_cast<uint4*>(x_perm),
-      status);
+      zero_pad, status);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -990,8 +1053,8 @@ cudaError_t launch_topk_permute_maps(const float* logits, const float* bias, int
 cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, int T, int E, int k, int score,
                                        int32_t* idx, float* gate, int32_t* hist, int* done, int32_t* counts,
                                        int32_t* offsets, int32_t* poffsets, int32_t* slot_row, int32_t* row_src,
-                                       float* row_gate, const void* x, int H, void* x_perm, int* status,
-                                       cudaStream_t st) {
+                                       float* row_gate, const void* x, int H, void* x_perm, int zero_pad,
+                                       int* status, cudaStream_t st) {
   const int NB = chunks_of(T, k);
   if (raw_histograms(T, E, k)) {
     topk_hist<1>(logits, bias, T, E, k, score, idx, gate, hist, slot_row, done, counts, NB, st);
@@ -1008,13 +1071,13 @@ cudaError_t launch_topk_permute_gather(const float* logits, const float* bias, i
     count_launches(1);
   }
   return launch_gather_scatter(x, idx, gate, T, E, k, H, hist, counts, offsets, poffsets, slot_row, row_src, row_gate,
-                               x_perm, status, st);
+                               x_perm, zero_pad, status, st);
 }
 
 cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, int E, int k, int32_t* hist,
                                   int* done, int32_t* counts, int32_t* offsets, int32_t* poffsets, int32_t* slot_row,
-                                  int32_t* row_src, float* row_gate, const void* x, int H, void* x_perm, int* status,
-                                  cudaStream_t st) {
+                                  int32_t* row_src, float* row_gate, const void* x, int H, void* x_perm, int zero_pad,
+                                  int* status, cudaStream_t st) {
   const long long npairs = (long long)T * k;
   const int NB = chunks_of(T, k);
   if (raw_histograms(T, E, k)) {
@@ -1037,13 +1100,21 @@ cudaError_t launch_permute_gather(const int32_t* idx, const float* gate, int T, 
     count_launches(1);
   }
   return launch_gather_scatter(x, idx, gate, T, E, k, H, hist, counts, offsets, poffsets, slot_row, row_src, row_gate,
-                               x_perm, status, st);
+                               x_perm, zero_pad, status, st);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_row, int T, int k, int H, void* x_perm,
                                cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   launch_k(gather_kernel, T, 128, 0, st, static_cast<const uint4*>(x), slot_row, k, H / 8, static_cast<uint4*>(x_perm));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_zero(const void* x, const int32_t* slot_row, int T, int k, int E,
+                                   const int32_t* counts, int H, void* x_perm, cudaStream_t st) {
+  launch_k(gather_zero_kernel, T > 0 ? T : 1, 128, 0, st, static_cast<const uint4*>(x), slot_row, T, k, E, counts,
+           H / 8, static_cast<uint4*>(x_perm));
   count_launches(1);
   return cudaGetLastError();
 }
