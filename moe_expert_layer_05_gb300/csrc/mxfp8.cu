@@ -201,11 +201,23 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint4* __rest
   if (threadIdx.x < k) s_rows[threadIdx.x] = slot_row[static_cast<long long>(t) * k + threadIdx.x];
   __syncthreads();
   const int nv = H / 16;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    const uint4 c = __ldg(codes_tok + static_cast<long long>(t) * nv + v);
+  const uint4* src = codes_tok + static_cast<long long>(t) * nv;
+  for (int v0 = threadIdx.x; v0 < nv; v0 += 4 * blockDim.x) {
+    uint4 c[4];                                    // four 16-byte loads in flight before the stores
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * blockDim.x;
+      if (v < nv) c[u] = __ldg(src + v);
+    }
     for (int i = 0; i < k; ++i) {
       const int r = s_rows[i];
-      if (r >= 0) codes_perm[static_cast<long long>(r) * nv + v] = c;
+      if (r < 0) continue;
+      uint4* dst = codes_perm + static_cast<long long>(r) * nv;
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < nv) dst[v] = c[u];
+      }
     }
   }
   // scales: a row's four blocks of one 128-column tile are four adjacent
