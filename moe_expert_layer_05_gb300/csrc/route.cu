@@ -2,10 +2,11 @@
 //
 //  * top-k gating: one warp per token, warp-shuffle arg-max k times;
 //  * permutation: a stable counting sort of the T*k (token, slot) pairs by
-//    expert, done entirely on the device (per-block histograms, one scan
-//    block, a scatter) so the host never sees the expert sizes — the
-//    sync-free, dynamic-shape permutation of the Megatron Core MoE summary
-//    (technical summary 1 and 2.4);
+//    expert, done entirely on the device (per-block histograms and ranks, a
+//    scan of the histogram columns, the maps worked out inside the row copy)
+//    so the host never sees the expert sizes — the sync-free, dynamic-shape
+//    permutation of the Megatron Core MoE summary (technical summary 1 and
+//    2.4);
 //  * gather / combine: 16-byte vector copies of token rows; the combine is an
 //    unweighted fp32 sum because the gate was applied inside the expert
 //    (technical summary 2.2, memory-efficient permutation).
@@ -244,14 +245,16 @@ __device__ __forceinline__ int scan_column(int32_t* __restrict__ col, int NB, in
 }
 
 // ------------------------------------------- permutation in two launches
-// The histogram launch (count_rank_kernel, or topk_hist_kernel with RANKS)
-// also leaves each pair's stable rank inside its chunk in slot_row (-1 for a
-// dropped pair).  With LAST_SCAN (small problems: NB * E <= kLastScanEntries)
-// the last of its blocks to finish -- found by an atomic count of finished
-// blocks, no block waits for another -- scans the histogram columns and
-// writes counts, so the scan needs no launch of its own; otherwise
-// scan_cols_kernel runs between the two launches.  gather_scatter_kernel then
-// turns the ranks into rows and copies the token rows in the same launch.
+// The histogram launch (count_rank_kernel, or topk_hist_kernel with MODE 1
+// or 2) also leaves each pair's stable rank inside its chunk in slot_row (-1
+// for a dropped pair).  The column scan then takes one of three forms: with
+// at most 32 chunks and 32 experts none at all (gather_scatter_kernel RAW
+// sums the columns it needs itself); with LAST_SCAN (NB * E <=
+// kLastScanEntries) the last of the histogram blocks to finish -- found by
+// an atomic count of finished blocks, no block waits for another -- scans the
+// columns and writes counts; otherwise scan_cols_kernel runs between the two
+// launches.  gather_scatter_kernel turns the ranks into rows and copies the
+// token rows in the same launch.
 constexpr int kLastScanEntries = 8192;
 // gather_scatter_kernel: a block per token, warp 0 deriving the expert
 // offsets while warp 1 fetches the pairs' maps.  Where all blocks fit on the
