@@ -99,6 +99,9 @@ __device__ __forceinline__ void topk_one_token(const float* __restrict__ row, co
 // Route one token in one thread (few experts: E <= kThreadTopkE): the same
 // keys, tie rule, slot order and gate arithmetic as topk_one_token, so the
 // result is identical; a warp then routes 32 tokens at once instead of one.
+// The slot loop is not unrolled (only the scan over the experts is): the
+// kernel's code stays small, which matters because its instructions are
+// fetched cold at every step.
 constexpr int kThreadTopkE = 16;
 __device__ __forceinline__ void topk_one_token_thread(const float* __restrict__ row, const float* __restrict__ bias,
                                                       int E, int k, int score, int32_t* __restrict__ idx_out,
@@ -115,40 +118,29 @@ __device__ __forceinline__ void topk_one_token_thread(const float* __restrict__ 
     }
     if (key[e] != key[e]) key[e] = -INFINITY;   // as in topk_one_token
   }
-  // slots unrolled to the bound and guarded by k, so every array stays in registers
+  // pass 1: the slots in order, their weights summed in slot order
   uint32_t taken = 0;
-  float slot_logit[kThreadTopkE];
-  int slot_id[kThreadTopkE];
-  #pragma unroll
-  for (int s = 0; s < kThreadTopkE; ++s) {
-    if (s < k) {
-      Cand best{0.f, 0.f, INT_MAX};
-      #pragma unroll
-      for (int e = 0; e < kThreadTopkE; ++e) {
-        Cand c{key[e], lg[e], (e < E && !((taken >> e) & 1u)) ? e : INT_MAX};
-        if (better(c, best)) best = c;
-      }
-      taken |= 1u << best.id;
-      slot_logit[s] = best.logit;
-      slot_id[s] = best.id;
+  float l0 = 0.f, sum = 0.f;
+  #pragma unroll 1
+  for (int s = 0; s < k; ++s) {
+    Cand best{0.f, 0.f, INT_MAX};
+    #pragma unroll
+    for (int e = 0; e < kThreadTopkE; ++e) {
+      Cand c{key[e], lg[e], (e < E && !((taken >> e) & 1u)) ? e : INT_MAX};
+      if (better(c, best)) best = c;
     }
+    taken |= 1u << best.id;
+    if (s == 0) l0 = best.logit;                          // slot 0 has the largest logit
+    sum += (score == 0) ? expf(best.logit - l0) : 1.0f / (1.0f + expf(-best.logit));
+    idx_out[s] = best.id;
+    s_idx_out[s] = best.id;
   }
-  float w[kThreadTopkE];
-  float sum = 0.f;                                        // slot order, as the warp version
-  #pragma unroll
-  for (int s = 0; s < kThreadTopkE; ++s) {
-    if (s < k) {
-      w[s] = (score == 0) ? expf(slot_logit[s] - slot_logit[0]) : 1.0f / (1.0f + expf(-slot_logit[s]));
-      sum += w[s];
-    }
-  }
-  #pragma unroll
-  for (int s = 0; s < kThreadTopkE; ++s) {
-    if (s < k) {
-      idx_out[s] = slot_id[s];
-      gate_out[s] = w[s] / sum;
-      s_idx_out[s] = slot_id[s];
-    }
+  // pass 2: each slot's weight again (the same expression on the same logit)
+  // over the sum
+  #pragma unroll 1
+  for (int s = 0; s < k; ++s) {
+    const float l = row[s_idx_out[s]];
+    gate_out[s] = ((score == 0) ? expf(l - l0) : 1.0f / (1.0f + expf(-l))) / sum;
   }
 }
 
