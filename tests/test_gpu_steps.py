@@ -213,6 +213,28 @@ def test_permute_is_deterministic(lib, T, E):
         assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1]) and torch.equal(o[2], outs[0][2])
 
 
+def test_launch_chaining_orders_around_other_kernels(lib):
+    """Every library kernel waits for the kernel before it in the stream
+    (griddepcontrol.wait) and torch's kernels after it wait for it: a torch
+    write of x just before moe_permute is seen, one just after is not."""
+    T, E, k, H = 2048, 8, 2, 512
+    idx = torch.from_numpy(random_topk_indices(T, E, k, seed=5)).to(DEV)
+    cfg = api.make_config(T, H, E, k, 128)
+    ws = _ws(cfg)
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    for rep in range(3):
+        cap, b = _perm_buffers(cfg)
+        x.fill_(float(rep + 1))                                   # a torch kernel right before
+        api.moe_permute(cfg, x, idx, None, b["counts"], b["offsets"], b["poffsets"], b["slot_row"],
+                        b["row_src"], None, b["x_perm"], 1, ws)
+        x.fill_(-5.0)                                             # and one right after
+        torch.cuda.synchronize()
+        used = int(b["poffsets"][-1])
+        rows = b["x_perm"][:used][b["row_src"][:used] >= 0].float()
+        assert rows.numel() == T * k * H and torch.all(rows == float(rep + 1)), rep
+    assert _status(ws) == 0
+
+
 def test_permute_bad_index_sets_status(lib):
     """An out-of-range expert id is an input error the kernel bounds-checks:
     the pair is dropped, nothing out of range is written, the status word says so."""
