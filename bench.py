@@ -822,7 +822,7 @@ def run_ours(args) -> dict | None:
 
 
 # ---------------------------------------------------------------- profiler captures
-PROFILE_OPS = GEMM_OPS + ("permute", "combine", "step")
+PROFILE_OPS = GEMM_OPS + ("router", "permute", "combine", "step")
 
 
 def profile_op(args) -> dict:
@@ -864,7 +864,7 @@ def profile_op(args) -> dict:
         torch.cuda.profiler.stop()
         return {"profile_op": "step", "workload": w.name, "T": w.T, "E": w.E,
                 "launches": api.moe_kernel_launches() - l0, "status": api.moe_read_device_status(layer.ws)}
-    if args.profile_op in ("permute", "combine"):
+    if args.profile_op in ("router", "permute", "combine"):
         cfg = api.make_config(w.T, w.H, w.E, w.k, w.F, 0, w.score, "bf16")   # the routing and row copies only
         d = make_router_inputs_on_device(w, dev, seed=0)
         T, E, k, H = w.T, w.E, w.k, w.H
@@ -883,7 +883,10 @@ def profile_op(args) -> dict:
                                        0, ws)
         perm()
         y = torch.empty_like(d["x"])
-        call = perm if args.profile_op == "permute" else (lambda: api.moe_unpermute(cfg, rows, slot_row, None, y))
+        call = {"permute": perm,
+                "combine": lambda: api.moe_unpermute(cfg, rows, slot_row, None, y),
+                "router": lambda: api.moe_router_topk(cfg, d["x"], d["w_router"], bias, logits, idx, gate, ws),
+                }[args.profile_op]
         call()
         torch.cuda.synchronize()
         torch.cuda.profiler.start()
@@ -891,7 +894,7 @@ def profile_op(args) -> dict:
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
         return {"profile_op": args.profile_op, "workload": w.name, "T": T, "E": E,
-                "algorithmic_bytes": (1 + k) * T * H * 2, "status": api.moe_read_device_status(ws),
+                "algorithmic_bytes": (1 + k) * T * H * 2 if args.profile_op != "router" else None, "status": api.moe_read_device_status(ws),
                 "max_memory_gb": torch.cuda.max_memory_allocated(dev) / 1e9}
     if w.dtype == "nvfp4":
         return profile_op_nvfp4(args, w, dev)

@@ -38,50 +38,54 @@ __device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
   return a.key > b.key || (a.key == b.key && a.id < b.id);
 }
 
-__device__ __forceinline__ Cand shfl_cand(const Cand& c, int src_mask) {
-  Cand o;
-  o.key = __shfl_xor_sync(kFull, c.key, src_mask);
-  o.logit = __shfl_xor_sync(kFull, c.logit, src_mask);
-  o.id = __shfl_xor_sync(kFull, c.id, src_mask);
-  return o;
+// A key as an unsigned integer with the same order (-0 taken as +0 first, so
+// that keys equal as floats stay equal); 0 lies below every key (-inf maps to
+// 0x007FFFFF) and marks an expert that is taken or absent.
+__device__ __forceinline__ uint32_t ordered_key(float key) {
+  const uint32_t u = __float_as_uint(key + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Route one token (the whole warp): lane s < k receives slot s's expert and gate.
+// Lane l holds experts l, l + 32, ...  Each slot is one warp maximum of the
+// keys and one warp minimum of the ids that reach it (ties go to the lower id),
+// the same order as better() on (key, id).
 template <int PER_LANE>
 __device__ __forceinline__ void topk_one_token(const float* __restrict__ row, const float* __restrict__ bias, int E,
                                                int k, int score, int lane, int& out_id, float& out_gate) {
-  float lg[PER_LANE], key[PER_LANE];
-  uint32_t taken = 0;
+  uint32_t okey[PER_LANE];
   #pragma unroll
   for (int j = 0; j < PER_LANE; ++j) {
     const int e = lane + 32 * j;
-    lg[j] = (e < E) ? row[e] : 0.f;
+    const float lg = (e < E) ? row[e] : 0.f;
+    float key;
     if (score == 0) {
-      key[j] = lg[j];
+      key = lg;
     } else {
-      key[j] = 1.0f / (1.0f + expf(-lg[j]));
-      if (bias != nullptr && e < E) key[j] += bias[e];
+      key = 1.0f / (1.0f + expf(-lg));
+      if (bias != nullptr && e < E) key += bias[e];
     }
-    if (key[j] != key[j]) key[j] = -INFINITY;   // NaN ranks last: the order stays total
-    if (e >= E) taken |= 1u << j;
+    if (key != key) key = -INFINITY;   // NaN ranks last: the order stays total
+    okey[j] = (e < E) ? ordered_key(key) : 0u;
   }
-  float my_logit = 0.f;  // lane s keeps slot s
-  int my_id = 0;
+  int my_id = 0;  // lane s keeps slot s
   for (int s = 0; s < k; ++s) {
-    Cand best{0.f, 0.f, INT_MAX};
+    uint32_t bk = 0u;
+    int bj = 0;
     #pragma unroll
-    for (int j = 0; j < PER_LANE; ++j) {
-      Cand c{key[j], lg[j], (taken >> j) & 1u ? INT_MAX : lane + 32 * j};
-      if (better(c, best)) best = c;
+    for (int j = 0; j < PER_LANE; ++j)   // strict: the lane's lowest id among equal keys
+      if (okey[j] > bk) { bk = okey[j]; bj = j; }
+    const uint32_t m = __reduce_max_sync(kFull, bk);
+    const uint32_t id = __reduce_min_sync(kFull, (bk == m && m != 0u) ? static_cast<uint32_t>(lane + 32 * bj)
+                                                                       : 0xFFFFFFFFu);
+    if (id != 0xFFFFFFFFu && static_cast<int>(id & 31u) == lane) {
+      #pragma unroll
+      for (int j = 0; j < PER_LANE; ++j)
+        if (j == static_cast<int>(id >> 5)) okey[j] = 0u;
     }
-    #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-      const Cand o = shfl_cand(best, m);
-      if (better(o, best)) best = o;
-    }
-    if ((best.id & 31) == lane) taken |= 1u << (best.id >> 5);
-    if (lane == s) { my_logit = best.logit; my_id = best.id; }
+    if (lane == s) my_id = id != 0xFFFFFFFFu ? static_cast<int>(id) : 0;
   }
+  const float my_logit = (lane < k) ? row[my_id] : 0.f;
   // gates of the chosen k, normalised over them
   float w;
   if (score == 0) {
