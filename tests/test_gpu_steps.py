@@ -89,6 +89,27 @@ def test_topk_gating(lib, score, T, E, k, grid):
     np.testing.assert_allclose(f64(gate).sum(1), 1.0, atol=2e-6)
 
 
+@pytest.mark.parametrize("E", [8, 64, 256])
+def test_topk_signed_zero_keys_tie(lib, E):
+    """Softmax keys are the logits: -0.0 and +0.0 are equal keys, so they tie
+    and the lower expert id comes first whichever of the two carries the sign
+    (the warp path ranks integer images of the keys, with -0 folded into +0)."""
+    T, k = 64, 4
+    lg = np.full((T, E), -1.0, np.float32)
+    rng = np.random.default_rng(E)
+    for t in range(T):
+        a, b, c = rng.choice(E, 3, replace=False)
+        lg[t, a], lg[t, b] = (-0.0, 0.0) if t % 2 else (0.0, -0.0)
+        lg[t, c] = -0.0 if t % 3 else 0.5
+    cfg = api.make_config(T, 128, E, k, 128, score="softmax")
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    api.moe_topk_gating(cfg, torch.from_numpy(lg).to(DEV), None, idx, gate)
+    torch.cuda.synchronize()
+    want = O.topk_select(O.selection_keys_f32(lg, "softmax", None), k)
+    np.testing.assert_array_equal(i64(idx), want)
+
+
 @pytest.mark.parametrize("score", ["softmax", "sigmoid"])
 @pytest.mark.parametrize("T,E,k", [(96, 8, 2), (96, 64, 8), (40, 16, 16)])
 def test_topk_nan_logits_rank_last(lib, score, T, E, k):
